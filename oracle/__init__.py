@@ -1,0 +1,128 @@
+"""The oracle for the FP16 HGEMM, C = A·B (test infrastructure).
+
+Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
+leg may import this package. The product path in
+``tensor_core_dense_fp16_gb300`` never does, and the two share no code.
+
+The arithmetic lives in ``hgemm_oracle.c`` (plain C, FP64 sum in increasing
+k, one round-to-nearest-even to FP16 at the end); this module only compiles
+it with gcc and marshals numpy arrays into it.
+
+Pins: every function here is pinned in ``tests/test_oracle.py`` against
+things other than itself (exact rational arithmetic on tiny shapes, identity
+and zero operands, integer operands against an int64 product, numpy's FP64
+matmul, numpy's FP16 rounding, and the hand-derived fixtures in
+``tests/golden/``).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "hgemm_oracle.c")
+_LIB = os.path.join(_HERE, "_build", "liboracle.so")
+_CFLAGS = ["-O2", "-std=c11", "-fno-fast-math", "-ffp-contract=off", "-fPIC",
+           "-shared", "-pthread"]
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compiles liboracle.so with gcc if it is missing or older than its source."""
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+        return _LIB
+    os.makedirs(os.path.dirname(_LIB), exist_ok=True)
+    tmp = _LIB + f".{os.getpid()}.tmp"
+    subprocess.run(["gcc", *_CFLAGS, "-o", tmp, _SRC, "-lm"], check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        i64, u16p, f64p = ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p
+        lib.oracle_hgemm.argtypes = [u16p, u16p, u16p, i64, i64, i64, ctypes.c_int]
+        lib.oracle_hgemm.restype = ctypes.c_int
+        lib.oracle_hgemm_sums_f64.argtypes = [u16p, u16p, f64p, i64, i64, i64, ctypes.c_int]
+        lib.oracle_hgemm_sums_f64.restype = ctypes.c_int
+        lib.oracle_hgemm_entries.argtypes = [u16p, u16p, i64, ctypes.c_void_p,
+                                             ctypes.c_void_p, i64, u16p]
+        lib.oracle_hgemm_entries.restype = None
+        lib.oracle_fp16_to_double.argtypes = [ctypes.c_uint16]
+        lib.oracle_fp16_to_double.restype = ctypes.c_double
+        lib.oracle_double_to_fp16.argtypes = [ctypes.c_double]
+        lib.oracle_double_to_fp16.restype = ctypes.c_uint16
+        _lib = lib
+    return _lib
+
+
+def _threads(nthreads):
+    return int(nthreads) if nthreads else (os.cpu_count() or 1)
+
+
+def _operands(a, b):
+    a = np.ascontiguousarray(a, dtype=np.float16)
+    b = np.ascontiguousarray(b, dtype=np.float16)
+    if a.ndim != 2 or b.ndim != 2 or a.shape[1] != b.shape[1]:
+        raise ValueError("a must be (M, K) and b (N, K): row j of b is column j of B")
+    return a, b
+
+
+def hgemm(a: np.ndarray, b: np.ndarray, nthreads: int | None = None) -> np.ndarray:
+    """C (M, N) float16 for A = a (M, K) and B whose column j is b[j] (b is (N, K))."""
+    a, b = _operands(a, b)
+    M, K = a.shape
+    N = b.shape[0]
+    c = np.empty((M, N), dtype=np.float16)
+    rc = _load().oracle_hgemm(a.ctypes.data, b.ctypes.data, c.ctypes.data, M, N, K,
+                              _threads(nthreads))
+    if rc != 0:
+        raise MemoryError("oracle_hgemm could not allocate its thread bookkeeping")
+    return c
+
+
+def sums_f64(a: np.ndarray, b: np.ndarray, nthreads: int | None = None) -> np.ndarray:
+    """The FP64 sums before the final rounding, (M, N) float64."""
+    a, b = _operands(a, b)
+    M, K = a.shape
+    N = b.shape[0]
+    s = np.empty((M, N), dtype=np.float64)
+    rc = _load().oracle_hgemm_sums_f64(a.ctypes.data, b.ctypes.data, s.ctypes.data, M, N, K,
+                                       _threads(nthreads))
+    if rc != 0:
+        raise MemoryError("oracle_hgemm_sums_f64 could not allocate its thread bookkeeping")
+    return s
+
+
+def entries(a: np.ndarray, b: np.ndarray, rows, cols) -> np.ndarray:
+    """C[rows[t], cols[t]] for each t, float16; for shapes too large to do whole."""
+    a, b = _operands(a, b)
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    cols = np.ascontiguousarray(cols, dtype=np.int64)
+    if rows.shape != cols.shape:
+        raise ValueError("rows and cols must have the same length")
+    if rows.size and (rows.min() < 0 or rows.max() >= a.shape[0]
+                      or cols.min() < 0 or cols.max() >= b.shape[0]):
+        raise IndexError("entry index out of range")
+    out = np.empty(rows.shape, dtype=np.float16)
+    _load().oracle_hgemm_entries(a.ctypes.data, b.ctypes.data, a.shape[1], rows.ctypes.data,
+                                 cols.ctypes.data, rows.size, out.ctypes.data)
+    return out
+
+
+def fp16_to_double(bits: int) -> float:
+    """Decodes one binary16 bit pattern."""
+    return _load().oracle_fp16_to_double(bits & 0xFFFF)
+
+
+def double_to_fp16(x: float) -> int:
+    """Rounds one double to the nearest binary16 (ties to even); returns the bits."""
+    return int(_load().oracle_double_to_fp16(float(x)))

@@ -1,0 +1,184 @@
+/*
+ * The oracle for the FP16 HGEMM C = A·B. TEST INFRASTRUCTURE ONLY: the
+ * tests, the smoke check and the benchmark's CPU-baseline leg are the only
+ * code allowed to load it. It shares no code, header or table with the CUDA
+ * path in tensor_core_dense_fp16_gb300/.
+ *
+ * What it computes (the plain definition; no blocking, no reordering):
+ *
+ *     C[i*N + j] = fp16_rne( sum_{k=0}^{K-1} (double)A[i*K + k] * (double)B[j*K + k] )
+ *
+ *  - Problem and layouts: "Nvidia Tensor Core-MMA PTX编程入门", §4 示例 — A is
+ *    M×K row-major, B is K×N column-major (column j is K contiguous values),
+ *    C is M×N row-major, all FP16.
+ *  - Products of FP16 values, summed at higher precision than FP16:
+ *    "GPU架构与CUDA", 混合精度核函数 (FP16 × FP16 accumulated in FP32). The
+ *    oracle sums in FP64, which is at least as precise: every FP16×FP16
+ *    product is exact in FP64 (11 + 11 significand bits fit in 53), and the
+ *    sum runs in increasing k.
+ *  - Terms outside the matrix contribute nothing and nothing outside C is
+ *    written: "GPU架构与CUDA", 共享内存与分块 (zero-filled tile loads, the
+ *    guarded store). Here that is simply the loop bounds.
+ *  - The pages do not state how the accumulator becomes FP16; the reading
+ *    taken is one IEEE round-to-nearest-even (overflow to ±Inf).
+ *
+ * Build: gcc -O2 -fno-fast-math -ffp-contract=off (no FMA contraction, so
+ * x86-64 and AArch64 hosts produce identical bits).
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+
+/* ---- FP16 (IEEE binary16) <-> double, written out from the format ---- */
+
+/* binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits. */
+double oracle_fp16_to_double(uint16_t h)
+{
+    const int sign = (h >> 15) & 1;
+    const int expo = (h >> 10) & 0x1f;
+    const int frac = h & 0x3ff;
+    double v;
+    if (expo == 0) {
+        v = ldexp((double)frac, -24);            /* subnormal: frac · 2^-24 */
+    } else if (expo == 31) {
+        v = frac ? NAN : INFINITY;
+    } else {
+        v = ldexp((double)(1024 + frac), expo - 25); /* (1.frac) · 2^(e-15) */
+    }
+    return sign ? -v : v;
+}
+
+/* Round a double to the nearest binary16, ties to even. */
+uint16_t oracle_double_to_fp16(double x)
+{
+    if (isnan(x))
+        return 0x7e00;
+    const uint16_t sign = signbit(x) ? 0x8000 : 0;
+    double a = fabs(x);
+    /* 65504 is the largest finite value; the midpoint to 2^16 is 65520 and a
+     * tie there goes to the even neighbour, 2^16, which overflows. */
+    if (a >= 65520.0)
+        return sign | 0x7c00;
+    if (a < ldexp(1.0, -14)) {
+        /* subnormal range: the grid is multiples of 2^-24; rint rounds to the
+         * nearest integer, ties to even (default rounding mode). A result of
+         * 1024 is the smallest normal, whose encoding is also 1024. */
+        double q = rint(a * ldexp(1.0, 24));
+        return sign | (uint16_t)q;
+    }
+    int e2;
+    double f = frexp(a, &e2);      /* a = f · 2^e2, f in [0.5, 1) */
+    int e = e2 - 1;                /* a = (2f) · 2^e, 2f in [1, 2) */
+    double q = rint(ldexp(f, 11)); /* (2f)·1024, rounded: in [1024, 2048] */
+    if (q == 2048.0) {
+        q = 1024.0;
+        e += 1;
+    }
+    if (e > 15)
+        return sign | 0x7c00;
+    return sign | (uint16_t)(((e + 15) << 10) | ((int)q - 1024));
+}
+
+/* ---- the contraction ---- */
+
+/* One entry, pre-rounding: sum over k in increasing order, in FP64. */
+static double dot_f64(const uint16_t *A, const uint16_t *B, int64_t i, int64_t j, int64_t K)
+{
+    double s = 0.0;
+    const uint16_t *a = A + i * K;
+    const uint16_t *b = B + j * K;
+    for (int64_t k = 0; k < K; ++k)
+        s += oracle_fp16_to_double(a[k]) * oracle_fp16_to_double(b[k]);
+    return s;
+}
+
+struct rows_job {
+    const uint16_t *A, *B;
+    uint16_t *C;     /* FP16 result, or NULL */
+    double *S;       /* FP64 pre-rounding sums, or NULL */
+    int64_t M, N, K;
+    int64_t row_lo, row_hi;
+};
+
+static void *rows_worker(void *arg)
+{
+    struct rows_job *jb = (struct rows_job *)arg;
+    for (int64_t i = jb->row_lo; i < jb->row_hi; ++i)
+        for (int64_t j = 0; j < jb->N; ++j) {
+            double s = dot_f64(jb->A, jb->B, i, j, jb->K);
+            if (jb->S)
+                jb->S[i * jb->N + j] = s;
+            if (jb->C)
+                jb->C[i * jb->N + j] = oracle_double_to_fp16(s);
+        }
+    return NULL;
+}
+
+/* Runs rows [0, M) split over `nthreads` threads (1 if nthreads < 1). */
+static int run_rows(const uint16_t *A, const uint16_t *B, uint16_t *C, double *S,
+                    int64_t M, int64_t N, int64_t K, int nthreads)
+{
+    if (M <= 0 || N <= 0)
+        return 0;
+    if (nthreads < 1)
+        nthreads = 1;
+    if (nthreads > M)
+        nthreads = (int)M;
+    pthread_t *th = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    struct rows_job *jobs = (struct rows_job *)calloc((size_t)nthreads, sizeof(struct rows_job));
+    if (!th || !jobs) {
+        free(th);
+        free(jobs);
+        return -1;
+    }
+    char *live = (char *)calloc((size_t)nthreads, 1);
+    if (!live) {
+        free(th);
+        free(jobs);
+        return -1;
+    }
+    for (int t = 0; t < nthreads; ++t) {
+        struct rows_job jb = {A, B, C, S, M, N, K, M * t / nthreads, M * (t + 1) / nthreads};
+        jobs[t] = jb;
+        if (t == 0)
+            continue;
+        if (pthread_create(&th[t], NULL, rows_worker, &jobs[t]) == 0)
+            live[t] = 1;
+        else
+            rows_worker(&jobs[t]);   /* could not start a thread: do it here */
+    }
+    rows_worker(&jobs[0]);
+    for (int t = 1; t < nthreads; ++t)
+        if (live[t])
+            pthread_join(th[t], NULL);
+    free(live);
+    free(th);
+    free(jobs);
+    return 0;
+}
+
+/* C (M×N row-major FP16) = A·B as defined above. Returns 0, or -1 if memory
+ * for the thread bookkeeping could not be had. */
+int oracle_hgemm(const uint16_t *A, const uint16_t *B, uint16_t *C,
+                 int64_t M, int64_t N, int64_t K, int nthreads)
+{
+    return run_rows(A, B, C, NULL, M, N, K, nthreads);
+}
+
+/* The FP64 sums before the final rounding (M×N row-major doubles). */
+int oracle_hgemm_sums_f64(const uint16_t *A, const uint16_t *B, double *S,
+                          int64_t M, int64_t N, int64_t K, int nthreads)
+{
+    return run_rows(A, B, NULL, S, M, N, K, nthreads);
+}
+
+/* Selected entries (rows[t], cols[t]) for t < count, for spot checks of
+ * shapes too large to compute whole. */
+void oracle_hgemm_entries(const uint16_t *A, const uint16_t *B, int64_t K,
+                          const int64_t *rows, const int64_t *cols, int64_t count,
+                          uint16_t *out)
+{
+    for (int64_t t = 0; t < count; ++t)
+        out[t] = oracle_double_to_fp16(dot_f64(A, B, rows[t], cols[t], K));
+}

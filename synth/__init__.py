@@ -1,0 +1,104 @@
+"""Seeded synthetic operands for the FP16 HGEMM C = A·B.
+
+This module is shared by the tests and the benchmark. It holds no arithmetic
+of the method itself (no products, no sums, no output rounding): it only
+draws the two operands, so that the oracle and the CUDA path can be fed the
+same bytes.
+
+Layouts follow the problem statement of "Nvidia Tensor Core-MMA PTX编程入门",
+§4 示例: A is M×K row-major (element (i, k) at A[i*K + k]) and B is K×N
+column-major, stored as N columns of K contiguous values (element (k, j) at
+B[j*K + k]). Both arrays are returned as ``numpy.float16`` in that storage
+order.
+
+Random numbers come from splitmix64 in counter form: draw number t of a
+stream with seed s is mix(s + (t + 1)·γ) with γ = 0x9E3779B97F4A7C15 and mix
+the splitmix64 finaliser (Steele, Lea and Flood, "Fast splittable
+pseudorandom number generators", OOPSLA 2014). A uniform in [0, 1) is the top
+53 bits scaled by 2^-53. The A stream uses draws 0 .. M*K-1 in A's storage
+order; the B stream continues with draws M*K .. M*K+N*K-1 in B's storage
+order (Gaussian draws take two uniforms per value, so their counters double).
+
+Value recipes (the workloads of the benchmark configurations):
+  * ``uniform``  : 2u - 1 rounded to the nearest FP16 (ties to even);
+  * ``int``      : floor(5u) - 2, i.e. integers uniform in {-2, ..., 2};
+  * ``normal``   : Box-Muller on consecutive uniform pairs
+                   z = sqrt(-2 ln(1 - u1)) * cos(2π u2); A ~ N(0, 1) and
+                   B ~ N(0, 1)/sqrt(K), each rounded to FP16.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+GAMMA = np.uint64(0x9E3779B97F4A7C15)
+_M1 = np.uint64(0xBF58476D1CE4E5B9)
+_M2 = np.uint64(0x94D049BB133111EB)
+
+# chunking keeps the float64 temporaries of the 8192 x 8192 operands bounded
+_CHUNK = 1 << 22
+
+
+def splitmix64(seed: int, start: int, count: int) -> np.ndarray:
+    """Draws ``start .. start+count-1`` of the splitmix64 stream ``seed``."""
+    t = np.arange(start + 1, start + count + 1, dtype=np.uint64)
+    with np.errstate(over="ignore"):
+        z = np.uint64(seed & 0xFFFFFFFFFFFFFFFF) + t * GAMMA
+        z = (z ^ (z >> np.uint64(30))) * _M1
+        z = (z ^ (z >> np.uint64(27))) * _M2
+        z = z ^ (z >> np.uint64(31))
+    return z
+
+
+def uniform01(seed: int, start: int, count: int) -> np.ndarray:
+    """u = (x >> 11) · 2^-53, exactly representable in float64, in [0, 1)."""
+    x = splitmix64(seed, start, count)
+    return (x >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
+
+
+def _fill(seed: int, start: int, count: int, kind: str, scale: float) -> np.ndarray:
+    out = np.empty(count, dtype=np.float16)
+    per = 2 if kind == "normal" else 1
+    for lo in range(0, count, _CHUNK):
+        n = min(_CHUNK, count - lo)
+        if kind == "uniform":
+            v = 2.0 * uniform01(seed, start + lo, n) - 1.0
+        elif kind == "int":
+            v = np.floor(5.0 * uniform01(seed, start + lo, n)) - 2.0
+        elif kind == "normal":
+            u = uniform01(seed, start + per * lo, per * n)
+            u1, u2 = u[0::2], u[1::2]
+            v = np.sqrt(-2.0 * np.log1p(-u1)) * np.cos(2.0 * np.pi * u2) * scale
+        else:
+            raise ValueError(f"unknown value kind {kind!r}")
+        out[lo:lo + n] = v.astype(np.float16)
+    return out
+
+
+def operands(M: int, N: int, K: int, seed: int, kind: str = "uniform"):
+    """Returns (A, B): A as an (M, K) array, B as an (N, K) array whose row j
+    is column j of the K×N operand, both float16 and C-contiguous."""
+    per = 2 if kind == "normal" else 1
+    b_scale = 1.0 / np.sqrt(K) if (kind == "normal" and K > 0) else 1.0
+    a = _fill(seed, 0, M * K, kind, 1.0).reshape(M, K)
+    b = _fill(seed, per * M * K, N * K, kind, b_scale).reshape(N, K)
+    return a, b
+
+
+# The benchmark workloads, each named by what it is. The integer variant of
+# the 256-cube uses the same shape with the seed offset by 100.
+WORKLOADS = {
+    "hgemm_256": dict(M=256, N=256, K=256, kind="uniform", seed=1000),
+    "hgemm_256_int": dict(M=256, N=256, K=256, kind="int", seed=1100),
+    "hgemm_2048": dict(M=2048, N=2048, K=2048, kind="uniform", seed=1001),
+    "hgemm_1000_ragged": dict(M=1000, N=1000, K=1000, kind="uniform", seed=1002),
+    "hgemm_8192": dict(M=8192, N=8192, K=8192, kind="normal", seed=1003),
+    "hgemm_4096x256x4096_skinny": dict(M=4096, N=256, K=4096, kind="uniform", seed=1004),
+}
+
+
+def workload(name: str):
+    """(A, B, spec) for a named workload."""
+    spec = WORKLOADS[name]
+    a, b = operands(spec["M"], spec["N"], spec["K"], spec["seed"], spec["kind"])
+    return a, b, spec

@@ -1,0 +1,262 @@
+"""Pins for the oracle, each against something other than the oracle itself.
+
+CPU only. The pins are chosen so that a plausible slip anywhere in the
+oracle fails at least one of them: a wrong rounding mode (tie fixtures,
+exhaustive codec, numpy rounding), a transposed or mis-indexed operand
+(identity operands, non-symmetric brute force), a dropped term (brute force,
+integer exactness), FP16-width accumulation (the wide-accumulation fixture),
+an overflow or subnormal slip (fixtures, exhaustive codec).
+"""
+
+import os
+import random
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+
+# ---------------------------------------------------------------------------
+# A textbook binary16 rounding on exact rationals, written independently of
+# the oracle's frexp/rint code: used by the brute-force pin.
+
+
+def fraction_to_fp16_bits(x: Fraction) -> int:
+    """Round-to-nearest-even of an exact rational to IEEE binary16 bits."""
+    sign = 0x8000 if x < 0 else 0
+    a = -x if x < 0 else x
+    if a == 0:
+        return sign
+    # exponent e with 2^e <= a < 2^(e+1), clamped to the subnormal floor -14
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    if Fraction(2) ** e > a:
+        e -= 1
+    elif Fraction(2) ** (e + 1) <= a:
+        e += 1
+    e = max(e, -14)
+    quantum = Fraction(2) ** (e - 10)
+    n = a / quantum
+    fl = n.numerator // n.denominator
+    rem = n - fl
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and fl % 2 == 1):
+        fl += 1
+    # fl is the significand on the 2^(e-10) grid, in [0, 2048]
+    if fl == 2048:
+        fl, e = 1024, e + 1
+    if e > 15:
+        return sign | 0x7C00
+    if fl < 1024:  # subnormal (only reachable with e == -14)
+        return sign | fl
+    return sign | ((e + 15) << 10) | (fl - 1024)
+
+
+def bits(x: np.ndarray) -> np.ndarray:
+    return np.ascontiguousarray(x, dtype=np.float16).view(np.uint16)
+
+
+def random_fp16(rng, shape, lo_exp=-6, hi_exp=4):
+    """Random FP16 values over several binades, both signs, some zeros."""
+    mant = rng.integers(0, 1024, size=shape)
+    expo = rng.integers(lo_exp + 15, hi_exp + 15, size=shape)
+    sgn = rng.integers(0, 2, size=shape)
+    b = (sgn << 15) | (expo << 10) | mant
+    b = np.where(rng.random(shape) < 0.05, 0, b)
+    return b.astype(np.uint16).view(np.float16)
+
+
+# ---------------------------------------------------------------------------
+# golden fixtures (hand-derived; citations in the file)
+
+
+def load_golden(path):
+    cases, cur = [], None
+    with open(path, encoding="utf-8") as f:
+        for raw in f:
+            line = raw.split("#", 1)[0].strip()
+            if not line:
+                continue
+            tag, *rest = line.split()
+            if tag == "case":
+                cur = {"name": rest[0]}
+                cases.append(cur)
+            elif tag == "dims":
+                cur["dims"] = tuple(int(v) for v in rest)
+            elif tag in ("A", "B"):
+                cur[tag] = [float(v) for v in rest]
+            elif tag == "C":
+                cur["C"] = [int(v, 16) for v in rest]
+    return cases
+
+
+def test_golden_hand_worked_cases(golden_dir):
+    cases = load_golden(os.path.join(golden_dir, "hand_worked_cases.txt"))
+    assert len(cases) >= 6
+    for cs in cases:
+        M, N, K = cs["dims"]
+        a = np.array(cs["A"], dtype=np.float64).reshape(M, K)
+        b = np.array(cs["B"], dtype=np.float64).reshape(N, K)
+        # every fixture value must be exactly representable
+        assert np.array_equal(a.astype(np.float16).astype(np.float64), a), cs["name"]
+        assert np.array_equal(b.astype(np.float16).astype(np.float64), b), cs["name"]
+        c = oracle.hgemm(a.astype(np.float16), b.astype(np.float16))
+        got = bits(c).reshape(-1).tolist()
+        assert got == cs["C"], (cs["name"], [hex(v) for v in got])
+
+
+# ---------------------------------------------------------------------------
+# the FP16 codec
+
+
+def test_decode_exhaustive_against_numpy():
+    allbits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = allbits.view(np.float16).astype(np.float64)
+    got = np.array([oracle.fp16_to_double(int(h)) for h in allbits])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(ref[~nan]))
+
+
+def test_encode_roundtrip_exhaustive():
+    for h in range(65536):
+        e, f = (h >> 10) & 0x1F, h & 0x3FF
+        if e == 31 and f:
+            continue  # NaN payloads are not preserved
+        assert oracle.double_to_fp16(oracle.fp16_to_double(h)) == h, hex(h)
+
+
+def test_encode_against_numpy_including_exact_midpoints():
+    rng = np.random.default_rng(7)
+    xs = []
+    # every midpoint between adjacent finite FP16 values (exact in float64),
+    # and points just either side of it
+    pos = np.arange(0, 0x7C00, dtype=np.uint16).view(np.float16).astype(np.float64)
+    mids = (pos[:-1] + pos[1:]) / 2
+    xs += list(mids) + list(np.nextafter(mids, 0)) + list(np.nextafter(mids, np.inf))
+    xs += [65504.0, 65519.99, 65520.0, 65536.0, 1e6, 2.0 ** -25, 2.0 ** -26, 3 * 2.0 ** -26]
+    xs += list(rng.standard_normal(20000) * 10.0 ** rng.uniform(-9, 5, 20000))
+    xs = np.array(xs, dtype=np.float64)
+    xs = np.concatenate([xs, -xs])
+    with np.errstate(over="ignore"):
+        ref = xs.astype(np.float16).view(np.uint16)
+    got = np.array([oracle.double_to_fp16(x) for x in xs], dtype=np.uint16)
+    bad = np.nonzero(got != ref)[0]
+    assert bad.size == 0, [(xs[i], hex(got[i]), hex(ref[i])) for i in bad[:5]]
+
+
+# ---------------------------------------------------------------------------
+# the contraction
+
+
+def test_bruteforce_exact_rationals_tiny_shapes():
+    """With K <= 6 the FP64 sum of FP16 products is exact; the oracle must
+    equal the exact rational sum rounded to FP16 (ties to even), bit for bit."""
+    rng = np.random.default_rng(11)
+    for trial in range(60):
+        M, N, K = (int(v) for v in rng.integers(1, 7, size=3))
+        a = random_fp16(rng, (M, K))
+        b = random_fp16(rng, (N, K))
+        got = bits(oracle.hgemm(a, b))
+        for i in range(M):
+            for j in range(N):
+                s = sum(Fraction(float(a[i, k])) * Fraction(float(b[j, k])) for k in range(K))
+                assert got[i, j] == fraction_to_fp16_bits(s), (trial, i, j, s)
+
+
+def test_bruteforce_handmade_ties():
+    """Sums built to land exactly on FP16 midpoints at several binades."""
+    rnd = random.Random(5)
+    for _ in range(200):
+        e = rnd.randint(-10, 13)
+        q = Fraction(2) ** (e - 10)  # FP16 spacing in binade 2^e
+        n = rnd.randint(1024, 2047)
+        target = (n + Fraction(1, 2)) * q  # a midpoint
+        x = float(n * q)
+        y = float(q / 2)
+        a = np.array([[x, y]], dtype=np.float16)
+        b = np.array([[1.0, 1.0]], dtype=np.float16)
+        if float(a[0, 0]) != x or float(a[0, 1]) != y:
+            continue  # y underflowed FP16; skip
+        got = int(bits(oracle.hgemm(a, b))[0, 0])
+        assert got == fraction_to_fp16_bits(target), (e, n)
+
+
+def test_identity_and_zero_operands():
+    rng = np.random.default_rng(3)
+    M, K, N = 37, 29, 23
+    b = random_fp16(rng, (N, K))
+    # A = I (M = K): C[i, j] = B[i, j] = b[j, i]
+    eye_k = np.eye(K, dtype=np.float16)
+    c = oracle.hgemm(eye_k, b)
+    assert np.array_equal(bits(c), bits(b.T))
+    # B = I (K = N): C = A exactly
+    a = random_fp16(rng, (M, K))
+    c = oracle.hgemm(a, np.eye(K, dtype=np.float16))
+    assert np.array_equal(bits(c), bits(a))
+    # zeros give +0 everywhere
+    assert np.all(bits(oracle.hgemm(np.zeros((M, K), np.float16), b)) == 0)
+    assert np.all(bits(oracle.hgemm(a, np.zeros((N, K), np.float16))) == 0)
+    # a permutation picks single columns, in order
+    perm = rng.permutation(K)
+    p = np.zeros((K, K), dtype=np.float16)
+    p[np.arange(K), perm] = 1
+    c = oracle.hgemm(p, b)  # C[i, j] = b[j, perm[i]]
+    assert np.array_equal(bits(c), bits(b[:, perm].T))
+
+
+def test_rank_one_closed_form():
+    """A = 1 (all ones), column j of B constant c_j: C[i, j] = K * c_j."""
+    M, N, K = 5, 7, 12
+    cvals = np.array([0.5, -1.25, 3.0, 0.0, 2.0, -0.75, 8.0], dtype=np.float16)
+    a = np.ones((M, K), dtype=np.float16)
+    b = np.repeat(cvals[:, None], K, axis=1)
+    c = oracle.hgemm(a, b).astype(np.float64)
+    assert np.array_equal(c, np.tile(K * cvals.astype(np.float64), (M, 1)))
+
+
+@pytest.mark.parametrize("M,N,K", [(17, 13, 256), (64, 64, 256), (100, 3, 250)])
+def test_integer_operands_equal_int64_product(M, N, K):
+    """Entries in {-2..2} with K <= 256: |C| <= 1024, every value exact."""
+    rng = np.random.default_rng(M * 1000 + N)
+    ai = rng.integers(-2, 3, size=(M, K))
+    bi = rng.integers(-2, 3, size=(N, K))
+    c = oracle.hgemm(ai.astype(np.float16), bi.astype(np.float16))
+    assert np.array_equal(c.astype(np.int64), ai @ bi.T)
+
+
+@pytest.mark.parametrize("M,N,K", [(64, 64, 64), (256, 8, 1000)])
+def test_fp64_sums_against_numpy_matmul(M, N, K):
+    rng = np.random.default_rng(M + N + K)
+    a = (2 * rng.random((M, K)) - 1).astype(np.float16)
+    b = (2 * rng.random((N, K)) - 1).astype(np.float16)
+    s = oracle.sums_f64(a, b)
+    ref = a.astype(np.float64) @ b.astype(np.float64).T
+    scale = np.abs(a.astype(np.float64)) @ np.abs(b.astype(np.float64)).T
+    assert np.all(np.abs(s - ref) <= 1e-12 * np.maximum(scale, 1e-300))
+    # the FP16 result is the sums rounded, element by element
+    c = oracle.hgemm(a, b)
+    assert np.array_equal(bits(c), bits(s.astype(np.float16)))
+
+
+def test_entries_and_threads_agree_with_full_product():
+    rng = np.random.default_rng(17)
+    a = (2 * rng.random((45, 130)) - 1).astype(np.float16)
+    b = (2 * rng.random((33, 130)) - 1).astype(np.float16)
+    full = oracle.hgemm(a, b, nthreads=1)
+    for nt in (2, 5, 64):
+        assert np.array_equal(bits(oracle.hgemm(a, b, nthreads=nt)), bits(full))
+    rows = rng.integers(0, 45, size=200)
+    cols = rng.integers(0, 33, size=200)
+    assert np.array_equal(bits(oracle.entries(a, b, rows, cols)), bits(full[rows, cols]))
+
+
+def test_degenerate_shapes():
+    a = np.zeros((0, 5), np.float16)
+    b = np.ones((4, 5), np.float16)
+    assert oracle.hgemm(a, b).shape == (0, 4)
+    # K = 0: every entry is the empty sum, +0
+    c = oracle.hgemm(np.zeros((3, 0), np.float16), np.zeros((2, 0), np.float16))
+    assert c.shape == (3, 2) and np.all(bits(c) == 0)
+    with pytest.raises(ValueError):
+        oracle.hgemm(np.zeros((3, 4), np.float16), np.zeros((2, 5), np.float16))
