@@ -1,0 +1,448 @@
+#!/usr/bin/env python
+"""Benchmark of the FP16 HGEMM C = A·B on GB300.
+
+One step is one C = A·B through the C ABI on the workload's operands, which
+are resident in HBM before the timed region starts. Every timed launch is
+bracketed by CUDA events on the stream it is launched on, and L2 is flushed
+(a write of twice its size) before each launch, outside the events.
+
+Prints one JSON line on rank 0. Under torchrun each rank runs an independent
+replica of the workload on its own GPU (the product does not shard: there is
+no data-path collective); `value` is the work of all ranks over the slowest
+rank's time.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME]
+
+`--impl reference` times the oracle (plain C, FP64) on this host's cores on a
+bounded sample of the same workload: the comparison program, not a target.
+"""
+
+from __future__ import annotations
+
+import argparse
+import datetime
+import glob
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "HGEMM TFLOP/s (2MNK/t) at 8192³ fp16 and % of GB300 dense FP16 peak"
+UNIT = "TFLOP/s"
+DEFAULT_WORKLOAD = "hgemm_8192"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# Nominal dense FP16 : BF16 tensor throughput on this architecture (both
+# 2.25 PFLOP/s dense per GPU), so the BF16 measured peak is the FP16 peak.
+FP16_PER_BF16 = 1.0
+DESCRIPTIONS = {
+    "hgemm_8192": "M=N=K=8192 fp16; A row-major N(0,1), B col-major N(0,1)/sqrt(K); "
+                  "fp32 accumulate; C fp16 row-major",
+    "hgemm_2048": "M=N=K=2048 fp16; A, B uniform[-1,1]",
+    "hgemm_1000_ragged": "M=N=K=1000 fp16 (ragged tiles); A, B uniform[-1,1]",
+    "hgemm_256": "M=N=K=256 fp16; A, B uniform[-1,1]",
+    "hgemm_256_int": "M=N=K=256 fp16; A, B integers in {-2..2}",
+    "hgemm_4096x256x4096_skinny": "M=4096, N=256, K=4096 fp16; A, B uniform[-1,1] "
+                                  "(bandwidth-bound)",
+}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer measurement")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="target CPU time of the oracle sample")
+    ap.add_argument("--reference-seconds", type=float, default=120.0,
+                    help="target wall time of a whole --impl reference run")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------- helpers
+
+def flops_of(spec):
+    return 2.0 * spec["M"] * spec["N"] * spec["K"]
+
+
+def bytes_of(spec):
+    M, N, K = spec["M"], spec["N"], spec["K"]
+    return 2.0 * (M * K + N * K + M * N)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_sources_sha():
+    h = hashlib.sha256()
+    files = sorted(glob.glob(os.path.join(ROOT, "tensor_core_dense_fp16_gb300", "csrc", "*")))
+    for f in files:
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel, workload, sha):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel sources (a `traffic_record:` JSON line in profiles/)."""
+    for path in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.md"))):
+        with open(path, encoding="utf-8") as f:
+            for line in f:
+                m = re.match(r"\s*traffic_record:\s*(\{.*\})\s*$", line)
+                if not m:
+                    continue
+                try:
+                    rec = json.loads(m.group(1))
+                except ValueError:
+                    continue
+                if (rec.get("kernel") == kernel and rec.get("workload") == workload
+                        and rec.get("source_sha") == sha):
+                    return float(rec["bytes_per_launch"])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling in the background."""
+
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        self.t_start = time.time()
+
+    def mark(self):
+        return time.time()
+
+    def stop(self, t0, t1):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 10:
+                    try:
+                        ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f")
+                    except ValueError:
+                        continue
+                    rows.append([ts.timestamp()] + parts[2:])
+        os.unlink(self.path)
+        # keep the samples taken inside the timed region, widened by one
+        # sampling period so that a short region still gets one
+        inside = [r for r in rows if t0 - 0.1 <= r[0] <= t1 + 0.1]
+        use = inside or rows[-3:]
+        sm = [float(r[1]) for r in use if _num(r[1])]
+        smax = [float(r[2]) for r in use if _num(r[2])]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in use for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(use),
+                "power_w_max": max((float(r[3]) for r in use if _num(r[3])), default=None)}
+
+
+def _num(s):
+    try:
+        float(s)
+        return True
+    except ValueError:
+        return False
+
+
+def nvsmi_id(torch, dev, local):
+    """An nvidia-smi --id for this process's GPU (nvidia-smi ignores
+    CUDA_VISIBLE_DEVICES, so prefer the device UUID)."""
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        if u:
+            return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        pass
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        ids = [v.strip() for v in vis.split(",") if v.strip()]
+        if local < len(ids):
+            return ids[local]
+    return str(local)
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ------------------------------------------------------------ the oracle leg
+
+def oracle_sample(spec, a, b, target_s, nthreads):
+    """Times the oracle on whole rows of C: returns (flops, seconds, rows)."""
+    import oracle
+    N, K = spec["N"], spec["K"]
+    # calibrate on one row per thread, then size the sample to target_s
+    rows = min(nthreads, spec["M"])
+    t = time.perf_counter()
+    oracle.hgemm(a[:rows], b, nthreads=nthreads)
+    dt = time.perf_counter() - t
+    if dt < target_s:
+        scale = max(1, int(target_s / max(dt, 1e-6)))
+        rows = min(spec["M"], rows * scale)
+        t = time.perf_counter()
+        oracle.hgemm(a[:rows], b, nthreads=nthreads)
+        dt = time.perf_counter() - t
+    return 2.0 * rows * N * K, dt, rows
+
+
+def run_reference(args, spec, a, b, world, rank):
+    if rank != 0:
+        return 0
+    nthreads = os.cpu_count() or 1
+    per_step = max(0.5, args.reference_seconds / max(1, args.steps + args.warmup))
+    import oracle
+    oracle.build()
+    N, K = spec["N"], spec["K"]
+    rows = min(nthreads, spec["M"])
+    t = time.perf_counter()
+    oracle.hgemm(a[:rows], b, nthreads=nthreads)
+    dt = time.perf_counter() - t
+    base = rows
+    rows = min(spec["M"], int(rows * per_step / max(dt, 1e-6)))
+    rows = max(base, rows - rows % base)  # whole rows, a multiple of the thread count
+    times = []
+    for i in range(args.warmup + args.steps):
+        t = time.perf_counter()
+        oracle.hgemm(a[:rows], b, nthreads=nthreads)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t)
+    total = sum(times)
+    value = 2.0 * rows * N * K * len(times) / total / 1e12
+    sample = (f"{rows} whole rows of C per step ({rows}x{N} outputs, K={K}) of the "
+              f"{args.workload} workload; FP64 oracle, {nthreads} threads")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / len(times), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{args.workload}: {DESCRIPTIONS.get(args.workload, '')}",
+                   "M": spec["M"], "N": spec["N"], "K": spec["K"], "seed": spec["seed"]},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": nthreads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------- our leg
+
+def run_ours(args, spec, a, b, world, rank, local):
+    import torch
+    import tensor_core_dense_fp16_gb300 as tc
+
+    tc.load()  # fails loudly if the extension is missing
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    M, N, K = spec["M"], spec["N"], spec["K"]
+    flops = flops_of(spec)
+    stream = torch.cuda.current_stream(dev)
+
+    da = torch.from_numpy(a).to(dev)
+    db = torch.from_numpy(b).to(dev)
+    dc = torch.empty((M, N), dtype=torch.float16, device=dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2 // 4 + 1, dtype=torch.float32, device=dev)
+    path = tc.hgemm_select_path(da, db, dc, M, N, K)
+
+    def step():
+        tc.hgemm(da, db, dc, M, N, K, stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    if tc.hgemm_device_status(stream) != tc.HGEMM_OK:
+        raise RuntimeError("a kernel wait timed out during warm-up")
+
+    sampler = ClockSampler(nvsmi_id(torch, dev, local))
+    sampler.start()
+    time.sleep(0.15)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t0 = time.time()
+    for s, e in evs:
+        flush.zero_()
+        s.record(stream)
+        step()
+        e.record(stream)
+    torch.cuda.synchronize(dev)
+    t1 = time.time()
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop(t0, t1)
+    if tc.hgemm_device_status(stream) != tc.HGEMM_OK:
+        raise RuntimeError("a kernel wait timed out in the timed region")
+    times_ms = [s.elapsed_time(e) for s, e in evs]
+    total_ms = sum(times_ms)
+    if dist:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    mean_ms = total_ms / args.steps
+    median_ms = statistics.median(times_ms)
+    value = world * args.steps * flops / (total_ms * 1e-3) / 1e12
+
+    # ---- end to end through the host-buffer entry point
+    e2e = None
+    if not args.no_e2e:
+        ha = torch.from_numpy(a).pin_memory()
+        hb = torch.from_numpy(b).pin_memory()
+        hc = torch.empty((M, N), dtype=torch.float16).pin_memory()
+        e_steps = max(3, min(args.steps, 20))
+        for _ in range(2):
+            tc.hgemm_host(ha, hb, hc, M, N, K, da, db, dc, stream)
+        torch.cuda.synchronize(dev)
+        s_ev, e_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if dist:
+            dist.barrier()
+        s_ev.record(stream)
+        for _ in range(e_steps):
+            tc.hgemm_host(ha, hb, hc, M, N, K, da, db, dc, stream)
+        e_ev.record(stream)
+        torch.cuda.synchronize(dev)
+        e_ms = s_ev.elapsed_time(e_ev)
+        if dist:
+            t = torch.tensor([e_ms], dtype=torch.float64, device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        if tc.hgemm_device_status(stream) != tc.HGEMM_OK:
+            raise RuntimeError("a kernel wait timed out in the end-to-end run")
+        e2e = {"value": world * e_steps * flops / (e_ms * 1e-3) / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": 2 * (M * K + N * K), "d2h_bytes_per_step": 2 * M * N,
+               "ms_per_step": e_ms / e_steps}
+
+    # ---- roofline of the dominant (only) kernel
+    peaks, peak_src = load_peaks()
+    kernel = {tc.HGEMM_PATH_TC: "hgemm_tc", tc.HGEMM_PATH_SKINNY: "hgemm_skinny",
+              tc.HGEMM_PATH_GENERIC: "hgemm_generic"}.get(path, "other")
+    ai = flops / bytes_of(spec)
+    ridge = peaks["bf16_tflops"] * FP16_PER_BF16 * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    sha = kernel_sources_sha()
+    traffic = profiled_traffic(kernel, args.workload, sha)
+    if ai >= ridge:
+        peak = peaks["bf16_tflops"] * FP16_PER_BF16
+        achieved = flops / (mean_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": traffic,
+                "peak_source": f"{peak_src}: bf16_tflops (burst) x {FP16_PER_BF16} fp16/bf16"}
+    else:
+        peak = peaks["hbm_gbs"]
+        achieved = bytes_of(spec) / (mean_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": traffic,
+                "peak_source": f"{peak_src}: hbm_gbs"}
+    roof.update({"kernel": kernel, "algorithmic_flops": flops,
+                 "algorithmic_bytes": bytes_of(spec), "source_sha": sha})
+
+    # ---- the oracle on this host's cores (rank 0, one GPU only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        nthreads = os.cpu_count() or 1
+        fl, dt, rows = oracle_sample(spec, a, b, args.cpu_seconds, nthreads)
+        cpu = {"value": fl / dt / 1e12, "unit": UNIT, "cores": nthreads, "kind": "oracle",
+               "sample": f"{rows} whole rows of C ({rows}x{N} outputs, K={K}) of the "
+                         f"{args.workload} workload in {dt:.1f} s; FP64 oracle, "
+                         f"{nthreads} threads"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_ms,
+            "ms_per_step_median": median_ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+            "config": {"workload": f"{args.workload}: {DESCRIPTIONS.get(args.workload, '')}",
+                       "M": M, "N": N, "K": K, "seed": spec["seed"],
+                       "l2": "flushed before every timed launch (write of 2x L2 size, "
+                             "outside the events)",
+                       "inputs": "resident in HBM", "path": kernel,
+                       "parallelism": f"replicas x{world}"},
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": args.steps, "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    world, rank, local = dist_setup()
+    if args.impl == "reference" and rank != 0:
+        return 0
+    a, b, spec = synth.workload(args.workload)
+    if args.impl == "reference":
+        return run_reference(args, spec, a, b, world, rank)
+    return run_ours(args, spec, a, b, world, rank, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,154 @@
+/*
+ * hgemm.h — C ABI of the GB300 (sm_103a) FP16 tensor-core GEMM, C = A·B.
+ *
+ * The operation, as stated in "Nvidia Tensor Core-MMA PTX编程入门", §4 示例:
+ * C = A·B with A an M×K row-major matrix, B a K×N column-major matrix and C
+ * an M×N row-major matrix, all IEEE binary16 (FP16). In memory:
+ *
+ *     A(i, k) = A[i*K + k]      0 <= i < M, 0 <= k < K
+ *     B(k, j) = B[j*K + k]      0 <= j < N   (each column of B is contiguous)
+ *     C(i, j) = C[i*N + j]
+ *
+ * Products are accumulated in FP32 ("GPU架构与CUDA", 混合精度核函数: FP16 × FP16
+ * accumulated in FP32) and each output is rounded once to FP16, round to
+ * nearest even. C is overwritten; there is no alpha, beta or accumulation
+ * into C. Terms outside the matrices contribute nothing and nothing outside
+ * the M×N region of C is written ("GPU架构与CUDA", 共享内存与分块: zero-filled
+ * tile loads and a guarded store).
+ *
+ * Element type: FP16 values are passed as their 16-bit patterns
+ * (hgemm_half_t); __half, torch.float16 and numpy.float16 share the layout.
+ *
+ * Streams ("GPU架构与CUDA", 流与并发): every entry point that computes only
+ * enqueues work on the caller's stream and returns; results are ready once
+ * the stream has been synchronised. Nothing here synchronises unless its
+ * comment says so.
+ *
+ * Ownership: the caller allocates, owns and frees every buffer. The library
+ * allocates no device memory and keeps no pointer after a call returns.
+ * Inputs must not be written while the enqueued work runs.
+ *
+ * Errors: every int-returning call returns HGEMM_OK (0) or a negative status
+ * below. A failing call enqueues nothing. After HGEMM_ERR_CUDA, the CUDA
+ * error that caused it is returned by hgemm_last_cuda_error() on the same
+ * host thread.
+ *
+ * Device: the kernels are built for sm_103a only (GB300). On any other device
+ * the computing calls return HGEMM_ERR_UNSUPPORTED_DEVICE; there is no
+ * fallback path of any kind.
+ */
+#ifndef HGEMM_H_
+#define HGEMM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define HGEMM_API __attribute__((visibility("default")))
+#else
+#define HGEMM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t hgemm_half_t; /* IEEE binary16 bit pattern */
+
+/* status codes */
+#define HGEMM_OK 0
+#define HGEMM_ERR_INVALID_ARG (-1)        /* negative or too large dimension, NULL pointer */
+#define HGEMM_ERR_ALIAS (-2)              /* C overlaps A or B */
+#define HGEMM_ERR_UNSUPPORTED_DEVICE (-3) /* current device is not compute capability 10.3 */
+#define HGEMM_ERR_CUDA (-4)               /* a CUDA runtime/driver call failed (see hgemm_last_cuda_error) */
+#define HGEMM_ERR_TIMEOUT (-5)            /* a kernel's bounded wait gave up (see hgemm_device_status) */
+
+/* kernel paths, as reported by hgemm_select_path */
+#define HGEMM_PATH_NONE 0     /* M == 0 or N == 0: nothing to do */
+#define HGEMM_PATH_ZERO 1     /* K == 0: C is filled with +0 (the empty sum) */
+#define HGEMM_PATH_TC 2       /* tcgen05 + TMA persistent kernel, 128×256 tiles */
+#define HGEMM_PATH_SKINNY 3   /* tcgen05 + TMA kernel for small N, split over K */
+#define HGEMM_PATH_GENERIC 4  /* tcgen05 kernel fed by plain loads: any alignment */
+
+/* Largest M, N or K accepted (TMA coordinates are signed 32-bit). */
+#define HGEMM_MAX_DIM ((int64_t)0x7FFFFFFF)
+
+/*
+ * hgemm — C = A·B on `stream` (see the top of this file for layouts).
+ *
+ *   A, B, C  device pointers (or managed memory visible to the current
+ *            device). Any alignment is accepted: when A, B, C are 16-byte
+ *            aligned and K and N are multiples of 8 the TMA-fed kernels run,
+ *            otherwise a kernel with plain loads does the same arithmetic.
+ *   M, N, K  0 <= M, N, K <= HGEMM_MAX_DIM. M == 0 or N == 0 is a no-op;
+ *            K == 0 sets every C(i, j) to +0. A and B may be NULL when their
+ *            size is 0, C when M*N == 0.
+ *   stream   CUDA stream of the current device (0 = legacy default stream).
+ *
+ * Returns HGEMM_OK once the work is enqueued, else an error status and
+ * nothing is enqueued: HGEMM_ERR_INVALID_ARG, HGEMM_ERR_ALIAS (the bytes of C
+ * overlap those of A or B), HGEMM_ERR_UNSUPPORTED_DEVICE, HGEMM_ERR_CUDA
+ * (launch or tensor-map encoding failure).
+ */
+HGEMM_API int hgemm(const hgemm_half_t *A, const hgemm_half_t *B, hgemm_half_t *C,
+          int64_t M, int64_t N, int64_t K, cudaStream_t stream);
+
+/*
+ * hgemm_host — the same product for operands held in HOST memory.
+ *
+ * Enqueues on `stream`, in order: copies of hA -> dA (M*K values) and
+ * hB -> dB (N*K values), hgemm(dA, dB, dC, M, N, K, stream), and a copy
+ * dC -> hC (M*N values). The caller provides the device buffers dA, dB, dC
+ * (same rules as hgemm) and owns every buffer. Host buffers should be
+ * page-locked for the copies to be asynchronous; hC is valid once `stream`
+ * has been synchronised. Same return values as hgemm.
+ */
+HGEMM_API int hgemm_host(const hgemm_half_t *hA, const hgemm_half_t *hB, hgemm_half_t *hC,
+               int64_t M, int64_t N, int64_t K,
+               hgemm_half_t *dA, hgemm_half_t *dB, hgemm_half_t *dC,
+               cudaStream_t stream);
+
+/*
+ * hgemm_select_path — the HGEMM_PATH_* that hgemm would run for these
+ * arguments on a GB300, or a negative status for invalid arguments. Pure
+ * host logic: touches no device and needs no GPU. Honours hgemm_force_path.
+ */
+HGEMM_API int hgemm_select_path(const void *A, const void *B, const void *C,
+                      int64_t M, int64_t N, int64_t K);
+
+/*
+ * hgemm_force_path — overrides path selection for later calls in this
+ * process (testing and profiling). `path` is HGEMM_PATH_TC,
+ * HGEMM_PATH_SKINNY or HGEMM_PATH_GENERIC, or -1 to restore automatic
+ * selection. A forced TMA path (TC or SKINNY) still falls back to GENERIC
+ * when the operands are not aligned for TMA. Returns HGEMM_OK or
+ * HGEMM_ERR_INVALID_ARG.
+ */
+HGEMM_API int hgemm_force_path(int path);
+
+/*
+ * hgemm_device_status — synchronises `stream`, then reads and clears the
+ * library's device watchdog word on the current device. Every wait inside the
+ * kernels is bounded in time; a wait that gives up records itself there and
+ * its kernel returns early, leaving C incomplete. Returns HGEMM_OK,
+ * HGEMM_ERR_TIMEOUT, or HGEMM_ERR_CUDA if the synchronisation failed.
+ */
+HGEMM_API int hgemm_device_status(cudaStream_t stream);
+
+/* hgemm_last_cuda_error — the cudaError_t behind the last HGEMM_ERR_CUDA
+ * returned on this host thread (0 if none). */
+HGEMM_API int hgemm_last_cuda_error(void);
+
+/* hgemm_status_string — static text for a status code; never NULL. */
+HGEMM_API const char *hgemm_status_string(int status);
+
+/* hgemm_version — (major << 16) | minor of this library. */
+HGEMM_API int hgemm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HGEMM_H_ */

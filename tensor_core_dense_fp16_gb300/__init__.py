@@ -1,0 +1,219 @@
+"""Python binding of libhgemm.so, the GB300 FP16 tensor-core GEMM C = A·B.
+
+Argument marshalling only: every step of the product runs in the library's
+CUDA kernels (see ``include/hgemm.h`` for the contract). Functions carry the
+C names. Matrices may be given as torch tensors (their ``data_ptr()`` is
+passed), numpy arrays (host memory, for ``hgemm_host``) or raw integer
+addresses. Streams may be a ``torch.cuda.Stream``, a raw handle, or None for
+torch's current stream.
+
+Layouts, as in "Nvidia Tensor Core-MMA PTX编程入门", §4 示例: A is M×K
+row-major, B is K×N column-major (pass it as an (N, K) row-major array whose
+row j is column j of B), C is M×N row-major; all FP16.
+
+If the shared library has not been built, every call raises: there is no
+fallback implementation.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+__all__ = [
+    "HGEMM_OK", "HGEMM_ERR_INVALID_ARG", "HGEMM_ERR_ALIAS", "HGEMM_ERR_UNSUPPORTED_DEVICE",
+    "HGEMM_ERR_CUDA", "HGEMM_ERR_TIMEOUT", "HGEMM_PATH_NONE", "HGEMM_PATH_ZERO",
+    "HGEMM_PATH_TC", "HGEMM_PATH_SKINNY", "HGEMM_PATH_GENERIC", "HGEMM_MAX_DIM",
+    "HgemmError", "library_path", "load", "hgemm", "hgemm_host", "hgemm_select_path",
+    "hgemm_force_path", "hgemm_device_status", "hgemm_last_cuda_error",
+    "hgemm_status_string", "hgemm_version", "matmul",
+]
+
+HGEMM_OK = 0
+HGEMM_ERR_INVALID_ARG = -1
+HGEMM_ERR_ALIAS = -2
+HGEMM_ERR_UNSUPPORTED_DEVICE = -3
+HGEMM_ERR_CUDA = -4
+HGEMM_ERR_TIMEOUT = -5
+
+HGEMM_PATH_NONE = 0
+HGEMM_PATH_ZERO = 1
+HGEMM_PATH_TC = 2
+HGEMM_PATH_SKINNY = 3
+HGEMM_PATH_GENERIC = 4
+
+HGEMM_MAX_DIM = 0x7FFFFFFF
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "_build", "libhgemm.so")
+_lib = None
+
+
+class HgemmError(RuntimeError):
+    """A negative status from libhgemm."""
+
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = f"{where}: {hgemm_status_string(status)} (status {status})"
+        if status == HGEMM_ERR_CUDA:
+            msg += f", cudaError {hgemm_last_cuda_error()}"
+        super().__init__(msg)
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load():
+    """Loads libhgemm.so (built by tensor_core_dense_fp16_gb300.build.build())."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise RuntimeError(
+            f"{_LIB_PATH} is missing: build it with "
+            "`python -c 'import __graft_entry__ as g; g.build()'` (needs nvcc)")
+    lib = ctypes.CDLL(_LIB_PATH)
+    vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    lib.hgemm.argtypes = [vp, vp, vp, i64, i64, i64, vp]
+    lib.hgemm.restype = i32
+    lib.hgemm_host.argtypes = [vp, vp, vp, i64, i64, i64, vp, vp, vp, vp]
+    lib.hgemm_host.restype = i32
+    lib.hgemm_select_path.argtypes = [vp, vp, vp, i64, i64, i64]
+    lib.hgemm_select_path.restype = i32
+    lib.hgemm_force_path.argtypes = [i32]
+    lib.hgemm_force_path.restype = i32
+    lib.hgemm_device_status.argtypes = [vp]
+    lib.hgemm_device_status.restype = i32
+    lib.hgemm_last_cuda_error.argtypes = []
+    lib.hgemm_last_cuda_error.restype = i32
+    lib.hgemm_status_string.argtypes = [i32]
+    lib.hgemm_status_string.restype = ctypes.c_char_p
+    lib.hgemm_version.argtypes = []
+    lib.hgemm_version.restype = i32
+    _lib = lib
+    return lib
+
+
+# ----------------------------------------------------------------- marshalling
+
+def _ptr(x) -> int | None:
+    """Address of a torch tensor, numpy array, ctypes object or integer."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):          # torch.Tensor
+        return int(x.data_ptr())
+    if hasattr(x, "ctypes"):            # numpy.ndarray
+        return int(x.ctypes.data)
+    if isinstance(x, ctypes.c_void_p):
+        return x.value
+    raise TypeError(f"cannot take the address of {type(x).__name__}")
+
+
+def _check_tensor(x, name: str, on_device: bool | None):
+    """dtype and contiguity checks for torch tensors and numpy arrays."""
+    if hasattr(x, "data_ptr") and hasattr(x, "dtype"):
+        import torch
+        if x.dtype != torch.float16:
+            raise TypeError(f"{name} must be torch.float16, got {x.dtype}")
+        if not x.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        if on_device is True and not x.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if on_device is False and x.is_cuda:
+            raise ValueError(f"{name} must be a host tensor")
+    elif hasattr(x, "ctypes") and hasattr(x, "dtype"):
+        import numpy as np
+        if x.dtype != np.float16:
+            raise TypeError(f"{name} must be float16, got {x.dtype}")
+        if not x.flags["C_CONTIGUOUS"]:
+            raise ValueError(f"{name} must be C-contiguous")
+        if on_device is True:
+            raise ValueError(f"{name} must be device memory, got a numpy array")
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        import torch
+        return int(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return stream
+    if hasattr(stream, "cuda_stream"):
+        return int(stream.cuda_stream)
+    raise TypeError(f"cannot use {type(stream).__name__} as a CUDA stream")
+
+
+def _raise_on(status: int, where: str) -> int:
+    if status < 0:
+        raise HgemmError(status, where)
+    return status
+
+
+# --------------------------------------------------------------------- the ABI
+
+def hgemm(A, B, C, M: int, N: int, K: int, stream=None) -> None:
+    """C = A·B on `stream` (enqueued; synchronise the stream to read C)."""
+    for x, n in ((A, "A"), (B, "B"), (C, "C")):
+        _check_tensor(x, n, True)
+    _raise_on(load().hgemm(_ptr(A), _ptr(B), _ptr(C), M, N, K, _stream(stream)), "hgemm")
+
+
+def hgemm_host(hA, hB, hC, M: int, N: int, K: int, dA, dB, dC, stream=None) -> None:
+    """Host operands: H2D copies, the product and the D2H copy, all on `stream`."""
+    for x, n in ((hA, "hA"), (hB, "hB"), (hC, "hC")):
+        _check_tensor(x, n, False)
+    for x, n in ((dA, "dA"), (dB, "dB"), (dC, "dC")):
+        _check_tensor(x, n, True)
+    _raise_on(load().hgemm_host(_ptr(hA), _ptr(hB), _ptr(hC), M, N, K, _ptr(dA), _ptr(dB),
+                                _ptr(dC), _stream(stream)), "hgemm_host")
+
+
+def hgemm_select_path(A, B, C, M: int, N: int, K: int) -> int:
+    """The HGEMM_PATH_* hgemm would take (host logic only; raises on bad args)."""
+    return _raise_on(load().hgemm_select_path(_ptr(A), _ptr(B), _ptr(C), M, N, K),
+                     "hgemm_select_path")
+
+
+def hgemm_force_path(path: int) -> None:
+    _raise_on(load().hgemm_force_path(path), "hgemm_force_path")
+
+
+def hgemm_device_status(stream=None) -> int:
+    """Synchronises `stream`; returns HGEMM_OK or HGEMM_ERR_TIMEOUT (raises otherwise)."""
+    st = load().hgemm_device_status(_stream(stream))
+    if st in (HGEMM_OK, HGEMM_ERR_TIMEOUT):
+        return st
+    raise HgemmError(st, "hgemm_device_status")
+
+
+def hgemm_last_cuda_error() -> int:
+    return int(load().hgemm_last_cuda_error())
+
+
+def hgemm_status_string(status: int) -> str:
+    return load().hgemm_status_string(status).decode()
+
+
+def hgemm_version() -> tuple[int, int]:
+    v = int(load().hgemm_version())
+    return v >> 16, v & 0xFFFF
+
+
+def matmul(a, b_cols, out=None, stream=None):
+    """Convenience: a (M, K) and b_cols (N, K) CUDA float16 tensors -> (M, N).
+
+    Row j of ``b_cols`` is column j of B. Allocates ``out`` with torch if not
+    given (the library itself never allocates)."""
+    import torch
+    M, K = a.shape
+    N, K2 = b_cols.shape
+    if K != K2:
+        raise ValueError(f"inner dimensions differ: {K} vs {K2}")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=a.device)
+    elif tuple(out.shape) != (M, N):
+        raise ValueError(f"out must be ({M}, {N})")
+    hgemm(a, b_cols, out, M, N, K, stream)
+    return out

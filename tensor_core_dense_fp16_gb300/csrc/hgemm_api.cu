@@ -1,0 +1,285 @@
+// hgemm_api.cu — the C ABI declared in include/hgemm.h: argument checks,
+// path selection, TMA tensor-map encoding and kernel dispatch.
+//
+// The entry point follows the launcher of "Nvidia Tensor Core-MMA PTX编程入门",
+// §4 示例 (pointers to A, B, C and the sizes M, N, K; the launcher picks the
+// grid) and adds the caller's stream ("GPU架构与CUDA", 流与并发). The library
+// never allocates device memory: buffers come from the caller, who owns them
+// ("GPU架构与CUDA", 内存池分配器: allocation belongs to a caching allocator
+// such as PyTorch's, not to every call).
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include "hgemm.h"
+#include "internal.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;  // 2 s per wait
+
+thread_local int t_last_cuda_error = 0;
+std::atomic<int> g_forced_path{-1};
+std::atomic<unsigned long long> g_timeout_ns{kDefaultTimeoutNs};
+
+struct DeviceState {
+  std::atomic<int> ready{0};  // 0 unknown, 1 supported, -1 unsupported
+  int num_sms = 0;
+  int* status = nullptr;
+};
+DeviceState g_devices[kMaxDevices];
+std::mutex g_device_mu;
+
+int cuda_fail(cudaError_t e) {
+  t_last_cuda_error = static_cast<int>(e);
+  return HGEMM_ERR_CUDA;
+}
+
+// Checks the current device once: compute capability 10.3 and the watchdog
+// word's address. Returns HGEMM_OK and the state, or an error status.
+int current_device(DeviceState** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= kMaxDevices) return HGEMM_ERR_UNSUPPORTED_DEVICE;
+  DeviceState& st = g_devices[dev];
+  int r = st.ready.load(std::memory_order_acquire);
+  if (r == 0) {
+    std::lock_guard<std::mutex> lock(g_device_mu);
+    r = st.ready.load(std::memory_order_relaxed);
+    if (r == 0) {
+      int major = 0, minor = 0, sms = 0;
+      if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+          (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+          (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+        return cuda_fail(e);
+      if (major != 10 || minor != 3) {
+        r = -1;
+      } else {
+        int* status = nullptr;
+        if ((e = hg::status_word_address(&status)) != cudaSuccess) return cuda_fail(e);
+        st.num_sms = sms;
+        st.status = status;
+        r = 1;
+      }
+      st.ready.store(r, std::memory_order_release);
+    }
+  }
+  if (r < 0) return HGEMM_ERR_UNSUPPORTED_DEVICE;
+  *out = &st;
+  return HGEMM_OK;
+}
+
+bool ranges_overlap(const void* a, uint64_t abytes, const void* b, uint64_t bbytes) {
+  if (!a || !b || abytes == 0 || bbytes == 0) return false;
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + bbytes && b0 < a0 + abytes;
+}
+
+// Host-only argument checks shared by every entry point.
+int validate(const void* A, const void* B, const void* C, int64_t M, int64_t N, int64_t K) {
+  if (M < 0 || N < 0 || K < 0 || M > HGEMM_MAX_DIM || N > HGEMM_MAX_DIM || K > HGEMM_MAX_DIM)
+    return HGEMM_ERR_INVALID_ARG;
+  // element counts (each < 2^62) and byte counts (< 2^63) cannot overflow
+  const unsigned __int128 mk = static_cast<unsigned __int128>(M) * K;
+  const unsigned __int128 nk = static_cast<unsigned __int128>(N) * K;
+  const unsigned __int128 mn = static_cast<unsigned __int128>(M) * N;
+  const unsigned __int128 lim = static_cast<unsigned __int128>(1) << 61;
+  if (mk >= lim || nk >= lim || mn >= lim) return HGEMM_ERR_INVALID_ARG;
+  if ((mk && !A) || (nk && !B) || (mn && !C)) return HGEMM_ERR_INVALID_ARG;
+  if (mn && (ranges_overlap(C, 2 * static_cast<uint64_t>(mn), A, 2 * static_cast<uint64_t>(mk)) ||
+             ranges_overlap(C, 2 * static_cast<uint64_t>(mn), B, 2 * static_cast<uint64_t>(nk))))
+    return HGEMM_ERR_ALIAS;
+  return HGEMM_OK;
+}
+
+bool tma_ok(const void* A, const void* B, const void* C, int64_t N, int64_t K) {
+  auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+  return al16(A) && al16(B) && al16(C) && (K % 8 == 0) && (N % 8 == 0);
+}
+
+int choose_path(const void* A, const void* B, const void* C, int64_t M, int64_t N, int64_t K) {
+  if (M == 0 || N == 0) return HGEMM_PATH_NONE;
+  if (K == 0) return HGEMM_PATH_ZERO;
+  const bool tma = tma_ok(A, B, C, N, K);
+  const int forced = g_forced_path.load(std::memory_order_relaxed);
+  if (forced == HGEMM_PATH_GENERIC || !tma) return HGEMM_PATH_GENERIC;
+  if (forced == HGEMM_PATH_TC) return HGEMM_PATH_TC;
+  return HGEMM_PATH_TC;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// Tensor map of a row-major FP16 matrix [rows][cols] read or written in
+// boxes of box_rows × box_cols (box_cols * 2 == 128 bytes: one swizzle row).
+int encode_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_rows,
+               int box_cols) {
+  auto encode = tensor_map_encoder();
+  if (!encode) return cuda_fail(cudaErrorNotSupported);
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t elem_strides[2] = {1, 1};
+  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims,
+                      strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue);
+  return HGEMM_OK;
+}
+
+int run_tc(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+           const DeviceState& dev, cudaStream_t stream) {
+  CUtensorMap ma, mb, mc;
+  int rc;
+  if ((rc = encode_map(&ma, A, M, K, hg::kTcBM, hg::kTcBK)) != HGEMM_OK) return rc;
+  if ((rc = encode_map(&mb, B, N, K, hg::kTcBN, hg::kTcBK)) != HGEMM_OK) return rc;
+  if ((rc = encode_map(&mc, C, M, N, hg::kEpiRows, hg::kEpiCols)) != HGEMM_OK) return rc;
+  hg::TcArgs args{};
+  args.M = static_cast<int>(M);
+  args.N = static_cast<int>(N);
+  args.K = static_cast<int>(K);
+  args.num_m = static_cast<int>((M + hg::kTcBM - 1) / hg::kTcBM);
+  args.num_n = static_cast<int>((N + hg::kTcBN - 1) / hg::kTcBN);
+  args.num_kb = static_cast<int>((K + hg::kTcBK - 1) / hg::kTcBK);
+  const int64_t tiles = static_cast<int64_t>(args.num_m) * args.num_n;
+  if (tiles > 0x7FFFFFFF) return HGEMM_ERR_INVALID_ARG;
+  args.num_tiles = static_cast<int>(tiles);
+  args.group_m = 16;
+  args.grid = static_cast<int>(tiles < dev.num_sms ? tiles : dev.num_sms);
+  args.status = dev.status;
+  args.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
+  cudaError_t e = hg::launch_tc_128x256(ma, mb, mc, args, stream);
+  return e == cudaSuccess ? HGEMM_OK : cuda_fail(e);
+}
+
+int dispatch(const hgemm_half_t* A, const hgemm_half_t* B, hgemm_half_t* C, int64_t M, int64_t N,
+             int64_t K, const DeviceState& dev, cudaStream_t stream) {
+  cudaError_t e;
+  switch (choose_path(A, B, C, M, N, K)) {
+    case HGEMM_PATH_NONE:
+      return HGEMM_OK;
+    case HGEMM_PATH_ZERO:
+      e = hg::launch_zero_fill(C, M * N, stream);
+      return e == cudaSuccess ? HGEMM_OK : cuda_fail(e);
+    case HGEMM_PATH_TC:
+      return run_tc(A, B, C, M, N, K, dev, stream);
+    default: {
+      hg::PlainArgs pa{A, B, C, M, N, K, dev.status, g_timeout_ns.load()};
+      e = hg::launch_generic(pa, dev.num_sms, stream);
+      return e == cudaSuccess ? HGEMM_OK : cuda_fail(e);
+    }
+  }
+}
+
+}  // namespace
+
+extern "C" {
+
+int hgemm(const hgemm_half_t* A, const hgemm_half_t* B, hgemm_half_t* C, int64_t M, int64_t N,
+          int64_t K, cudaStream_t stream) {
+  int rc = validate(A, B, C, M, N, K);
+  if (rc != HGEMM_OK) return rc;
+  if (M == 0 || N == 0) return HGEMM_OK;
+  DeviceState* dev = nullptr;
+  if ((rc = current_device(&dev)) != HGEMM_OK) return rc;
+  return dispatch(A, B, C, M, N, K, *dev, stream);
+}
+
+int hgemm_host(const hgemm_half_t* hA, const hgemm_half_t* hB, hgemm_half_t* hC, int64_t M,
+               int64_t N, int64_t K, hgemm_half_t* dA, hgemm_half_t* dB, hgemm_half_t* dC,
+               cudaStream_t stream) {
+  int rc = validate(dA, dB, dC, M, N, K);
+  if (rc != HGEMM_OK) return rc;
+  if ((M * K && !hA) || (N * K && !hB) || (M * N && !hC)) return HGEMM_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return HGEMM_OK;
+  DeviceState* dev = nullptr;
+  if ((rc = current_device(&dev)) != HGEMM_OK) return rc;
+  cudaError_t e;
+  if (M * K &&
+      (e = cudaMemcpyAsync(dA, hA, 2 * M * K, cudaMemcpyHostToDevice, stream)) != cudaSuccess)
+    return cuda_fail(e);
+  if (N * K &&
+      (e = cudaMemcpyAsync(dB, hB, 2 * N * K, cudaMemcpyHostToDevice, stream)) != cudaSuccess)
+    return cuda_fail(e);
+  if ((rc = dispatch(dA, dB, dC, M, N, K, *dev, stream)) != HGEMM_OK) return rc;
+  if ((e = cudaMemcpyAsync(hC, dC, 2 * M * N, cudaMemcpyDeviceToHost, stream)) != cudaSuccess)
+    return cuda_fail(e);
+  return HGEMM_OK;
+}
+
+int hgemm_select_path(const void* A, const void* B, const void* C, int64_t M, int64_t N,
+                      int64_t K) {
+  int rc = validate(A, B, C, M, N, K);
+  if (rc != HGEMM_OK) return rc;
+  return choose_path(A, B, C, M, N, K);
+}
+
+int hgemm_force_path(int path) {
+  if (path != -1 && path != HGEMM_PATH_TC && path != HGEMM_PATH_SKINNY &&
+      path != HGEMM_PATH_GENERIC)
+    return HGEMM_ERR_INVALID_ARG;
+  g_forced_path.store(path);
+  return HGEMM_OK;
+}
+
+int hgemm_device_status(cudaStream_t stream) {
+  DeviceState* dev = nullptr;
+  int rc = current_device(&dev);
+  if (rc != HGEMM_OK) return rc;
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+  int word = 0;
+  if ((e = cudaMemcpy(&word, dev->status, sizeof(int), cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return cuda_fail(e);
+  if (word != 0) {
+    const int zero = 0;
+    if ((e = cudaMemcpy(dev->status, &zero, sizeof(int), cudaMemcpyHostToDevice)) != cudaSuccess)
+      return cuda_fail(e);
+    return HGEMM_ERR_TIMEOUT;
+  }
+  return HGEMM_OK;
+}
+
+int hgemm_last_cuda_error(void) { return t_last_cuda_error; }
+
+const char* hgemm_status_string(int status) {
+  switch (status) {
+    case HGEMM_OK:
+      return "ok";
+    case HGEMM_ERR_INVALID_ARG:
+      return "invalid argument (dimension out of range or NULL pointer)";
+    case HGEMM_ERR_ALIAS:
+      return "C overlaps A or B";
+    case HGEMM_ERR_UNSUPPORTED_DEVICE:
+      return "current device is not an sm_103 (GB300) GPU";
+    case HGEMM_ERR_CUDA:
+      return "a CUDA call failed (see hgemm_last_cuda_error)";
+    case HGEMM_ERR_TIMEOUT:
+      return "a kernel wait timed out; the output is incomplete";
+    default:
+      return "unknown status";
+  }
+}
+
+int hgemm_version(void) { return (0 << 16) | 1; }
+
+}  // extern "C"

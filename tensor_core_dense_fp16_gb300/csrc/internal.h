@@ -1,0 +1,60 @@
+// internal.h — host-side interface between the C-ABI layer (hgemm_api.cu)
+// and the kernel translation units. Not part of the public ABI.
+#pragma once
+
+#include <cstdint>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace hg {
+
+// Watchdog codes written to the device status word by a wait that gave up.
+enum WatchdogCode : int {
+  kWdNone = 0,
+  kWdProducerEmpty = 1,   // TMA producer waiting for a free smem stage
+  kWdMmaFull = 2,         // MMA issuer waiting for a loaded smem stage
+  kWdMmaAccEmpty = 3,     // MMA issuer waiting for the epilogue to free TMEM
+  kWdEpiAccFull = 4,      // epilogue waiting for a finished accumulator
+  kWdDrain = 5,           // end-of-kernel drain of in-flight copies or MMAs
+};
+
+// Everything a tensor-core launch needs besides the tensor maps.
+struct TcArgs {
+  int M, N, K;
+  int num_m, num_n, num_kb;  // tiles along M and N, 64-wide K blocks
+  int num_tiles;
+  int group_m;               // rasterisation group height (in M tiles)
+  int grid;                  // persistent CTAs
+  int* status;               // device watchdog word
+  unsigned long long timeout_ns;
+};
+
+// Plain-pointer launch arguments for the kernels that do not use TMA.
+struct PlainArgs {
+  const uint16_t* A;
+  const uint16_t* B;
+  uint16_t* C;
+  int64_t M, N, K;
+  int* status;
+  unsigned long long timeout_ns;
+};
+
+// Launchers (each enqueues one kernel on `stream` and returns the launch
+// error, if any). Shared-memory attributes are set on first use per device.
+cudaError_t launch_tc_128x256(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
+                              const TcArgs& args, cudaStream_t stream);
+cudaError_t launch_zero_fill(uint16_t* C, int64_t count, cudaStream_t stream);
+cudaError_t launch_generic(const PlainArgs& args, int num_sms, cudaStream_t stream);
+
+// Address of the device watchdog word on the current device.
+cudaError_t status_word_address(int** addr);
+
+// Tile geometry of the tensor-core path, for the host-side tensor maps.
+constexpr int kTcBM = 128;
+constexpr int kTcBN = 256;
+constexpr int kTcBK = 64;
+constexpr int kEpiRows = 32;   // rows of one staged C box (one epilogue warp)
+constexpr int kEpiCols = 64;   // columns of one staged C box (128 bytes)
+
+}  // namespace hg

@@ -1,0 +1,139 @@
+"""The C-ABI boundary on the host: the library loads, exports every symbol the
+header declares, and its host-only logic (argument checks, path selection,
+status text) behaves as documented. No computing call is made here."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import tensor_core_dense_fp16_gb300 as tc
+from tensor_core_dense_fp16_gb300 import build as tcbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "hgemm.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    tcbuild.build()
+    return tc.load()
+
+
+def declared_functions():
+    text = open(HEADER, encoding="utf-8").read()
+    return re.findall(r"HGEMM_API\s+[\w\s\*]+?\b(hgemm\w*)\s*\(", text)
+
+
+def declared_constants():
+    text = open(HEADER, encoding="utf-8").read()
+    out = {}
+    for name, val in re.findall(r"#define\s+(HGEMM_(?:OK|ERR_\w+|PATH_\w+))\s+\(?(-?\d+)\)?", text):
+        out[name] = int(val)
+    return out
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert {"hgemm", "hgemm_host", "hgemm_select_path", "hgemm_force_path",
+            "hgemm_device_status", "hgemm_last_cuda_error", "hgemm_status_string",
+            "hgemm_version"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+        # and the binding exposes the same name
+        assert callable(getattr(tc, n)), n
+
+
+def test_binding_constants_match_header():
+    consts = declared_constants()
+    assert len(consts) >= 11
+    for name, val in consts.items():
+        assert getattr(tc, name) == val, name
+
+
+def test_status_strings(lib):
+    for code in (0, -1, -2, -3, -4, -5):
+        s = tc.hgemm_status_string(code)
+        assert s and s != "unknown status"
+    assert tc.hgemm_status_string(-99) == "unknown status"
+    assert tc.hgemm_version() == (0, 1)
+
+
+A16, B16, C16 = 0x10000000, 0x20000000, 0x30000000  # 16-byte aligned, disjoint
+
+
+def test_path_selection(lib):
+    sel = tc.hgemm_select_path
+    assert sel(A16, B16, C16, 0, 5, 5) == tc.HGEMM_PATH_NONE
+    assert sel(A16, B16, C16, 5, 0, 5) == tc.HGEMM_PATH_NONE
+    assert sel(A16, B16, C16, 4, 8, 0) == tc.HGEMM_PATH_ZERO
+    assert sel(A16, B16, C16, 8192, 8192, 8192) == tc.HGEMM_PATH_TC
+    assert sel(A16, B16, C16, 1000, 1000, 1000) == tc.HGEMM_PATH_TC
+    # TMA needs 16-byte row pitches and 16-byte base addresses
+    assert sel(A16, B16, C16, 64, 64, 1001) == tc.HGEMM_PATH_GENERIC
+    assert sel(A16, B16, C16, 64, 1001, 64) == tc.HGEMM_PATH_GENERIC
+    assert sel(A16 + 2, B16, C16, 64, 64, 64) == tc.HGEMM_PATH_GENERIC
+    assert sel(A16, B16 + 8, C16, 64, 64, 64) == tc.HGEMM_PATH_GENERIC
+    assert sel(A16, B16, C16 + 4, 64, 64, 64) == tc.HGEMM_PATH_GENERIC
+    # M is free: any M works with TMA
+    assert sel(A16, B16, C16, 1001, 64, 64) == tc.HGEMM_PATH_TC
+
+
+def test_forced_paths(lib):
+    try:
+        tc.hgemm_force_path(tc.HGEMM_PATH_GENERIC)
+        assert tc.hgemm_select_path(A16, B16, C16, 256, 256, 256) == tc.HGEMM_PATH_GENERIC
+        tc.hgemm_force_path(tc.HGEMM_PATH_TC)
+        assert tc.hgemm_select_path(A16, B16, C16, 256, 256, 256) == tc.HGEMM_PATH_TC
+        # a forced TMA path still needs TMA-able operands
+        assert tc.hgemm_select_path(A16, B16, C16, 256, 256, 255) == tc.HGEMM_PATH_GENERIC
+        with pytest.raises(tc.HgemmError):
+            tc.hgemm_force_path(77)
+    finally:
+        tc.hgemm_force_path(-1)
+    assert tc.hgemm_select_path(A16, B16, C16, 256, 256, 256) == tc.HGEMM_PATH_TC
+
+
+def test_invalid_arguments_rejected_before_any_device_work(lib):
+    bad = [
+        (A16, B16, C16, -1, 4, 4),
+        (A16, B16, C16, 4, -1, 4),
+        (A16, B16, C16, 4, 4, -1),
+        (A16, B16, C16, 1 << 31, 4, 4),
+        (A16, B16, C16, 4, 4, 1 << 40),
+        (None, B16, C16, 4, 4, 4),
+        (A16, None, C16, 4, 4, 4),
+        (A16, B16, None, 4, 4, 4),
+        (A16, B16, C16, (1 << 31) - 1, (1 << 31) - 1, 8),  # M*N elements >= 2^61
+    ]
+    for args in bad:
+        assert lib.hgemm(*args, None) == tc.HGEMM_ERR_INVALID_ARG, args
+        assert lib.hgemm_select_path(*args) == tc.HGEMM_ERR_INVALID_ARG, args
+    # NULL operands are fine when their size is zero
+    assert lib.hgemm_select_path(None, None, None, 0, 0, 0) == tc.HGEMM_PATH_NONE
+    assert lib.hgemm_select_path(None, None, C16, 4, 4, 0) == tc.HGEMM_PATH_ZERO
+
+
+def test_alias_detection(lib):
+    M, N, K = 64, 64, 64
+    a_bytes = M * K * 2
+    # C overlapping the tail of A
+    assert lib.hgemm_select_path(A16, B16, A16 + a_bytes - 2, M, N, K) == tc.HGEMM_ERR_ALIAS
+    assert lib.hgemm(A16, B16, A16 + a_bytes - 2, M, N, K, None) == tc.HGEMM_ERR_ALIAS
+    # C overlapping the head of B
+    assert lib.hgemm_select_path(A16, B16, B16 - 16, M, N, K) == tc.HGEMM_ERR_ALIAS
+    # adjacent but disjoint is fine
+    assert lib.hgemm_select_path(A16, B16, A16 + a_bytes, M, N, K) == tc.HGEMM_PATH_TC
+    # A and B may alias each other (both are read-only)
+    assert lib.hgemm_select_path(A16, A16, C16, M, N, K) == tc.HGEMM_PATH_TC
+
+
+def test_binding_type_checks():
+    torch = pytest.importorskip("torch")
+    a = torch.zeros(4, 4, dtype=torch.float32)
+    with pytest.raises(TypeError):
+        tc.hgemm(a, a, a, 4, 4, 4, stream=0)
+    h = torch.zeros(4, 4, dtype=torch.float16)
+    with pytest.raises(ValueError):
+        tc.hgemm(h, h, h, 4, 4, 4, stream=0)  # host tensors for a device call

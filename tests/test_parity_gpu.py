@@ -1,0 +1,206 @@
+"""Parity of the CUDA path with the oracle, element by element, through the
+C ABI (GPU only).
+
+Workloads are the benchmark configurations (seeded, synthetic): the 256-cube
+with uniform and integer operands, 2048-cube, the ragged 1000-cube, the
+skinny 4096×256×4096 and, at full size, the 8192-cube checked on sampled
+entries plus properties that hold at any size. Integer operands must match
+bit for bit (every partial sum is an exact integer in FP32); random operands
+within |gpu − ref| <= 1e-2·max(1, |ref|).
+"""
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+import tensor_core_dense_fp16_gb300 as tc
+from gpu_helpers import assert_close, oracle_threads, run_gpu, to_device, torch_cuda
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("name", ["hgemm_256", "hgemm_256_int", "hgemm_2048",
+                                  "hgemm_1000_ragged", "hgemm_4096x256x4096_skinny"])
+def test_workload_matches_oracle(name):
+    a, b, spec = synth.workload(name)
+    ref = oracle.hgemm(a, b, nthreads=oracle_threads())
+    got = run_gpu(a, b)
+    assert_close(got, ref, exact=(spec["kind"] == "int"), what=name)
+
+
+def test_integer_operands_ragged_bit_exact():
+    # 1000×1000 output (ragged tiles in M and N), K = 256: |C| <= 1024
+    a, b = synth.operands(1000, 1000, 256, seed=1102, kind="int")
+    ref = oracle.hgemm(a, b, nthreads=oracle_threads())
+    assert_close(run_gpu(a, b), ref, exact=True, what="int 1000x1000x256")
+
+
+def test_8192_cube_sampled_entries_and_properties():
+    torch = torch_cuda()
+    a, b, spec = synth.workload("hgemm_8192")
+    M, N, K = spec["M"], spec["N"], spec["K"]
+    da, db = to_device(a), to_device(b)
+    dc = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    tc.hgemm(da, db, dc, M, N, K)
+    assert tc.hgemm_device_status() == tc.HGEMM_OK
+    c = dc.cpu().numpy()
+    rng = np.random.default_rng(8192)
+    rows = list(rng.integers(0, M, 3000))
+    cols = list(rng.integers(0, N, 3000))
+    # tile corners and edges of the 128×256 tiling, and the matrix corners
+    for i in (0, 127, 128, 4095, 4096, M - 1):
+        for j in (0, 255, 256, 4095, 4096, N - 1):
+            rows.append(i)
+            cols.append(j)
+    rows, cols = np.array(rows), np.array(cols)
+    ref = oracle.entries(a, b, rows, cols)
+    assert_close(c[rows, cols], ref, what="8192^3 sampled")
+    # properties at full size: finite, and C ~ N(0, 1) by construction
+    cf = c.astype(np.float32)
+    assert np.isfinite(cf).all()
+    assert abs(float(cf.std()) - 1.0) < 0.02
+    # doubling B is exact in FP16 and in FP32 accumulation: C doubles bitwise
+    dc2 = torch.empty_like(dc)
+    tc.hgemm(da, db * 2, dc2, M, N, K)
+    assert tc.hgemm_device_status() == tc.HGEMM_OK
+    assert torch.equal(dc2, dc * 2)
+
+
+EDGE = [1, 7, 8, 15, 16, 17, 127, 128, 129, 1000, 1001]
+
+
+def _edge_cases(aligned):
+    rng = np.random.default_rng(99 if aligned else 98)
+    cases = set()
+    for M in EDGE:
+        for N in EDGE:
+            for K in EDGE:
+                if aligned and (N % 8 or K % 8):
+                    continue
+                cases.add((M, N, K))
+    cases = sorted(cases)
+    # a deterministic subset keeps the run short; the extremes always stay in
+    keep = [c for c in cases if c[0] in (1, 1001) and c[1] in (1, 8, 1000, 1001)]
+    picked = rng.choice(len(cases), size=min(40, len(cases)), replace=False)
+    return sorted(set(keep) | {cases[i] for i in picked})
+
+
+@pytest.mark.parametrize("M,N,K", _edge_cases(aligned=True))
+def test_edges_tensor_core_path(M, N, K):
+    a, b = synth.operands(M, N, K, seed=M * 131 + N * 7 + K, kind="uniform")
+    ref = oracle.hgemm(a, b, nthreads=oracle_threads())
+    # with 16-byte aligned buffers (as torch allocates) these take a TMA path
+    assert tc.hgemm_select_path(0x10000000, 0x20000000, 0x30000000, M, N, K) in (
+        tc.HGEMM_PATH_TC, tc.HGEMM_PATH_SKINNY)
+    assert_close(run_gpu(a, b), ref, what=f"tc {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M,N,K", _edge_cases(aligned=False))
+def test_edges_generic_path(M, N, K):
+    a, b = synth.operands(M, N, K, seed=M * 131 + N * 7 + K + 5, kind="uniform")
+    ref = oracle.hgemm(a, b, nthreads=oracle_threads())
+    assert_close(run_gpu(a, b, path=tc.HGEMM_PATH_GENERIC), ref, what=f"generic {M}x{N}x{K}")
+
+
+def test_misaligned_pointers_take_the_generic_path():
+    torch = torch_cuda()
+    M, N, K = 130, 72, 96
+    a, b = synth.operands(M, N, K, seed=4242, kind="uniform")
+    ref = oracle.hgemm(a, b)
+    # operands at an odd 2-byte offset inside larger buffers
+    ba = torch.zeros(M * K + 1, dtype=torch.float16, device="cuda")
+    bb = torch.zeros(N * K + 1, dtype=torch.float16, device="cuda")
+    bc = torch.zeros(M * N + 1, dtype=torch.float16, device="cuda")
+    ba[1:] = torch.from_numpy(a.reshape(-1)).cuda()
+    bb[1:] = torch.from_numpy(b.reshape(-1)).cuda()
+    pa, pb, pc = ba.data_ptr() + 2, bb.data_ptr() + 2, bc.data_ptr() + 2
+    assert tc.hgemm_select_path(pa, pb, pc, M, N, K) == tc.HGEMM_PATH_GENERIC
+    assert tc.load().hgemm(pa, pb, pc, M, N, K, torch.cuda.current_stream().cuda_stream) == 0
+    assert tc.hgemm_device_status() == tc.HGEMM_OK
+    assert_close(bc[1:].cpu().numpy().reshape(M, N), ref, what="misaligned")
+
+
+@pytest.mark.parametrize("path", [tc.HGEMM_PATH_TC, tc.HGEMM_PATH_GENERIC])
+def test_guard_bands_untouched(path):
+    """Nothing outside C is written: C sits inside a sentinel-filled buffer."""
+    torch = torch_cuda()
+    M, N, K = 200, 136, 72   # ragged in M and N against 128×256 tiles
+    pad = 4096
+    a, b = synth.operands(M, N, K, seed=77, kind="uniform")
+    ref = oracle.hgemm(a, b)
+    sentinel = 0x7E01  # a NaN pattern no result can take
+    buf = torch.full((pad + M * N + pad,), sentinel, dtype=torch.int16, device="cuda")
+    da, db = to_device(a), to_device(b)
+    c_ptr = buf.data_ptr() + 2 * pad
+    tc.hgemm_force_path(path)
+    try:
+        assert tc.load().hgemm(da.data_ptr(), db.data_ptr(), c_ptr, M, N, K,
+                               torch.cuda.current_stream().cuda_stream) == 0
+    finally:
+        tc.hgemm_force_path(-1)
+    assert tc.hgemm_device_status() == tc.HGEMM_OK
+    host = buf.cpu().numpy().view(np.uint16)
+    assert np.all(host[:pad] == sentinel) and np.all(host[pad + M * N:] == sentinel)
+    assert_close(host[pad:pad + M * N].view(np.float16).reshape(M, N), ref, what="guarded C")
+
+
+def test_degenerate_sizes():
+    torch = torch_cuda()
+    # K = 0: C is the empty sum, +0
+    c = torch.full((33, 40), 3.0, dtype=torch.float16, device="cuda")
+    e = torch.empty((0,), dtype=torch.float16, device="cuda")
+    tc.hgemm(e, e, c, 33, 40, 0)
+    assert tc.hgemm_device_status() == tc.HGEMM_OK
+    assert torch.count_nonzero(c).item() == 0
+    assert not torch.signbit(c).any()
+    # M = 0 or N = 0: nothing happens, nothing is touched
+    a = torch.ones((5, 16), dtype=torch.float16, device="cuda")
+    c2 = torch.full((5, 1), 7.0, dtype=torch.float16, device="cuda")
+    tc.hgemm(e, a, c2, 0, 5, 16)
+    tc.hgemm(a, e, c2, 5, 0, 16)
+    torch.cuda.synchronize()
+    assert torch.all(c2 == 7.0)
+    # 1×1×1
+    got = run_gpu(np.array([[1.5]], np.float16), np.array([[-2.0]], np.float16))
+    assert float(got[0, 0]) == -3.0
+
+
+def test_host_entry_point_matches_device_entry_point():
+    torch = torch_cuda()
+    M, N, K = 1000, 1000, 1000
+    a, b, _ = synth.workload("hgemm_1000_ragged")
+    want = run_gpu(a, b)
+    ha = torch.from_numpy(a).pin_memory()
+    hb = torch.from_numpy(b).pin_memory()
+    hc = torch.empty((M, N), dtype=torch.float16).pin_memory()
+    da = torch.empty_like(ha, device="cuda")
+    db = torch.empty_like(hb, device="cuda")
+    dc = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    tc.hgemm_host(ha, hb, hc, M, N, K, da, db, dc)
+    assert tc.hgemm_device_status() == tc.HGEMM_OK
+    assert np.array_equal(hc.numpy().view(np.uint16), want.view(np.uint16))
+
+
+def test_side_stream_and_repeatability():
+    torch = torch_cuda()
+    a, b, spec = synth.workload("hgemm_2048")
+    M, N, K = spec["M"], spec["N"], spec["K"]
+    da, db = to_device(a), to_device(b)
+    s = torch.cuda.Stream()
+    outs = []
+    for _ in range(3):
+        dc = torch.empty((M, N), dtype=torch.float16, device="cuda")
+        with torch.cuda.stream(s):
+            tc.hgemm(da, db, dc, M, N, K, s)
+        outs.append(dc)
+    assert tc.hgemm_device_status(s) == tc.HGEMM_OK
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+
+
+def test_unsupported_arguments_raise():
+    torch = torch_cuda()
+    a = torch.ones((4, 8), dtype=torch.float16, device="cuda")
+    with pytest.raises(tc.HgemmError) as ei:
+        tc.hgemm(a, a, a, 4, 4, 8)   # C aliases A
+    assert ei.value.status == tc.HGEMM_ERR_ALIAS
