@@ -63,7 +63,7 @@ DESCRIPTIONS = {
 def parse_args():
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
@@ -145,7 +145,7 @@ class ClockSampler:
             self.out = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=self.out, stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
@@ -178,7 +178,7 @@ class ClockSampler:
         os.unlink(self.path)
         # keep the samples taken inside the timed region, widened by one
         # sampling period so that a short region still gets one
-        inside = [r for r in rows if t0 - 0.1 <= r[0] <= t1 + 0.1]
+        inside = [r for r in rows if t0 - 0.02 <= r[0] <= t1 + 0.02]
         use = inside or rows[-3:]
         sm = [float(r[1]) for r in use if _num(r[1])]
         smax = [float(r[2]) for r in use if _num(r[2])]
@@ -379,8 +379,9 @@ def run_ours(args, spec, a, b, world, rank, local):
 
     # ---- roofline of the dominant (only) kernel
     peaks, peak_src = load_peaks()
-    kernel = {tc.HGEMM_PATH_TC: "hgemm_tc", tc.HGEMM_PATH_SKINNY: "hgemm_skinny",
-              tc.HGEMM_PATH_GENERIC: "hgemm_generic"}.get(path, "other")
+    kernel = {tc.HGEMM_PATH_TC: "hgemm_tc_kernel", tc.HGEMM_PATH_TC_PAIR: "hgemm_tc2_kernel",
+              tc.HGEMM_PATH_SKINNY: "hgemm_skinny_kernel",
+              tc.HGEMM_PATH_GENERIC: "hgemm_generic_kernel"}.get(path, f"path {path}")
     ai = flops / bytes_of(spec)
     ridge = peaks["bf16_tflops"] * FP16_PER_BF16 * 1e12 / (peaks["hbm_gbs"] * 1e9)
     sha = kernel_sources_sha()

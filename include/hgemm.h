@@ -68,9 +68,10 @@ typedef uint16_t hgemm_half_t; /* IEEE binary16 bit pattern */
 /* kernel paths, as reported by hgemm_select_path */
 #define HGEMM_PATH_NONE 0     /* M == 0 or N == 0: nothing to do */
 #define HGEMM_PATH_ZERO 1     /* K == 0: C is filled with +0 (the empty sum) */
-#define HGEMM_PATH_TC 2       /* tcgen05 + TMA persistent kernel, 128×256 tiles */
+#define HGEMM_PATH_TC 2       /* tcgen05 + TMA persistent kernel, one CTA per 128×256 tile */
 #define HGEMM_PATH_SKINNY 3   /* tcgen05 + TMA kernel for small N, split over K */
-#define HGEMM_PATH_GENERIC 4  /* tcgen05 kernel fed by plain loads: any alignment */
+#define HGEMM_PATH_GENERIC 4  /* kernel fed by plain loads: any alignment */
+#define HGEMM_PATH_TC_PAIR 5  /* tcgen05 + TMA persistent kernel, CTA pairs per 256×256 tile */
 
 /* Largest M, N or K accepted (TMA coordinates are signed 32-bit). */
 #define HGEMM_MAX_DIM ((int64_t)0x7FFFFFFF)
@@ -121,10 +122,14 @@ HGEMM_API int hgemm_select_path(const void *A, const void *B, const void *C,
 /*
  * hgemm_force_path — overrides path selection for later calls in this
  * process (testing and profiling). `path` is HGEMM_PATH_TC,
- * HGEMM_PATH_SKINNY or HGEMM_PATH_GENERIC, or -1 to restore automatic
- * selection. A forced TMA path (TC or SKINNY) still falls back to GENERIC
+ * HGEMM_PATH_TC_PAIR, HGEMM_PATH_SKINNY or HGEMM_PATH_GENERIC, or -1 to
+ * restore automatic selection. A forced TMA path still falls back to GENERIC
  * when the operands are not aligned for TMA. Returns HGEMM_OK or
  * HGEMM_ERR_INVALID_ARG.
+ *
+ * Tuning override read once per process: the environment variable
+ * HGEMM_GROUP_M (a positive integer) sets how many M-tiles the tensor-core
+ * kernels' grouped raster order keeps together (default 16).
  */
 HGEMM_API int hgemm_force_path(int path);
 

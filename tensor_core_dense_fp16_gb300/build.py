@@ -20,8 +20,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libhgemm.so")
-SOURCES = ["hgemm_api.cu", "hgemm_tc.cu", "hgemm_generic.cu"]
-HEADERS = ["ptx.cuh", "internal.h"]
+SOURCES = ["hgemm_api.cu", "hgemm_tc.cu", "hgemm_tc2.cu", "hgemm_generic.cu"]
+HEADERS = ["ptx.cuh", "internal.h", "kernel_common.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",

@@ -9,6 +9,7 @@
 // such as PyTorch's, not to every call).
 #include <atomic>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -110,8 +111,19 @@ int choose_path(const void* A, const void* B, const void* C, int64_t M, int64_t 
   const bool tma = tma_ok(A, B, C, N, K);
   const int forced = g_forced_path.load(std::memory_order_relaxed);
   if (forced == HGEMM_PATH_GENERIC || !tma) return HGEMM_PATH_GENERIC;
-  if (forced == HGEMM_PATH_TC) return HGEMM_PATH_TC;
-  return HGEMM_PATH_TC;
+  if (forced == HGEMM_PATH_TC || forced == HGEMM_PATH_TC_PAIR) return forced;
+  // A CTA pair covers 256 rows; with 128 rows or fewer half of it would idle.
+  if (M <= hg::kTcBM) return HGEMM_PATH_TC;
+  return HGEMM_PATH_TC_PAIR;
+}
+
+int group_m_setting() {
+  static const int v = [] {
+    const char* e = std::getenv("HGEMM_GROUP_M");
+    const int x = e ? std::atoi(e) : 0;
+    return x > 0 ? x : 16;
+  }();
+  return v;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
@@ -163,11 +175,37 @@ int run_tc(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t 
   const int64_t tiles = static_cast<int64_t>(args.num_m) * args.num_n;
   if (tiles > 0x7FFFFFFF) return HGEMM_ERR_INVALID_ARG;
   args.num_tiles = static_cast<int>(tiles);
-  args.group_m = 16;
+  args.group_m = group_m_setting();
   args.grid = static_cast<int>(tiles < dev.num_sms ? tiles : dev.num_sms);
   args.status = dev.status;
   args.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
   cudaError_t e = hg::launch_tc_128x256(ma, mb, mc, args, stream);
+  return e == cudaSuccess ? HGEMM_OK : cuda_fail(e);
+}
+
+int run_tc_pair(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                const DeviceState& dev, cudaStream_t stream) {
+  CUtensorMap ma, mb, mc;
+  int rc;
+  if ((rc = encode_map(&ma, A, M, K, hg::kTcBM, hg::kTcBK)) != HGEMM_OK) return rc;
+  if ((rc = encode_map(&mb, B, N, K, hg::kPairBN / 2, hg::kTcBK)) != HGEMM_OK) return rc;
+  if ((rc = encode_map(&mc, C, M, N, hg::kEpiRows, hg::kEpiCols)) != HGEMM_OK) return rc;
+  hg::TcArgs args{};
+  args.M = static_cast<int>(M);
+  args.N = static_cast<int>(N);
+  args.K = static_cast<int>(K);
+  args.num_m = static_cast<int>((M + 2 * hg::kTcBM - 1) / (2 * hg::kTcBM));
+  args.num_n = static_cast<int>((N + hg::kPairBN - 1) / hg::kPairBN);
+  args.num_kb = static_cast<int>((K + hg::kTcBK - 1) / hg::kTcBK);
+  const int64_t tiles = static_cast<int64_t>(args.num_m) * args.num_n;
+  if (tiles > 0x3FFFFFFF) return HGEMM_ERR_INVALID_ARG;
+  args.num_tiles = static_cast<int>(tiles);
+  args.group_m = group_m_setting();
+  const int64_t clusters = hg::pair_max_clusters(dev.num_sms);
+  args.grid = static_cast<int>(2 * (tiles < clusters ? tiles : clusters));
+  args.status = dev.status;
+  args.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
+  cudaError_t e = hg::launch_tc_pair(ma, mb, mc, args, stream);
   return e == cudaSuccess ? HGEMM_OK : cuda_fail(e);
 }
 
@@ -182,6 +220,8 @@ int dispatch(const hgemm_half_t* A, const hgemm_half_t* B, hgemm_half_t* C, int6
       return e == cudaSuccess ? HGEMM_OK : cuda_fail(e);
     case HGEMM_PATH_TC:
       return run_tc(A, B, C, M, N, K, dev, stream);
+    case HGEMM_PATH_TC_PAIR:
+      return run_tc_pair(A, B, C, M, N, K, dev, stream);
     default: {
       hg::PlainArgs pa{A, B, C, M, N, K, dev.status, g_timeout_ns.load()};
       e = hg::launch_generic(pa, dev.num_sms, stream);
@@ -234,8 +274,8 @@ int hgemm_select_path(const void* A, const void* B, const void* C, int64_t M, in
 }
 
 int hgemm_force_path(int path) {
-  if (path != -1 && path != HGEMM_PATH_TC && path != HGEMM_PATH_SKINNY &&
-      path != HGEMM_PATH_GENERIC)
+  if (path != -1 && path != HGEMM_PATH_TC && path != HGEMM_PATH_TC_PAIR &&
+      path != HGEMM_PATH_SKINNY && path != HGEMM_PATH_GENERIC)
     return HGEMM_ERR_INVALID_ARG;
   g_forced_path.store(path);
   return HGEMM_OK;

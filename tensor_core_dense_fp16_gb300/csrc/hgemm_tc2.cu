@@ -1,0 +1,327 @@
+// hgemm_tc2.cu — the CTA-pair tensor-core path of C = A·B on sm_103a.
+//
+// Same contract as hgemm_tc.cu (the HGEMM of "Nvidia Tensor Core-MMA
+// PTX编程入门", §4 示例, FP32 accumulation per "GPU架构与CUDA", 混合精度核函数,
+// zero-filled edges and clipped stores per "GPU架构与CUDA", 共享内存与分块), with
+// a larger output tile shared by two SMs:
+//   * clusters of two CTAs (one per SM of a TPC) own 256×256 output tiles;
+//     CTA r of the pair loads rows [128r, 128r+128) of the tile's A slab and
+//     rows [128r, 128r+128) of its B slab (B stored N×K), 64 K-columns per
+//     stage, into a 6-deep ring of 128-byte-swizzled shared memory;
+//   * the even CTA issues tcgen05.mma.cta_group::2 (M=256, N=256, K=16): the
+//     tensor cores of both SMs read both CTAs' operand halves, and each CTA's
+//     TMEM receives its 128 accumulator rows (256 FP32 columns, two buffers);
+//   * both CTAs' TMA loads complete on the even CTA's "full" barrier; MMA
+//     completion is multicast to both CTAs' "empty" and "accumulator full"
+//     barriers; both CTAs' epilogues release an accumulator buffer by arriving
+//     on the even CTA's "accumulator empty" barrier;
+//   * each CTA's four epilogue warps drain its TMEM half exactly as in the
+//     single-CTA kernel (tcgen05.ld, round to nearest even, swizzled staging,
+//     clipped TMA stores).
+// Per SM, a stage is 32 KB instead of 48 KB for the same MMA work, which
+// allows six stages in flight and halves each SM's share of B traffic.
+#include <cuda_fp16.h>
+
+#include "internal.h"
+#include "kernel_common.cuh"
+#include "ptx.cuh"
+
+namespace hg {
+namespace {
+
+template <int STAGES_>
+struct PairCfg {
+  static constexpr int BM = 2 * kTcBM;   // cluster tile rows
+  static constexpr int BN = kPairBN;     // cluster tile columns
+  static constexpr int ROWS = kTcBM;     // A rows per CTA
+  static constexpr int BROWS = BN / 2;   // B rows (tile columns) per CTA
+  static constexpr int BK = kTcBK;
+  static constexpr int STAGES = STAGES_;
+  static constexpr int UMMA_K = 16;
+  static constexpr int A_BYTES = ROWS * BK * 2;
+  static constexpr int B_BYTES = BROWS * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // landed in each CTA
+  static constexpr int TX_BYTES = 2 * STAGE_BYTES;          // expected by the even CTA
+  static constexpr int EPI_WARPS = 4;
+  static constexpr int C_BOX_BYTES = kEpiRows * kEpiCols * 2;
+  static constexpr int C_BUFS = 2;
+  static constexpr int C_BYTES = EPI_WARPS * C_BUFS * C_BOX_BYTES;
+  static constexpr int ACC_COLS = BN;
+  static constexpr int TMEM_COLS = 2 * ACC_COLS;
+  static constexpr int OFF_A = 0;
+  static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
+  static constexpr int OFF_C = OFF_B + STAGES * B_BYTES;
+  static constexpr int OFF_BAR = OFF_C + C_BYTES;
+  static constexpr int NUM_BARS = 2 * STAGES + 4 + 1;
+  static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+  static constexpr int THREADS = 192;
+  static constexpr uint32_t IDESC = idesc_f16_f32acc(BM, BN);
+
+  static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "1024-byte aligned stages");
+  static_assert(TMEM_COLS == 512, "two 256-column FP32 accumulators");
+  static_assert(SMEM_BYTES <= 232448, "exceeds 227 KB of shared memory per CTA");
+};
+
+template <int STAGES>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
+    hgemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const __grid_constant__ CUtensorMap tmC, const TcArgs p) {
+  using Cfg = PairCfg<STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t sA = sbase + Cfg::OFF_A;
+  const uint32_t sB = sbase + Cfg::OFF_B;
+  const uint32_t bar0 = sbase + Cfg::OFF_BAR;
+  const uint32_t drain_bar = bar0 + 8 * (2 * STAGES + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::OFF_MISC + 4);
+
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  auto accf_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
+  auto acce_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();  // 0: issues the pair MMAs
+  const int cluster_id = blockIdx.x >> 1;
+  const int num_clusters = gridDim.x >> 1;
+  const Watchdog wd{abort_flag, p.status, p.timeout_ns};
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);   // even CTA's arrive.expect_tx; TMA bytes of both CTAs
+      mbar_init(empty_bar(s), 1);  // multicast tcgen05.commit
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(accf_bar(b), 1);                     // multicast tcgen05.commit
+      mbar_init(acce_bar(b), 2 * Cfg::EPI_WARPS);    // every epilogue warp of the pair
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    prefetch_tensormap(&tmA);
+    prefetch_tensormap(&tmB);
+    prefetch_tensormap(&tmC);
+  }
+  if (warp == 1) {
+    tmem_alloc_cg2(smem_u32(tmem_slot), Cfg::TMEM_COLS);
+    tmem_relinquish_alloc_permit_cg2();
+  }
+  // barrier initialisation must be visible to the peer before any remote
+  // arrive or TMA completion can target it
+  tc_fence_before_sync();
+  cluster_sync();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer (both CTAs)
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      long long issued = 0;
+      bool ok = true;
+      for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters) {
+        int mb, nb;
+        tile_coords(t, p.num_m, p.num_n, p.group_m, mb, nb);
+        const int ya = mb * Cfg::BM + static_cast<int>(rank) * Cfg::ROWS;
+        const int yb = nb * Cfg::BN + static_cast<int>(rank) * Cfg::BROWS;
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!wait_phase_cluster(empty_bar(stage), phase ^ 1u, wd, kWdProducerEmpty)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = mapa_shared(full_bar(stage), 0);
+          if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), Cfg::TX_BYTES);
+          tma_load_2d_cg2(sA + stage * Cfg::A_BYTES, &tmA, fb, kb * Cfg::BK, ya);
+          tma_load_2d_cg2(sB + stage * Cfg::B_BYTES, &tmB, fb, kb * Cfg::BK, yb);
+          ++issued;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // Drain. The even CTA's full barriers count the bytes of both CTAs, so
+      // their completion means both CTAs' copies landed. The odd CTA waits
+      // instead until the MMAs consumed its last stages (the empty barrier
+      // phase that follows each of its loads).
+      int s = stage;
+      uint32_t ph = phase;
+      for (long long i = 0; i < issued && i < STAGES; ++i) {
+        if (s == 0) {
+          s = STAGES - 1;
+          ph ^= 1u;
+        } else {
+          --s;
+        }
+        if (rank == 0)
+          wait_drain(full_bar(s), ph, wd);
+        else
+          wait_drain_cluster(empty_bar(s), ph, wd);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------------------------------------- MMA issuer (even CTA)
+    if (rank == 0 && lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters) {
+        if (!wait_phase_cluster(acce_bar(acc), acc_phase ^ 1u, wd, kWdMmaAccEmpty)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * Cfg::ACC_COLS);
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!wait_phase_cluster(full_bar(stage), phase, wd, kWdMmaFull)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint64_t a_desc = sdesc_kmajor_sw128(sA + stage * Cfg::A_BYTES);
+          const uint64_t b_desc = sdesc_kmajor_sw128(sB + stage * Cfg::B_BYTES);
+#pragma unroll
+          for (int k = 0; k < Cfg::BK / Cfg::UMMA_K; ++k)
+            mma_f16_ss_cg2(d_tmem, a_desc + 2u * k, b_desc + 2u * k, Cfg::IDESC,
+                           (kb > 0 || k > 0) ? 1u : 0u);
+          mma_commit_cg2_multicast(empty_bar(stage), 0x3);  // frees the stage in both CTAs
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit_cg2_multicast(accf_bar(acc), 0x3);  // both TMEM halves complete
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      mma_commit_cg2_multicast(drain_bar, 0x1);
+      wait_drain(drain_bar, 0, wd);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------ epilogue (both CTAs)
+    const int q = warp & 3;
+    uint8_t* cbuf_base = smem + Cfg::OFF_C + q * Cfg::C_BUFS * Cfg::C_BOX_BYTES;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    int cb = 0;
+    for (int t = cluster_id; t < p.num_tiles; t += num_clusters) {
+      int mb, nb;
+      tile_coords(t, p.num_m, p.num_n, p.group_m, mb, nb);
+      int ok = 1;
+      if (lane == 0)
+        ok = wait_phase_cluster(accf_bar(acc), acc_phase, wd, kWdEpiAccFull) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after_sync();
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                             static_cast<uint32_t>(acc * Cfg::ACC_COLS);
+      const int y0 = mb * Cfg::BM + static_cast<int>(rank) * Cfg::ROWS + q * kEpiRows;
+#pragma unroll 1
+      for (int c = 0; c < Cfg::BN / kEpiCols; ++c) {
+        uint32_t v0[32], v1[32];
+        tmem_ld_32x32b_x32(t_row + c * kEpiCols, v0);
+        tmem_ld_32x32b_x32(t_row + c * kEpiCols + 32, v1);
+        tmem_ld_wait(v0);
+        tmem_ld_wait(v1);
+        if (c == Cfg::BN / kEpiCols - 1) {
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(mapa_shared(acce_bar(acc), 0));
+        }
+        const int x0 = nb * Cfg::BN + c * kEpiCols;
+        if (x0 >= p.N || y0 >= p.M) continue;
+        if (lane == 0) bulk_wait_group_read<1>();
+        __syncwarp();
+        uint8_t* buf = cbuf_base + cb * Cfg::C_BOX_BYTES;
+        uint8_t* row = buf + lane * 128;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t* v = (j < 4) ? (v0 + 8 * j) : (v1 + 8 * (j - 4));
+          uint4 pk;
+          pk.x = pack_half2(v[0], v[1]);
+          pk.y = pack_half2(v[2], v[3]);
+          pk.z = pack_half2(v[4], v[5]);
+          pk.w = pack_half2(v[6], v[7]);
+          *reinterpret_cast<uint4*>(row + ((j ^ (lane & 7)) << 4)) = pk;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&tmC, smem_u32(buf), x0, y0);
+          bulk_commit_group();
+        }
+        cb ^= 1;
+      }
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+    if (lane == 0) bulk_wait_group<0>();
+    __syncwarp();
+  }
+
+  // Neither CTA frees TMEM before the pair's last MMA and last TMEM read.
+  tc_fence_before_sync();
+  cluster_sync();
+  tc_fence_after_sync();
+  if (warp == 1) tmem_dealloc_cg2(tmem_base, Cfg::TMEM_COLS);
+}
+
+constexpr int kPairStages = 6;
+
+}  // namespace
+
+int pair_max_clusters(int num_sms) {
+  using Cfg = PairCfg<kPairStages>;
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return num_sms / 2;
+  if (cached[dev] > 0) return cached[dev];
+  auto kern = hgemm_tc2_kernel<kPairStages>;
+  int n = 0;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) ==
+      cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(num_sms & ~1));
+    cfg.blockDim = dim3(Cfg::THREADS);
+    cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
+  }
+  (void)cudaGetLastError();
+  if (n <= 0) n = num_sms / 2;
+  cached[dev] = n;
+  return n;
+}
+
+cudaError_t launch_tc_pair(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
+                           const TcArgs& args, cudaStream_t stream) {
+  using Cfg = PairCfg<kPairStages>;
+  static bool attr_done[64] = {};
+  auto kern = hgemm_tc2_kernel<kPairStages>;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !attr_done[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_done[dev] = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(args.grid));
+  cfg.blockDim = dim3(Cfg::THREADS);
+  cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+  cfg.stream = stream;
+  return cudaLaunchKernelEx(&cfg, kern, a, b, c, args);
+}
+
+}  // namespace hg

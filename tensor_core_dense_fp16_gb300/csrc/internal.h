@@ -44,6 +44,10 @@ struct PlainArgs {
 // error, if any). Shared-memory attributes are set on first use per device.
 cudaError_t launch_tc_128x256(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
                               const TcArgs& args, cudaStream_t stream);
+cudaError_t launch_tc_pair(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
+                           const TcArgs& args, cudaStream_t stream);
+// Largest number of co-resident 2-CTA clusters of the pair kernel.
+int pair_max_clusters(int num_sms);
 cudaError_t launch_zero_fill(uint16_t* C, int64_t count, cudaStream_t stream);
 cudaError_t launch_generic(const PlainArgs& args, int num_sms, cudaStream_t stream);
 
@@ -54,6 +58,7 @@ cudaError_t status_word_address(int** addr);
 constexpr int kTcBM = 128;
 constexpr int kTcBN = 256;
 constexpr int kTcBK = 64;
+constexpr int kPairBN = 256;   // pair kernel: 256×256 tiles, 128 B rows per CTA
 constexpr int kEpiRows = 32;   // rows of one staged C box (one epilogue warp)
 constexpr int kEpiCols = 64;   // columns of one staged C box (128 bytes)
 

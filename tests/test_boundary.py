@@ -68,8 +68,11 @@ def test_path_selection(lib):
     assert sel(A16, B16, C16, 0, 5, 5) == tc.HGEMM_PATH_NONE
     assert sel(A16, B16, C16, 5, 0, 5) == tc.HGEMM_PATH_NONE
     assert sel(A16, B16, C16, 4, 8, 0) == tc.HGEMM_PATH_ZERO
-    assert sel(A16, B16, C16, 8192, 8192, 8192) == tc.HGEMM_PATH_TC
-    assert sel(A16, B16, C16, 1000, 1000, 1000) == tc.HGEMM_PATH_TC
+    assert sel(A16, B16, C16, 8192, 8192, 8192) == tc.HGEMM_PATH_TC_PAIR
+    assert sel(A16, B16, C16, 1000, 1000, 1000) == tc.HGEMM_PATH_TC_PAIR
+    # 128 rows or fewer: one CTA per tile (a pair would leave half idle)
+    assert sel(A16, B16, C16, 128, 4096, 4096) == tc.HGEMM_PATH_TC
+    assert sel(A16, B16, C16, 129, 4096, 4096) == tc.HGEMM_PATH_TC_PAIR
     # TMA needs 16-byte row pitches and 16-byte base addresses
     assert sel(A16, B16, C16, 64, 64, 1001) == tc.HGEMM_PATH_GENERIC
     assert sel(A16, B16, C16, 64, 1001, 64) == tc.HGEMM_PATH_GENERIC
@@ -77,7 +80,8 @@ def test_path_selection(lib):
     assert sel(A16, B16 + 8, C16, 64, 64, 64) == tc.HGEMM_PATH_GENERIC
     assert sel(A16, B16, C16 + 4, 64, 64, 64) == tc.HGEMM_PATH_GENERIC
     # M is free: any M works with TMA
-    assert sel(A16, B16, C16, 1001, 64, 64) == tc.HGEMM_PATH_TC
+    assert sel(A16, B16, C16, 1001, 64, 64) == tc.HGEMM_PATH_TC_PAIR
+    assert sel(A16, B16, C16, 1, 64, 64) == tc.HGEMM_PATH_TC
 
 
 def test_forced_paths(lib):
@@ -86,13 +90,15 @@ def test_forced_paths(lib):
         assert tc.hgemm_select_path(A16, B16, C16, 256, 256, 256) == tc.HGEMM_PATH_GENERIC
         tc.hgemm_force_path(tc.HGEMM_PATH_TC)
         assert tc.hgemm_select_path(A16, B16, C16, 256, 256, 256) == tc.HGEMM_PATH_TC
+        tc.hgemm_force_path(tc.HGEMM_PATH_TC_PAIR)
+        assert tc.hgemm_select_path(A16, B16, C16, 64, 256, 256) == tc.HGEMM_PATH_TC_PAIR
         # a forced TMA path still needs TMA-able operands
         assert tc.hgemm_select_path(A16, B16, C16, 256, 256, 255) == tc.HGEMM_PATH_GENERIC
         with pytest.raises(tc.HgemmError):
             tc.hgemm_force_path(77)
     finally:
         tc.hgemm_force_path(-1)
-    assert tc.hgemm_select_path(A16, B16, C16, 256, 256, 256) == tc.HGEMM_PATH_TC
+    assert tc.hgemm_select_path(A16, B16, C16, 256, 256, 256) == tc.HGEMM_PATH_TC_PAIR
 
 
 def test_invalid_arguments_rejected_before_any_device_work(lib):
