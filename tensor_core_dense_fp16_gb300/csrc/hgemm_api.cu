@@ -33,9 +33,16 @@ struct DeviceState {
   std::atomic<int> ready{0};  // 0 unknown, 1 supported, -1 unsupported
   int num_sms = 0;
   int* status = nullptr;
+  hg::DeviceProfile prof{};
 };
 DeviceState g_devices[kMaxDevices];
 std::mutex g_device_mu;
+
+// Nominal GB300 figures, used by hgemm_select_path before any device has
+// been used in this process: 152 SMs, 76 SM pairs, and (conservatively) as
+// many 4- and 8-CTA clusters as whole groups of SMs.
+constexpr hg::DeviceProfile kNominalProfile{152, 76, 38, 16};
+std::atomic<const hg::DeviceProfile*> g_last_profile{&kNominalProfile};
 
 int cuda_fail(cudaError_t e) {
   t_last_cuda_error = static_cast<int>(e);
@@ -67,12 +74,17 @@ int current_device(DeviceState** out) {
         if ((e = hg::status_word_address(&status)) != cudaSuccess) return cuda_fail(e);
         st.num_sms = sms;
         st.status = status;
+        st.prof.num_sms = sms;
+        st.prof.pair_clusters = hg::pair_max_clusters(sms);
+        st.prof.split2_clusters = hg::skinny_max_clusters(2, sms);
+        st.prof.split4_clusters = hg::skinny_max_clusters(4, sms);
         r = 1;
       }
       st.ready.store(r, std::memory_order_release);
     }
   }
   if (r < 0) return HGEMM_ERR_UNSUPPORTED_DEVICE;
+  g_last_profile.store(&st.prof, std::memory_order_release);
   *out = &st;
   return HGEMM_OK;
 }
@@ -105,17 +117,57 @@ bool tma_ok(const void* A, const void* B, const void* C, int64_t N, int64_t K) {
   return al16(A) && al16(B) && al16(C) && (K % 8 == 0) && (N % 8 == 0);
 }
 
-int choose_path(const void* A, const void* B, const void* C, int64_t M, int64_t N, int64_t K) {
+int choose_path(const void* A, const void* B, const void* C, int64_t M, int64_t N, int64_t K,
+                const hg::DeviceProfile& prof, int* split) {
+  *split = 1;
   if (M == 0 || N == 0) return HGEMM_PATH_NONE;
   if (K == 0) return HGEMM_PATH_ZERO;
   const bool tma = tma_ok(A, B, C, N, K);
   const int forced = g_forced_path.load(std::memory_order_relaxed);
   if (forced == HGEMM_PATH_GENERIC || !tma) return HGEMM_PATH_GENERIC;
+  return hg::choose_tma_path(M, N, K, prof, forced, split);
+}
+
+}  // namespace
+
+namespace hg {
+
+int choose_tma_path(int64_t M, int64_t N, int64_t K, const DeviceProfile& dev, int forced,
+                    int* split) {
+  *split = 1;
+  const int64_t tiles = ((M + 2 * kTcBM - 1) / (2 * kTcBM)) * ((N + kPairBN - 1) / kPairBN);
+  const int64_t num_kb = (K + kTcBK - 1) / kTcBK;
+  // split-K: 4 slices when there are K blocks for them and the 8-CTA
+  // clusters of all tiles fit on the device at once, else 2
+  auto best_split = [&](bool need_idle) -> int {
+    if (need_idle && 2 * tiles > dev.pair_clusters) return 1;  // pairs already fill the GPU
+    if (num_kb >= 4 && tiles <= dev.split4_clusters && (!need_idle || 4 * tiles <= dev.pair_clusters))
+      return 4;
+    if (num_kb >= 2 && tiles <= dev.split2_clusters) return 2;
+    return 1;
+  };
   if (forced == HGEMM_PATH_TC || forced == HGEMM_PATH_TC_PAIR) return forced;
+  if (forced == HGEMM_PATH_SKINNY) {
+    const int s = best_split(false);
+    if (s > 1) {
+      *split = s;
+      return HGEMM_PATH_SKINNY;
+    }
+    return HGEMM_PATH_TC_PAIR;
+  }
+  const int s = best_split(true);
+  if (s > 1) {
+    *split = s;
+    return HGEMM_PATH_SKINNY;
+  }
   // A CTA pair covers 256 rows; with 128 rows or fewer half of it would idle.
-  if (M <= hg::kTcBM) return HGEMM_PATH_TC;
+  if (M <= kTcBM) return HGEMM_PATH_TC;
   return HGEMM_PATH_TC_PAIR;
 }
+
+}  // namespace hg
+
+namespace {
 
 int group_m_setting() {
   static const int v = [] {
@@ -209,10 +261,36 @@ int run_tc_pair(const void* A, const void* B, void* C, int64_t M, int64_t N, int
   return e == cudaSuccess ? HGEMM_OK : cuda_fail(e);
 }
 
+int run_skinny(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int split,
+               const DeviceState& dev, cudaStream_t stream) {
+  CUtensorMap ma, mb, mc;
+  int rc;
+  if ((rc = encode_map(&ma, A, M, K, hg::kTcBM, hg::kTcBK)) != HGEMM_OK) return rc;
+  if ((rc = encode_map(&mb, B, N, K, hg::kPairBN / 2, hg::kTcBK)) != HGEMM_OK) return rc;
+  if ((rc = encode_map(&mc, C, M, N, hg::kEpiRows, hg::kEpiCols)) != HGEMM_OK) return rc;
+  hg::TcArgs args{};
+  args.M = static_cast<int>(M);
+  args.N = static_cast<int>(N);
+  args.K = static_cast<int>(K);
+  args.num_m = static_cast<int>((M + 2 * hg::kTcBM - 1) / (2 * hg::kTcBM));
+  args.num_n = static_cast<int>((N + hg::kPairBN - 1) / hg::kPairBN);
+  args.num_kb = static_cast<int>((K + hg::kTcBK - 1) / hg::kTcBK);
+  const int64_t tiles = static_cast<int64_t>(args.num_m) * args.num_n;
+  if (tiles * 2 * split > 0x7FFFFFFF) return HGEMM_ERR_INVALID_ARG;
+  args.num_tiles = static_cast<int>(tiles);
+  args.group_m = 1;
+  args.grid = static_cast<int>(tiles * 2 * split);
+  args.status = dev.status;
+  args.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
+  cudaError_t e = hg::launch_skinny(split, ma, mb, mc, args, stream);
+  return e == cudaSuccess ? HGEMM_OK : cuda_fail(e);
+}
+
 int dispatch(const hgemm_half_t* A, const hgemm_half_t* B, hgemm_half_t* C, int64_t M, int64_t N,
              int64_t K, const DeviceState& dev, cudaStream_t stream) {
   cudaError_t e;
-  switch (choose_path(A, B, C, M, N, K)) {
+  int split = 1;
+  switch (choose_path(A, B, C, M, N, K, dev.prof, &split)) {
     case HGEMM_PATH_NONE:
       return HGEMM_OK;
     case HGEMM_PATH_ZERO:
@@ -222,6 +300,8 @@ int dispatch(const hgemm_half_t* A, const hgemm_half_t* B, hgemm_half_t* C, int6
       return run_tc(A, B, C, M, N, K, dev, stream);
     case HGEMM_PATH_TC_PAIR:
       return run_tc_pair(A, B, C, M, N, K, dev, stream);
+    case HGEMM_PATH_SKINNY:
+      return run_skinny(A, B, C, M, N, K, split, dev, stream);
     default: {
       hg::PlainArgs pa{A, B, C, M, N, K, dev.status, g_timeout_ns.load()};
       e = hg::launch_generic(pa, dev.num_sms, stream);
@@ -270,7 +350,8 @@ int hgemm_select_path(const void* A, const void* B, const void* C, int64_t M, in
                       int64_t K) {
   int rc = validate(A, B, C, M, N, K);
   if (rc != HGEMM_OK) return rc;
-  return choose_path(A, B, C, M, N, K);
+  int split = 1;
+  return choose_path(A, B, C, M, N, K, *g_last_profile.load(std::memory_order_acquire), &split);
 }
 
 int hgemm_force_path(int path) {

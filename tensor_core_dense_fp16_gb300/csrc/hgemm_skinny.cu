@@ -1,0 +1,382 @@
+// hgemm_skinny.cu — C = A·B when the output has too few 256×256 tiles to
+// occupy the GPU (a small N or M against a long K, e.g. 4096×256×4096: the
+// off-diagonal update of a recursive TRMM with a 4096×256 right-hand side, as
+// in "异构计算中高性能TRMM与TRSM的递归算法实现", §2.2 and §5.1). Such shapes are
+// bound by the bytes of A, so the design goal is that every SM streams A.
+//
+// Same contract as the other paths ("Nvidia Tensor Core-MMA PTX编程入门", §4
+// 示例; FP32 accumulation, "GPU架构与CUDA", 混合精度核函数; zero-filled edges and
+// clipped stores, "GPU架构与CUDA", 共享内存与分块).
+//
+// Design:
+//   * one cluster of 2·S CTAs per 256×256 output tile; CTA rank r belongs to
+//     K-slice p = r / 2 and tile half h = r % 2; pair p (ranks 2p, 2p+1) runs
+//     the CTA-pair main loop of hgemm_tc2.cu over its contiguous range of
+//     64-wide K blocks, so A is read from memory exactly once over the grid;
+//   * each CTA ends with a 128×256 FP32 partial sum in its TMEM;
+//   * the S partials of a half are reduced through distributed shared
+//     memory: the 256 columns are cut into S column ranges, the CTA of slice
+//     p owns range p, and every CTA writes its other ranges into the owners'
+//     shared memory (the operand ring, free once all MMAs finished); after a
+//     cluster barrier each owner adds the S partials in slice order (so the
+//     result does not depend on timing), rounds to FP16 and TMA-stores its
+//     128-row × (256/S)-column block of C.
+// No global scratch memory is used.
+#include <cuda_fp16.h>
+
+#include "internal.h"
+#include "kernel_common.cuh"
+#include "ptx.cuh"
+
+namespace hg {
+namespace {
+
+constexpr int kSkStages = 6;
+
+template <int SPLIT>
+struct SkCfg {
+  static constexpr int BM = 2 * kTcBM;   // tile rows (both CTAs of a pair)
+  static constexpr int BN = kPairBN;     // tile columns
+  static constexpr int ROWS = kTcBM;     // rows per CTA
+  static constexpr int BROWS = BN / 2;   // B rows per CTA
+  static constexpr int BK = kTcBK;
+  static constexpr int STAGES = kSkStages;
+  static constexpr int UMMA_K = 16;
+  static constexpr int A_BYTES = ROWS * BK * 2;
+  static constexpr int B_BYTES = BROWS * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int TX_BYTES = 2 * STAGE_BYTES;
+  static constexpr int OWN_COLS = BN / SPLIT;                 // columns reduced per CTA
+  static constexpr int SLOT_BYTES = ROWS * OWN_COLS * 4;      // one FP32 partial block
+  static constexpr int RECV_BYTES = SPLIT * SLOT_BYTES;       // slot p from slice p
+  static constexpr int OFF_A = 0;
+  static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
+  static constexpr int OFF_C = OFF_B + STAGES * B_BYTES;     // FP16 staging of C
+  static constexpr int C_WARP_BYTES = kEpiRows * OWN_COLS * 2;
+  static constexpr int C_BYTES = 4 * ((C_WARP_BYTES + 1023) / 1024) * 1024;
+  static constexpr int OFF_BAR = OFF_C + C_BYTES;
+  static constexpr int NUM_BARS = 2 * STAGES + 2;  // full, empty, accumulator full, drain
+  static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+  static constexpr int THREADS = 192;
+  static constexpr int TMEM_COLS = BN;
+  static constexpr uint32_t IDESC = idesc_f16_f32acc(BM, BN);
+
+  static_assert(RECV_BYTES <= OFF_C, "receive slots reuse the operand ring");
+  static_assert(OWN_COLS % 32 == 0, "column ranges are whole 32-column TMEM loads");
+  static_assert(SMEM_BYTES <= 232448, "exceeds 227 KB of shared memory per CTA");
+};
+
+template <int SPLIT>
+__global__ void __launch_bounds__(192, 1)
+    hgemm_skinny_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmC, const TcArgs p) {
+  using Cfg = SkCfg<SPLIT>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t sA = sbase + Cfg::OFF_A;
+  const uint32_t sB = sbase + Cfg::OFF_B;
+  const uint32_t bar0 = sbase + Cfg::OFF_BAR;
+  const uint32_t accf_bar = bar0 + 8u * (2 * Cfg::STAGES);
+  const uint32_t drain_bar = accf_bar + 8u;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::OFF_MISC + 4);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (Cfg::STAGES + s); };
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int slice = static_cast<int>(rank >> 1);  // K-slice p
+  const int half = static_cast<int>(rank & 1);    // tile rows [128h, 128h+128)
+  const uint32_t leader = rank & ~1u;             // even CTA of this pair
+  const uint16_t pair_mask = static_cast<uint16_t>(0x3u << leader);
+  const int tile = blockIdx.x / (2 * SPLIT);
+  const int mb = tile / p.num_n;
+  const int nb = tile % p.num_n;
+  const int kb0 = static_cast<int>(static_cast<long long>(p.num_kb) * slice / SPLIT);
+  const int kb1 = static_cast<int>(static_cast<long long>(p.num_kb) * (slice + 1) / SPLIT);
+  const Watchdog wd{abort_flag, p.status, p.timeout_ns};
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < Cfg::STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    mbar_init(accf_bar, 1);
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    prefetch_tensormap(&tmA);
+    prefetch_tensormap(&tmB);
+    prefetch_tensormap(&tmC);
+  }
+  if (warp == 1) {
+    tmem_alloc_cg2(smem_u32(tmem_slot), Cfg::TMEM_COLS);
+    tmem_relinquish_alloc_permit_cg2();
+  }
+  tc_fence_before_sync();
+  cluster_sync();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+
+  int ok = 1;
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer (all CTAs)
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      long long issued = 0;
+      const int ya = mb * Cfg::BM + half * Cfg::ROWS;
+      const int yb = nb * Cfg::BN + half * Cfg::BROWS;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!wait_phase_cluster(empty_bar(stage), phase ^ 1u, wd, kWdProducerEmpty)) break;
+        const uint32_t fb = mapa_shared(full_bar(stage), leader);
+        if (rank == leader) mbar_arrive_expect_tx(full_bar(stage), Cfg::TX_BYTES);
+        tma_load_2d_cg2(sA + stage * Cfg::A_BYTES, &tmA, fb, kb * Cfg::BK, ya);
+        tma_load_2d_cg2(sB + stage * Cfg::B_BYTES, &tmB, fb, kb * Cfg::BK, yb);
+        ++issued;
+        if (++stage == Cfg::STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      int s = stage;
+      uint32_t ph = phase;
+      for (long long i = 0; i < issued && i < Cfg::STAGES; ++i) {
+        if (s == 0) {
+          s = Cfg::STAGES - 1;
+          ph ^= 1u;
+        } else {
+          --s;
+        }
+        if (rank == leader)
+          wait_drain(full_bar(s), ph, wd);
+        else
+          wait_drain_cluster(empty_bar(s), ph, wd);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // --------------------------------------------- MMA issuer (even CTAs)
+    if (rank == leader && lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool good = true;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!wait_phase_cluster(full_bar(stage), phase, wd, kWdMmaFull)) {
+          good = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint64_t a_desc = sdesc_kmajor_sw128(sA + stage * Cfg::A_BYTES);
+        const uint64_t b_desc = sdesc_kmajor_sw128(sB + stage * Cfg::B_BYTES);
+#pragma unroll
+        for (int k = 0; k < Cfg::BK / Cfg::UMMA_K; ++k)
+          mma_f16_ss_cg2(tmem_base, a_desc + 2u * k, b_desc + 2u * k, Cfg::IDESC,
+                         (kb > kb0 || k > 0) ? 1u : 0u);
+        mma_commit_cg2_multicast(empty_bar(stage), pair_mask);
+        if (++stage == Cfg::STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (good) mma_commit_cg2_multicast(accf_bar, pair_mask);
+      mma_commit_cg2_multicast(drain_bar, static_cast<uint16_t>(1u << leader));
+      wait_drain(drain_bar, 0, wd);
+    }
+    __syncwarp();
+  } else {
+    // epilogue warps: this CTA's partial is complete once the pair's MMAs are
+    if (lane == 0) ok = wait_phase_cluster(accf_bar, 0, wd, kWdEpiAccFull) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    tc_fence_after_sync();
+  }
+
+  // 1: every pair's MMAs are done, so every CTA's operand ring is free
+  cluster_sync();
+
+  const int q = warp & 3;  // TMEM lanes / tile rows 32q .. 32q+31 of this CTA
+  const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+  const int row = q * 32 + lane;
+  if (warp >= 2 && ok) {
+    // send the column ranges owned by the other slices to their owners
+    for (int j = 0; j < SPLIT; ++j) {
+      if (j == slice) continue;
+      const uint32_t dst_rank = static_cast<uint32_t>(2 * j + half);
+      const uint32_t slot = mapa_shared(sbase + slice * Cfg::SLOT_BYTES, dst_rank);
+#pragma unroll 1
+      for (int c32 = 0; c32 < Cfg::OWN_COLS / 32; ++c32) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(t_row + j * Cfg::OWN_COLS + c32 * 32, v);
+        tmem_ld_wait(v);
+        // row-major FP32 rows of OWN_COLS; 16-byte chunks XOR-swizzled by row
+        // so that the 32 rows of a warp spread over the banks
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int chunk = c32 * 8 + u;
+          const int pos = chunk ^ (row & (Cfg::OWN_COLS / 4 - 1) & 15);
+          st_cluster_v4(slot + row * (Cfg::OWN_COLS * 4) + pos * 16, v[4 * u], v[4 * u + 1],
+                        v[4 * u + 2], v[4 * u + 3]);
+        }
+      }
+    }
+  }
+
+  // 2: every partial has been delivered
+  cluster_sync();
+
+  if (warp >= 2 && ok) {
+    const int x0 = nb * Cfg::BN + slice * Cfg::OWN_COLS;
+    const int y0 = mb * Cfg::BM + half * Cfg::ROWS + q * kEpiRows;
+    uint8_t* cbuf = smem + Cfg::OFF_C + q * (Cfg::C_BYTES / 4);
+#pragma unroll 1
+    for (int c32 = 0; c32 < Cfg::OWN_COLS / 32; ++c32) {
+      uint32_t own[32];
+      tmem_ld_32x32b_x32(t_row + slice * Cfg::OWN_COLS + c32 * 32, own);
+      tmem_ld_wait(own);
+      float acc[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+      // add the slices in order 0, 1, ..., SPLIT-1 (slice 0 first, exactly)
+      for (int sl = 0; sl < SPLIT; ++sl) {
+        if (sl == slice) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) acc[i] = (sl == 0) ? __uint_as_float(own[i]) : acc[i] + __uint_as_float(own[i]);
+        } else {
+          const uint8_t* src = smem + sl * Cfg::SLOT_BYTES + row * (Cfg::OWN_COLS * 4);
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int chunk = c32 * 8 + u;
+            const int pos = chunk ^ (row & (Cfg::OWN_COLS / 4 - 1) & 15);
+            const float4 f = *reinterpret_cast<const float4*>(src + pos * 16);
+            if (sl == 0) {
+              acc[4 * u] = f.x;
+              acc[4 * u + 1] = f.y;
+              acc[4 * u + 2] = f.z;
+              acc[4 * u + 3] = f.w;
+            } else {
+              acc[4 * u] += f.x;
+              acc[4 * u + 1] += f.y;
+              acc[4 * u + 2] += f.z;
+              acc[4 * u + 3] += f.w;
+            }
+          }
+        }
+      }
+      // FP16 row segment (64 bytes) into the 128-byte-swizzled staging box
+      // (rows of OWN_COLS*2 bytes; a 64-column range is one 128-byte row)
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        uint4 pk;
+        pk.x = pack_half2(__float_as_uint(acc[8 * u]), __float_as_uint(acc[8 * u + 1]));
+        pk.y = pack_half2(__float_as_uint(acc[8 * u + 2]), __float_as_uint(acc[8 * u + 3]));
+        pk.z = pack_half2(__float_as_uint(acc[8 * u + 4]), __float_as_uint(acc[8 * u + 5]));
+        pk.w = pack_half2(__float_as_uint(acc[8 * u + 6]), __float_as_uint(acc[8 * u + 7]));
+        const int chunk = c32 * 4 + u;  // 16-byte chunk within the row
+        const int box = chunk >> 3;     // 64-column box
+        const int cin = chunk & 7;
+        *reinterpret_cast<uint4*>(cbuf + box * (kEpiRows * 128) + lane * 128 +
+                                  ((cin ^ (lane & 7)) << 4)) = pk;
+      }
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0 && y0 < p.M) {
+      for (int box = 0; box < Cfg::OWN_COLS / kEpiCols; ++box) {
+        const int x = x0 + box * kEpiCols;
+        if (x < p.N) tma_store_2d(&tmC, smem_u32(cbuf + box * (kEpiRows * 128)), x, y0);
+      }
+      bulk_commit_group();
+      bulk_wait_group<0>();
+    }
+    __syncwarp();
+  }
+
+  tc_fence_before_sync();
+  cluster_sync();
+  tc_fence_after_sync();
+  if (warp == 1) tmem_dealloc_cg2(tmem_base, Cfg::TMEM_COLS);
+}
+
+template <int SPLIT>
+cudaError_t launch_split(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
+                         const TcArgs& args, cudaStream_t stream) {
+  using Cfg = SkCfg<SPLIT>;
+  static bool attr_done[64] = {};
+  auto kern = hgemm_skinny_kernel<SPLIT>;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !attr_done[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_done[dev] = true;
+  }
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2 * SPLIT;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(args.num_tiles * 2 * SPLIT));
+  cfg.blockDim = dim3(Cfg::THREADS);
+  cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, a, b, c, args);
+}
+
+template <int SPLIT>
+int max_clusters_split(int num_sms) {
+  using Cfg = SkCfg<SPLIT>;
+  auto kern = hgemm_skinny_kernel<SPLIT>;
+  int n = 0;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) ==
+      cudaSuccess) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2 * SPLIT;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>((num_sms / (2 * SPLIT)) * 2 * SPLIT));
+    cfg.blockDim = dim3(Cfg::THREADS);
+    cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
+  }
+  (void)cudaGetLastError();
+  return n;
+}
+
+}  // namespace
+
+int skinny_max_clusters(int split, int num_sms) {
+  switch (split) {
+    case 2:
+      return max_clusters_split<2>(num_sms);
+    case 4:
+      return max_clusters_split<4>(num_sms);
+    default:
+      return 0;
+  }
+}
+
+cudaError_t launch_skinny(int split, const CUtensorMap& a, const CUtensorMap& b,
+                          const CUtensorMap& c, const TcArgs& args, cudaStream_t stream) {
+  switch (split) {
+    case 2:
+      return launch_split<2>(a, b, c, args, stream);
+    case 4:
+      return launch_split<4>(a, b, c, args, stream);
+    default:
+      return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace hg

@@ -48,11 +48,31 @@ cudaError_t launch_tc_pair(const CUtensorMap& a, const CUtensorMap& b, const CUt
                            const TcArgs& args, cudaStream_t stream);
 // Largest number of co-resident 2-CTA clusters of the pair kernel.
 int pair_max_clusters(int num_sms);
+// Split-K cluster kernel for few output tiles: `split` K-slices (2 or 4),
+// one cluster of 2*split CTAs per 256×256 tile (args.num_tiles of them).
+cudaError_t launch_skinny(int split, const CUtensorMap& a, const CUtensorMap& b,
+                          const CUtensorMap& c, const TcArgs& args, cudaStream_t stream);
+// Largest number of co-resident clusters of the split-K kernel.
+int skinny_max_clusters(int split, int num_sms);
 cudaError_t launch_zero_fill(uint16_t* C, int64_t count, cudaStream_t stream);
 cudaError_t launch_generic(const PlainArgs& args, int num_sms, cudaStream_t stream);
 
 // Address of the device watchdog word on the current device.
 cudaError_t status_word_address(int** addr);
+
+// Co-residency limits of the cluster kernels on one device, measured once
+// (or nominal GB300 figures when no device has been queried).
+struct DeviceProfile {
+  int num_sms;
+  int pair_clusters;    // co-resident 2-CTA clusters of the pair kernel
+  int split2_clusters;  // co-resident 4-CTA clusters of the split-K kernel
+  int split4_clusters;  // co-resident 8-CTA clusters of the split-K kernel
+};
+
+// Kernel choice for a TMA-able product. Returns an HGEMM_PATH_* value and,
+// for the split-K path, the number of K-slices in *split.
+int choose_tma_path(int64_t M, int64_t N, int64_t K, const DeviceProfile& dev, int forced,
+                    int* split);
 
 // Tile geometry of the tensor-core path, for the host-side tensor maps.
 constexpr int kTcBM = 128;

@@ -324,4 +324,12 @@ __device__ __forceinline__ void mma_commit_cg2_multicast(uint32_t bar, uint16_t 
       : "memory");
 }
 
+// 16-byte store to shared memory of any CTA of the cluster.
+__device__ __forceinline__ void st_cluster_v4(uint32_t cluster_addr, uint32_t a, uint32_t b,
+                                              uint32_t c, uint32_t d) {
+  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr), "r"(a),
+               "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+
 }  // namespace hg

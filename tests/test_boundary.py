@@ -68,11 +68,18 @@ def test_path_selection(lib):
     assert sel(A16, B16, C16, 0, 5, 5) == tc.HGEMM_PATH_NONE
     assert sel(A16, B16, C16, 5, 0, 5) == tc.HGEMM_PATH_NONE
     assert sel(A16, B16, C16, 4, 8, 0) == tc.HGEMM_PATH_ZERO
+    # many 256x256 tiles: CTA pairs
     assert sel(A16, B16, C16, 8192, 8192, 8192) == tc.HGEMM_PATH_TC_PAIR
-    assert sel(A16, B16, C16, 1000, 1000, 1000) == tc.HGEMM_PATH_TC_PAIR
-    # 128 rows or fewer: one CTA per tile (a pair would leave half idle)
-    assert sel(A16, B16, C16, 128, 4096, 4096) == tc.HGEMM_PATH_TC
-    assert sel(A16, B16, C16, 129, 4096, 4096) == tc.HGEMM_PATH_TC_PAIR
+    assert sel(A16, B16, C16, 2048, 2048, 2048) == tc.HGEMM_PATH_TC_PAIR
+    # few tiles and a long K: split K over clusters of pairs
+    assert sel(A16, B16, C16, 4096, 256, 4096) == tc.HGEMM_PATH_SKINNY
+    assert sel(A16, B16, C16, 1000, 1000, 1000) == tc.HGEMM_PATH_SKINNY
+    assert sel(A16, B16, C16, 256, 256, 256) == tc.HGEMM_PATH_SKINNY
+    # too little K to split: one K block
+    assert sel(A16, B16, C16, 4096, 256, 64) == tc.HGEMM_PATH_TC_PAIR
+    assert sel(A16, B16, C16, 128, 256, 64) == tc.HGEMM_PATH_TC
+    # 128 rows or fewer with many tiles: one CTA per 128x256 tile
+    assert sel(A16, B16, C16, 128, 16384, 4096) == tc.HGEMM_PATH_TC
     # TMA needs 16-byte row pitches and 16-byte base addresses
     assert sel(A16, B16, C16, 64, 64, 1001) == tc.HGEMM_PATH_GENERIC
     assert sel(A16, B16, C16, 64, 1001, 64) == tc.HGEMM_PATH_GENERIC
@@ -82,6 +89,7 @@ def test_path_selection(lib):
     # M is free: any M works with TMA
     assert sel(A16, B16, C16, 1001, 64, 64) == tc.HGEMM_PATH_TC_PAIR
     assert sel(A16, B16, C16, 1, 64, 64) == tc.HGEMM_PATH_TC
+    assert sel(A16, B16, C16, 1, 64, 4096) == tc.HGEMM_PATH_SKINNY
 
 
 def test_forced_paths(lib):
@@ -92,13 +100,18 @@ def test_forced_paths(lib):
         assert tc.hgemm_select_path(A16, B16, C16, 256, 256, 256) == tc.HGEMM_PATH_TC
         tc.hgemm_force_path(tc.HGEMM_PATH_TC_PAIR)
         assert tc.hgemm_select_path(A16, B16, C16, 64, 256, 256) == tc.HGEMM_PATH_TC_PAIR
+        tc.hgemm_force_path(tc.HGEMM_PATH_SKINNY)
+        assert tc.hgemm_select_path(A16, B16, C16, 8192, 8192, 8192) == tc.HGEMM_PATH_TC_PAIR
+        assert tc.hgemm_select_path(A16, B16, C16, 512, 512, 512) == tc.HGEMM_PATH_SKINNY
+        # a single K block cannot be split
+        assert tc.hgemm_select_path(A16, B16, C16, 512, 512, 64) == tc.HGEMM_PATH_TC_PAIR
         # a forced TMA path still needs TMA-able operands
         assert tc.hgemm_select_path(A16, B16, C16, 256, 256, 255) == tc.HGEMM_PATH_GENERIC
         with pytest.raises(tc.HgemmError):
             tc.hgemm_force_path(77)
     finally:
         tc.hgemm_force_path(-1)
-    assert tc.hgemm_select_path(A16, B16, C16, 256, 256, 256) == tc.HGEMM_PATH_TC_PAIR
+    assert tc.hgemm_select_path(A16, B16, C16, 256, 256, 256) == tc.HGEMM_PATH_SKINNY
 
 
 def test_invalid_arguments_rejected_before_any_device_work(lib):

@@ -20,7 +20,8 @@ from gpu_helpers import assert_close, oracle_threads, run_gpu, to_device, torch_
 pytestmark = pytest.mark.gpu
 
 
-TMA_PATHS = [None, tc.HGEMM_PATH_TC, tc.HGEMM_PATH_TC_PAIR]   # None: automatic choice
+TMA_PATHS = [None, tc.HGEMM_PATH_TC, tc.HGEMM_PATH_TC_PAIR,
+             tc.HGEMM_PATH_SKINNY]   # None: automatic choice
 
 
 @pytest.mark.parametrize("path", TMA_PATHS)
@@ -78,7 +79,8 @@ def test_8192_cube_sampled_entries_and_properties():
     assert torch.equal(dc2[normal], dc[normal] * 2)
 
 
-@pytest.mark.parametrize("path", [tc.HGEMM_PATH_TC, tc.HGEMM_PATH_TC_PAIR, tc.HGEMM_PATH_GENERIC])
+@pytest.mark.parametrize("path", [tc.HGEMM_PATH_TC, tc.HGEMM_PATH_TC_PAIR, tc.HGEMM_PATH_SKINNY,
+                                  tc.HGEMM_PATH_GENERIC])
 def test_subnormal_operands_are_honoured(path):
     """FP16 subnormal inputs keep their value (no flush to zero): each case's
     single product is exact and lands on a normal FP16 value."""
@@ -114,7 +116,8 @@ def _edge_cases(aligned):
     return sorted(set(keep) | {cases[i] for i in picked})
 
 
-@pytest.mark.parametrize("path", [tc.HGEMM_PATH_TC, tc.HGEMM_PATH_TC_PAIR])
+@pytest.mark.parametrize("path", [tc.HGEMM_PATH_TC, tc.HGEMM_PATH_TC_PAIR,
+                                  tc.HGEMM_PATH_SKINNY])
 @pytest.mark.parametrize("M,N,K", _edge_cases(aligned=True))
 def test_edges_tensor_core_paths(M, N, K, path):
     a, b = synth.operands(M, N, K, seed=M * 131 + N * 7 + K, kind="uniform")
@@ -150,7 +153,8 @@ def test_misaligned_pointers_take_the_generic_path():
     assert_close(bc[1:].cpu().numpy().reshape(M, N), ref, what="misaligned")
 
 
-@pytest.mark.parametrize("path", [tc.HGEMM_PATH_TC, tc.HGEMM_PATH_TC_PAIR, tc.HGEMM_PATH_GENERIC])
+@pytest.mark.parametrize("path", [tc.HGEMM_PATH_TC, tc.HGEMM_PATH_TC_PAIR, tc.HGEMM_PATH_SKINNY,
+                                  tc.HGEMM_PATH_GENERIC])
 def test_guard_bands_untouched(path):
     """Nothing outside C is written: C sits inside a sentinel-filled buffer."""
     torch = torch_cuda()
