@@ -127,9 +127,11 @@ HGEMM_API int hgemm_select_path(const void *A, const void *B, const void *C,
  * when the operands are not aligned for TMA. Returns HGEMM_OK or
  * HGEMM_ERR_INVALID_ARG.
  *
- * Tuning override read once per process: the environment variable
+ * Tuning overrides read once per process from the environment:
  * HGEMM_GROUP_M (a positive integer) sets how many M-tiles the tensor-core
- * kernels' grouped raster order keeps together (default 16).
+ * kernels' grouped raster order keeps together (default 12);
+ * HGEMM_TAIL_SPLIT=0 keeps whole 256×256 tiles in the last, partly filled
+ * wave of the CTA-pair kernel instead of cutting them into halves.
  */
 HGEMM_API int hgemm_force_path(int path);
 

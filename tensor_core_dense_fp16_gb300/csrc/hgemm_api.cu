@@ -38,10 +38,11 @@ struct DeviceState {
 DeviceState g_devices[kMaxDevices];
 std::mutex g_device_mu;
 
-// Nominal GB300 figures, used by hgemm_select_path before any device has
-// been used in this process: 152 SMs, 76 SM pairs, and (conservatively) as
-// many 4- and 8-CTA clusters as whole groups of SMs.
-constexpr hg::DeviceProfile kNominalProfile{152, 76, 38, 16};
+// GB300 figures, used by hgemm_select_path before any device has been used
+// in this process: 152 SMs; co-resident clusters of 2, 4, 6 and 8 CTAs of
+// ~225 KB of shared memory each, as cudaOccupancyMaxActiveClusters reports
+// them on this part.
+constexpr hg::DeviceProfile kNominalProfile{152, 76, 36, 23, 15};
 std::atomic<const hg::DeviceProfile*> g_last_profile{&kNominalProfile};
 
 int cuda_fail(cudaError_t e) {
@@ -77,6 +78,7 @@ int current_device(DeviceState** out) {
         st.prof.num_sms = sms;
         st.prof.pair_clusters = hg::pair_max_clusters(sms);
         st.prof.split2_clusters = hg::skinny_max_clusters(2, sms);
+        st.prof.split3_clusters = hg::skinny_max_clusters(3, sms);
         st.prof.split4_clusters = hg::skinny_max_clusters(4, sms);
         r = 1;
       }
@@ -137,13 +139,18 @@ int choose_tma_path(int64_t M, int64_t N, int64_t K, const DeviceProfile& dev, i
   *split = 1;
   const int64_t tiles = ((M + 2 * kTcBM - 1) / (2 * kTcBM)) * ((N + kPairBN - 1) / kPairBN);
   const int64_t num_kb = (K + kTcBK - 1) / kTcBK;
-  // split-K: 4 slices when there are K blocks for them and the 8-CTA
-  // clusters of all tiles fit on the device at once, else 2
+  // split-K: the most slices (4, 3 or 2) whose clusters all fit on the device
+  // at once, with at least one K block per slice; `need_idle` requires that
+  // the pair kernel would leave at least half of the SM pairs idle and that
+  // the split does not ask for more pairs than the device has
   auto best_split = [&](bool need_idle) -> int {
     if (need_idle && 2 * tiles > dev.pair_clusters) return 1;  // pairs already fill the GPU
-    if (num_kb >= 4 && tiles <= dev.split4_clusters && (!need_idle || 4 * tiles <= dev.pair_clusters))
-      return 4;
-    if (num_kb >= 2 && tiles <= dev.split2_clusters) return 2;
+    const int fits[5] = {0, 0, dev.split2_clusters, dev.split3_clusters, dev.split4_clusters};
+    for (int s = 4; s >= 2; --s) {
+      if (num_kb < s || tiles > fits[s]) continue;
+      if (need_idle && s * tiles > dev.pair_clusters) continue;
+      return s;
+    }
     return 1;
   };
   if (forced == HGEMM_PATH_TC || forced == HGEMM_PATH_TC_PAIR) return forced;
@@ -169,11 +176,19 @@ int choose_tma_path(int64_t M, int64_t N, int64_t K, const DeviceProfile& dev, i
 
 namespace {
 
+bool tail_split_setting() {
+  static const bool v = [] {
+    const char* e = std::getenv("HGEMM_TAIL_SPLIT");
+    return !(e && e[0] == '0');
+  }();
+  return v;
+}
+
 int group_m_setting() {
   static const int v = [] {
     const char* e = std::getenv("HGEMM_GROUP_M");
     const int x = e ? std::atoi(e) : 0;
-    return x > 0 ? x : 16;
+    return x > 0 ? x : 12;
   }();
   return v;
 }
@@ -227,6 +242,7 @@ int run_tc(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t 
   const int64_t tiles = static_cast<int64_t>(args.num_m) * args.num_n;
   if (tiles > 0x7FFFFFFF) return HGEMM_ERR_INVALID_ARG;
   args.num_tiles = static_cast<int>(tiles);
+  args.full_tiles = args.num_tiles;
   args.group_m = group_m_setting();
   args.grid = static_cast<int>(tiles < dev.num_sms ? tiles : dev.num_sms);
   args.status = dev.status;
@@ -237,10 +253,11 @@ int run_tc(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t 
 
 int run_tc_pair(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
                 const DeviceState& dev, cudaStream_t stream) {
-  CUtensorMap ma, mb, mc;
+  CUtensorMap ma, mb, mbh, mc;
   int rc;
   if ((rc = encode_map(&ma, A, M, K, hg::kTcBM, hg::kTcBK)) != HGEMM_OK) return rc;
   if ((rc = encode_map(&mb, B, N, K, hg::kPairBN / 2, hg::kTcBK)) != HGEMM_OK) return rc;
+  if ((rc = encode_map(&mbh, B, N, K, hg::kPairBN / 4, hg::kTcBK)) != HGEMM_OK) return rc;
   if ((rc = encode_map(&mc, C, M, N, hg::kEpiRows, hg::kEpiCols)) != HGEMM_OK) return rc;
   hg::TcArgs args{};
   args.M = static_cast<int>(M);
@@ -251,13 +268,19 @@ int run_tc_pair(const void* A, const void* B, void* C, int64_t M, int64_t N, int
   args.num_kb = static_cast<int>((K + hg::kTcBK - 1) / hg::kTcBK);
   const int64_t tiles = static_cast<int64_t>(args.num_m) * args.num_n;
   if (tiles > 0x3FFFFFFF) return HGEMM_ERR_INVALID_ARG;
-  args.num_tiles = static_cast<int>(tiles);
-  args.group_m = group_m_setting();
   const int64_t clusters = hg::pair_max_clusters(dev.num_sms);
-  args.grid = static_cast<int>(2 * (tiles < clusters ? tiles : clusters));
+  // Tail of the last wave: if at most half of the clusters would get a tile
+  // in it, cut those tiles into two 128-column halves.
+  const int64_t full_waves = tiles / clusters;
+  const int64_t rest = tiles - full_waves * clusters;
+  const bool halve = tail_split_setting() && full_waves > 0 && rest > 0 && 2 * rest <= clusters;
+  args.full_tiles = static_cast<int>(halve ? tiles - rest : tiles);
+  args.num_tiles = static_cast<int>(halve ? tiles + rest : tiles);
+  args.group_m = group_m_setting();
+  args.grid = static_cast<int>(2 * (args.num_tiles < clusters ? args.num_tiles : clusters));
   args.status = dev.status;
   args.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
-  cudaError_t e = hg::launch_tc_pair(ma, mb, mc, args, stream);
+  cudaError_t e = hg::launch_tc_pair(ma, mb, mbh, mc, args, stream);
   return e == cudaSuccess ? HGEMM_OK : cuda_fail(e);
 }
 
@@ -278,6 +301,7 @@ int run_skinny(const void* A, const void* B, void* C, int64_t M, int64_t N, int6
   const int64_t tiles = static_cast<int64_t>(args.num_m) * args.num_n;
   if (tiles * 2 * split > 0x7FFFFFFF) return HGEMM_ERR_INVALID_ARG;
   args.num_tiles = static_cast<int>(tiles);
+  args.full_tiles = args.num_tiles;
   args.group_m = 1;
   args.grid = static_cast<int>(tiles * 2 * split);
   args.status = dev.status;

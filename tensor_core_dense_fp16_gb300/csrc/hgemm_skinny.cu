@@ -15,12 +15,14 @@
 //     64-wide K blocks, so A is read from memory exactly once over the grid;
 //   * each CTA ends with a 128×256 FP32 partial sum in its TMEM;
 //   * the S partials of a half are reduced through distributed shared
-//     memory: the 256 columns are cut into S column ranges, the CTA of slice
-//     p owns range p, and every CTA writes its other ranges into the owners'
-//     shared memory (the operand ring, free once all MMAs finished); after a
-//     cluster barrier each owner adds the S partials in slice order (so the
-//     result does not depend on timing), rounds to FP16 and TMA-stores its
-//     128-row × (256/S)-column block of C.
+//     memory: the 256 columns are cut into S ranges of whole 64-column
+//     units, the CTA of slice p owns range p. After a cluster barrier (every
+//     pair's MMAs done, so every operand ring is free), each epilogue warp
+//     stages its 32 rows of every foreign range in its own shared memory and
+//     pushes them with one bulk copy per owner into the owner's ring; the
+//     owner's barrier counts the bytes. Each owner then adds the S partials in
+//     slice order (so the result does not depend on timing), rounds to FP16
+//     and TMA-stores its 128-row block of C.
 // No global scratch memory is used.
 #include <cuda_fp16.h>
 
@@ -32,6 +34,9 @@ namespace hg {
 namespace {
 
 constexpr int kSkStages = 6;
+
+// Column range of K-slice p, in 64-column units of the 256-column tile.
+__host__ __device__ constexpr int owned_unit(int p, int split) { return (4 * p) / split; }
 
 template <int SPLIT>
 struct SkCfg {
@@ -46,26 +51,39 @@ struct SkCfg {
   static constexpr int B_BYTES = BROWS * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int TX_BYTES = 2 * STAGE_BYTES;
-  static constexpr int OWN_COLS = BN / SPLIT;                 // columns reduced per CTA
-  static constexpr int SLOT_BYTES = ROWS * OWN_COLS * 4;      // one FP32 partial block
-  static constexpr int RECV_BYTES = SPLIT * SLOT_BYTES;       // slot p from slice p
+  static constexpr int RING_BYTES = STAGES * STAGE_BYTES;     // reused for the reduction
+  static constexpr int MAX_OWN_COLS = 64 * (owned_unit(SPLIT, SPLIT) - owned_unit(SPLIT - 1, SPLIT));
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
   static constexpr int OFF_C = OFF_B + STAGES * B_BYTES;     // FP16 staging of C
-  static constexpr int C_WARP_BYTES = kEpiRows * OWN_COLS * 2;
-  static constexpr int C_BYTES = 4 * ((C_WARP_BYTES + 1023) / 1024) * 1024;
+  static constexpr int C_WARP_BYTES = kEpiRows * MAX_OWN_COLS * 2;
+  static constexpr int C_BYTES = 4 * C_WARP_BYTES;
   static constexpr int OFF_BAR = OFF_C + C_BYTES;
-  static constexpr int NUM_BARS = 2 * STAGES + 2;  // full, empty, accumulator full, drain
+  // full, empty, accumulator full, drain, partials received
+  static constexpr int NUM_BARS = 2 * STAGES + 3;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
   static constexpr int THREADS = 192;
   static constexpr int TMEM_COLS = BN;
   static constexpr uint32_t IDESC = idesc_f16_f32acc(BM, BN);
 
-  static_assert(RECV_BYTES <= OFF_C, "receive slots reuse the operand ring");
-  static_assert(OWN_COLS % 32 == 0, "column ranges are whole 32-column TMEM loads");
+  // bytes a CTA owning `cols` columns receives (S-1 blocks) plus sends
+  // (its partial outside its range), FP32, 128 rows
+  static constexpr int exchange_bytes(int cols) {
+    return (SPLIT - 1) * ROWS * cols * 4 + ROWS * (BN - cols) * 4;
+  }
+  static_assert(exchange_bytes(MAX_OWN_COLS) <= RING_BYTES, "reduction fits in the ring");
+  static_assert(exchange_bytes(64) <= RING_BYTES, "reduction fits in the ring");
   static_assert(SMEM_BYTES <= 232448, "exceeds 227 KB of shared memory per CTA");
+  static_assert(C_WARP_BYTES % 1024 == 0, "staging boxes stay 1024-byte aligned");
 };
+
+// Swizzled FP32 block of `cols` columns: row r occupies cols*4 bytes at
+// r*cols*4, and its 16-byte chunk c sits at chunk position c ^ (r % 8), so
+// the 32 rows written by a warp at once spread over all banks.
+__device__ __forceinline__ uint32_t f32_block_offset(int r, int c, int cols) {
+  return static_cast<uint32_t>(r * cols * 4 + ((c ^ (r & 7)) << 4));
+}
 
 template <int SPLIT>
 __global__ void __launch_bounds__(192, 1)
@@ -81,6 +99,7 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t bar0 = sbase + Cfg::OFF_BAR;
   const uint32_t accf_bar = bar0 + 8u * (2 * Cfg::STAGES);
   const uint32_t drain_bar = accf_bar + 8u;
+  const uint32_t recv_bar = drain_bar + 8u;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::OFF_MISC + 4);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
@@ -98,6 +117,8 @@ __global__ void __launch_bounds__(192, 1)
   const int nb = tile % p.num_n;
   const int kb0 = static_cast<int>(static_cast<long long>(p.num_kb) * slice / SPLIT);
   const int kb1 = static_cast<int>(static_cast<long long>(p.num_kb) * (slice + 1) / SPLIT);
+  const int own_c0 = 64 * owned_unit(slice, SPLIT);  // this CTA's column range
+  const int own_cols = 64 * owned_unit(slice + 1, SPLIT) - own_c0;
   const Watchdog wd{abort_flag, p.status, p.timeout_ns};
 
   if (threadIdx.x == 0) {
@@ -107,6 +128,9 @@ __global__ void __launch_bounds__(192, 1)
     }
     mbar_init(accf_bar, 1);
     mbar_init(drain_bar, 1);
+    mbar_init(recv_bar, 1);
+    // the partials of the other slices for this CTA's range, from 4 warps each
+    mbar_arrive_expect_tx(recv_bar, static_cast<uint32_t>((SPLIT - 1) * Cfg::ROWS * own_cols * 4));
     *abort_flag = 0;
     fence_barrier_init();
     prefetch_tensormap(&tmA);
@@ -195,106 +219,118 @@ __global__ void __launch_bounds__(192, 1)
     tc_fence_after_sync();
   }
 
-  // 1: every pair's MMAs are done, so every CTA's operand ring is free
+  // every pair's MMAs are done, so every CTA's operand ring is free
   cluster_sync();
 
   const int q = warp & 3;  // TMEM lanes / tile rows 32q .. 32q+31 of this CTA
   const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
   const int row = q * 32 + lane;
+  // ring layout for the exchange: receive slots first, then send staging
+  const uint32_t recv_base = sbase;
+  const uint32_t send_base = sbase + static_cast<uint32_t>((SPLIT - 1) * Cfg::ROWS * own_cols * 4);
   if (warp >= 2 && ok) {
-    // send the column ranges owned by the other slices to their owners
+    uint32_t send_off = send_base;
     for (int j = 0; j < SPLIT; ++j) {
       if (j == slice) continue;
-      const uint32_t dst_rank = static_cast<uint32_t>(2 * j + half);
-      const uint32_t slot = mapa_shared(sbase + slice * Cfg::SLOT_BYTES, dst_rank);
+      const int c0 = 64 * owned_unit(j, SPLIT);
+      const int cols = 64 * owned_unit(j + 1, SPLIT) - c0;
+      uint8_t* blk = smem + (send_off - sbase);
 #pragma unroll 1
-      for (int c32 = 0; c32 < Cfg::OWN_COLS / 32; ++c32) {
+      for (int c32 = 0; c32 < cols / 32; ++c32) {
         uint32_t v[32];
-        tmem_ld_32x32b_x32(t_row + j * Cfg::OWN_COLS + c32 * 32, v);
+        tmem_ld_32x32b_x32(t_row + c0 + c32 * 32, v);
         tmem_ld_wait(v);
-        // row-major FP32 rows of OWN_COLS; 16-byte chunks XOR-swizzled by row
-        // so that the 32 rows of a warp spread over the banks
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int chunk = c32 * 8 + u;
-          const int pos = chunk ^ (row & (Cfg::OWN_COLS / 4 - 1) & 15);
-          st_cluster_v4(slot + row * (Cfg::OWN_COLS * 4) + pos * 16, v[4 * u], v[4 * u + 1],
-                        v[4 * u + 2], v[4 * u + 3]);
-        }
+        for (int u = 0; u < 8; ++u)
+          *reinterpret_cast<uint4*>(blk + f32_block_offset(row, c32 * 8 + u, cols)) =
+              make_uint4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
       }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        // this warp's 32 rows, into slot `slice` (counted among j's senders)
+        const uint32_t dst_rank = static_cast<uint32_t>(2 * j + half);
+        const int idx = slice < j ? slice : slice - 1;
+        const uint32_t rows_off = static_cast<uint32_t>(q * 32 * cols * 4);
+        const uint32_t dst = mapa_shared(recv_base + idx * Cfg::ROWS * cols * 4 + rows_off, dst_rank);
+        bulk_copy_to_cluster(dst, send_off + rows_off, static_cast<uint32_t>(32 * cols * 4),
+                             mapa_shared(recv_bar, dst_rank));
+      }
+      send_off += static_cast<uint32_t>(Cfg::ROWS * cols * 4);
     }
-  }
 
-  // 2: every partial has been delivered
-  cluster_sync();
-
-  if (warp >= 2 && ok) {
-    const int x0 = nb * Cfg::BN + slice * Cfg::OWN_COLS;
-    const int y0 = mb * Cfg::BM + half * Cfg::ROWS + q * kEpiRows;
-    uint8_t* cbuf = smem + Cfg::OFF_C + q * (Cfg::C_BYTES / 4);
+    // own range: wait for the other slices' blocks, add in slice order
+    int got = 1;
+    if (lane == 0) got = wait_phase_cluster(recv_bar, 0, wd, kWdReduce) ? 1 : 0;
+    got = __shfl_sync(0xffffffffu, got, 0);
+    if (got) {
+      const int x0 = nb * Cfg::BN + own_c0;
+      const int y0 = mb * Cfg::BM + half * Cfg::ROWS + q * kEpiRows;
+      uint8_t* cbuf = smem + Cfg::OFF_C + q * Cfg::C_WARP_BYTES;
 #pragma unroll 1
-    for (int c32 = 0; c32 < Cfg::OWN_COLS / 32; ++c32) {
-      uint32_t own[32];
-      tmem_ld_32x32b_x32(t_row + slice * Cfg::OWN_COLS + c32 * 32, own);
-      tmem_ld_wait(own);
-      float acc[32];
+      for (int c32 = 0; c32 < own_cols / 32; ++c32) {
+        uint32_t own[32];
+        tmem_ld_32x32b_x32(t_row + own_c0 + c32 * 32, own);
+        tmem_ld_wait(own);
+        float acc[32];
+        for (int sl = 0; sl < SPLIT; ++sl) {
+          if (sl == slice) {
 #pragma unroll
-      for (int i = 0; i < 32; ++i) acc[i] = 0.f;
-      // add the slices in order 0, 1, ..., SPLIT-1 (slice 0 first, exactly)
-      for (int sl = 0; sl < SPLIT; ++sl) {
-        if (sl == slice) {
+            for (int i = 0; i < 32; ++i)
+              acc[i] = (sl == 0) ? __uint_as_float(own[i]) : acc[i] + __uint_as_float(own[i]);
+          } else {
+            const int idx = sl < slice ? sl : sl - 1;
+            const uint8_t* blk = smem + idx * Cfg::ROWS * own_cols * 4;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) acc[i] = (sl == 0) ? __uint_as_float(own[i]) : acc[i] + __uint_as_float(own[i]);
-        } else {
-          const uint8_t* src = smem + sl * Cfg::SLOT_BYTES + row * (Cfg::OWN_COLS * 4);
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const int chunk = c32 * 8 + u;
-            const int pos = chunk ^ (row & (Cfg::OWN_COLS / 4 - 1) & 15);
-            const float4 f = *reinterpret_cast<const float4*>(src + pos * 16);
-            if (sl == 0) {
-              acc[4 * u] = f.x;
-              acc[4 * u + 1] = f.y;
-              acc[4 * u + 2] = f.z;
-              acc[4 * u + 3] = f.w;
-            } else {
-              acc[4 * u] += f.x;
-              acc[4 * u + 1] += f.y;
-              acc[4 * u + 2] += f.z;
-              acc[4 * u + 3] += f.w;
+            for (int u = 0; u < 8; ++u) {
+              const float4 f =
+                  *reinterpret_cast<const float4*>(blk + f32_block_offset(row, c32 * 8 + u, own_cols));
+              if (sl == 0) {
+                acc[4 * u] = f.x;
+                acc[4 * u + 1] = f.y;
+                acc[4 * u + 2] = f.z;
+                acc[4 * u + 3] = f.w;
+              } else {
+                acc[4 * u] += f.x;
+                acc[4 * u + 1] += f.y;
+                acc[4 * u + 2] += f.z;
+                acc[4 * u + 3] += f.w;
+              }
             }
           }
         }
-      }
-      // FP16 row segment (64 bytes) into the 128-byte-swizzled staging box
-      // (rows of OWN_COLS*2 bytes; a 64-column range is one 128-byte row)
+        // 32 FP16 columns (64 bytes) into the 128-byte-swizzled staging box
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        uint4 pk;
-        pk.x = pack_half2(__float_as_uint(acc[8 * u]), __float_as_uint(acc[8 * u + 1]));
-        pk.y = pack_half2(__float_as_uint(acc[8 * u + 2]), __float_as_uint(acc[8 * u + 3]));
-        pk.z = pack_half2(__float_as_uint(acc[8 * u + 4]), __float_as_uint(acc[8 * u + 5]));
-        pk.w = pack_half2(__float_as_uint(acc[8 * u + 6]), __float_as_uint(acc[8 * u + 7]));
-        const int chunk = c32 * 4 + u;  // 16-byte chunk within the row
-        const int box = chunk >> 3;     // 64-column box
-        const int cin = chunk & 7;
-        *reinterpret_cast<uint4*>(cbuf + box * (kEpiRows * 128) + lane * 128 +
-                                  ((cin ^ (lane & 7)) << 4)) = pk;
+        for (int u = 0; u < 4; ++u) {
+          uint4 pk;
+          pk.x = pack_half2(__float_as_uint(acc[8 * u]), __float_as_uint(acc[8 * u + 1]));
+          pk.y = pack_half2(__float_as_uint(acc[8 * u + 2]), __float_as_uint(acc[8 * u + 3]));
+          pk.z = pack_half2(__float_as_uint(acc[8 * u + 4]), __float_as_uint(acc[8 * u + 5]));
+          pk.w = pack_half2(__float_as_uint(acc[8 * u + 6]), __float_as_uint(acc[8 * u + 7]));
+          const int chunk = c32 * 4 + u;  // 16-byte chunk within the row
+          const int box = chunk >> 3;     // 64-column box
+          const int cin = chunk & 7;
+          *reinterpret_cast<uint4*>(cbuf + box * (kEpiRows * 128) + lane * 128 +
+                                    ((cin ^ (lane & 7)) << 4)) = pk;
+        }
       }
-    }
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0 && y0 < p.M) {
-      for (int box = 0; box < Cfg::OWN_COLS / kEpiCols; ++box) {
-        const int x = x0 + box * kEpiCols;
-        if (x < p.N) tma_store_2d(&tmC, smem_u32(cbuf + box * (kEpiRows * 128)), x, y0);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0 && y0 < p.M) {
+        for (int box = 0; box < own_cols / kEpiCols; ++box) {
+          const int x = x0 + box * kEpiCols;
+          if (x < p.N) tma_store_2d(&tmC, smem_u32(cbuf + box * (kEpiRows * 128)), x, y0);
+        }
+        bulk_commit_group();
+        bulk_wait_group<0>();
       }
-      bulk_commit_group();
-      bulk_wait_group<0>();
+      __syncwarp();
     }
-    __syncwarp();
   }
 
+  // No CTA leaves while a copy into or out of its shared memory may be in
+  // flight (every owner has received all its bytes before it gets here), and
+  // neither CTA of a pair frees TMEM before the other is done with it.
   tc_fence_before_sync();
   cluster_sync();
   tc_fence_after_sync();
@@ -360,6 +396,8 @@ int skinny_max_clusters(int split, int num_sms) {
   switch (split) {
     case 2:
       return max_clusters_split<2>(num_sms);
+    case 3:
+      return max_clusters_split<3>(num_sms);
     case 4:
       return max_clusters_split<4>(num_sms);
     default:
@@ -372,6 +410,8 @@ cudaError_t launch_skinny(int split, const CUtensorMap& a, const CUtensorMap& b,
   switch (split) {
     case 2:
       return launch_split<2>(a, b, c, args, stream);
+    case 3:
+      return launch_split<3>(a, b, c, args, stream);
     case 4:
       return launch_split<4>(a, b, c, args, stream);
     default:

@@ -20,6 +20,10 @@
 //     clipped TMA stores).
 // Per SM, a stage is 32 KB instead of 48 KB for the same MMA work, which
 // allows six stages in flight and halves each SM's share of B traffic.
+//
+// Wave tail: when the tiles do not fill the last wave of clusters, the tiles
+// of that wave are cut into two 256×128 halves (N=128 pair MMAs) so that
+// twice as many clusters share them and the tail lasts half a tile.
 #include <cuda_fp16.h>
 
 #include "internal.h"
@@ -57,16 +61,41 @@ struct PairCfg {
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
   static constexpr int THREADS = 192;
   static constexpr uint32_t IDESC = idesc_f16_f32acc(BM, BN);
+  static constexpr uint32_t IDESC_HALF = idesc_f16_f32acc(BM, BN / 2);
+  static constexpr int TX_BYTES_HALF = 2 * (A_BYTES + B_BYTES / 2);
 
   static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "1024-byte aligned stages");
   static_assert(TMEM_COLS == 512, "two 256-column FP32 accumulators");
   static_assert(SMEM_BYTES <= 232448, "exceeds 227 KB of shared memory per CTA");
 };
 
+// Work unit t: a whole 256×256 tile below p.full_tiles, else one 128-column
+// half of a tile (two consecutive units per tile), in raster order.
+struct PairTile {
+  int mb, nb;
+  int n0;     // first column of C
+  int ncols;  // 256 or 128
+};
+
+__device__ __forceinline__ PairTile pair_tile(int t, const TcArgs& p) {
+  PairTile w;
+  int whole = t, half = -1;
+  if (t >= p.full_tiles) {
+    const int h = t - p.full_tiles;
+    whole = p.full_tiles + (h >> 1);
+    half = h & 1;
+  }
+  tile_coords(whole, p.num_m, p.num_n, p.group_m, w.mb, w.nb);
+  w.n0 = w.nb * kPairBN + (half < 0 ? 0 : half * (kPairBN / 2));
+  w.ncols = half < 0 ? kPairBN : kPairBN / 2;
+  return w;
+}
+
 template <int STAGES>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     hgemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                     const __grid_constant__ CUtensorMap tmC, const TcArgs p) {
+                     const __grid_constant__ CUtensorMap tmBh, const __grid_constant__ CUtensorMap tmC,
+                     const TcArgs p) {
   using Cfg = PairCfg<STAGES>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -105,6 +134,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     fence_barrier_init();
     prefetch_tensormap(&tmA);
     prefetch_tensormap(&tmB);
+    prefetch_tensormap(&tmBh);
     prefetch_tensormap(&tmC);
   }
   if (warp == 1) {
@@ -126,19 +156,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
       long long issued = 0;
       bool ok = true;
       for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters) {
-        int mb, nb;
-        tile_coords(t, p.num_m, p.num_n, p.group_m, mb, nb);
-        const int ya = mb * Cfg::BM + static_cast<int>(rank) * Cfg::ROWS;
-        const int yb = nb * Cfg::BN + static_cast<int>(rank) * Cfg::BROWS;
+        const PairTile w = pair_tile(t, p);
+        const bool whole = w.ncols == Cfg::BN;
+        const int ya = w.mb * Cfg::BM + static_cast<int>(rank) * Cfg::ROWS;
+        const int yb = w.n0 + static_cast<int>(rank) * (w.ncols / 2);
+        const CUtensorMap* mapb = whole ? &tmB : &tmBh;
+        const uint32_t tx = whole ? Cfg::TX_BYTES : Cfg::TX_BYTES_HALF;
         for (int kb = 0; kb < p.num_kb; ++kb) {
           if (!wait_phase_cluster(empty_bar(stage), phase ^ 1u, wd, kWdProducerEmpty)) {
             ok = false;
             break;
           }
           const uint32_t fb = mapa_shared(full_bar(stage), 0);
-          if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), Cfg::TX_BYTES);
+          if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), tx);
           tma_load_2d_cg2(sA + stage * Cfg::A_BYTES, &tmA, fb, kb * Cfg::BK, ya);
-          tma_load_2d_cg2(sB + stage * Cfg::B_BYTES, &tmB, fb, kb * Cfg::BK, yb);
+          tma_load_2d_cg2(sB + stage * Cfg::B_BYTES, mapb, fb, kb * Cfg::BK, yb);
           ++issued;
           if (++stage == STAGES) {
             stage = 0;
@@ -175,6 +207,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
       uint32_t acc_phase = 0;
       bool ok = true;
       for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters) {
+        const uint32_t idesc = t < p.full_tiles ? Cfg::IDESC : Cfg::IDESC_HALF;
         if (!wait_phase_cluster(acce_bar(acc), acc_phase ^ 1u, wd, kWdMmaAccEmpty)) {
           ok = false;
           break;
@@ -191,7 +224,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
           const uint64_t b_desc = sdesc_kmajor_sw128(sB + stage * Cfg::B_BYTES);
 #pragma unroll
           for (int k = 0; k < Cfg::BK / Cfg::UMMA_K; ++k)
-            mma_f16_ss_cg2(d_tmem, a_desc + 2u * k, b_desc + 2u * k, Cfg::IDESC,
+            mma_f16_ss_cg2(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc,
                            (kb > 0 || k > 0) ? 1u : 0u);
           mma_commit_cg2_multicast(empty_bar(stage), 0x3);  // frees the stage in both CTAs
           if (++stage == STAGES) {
@@ -216,8 +249,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     uint32_t acc_phase = 0;
     int cb = 0;
     for (int t = cluster_id; t < p.num_tiles; t += num_clusters) {
-      int mb, nb;
-      tile_coords(t, p.num_m, p.num_n, p.group_m, mb, nb);
+      const PairTile w = pair_tile(t, p);
+      const int chunks = w.ncols / kEpiCols;
       int ok = 1;
       if (lane == 0)
         ok = wait_phase_cluster(accf_bar(acc), acc_phase, wd, kWdEpiAccFull) ? 1 : 0;
@@ -226,20 +259,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
       tc_fence_after_sync();
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                              static_cast<uint32_t>(acc * Cfg::ACC_COLS);
-      const int y0 = mb * Cfg::BM + static_cast<int>(rank) * Cfg::ROWS + q * kEpiRows;
+      const int y0 = w.mb * Cfg::BM + static_cast<int>(rank) * Cfg::ROWS + q * kEpiRows;
 #pragma unroll 1
-      for (int c = 0; c < Cfg::BN / kEpiCols; ++c) {
+      for (int c = 0; c < chunks; ++c) {
         uint32_t v0[32], v1[32];
         tmem_ld_32x32b_x32(t_row + c * kEpiCols, v0);
         tmem_ld_32x32b_x32(t_row + c * kEpiCols + 32, v1);
         tmem_ld_wait(v0);
         tmem_ld_wait(v1);
-        if (c == Cfg::BN / kEpiCols - 1) {
+        if (c == chunks - 1) {
           tc_fence_before_sync();
           __syncwarp();
           if (lane == 0) mbar_arrive_cluster(mapa_shared(acce_bar(acc), 0));
         }
-        const int x0 = nb * Cfg::BN + c * kEpiCols;
+        const int x0 = w.n0 + c * kEpiCols;
         if (x0 >= p.N || y0 >= p.M) continue;
         if (lane == 0) bulk_wait_group_read<1>();
         __syncwarp();
@@ -303,8 +336,8 @@ int pair_max_clusters(int num_sms) {
   return n;
 }
 
-cudaError_t launch_tc_pair(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
-                           const TcArgs& args, cudaStream_t stream) {
+cudaError_t launch_tc_pair(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b_half,
+                           const CUtensorMap& c, const TcArgs& args, cudaStream_t stream) {
   using Cfg = PairCfg<kPairStages>;
   static bool attr_done[64] = {};
   auto kern = hgemm_tc2_kernel<kPairStages>;
@@ -321,7 +354,7 @@ cudaError_t launch_tc_pair(const CUtensorMap& a, const CUtensorMap& b, const CUt
   cfg.blockDim = dim3(Cfg::THREADS);
   cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
   cfg.stream = stream;
-  return cudaLaunchKernelEx(&cfg, kern, a, b, c, args);
+  return cudaLaunchKernelEx(&cfg, kern, a, b, b_half, c, args);
 }
 
 }  // namespace hg

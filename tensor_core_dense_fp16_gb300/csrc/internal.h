@@ -17,13 +17,16 @@ enum WatchdogCode : int {
   kWdMmaAccEmpty = 3,     // MMA issuer waiting for the epilogue to free TMEM
   kWdEpiAccFull = 4,      // epilogue waiting for a finished accumulator
   kWdDrain = 5,           // end-of-kernel drain of in-flight copies or MMAs
+  kWdReduce = 6,          // split-K owner waiting for the other slices' partials
 };
 
 // Everything a tensor-core launch needs besides the tensor maps.
 struct TcArgs {
   int M, N, K;
   int num_m, num_n, num_kb;  // tiles along M and N, 64-wide K blocks
-  int num_tiles;
+  int num_tiles;             // work units: full tiles, then half tiles
+  int full_tiles;            // units below this index are whole tiles; the rest are
+                             // 128-column halves of the last tiles (pair kernel)
   int group_m;               // rasterisation group height (in M tiles)
   int grid;                  // persistent CTAs
   int* status;               // device watchdog word
@@ -44,11 +47,12 @@ struct PlainArgs {
 // error, if any). Shared-memory attributes are set on first use per device.
 cudaError_t launch_tc_128x256(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
                               const TcArgs& args, cudaStream_t stream);
-cudaError_t launch_tc_pair(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
-                           const TcArgs& args, cudaStream_t stream);
+// b_half: the B map with 64-row boxes, for the half tiles of the last wave.
+cudaError_t launch_tc_pair(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b_half,
+                           const CUtensorMap& c, const TcArgs& args, cudaStream_t stream);
 // Largest number of co-resident 2-CTA clusters of the pair kernel.
 int pair_max_clusters(int num_sms);
-// Split-K cluster kernel for few output tiles: `split` K-slices (2 or 4),
+// Split-K cluster kernel for few output tiles: `split` K-slices (2, 3 or 4),
 // one cluster of 2*split CTAs per 256×256 tile (args.num_tiles of them).
 cudaError_t launch_skinny(int split, const CUtensorMap& a, const CUtensorMap& b,
                           const CUtensorMap& c, const TcArgs& args, cudaStream_t stream);
@@ -66,7 +70,8 @@ struct DeviceProfile {
   int num_sms;
   int pair_clusters;    // co-resident 2-CTA clusters of the pair kernel
   int split2_clusters;  // co-resident 4-CTA clusters of the split-K kernel
-  int split4_clusters;  // co-resident 8-CTA clusters of the split-K kernel
+  int split3_clusters;  // co-resident 6-CTA clusters
+  int split4_clusters;  // co-resident 8-CTA clusters
 };
 
 // Kernel choice for a TMA-able product. Returns an HGEMM_PATH_* value and,

@@ -97,6 +97,15 @@ def test_subnormal_operands_are_honoured(path):
         assert float(got[3, 7]) == x * y + 0.5
 
 
+@pytest.mark.parametrize("M,N,K", [(2600, 2040, 136), (2560, 2048, 64), (8192, 1024, 72)])
+def test_pair_kernel_last_wave_halves(M, N, K):
+    """More 256x256 tiles than one wave of CTA pairs, with a short last wave:
+    the last wave's tiles run as 128-column halves."""
+    a, b = synth.operands(M, N, K, seed=M + N + K, kind="uniform")
+    ref = oracle.hgemm(a, b, nthreads=oracle_threads())
+    assert_close(run_gpu(a, b, path=tc.HGEMM_PATH_TC_PAIR), ref, what=f"pair tail {M}x{N}x{K}")
+
+
 EDGE = [1, 7, 8, 15, 16, 17, 127, 128, 129, 1000, 1001]
 
 
