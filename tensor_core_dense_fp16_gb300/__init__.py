@@ -23,7 +23,8 @@ import os
 __all__ = [
     "HGEMM_OK", "HGEMM_ERR_INVALID_ARG", "HGEMM_ERR_ALIAS", "HGEMM_ERR_UNSUPPORTED_DEVICE",
     "HGEMM_ERR_CUDA", "HGEMM_ERR_TIMEOUT", "HGEMM_PATH_NONE", "HGEMM_PATH_ZERO",
-    "HGEMM_PATH_TC", "HGEMM_PATH_SKINNY", "HGEMM_PATH_GENERIC", "HGEMM_PATH_TC_PAIR", "HGEMM_MAX_DIM",
+    "HGEMM_PATH_TC", "HGEMM_PATH_SKINNY", "HGEMM_PATH_GENERIC", "HGEMM_PATH_TC_PAIR",
+    "HGEMM_PATH_TC_WIDE", "HGEMM_MAX_DIM",
     "HgemmError", "library_path", "load", "hgemm", "hgemm_host", "hgemm_select_path",
     "hgemm_force_path", "hgemm_device_status", "hgemm_last_cuda_error",
     "hgemm_status_string", "hgemm_version", "matmul",
@@ -42,6 +43,7 @@ HGEMM_PATH_TC = 2
 HGEMM_PATH_SKINNY = 3
 HGEMM_PATH_GENERIC = 4
 HGEMM_PATH_TC_PAIR = 5
+HGEMM_PATH_TC_WIDE = 6
 
 HGEMM_MAX_DIM = 0x7FFFFFFF
 

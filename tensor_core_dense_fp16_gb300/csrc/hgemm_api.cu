@@ -153,7 +153,8 @@ int choose_tma_path(int64_t M, int64_t N, int64_t K, const DeviceProfile& dev, i
     }
     return 1;
   };
-  if (forced == HGEMM_PATH_TC || forced == HGEMM_PATH_TC_PAIR) return forced;
+  if (forced == HGEMM_PATH_TC || forced == HGEMM_PATH_TC_PAIR || forced == HGEMM_PATH_TC_WIDE)
+    return forced;
   if (forced == HGEMM_PATH_SKINNY) {
     const int s = best_split(false);
     if (s > 1) {
@@ -284,6 +285,33 @@ int run_tc_pair(const void* A, const void* B, void* C, int64_t M, int64_t N, int
   return e == cudaSuccess ? HGEMM_OK : cuda_fail(e);
 }
 
+int run_tc_wide(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                const DeviceState& dev, cudaStream_t stream) {
+  CUtensorMap ma, mb, mc;
+  int rc;
+  if ((rc = encode_map(&ma, A, M, K, hg::kTcBM, hg::kTcBK)) != HGEMM_OK) return rc;
+  if ((rc = encode_map(&mb, B, N, K, hg::kPairBN / 2, hg::kTcBK)) != HGEMM_OK) return rc;
+  if ((rc = encode_map(&mc, C, M, N, hg::kEpiRows, hg::kEpiCols)) != HGEMM_OK) return rc;
+  hg::TcArgs args{};
+  args.M = static_cast<int>(M);
+  args.N = static_cast<int>(N);
+  args.K = static_cast<int>(K);
+  args.num_m = static_cast<int>((M + 2 * hg::kTcBM - 1) / (2 * hg::kTcBM));
+  args.num_n = static_cast<int>((N + 2 * hg::kPairBN - 1) / (2 * hg::kPairBN));
+  args.num_kb = static_cast<int>((K + hg::kTcBK - 1) / hg::kTcBK);
+  const int64_t tiles = static_cast<int64_t>(args.num_m) * args.num_n;
+  if (tiles > 0x3FFFFFFF) return HGEMM_ERR_INVALID_ARG;
+  args.num_tiles = static_cast<int>(tiles);
+  args.full_tiles = args.num_tiles;
+  args.group_m = group_m_setting();
+  const int64_t clusters = hg::wide_max_clusters(dev.num_sms);
+  args.grid = static_cast<int>(2 * (tiles < clusters ? tiles : clusters));
+  args.status = dev.status;
+  args.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
+  cudaError_t e = hg::launch_tc_wide(ma, mb, mc, args, stream);
+  return e == cudaSuccess ? HGEMM_OK : cuda_fail(e);
+}
+
 int run_skinny(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int split,
                const DeviceState& dev, cudaStream_t stream) {
   CUtensorMap ma, mb, mc;
@@ -324,6 +352,8 @@ int dispatch(const hgemm_half_t* A, const hgemm_half_t* B, hgemm_half_t* C, int6
       return run_tc(A, B, C, M, N, K, dev, stream);
     case HGEMM_PATH_TC_PAIR:
       return run_tc_pair(A, B, C, M, N, K, dev, stream);
+    case HGEMM_PATH_TC_WIDE:
+      return run_tc_wide(A, B, C, M, N, K, dev, stream);
     case HGEMM_PATH_SKINNY:
       return run_skinny(A, B, C, M, N, K, split, dev, stream);
     default: {
@@ -380,7 +410,7 @@ int hgemm_select_path(const void* A, const void* B, const void* C, int64_t M, in
 
 int hgemm_force_path(int path) {
   if (path != -1 && path != HGEMM_PATH_TC && path != HGEMM_PATH_TC_PAIR &&
-      path != HGEMM_PATH_SKINNY && path != HGEMM_PATH_GENERIC)
+      path != HGEMM_PATH_TC_WIDE && path != HGEMM_PATH_SKINNY && path != HGEMM_PATH_GENERIC)
     return HGEMM_ERR_INVALID_ARG;
   g_forced_path.store(path);
   return HGEMM_OK;

@@ -156,7 +156,7 @@ __global__ void __launch_bounds__(192, 1)
       const int ya = mb * Cfg::BM + half * Cfg::ROWS;
       const int yb = nb * Cfg::BN + half * Cfg::BROWS;
       for (int kb = kb0; kb < kb1; ++kb) {
-        if (!wait_phase_cluster(empty_bar(stage), phase ^ 1u, wd, kWdProducerEmpty)) break;
+        if (!wait_phase(empty_bar(stage), phase ^ 1u, wd, kWdProducerEmpty)) break;
         const uint32_t fb = mapa_shared(full_bar(stage), leader);
         if (rank == leader) mbar_arrive_expect_tx(full_bar(stage), Cfg::TX_BYTES);
         tma_load_2d_cg2(sA + stage * Cfg::A_BYTES, &tmA, fb, kb * Cfg::BK, ya);
@@ -190,7 +190,7 @@ __global__ void __launch_bounds__(192, 1)
       uint32_t phase = 0;
       bool good = true;
       for (int kb = kb0; kb < kb1; ++kb) {
-        if (!wait_phase_cluster(full_bar(stage), phase, wd, kWdMmaFull)) {
+        if (!wait_phase(full_bar(stage), phase, wd, kWdMmaFull)) {
           good = false;
           break;
         }
@@ -214,7 +214,7 @@ __global__ void __launch_bounds__(192, 1)
     __syncwarp();
   } else {
     // epilogue warps: this CTA's partial is complete once the pair's MMAs are
-    if (lane == 0) ok = wait_phase_cluster(accf_bar, 0, wd, kWdEpiAccFull) ? 1 : 0;
+    if (lane == 0) ok = wait_phase(accf_bar, 0, wd, kWdEpiAccFull) ? 1 : 0;
     ok = __shfl_sync(0xffffffffu, ok, 0);
     tc_fence_after_sync();
   }

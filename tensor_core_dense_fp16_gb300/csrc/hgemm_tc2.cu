@@ -163,7 +163,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
         const CUtensorMap* mapb = whole ? &tmB : &tmBh;
         const uint32_t tx = whole ? Cfg::TX_BYTES : Cfg::TX_BYTES_HALF;
         for (int kb = 0; kb < p.num_kb; ++kb) {
-          if (!wait_phase_cluster(empty_bar(stage), phase ^ 1u, wd, kWdProducerEmpty)) {
+          if (!wait_phase(empty_bar(stage), phase ^ 1u, wd, kWdProducerEmpty)) {
             ok = false;
             break;
           }
@@ -215,7 +215,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * Cfg::ACC_COLS);
         for (int kb = 0; kb < p.num_kb; ++kb) {
-          if (!wait_phase_cluster(full_bar(stage), phase, wd, kWdMmaFull)) {
+          if (!wait_phase(full_bar(stage), phase, wd, kWdMmaFull)) {
             ok = false;
             break;
           }
@@ -253,7 +253,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
       const int chunks = w.ncols / kEpiCols;
       int ok = 1;
       if (lane == 0)
-        ok = wait_phase_cluster(accf_bar(acc), acc_phase, wd, kWdEpiAccFull) ? 1 : 0;
+        ok = wait_phase(accf_bar(acc), acc_phase, wd, kWdEpiAccFull) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       tc_fence_after_sync();

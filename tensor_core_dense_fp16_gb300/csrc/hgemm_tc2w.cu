@@ -1,0 +1,329 @@
+// hgemm_tc2w.cu — the wide CTA-pair path of C = A·B on sm_103a: 256×512
+// output tiles per pair of CTAs.
+//
+// Same contract as the other tensor-core paths (the HGEMM of "Nvidia Tensor
+// Core-MMA PTX编程入门", §4 示例; FP32 accumulation per "GPU架构与CUDA",
+// 混合精度核函数; zero-filled edges and clipped stores per "GPU架构与CUDA",
+// 共享内存与分块).
+//
+// Why wider tiles: at 256×256 per pair the main loop is limited by the
+// aggregate bandwidth from L2 to the SMs, not by the tensor cores (each SM
+// needs 32 KB of operands per 64-wide K block for 2·128·256·64 flops). With
+// 512 columns per pair, each SM loads 128 rows of A and 256 rows of B per K
+// block (48 KB) for twice the MMA work: 25% fewer operand bytes per flop,
+// without giving up any SM (clusters stay at two CTAs).
+//
+// Layout of the work:
+//   * CTA r of a pair loads A rows [128r, 128r+128) of the tile and, for each
+//     256-column half h of the tile, B rows [256h + 128r, 256h + 128r + 128)
+//     (B stored N×K), into a 4-deep ring of 48 KB stages;
+//   * the even CTA issues, per K step, two tcgen05.mma.cta_group::2 (M=256,
+//     N=256, K=16), one per column half, into two FP32 accumulators that
+//     together fill TMEM (2×256 columns);
+//   * the epilogue drains half 0, releases it, then drains half 1; the next
+//     tile's MMAs for a half start as soon as that half is released, so half
+//     of the epilogue overlaps the next tile's main loop;
+//   * epilogue, edges and watchdog as in hgemm_tc2.cu.
+#include <cuda_fp16.h>
+
+#include "internal.h"
+#include "kernel_common.cuh"
+#include "ptx.cuh"
+
+namespace hg {
+namespace {
+
+struct WideCfg {
+  static constexpr int BM = 2 * kTcBM;    // tile rows
+  static constexpr int BN = 2 * kPairBN;  // tile columns (two 256-column halves)
+  static constexpr int ROWS = kTcBM;      // A rows per CTA
+  static constexpr int BROWS = kPairBN / 2;  // B rows per CTA per half
+  static constexpr int BK = kTcBK;
+  static constexpr int STAGES = 4;
+  static constexpr int UMMA_K = 16;
+  static constexpr int A_BYTES = ROWS * BK * 2;          // 16 KB
+  static constexpr int BH_BYTES = BROWS * BK * 2;        // 16 KB per half
+  static constexpr int B_BYTES = 2 * BH_BYTES;           // 32 KB
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 48 KB landed in each CTA
+  static constexpr int TX_BYTES = 2 * STAGE_BYTES;        // expected by the even CTA
+  static constexpr int EPI_WARPS = 4;
+  static constexpr int C_BOX_BYTES = kEpiRows * kEpiCols * 2;
+  static constexpr int C_BUFS = 2;
+  static constexpr int C_BYTES = EPI_WARPS * C_BUFS * C_BOX_BYTES;
+  static constexpr int HALF_COLS = kPairBN;              // TMEM columns per half
+  static constexpr int TMEM_COLS = 2 * HALF_COLS;
+  static constexpr int OFF_A = 0;
+  static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
+  static constexpr int OFF_C = OFF_B + STAGES * B_BYTES;
+  static constexpr int OFF_BAR = OFF_C + C_BYTES;
+  // full[S], empty[S], accumulator full, accumulator-half empty[2], drain
+  static constexpr int NUM_BARS = 2 * STAGES + 1 + 2 + 1;
+  static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+  static constexpr int THREADS = 192;
+  static constexpr uint32_t IDESC = idesc_f16_f32acc(BM, kPairBN);
+
+  static_assert(A_BYTES % 1024 == 0 && BH_BYTES % 1024 == 0, "1024-byte aligned stages");
+  static_assert(TMEM_COLS == 512, "two 256-column FP32 accumulators fill TMEM");
+  static_assert(SMEM_BYTES <= 232448, "exceeds 227 KB of shared memory per CTA");
+};
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
+    hgemm_tc2w_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                      const __grid_constant__ CUtensorMap tmC, const TcArgs p) {
+  using Cfg = WideCfg;
+  constexpr int STAGES = Cfg::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t sA = sbase + Cfg::OFF_A;
+  const uint32_t sB = sbase + Cfg::OFF_B;
+  const uint32_t bar0 = sbase + Cfg::OFF_BAR;
+  const uint32_t accf_bar = bar0 + 8u * (2 * STAGES);
+  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 3);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::OFF_MISC + 4);
+
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  auto acce_bar = [&](int h) { return bar0 + 8u * (2 * STAGES + 1 + h); };
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();  // 0: issues the pair MMAs
+  const int cluster_id = blockIdx.x >> 1;
+  const int num_clusters = gridDim.x >> 1;
+  const Watchdog wd{abort_flag, p.status, p.timeout_ns};
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);   // even CTA's arrive.expect_tx; TMA bytes of both CTAs
+      mbar_init(empty_bar(s), 1);  // multicast tcgen05.commit
+    }
+    mbar_init(accf_bar, 1);                          // multicast tcgen05.commit per tile
+    mbar_init(acce_bar(0), 2 * Cfg::EPI_WARPS);      // every epilogue warp of the pair
+    mbar_init(acce_bar(1), 2 * Cfg::EPI_WARPS);
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    prefetch_tensormap(&tmA);
+    prefetch_tensormap(&tmB);
+    prefetch_tensormap(&tmC);
+  }
+  if (warp == 1) {
+    tmem_alloc_cg2(smem_u32(tmem_slot), Cfg::TMEM_COLS);
+    tmem_relinquish_alloc_permit_cg2();
+  }
+  tc_fence_before_sync();
+  cluster_sync();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer (both CTAs)
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      long long issued = 0;
+      bool ok = true;
+      for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters) {
+        int mb, nb;
+        tile_coords(t, p.num_m, p.num_n, p.group_m, mb, nb);
+        const int ya = mb * Cfg::BM + static_cast<int>(rank) * Cfg::ROWS;
+        const int yb = nb * Cfg::BN + static_cast<int>(rank) * Cfg::BROWS;
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!wait_phase(empty_bar(stage), phase ^ 1u, wd, kWdProducerEmpty)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = mapa_shared(full_bar(stage), 0);
+          if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), Cfg::TX_BYTES);
+          const uint32_t sb = sB + stage * Cfg::B_BYTES;
+          tma_load_2d_cg2(sA + stage * Cfg::A_BYTES, &tmA, fb, kb * Cfg::BK, ya);
+          tma_load_2d_cg2(sb, &tmB, fb, kb * Cfg::BK, yb);
+          tma_load_2d_cg2(sb + Cfg::BH_BYTES, &tmB, fb, kb * Cfg::BK, yb + kPairBN);
+          ++issued;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // Drain, as in the 256×256 pair kernel.
+      int s = stage;
+      uint32_t ph = phase;
+      for (long long i = 0; i < issued && i < STAGES; ++i) {
+        if (s == 0) {
+          s = STAGES - 1;
+          ph ^= 1u;
+        } else {
+          --s;
+        }
+        if (rank == 0)
+          wait_drain(full_bar(s), ph, wd);
+        else
+          wait_drain_cluster(empty_bar(s), ph, wd);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------------------------------------- MMA issuer (even CTA)
+    if (rank == 0 && lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t tile_phase = 0;  // parity of this CTA's tile count
+      bool ok = true;
+      for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters) {
+        for (int kb = 0; ok && kb < p.num_kb; ++kb) {
+          if (!wait_phase(full_bar(stage), phase, wd, kWdMmaFull)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint64_t a_desc = sdesc_kmajor_sw128(sA + stage * Cfg::A_BYTES);
+          const uint32_t sb = sB + stage * Cfg::B_BYTES;
+          for (int h = 0; h < 2; ++h) {
+            if (kb == 0) {
+              // the previous tile's half h must have been drained
+              if (!wait_phase_cluster(acce_bar(h), tile_phase ^ 1u, wd, kWdMmaAccEmpty)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after_sync();
+            }
+            const uint64_t b_desc = sdesc_kmajor_sw128(sb + h * Cfg::BH_BYTES);
+            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(h * Cfg::HALF_COLS);
+#pragma unroll
+            for (int k = 0; k < Cfg::BK / Cfg::UMMA_K; ++k)
+              mma_f16_ss_cg2(d_tmem, a_desc + 2u * k, b_desc + 2u * k, Cfg::IDESC,
+                             (kb > 0 || k > 0) ? 1u : 0u);
+          }
+          if (!ok) break;
+          mma_commit_cg2_multicast(empty_bar(stage), 0x3);  // frees the stage in both CTAs
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit_cg2_multicast(accf_bar, 0x3);  // both halves of both CTAs complete
+        tile_phase ^= 1u;
+      }
+      mma_commit_cg2_multicast(drain_bar, 0x1);
+      wait_drain(drain_bar, 0, wd);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------ epilogue (both CTAs)
+    const int q = warp & 3;
+    uint8_t* cbuf_base = smem + Cfg::OFF_C + q * Cfg::C_BUFS * Cfg::C_BOX_BYTES;
+    uint32_t tile_phase = 0;
+    int cb = 0;
+    for (int t = cluster_id; t < p.num_tiles; t += num_clusters) {
+      int mb, nb;
+      tile_coords(t, p.num_m, p.num_n, p.group_m, mb, nb);
+      int ok = 1;
+      if (lane == 0) ok = wait_phase(accf_bar, tile_phase, wd, kWdEpiAccFull) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after_sync();
+      const int y0 = mb * Cfg::BM + static_cast<int>(rank) * Cfg::ROWS + q * kEpiRows;
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                               static_cast<uint32_t>(h * Cfg::HALF_COLS);
+        constexpr int chunks = kPairBN / kEpiCols;
+#pragma unroll 1
+        for (int c = 0; c < chunks; ++c) {
+          uint32_t v0[32], v1[32];
+          tmem_ld_32x32b_x32(t_row + c * kEpiCols, v0);
+          tmem_ld_32x32b_x32(t_row + c * kEpiCols + 32, v1);
+          tmem_ld_wait(v0);
+          tmem_ld_wait(v1);
+          if (c == chunks - 1) {
+            // half h has been read: the next tile's MMAs may overwrite it
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(mapa_shared(acce_bar(h), 0));
+          }
+          const int x0 = nb * Cfg::BN + h * kPairBN + c * kEpiCols;
+          if (x0 >= p.N || y0 >= p.M) continue;
+          if (lane == 0) bulk_wait_group_read<1>();
+          __syncwarp();
+          uint8_t* buf = cbuf_base + cb * Cfg::C_BOX_BYTES;
+          uint8_t* row = buf + lane * 128;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint32_t* v = (j < 4) ? (v0 + 8 * j) : (v1 + 8 * (j - 4));
+            uint4 pk;
+            pk.x = pack_half2(v[0], v[1]);
+            pk.y = pack_half2(v[2], v[3]);
+            pk.z = pack_half2(v[4], v[5]);
+            pk.w = pack_half2(v[6], v[7]);
+            *reinterpret_cast<uint4*>(row + ((j ^ (lane & 7)) << 4)) = pk;
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmC, smem_u32(buf), x0, y0);
+            bulk_commit_group();
+          }
+          cb ^= 1;
+        }
+      }
+      tile_phase ^= 1u;
+    }
+    if (lane == 0) bulk_wait_group<0>();
+    __syncwarp();
+  }
+
+  // Neither CTA frees TMEM before the pair's last MMA and last TMEM read.
+  tc_fence_before_sync();
+  cluster_sync();
+  tc_fence_after_sync();
+  if (warp == 1) tmem_dealloc_cg2(tmem_base, Cfg::TMEM_COLS);
+}
+
+}  // namespace
+
+int wide_max_clusters(int num_sms) {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return num_sms / 2;
+  if (cached[dev] > 0) return cached[dev];
+  int n = 0;
+  if (cudaFuncSetAttribute(hgemm_tc2w_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           WideCfg::SMEM_BYTES) == cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(num_sms & ~1));
+    cfg.blockDim = dim3(WideCfg::THREADS);
+    cfg.dynamicSmemBytes = WideCfg::SMEM_BYTES;
+    if (cudaOccupancyMaxActiveClusters(&n, hgemm_tc2w_kernel, &cfg) != cudaSuccess) n = 0;
+  }
+  (void)cudaGetLastError();
+  if (n <= 0) n = num_sms / 2;
+  cached[dev] = n;
+  return n;
+}
+
+cudaError_t launch_tc_wide(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
+                           const TcArgs& args, cudaStream_t stream) {
+  static bool attr_done[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !attr_done[dev]) {
+    e = cudaFuncSetAttribute(hgemm_tc2w_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             WideCfg::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_done[dev] = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(args.grid));
+  cfg.blockDim = dim3(WideCfg::THREADS);
+  cfg.dynamicSmemBytes = WideCfg::SMEM_BYTES;
+  cfg.stream = stream;
+  return cudaLaunchKernelEx(&cfg, hgemm_tc2w_kernel, a, b, c, args);
+}
+
+}  // namespace hg

@@ -52,6 +52,10 @@ cudaError_t launch_tc_pair(const CUtensorMap& a, const CUtensorMap& b, const CUt
                            const CUtensorMap& c, const TcArgs& args, cudaStream_t stream);
 // Largest number of co-resident 2-CTA clusters of the pair kernel.
 int pair_max_clusters(int num_sms);
+// Wide pair kernel: 256×512 tiles per CTA pair.
+cudaError_t launch_tc_wide(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
+                           const TcArgs& args, cudaStream_t stream);
+int wide_max_clusters(int num_sms);
 // Split-K cluster kernel for few output tiles: `split` K-slices (2, 3 or 4),
 // one cluster of 2*split CTAs per 256×256 tile (args.num_tiles of them).
 cudaError_t launch_skinny(int split, const CUtensorMap& a, const CUtensorMap& b,

@@ -52,8 +52,11 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const 
   return true;
 }
 
-// The same with cluster-scope acquire, for barriers that receive arrivals or
-// transaction bytes from the other CTA of a pair.
+// The same with cluster-scope acquire, for barriers that other threads of
+// the cluster arrive on remotely (ordinary arrivals carry their release to
+// the waiter only at cluster scope). Barriers completed by TMA transaction
+// bytes or by tcgen05.commit, even from the other CTA of a pair, are waited
+// on at CTA scope.
 __device__ __forceinline__ bool wait_phase_cluster(uint32_t bar, uint32_t parity,
                                                    const Watchdog& wd, int code) {
   if (mbar_try_wait_cluster(bar, parity)) return true;

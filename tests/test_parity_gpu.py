@@ -20,7 +20,7 @@ from gpu_helpers import assert_close, oracle_threads, run_gpu, to_device, torch_
 pytestmark = pytest.mark.gpu
 
 
-TMA_PATHS = [None, tc.HGEMM_PATH_TC, tc.HGEMM_PATH_TC_PAIR,
+TMA_PATHS = [None, tc.HGEMM_PATH_TC, tc.HGEMM_PATH_TC_PAIR, tc.HGEMM_PATH_TC_WIDE,
              tc.HGEMM_PATH_SKINNY]   # None: automatic choice
 
 
@@ -79,8 +79,8 @@ def test_8192_cube_sampled_entries_and_properties():
     assert torch.equal(dc2[normal], dc[normal] * 2)
 
 
-@pytest.mark.parametrize("path", [tc.HGEMM_PATH_TC, tc.HGEMM_PATH_TC_PAIR, tc.HGEMM_PATH_SKINNY,
-                                  tc.HGEMM_PATH_GENERIC])
+@pytest.mark.parametrize("path", [tc.HGEMM_PATH_TC, tc.HGEMM_PATH_TC_PAIR, tc.HGEMM_PATH_TC_WIDE,
+                                  tc.HGEMM_PATH_SKINNY, tc.HGEMM_PATH_GENERIC])
 def test_subnormal_operands_are_honoured(path):
     """FP16 subnormal inputs keep their value (no flush to zero): each case's
     single product is exact and lands on a normal FP16 value."""
@@ -98,12 +98,14 @@ def test_subnormal_operands_are_honoured(path):
 
 
 @pytest.mark.parametrize("M,N,K", [(2600, 2040, 136), (2560, 2048, 64), (8192, 1024, 72)])
-def test_pair_kernel_last_wave_halves(M, N, K):
-    """More 256x256 tiles than one wave of CTA pairs, with a short last wave:
-    the last wave's tiles run as 128-column halves."""
+@pytest.mark.parametrize("path", [tc.HGEMM_PATH_TC_PAIR, tc.HGEMM_PATH_TC_WIDE])
+def test_pair_kernels_several_waves(M, N, K, path):
+    """More tiles than one wave of CTA pairs, with a short last wave (the
+    256x256 kernel runs the last wave's tiles as 128-column halves; the
+    256x512 kernel walks several tiles per pair, reusing its accumulator)."""
     a, b = synth.operands(M, N, K, seed=M + N + K, kind="uniform")
     ref = oracle.hgemm(a, b, nthreads=oracle_threads())
-    assert_close(run_gpu(a, b, path=tc.HGEMM_PATH_TC_PAIR), ref, what=f"pair tail {M}x{N}x{K}")
+    assert_close(run_gpu(a, b, path=path), ref, what=f"path {path} {M}x{N}x{K}")
 
 
 EDGE = [1, 7, 8, 15, 16, 17, 127, 128, 129, 1000, 1001]
@@ -125,7 +127,7 @@ def _edge_cases(aligned):
     return sorted(set(keep) | {cases[i] for i in picked})
 
 
-@pytest.mark.parametrize("path", [tc.HGEMM_PATH_TC, tc.HGEMM_PATH_TC_PAIR,
+@pytest.mark.parametrize("path", [tc.HGEMM_PATH_TC, tc.HGEMM_PATH_TC_PAIR, tc.HGEMM_PATH_TC_WIDE,
                                   tc.HGEMM_PATH_SKINNY])
 @pytest.mark.parametrize("M,N,K", _edge_cases(aligned=True))
 def test_edges_tensor_core_paths(M, N, K, path):
@@ -162,8 +164,8 @@ def test_misaligned_pointers_take_the_generic_path():
     assert_close(bc[1:].cpu().numpy().reshape(M, N), ref, what="misaligned")
 
 
-@pytest.mark.parametrize("path", [tc.HGEMM_PATH_TC, tc.HGEMM_PATH_TC_PAIR, tc.HGEMM_PATH_SKINNY,
-                                  tc.HGEMM_PATH_GENERIC])
+@pytest.mark.parametrize("path", [tc.HGEMM_PATH_TC, tc.HGEMM_PATH_TC_PAIR, tc.HGEMM_PATH_TC_WIDE,
+                                  tc.HGEMM_PATH_SKINNY, tc.HGEMM_PATH_GENERIC])
 def test_guard_bands_untouched(path):
     """Nothing outside C is written: C sits inside a sentinel-filled buffer."""
     torch = torch_cuda()
