@@ -396,6 +396,7 @@ def run_ours(args, spec, a, b, world, rank, local):
     # ---- roofline of the dominant (only) kernel
     peaks, peak_src = load_peaks()
     kernel = {tc.HGEMM_PATH_TC: "hgemm_tc_kernel", tc.HGEMM_PATH_TC_PAIR: "hgemm_tc2_kernel",
+              tc.HGEMM_PATH_TC_WIDE: "hgemm_tc2w_kernel",
               tc.HGEMM_PATH_SKINNY: "hgemm_skinny_kernel",
               tc.HGEMM_PATH_GENERIC: "hgemm_generic_kernel"}.get(path, f"path {path}")
     ai = flops / bytes_of(spec)

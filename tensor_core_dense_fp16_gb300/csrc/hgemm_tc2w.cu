@@ -23,7 +23,7 @@
 //   * the epilogue drains half 0, releases it, then drains half 1; the next
 //     tile's MMAs for a half start as soon as that half is released, so half
 //     of the epilogue overlaps the next tile's main loop;
-//   * epilogue, edges and watchdog as in hgemm_tc2.cu.
+//   * serpentine K, epilogue, edges and watchdog as in hgemm_tc2.cu.
 #include <cuda_fp16.h>
 
 #include "internal.h"
@@ -132,7 +132,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
         tile_coords(t, p.num_m, p.num_n, p.group_m, mb, nb);
         const int ya = mb * Cfg::BM + static_cast<int>(rank) * Cfg::ROWS;
         const int yb = nb * Cfg::BN + static_cast<int>(rank) * Cfg::BROWS;
-        for (int kb = 0; kb < p.num_kb; ++kb) {
+        // serpentine K (see hgemm_tc2.cu)
+        const bool reverse = (((t - cluster_id) / num_clusters) & 1) != 0;
+        for (int step = 0; step < p.num_kb; ++step) {
+          const int kb = reverse ? p.num_kb - 1 - step : step;
           if (!wait_phase(empty_bar(stage), phase ^ 1u, wd, kWdProducerEmpty)) {
             ok = false;
             break;
@@ -196,6 +199,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
             const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(h * Cfg::HALF_COLS);
 #pragma unroll
             for (int k = 0; k < Cfg::BK / Cfg::UMMA_K; ++k)
+              // kb counts K steps in load order; the first one overwrites
               mma_f16_ss_cg2(d_tmem, a_desc + 2u * k, b_desc + 2u * k, Cfg::IDESC,
                              (kb > 0 || k > 0) ? 1u : 0u);
           }

@@ -68,9 +68,12 @@ def test_path_selection(lib):
     assert sel(A16, B16, C16, 0, 5, 5) == tc.HGEMM_PATH_NONE
     assert sel(A16, B16, C16, 5, 0, 5) == tc.HGEMM_PATH_NONE
     assert sel(A16, B16, C16, 4, 8, 0) == tc.HGEMM_PATH_ZERO
-    # many 256x256 tiles: CTA pairs
-    assert sel(A16, B16, C16, 8192, 8192, 8192) == tc.HGEMM_PATH_TC_PAIR
+    # enough 256x512 tiles for every CTA pair: wide pair tiles
+    assert sel(A16, B16, C16, 8192, 8192, 8192) == tc.HGEMM_PATH_TC_WIDE
+    assert sel(A16, B16, C16, 4096, 4096, 4096) == tc.HGEMM_PATH_TC_WIDE
+    # fewer: 256x256 pair tiles
     assert sel(A16, B16, C16, 2048, 2048, 2048) == tc.HGEMM_PATH_TC_PAIR
+    assert sel(A16, B16, C16, 4096, 2048, 1024) == tc.HGEMM_PATH_TC_PAIR
     # few tiles and a long K: split K over clusters of pairs
     assert sel(A16, B16, C16, 4096, 256, 4096) == tc.HGEMM_PATH_SKINNY
     assert sel(A16, B16, C16, 1000, 1000, 1000) == tc.HGEMM_PATH_SKINNY
@@ -100,6 +103,8 @@ def test_forced_paths(lib):
         assert tc.hgemm_select_path(A16, B16, C16, 256, 256, 256) == tc.HGEMM_PATH_TC
         tc.hgemm_force_path(tc.HGEMM_PATH_TC_PAIR)
         assert tc.hgemm_select_path(A16, B16, C16, 64, 256, 256) == tc.HGEMM_PATH_TC_PAIR
+        tc.hgemm_force_path(tc.HGEMM_PATH_TC_WIDE)
+        assert tc.hgemm_select_path(A16, B16, C16, 256, 256, 256) == tc.HGEMM_PATH_TC_WIDE
         tc.hgemm_force_path(tc.HGEMM_PATH_SKINNY)
         assert tc.hgemm_select_path(A16, B16, C16, 8192, 8192, 8192) == tc.HGEMM_PATH_TC_PAIR
         assert tc.hgemm_select_path(A16, B16, C16, 512, 512, 512) == tc.HGEMM_PATH_SKINNY
