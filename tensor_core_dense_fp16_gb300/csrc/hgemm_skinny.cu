@@ -59,8 +59,9 @@ struct SkCfg {
   static constexpr int C_WARP_BYTES = kEpiRows * MAX_OWN_COLS * 2;
   static constexpr int C_BYTES = 4 * C_WARP_BYTES;
   static constexpr int OFF_BAR = OFF_C + C_BYTES;
-  // full, empty, accumulator full, drain, partials received
-  static constexpr int NUM_BARS = 2 * STAGES + 3;
+  // full, empty, accumulator full, drain, partials received, owner ready
+  // (one per slice), partials acknowledged
+  static constexpr int NUM_BARS = 2 * STAGES + 3 + 4 + 1;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
   static constexpr int THREADS = 192;
@@ -100,6 +101,8 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t accf_bar = bar0 + 8u * (2 * Cfg::STAGES);
   const uint32_t drain_bar = accf_bar + 8u;
   const uint32_t recv_bar = drain_bar + 8u;
+  const uint32_t ready_bar0 = recv_bar + 8u;     // ready_bar0 + 8j: owner j may receive
+  const uint32_t ack_bar = ready_bar0 + 8u * 4;  // every owner has received from us
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::OFF_MISC + 4);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
@@ -131,6 +134,8 @@ __global__ void __launch_bounds__(192, 1)
     mbar_init(recv_bar, 1);
     // the partials of the other slices for this CTA's range, from 4 warps each
     mbar_arrive_expect_tx(recv_bar, static_cast<uint32_t>((SPLIT - 1) * Cfg::ROWS * own_cols * 4));
+    for (int j = 0; j < 4; ++j) mbar_init(ready_bar0 + 8u * j, 1);
+    mbar_init(ack_bar, SPLIT - 1);
     *abort_flag = 0;
     fence_barrier_init();
     prefetch_tensormap(&tmA);
@@ -217,10 +222,13 @@ __global__ void __launch_bounds__(192, 1)
     if (lane == 0) ok = wait_phase(accf_bar, 0, wd, kWdEpiAccFull) ? 1 : 0;
     ok = __shfl_sync(0xffffffffu, ok, 0);
     tc_fence_after_sync();
+    // this CTA's operand ring is now free: tell the other slices of the same
+    // half that they may send their partials of our column range
+    if (warp == 2 && lane == 0 && ok)
+      for (int s2 = 0; s2 < SPLIT; ++s2)
+        if (s2 != slice)
+          mbar_arrive_cluster(mapa_shared(ready_bar0 + 8u * slice, static_cast<uint32_t>(2 * s2 + half)));
   }
-
-  // every pair's MMAs are done, so every CTA's operand ring is free
-  cluster_sync();
 
   const int q = warp & 3;  // TMEM lanes / tile rows 32q .. 32q+31 of this CTA
   const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
@@ -235,6 +243,11 @@ __global__ void __launch_bounds__(192, 1)
       const int c0 = 64 * owned_unit(j, SPLIT);
       const int cols = 64 * owned_unit(j + 1, SPLIT) - c0;
       uint8_t* blk = smem + (send_off - sbase);
+      // owner j's ring must be free before our copy lands in it
+      int rdy = 1;
+      if (lane == 0) rdy = wait_phase_cluster(ready_bar0 + 8u * j, 0, wd, kWdReduce) ? 1 : 0;
+      rdy = __shfl_sync(0xffffffffu, rdy, 0);
+      if (!rdy) break;
 #pragma unroll 1
       for (int c32 = 0; c32 < cols / 32; ++c32) {
         uint32_t v[32];
@@ -263,6 +276,9 @@ __global__ void __launch_bounds__(192, 1)
     int got = 1;
     if (lane == 0) got = wait_phase_cluster(recv_bar, 0, wd, kWdReduce) ? 1 : 0;
     got = __shfl_sync(0xffffffffu, got, 0);
+    if (got && warp == 2 && lane == 0)
+      for (int s2 = 0; s2 < SPLIT; ++s2)
+        if (s2 != slice) mbar_arrive_cluster(mapa_shared(ack_bar, static_cast<uint32_t>(2 * s2 + half)));
     if (got) {
       const int x0 = nb * Cfg::BN + own_c0;
       const int y0 = mb * Cfg::BM + half * Cfg::ROWS + q * kEpiRows;
@@ -328,11 +344,13 @@ __global__ void __launch_bounds__(192, 1)
     }
   }
 
-  // No CTA leaves while a copy into or out of its shared memory may be in
-  // flight (every owner has received all its bytes before it gets here), and
-  // neither CTA of a pair frees TMEM before the other is done with it.
+  // Leaving: every owner acknowledges once all partials have landed in its
+  // shared memory, so after our acknowledgements no copy reads our shared
+  // memory and nobody writes into it. The pair's collective TMEM release is
+  // reached by both CTAs only after both are done with TMEM.
+  if (warp == 2 && lane == 0 && ok) wait_phase_cluster(ack_bar, 0, wd, kWdReduce);
   tc_fence_before_sync();
-  cluster_sync();
+  __syncthreads();
   tc_fence_after_sync();
   if (warp == 1) tmem_dealloc_cg2(tmem_base, Cfg::TMEM_COLS);
 }
