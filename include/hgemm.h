@@ -146,6 +146,29 @@ HGEMM_API int hgemm_force_path(int path);
  */
 HGEMM_API int hgemm_device_status(cudaStream_t stream);
 
+/*
+ * hgemm_set_wait_timeout — time limit, in nanoseconds, of every wait inside
+ * the kernels of later calls in this process (0 restores the default, 2 s).
+ * Returns HGEMM_OK.
+ */
+HGEMM_API int hgemm_set_wait_timeout(unsigned long long ns);
+
+/* fault injection for testing the watchdog */
+#define HGEMM_INJECT_NONE 0
+#define HGEMM_INJECT_DROP_ARRIVAL 1 /* producer withholds its first stage's arrival */
+
+/*
+ * hgemm_debug_inject — testing aid for the watchdog. With
+ * HGEMM_INJECT_DROP_ARRIVAL, the TMA producer of the tensor-core kernels of
+ * later calls withholds the barrier arrival of its first stage (its copies
+ * are still issued and land), so the MMA issuer's bounded wait gives up: the
+ * kernel records HGEMM_ERR_TIMEOUT in the watchdog word, drains, frees TMEM
+ * and returns with C incomplete. No GPU fault is raised and the context
+ * stays usable. HGEMM_INJECT_NONE turns it off. Returns HGEMM_OK or
+ * HGEMM_ERR_INVALID_ARG.
+ */
+HGEMM_API int hgemm_debug_inject(int what);
+
 /* hgemm_last_cuda_error — the cudaError_t behind the last HGEMM_ERR_CUDA
  * returned on this host thread (0 if none). */
 HGEMM_API int hgemm_last_cuda_error(void);

@@ -27,7 +27,8 @@ __all__ = [
     "HGEMM_PATH_TC_WIDE", "HGEMM_MAX_DIM",
     "HgemmError", "library_path", "load", "hgemm", "hgemm_host", "hgemm_select_path",
     "hgemm_force_path", "hgemm_device_status", "hgemm_last_cuda_error",
-    "hgemm_status_string", "hgemm_version", "matmul",
+    "hgemm_status_string", "hgemm_version", "hgemm_set_wait_timeout", "hgemm_debug_inject",
+    "HGEMM_INJECT_NONE", "HGEMM_INJECT_DROP_ARRIVAL", "matmul",
 ]
 
 HGEMM_OK = 0
@@ -46,6 +47,9 @@ HGEMM_PATH_TC_PAIR = 5
 HGEMM_PATH_TC_WIDE = 6
 
 HGEMM_MAX_DIM = 0x7FFFFFFF
+
+HGEMM_INJECT_NONE = 0
+HGEMM_INJECT_DROP_ARRIVAL = 1
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "_build", "libhgemm.so")
@@ -94,6 +98,10 @@ def load():
     lib.hgemm_status_string.restype = ctypes.c_char_p
     lib.hgemm_version.argtypes = []
     lib.hgemm_version.restype = i32
+    lib.hgemm_set_wait_timeout.argtypes = [ctypes.c_ulonglong]
+    lib.hgemm_set_wait_timeout.restype = i32
+    lib.hgemm_debug_inject.argtypes = [i32]
+    lib.hgemm_debug_inject.restype = i32
     _lib = lib
     return lib
 
@@ -202,6 +210,16 @@ def hgemm_status_string(status: int) -> str:
 def hgemm_version() -> tuple[int, int]:
     v = int(load().hgemm_version())
     return v >> 16, v & 0xFFFF
+
+
+def hgemm_set_wait_timeout(ns: int) -> None:
+    """Time limit of every in-kernel wait for later calls (0: default 2 s)."""
+    _raise_on(load().hgemm_set_wait_timeout(int(ns)), "hgemm_set_wait_timeout")
+
+
+def hgemm_debug_inject(what: int) -> None:
+    """Testing aid for the watchdog (HGEMM_INJECT_*); see include/hgemm.h."""
+    _raise_on(load().hgemm_debug_inject(int(what)), "hgemm_debug_inject")
 
 
 def matmul(a, b_cols, out=None, stream=None):

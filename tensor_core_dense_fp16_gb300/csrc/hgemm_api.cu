@@ -28,6 +28,7 @@ constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;  // 2 s per wait
 thread_local int t_last_cuda_error = 0;
 std::atomic<int> g_forced_path{-1};
 std::atomic<unsigned long long> g_timeout_ns{kDefaultTimeoutNs};
+std::atomic<int> g_inject{HGEMM_INJECT_NONE};
 
 struct DeviceState {
   std::atomic<int> ready{0};  // 0 unknown, 1 supported, -1 unsupported
@@ -252,6 +253,7 @@ int run_tc(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t 
   args.grid = static_cast<int>(tiles < dev.num_sms ? tiles : dev.num_sms);
   args.status = dev.status;
   args.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
+  args.inject = g_inject.load(std::memory_order_relaxed);
   cudaError_t e = hg::launch_tc_128x256(ma, mb, mc, args, stream);
   return e == cudaSuccess ? HGEMM_OK : cuda_fail(e);
 }
@@ -285,6 +287,7 @@ int run_tc_pair(const void* A, const void* B, void* C, int64_t M, int64_t N, int
   args.grid = static_cast<int>(2 * (args.num_tiles < clusters ? args.num_tiles : clusters));
   args.status = dev.status;
   args.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
+  args.inject = g_inject.load(std::memory_order_relaxed);
   cudaError_t e = hg::launch_tc_pair(ma, mb, mbh, mc, args, stream);
   return e == cudaSuccess ? HGEMM_OK : cuda_fail(e);
 }
@@ -312,6 +315,7 @@ int run_tc_wide(const void* A, const void* B, void* C, int64_t M, int64_t N, int
   args.grid = static_cast<int>(2 * (tiles < clusters ? tiles : clusters));
   args.status = dev.status;
   args.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
+  args.inject = g_inject.load(std::memory_order_relaxed);
   cudaError_t e = hg::launch_tc_wide(ma, mb, mc, args, stream);
   return e == cudaSuccess ? HGEMM_OK : cuda_fail(e);
 }
@@ -338,6 +342,7 @@ int run_skinny(const void* A, const void* B, void* C, int64_t M, int64_t N, int6
   args.grid = static_cast<int>(tiles * 2 * split);
   args.status = dev.status;
   args.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
+  args.inject = g_inject.load(std::memory_order_relaxed);
   cudaError_t e = hg::launch_skinny(split, ma, mb, mc, args, stream);
   return e == cudaSuccess ? HGEMM_OK : cuda_fail(e);
 }
@@ -435,6 +440,17 @@ int hgemm_device_status(cudaStream_t stream) {
       return cuda_fail(e);
     return HGEMM_ERR_TIMEOUT;
   }
+  return HGEMM_OK;
+}
+
+int hgemm_set_wait_timeout(unsigned long long ns) {
+  g_timeout_ns.store(ns ? ns : kDefaultTimeoutNs);
+  return HGEMM_OK;
+}
+
+int hgemm_debug_inject(int what) {
+  if (what != HGEMM_INJECT_NONE && what != HGEMM_INJECT_DROP_ARRIVAL) return HGEMM_ERR_INVALID_ARG;
+  g_inject.store(what);
   return HGEMM_OK;
 }
 

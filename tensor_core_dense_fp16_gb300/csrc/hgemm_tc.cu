@@ -142,7 +142,8 @@ __global__ void __launch_bounds__(192, 1)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(full_bar(stage), Cfg::STAGE_BYTES);
+          if (!(p.inject == 1 && issued == 0))  // testing aid: withhold one arrival
+            mbar_arrive_expect_tx(full_bar(stage), Cfg::STAGE_BYTES);
           tma_load_2d(sA + stage * Cfg::A_BYTES, &tmA, full_bar(stage), kb * Cfg::BK, mb * Cfg::BM);
           tma_load_2d(sB + stage * Cfg::B_BYTES, &tmB, full_bar(stage), kb * Cfg::BK, nb * BN);
           ++issued;

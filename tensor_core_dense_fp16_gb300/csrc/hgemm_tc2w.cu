@@ -141,7 +141,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
             break;
           }
           const uint32_t fb = mapa_shared(full_bar(stage), 0);
-          if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), Cfg::TX_BYTES);
+          if (rank == 0 && !(p.inject == 1 && issued == 0))  // testing aid: withhold one arrival
+            mbar_arrive_expect_tx(full_bar(stage), Cfg::TX_BYTES);
           const uint32_t sb = sB + stage * Cfg::B_BYTES;
           tma_load_2d_cg2(sA + stage * Cfg::A_BYTES, &tmA, fb, kb * Cfg::BK, ya);
           tma_load_2d_cg2(sb, &tmB, fb, kb * Cfg::BK, yb);

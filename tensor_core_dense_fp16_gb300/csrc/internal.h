@@ -31,6 +31,7 @@ struct TcArgs {
   int grid;                  // persistent CTAs
   int* status;               // device watchdog word
   unsigned long long timeout_ns;
+  int inject;                // HGEMM_INJECT_* (testing the watchdog)
 };
 
 // Plain-pointer launch arguments for the kernels that do not use TMA.

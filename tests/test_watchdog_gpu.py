@@ -1,0 +1,47 @@
+"""Failure detection without a GPU fault: every wait inside the kernels is
+bounded in time. The testing hook makes a kernel's TMA producer withhold one
+barrier arrival (its copies still land), so the MMA issuer's wait runs out;
+the kernel must record the timeout, drain, free TMEM and return, the host
+must read HGEMM_ERR_TIMEOUT, and the context must stay usable."""
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+import tensor_core_dense_fp16_gb300 as tc
+from gpu_helpers import assert_close, run_gpu, to_device, torch_cuda
+
+
+def test_hook_arguments_are_checked():
+    tc.load()
+    with pytest.raises(tc.HgemmError):
+        tc.hgemm_debug_inject(99)
+    tc.hgemm_debug_inject(tc.HGEMM_INJECT_NONE)
+    tc.hgemm_set_wait_timeout(0)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("path", [tc.HGEMM_PATH_TC, tc.HGEMM_PATH_TC_PAIR, tc.HGEMM_PATH_TC_WIDE])
+def test_withheld_arrival_times_out_and_the_context_survives(path):
+    torch = torch_cuda()
+    M = N = K = 512
+    a, b = synth.operands(M, N, K, seed=31, kind="uniform")
+    da, db = to_device(a), to_device(b)
+    dc = torch.zeros((M, N), dtype=torch.float16, device="cuda")
+    assert tc.hgemm_device_status() == tc.HGEMM_OK
+    tc.hgemm_set_wait_timeout(50_000_000)   # 50 ms per wait
+    tc.hgemm_debug_inject(tc.HGEMM_INJECT_DROP_ARRIVAL)
+    tc.hgemm_force_path(path)
+    try:
+        tc.hgemm(da, db, dc, M, N, K)
+        assert tc.hgemm_device_status() == tc.HGEMM_ERR_TIMEOUT
+        # the word was cleared by the read
+        assert tc.hgemm_device_status() == tc.HGEMM_OK
+    finally:
+        tc.hgemm_debug_inject(tc.HGEMM_INJECT_NONE)
+        tc.hgemm_set_wait_timeout(0)
+        tc.hgemm_force_path(-1)
+    # the same context computes correctly afterwards
+    ref = oracle.hgemm(a, b)
+    assert_close(run_gpu(a, b, path=path), ref, what=f"after timeout, path {path}")
