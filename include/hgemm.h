@@ -59,7 +59,7 @@ typedef uint16_t hgemm_half_t; /* IEEE binary16 bit pattern */
 
 /* status codes */
 #define HGEMM_OK 0
-#define HGEMM_ERR_INVALID_ARG (-1)        /* negative or too large dimension, NULL pointer */
+#define HGEMM_ERR_INVALID_ARG (-1)        /* bad dimension, NULL or odd pointer */
 #define HGEMM_ERR_ALIAS (-2)              /* C overlaps A or B */
 #define HGEMM_ERR_UNSUPPORTED_DEVICE (-3) /* current device is not compute capability 10.3 */
 #define HGEMM_ERR_CUDA (-4)               /* a CUDA runtime/driver call failed (see hgemm_last_cuda_error) */
@@ -70,7 +70,7 @@ typedef uint16_t hgemm_half_t; /* IEEE binary16 bit pattern */
 #define HGEMM_PATH_ZERO 1     /* K == 0: C is filled with +0 (the empty sum) */
 #define HGEMM_PATH_TC 2       /* tcgen05 + TMA persistent kernel, one CTA per 128×256 tile */
 #define HGEMM_PATH_SKINNY 3   /* tcgen05 + TMA kernel for small N, split over K */
-#define HGEMM_PATH_GENERIC 4  /* kernel fed by plain loads: any alignment */
+#define HGEMM_PATH_GENERIC 4  /* tcgen05 kernel fed by plain loads: any alignment */
 #define HGEMM_PATH_TC_PAIR 5  /* tcgen05 + TMA persistent kernel, CTA pairs per 256×256 tile */
 #define HGEMM_PATH_TC_WIDE 6  /* tcgen05 + TMA persistent kernel, CTA pairs per 256×512 tile */
 
@@ -81,9 +81,10 @@ typedef uint16_t hgemm_half_t; /* IEEE binary16 bit pattern */
  * hgemm — C = A·B on `stream` (see the top of this file for layouts).
  *
  *   A, B, C  device pointers (or managed memory visible to the current
- *            device). Any alignment is accepted: when A, B, C are 16-byte
- *            aligned and K and N are multiples of 8 the TMA-fed kernels run,
- *            otherwise a kernel with plain loads does the same arithmetic.
+ *            device), each at least 2-byte aligned (FP16 elements). When A,
+ *            B, C are 16-byte aligned and K and N are multiples of 8 the
+ *            TMA-fed kernels run; otherwise a tensor-core kernel fed by plain
+ *            loads does the same arithmetic.
  *   M, N, K  0 <= M, N, K <= HGEMM_MAX_DIM. M == 0 or N == 0 is a no-op;
  *            K == 0 sets every C(i, j) to +0. A and B may be NULL when their
  *            size is 0, C when M*N == 0.

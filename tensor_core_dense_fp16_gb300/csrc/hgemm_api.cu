@@ -109,6 +109,10 @@ int validate(const void* A, const void* B, const void* C, int64_t M, int64_t N, 
   const unsigned __int128 lim = static_cast<unsigned __int128>(1) << 61;
   if (mk >= lim || nk >= lim || mn >= lim) return HGEMM_ERR_INVALID_ARG;
   if ((mk && !A) || (nk && !B) || (mn && !C)) return HGEMM_ERR_INVALID_ARG;
+  // FP16 elements: every pointer must be at least 2-byte aligned
+  if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B) |
+       reinterpret_cast<uintptr_t>(C)) & 1u)
+    return HGEMM_ERR_INVALID_ARG;
   if (mn && (ranges_overlap(C, 2 * static_cast<uint64_t>(mn), A, 2 * static_cast<uint64_t>(mk)) ||
              ranges_overlap(C, 2 * static_cast<uint64_t>(mn), B, 2 * static_cast<uint64_t>(nk))))
     return HGEMM_ERR_ALIAS;

@@ -1,80 +1,214 @@
 // hgemm_generic.cu — C = A·B for operands that TMA cannot describe (a base
 // pointer not 16-byte aligned, or K or N not a multiple of 8, so that a row
-// pitch is not a multiple of 16 bytes).
+// pitch is not a multiple of 16 bytes). Any 2-byte-aligned FP16 pointers.
 //
-// Same arithmetic contract as the tensor-core path: FP16 inputs, FP32
-// accumulation ("GPU架构与CUDA", 混合精度核函数), one round-to-nearest-even to
-// FP16. Edge handling follows "GPU架构与CUDA", 共享内存与分块: tiles are staged
-// in shared memory with out-of-range elements replaced by zero, and only
-// in-range outputs are stored. Each FP16 product is exact in FP32, so every
-// step here is an FP32 add of an exact product.
+// Same arithmetic contract as the other paths: FP16 inputs, FP32
+// accumulation on the tensor cores ("GPU架构与CUDA", 混合精度核函数), one
+// round-to-nearest-even to FP16. Edge handling follows "GPU架构与CUDA",
+// 共享内存与分块: tiles are staged in shared memory with out-of-range elements
+// replaced by zero, and only in-range outputs are stored.
 //
-// Layout of the work: a 64×64 output tile per 256-thread block, K staged 32
-// at a time; each thread owns a 4×4 patch of the tile.
+// Design: one CTA per 128×128 output tile.
+//   * warps 0–3 (128 threads) are the loaders: thread t copies row t of the
+//     A tile and row t of the B tile for one 64-wide K block with 2-byte loads
+//     (bounds-checked, zero outside the matrices) and writes them, 16 bytes
+//     at a time, into the same 128-byte-swizzled K-major layout that a TMA
+//     copy would produce; a 4-stage ring, one barrier arrival per warp;
+//   * warp 8 (one thread) issues tcgen05.mma (M=128, N=128, K=16) into an
+//     FP32 accumulator in TMEM;
+//   * warps 4–7 read the accumulator with tcgen05.ld, round to FP16 and store
+//     each in-range element (C need not be aligned beyond 2 bytes).
 #include <cuda_fp16.h>
 
 #include "internal.h"
+#include "kernel_common.cuh"
+#include "ptx.cuh"
 
 namespace hg {
 namespace {
 
-constexpr int GT_M = 64, GT_N = 64, GT_K = 32;
+struct GenCfg {
+  static constexpr int BM = 128, BN = 128, BK = 64, STAGES = 4, UMMA_K = 16;
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int OFF_A = 0;
+  static constexpr int OFF_B = STAGES * A_BYTES;
+  static constexpr int OFF_BAR = OFF_B + STAGES * B_BYTES;
+  static constexpr int NUM_BARS = 2 * STAGES + 2;  // full, empty, accumulator full, drain
+  static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+  static constexpr int LOADER_WARPS = 4;
+  static constexpr int EPI_WARP0 = 4;  // warps 4..7: warp w reads TMEM lanes 32*(w%4)..
+  static constexpr int MMA_WARP = 8;
+  static constexpr int THREADS = 9 * 32;
+  static constexpr int TMEM_COLS = BN;
+  static constexpr uint32_t IDESC = idesc_f16_f32acc(BM, BN);
+  static_assert(SMEM_BYTES <= 232448, "exceeds 227 KB of shared memory per CTA");
+};
 
-__global__ void __launch_bounds__(256)
-    hgemm_generic_kernel(const uint16_t* __restrict__ A, const uint16_t* __restrict__ B,
-                         uint16_t* __restrict__ C, int64_t M, int64_t N, int64_t K,
-                         int64_t tiles_n) {
-  // sA[k][i] and sB[k][j]: K-major staging, padded against bank conflicts
-  __shared__ float sA[GT_K][GT_M + 4];
-  __shared__ float sB[GT_K][GT_N + 4];
-  const int64_t m0 = static_cast<int64_t>(blockIdx.x / tiles_n) * GT_M;
-  const int64_t n0 = static_cast<int64_t>(blockIdx.x % tiles_n) * GT_N;
-  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-  float acc[4][4] = {};
-  for (int64_t k0 = 0; k0 < K; k0 += GT_K) {
-    for (int e = threadIdx.x; e < GT_M * GT_K; e += 256) {
-      const int r = e / GT_K, kk = e % GT_K;
-      const int64_t gi = m0 + r, gk = k0 + kk;
-      sA[kk][r] = (gi < M && gk < K) ? __half2float(__ushort_as_half(A[gi * K + gk])) : 0.f;
-      const int64_t gj = n0 + r;
-      sB[kk][r] = (gj < N && gk < K) ? __half2float(__ushort_as_half(B[gj * K + gk])) : 0.f;
-    }
-    __syncthreads();
-#pragma unroll 8
-    for (int kk = 0; kk < GT_K; ++kk) {
-      float a[4], b[4];
+// Row r of a K block (64 values from `src`, valid values `n`), zero-padded,
+// into the 128-byte-swizzled K-major row r of a shared-memory tile.
+__device__ __forceinline__ void load_row_swizzled(const uint16_t* __restrict__ src, int n, uint8_t* tile,
+                                                  int r) {
+  uint8_t* row = tile + r * 128;
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        a[u] = sA[kk][ty * 4 + u];
-        b[u] = sB[kk][tx * 4 + u];
+  for (int j = 0; j < 8; ++j) {
+    uint32_t w[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int k = 8 * j + 2 * u;
+      const uint32_t lo = (k < n) ? static_cast<uint32_t>(__ldg(src + k)) : 0u;
+      const uint32_t hi = (k + 1 < n) ? static_cast<uint32_t>(__ldg(src + k + 1)) : 0u;
+      w[u] = lo | (hi << 16);
+    }
+    *reinterpret_cast<uint4*>(row + ((j ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+__global__ void __launch_bounds__(GenCfg::THREADS, 1)
+    hgemm_generic_kernel(const PlainArgs p, int tiles_n, int num_kb) {
+  using Cfg = GenCfg;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + Cfg::OFF_BAR;
+  const uint32_t accf_bar = bar0 + 8u * (2 * Cfg::STAGES);
+  const uint32_t drain_bar = accf_bar + 8u;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::OFF_MISC + 4);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (Cfg::STAGES + s); };
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int64_t m0 = static_cast<int64_t>(blockIdx.x / tiles_n) * Cfg::BM;
+  const int64_t n0 = static_cast<int64_t>(blockIdx.x % tiles_n) * Cfg::BN;
+  const Watchdog wd{abort_flag, p.status, p.timeout_ns};
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < Cfg::STAGES; ++s) {
+      mbar_init(full_bar(s), Cfg::LOADER_WARPS);  // one arrival per loader warp
+      mbar_init(empty_bar(s), 1);                 // tcgen05.commit
+    }
+    mbar_init(accf_bar, 1);
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == Cfg::MMA_WARP) {
+    tmem_alloc(smem_u32(tmem_slot), Cfg::TMEM_COLS);
+    tmem_relinquish_alloc_permit();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp < Cfg::LOADER_WARPS) {
+    // ------------------------------------------------------------ loaders
+    const int r = threadIdx.x;  // tile row 0..127
+    const int64_t gi = m0 + r, gj = n0 + r;
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int kb = 0; kb < num_kb; ++kb) {
+      int ok = 1;
+      if (lane == 0) ok = wait_phase(empty_bar(stage), phase ^ 1u, wd, kWdProducerEmpty) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      const int64_t k0 = static_cast<int64_t>(kb) * Cfg::BK;
+      const int64_t kn = p.K - k0 < Cfg::BK ? p.K - k0 : Cfg::BK;
+      load_row_swizzled(p.A + gi * p.K + k0, gi < p.M ? static_cast<int>(kn) : 0,
+                        smem + Cfg::OFF_A + stage * Cfg::A_BYTES, r);
+      load_row_swizzled(p.B + gj * p.K + k0, gj < p.N ? static_cast<int>(kn) : 0,
+                        smem + Cfg::OFF_B + stage * Cfg::B_BYTES, r);
+      fence_proxy_async_smem();  // generic-proxy writes before tensor-core reads
+      __syncwarp();
+      if (lane == 0) mbar_arrive(full_bar(stage));
+      if (++stage == Cfg::STAGES) {
+        stage = 0;
+        phase ^= 1u;
       }
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-#pragma unroll
-        for (int v = 0; v < 4; ++v) acc[u][v] = __fmaf_rn(a[u], b[v], acc[u][v]);
     }
-    __syncthreads();
-  }
+  } else if (warp == Cfg::MMA_WARP) {
+    // -------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int kb = 0; kb < num_kb; ++kb) {
+        if (!wait_phase(full_bar(stage), phase, wd, kWdMmaFull)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint64_t a_desc = sdesc_kmajor_sw128(sbase + Cfg::OFF_A + stage * Cfg::A_BYTES);
+        const uint64_t b_desc = sdesc_kmajor_sw128(sbase + Cfg::OFF_B + stage * Cfg::B_BYTES);
 #pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    const int64_t gi = m0 + ty * 4 + u;
-    if (gi >= M) continue;
+        for (int k = 0; k < Cfg::BK / Cfg::UMMA_K; ++k)
+          mma_f16_ss(tmem_base, a_desc + 2u * k, b_desc + 2u * k, Cfg::IDESC,
+                     (kb > 0 || k > 0) ? 1u : 0u);
+        mma_commit(empty_bar(stage));
+        if (++stage == Cfg::STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (ok) mma_commit(accf_bar);
+      mma_commit(drain_bar);
+      wait_drain(drain_bar, 0, wd);
+    }
+    __syncwarp();
+  } else {
+    // ----------------------------------------------------------- epilogue
+    const int q = warp & 3;
+    int ok = 1;
+    if (lane == 0) ok = wait_phase(accf_bar, 0, wd, kWdEpiAccFull) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (ok) {
+      tc_fence_after_sync();
+      const int64_t gi = m0 + q * 32 + lane;
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+#pragma unroll 1
+      for (int c = 0; c < Cfg::BN / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(t_row + c * 32, v);
+        tmem_ld_wait(v);
+        if (gi < p.M) {
+          uint16_t* dst = p.C + gi * p.N + n0 + c * 32;
 #pragma unroll
-    for (int v = 0; v < 4; ++v) {
-      const int64_t gj = n0 + tx * 4 + v;
-      if (gj < N) C[gi * N + gj] = __half_as_ushort(__float2half_rn(acc[u][v]));
+          for (int j = 0; j < 32; ++j)
+            if (n0 + c * 32 + j < p.N) dst[j] = __half_as_ushort(__float2half_rn(__uint_as_float(v[j])));
+        }
+      }
     }
   }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  if (warp == Cfg::MMA_WARP) tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
 }
 
 }  // namespace
 
 cudaError_t launch_generic(const PlainArgs& args, int /*num_sms*/, cudaStream_t stream) {
-  const int64_t tiles_n = (args.N + GT_N - 1) / GT_N;
-  const int64_t tiles = tiles_n * ((args.M + GT_M - 1) / GT_M);
-  if (tiles > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
-  hgemm_generic_kernel<<<static_cast<unsigned>(tiles), 256, 0, stream>>>(
-      args.A, args.B, args.C, args.M, args.N, args.K, tiles_n);
+  static bool attr_done[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !attr_done[dev]) {
+    e = cudaFuncSetAttribute(hgemm_generic_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             GenCfg::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_done[dev] = true;
+  }
+  const int64_t tiles_n = (args.N + GenCfg::BN - 1) / GenCfg::BN;
+  const int64_t tiles = tiles_n * ((args.M + GenCfg::BM - 1) / GenCfg::BM);
+  const int64_t num_kb = (args.K + GenCfg::BK - 1) / GenCfg::BK;
+  if (tiles > 0x7FFFFFFF || num_kb > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
+  hgemm_generic_kernel<<<static_cast<unsigned>(tiles), GenCfg::THREADS, GenCfg::SMEM_BYTES, stream>>>(
+      args, static_cast<int>(tiles_n), static_cast<int>(num_kb));
   return cudaGetLastError();
 }
 

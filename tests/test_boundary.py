@@ -130,6 +130,9 @@ def test_invalid_arguments_rejected_before_any_device_work(lib):
         (A16, None, C16, 4, 4, 4),
         (A16, B16, None, 4, 4, 4),
         (A16, B16, C16, (1 << 31) - 1, (1 << 31) - 1, 8),  # M*N elements >= 2^61
+        (A16 + 1, B16, C16, 4, 4, 4),  # FP16 pointers must be 2-byte aligned
+        (A16, B16 + 3, C16, 4, 4, 4),
+        (A16, B16, C16 + 5, 4, 4, 4),
     ]
     for args in bad:
         assert lib.hgemm(*args, None) == tc.HGEMM_ERR_INVALID_ARG, args
