@@ -101,12 +101,18 @@ HGEMM_API int hgemm(const hgemm_half_t *A, const hgemm_half_t *B, hgemm_half_t *
 /*
  * hgemm_host — the same product for operands held in HOST memory.
  *
- * Enqueues on `stream`, in order: copies of hA -> dA (M*K values) and
- * hB -> dB (N*K values), hgemm(dA, dB, dC, M, N, K, stream), and a copy
- * dC -> hC (M*N values). The caller provides the device buffers dA, dB, dC
- * (same rules as hgemm) and owns every buffer. Host buffers should be
- * page-locked for the copies to be asynchronous; hC is valid once `stream`
- * has been synchronised. Same return values as hgemm.
+ * Copies hA -> dA (M*K values) and hB -> dB (N*K values), computes
+ * C = A·B into dC (same rules as hgemm) and copies dC -> hC (M*N values).
+ * All of it happens after the work already enqueued on `stream`, and
+ * `stream` completes only after the last copy back. For problems of 32 MB
+ * or more with M >= 2048 the work is pipelined over row chunks: B is copied
+ * first, then chunk i's rows of A are copied on a helper stream while the
+ * product of the previous chunk runs on `stream` and a second helper stream
+ * copies finished rows of C back (helper streams and events are created once
+ * per device and kept; no device memory is allocated). The caller provides
+ * and owns every buffer. Host buffers should be page-locked for the copies
+ * to be asynchronous; hC is valid once `stream` has been synchronised. Same
+ * return values as hgemm.
  */
 HGEMM_API int hgemm_host(const hgemm_half_t *hA, const hgemm_half_t *hB, hgemm_half_t *hC,
                int64_t M, int64_t N, int64_t K,

@@ -377,6 +377,35 @@ int dispatch(const hgemm_half_t* A, const hgemm_half_t* B, hgemm_half_t* C, int6
   }
 }
 
+// Helper streams and events of the host-buffer entry point, created once per
+// device and kept for the life of the process (no device memory).
+struct HostPipe {
+  bool ready = false;
+  cudaStream_t in = nullptr, out = nullptr;
+  static constexpr int kEvents = 2 + 2 * 16;
+  cudaEvent_t ev[kEvents] = {};
+};
+HostPipe g_pipes[kMaxDevices];
+std::mutex g_pipe_mu;
+
+int pipe_for_current_device(HostPipe** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= kMaxDevices) return HGEMM_ERR_UNSUPPORTED_DEVICE;
+  HostPipe& hp = g_pipes[dev];
+  if (!hp.ready) {
+    if ((e = cudaStreamCreateWithFlags(&hp.in, cudaStreamNonBlocking)) != cudaSuccess ||
+        (e = cudaStreamCreateWithFlags(&hp.out, cudaStreamNonBlocking)) != cudaSuccess)
+      return cuda_fail(e);
+    for (auto& ev : hp.ev)
+      if ((e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming)) != cudaSuccess) return cuda_fail(e);
+    hp.ready = true;
+  }
+  *out = &hp;
+  return HGEMM_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -401,14 +430,59 @@ int hgemm_host(const hgemm_half_t* hA, const hgemm_half_t* hB, hgemm_half_t* hC,
   DeviceState* dev = nullptr;
   if ((rc = current_device(&dev)) != HGEMM_OK) return rc;
   cudaError_t e;
-  if (M * K &&
-      (e = cudaMemcpyAsync(dA, hA, 2 * M * K, cudaMemcpyHostToDevice, stream)) != cudaSuccess)
+  // Row chunks of A and C pipeline the copies with the product: chunk i's
+  // rows of C are computed as soon as its rows of A (and all of B) have
+  // landed, while later rows of A are still arriving and earlier rows of C
+  // are copied back. Small problems take a single chunk.
+  const int64_t bytes = 2 * (M * K + N * K + M * N);
+  int64_t chunks = (bytes >= (int64_t{32} << 20) && M >= 2048) ? 8 : 1;
+  int64_t rows = (M + chunks - 1) / chunks;
+  rows = (rows + 255) / 256 * 256;
+  chunks = (M + rows - 1) / rows;
+  if (chunks <= 1) {
+    if (M * K &&
+        (e = cudaMemcpyAsync(dA, hA, 2 * M * K, cudaMemcpyHostToDevice, stream)) != cudaSuccess)
+      return cuda_fail(e);
+    if (N * K &&
+        (e = cudaMemcpyAsync(dB, hB, 2 * N * K, cudaMemcpyHostToDevice, stream)) != cudaSuccess)
+      return cuda_fail(e);
+    if ((rc = dispatch(dA, dB, dC, M, N, K, *dev, stream)) != HGEMM_OK) return rc;
+    if ((e = cudaMemcpyAsync(hC, dC, 2 * M * N, cudaMemcpyDeviceToHost, stream)) != cudaSuccess)
+      return cuda_fail(e);
+    return HGEMM_OK;
+  }
+  std::lock_guard<std::mutex> lock(g_pipe_mu);
+  HostPipe* hp = nullptr;
+  if ((rc = pipe_for_current_device(&hp)) != HGEMM_OK) return rc;
+  cudaEvent_t* ev = hp->ev;
+  // everything starts after the work already on `stream`
+  if ((e = cudaEventRecord(ev[0], stream)) != cudaSuccess ||
+      (e = cudaStreamWaitEvent(hp->in, ev[0], 0)) != cudaSuccess ||
+      (e = cudaStreamWaitEvent(hp->out, ev[0], 0)) != cudaSuccess)
     return cuda_fail(e);
-  if (N * K &&
-      (e = cudaMemcpyAsync(dB, hB, 2 * N * K, cudaMemcpyHostToDevice, stream)) != cudaSuccess)
+  if ((e = cudaMemcpyAsync(dB, hB, 2 * N * K, cudaMemcpyHostToDevice, hp->in)) != cudaSuccess)
     return cuda_fail(e);
-  if ((rc = dispatch(dA, dB, dC, M, N, K, *dev, stream)) != HGEMM_OK) return rc;
-  if ((e = cudaMemcpyAsync(hC, dC, 2 * M * N, cudaMemcpyDeviceToHost, stream)) != cudaSuccess)
+  for (int64_t i = 0; i < chunks; ++i) {
+    const int64_t r0 = i * rows;
+    const int64_t mi = (M - r0 < rows) ? M - r0 : rows;
+    cudaEvent_t in_done = ev[2 + 2 * i], prod_done = ev[3 + 2 * i];
+    if (K && (e = cudaMemcpyAsync(dA + r0 * K, hA + r0 * K, 2 * mi * K, cudaMemcpyHostToDevice,
+                                  hp->in)) != cudaSuccess)
+      return cuda_fail(e);
+    if ((e = cudaEventRecord(in_done, hp->in)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(stream, in_done, 0)) != cudaSuccess)
+      return cuda_fail(e);
+    if ((rc = dispatch(dA + r0 * K, dB, dC + r0 * N, mi, N, K, *dev, stream)) != HGEMM_OK) return rc;
+    if ((e = cudaEventRecord(prod_done, stream)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(hp->out, prod_done, 0)) != cudaSuccess)
+      return cuda_fail(e);
+    if ((e = cudaMemcpyAsync(hC + r0 * N, dC + r0 * N, 2 * mi * N, cudaMemcpyDeviceToHost,
+                             hp->out)) != cudaSuccess)
+      return cuda_fail(e);
+  }
+  // `stream` completes only after the last copy back
+  if ((e = cudaEventRecord(ev[1], hp->out)) != cudaSuccess ||
+      (e = cudaStreamWaitEvent(stream, ev[1], 0)) != cudaSuccess)
     return cuda_fail(e);
   return HGEMM_OK;
 }

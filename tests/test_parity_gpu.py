@@ -226,6 +226,29 @@ def test_host_entry_point_matches_device_entry_point():
     assert np.array_equal(hc.numpy().view(np.uint16), want.view(np.uint16))
 
 
+def test_host_entry_point_pipelined_chunks():
+    """Large enough to be pipelined over row chunks (ragged last chunk)."""
+    torch = torch_cuda()
+    M, N, K = 4100, 1024, 4096
+    a, b = synth.operands(M, N, K, seed=4100, kind="uniform")
+    ha = torch.from_numpy(a).pin_memory()
+    hb = torch.from_numpy(b).pin_memory()
+    hc = torch.full((M, N), float("nan"), dtype=torch.float16).pin_memory()
+    da = torch.empty_like(ha, device="cuda")
+    db = torch.empty_like(hb, device="cuda")
+    dc = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    s = torch.cuda.Stream()
+    for _ in range(2):  # twice: reused helper streams and events
+        tc.hgemm_host(ha, hb, hc, M, N, K, da, db, dc, s)
+        assert tc.hgemm_device_status(s) == tc.HGEMM_OK
+    c = hc.numpy()
+    assert not np.isnan(c.astype(np.float32)).any()
+    rng = np.random.default_rng(5)
+    rows = np.concatenate([rng.integers(0, M, 1500), [0, 767, 768, M - 1]])
+    cols = np.concatenate([rng.integers(0, N, 1500), [0, 1, N - 1, 512]])
+    assert_close(c[rows, cols], oracle.entries(a, b, rows, cols), what="pipelined host call")
+
+
 def test_side_stream_and_repeatability():
     torch = torch_cuda()
     a, b, spec = synth.workload("hgemm_2048")
