@@ -105,9 +105,22 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_sources_sha():
+# The source file of each kernel; with the shared headers and the build
+# flags it determines the compiled kernel, so a recorded ncu traffic figure
+# stays valid while their hash is unchanged.
+KERNEL_SOURCES = {"hgemm_tc_kernel": "hgemm_tc.cu", "hgemm_tc2_kernel": "hgemm_tc2.cu",
+                  "hgemm_tc2w_kernel": "hgemm_tc2w.cu", "hgemm_skinny_kernel": "hgemm_skinny.cu",
+                  "hgemm_generic_kernel": "hgemm_generic.cu"}
+SHARED_SOURCES = ["internal.h", "kernel_common.cuh", "ptx.cuh"]
+
+
+def kernel_sources_sha(kernel):
     h = hashlib.sha256()
-    files = sorted(glob.glob(os.path.join(ROOT, "tensor_core_dense_fp16_gb300", "csrc", "*")))
+    pkg = os.path.join(ROOT, "tensor_core_dense_fp16_gb300")
+    files = [os.path.join(pkg, "csrc", n) for n in SHARED_SOURCES]
+    if kernel in KERNEL_SOURCES:
+        files.append(os.path.join(pkg, "csrc", KERNEL_SOURCES[kernel]))
+    files.append(os.path.join(pkg, "build.py"))
     for f in files:
         h.update(os.path.basename(f).encode())
         with open(f, "rb") as fh:
@@ -270,7 +283,7 @@ def run_reference(args, spec, a, b, world, rank):
     if rank != 0:
         return 0
     nthreads = os.cpu_count() or 1
-    per_step = max(0.5, args.reference_seconds / max(1, args.steps + args.warmup))
+    per_step = max(0.05, args.reference_seconds / max(1, args.steps + args.warmup))
     import oracle
     oracle.build()
     N, K = spec["N"], spec["K"]
@@ -401,7 +414,7 @@ def run_ours(args, spec, a, b, world, rank, local):
               tc.HGEMM_PATH_GENERIC: "hgemm_generic_kernel"}.get(path, f"path {path}")
     ai = flops / bytes_of(spec)
     ridge = peaks["bf16_tflops"] * FP16_PER_BF16 * 1e12 / (peaks["hbm_gbs"] * 1e9)
-    sha = kernel_sources_sha()
+    sha = kernel_sources_sha(kernel)
     traffic = profiled_traffic(kernel, args.workload, sha)
     if ai >= ridge:
         peak = peaks["bf16_tflops"] * FP16_PER_BF16

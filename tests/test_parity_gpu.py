@@ -146,6 +146,23 @@ def test_edges_generic_path(M, N, K):
     assert_close(run_gpu(a, b, path=tc.HGEMM_PATH_GENERIC), ref, what=f"generic {M}x{N}x{K}")
 
 
+@pytest.mark.parametrize("M,N,K", [(3_000_001, 8, 8), (136, 600_000, 16)])
+def test_very_tall_and_very_wide_outputs(M, N, K):
+    """Millions of rows (or columns): tile counts far beyond one wave."""
+    a, b = synth.operands(M, N, K, seed=M % 1000 + N % 1000, kind="uniform")
+    ref = oracle.hgemm(a, b, nthreads=oracle_threads())
+    assert_close(run_gpu(a, b), ref, what=f"{M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("path", [None, tc.HGEMM_PATH_TC_PAIR])
+def test_very_long_k(path):
+    """K = 32768: 512 K blocks accumulated in one TMEM accumulator."""
+    M, N, K = 256, 264, 32768
+    a, b = synth.operands(M, N, K, seed=32768, kind="uniform")
+    ref = oracle.hgemm(a, b, nthreads=oracle_threads())
+    assert_close(run_gpu(a, b, path=path), ref, what=f"long K path {path}")
+
+
 def test_misaligned_pointers_take_the_generic_path():
     torch = torch_cuda()
     M, N, K = 130, 72, 96
