@@ -168,7 +168,9 @@ int choose_tma_path(int64_t M, int64_t N, int64_t K, const DeviceProfile& dev, i
     }
     return HGEMM_PATH_TC_PAIR;
   }
-  const int s = best_split(true);
+  // Exchanging the partial sums costs a few microseconds; splitting pays
+  // when each pair would otherwise walk a long K (48 blocks or more).
+  const int s = num_kb >= 48 ? best_split(true) : 1;
   if (s > 1) {
     *split = s;
     return HGEMM_PATH_SKINNY;
@@ -264,12 +266,6 @@ int run_tc(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t 
 
 int run_tc_pair(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
                 const DeviceState& dev, cudaStream_t stream) {
-  CUtensorMap ma, mb, mbh, mc;
-  int rc;
-  if ((rc = encode_map(&ma, A, M, K, hg::kTcBM, hg::kTcBK)) != HGEMM_OK) return rc;
-  if ((rc = encode_map(&mb, B, N, K, hg::kPairBN / 2, hg::kTcBK)) != HGEMM_OK) return rc;
-  if ((rc = encode_map(&mbh, B, N, K, hg::kPairBN / 4, hg::kTcBK)) != HGEMM_OK) return rc;
-  if ((rc = encode_map(&mc, C, M, N, hg::kEpiRows, hg::kEpiCols)) != HGEMM_OK) return rc;
   hg::TcArgs args{};
   args.M = static_cast<int>(M);
   args.N = static_cast<int>(N);
@@ -278,21 +274,38 @@ int run_tc_pair(const void* A, const void* B, void* C, int64_t M, int64_t N, int
   args.num_n = static_cast<int>((N + hg::kPairBN - 1) / hg::kPairBN);
   args.num_kb = static_cast<int>((K + hg::kTcBK - 1) / hg::kTcBK);
   const int64_t tiles = static_cast<int64_t>(args.num_m) * args.num_n;
-  if (tiles > 0x3FFFFFFF) return HGEMM_ERR_INVALID_ARG;
+  if (tiles > 0x1FFFFFFF) return HGEMM_ERR_INVALID_ARG;
   const int64_t clusters = hg::pair_max_clusters(dev.num_sms);
-  // Tail of the last wave: if at most half of the clusters would get a tile
-  // in it, cut those tiles into two 128-column halves.
+  // Last (or only) wave: if its tiles leave at least half of the clusters
+  // idle, cut them into 128-column parts, or 64-column ones when even those
+  // leave half idle and the tiles' columns reach past 128 of them.
   const int64_t full_waves = tiles / clusters;
   const int64_t rest = tiles - full_waves * clusters;
-  const bool halve = tail_split_setting() && full_waves > 0 && rest > 0 && 2 * rest <= clusters;
-  args.full_tiles = static_cast<int>(halve ? tiles - rest : tiles);
-  args.num_tiles = static_cast<int>(halve ? tiles + rest : tiles);
+  int parts = 1;
+  if (tail_split_setting() && rest > 0 && 2 * rest <= clusters) {
+    parts = 2;
+    const int64_t last_cols = N - static_cast<int64_t>(args.num_n - 1) * hg::kPairBN;
+    if (4 * rest <= clusters && (args.num_n > 1 || last_cols > 128)) parts = 4;
+  }
+  args.part_cols = hg::kPairBN / parts;
+  args.full_tiles = static_cast<int>(parts > 1 ? tiles - rest : tiles);
+  // stages hold whole-tile operands, or a part's when every unit is a part
+  args.stage_bytes = hg::kTcBM * hg::kTcBK * 2 +
+                     (args.full_tiles > 0 ? hg::kPairBN / 2 : args.part_cols / 2) * hg::kTcBK * 2;
+  args.stages = hg::kPairRingBytes / args.stage_bytes;
+  args.num_tiles = static_cast<int>(parts > 1 ? tiles - rest + parts * rest : tiles);
   args.group_m = group_m_setting();
   args.grid = static_cast<int>(2 * (args.num_tiles < clusters ? args.num_tiles : clusters));
   args.status = dev.status;
   args.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
   args.inject = g_inject.load(std::memory_order_relaxed);
-  cudaError_t e = hg::launch_tc_pair(ma, mb, mbh, mc, args, stream);
+  CUtensorMap ma, mb, mbp, mc;
+  int rc;
+  if ((rc = encode_map(&ma, A, M, K, hg::kTcBM, hg::kTcBK)) != HGEMM_OK) return rc;
+  if ((rc = encode_map(&mb, B, N, K, hg::kPairBN / 2, hg::kTcBK)) != HGEMM_OK) return rc;
+  if ((rc = encode_map(&mbp, B, N, K, args.part_cols / 2, hg::kTcBK)) != HGEMM_OK) return rc;
+  if ((rc = encode_map(&mc, C, M, N, hg::kEpiRows, hg::kEpiCols)) != HGEMM_OK) return rc;
+  cudaError_t e = hg::launch_tc_pair(ma, mb, mbp, mc, args, stream);
   return e == cudaSuccess ? HGEMM_OK : cuda_fail(e);
 }
 

@@ -273,7 +273,7 @@ __global__ void __launch_bounds__(192, 1)
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
-    if (lane == 0) bulk_wait_group<0>();
+    if (lane == 0) bulk_wait_group_read<0>();  // staging read; the writes finish with the grid
     __syncwarp();
   }
 

@@ -19,11 +19,15 @@
 //     single-CTA kernel (tcgen05.ld, round to nearest even, swizzled staging,
 //     clipped TMA stores).
 // Per SM, a stage is 32 KB instead of 48 KB for the same MMA work, which
-// allows six stages in flight and halves each SM's share of B traffic.
+// allows six stages in flight and halves each SM's share of B traffic. When
+// every unit of a launch is a tile part, a stage shrinks to the part's bytes
+// (24 or 20 KB) and the same ring holds eight or nine of them: an SM takes
+// in at most ~112 GB/s, so more bytes in flight are what hides DRAM latency.
 //
-// Wave tail: when the tiles do not fill the last wave of clusters, the tiles
-// of that wave are cut into two 256×128 halves (N=128 pair MMAs) so that
-// twice as many clusters share them and the tail lasts half a tile.
+// Wave tail: when the tiles do not fill the last wave of clusters (or the
+// only one), the tiles of that wave are cut into parts of 128 or 64 columns
+// (N=128 or N=64 pair MMAs) so that two or four times as many clusters share
+// them and the wave lasts a half or a quarter of a tile.
 //
 // Serpentine K: rounds of tiles alternate the direction in which they walk
 // K, so each round starts on operand blocks that the previous round read
@@ -37,85 +41,90 @@
 namespace hg {
 namespace {
 
-template <int STAGES_>
+template <int MAX_STAGES_>
 struct PairCfg {
   static constexpr int BM = 2 * kTcBM;   // cluster tile rows
   static constexpr int BN = kPairBN;     // cluster tile columns
   static constexpr int ROWS = kTcBM;     // A rows per CTA
   static constexpr int BROWS = BN / 2;   // B rows (tile columns) per CTA
   static constexpr int BK = kTcBK;
-  static constexpr int STAGES = STAGES_;
+  static constexpr int MAX_STAGES = MAX_STAGES_;
   static constexpr int UMMA_K = 16;
   static constexpr int A_BYTES = ROWS * BK * 2;
   static constexpr int B_BYTES = BROWS * BK * 2;
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // landed in each CTA
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // whole tiles: landed in each CTA
   static constexpr int TX_BYTES = 2 * STAGE_BYTES;          // expected by the even CTA
+  static constexpr int RING_BYTES = kPairRingBytes;         // six whole-tile stages
+  static_assert(RING_BYTES == 6 * STAGE_BYTES, "the ring holds six whole-tile stages");
   static constexpr int EPI_WARPS = 4;
   static constexpr int C_BOX_BYTES = kEpiRows * kEpiCols * 2;
   static constexpr int C_BUFS = 2;
   static constexpr int C_BYTES = EPI_WARPS * C_BUFS * C_BOX_BYTES;
   static constexpr int ACC_COLS = BN;
   static constexpr int TMEM_COLS = 2 * ACC_COLS;
-  static constexpr int OFF_A = 0;
-  static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
-  static constexpr int OFF_C = OFF_B + STAGES * B_BYTES;
+  static constexpr int OFF_RING = 0;                        // stage s: A, then B
+  static constexpr int OFF_C = OFF_RING + RING_BYTES;
   static constexpr int OFF_BAR = OFF_C + C_BYTES;
-  static constexpr int NUM_BARS = 2 * STAGES + 4 + 1;
+  static constexpr int NUM_BARS = 2 * MAX_STAGES + 4 + 1;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
   static constexpr int THREADS = 192;
   static constexpr uint32_t IDESC = idesc_f16_f32acc(BM, BN);
-  static constexpr uint32_t IDESC_HALF = idesc_f16_f32acc(BM, BN / 2);
-  static constexpr int TX_BYTES_HALF = 2 * (A_BYTES + B_BYTES / 2);
 
   static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "1024-byte aligned stages");
+  static_assert(RING_BYTES / (A_BYTES + 32 * BK * 2) <= MAX_STAGES, "barriers for the narrowest stages");
   static_assert(TMEM_COLS == 512, "two 256-column FP32 accumulators");
   static_assert(SMEM_BYTES <= 232448, "exceeds 227 KB of shared memory per CTA");
 };
 
-// Work unit t: a whole 256×256 tile below p.full_tiles, else one 128-column
-// half of a tile (two consecutive units per tile), in raster order.
+// Work unit t: a whole 256×256 tile below p.full_tiles, else one part of
+// p.part_cols (128 or 64) columns of a tile (256 / part_cols consecutive
+// units per tile), in raster order.
 struct PairTile {
   int mb, nb;
   int n0;     // first column of C
-  int ncols;  // 256 or 128
+  int ncols;  // 256, 128 or 64
 };
 
 __device__ __forceinline__ PairTile pair_tile(int t, const TcArgs& p) {
   PairTile w;
-  int whole = t, half = -1;
+  int whole = t, part = -1;
   if (t >= p.full_tiles) {
+    const int parts = kPairBN / p.part_cols;
     const int h = t - p.full_tiles;
-    whole = p.full_tiles + (h >> 1);
-    half = h & 1;
+    whole = p.full_tiles + h / parts;
+    part = h - (h / parts) * parts;
   }
   tile_coords(whole, p.num_m, p.num_n, p.group_m, w.mb, w.nb);
-  w.n0 = w.nb * kPairBN + (half < 0 ? 0 : half * (kPairBN / 2));
-  w.ncols = half < 0 ? kPairBN : kPairBN / 2;
+  w.n0 = w.nb * kPairBN + (part < 0 ? 0 : part * p.part_cols);
+  w.ncols = part < 0 ? kPairBN : p.part_cols;
   return w;
 }
 
-template <int STAGES>
+template <int MAX_STAGES>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     hgemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmBh, const __grid_constant__ CUtensorMap tmC,
                      const TcArgs p) {
-  using Cfg = PairCfg<STAGES>;
+  using Cfg = PairCfg<MAX_STAGES>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t sA = sbase + Cfg::OFF_A;
-  const uint32_t sB = sbase + Cfg::OFF_B;
+  // ring geometry of this launch: p.stages stages of p.stage_bytes (A first)
+  const int STAGES = p.stages;
+  const uint32_t stage_bytes = static_cast<uint32_t>(p.stage_bytes);
+  const uint32_t sA = sbase + Cfg::OFF_RING;
+  const uint32_t sB = sA + Cfg::A_BYTES;
   const uint32_t bar0 = sbase + Cfg::OFF_BAR;
-  const uint32_t drain_bar = bar0 + 8 * (2 * STAGES + 4);
+  const uint32_t drain_bar = bar0 + 8 * (2 * MAX_STAGES + 4);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::OFF_MISC + 4);
 
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
-  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
-  auto accf_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
-  auto acce_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (MAX_STAGES + s); };
+  auto accf_bar = [&](int b) { return bar0 + 8u * (2 * MAX_STAGES + b); };
+  auto acce_bar = [&](int b) { return bar0 + 8u * (2 * MAX_STAGES + 2 + b); };
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -164,8 +173,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
         const bool whole = w.ncols == Cfg::BN;
         const int ya = w.mb * Cfg::BM + static_cast<int>(rank) * Cfg::ROWS;
         const int yb = w.n0 + static_cast<int>(rank) * (w.ncols / 2);
-        const CUtensorMap* mapb = whole ? &tmB : &tmBh;
-        const uint32_t tx = whole ? Cfg::TX_BYTES : Cfg::TX_BYTES_HALF;
+        const CUtensorMap* mapb = whole ? &tmB : &tmBh;  // tmBh: part_cols / 2 rows per CTA
+        const uint32_t tx = whole ? Cfg::TX_BYTES : 2u * (Cfg::A_BYTES + (w.ncols / 2) * Cfg::BK * 2);
         // serpentine K: every other round of tiles walks K backwards, so it
         // starts on the K blocks the previous round read last (still in L2)
         const bool reverse = (((t - cluster_id) / num_clusters) & 1) != 0;
@@ -178,8 +187,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
           const uint32_t fb = mapa_shared(full_bar(stage), 0);
           if (rank == 0 && !(p.inject == 1 && issued == 0))  // testing aid: withhold one arrival
             mbar_arrive_expect_tx(full_bar(stage), tx);
-          tma_load_2d_cg2(sA + stage * Cfg::A_BYTES, &tmA, fb, kb * Cfg::BK, ya);
-          tma_load_2d_cg2(sB + stage * Cfg::B_BYTES, mapb, fb, kb * Cfg::BK, yb);
+          tma_load_2d_cg2(sA + stage * stage_bytes, &tmA, fb, kb * Cfg::BK, ya);
+          tma_load_2d_cg2(sB + stage * stage_bytes, mapb, fb, kb * Cfg::BK, yb);
           ++issued;
           if (++stage == STAGES) {
             stage = 0;
@@ -216,7 +225,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
       uint32_t acc_phase = 0;
       bool ok = true;
       for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters) {
-        const uint32_t idesc = t < p.full_tiles ? Cfg::IDESC : Cfg::IDESC_HALF;
+        const uint32_t idesc = t < p.full_tiles ? Cfg::IDESC : idesc_f16_f32acc(Cfg::BM, p.part_cols);
         if (!wait_phase_cluster(acce_bar(acc), acc_phase ^ 1u, wd, kWdMmaAccEmpty)) {
           ok = false;
           break;
@@ -229,8 +238,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
             break;
           }
           tc_fence_after_sync();
-          const uint64_t a_desc = sdesc_kmajor_sw128(sA + stage * Cfg::A_BYTES);
-          const uint64_t b_desc = sdesc_kmajor_sw128(sB + stage * Cfg::B_BYTES);
+          const uint64_t a_desc = sdesc_kmajor_sw128(sA + stage * stage_bytes);
+          const uint64_t b_desc = sdesc_kmajor_sw128(sB + stage * stage_bytes);
 #pragma unroll
           for (int k = 0; k < Cfg::BK / Cfg::UMMA_K; ++k)
             // kb counts the tile's K steps in load order (the producer may walk
@@ -310,7 +319,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
-    if (lane == 0) bulk_wait_group<0>();
+    if (lane == 0) bulk_wait_group_read<0>();  // staging read; the writes finish with the grid
     __syncwarp();
   }
 
@@ -321,7 +330,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
   if (warp == 1) tmem_dealloc_cg2(tmem_base, Cfg::TMEM_COLS);
 }
 
-constexpr int kPairStages = 6;
+constexpr int kPairStages = 10;  // barriers for up to ten stages (the ring holds six to nine)
 
 }  // namespace
 
@@ -347,7 +356,7 @@ int pair_max_clusters(int num_sms) {
   return n;
 }
 
-cudaError_t launch_tc_pair(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b_half,
+cudaError_t launch_tc_pair(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b_part,
                            const CUtensorMap& c, const TcArgs& args, cudaStream_t stream) {
   using Cfg = PairCfg<kPairStages>;
   static bool attr_done[64] = {};
@@ -365,7 +374,7 @@ cudaError_t launch_tc_pair(const CUtensorMap& a, const CUtensorMap& b, const CUt
   cfg.blockDim = dim3(Cfg::THREADS);
   cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
   cfg.stream = stream;
-  return cudaLaunchKernelEx(&cfg, kern, a, b, b_half, c, args);
+  return cudaLaunchKernelEx(&cfg, kern, a, b, b_part, c, args);
 }
 
 }  // namespace hg

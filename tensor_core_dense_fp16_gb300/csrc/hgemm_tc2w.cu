@@ -278,7 +278,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
       }
       tile_phase ^= 1u;
     }
-    if (lane == 0) bulk_wait_group<0>();
+    if (lane == 0) bulk_wait_group_read<0>();  // staging read; the writes finish with the grid
     __syncwarp();
   }
 

@@ -24,9 +24,11 @@ enum WatchdogCode : int {
 struct TcArgs {
   int M, N, K;
   int num_m, num_n, num_kb;  // tiles along M and N, 64-wide K blocks
-  int num_tiles;             // work units: full tiles, then half tiles
+  int num_tiles;             // work units: whole tiles, then tile parts
   int full_tiles;            // units below this index are whole tiles; the rest are
-                             // 128-column halves of the last tiles (pair kernel)
+                             // parts of part_cols columns of the last tiles (pair kernel)
+  int part_cols;             // 128 or 64
+  int stages, stage_bytes;   // operand ring geometry (pair kernel)
   int group_m;               // rasterisation group height (in M tiles)
   int grid;                  // persistent CTAs
   int* status;               // device watchdog word
@@ -48,8 +50,8 @@ struct PlainArgs {
 // error, if any). Shared-memory attributes are set on first use per device.
 cudaError_t launch_tc_128x256(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
                               const TcArgs& args, cudaStream_t stream);
-// b_half: the B map with 64-row boxes, for the half tiles of the last wave.
-cudaError_t launch_tc_pair(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b_half,
+// b_part: the B map with part_cols / 2-row boxes, for the tile parts of the last wave.
+cudaError_t launch_tc_pair(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b_part,
                            const CUtensorMap& c, const TcArgs& args, cudaStream_t stream);
 // Largest number of co-resident 2-CTA clusters of the pair kernel.
 int pair_max_clusters(int num_sms);
@@ -89,6 +91,7 @@ constexpr int kTcBM = 128;
 constexpr int kTcBN = 256;
 constexpr int kTcBK = 64;
 constexpr int kPairBN = 256;   // pair kernel: 256×256 tiles, 128 B rows per CTA
+constexpr int kPairRingBytes = 6 * 32768;  // pair kernel: six whole-tile stages of A and B
 constexpr int kEpiRows = 32;   // rows of one staged C box (one epilogue warp)
 constexpr int kEpiCols = 64;   // columns of one staged C box (128 bytes)
 

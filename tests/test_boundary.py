@@ -74,10 +74,16 @@ def test_path_selection(lib):
     # fewer: 256x256 pair tiles
     assert sel(A16, B16, C16, 2048, 2048, 2048) == tc.HGEMM_PATH_TC_PAIR
     assert sel(A16, B16, C16, 4096, 2048, 1024) == tc.HGEMM_PATH_TC_PAIR
-    # few tiles and a long K: split K over clusters of pairs
+    # few tiles and a long K (48 K blocks or more): split K over clusters of pairs
     assert sel(A16, B16, C16, 4096, 256, 4096) == tc.HGEMM_PATH_SKINNY
-    assert sel(A16, B16, C16, 1000, 1000, 1000) == tc.HGEMM_PATH_SKINNY
-    assert sel(A16, B16, C16, 256, 256, 256) == tc.HGEMM_PATH_SKINNY
+    assert sel(A16, B16, C16, 512, 512, 3072) == tc.HGEMM_PATH_SKINNY
+    # a shorter K is not worth the exchange of partial sums: 256-wide pair
+    # tiles cut into 128- or 64-column parts
+    assert sel(A16, B16, C16, 1000, 1000, 1000) == tc.HGEMM_PATH_TC_PAIR
+    assert sel(A16, B16, C16, 256, 256, 256) == tc.HGEMM_PATH_TC_PAIR
+    assert sel(A16, B16, C16, 4096, 256, 2048) == tc.HGEMM_PATH_TC_PAIR
+    # more than half of the pairs busy without splitting: no split
+    assert sel(A16, B16, C16, 256 * 39, 256, 4096) == tc.HGEMM_PATH_TC_PAIR
     # too little K to split: one K block
     assert sel(A16, B16, C16, 4096, 256, 64) == tc.HGEMM_PATH_TC_PAIR
     assert sel(A16, B16, C16, 128, 256, 64) == tc.HGEMM_PATH_TC
@@ -116,7 +122,7 @@ def test_forced_paths(lib):
             tc.hgemm_force_path(77)
     finally:
         tc.hgemm_force_path(-1)
-    assert tc.hgemm_select_path(A16, B16, C16, 256, 256, 256) == tc.HGEMM_PATH_SKINNY
+    assert tc.hgemm_select_path(A16, B16, C16, 256, 256, 256) == tc.HGEMM_PATH_TC_PAIR
 
 
 def test_invalid_arguments_rejected_before_any_device_work(lib):

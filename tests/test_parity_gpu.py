@@ -282,6 +282,72 @@ def test_side_stream_and_repeatability():
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
 
 
+# Tiles (of 256×256) for which the forced split-K path takes each slice count
+# S: the most slices whose clusters of 2·S CTAs all fit on the GPU at once
+# (15 clusters of 8, 23 of 6 and 36 of 4 CTAs on GB300).
+SPLIT_TILES = {4: 15, 3: 23, 2: 36}
+
+
+@pytest.mark.parametrize("split", sorted(SPLIT_TILES))
+def test_split_k_every_slice_count(split):
+    """Ragged M, N and K; 2·S+1 K blocks, so slices hold 2 or 3 blocks and
+    (for S = 3) the owned column ranges are uneven."""
+    tiles = SPLIT_TILES[split]
+    M, N, K = 256 * tiles - 13, 248, 64 * (2 * split) + 24
+    a, b = synth.operands(M, N, K, seed=500 + split, kind="uniform")
+    ref = oracle.hgemm(a, b, nthreads=oracle_threads())
+    assert_close(run_gpu(a, b, path=tc.HGEMM_PATH_SKINNY), ref, what=f"split {split}")
+
+
+@pytest.mark.parametrize("M,N,K", [(1000, 1000, 1000), (256, 256, 256), (300, 136, 2048),
+                                   (4096, 256, 2048), (600, 2000, 512)])
+def test_pair_tile_parts(M, N, K):
+    """One partial wave of tiles cut into 128- or 64-column parts."""
+    a, b = synth.operands(M, N, K, seed=M + 3 * N + 7 * K, kind="uniform")
+    ref = oracle.hgemm(a, b, nthreads=oracle_threads())
+    assert_close(run_gpu(a, b, path=tc.HGEMM_PATH_TC_PAIR), ref, what=f"parts {M}x{N}x{K}")
+
+
+def test_split_k_alternating_streams():
+    """Alternating streams with different operands on the split-K path."""
+    torch = torch_cuda()
+    M, N, K = 4096, 256, 4096
+    ops = [synth.operands(M, N, K, seed=900 + i, kind="uniform") for i in range(2)]
+    refs = [oracle.hgemm(a, b, nthreads=oracle_threads()) for a, b in ops]
+    dev = [(to_device(a), to_device(b)) for a, b in ops]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    torch.cuda.synchronize()
+    outs = []
+    for i in range(8):
+        da, db = dev[i % 2]
+        s = streams[(i // 2) % 2]
+        dc = torch.empty((M, N), dtype=torch.float16, device="cuda")
+        with torch.cuda.stream(s):
+            tc.hgemm(da, db, dc, M, N, K, s)
+        outs.append((i % 2, dc, s))
+    torch.cuda.synchronize()
+    assert tc.hgemm_device_status() == tc.HGEMM_OK
+    for which, dc, _ in outs:
+        assert_close(dc.cpu().numpy(), refs[which], what=f"operands {which}")
+
+
+def test_split_k_results_are_bit_identical_across_launches():
+    """Partial sums are added in slice order, whatever order slices finish in."""
+    torch = torch_cuda()
+    a, b, spec = synth.workload("hgemm_4096x256x4096_skinny")
+    M, N, K = spec["M"], spec["N"], spec["K"]
+    da, db = to_device(a), to_device(b)
+    first = None
+    for _ in range(20):
+        dc = torch.empty((M, N), dtype=torch.float16, device="cuda")
+        tc.hgemm(da, db, dc, M, N, K)
+        if first is None:
+            first = dc
+        else:
+            assert torch.equal(dc, first)
+    assert tc.hgemm_device_status() == tc.HGEMM_OK
+
+
 def test_unsupported_arguments_raise():
     torch = torch_cuda()
     a = torch.ones((4, 8), dtype=torch.float16, device="cuda")
