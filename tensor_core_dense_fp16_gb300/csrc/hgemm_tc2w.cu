@@ -20,9 +20,12 @@
 //   * the even CTA issues, per K step, two tcgen05.mma.cta_group::2 (M=256,
 //     N=256, K=16), one per column half, into two FP32 accumulators that
 //     together fill TMEM (2×256 columns);
-//   * the epilogue drains half 0, releases it, then drains half 1; the next
-//     tile's MMAs for a half start as soon as that half is released, so half
-//     of the epilogue overlaps the next tile's main loop;
+//   * eight epilogue warps drain the two halves at once (warps 2..5 half 0,
+//     warps 6..9 half 1, one TMEM lane quadrant each) and release each half
+//     as soon as it is read; the next tile's MMAs for a half start then. The
+//     whole 512-column accumulator fills TMEM, so this drain is the only
+//     pause of the tensor cores between tiles, and two warps per quadrant
+//     halve it (measured: +0.5% at 8192³, +1.6% at 4096³);
 //   * serpentine K, epilogue, edges and watchdog as in hgemm_tc2.cu.
 #include <cuda_fp16.h>
 
@@ -46,9 +49,9 @@ struct WideCfg {
   static constexpr int B_BYTES = 2 * BH_BYTES;           // 32 KB
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 48 KB landed in each CTA
   static constexpr int TX_BYTES = 2 * STAGE_BYTES;        // expected by the even CTA
-  static constexpr int EPI_WARPS = 4;
+  static constexpr int EPI_WARPS = 8;  // four per column half
   static constexpr int C_BOX_BYTES = kEpiRows * kEpiCols * 2;
-  static constexpr int C_BUFS = 2;
+  static constexpr int C_BUFS = 1;
   static constexpr int C_BYTES = EPI_WARPS * C_BUFS * C_BOX_BYTES;
   static constexpr int HALF_COLS = kPairBN;              // TMEM columns per half
   static constexpr int TMEM_COLS = 2 * HALF_COLS;
@@ -60,7 +63,7 @@ struct WideCfg {
   static constexpr int NUM_BARS = 2 * STAGES + 1 + 2 + 1;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
-  static constexpr int THREADS = 192;
+  static constexpr int THREADS = 320;
   static constexpr uint32_t IDESC = idesc_f16_f32acc(BM, kPairBN);
 
   static_assert(A_BYTES % 1024 == 0 && BH_BYTES % 1024 == 0, "1024-byte aligned stages");
@@ -68,7 +71,7 @@ struct WideCfg {
   static_assert(SMEM_BYTES <= 232448, "exceeds 227 KB of shared memory per CTA");
 };
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
     hgemm_tc2w_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const __grid_constant__ CUtensorMap tmC, const TcArgs p) {
   using Cfg = WideCfg;
@@ -102,8 +105,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
       mbar_init(empty_bar(s), 1);  // multicast tcgen05.commit
     }
     mbar_init(accf_bar, 1);                          // multicast tcgen05.commit per tile
-    mbar_init(acce_bar(0), 2 * Cfg::EPI_WARPS);      // every epilogue warp of the pair
-    mbar_init(acce_bar(1), 2 * Cfg::EPI_WARPS);
+    mbar_init(acce_bar(0), Cfg::EPI_WARPS);          // the pair's four warps of each half
+    mbar_init(acce_bar(1), Cfg::EPI_WARPS);
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -221,10 +224,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------ epilogue (both CTAs)
+    // warps 2..5 drain column half 0, warps 6..9 half 1, concurrently
     const int q = warp & 3;
-    uint8_t* cbuf_base = smem + Cfg::OFF_C + q * Cfg::C_BUFS * Cfg::C_BOX_BYTES;
+    const int h = (warp - 2) >> 2;
+    uint8_t* buf = smem + Cfg::OFF_C + (warp - 2) * Cfg::C_BOX_BYTES;
     uint32_t tile_phase = 0;
-    int cb = 0;
     for (int t = cluster_id; t < p.num_tiles; t += num_clusters) {
       int mb, nb;
       tile_coords(t, p.num_m, p.num_n, p.group_m, mb, nb);
@@ -234,46 +238,42 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
       if (!ok) break;
       tc_fence_after_sync();
       const int y0 = mb * Cfg::BM + static_cast<int>(rank) * Cfg::ROWS + q * kEpiRows;
-      for (int h = 0; h < 2; ++h) {
-        const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                               static_cast<uint32_t>(h * Cfg::HALF_COLS);
-        constexpr int chunks = kPairBN / kEpiCols;
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                             static_cast<uint32_t>(h * Cfg::HALF_COLS);
+      constexpr int chunks = kPairBN / kEpiCols;
 #pragma unroll 1
-        for (int c = 0; c < chunks; ++c) {
-          uint32_t v0[32], v1[32];
-          tmem_ld_32x32b_x32(t_row + c * kEpiCols, v0);
-          tmem_ld_32x32b_x32(t_row + c * kEpiCols + 32, v1);
-          tmem_ld_wait(v0);
-          tmem_ld_wait(v1);
-          if (c == chunks - 1) {
-            // half h has been read: the next tile's MMAs may overwrite it
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(mapa_shared(acce_bar(h), 0));
-          }
-          const int x0 = nb * Cfg::BN + h * kPairBN + c * kEpiCols;
-          if (x0 >= p.N || y0 >= p.M) continue;
-          if (lane == 0) bulk_wait_group_read<1>();
+      for (int c = 0; c < chunks; ++c) {
+        uint32_t v0[32], v1[32];
+        tmem_ld_32x32b_x32(t_row + c * kEpiCols, v0);
+        tmem_ld_32x32b_x32(t_row + c * kEpiCols + 32, v1);
+        tmem_ld_wait(v0);
+        tmem_ld_wait(v1);
+        if (c == chunks - 1) {
+          // half h has been read: the next tile's MMAs may overwrite it
+          tc_fence_before_sync();
           __syncwarp();
-          uint8_t* buf = cbuf_base + cb * Cfg::C_BOX_BYTES;
-          uint8_t* row = buf + lane * 128;
+          if (lane == 0) mbar_arrive_cluster(mapa_shared(acce_bar(h), 0));
+        }
+        const int x0 = nb * Cfg::BN + h * kPairBN + c * kEpiCols;
+        if (x0 >= p.N || y0 >= p.M) continue;
+        if (lane == 0) bulk_wait_group_read<0>();  // the previous store has read the box
+        __syncwarp();
+        uint8_t* row = buf + lane * 128;
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const uint32_t* v = (j < 4) ? (v0 + 8 * j) : (v1 + 8 * (j - 4));
-            uint4 pk;
-            pk.x = pack_half2(v[0], v[1]);
-            pk.y = pack_half2(v[2], v[3]);
-            pk.z = pack_half2(v[4], v[5]);
-            pk.w = pack_half2(v[6], v[7]);
-            *reinterpret_cast<uint4*>(row + ((j ^ (lane & 7)) << 4)) = pk;
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_2d(&tmC, smem_u32(buf), x0, y0);
-            bulk_commit_group();
-          }
-          cb ^= 1;
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t* v = (j < 4) ? (v0 + 8 * j) : (v1 + 8 * (j - 4));
+          uint4 pk;
+          pk.x = pack_half2(v[0], v[1]);
+          pk.y = pack_half2(v[2], v[3]);
+          pk.z = pack_half2(v[4], v[5]);
+          pk.w = pack_half2(v[6], v[7]);
+          *reinterpret_cast<uint4*>(row + ((j ^ (lane & 7)) << 4)) = pk;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&tmC, smem_u32(buf), x0, y0);
+          bulk_commit_group();
         }
       }
       tile_phase ^= 1u;
