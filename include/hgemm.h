@@ -140,9 +140,21 @@ HGEMM_API int hgemm_select_path(const void *A, const void *B, const void *C,
  * HGEMM_GROUP_M (a positive integer) sets how many M-tiles the tensor-core
  * kernels' grouped raster order keeps together (default 12);
  * HGEMM_TAIL_SPLIT=0 keeps whole 256×256 tiles in the last, partly filled
- * wave of the CTA-pair kernel instead of cutting them into halves.
+ * wave of the CTA-pair kernel instead of cutting them into 128- or
+ * 64-column parts.
  */
 HGEMM_API int hgemm_force_path(int path);
+
+/*
+ * hgemm_force_split — testing aid for the split-K path (HGEMM_PATH_SKINNY):
+ * later calls that take that path use `split` K-slices over tiles `tile_n`
+ * columns wide, when that configuration's clusters fit on the device at once
+ * and K has at least `split` blocks of 64 (otherwise the automatic choice
+ * stands). Configurations: (2, 128), (2, 256), (3, 256), (4, 256); (0, 0)
+ * restores the automatic choice. Returns HGEMM_OK or HGEMM_ERR_INVALID_ARG.
+ * Pure host state, process-wide.
+ */
+HGEMM_API int hgemm_force_split(int split, int tile_n);
 
 /*
  * hgemm_device_status — synchronises `stream`, then reads and clears the

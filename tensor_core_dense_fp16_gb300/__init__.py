@@ -28,6 +28,7 @@ __all__ = [
     "HgemmError", "library_path", "load", "hgemm", "hgemm_host", "hgemm_select_path",
     "hgemm_force_path", "hgemm_device_status", "hgemm_last_cuda_error",
     "hgemm_status_string", "hgemm_version", "hgemm_set_wait_timeout", "hgemm_debug_inject",
+    "hgemm_force_split",
     "HGEMM_INJECT_NONE", "HGEMM_INJECT_DROP_ARRIVAL", "matmul",
 ]
 
@@ -102,6 +103,8 @@ def load():
     lib.hgemm_set_wait_timeout.restype = i32
     lib.hgemm_debug_inject.argtypes = [i32]
     lib.hgemm_debug_inject.restype = i32
+    lib.hgemm_force_split.argtypes = [i32, i32]
+    lib.hgemm_force_split.restype = i32
     _lib = lib
     return lib
 
@@ -220,6 +223,11 @@ def hgemm_set_wait_timeout(ns: int) -> None:
 def hgemm_debug_inject(what: int) -> None:
     """Testing aid for the watchdog (HGEMM_INJECT_*); see include/hgemm.h."""
     _raise_on(load().hgemm_debug_inject(int(what)), "hgemm_debug_inject")
+
+
+def hgemm_force_split(split: int, tile_n: int) -> None:
+    """Testing aid: the split-K configuration for later calls ((0, 0): automatic)."""
+    _raise_on(load().hgemm_force_split(int(split), int(tile_n)), "hgemm_force_split")
 
 
 def matmul(a, b_cols, out=None, stream=None):

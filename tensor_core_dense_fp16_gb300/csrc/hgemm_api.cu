@@ -27,6 +27,7 @@ constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;  // 2 s per wait
 
 thread_local int t_last_cuda_error = 0;
 std::atomic<int> g_forced_path{-1};
+std::atomic<int> g_forced_split{0};  // split * 1024 + tile_n, or 0
 std::atomic<unsigned long long> g_timeout_ns{kDefaultTimeoutNs};
 std::atomic<int> g_inject{HGEMM_INJECT_NONE};
 
@@ -41,9 +42,9 @@ std::mutex g_device_mu;
 
 // GB300 figures, used by hgemm_select_path before any device has been used
 // in this process: 152 SMs; co-resident clusters of 2, 4, 6 and 8 CTAs of
-// ~225 KB of shared memory each, as cudaOccupancyMaxActiveClusters reports
-// them on this part.
-constexpr hg::DeviceProfile kNominalProfile{152, 76, 36, 23, 15};
+// ~200-225 KB of shared memory each, as cudaOccupancyMaxActiveClusters
+// reports them on this part.
+constexpr hg::DeviceProfile kNominalProfile{152, 76, 36, 23, 15, 36};
 std::atomic<const hg::DeviceProfile*> g_last_profile{&kNominalProfile};
 
 int cuda_fail(cudaError_t e) {
@@ -78,9 +79,10 @@ int current_device(DeviceState** out) {
         st.status = status;
         st.prof.num_sms = sms;
         st.prof.pair_clusters = hg::pair_max_clusters(sms);
-        st.prof.split2_clusters = hg::skinny_max_clusters(2, sms);
-        st.prof.split3_clusters = hg::skinny_max_clusters(3, sms);
-        st.prof.split4_clusters = hg::skinny_max_clusters(4, sms);
+        st.prof.split2_clusters = hg::skinny_max_clusters(2, 256, sms);
+        st.prof.split3_clusters = hg::skinny_max_clusters(3, 256, sms);
+        st.prof.split4_clusters = hg::skinny_max_clusters(4, 256, sms);
+        st.prof.split2n_clusters = hg::skinny_max_clusters(2, 128, sms);
         r = 1;
       }
       st.ready.store(r, std::memory_order_release);
@@ -125,14 +127,16 @@ bool tma_ok(const void* A, const void* B, const void* C, int64_t N, int64_t K) {
 }
 
 int choose_path(const void* A, const void* B, const void* C, int64_t M, int64_t N, int64_t K,
-                const hg::DeviceProfile& prof, int* split) {
+                const hg::DeviceProfile& prof, int* split, int* tile_n) {
   *split = 1;
+  *tile_n = hg::kPairBN;
   if (M == 0 || N == 0) return HGEMM_PATH_NONE;
   if (K == 0) return HGEMM_PATH_ZERO;
   const bool tma = tma_ok(A, B, C, N, K);
   const int forced = g_forced_path.load(std::memory_order_relaxed);
   if (forced == HGEMM_PATH_GENERIC || !tma) return HGEMM_PATH_GENERIC;
-  return hg::choose_tma_path(M, N, K, prof, forced, split);
+  const int fs = g_forced_split.load(std::memory_order_relaxed);
+  return hg::choose_tma_path(M, N, K, prof, forced, fs >> 10, fs & 1023, split, tile_n);
 }
 
 }  // namespace
@@ -140,41 +144,65 @@ int choose_path(const void* A, const void* B, const void* C, int64_t M, int64_t 
 namespace hg {
 
 int choose_tma_path(int64_t M, int64_t N, int64_t K, const DeviceProfile& dev, int forced,
-                    int* split) {
+                    int forced_split, int forced_tile_n, int* split, int* tile_n) {
   *split = 1;
-  const int64_t tiles = ((M + 2 * kTcBM - 1) / (2 * kTcBM)) * ((N + kPairBN - 1) / kPairBN);
+  *tile_n = kPairBN;
+  const int64_t num_m = (M + 2 * kTcBM - 1) / (2 * kTcBM);
   const int64_t num_kb = (K + kTcBK - 1) / kTcBK;
-  // split-K: the most slices (4, 3 or 2) whose clusters all fit on the device
-  // at once, with at least one K block per slice; `need_idle` requires that
-  // the pair kernel would leave at least half of the SM pairs idle and that
-  // the split does not ask for more pairs than the device has
-  auto best_split = [&](bool need_idle) -> int {
-    if (need_idle && 2 * tiles > dev.pair_clusters) return 1;  // pairs already fill the GPU
-    const int fits[5] = {0, 0, dev.split2_clusters, dev.split3_clusters, dev.split4_clusters};
-    for (int s = 4; s >= 2; --s) {
-      if (num_kb < s || tiles > fits[s]) continue;
-      if (need_idle && s * tiles > dev.pair_clusters) continue;
-      return s;
+  // Split-K configurations: S K-slices over 256-column tiles (S = 2, 3, 4)
+  // or 2 slices over 128-column tiles, one cluster of 2·S CTAs per tile.
+  // A configuration is usable when all its clusters fit on the device at
+  // once and every slice has a K block; `need_idle` also requires that the
+  // unsplit pair kernel would leave at least half of the SM pairs idle and
+  // that the split asks for no more pairs than the device has.
+  auto usable = [&](int s, int bn, bool need_idle) {
+    const int64_t tiles = num_m * ((N + bn - 1) / bn);
+    const int fits = bn == 128 ? (s == 2 ? dev.split2n_clusters : 0)
+                               : (s == 2 ? dev.split2_clusters
+                                  : s == 3 ? dev.split3_clusters
+                                  : s == 4 ? dev.split4_clusters : 0);
+    if (num_kb < s || tiles > fits) return false;
+    if (need_idle && (2 * num_m * ((N + kPairBN - 1) / kPairBN) > dev.pair_clusters ||
+                      s * tiles > dev.pair_clusters))
+      return false;
+    return true;
+  };
+  // Cost estimate in microseconds: each SM takes in its slice's operands at
+  // ~112 GB/s (measured cap of one SM's intake), and sends and receives its
+  // share of the FP32 partial sums at an effective ~21 GB/s (fitted to the
+  // measured launches of 4096×256×4096 in both tile widths).
+  auto cost = [&](int s, int bn) {
+    const double intake = static_cast<double>(num_kb) / s * (kTcBM + bn / 2) * kTcBK * 2;
+    const double exchange = static_cast<double>(kTcBM) * bn * 4 * (s - 1) / s;
+    return intake / 112e3 + exchange / 21e3;
+  };
+  auto choose = [&](bool need_idle) -> bool {
+    if (forced_split > 0 && usable(forced_split, forced_tile_n, false)) {
+      *split = forced_split;
+      *tile_n = forced_tile_n;
+      return true;
     }
-    return 1;
+    const int cand[4][2] = {{2, 128}, {4, 256}, {3, 256}, {2, 256}};
+    double best = 0;
+    bool found = false;
+    for (const auto& c : cand) {
+      if (!usable(c[0], c[1], need_idle)) continue;
+      const double t = cost(c[0], c[1]);
+      if (!found || t < best) {
+        best = t;
+        *split = c[0];
+        *tile_n = c[1];
+        found = true;
+      }
+    }
+    return found;
   };
   if (forced == HGEMM_PATH_TC || forced == HGEMM_PATH_TC_PAIR || forced == HGEMM_PATH_TC_WIDE)
     return forced;
-  if (forced == HGEMM_PATH_SKINNY) {
-    const int s = best_split(false);
-    if (s > 1) {
-      *split = s;
-      return HGEMM_PATH_SKINNY;
-    }
-    return HGEMM_PATH_TC_PAIR;
-  }
+  if (forced == HGEMM_PATH_SKINNY) return choose(false) ? HGEMM_PATH_SKINNY : HGEMM_PATH_TC_PAIR;
   // Exchanging the partial sums costs a few microseconds; splitting pays
   // when each pair would otherwise walk a long K (48 blocks or more).
-  const int s = num_kb >= 48 ? best_split(true) : 1;
-  if (s > 1) {
-    *split = s;
-    return HGEMM_PATH_SKINNY;
-  }
+  if (num_kb >= 48 && choose(true)) return HGEMM_PATH_SKINNY;
   // A CTA pair covers 256 rows; with 128 rows or fewer half of it would idle.
   if (M <= kTcBM) return HGEMM_PATH_TC;
   // 256×512 tiles move 25% fewer operand bytes per flop than 256×256 ones;
@@ -338,18 +366,18 @@ int run_tc_wide(const void* A, const void* B, void* C, int64_t M, int64_t N, int
 }
 
 int run_skinny(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int split,
-               const DeviceState& dev, cudaStream_t stream) {
+               int tile_n, const DeviceState& dev, cudaStream_t stream) {
   CUtensorMap ma, mb, mc;
   int rc;
   if ((rc = encode_map(&ma, A, M, K, hg::kTcBM, hg::kTcBK)) != HGEMM_OK) return rc;
-  if ((rc = encode_map(&mb, B, N, K, hg::kPairBN / 2, hg::kTcBK)) != HGEMM_OK) return rc;
+  if ((rc = encode_map(&mb, B, N, K, tile_n / 2, hg::kTcBK)) != HGEMM_OK) return rc;
   if ((rc = encode_map(&mc, C, M, N, hg::kEpiRows, hg::kEpiCols)) != HGEMM_OK) return rc;
   hg::TcArgs args{};
   args.M = static_cast<int>(M);
   args.N = static_cast<int>(N);
   args.K = static_cast<int>(K);
   args.num_m = static_cast<int>((M + 2 * hg::kTcBM - 1) / (2 * hg::kTcBM));
-  args.num_n = static_cast<int>((N + hg::kPairBN - 1) / hg::kPairBN);
+  args.num_n = static_cast<int>((N + tile_n - 1) / tile_n);
   args.num_kb = static_cast<int>((K + hg::kTcBK - 1) / hg::kTcBK);
   const int64_t tiles = static_cast<int64_t>(args.num_m) * args.num_n;
   if (tiles * 2 * split > 0x7FFFFFFF) return HGEMM_ERR_INVALID_ARG;
@@ -360,15 +388,15 @@ int run_skinny(const void* A, const void* B, void* C, int64_t M, int64_t N, int6
   args.status = dev.status;
   args.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
   args.inject = g_inject.load(std::memory_order_relaxed);
-  cudaError_t e = hg::launch_skinny(split, ma, mb, mc, args, stream);
+  cudaError_t e = hg::launch_skinny(split, tile_n, ma, mb, mc, args, stream);
   return e == cudaSuccess ? HGEMM_OK : cuda_fail(e);
 }
 
 int dispatch(const hgemm_half_t* A, const hgemm_half_t* B, hgemm_half_t* C, int64_t M, int64_t N,
              int64_t K, const DeviceState& dev, cudaStream_t stream) {
   cudaError_t e;
-  int split = 1;
-  switch (choose_path(A, B, C, M, N, K, dev.prof, &split)) {
+  int split = 1, tile_n = hg::kPairBN;
+  switch (choose_path(A, B, C, M, N, K, dev.prof, &split, &tile_n)) {
     case HGEMM_PATH_NONE:
       return HGEMM_OK;
     case HGEMM_PATH_ZERO:
@@ -381,7 +409,7 @@ int dispatch(const hgemm_half_t* A, const hgemm_half_t* B, hgemm_half_t* C, int6
     case HGEMM_PATH_TC_WIDE:
       return run_tc_wide(A, B, C, M, N, K, dev, stream);
     case HGEMM_PATH_SKINNY:
-      return run_skinny(A, B, C, M, N, K, split, dev, stream);
+      return run_skinny(A, B, C, M, N, K, split, tile_n, dev, stream);
     default: {
       hg::PlainArgs pa{A, B, C, M, N, K, dev.status, g_timeout_ns.load()};
       e = hg::launch_generic(pa, dev.num_sms, stream);
@@ -504,8 +532,16 @@ int hgemm_select_path(const void* A, const void* B, const void* C, int64_t M, in
                       int64_t K) {
   int rc = validate(A, B, C, M, N, K);
   if (rc != HGEMM_OK) return rc;
-  int split = 1;
-  return choose_path(A, B, C, M, N, K, *g_last_profile.load(std::memory_order_acquire), &split);
+  int split = 1, tile_n = hg::kPairBN;
+  return choose_path(A, B, C, M, N, K, *g_last_profile.load(std::memory_order_acquire), &split, &tile_n);
+}
+
+int hgemm_force_split(int split, int tile_n) {
+  const bool ok = (split == 0 && tile_n == 0) || (split == 2 && tile_n == 128) ||
+                  (tile_n == 256 && split >= 2 && split <= 4);
+  if (!ok) return HGEMM_ERR_INVALID_ARG;
+  g_forced_split.store(split * 1024 + tile_n);
+  return HGEMM_OK;
 }
 
 int hgemm_force_path(int path) {

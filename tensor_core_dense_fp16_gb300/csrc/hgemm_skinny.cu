@@ -33,26 +33,27 @@
 namespace hg {
 namespace {
 
-constexpr int kSkStages = 6;
+// Column range of K-slice p: [64·owned_unit(p), 64·owned_unit(p + 1)), in
+// 64-column units of a tile `units` units wide.
+__host__ __device__ constexpr int owned_unit(int p, int split, int units) { return (units * p) / split; }
 
-// Column range of K-slice p, in 64-column units of the 256-column tile.
-__host__ __device__ constexpr int owned_unit(int p, int split) { return (4 * p) / split; }
-
-template <int SPLIT>
+template <int SPLIT, int BN_>
 struct SkCfg {
   static constexpr int BM = 2 * kTcBM;   // tile rows (both CTAs of a pair)
-  static constexpr int BN = kPairBN;     // tile columns
+  static constexpr int BN = BN_;         // tile columns: 256 or 128
+  static constexpr int UNITS = BN / 64;
   static constexpr int ROWS = kTcBM;     // rows per CTA
   static constexpr int BROWS = BN / 2;   // B rows per CTA
   static constexpr int BK = kTcBK;
-  static constexpr int STAGES = kSkStages;
+  static constexpr int STAGES = BN == 256 ? 6 : 8;  // 32 KB or 24 KB per stage
   static constexpr int UMMA_K = 16;
   static constexpr int A_BYTES = ROWS * BK * 2;
   static constexpr int B_BYTES = BROWS * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int TX_BYTES = 2 * STAGE_BYTES;
   static constexpr int RING_BYTES = STAGES * STAGE_BYTES;     // reused for the reduction
-  static constexpr int MAX_OWN_COLS = 64 * (owned_unit(SPLIT, SPLIT) - owned_unit(SPLIT - 1, SPLIT));
+  // the last slice owns the most units
+  static constexpr int MAX_OWN_COLS = 64 * (owned_unit(SPLIT, SPLIT, UNITS) - owned_unit(SPLIT - 1, SPLIT, UNITS));
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
   static constexpr int OFF_C = OFF_B + STAGES * B_BYTES;     // FP16 staging of C
@@ -77,6 +78,7 @@ struct SkCfg {
   static_assert(exchange_bytes(64) <= RING_BYTES, "reduction fits in the ring");
   static_assert(SMEM_BYTES <= 232448, "exceeds 227 KB of shared memory per CTA");
   static_assert(C_WARP_BYTES % 1024 == 0, "staging boxes stay 1024-byte aligned");
+  static_assert(SPLIT <= UNITS, "every slice owns at least one 64-column unit");
 };
 
 // Swizzled FP32 block of `cols` columns: row r occupies cols*4 bytes at
@@ -86,11 +88,11 @@ __device__ __forceinline__ uint32_t f32_block_offset(int r, int c, int cols) {
   return static_cast<uint32_t>(r * cols * 4 + ((c ^ (r & 7)) << 4));
 }
 
-template <int SPLIT>
+template <int SPLIT, int BN>
 __global__ void __launch_bounds__(192, 1)
     hgemm_skinny_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC, const TcArgs p) {
-  using Cfg = SkCfg<SPLIT>;
+  using Cfg = SkCfg<SPLIT, BN>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -120,8 +122,8 @@ __global__ void __launch_bounds__(192, 1)
   const int nb = tile % p.num_n;
   const int kb0 = static_cast<int>(static_cast<long long>(p.num_kb) * slice / SPLIT);
   const int kb1 = static_cast<int>(static_cast<long long>(p.num_kb) * (slice + 1) / SPLIT);
-  const int own_c0 = 64 * owned_unit(slice, SPLIT);  // this CTA's column range
-  const int own_cols = 64 * owned_unit(slice + 1, SPLIT) - own_c0;
+  const int own_c0 = 64 * owned_unit(slice, SPLIT, Cfg::UNITS);  // this CTA's column range
+  const int own_cols = 64 * owned_unit(slice + 1, SPLIT, Cfg::UNITS) - own_c0;
   const Watchdog wd{abort_flag, p.status, p.timeout_ns};
 
   if (threadIdx.x == 0) {
@@ -241,8 +243,8 @@ __global__ void __launch_bounds__(192, 1)
     uint32_t send_off = send_base;
     for (int j = 0; j < SPLIT; ++j) {
       if (j == slice) continue;
-      const int c0 = 64 * owned_unit(j, SPLIT);
-      const int cols = 64 * owned_unit(j + 1, SPLIT) - c0;
+      const int c0 = 64 * owned_unit(j, SPLIT, Cfg::UNITS);
+      const int cols = 64 * owned_unit(j + 1, SPLIT, Cfg::UNITS) - c0;
       uint8_t* blk = smem + (send_off - sbase);
       // owner j's ring must be free before our copy lands in it
       int rdy = 1;
@@ -356,12 +358,12 @@ __global__ void __launch_bounds__(192, 1)
   if (warp == 1) tmem_dealloc_cg2(tmem_base, Cfg::TMEM_COLS);
 }
 
-template <int SPLIT>
+template <int SPLIT, int BN>
 cudaError_t launch_split(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
                          const TcArgs& args, cudaStream_t stream) {
-  using Cfg = SkCfg<SPLIT>;
+  using Cfg = SkCfg<SPLIT, BN>;
   static bool attr_done[64] = {};
-  auto kern = hgemm_skinny_kernel<SPLIT>;
+  auto kern = hgemm_skinny_kernel<SPLIT, BN>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -385,10 +387,10 @@ cudaError_t launch_split(const CUtensorMap& a, const CUtensorMap& b, const CUten
   return cudaLaunchKernelEx(&cfg, kern, a, b, c, args);
 }
 
-template <int SPLIT>
+template <int SPLIT, int BN>
 int max_clusters_split(int num_sms) {
-  using Cfg = SkCfg<SPLIT>;
-  auto kern = hgemm_skinny_kernel<SPLIT>;
+  using Cfg = SkCfg<SPLIT, BN>;
+  auto kern = hgemm_skinny_kernel<SPLIT, BN>;
   int n = 0;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) ==
       cudaSuccess) {
@@ -411,28 +413,31 @@ int max_clusters_split(int num_sms) {
 
 }  // namespace
 
-int skinny_max_clusters(int split, int num_sms) {
+int skinny_max_clusters(int split, int tile_n, int num_sms) {
+  if (tile_n == 128) return split == 2 ? max_clusters_split<2, 128>(num_sms) : 0;
   switch (split) {
     case 2:
-      return max_clusters_split<2>(num_sms);
+      return max_clusters_split<2, 256>(num_sms);
     case 3:
-      return max_clusters_split<3>(num_sms);
+      return max_clusters_split<3, 256>(num_sms);
     case 4:
-      return max_clusters_split<4>(num_sms);
+      return max_clusters_split<4, 256>(num_sms);
     default:
       return 0;
   }
 }
 
-cudaError_t launch_skinny(int split, const CUtensorMap& a, const CUtensorMap& b,
+cudaError_t launch_skinny(int split, int tile_n, const CUtensorMap& a, const CUtensorMap& b,
                           const CUtensorMap& c, const TcArgs& args, cudaStream_t stream) {
+  if (tile_n == 128) return split == 2 ? launch_split<2, 128>(a, b, c, args, stream) : cudaErrorInvalidValue;
+  if (tile_n != 256) return cudaErrorInvalidValue;
   switch (split) {
     case 2:
-      return launch_split<2>(a, b, c, args, stream);
+      return launch_split<2, 256>(a, b, c, args, stream);
     case 3:
-      return launch_split<3>(a, b, c, args, stream);
+      return launch_split<3, 256>(a, b, c, args, stream);
     case 4:
-      return launch_split<4>(a, b, c, args, stream);
+      return launch_split<4, 256>(a, b, c, args, stream);
     default:
       return cudaErrorInvalidValue;
   }

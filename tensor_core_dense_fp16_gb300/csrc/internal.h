@@ -59,12 +59,13 @@ int pair_max_clusters(int num_sms);
 cudaError_t launch_tc_wide(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
                            const TcArgs& args, cudaStream_t stream);
 int wide_max_clusters(int num_sms);
-// Split-K cluster kernel for few output tiles: `split` K-slices (2, 3 or 4),
-// one cluster of 2*split CTAs per 256×256 tile (args.num_tiles of them).
-cudaError_t launch_skinny(int split, const CUtensorMap& a, const CUtensorMap& b,
+// Split-K cluster kernel for few output tiles: `split` K-slices, one cluster
+// of 2*split CTAs per 256×tile_n tile (args.num_tiles of them); tile_n 256
+// with 2, 3 or 4 slices, or tile_n 128 with 2.
+cudaError_t launch_skinny(int split, int tile_n, const CUtensorMap& a, const CUtensorMap& b,
                           const CUtensorMap& c, const TcArgs& args, cudaStream_t stream);
 // Largest number of co-resident clusters of the split-K kernel.
-int skinny_max_clusters(int split, int num_sms);
+int skinny_max_clusters(int split, int tile_n, int num_sms);
 cudaError_t launch_zero_fill(uint16_t* C, int64_t count, cudaStream_t stream);
 cudaError_t launch_generic(const PlainArgs& args, int num_sms, cudaStream_t stream);
 
@@ -79,12 +80,15 @@ struct DeviceProfile {
   int split2_clusters;  // co-resident 4-CTA clusters of the split-K kernel
   int split3_clusters;  // co-resident 6-CTA clusters
   int split4_clusters;  // co-resident 8-CTA clusters
+  int split2n_clusters;  // co-resident 4-CTA clusters of the 128-column split-K kernel
 };
 
 // Kernel choice for a TMA-able product. Returns an HGEMM_PATH_* value and,
-// for the split-K path, the number of K-slices in *split.
+// for the split-K path, the number of K-slices in *split and the tile width
+// in *tile_n. forced: a forced HGEMM_PATH_* or -1; forced_split and
+// forced_tile_n: a forced split-K configuration or 0.
 int choose_tma_path(int64_t M, int64_t N, int64_t K, const DeviceProfile& dev, int forced,
-                    int* split);
+                    int forced_split, int forced_tile_n, int* split, int* tile_n);
 
 // Tile geometry of the tensor-core path, for the host-side tensor maps.
 constexpr int kTcBM = 128;

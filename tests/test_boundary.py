@@ -125,6 +125,20 @@ def test_forced_paths(lib):
     assert tc.hgemm_select_path(A16, B16, C16, 256, 256, 256) == tc.HGEMM_PATH_TC_PAIR
 
 
+def test_forced_split_configuration(lib):
+    for bad in [(1, 256), (5, 256), (3, 128), (2, 64), (0, 256)]:
+        with pytest.raises(tc.HgemmError):
+            tc.hgemm_force_split(*bad)
+    try:
+        tc.hgemm_force_path(tc.HGEMM_PATH_SKINNY)
+        for good in [(2, 128), (2, 256), (3, 256), (4, 256)]:
+            tc.hgemm_force_split(*good)
+            assert tc.hgemm_select_path(A16, B16, C16, 4096, 256, 4096) == tc.HGEMM_PATH_SKINNY
+    finally:
+        tc.hgemm_force_split(0, 0)
+        tc.hgemm_force_path(-1)
+
+
 def test_invalid_arguments_rejected_before_any_device_work(lib):
     bad = [
         (A16, B16, C16, -1, 4, 4),

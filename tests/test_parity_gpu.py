@@ -282,21 +282,26 @@ def test_side_stream_and_repeatability():
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
 
 
-# Tiles (of 256×256) for which the forced split-K path takes each slice count
-# S: the most slices whose clusters of 2·S CTAs all fit on the GPU at once
-# (15 clusters of 8, 23 of 6 and 36 of 4 CTAs on GB300).
-SPLIT_TILES = {4: 15, 3: 23, 2: 36}
+# Split-K configurations (slices, tile width) and a tile count whose clusters
+# of 2·S CTAs all fit on a GB300 at once (15 of 8, 23 of 6, 36 of 4 CTAs).
+SPLIT_CONFIGS = {(4, 256): 15, (3, 256): 23, (2, 256): 36, (2, 128): 36}
 
 
-@pytest.mark.parametrize("split", sorted(SPLIT_TILES))
-def test_split_k_every_slice_count(split):
+@pytest.mark.parametrize("split,tile_n", sorted(SPLIT_CONFIGS))
+def test_split_k_every_configuration(split, tile_n):
     """Ragged M, N and K; 2·S+1 K blocks, so slices hold 2 or 3 blocks and
     (for S = 3) the owned column ranges are uneven."""
-    tiles = SPLIT_TILES[split]
-    M, N, K = 256 * tiles - 13, 248, 64 * (2 * split) + 24
-    a, b = synth.operands(M, N, K, seed=500 + split, kind="uniform")
+    tiles = SPLIT_CONFIGS[(split, tile_n)]
+    n = 248 if tile_n == 256 else 120
+    M, N, K = 256 * tiles - 13, n, 64 * (2 * split) + 24
+    a, b = synth.operands(M, N, K, seed=500 + split + tile_n, kind="uniform")
     ref = oracle.hgemm(a, b, nthreads=oracle_threads())
-    assert_close(run_gpu(a, b, path=tc.HGEMM_PATH_SKINNY), ref, what=f"split {split}")
+    tc.hgemm_force_split(split, tile_n)
+    try:
+        got = run_gpu(a, b, path=tc.HGEMM_PATH_SKINNY)
+    finally:
+        tc.hgemm_force_split(0, 0)
+    assert_close(got, ref, what=f"split {split} x {tile_n}")
 
 
 @pytest.mark.parametrize("M,N,K", [(1000, 1000, 1000), (256, 256, 256), (300, 136, 2048),
