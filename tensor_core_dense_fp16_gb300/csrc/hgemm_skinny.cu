@@ -9,20 +9,23 @@
 // clipped stores, "GPU架构与CUDA", 共享内存与分块).
 //
 // Design:
-//   * one cluster of 2·S CTAs per 256×256 output tile; CTA rank r belongs to
-//     K-slice p = r / 2 and tile half h = r % 2; pair p (ranks 2p, 2p+1) runs
-//     the CTA-pair main loop of hgemm_tc2.cu over its contiguous range of
-//     64-wide K blocks, so A is read from memory exactly once over the grid;
-//   * each CTA ends with a 128×256 FP32 partial sum in its TMEM;
+//   * one cluster of 2·S CTAs per 256×BN output tile (BN = 256 with S = 2, 3
+//     or 4 slices, or BN = 128 with S = 2: half the partial sums to exchange
+//     for the same operand bytes per SM); CTA rank r belongs to K-slice
+//     p = r / 2 and tile half h = r % 2; pair p (ranks 2p, 2p+1) runs the
+//     CTA-pair main loop of hgemm_tc2.cu over its contiguous range of 64-wide
+//     K blocks, so A is read from memory exactly once over the grid;
+//   * each CTA ends with a 128×BN FP32 partial sum in its TMEM;
 //   * the S partials of a half are reduced through distributed shared
-//     memory: the 256 columns are cut into S ranges of whole 64-column
-//     units, the CTA of slice p owns range p. After a cluster barrier (every
-//     pair's MMAs done, so every operand ring is free), each epilogue warp
-//     stages its 32 rows of every foreign range in its own shared memory and
-//     pushes them with one bulk copy per owner into the owner's ring; the
-//     owner's barrier counts the bytes. Each owner then adds the S partials in
+//     memory: the columns are cut into S ranges of whole 64-column units, the
+//     CTA of slice p owns range p. Once an owner's own MMAs are done (its
+//     operand ring is free) it tells the senders of its half; each sender's
+//     epilogue warps stage their 32 rows of the owner's range in their own
+//     shared memory and push them with one bulk copy into the owner's ring,
+//     whose barrier counts the bytes. Each owner then adds the S partials in
 //     slice order (so the result does not depend on timing), rounds to FP16
-//     and TMA-stores its 128-row block of C.
+//     and TMA-stores its block of C, and acknowledges, so that no copy
+//     touches a CTA that has left.
 // No global scratch memory is used.
 #include <cuda_fp16.h>
 
