@@ -56,6 +56,13 @@ def _load():
         lib.oracle_hgemm_entries.argtypes = [u16p, u16p, i64, ctypes.c_void_p,
                                              ctypes.c_void_p, i64, u16p]
         lib.oracle_hgemm_entries.restype = None
+        lib.oracle_hgemm_ex.argtypes = [u16p, u16p, u16p, i64, i64, i64, ctypes.c_double,
+                                        ctypes.c_double, u16p, ctypes.c_int, ctypes.c_int]
+        lib.oracle_hgemm_ex.restype = ctypes.c_int
+        lib.oracle_hgemm_entries_ex.argtypes = [u16p, u16p, i64, ctypes.c_void_p, ctypes.c_void_p,
+                                                i64, ctypes.c_double, ctypes.c_double, u16p, u16p,
+                                                ctypes.c_int, u16p]
+        lib.oracle_hgemm_entries_ex.restype = None
         lib.oracle_fp16_to_double.argtypes = [ctypes.c_uint16]
         lib.oracle_fp16_to_double.restype = ctypes.c_double
         lib.oracle_double_to_fp16.argtypes = [ctypes.c_double]
@@ -115,6 +122,64 @@ def entries(a: np.ndarray, b: np.ndarray, rows, cols) -> np.ndarray:
     out = np.empty(rows.shape, dtype=np.float16)
     _load().oracle_hgemm_entries(a.ctypes.data, b.ctypes.data, a.shape[1], rows.ctypes.data,
                                  cols.ctypes.data, rows.size, out.ctypes.data)
+    return out
+
+
+def _epilogue_inputs(c, bias, shape, beta):
+    M, N = shape
+    if beta != 0.0:
+        if c is None:
+            raise ValueError("beta != 0 reads C: pass c")
+        c = np.ascontiguousarray(c, dtype=np.float16)
+        if c.shape != (M, N):
+            raise ValueError("c must be (M, N)")
+    if bias is not None:
+        bias = np.ascontiguousarray(bias, dtype=np.float16)
+        if bias.shape != (N,):
+            raise ValueError("bias must have length N")
+    return c, bias
+
+
+def hgemm_ex(a: np.ndarray, b: np.ndarray, c: np.ndarray | None = None, alpha: float = 1.0,
+             beta: float = 0.0, bias: np.ndarray | None = None, relu: bool = False,
+             nthreads: int | None = None) -> np.ndarray:
+    """The fused product, (M, N) float16:
+    fp16(f(alpha·A·B + beta·c + bias[j])), f = ReLU if relu; c is not read when beta == 0."""
+    a, b = _operands(a, b)
+    M, K = a.shape
+    N = b.shape[0]
+    c, bias = _epilogue_inputs(c, bias, (M, N), beta)
+    out = np.array(c, dtype=np.float16, copy=True) if c is not None else np.zeros((M, N), np.float16)
+    rc = _load().oracle_hgemm_ex(a.ctypes.data, b.ctypes.data, out.ctypes.data, M, N, K,
+                                 float(alpha), float(beta),
+                                 bias.ctypes.data if bias is not None else None, int(bool(relu)),
+                                 _threads(nthreads))
+    if rc != 0:
+        raise MemoryError("oracle_hgemm_ex could not allocate its thread bookkeeping")
+    return out
+
+
+def entries_ex(a: np.ndarray, b: np.ndarray, rows, cols, c: np.ndarray | None = None,
+               alpha: float = 1.0, beta: float = 0.0, bias: np.ndarray | None = None,
+               relu: bool = False) -> np.ndarray:
+    """Entries (rows[t], cols[t]) of the fused product; c is the whole previous C."""
+    a, b = _operands(a, b)
+    M, K = a.shape
+    N = b.shape[0]
+    c, bias = _epilogue_inputs(c, bias, (M, N), beta)
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    cols = np.ascontiguousarray(cols, dtype=np.int64)
+    if rows.shape != cols.shape:
+        raise ValueError("rows and cols must have the same length")
+    if rows.size and (rows.min() < 0 or rows.max() >= M or cols.min() < 0 or cols.max() >= N):
+        raise IndexError("entry index out of range")
+    c_old = np.ascontiguousarray(c[rows, cols]) if c is not None else None
+    out = np.empty(rows.shape, dtype=np.float16)
+    _load().oracle_hgemm_entries_ex(a.ctypes.data, b.ctypes.data, K, rows.ctypes.data,
+                                    cols.ctypes.data, rows.size, float(alpha), float(beta),
+                                    c_old.ctypes.data if c_old is not None else None,
+                                    bias.ctypes.data if bias is not None else None,
+                                    int(bool(relu)), out.ctypes.data)
     return out
 
 

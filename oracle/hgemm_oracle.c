@@ -22,6 +22,18 @@
  *  - The pages do not state how the accumulator becomes FP16; the reading
  *    taken is one IEEE round-to-nearest-even (overflow to ±Inf).
  *
+ * The fused variant (oracle_hgemm_ex) follows "GPU架构与CUDA", 核函数融合:
+ * the product, a bias add and a ReLU in one pass, the intermediate never
+ * leaving the pass. With the BLAS scaling the pages leave open:
+ *
+ *     C[i*N + j] = fp16_rne( f( alpha * S + beta * C_old[i*N + j] + bias[j] ) )
+ *
+ * where S is the FP64 sum above, bias (length N, one value per column of C,
+ * i.e. per output feature of the page's matmul(x, W) + bias) may be absent,
+ * f is max(·, 0) when relu is set and the identity otherwise, and C_old is
+ * not read at all when beta == 0 (so a NaN there does not propagate). All of
+ * it in FP64, one rounding at the end.
+ *
  * Build: gcc -O2 -fno-fast-math -ffp-contract=off (no FMA contraction, so
  * x86-64 and AArch64 hosts produce identical bits).
  */
@@ -104,12 +116,35 @@ static double dot_f64(const uint16_t *A, const uint16_t *B, int64_t i, int64_t j
     return s;
 }
 
+/* The fused epilogue's parameters; `on` == 0 means the plain product. */
+struct epilogue {
+    int on;
+    double alpha, beta;
+    const uint16_t *bias;   /* length N, or NULL */
+    int relu;
+};
+
+/* alpha·s + beta·c_old + bias, then the ReLU, all in FP64 (c_old is the
+ * entry's previous FP16 value, looked at only when beta != 0). */
+static double apply_epilogue(const struct epilogue *ep, double s, uint16_t c_old, int64_t j)
+{
+    double v = ep->alpha * s;
+    if (ep->beta != 0.0)
+        v += ep->beta * g_decode[c_old];
+    if (ep->bias)
+        v += g_decode[ep->bias[j]];
+    if (ep->relu && v < 0.0)
+        v = 0.0;
+    return v;
+}
+
 struct rows_job {
     const uint16_t *A, *B;
-    uint16_t *C;     /* FP16 result, or NULL */
+    uint16_t *C;     /* FP16 result (and, with a fused epilogue, C_old), or NULL */
     double *S;       /* FP64 pre-rounding sums, or NULL */
     int64_t M, N, K;
     int64_t row_lo, row_hi;
+    struct epilogue ep;
 };
 
 static void *rows_worker(void *arg)
@@ -120,15 +155,19 @@ static void *rows_worker(void *arg)
             double s = dot_f64(jb->A, jb->B, i, j, jb->K);
             if (jb->S)
                 jb->S[i * jb->N + j] = s;
-            if (jb->C)
-                jb->C[i * jb->N + j] = oracle_double_to_fp16(s);
+            if (jb->C) {
+                uint16_t *c = &jb->C[i * jb->N + j];
+                if (jb->ep.on)
+                    s = apply_epilogue(&jb->ep, s, *c, j);
+                *c = oracle_double_to_fp16(s);
+            }
         }
     return NULL;
 }
 
 /* Runs rows [0, M) split over `nthreads` threads (1 if nthreads < 1). */
 static int run_rows(const uint16_t *A, const uint16_t *B, uint16_t *C, double *S,
-                    int64_t M, int64_t N, int64_t K, int nthreads)
+                    int64_t M, int64_t N, int64_t K, int nthreads, struct epilogue ep)
 {
     pthread_once(&g_decode_once, fill_decode_table);
     if (M <= 0 || N <= 0)
@@ -151,7 +190,7 @@ static int run_rows(const uint16_t *A, const uint16_t *B, uint16_t *C, double *S
         return -1;
     }
     for (int t = 0; t < nthreads; ++t) {
-        struct rows_job jb = {A, B, C, S, M, N, K, M * t / nthreads, M * (t + 1) / nthreads};
+        struct rows_job jb = {A, B, C, S, M, N, K, M * t / nthreads, M * (t + 1) / nthreads, ep};
         jobs[t] = jb;
         if (t == 0)
             continue;
@@ -175,14 +214,26 @@ static int run_rows(const uint16_t *A, const uint16_t *B, uint16_t *C, double *S
 int oracle_hgemm(const uint16_t *A, const uint16_t *B, uint16_t *C,
                  int64_t M, int64_t N, int64_t K, int nthreads)
 {
-    return run_rows(A, B, C, NULL, M, N, K, nthreads);
+    const struct epilogue none = {0, 1.0, 0.0, NULL, 0};
+    return run_rows(A, B, C, NULL, M, N, K, nthreads, none);
+}
+
+/* The fused variant defined above: C is read (when beta != 0) and
+ * overwritten in place. */
+int oracle_hgemm_ex(const uint16_t *A, const uint16_t *B, uint16_t *C,
+                    int64_t M, int64_t N, int64_t K, double alpha, double beta,
+                    const uint16_t *bias, int relu, int nthreads)
+{
+    const struct epilogue ep = {1, alpha, beta, bias, relu};
+    return run_rows(A, B, C, NULL, M, N, K, nthreads, ep);
 }
 
 /* The FP64 sums before the final rounding (M×N row-major doubles). */
 int oracle_hgemm_sums_f64(const uint16_t *A, const uint16_t *B, double *S,
                           int64_t M, int64_t N, int64_t K, int nthreads)
 {
-    return run_rows(A, B, NULL, S, M, N, K, nthreads);
+    const struct epilogue none = {0, 1.0, 0.0, NULL, 0};
+    return run_rows(A, B, NULL, S, M, N, K, nthreads, none);
 }
 
 /* Selected entries (rows[t], cols[t]) for t < count, for spot checks of
@@ -194,4 +245,20 @@ void oracle_hgemm_entries(const uint16_t *A, const uint16_t *B, int64_t K,
     pthread_once(&g_decode_once, fill_decode_table);
     for (int64_t t = 0; t < count; ++t)
         out[t] = oracle_double_to_fp16(dot_f64(A, B, rows[t], cols[t], K));
+}
+
+/* Selected entries of the fused variant: c_old[t] is the previous value of
+ * entry (rows[t], cols[t]) (ignored when beta == 0; may then be NULL), bias
+ * has length N or is NULL. */
+void oracle_hgemm_entries_ex(const uint16_t *A, const uint16_t *B, int64_t K,
+                             const int64_t *rows, const int64_t *cols, int64_t count,
+                             double alpha, double beta, const uint16_t *c_old,
+                             const uint16_t *bias, int relu, uint16_t *out)
+{
+    pthread_once(&g_decode_once, fill_decode_table);
+    const struct epilogue ep = {1, alpha, beta, bias, relu};
+    for (int64_t t = 0; t < count; ++t) {
+        const double s = dot_f64(A, B, rows[t], cols[t], K);
+        out[t] = oracle_double_to_fp16(apply_epilogue(&ep, s, c_old ? c_old[t] : 0, cols[t]));
+    }
 }

@@ -260,3 +260,81 @@ def test_degenerate_shapes():
     assert c.shape == (3, 2) and np.all(bits(c) == 0)
     with pytest.raises(ValueError):
         oracle.hgemm(np.zeros((3, 4), np.float16), np.zeros((2, 5), np.float16))
+
+
+# ---------------------------------------------------------------------------
+# the fused variant: fp16(f(alpha·A·B + beta·C_old + bias[j])), f = ReLU or id
+
+
+def test_fused_reduces_to_the_plain_product():
+    """alpha = 1, beta = 0, no bias, no ReLU is the plain product, bit for bit."""
+    rng = np.random.default_rng(31)
+    a = random_fp16(rng, (37, 53))
+    b = random_fp16(rng, (29, 53))
+    assert np.array_equal(bits(oracle.hgemm_ex(a, b)), bits(oracle.hgemm(a, b)))
+
+
+@pytest.mark.parametrize("alpha,beta,relu", [(1.0, 1.0, False), (2.0, -1.0, True), (-0.5, 2.0, False),
+                                             (1.0, 0.0, True), (0.5, 0.5, True), (-1.0, 0.0, False)])
+def test_fused_integer_operands_exact(alpha, beta, relu):
+    """Integer A, B, C_old and bias with power-of-two alpha and beta: every
+    value is an exact multiple of 1/4 well inside FP16's integer range, so the
+    oracle must equal exact rational arithmetic on an int64 product; M != N
+    and a bias that differs per column catch a bias indexed by row or a
+    transposed C."""
+    rng = np.random.default_rng(int(100 * alpha + 10 * beta + relu) & 0xFFFF)
+    M, N, K = 23, 17, 48
+    ai = rng.integers(-2, 3, size=(M, K))
+    bi = rng.integers(-2, 3, size=(N, K))
+    ci = rng.integers(-60, 61, size=(M, N))
+    bias = rng.integers(-20, 21, size=N)
+    prod = ai.astype(np.int64) @ bi.astype(np.int64).T
+    want = np.empty((M, N), dtype=np.uint16)
+    for i in range(M):
+        for j in range(N):
+            v = Fraction(alpha) * int(prod[i, j]) + Fraction(beta) * int(ci[i, j]) + int(bias[j])
+            if relu and v < 0:
+                v = Fraction(0)
+            want[i, j] = fraction_to_fp16_bits(v)
+    got = oracle.hgemm_ex(ai.astype(np.float16), bi.astype(np.float16), ci.astype(np.float16),
+                          alpha=alpha, beta=beta, bias=bias.astype(np.float16), relu=relu)
+    g = bits(got)
+    zero = (want & 0x7FFF) == 0
+    assert np.array_equal(g[~zero], want[~zero])
+    assert np.all((g[zero] & 0x7FFF) == 0)
+
+
+def test_fused_rounds_once():
+    """S = 1024·2 + 1·1 = 2049 and C_old = 1: the exact 2050 is an FP16 value;
+    rounding S first (2049 -> 2048) and then adding would give 2049 -> 2048."""
+    a = np.array([[1024.0, 1.0]], np.float16)
+    b = np.array([[2.0, 1.0]], np.float16)
+    c = np.array([[1.0]], np.float16)
+    got = oracle.hgemm_ex(a, b, c, beta=1.0)
+    assert float(got[0, 0]) == 2050.0
+    assert float(oracle.hgemm(a, b)[0, 0]) == 2048.0   # 2049 alone is a tie to even
+
+
+def test_fused_beta_zero_does_not_read_c():
+    rng = np.random.default_rng(5)
+    a = random_fp16(rng, (9, 16))
+    b = random_fp16(rng, (7, 16))
+    bias = random_fp16(rng, (7,))
+    nan_c = np.full((9, 7), np.nan, np.float16)
+    got = oracle.hgemm_ex(a, b, nan_c, alpha=1.5, beta=0.0, bias=bias, relu=True)
+    assert not np.isnan(got.astype(np.float32)).any()
+    assert np.array_equal(bits(got), bits(oracle.hgemm_ex(a, b, None, alpha=1.5, bias=bias, relu=True)))
+    assert np.all(got.astype(np.float32) >= 0)
+
+
+def test_fused_entries_agree_with_full_product():
+    rng = np.random.default_rng(77)
+    a = random_fp16(rng, (40, 96))
+    b = random_fp16(rng, (33, 96))
+    c = random_fp16(rng, (40, 33))
+    bias = random_fp16(rng, (33,))
+    full = oracle.hgemm_ex(a, b, c, alpha=0.75, beta=-1.25, bias=bias, relu=True, nthreads=3)
+    rows = rng.integers(0, 40, 200)
+    cols = rng.integers(0, 33, 200)
+    part = oracle.entries_ex(a, b, rows, cols, c, alpha=0.75, beta=-1.25, bias=bias, relu=True)
+    assert np.array_equal(bits(part), bits(full[rows, cols]))
