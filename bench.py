@@ -81,7 +81,16 @@ def parse_args():
                     help="target CPU time of the oracle sample")
     ap.add_argument("--reference-seconds", type=float, default=120.0,
                     help="target wall time of a whole --impl reference run")
+    ap.add_argument("--epilogue", choices=sorted(EPILOGUES), default="none",
+                    help="fused epilogue through hgemm_ex (default: the plain product)")
     return ap.parse_args()
+
+
+# Fused epilogues of hgemm_ex: (alpha, beta, with bias, relu). bias_relu is the
+# kernel-fusion example of the CUDA chapter (matmul + bias + ReLU);
+# accumulate is C += A·B (the update step of a recursive TRMM).
+EPILOGUES = {"none": None, "bias_relu": (1.0, 0.0, True, True), "accumulate": (1.0, 1.0, False, False),
+             "accumulate_bias_relu": (1.0, 1.0, True, True)}
 
 
 # ------------------------------------------------------------------- helpers
@@ -90,9 +99,15 @@ def flops_of(spec):
     return 2.0 * spec["M"] * spec["N"] * spec["K"]
 
 
-def bytes_of(spec):
+def bytes_of(spec, epilogue=None):
+    """Algorithmic bytes: A and B read once, C written once; plus C read once
+    when beta != 0 and the bias read once."""
     M, N, K = spec["M"], spec["N"], spec["K"]
-    return 2.0 * (M * K + N * K + M * N)
+    extra = 0.0
+    if epilogue:
+        alpha, beta, with_bias, relu = epilogue
+        extra = (2.0 * M * N if beta != 0 else 0.0) + (2.0 * N if with_bias else 0.0)
+    return 2.0 * (M * K + N * K + M * N) + extra
 
 
 def load_peaks():
@@ -343,9 +358,20 @@ def run_ours(args, spec, a, b, world, rank, local):
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(2 * l2 // 4 + 1, dtype=torch.float32, device=dev)
     path = tc.hgemm_select_path(da, db, dc, M, N, K)
+    epi = EPILOGUES[args.epilogue]
+    if epi is not None and path == tc.HGEMM_PATH_TC_WIDE:
+        path = tc.HGEMM_PATH_TC_PAIR   # a fused epilogue takes 256x256 tiles there (hgemm.h)
+    if epi is None:
+        def step():
+            tc.hgemm(da, db, dc, M, N, K, stream)
+    else:
+        alpha, beta, with_bias, relu = epi
+        gen = torch.Generator(device="cpu").manual_seed(spec["seed"] + 7)
+        dbias = (torch.rand(N, generator=gen) - 0.5).half().to(dev) if with_bias else None
+        dc.copy_((torch.rand((M, N), generator=gen) - 0.5).half())
 
-    def step():
-        tc.hgemm(da, db, dc, M, N, K, stream)
+        def step():
+            tc.hgemm_ex(da, db, dc, M, N, K, alpha, beta, dbias, relu, stream)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -381,9 +407,9 @@ def run_ours(args, spec, a, b, world, rank, local):
     median_ms = statistics.median(times_ms)
     value = whole_job_tflops(world, args.steps, flops, total_ms)
 
-    # ---- end to end through the host-buffer entry point
+    # ---- end to end through the host-buffer entry point (the plain product)
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and epi is None:
         ha = torch.from_numpy(a).pin_memory()
         hb = torch.from_numpy(b).pin_memory()
         hc = torch.empty((M, N), dtype=torch.float16).pin_memory()
@@ -412,7 +438,8 @@ def run_ours(args, spec, a, b, world, rank, local):
               tc.HGEMM_PATH_TC_WIDE: "hgemm_tc2w_kernel",
               tc.HGEMM_PATH_SKINNY: "hgemm_skinny_kernel",
               tc.HGEMM_PATH_GENERIC: "hgemm_generic_kernel"}.get(path, f"path {path}")
-    ai = flops / bytes_of(spec)
+    nbytes = bytes_of(spec, epi)
+    ai = flops / nbytes
     ridge = peaks["bf16_tflops"] * FP16_PER_BF16 * 1e12 / (peaks["hbm_gbs"] * 1e9)
     sha = kernel_sources_sha(kernel)
     traffic = profiled_traffic(kernel, args.workload, sha)
@@ -424,12 +451,12 @@ def run_ours(args, spec, a, b, world, rank, local):
                 "peak_source": f"{peak_src}: bf16_tflops (burst) x {FP16_PER_BF16} fp16/bf16"}
     else:
         peak = peaks["hbm_gbs"]
-        achieved = bytes_of(spec) / (mean_ms * 1e-3) / 1e9
+        achieved = nbytes / (mean_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": traffic,
                 "peak_source": f"{peak_src}: hbm_gbs"}
     roof.update({"kernel": kernel, "algorithmic_flops": flops,
-                 "algorithmic_bytes": bytes_of(spec), "source_sha": sha})
+                 "algorithmic_bytes": nbytes, "source_sha": sha})
 
     # ---- the oracle on this host's cores (rank 0, one GPU only)
     cpu = None
@@ -454,6 +481,7 @@ def run_ours(args, spec, a, b, world, rank, local):
                        "l2": "flushed before every timed launch (write of 2x L2 size, "
                              "outside the events)",
                        "inputs": "resident in HBM", "path": kernel,
+                       "epilogue": args.epilogue,
                        "parallelism": f"replicas x{world}"},
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": args.steps, "clocks": clocks,

@@ -67,7 +67,7 @@ typedef uint16_t hgemm_half_t; /* IEEE binary16 bit pattern */
 
 /* kernel paths, as reported by hgemm_select_path */
 #define HGEMM_PATH_NONE 0     /* M == 0 or N == 0: nothing to do */
-#define HGEMM_PATH_ZERO 1     /* K == 0: C is filled with +0 (the empty sum) */
+#define HGEMM_PATH_ZERO 1     /* K == 0: C is filled with +0 (the empty sum; hgemm_ex: f(beta·C + bias)) */
 #define HGEMM_PATH_TC 2       /* tcgen05 + TMA persistent kernel, one CTA per 128×256 tile */
 #define HGEMM_PATH_SKINNY 3   /* tcgen05 + TMA kernel for small N, split over K */
 #define HGEMM_PATH_GENERIC 4  /* tcgen05 kernel fed by plain loads: any alignment */
@@ -99,6 +99,28 @@ HGEMM_API int hgemm(const hgemm_half_t *A, const hgemm_half_t *B, hgemm_half_t *
           int64_t M, int64_t N, int64_t K, cudaStream_t stream);
 
 /*
+ * hgemm_ex — the fused product of "GPU架构与CUDA", 核函数融合 (matmul, bias
+ * add and ReLU in one kernel: the intermediate never goes to memory), with
+ * BLAS-style scaling:
+ *
+ *   C[i·N + j] = fp16_rne( f( alpha · Σ_k A[i·K + k] · B[j·K + k]
+ *                             + beta · C_old[i·N + j] + bias[j] ) )
+ *
+ * f is max(·, 0) when relu != 0, else the identity; bias holds N FP16 values,
+ * one per column of C (an output feature of the page's matmul(x, W) + bias),
+ * or is NULL. The sum accumulates in FP32 on the tensor cores and the
+ * epilogue arithmetic is FP32, rounded once to FP16. When beta == 0, C is
+ * not read (a NaN there does not propagate); otherwise C is read and
+ * overwritten in place. Layouts, sizes, streams and ownership as for hgemm;
+ * bias must be 2-byte aligned and must not overlap C (HGEMM_ERR_ALIAS).
+ * hgemm(A, B, C, M, N, K, s) is hgemm_ex(A, B, C, M, N, K, 1, 0, NULL, 0, s).
+ * K = 0 gives C := f(beta · C_old + bias). Same return values as hgemm.
+ */
+HGEMM_API int hgemm_ex(const hgemm_half_t *A, const hgemm_half_t *B, hgemm_half_t *C,
+             int64_t M, int64_t N, int64_t K, float alpha, float beta,
+             const hgemm_half_t *bias, int relu, cudaStream_t stream);
+
+/*
  * hgemm_host — the same product for operands held in HOST memory.
  *
  * Copies hA -> dA (M*K values) and hB -> dB (N*K values), computes
@@ -123,6 +145,8 @@ HGEMM_API int hgemm_host(const hgemm_half_t *hA, const hgemm_half_t *hB, hgemm_h
  * hgemm_select_path — the HGEMM_PATH_* that hgemm would run for these
  * arguments on a GB300, or a negative status for invalid arguments. Pure
  * host logic: touches no device and needs no GPU. Honours hgemm_force_path.
+ * hgemm_ex with a fused epilogue takes the same path, except that it takes
+ * HGEMM_PATH_TC_PAIR where this reports HGEMM_PATH_TC_WIDE.
  */
 HGEMM_API int hgemm_select_path(const void *A, const void *B, const void *C,
                       int64_t M, int64_t N, int64_t K);

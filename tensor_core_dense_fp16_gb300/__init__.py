@@ -28,7 +28,7 @@ __all__ = [
     "HgemmError", "library_path", "load", "hgemm", "hgemm_host", "hgemm_select_path",
     "hgemm_force_path", "hgemm_device_status", "hgemm_last_cuda_error",
     "hgemm_status_string", "hgemm_version", "hgemm_set_wait_timeout", "hgemm_debug_inject",
-    "hgemm_force_split",
+    "hgemm_force_split", "hgemm_ex",
     "HGEMM_INJECT_NONE", "HGEMM_INJECT_DROP_ARRIVAL", "matmul",
 ]
 
@@ -85,6 +85,9 @@ def load():
     vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
     lib.hgemm.argtypes = [vp, vp, vp, i64, i64, i64, vp]
     lib.hgemm.restype = i32
+    lib.hgemm_ex.argtypes = [vp, vp, vp, i64, i64, i64, ctypes.c_float, ctypes.c_float, vp,
+                             i32, vp]
+    lib.hgemm_ex.restype = i32
     lib.hgemm_host.argtypes = [vp, vp, vp, i64, i64, i64, vp, vp, vp, vp]
     lib.hgemm_host.restype = i32
     lib.hgemm_select_path.argtypes = [vp, vp, vp, i64, i64, i64]
@@ -172,6 +175,17 @@ def hgemm(A, B, C, M: int, N: int, K: int, stream=None) -> None:
     for x, n in ((A, "A"), (B, "B"), (C, "C")):
         _check_tensor(x, n, True)
     _raise_on(load().hgemm(_ptr(A), _ptr(B), _ptr(C), M, N, K, _stream(stream)), "hgemm")
+
+
+def hgemm_ex(A, B, C, M: int, N: int, K: int, alpha: float = 1.0, beta: float = 0.0, bias=None,
+             relu: bool = False, stream=None) -> None:
+    """C = f(alpha·A·B + beta·C + bias[j]) on `stream`, f = ReLU if relu (see hgemm.h)."""
+    for x, n in ((A, "A"), (B, "B"), (C, "C")):
+        _check_tensor(x, n, True)
+    if bias is not None:
+        _check_tensor(bias, "bias", True)
+    _raise_on(load().hgemm_ex(_ptr(A), _ptr(B), _ptr(C), M, N, K, float(alpha), float(beta),
+                              _ptr(bias), int(bool(relu)), _stream(stream)), "hgemm_ex")
 
 
 def hgemm_host(hA, hB, hC, M: int, N: int, K: int, dA, dB, dC, stream=None) -> None:

@@ -47,6 +47,9 @@ std::mutex g_device_mu;
 constexpr hg::DeviceProfile kNominalProfile{152, 76, 36, 23, 15, 36};
 std::atomic<const hg::DeviceProfile*> g_last_profile{&kNominalProfile};
 
+// The plain product: the accumulator is stored as it is.
+constexpr hg::EpiArgs kPlainEpilogue{1.0f, 0.0f, nullptr, 0, 0};
+
 int cuda_fail(cudaError_t e) {
   t_last_cuda_error = static_cast<int>(e);
   return HGEMM_ERR_CUDA;
@@ -127,7 +130,7 @@ bool tma_ok(const void* A, const void* B, const void* C, int64_t N, int64_t K) {
 }
 
 int choose_path(const void* A, const void* B, const void* C, int64_t M, int64_t N, int64_t K,
-                const hg::DeviceProfile& prof, int* split, int* tile_n) {
+                const hg::DeviceProfile& prof, bool fused, int* split, int* tile_n) {
   *split = 1;
   *tile_n = hg::kPairBN;
   if (M == 0 || N == 0) return HGEMM_PATH_NONE;
@@ -136,7 +139,7 @@ int choose_path(const void* A, const void* B, const void* C, int64_t M, int64_t 
   const int forced = g_forced_path.load(std::memory_order_relaxed);
   if (forced == HGEMM_PATH_GENERIC || !tma) return HGEMM_PATH_GENERIC;
   const int fs = g_forced_split.load(std::memory_order_relaxed);
-  return hg::choose_tma_path(M, N, K, prof, forced, fs >> 10, fs & 1023, split, tile_n);
+  return hg::choose_tma_path(M, N, K, prof, forced, fs >> 10, fs & 1023, fused, split, tile_n);
 }
 
 }  // namespace
@@ -144,7 +147,7 @@ int choose_path(const void* A, const void* B, const void* C, int64_t M, int64_t 
 namespace hg {
 
 int choose_tma_path(int64_t M, int64_t N, int64_t K, const DeviceProfile& dev, int forced,
-                    int forced_split, int forced_tile_n, int* split, int* tile_n) {
+                    int forced_split, int forced_tile_n, bool fused, int* split, int* tile_n) {
   *split = 1;
   *tile_n = kPairBN;
   const int64_t num_m = (M + 2 * kTcBM - 1) / (2 * kTcBM);
@@ -205,10 +208,14 @@ int choose_tma_path(int64_t M, int64_t N, int64_t K, const DeviceProfile& dev, i
   if (num_kb >= 48 && choose(true)) return HGEMM_PATH_SKINNY;
   // A CTA pair covers 256 rows; with 128 rows or fewer half of it would idle.
   if (M <= kTcBM) return HGEMM_PATH_TC;
-  // 256×512 tiles move 25% fewer operand bytes per flop than 256×256 ones;
-  // take them when there are enough of them to give every pair a tile.
+  // 256×512 tiles move 25% fewer operand bytes per flop than 256×256 ones
+  // (measured in runs of 300 launches at 8192³: +1.5%, less power for the
+  // same work under the power cap); take them when there are enough of them
+  // to give every pair a tile. Their accumulator fills TMEM, so the tensor
+  // cores wait for each epilogue: with a fused epilogue the 256×256 tiles,
+  // whose accumulators are double-buffered, are faster (~8% at 8192³).
   const int64_t wide_tiles = ((M + 2 * kTcBM - 1) / (2 * kTcBM)) * ((N + 2 * kPairBN - 1) / (2 * kPairBN));
-  if (wide_tiles >= dev.pair_clusters) return HGEMM_PATH_TC_WIDE;
+  if (!fused && wide_tiles >= dev.pair_clusters) return HGEMM_PATH_TC_WIDE;
   return HGEMM_PATH_TC_PAIR;
 }
 
@@ -266,7 +273,7 @@ int encode_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, i
 }
 
 int run_tc(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
-           const DeviceState& dev, cudaStream_t stream) {
+           const hg::EpiArgs& epi, const DeviceState& dev, cudaStream_t stream) {
   CUtensorMap ma, mb, mc;
   int rc;
   if ((rc = encode_map(&ma, A, M, K, hg::kTcBM, hg::kTcBK)) != HGEMM_OK) return rc;
@@ -288,12 +295,14 @@ int run_tc(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t 
   args.status = dev.status;
   args.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
   args.inject = g_inject.load(std::memory_order_relaxed);
+  args.epi = epi;
+  args.C = static_cast<const uint16_t*>(C);
   cudaError_t e = hg::launch_tc_128x256(ma, mb, mc, args, stream);
   return e == cudaSuccess ? HGEMM_OK : cuda_fail(e);
 }
 
 int run_tc_pair(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
-                const DeviceState& dev, cudaStream_t stream) {
+                const hg::EpiArgs& epi, const DeviceState& dev, cudaStream_t stream) {
   hg::TcArgs args{};
   args.M = static_cast<int>(M);
   args.N = static_cast<int>(N);
@@ -327,6 +336,8 @@ int run_tc_pair(const void* A, const void* B, void* C, int64_t M, int64_t N, int
   args.status = dev.status;
   args.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
   args.inject = g_inject.load(std::memory_order_relaxed);
+  args.epi = epi;
+  args.C = static_cast<const uint16_t*>(C);
   CUtensorMap ma, mb, mbp, mc;
   int rc;
   if ((rc = encode_map(&ma, A, M, K, hg::kTcBM, hg::kTcBK)) != HGEMM_OK) return rc;
@@ -338,7 +349,7 @@ int run_tc_pair(const void* A, const void* B, void* C, int64_t M, int64_t N, int
 }
 
 int run_tc_wide(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
-                const DeviceState& dev, cudaStream_t stream) {
+                const hg::EpiArgs& epi, const DeviceState& dev, cudaStream_t stream) {
   CUtensorMap ma, mb, mc;
   int rc;
   if ((rc = encode_map(&ma, A, M, K, hg::kTcBM, hg::kTcBK)) != HGEMM_OK) return rc;
@@ -361,12 +372,14 @@ int run_tc_wide(const void* A, const void* B, void* C, int64_t M, int64_t N, int
   args.status = dev.status;
   args.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
   args.inject = g_inject.load(std::memory_order_relaxed);
+  args.epi = epi;
+  args.C = static_cast<const uint16_t*>(C);
   cudaError_t e = hg::launch_tc_wide(ma, mb, mc, args, stream);
   return e == cudaSuccess ? HGEMM_OK : cuda_fail(e);
 }
 
 int run_skinny(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int split,
-               int tile_n, const DeviceState& dev, cudaStream_t stream) {
+               int tile_n, const hg::EpiArgs& epi, const DeviceState& dev, cudaStream_t stream) {
   CUtensorMap ma, mb, mc;
   int rc;
   if ((rc = encode_map(&ma, A, M, K, hg::kTcBM, hg::kTcBK)) != HGEMM_OK) return rc;
@@ -388,30 +401,32 @@ int run_skinny(const void* A, const void* B, void* C, int64_t M, int64_t N, int6
   args.status = dev.status;
   args.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
   args.inject = g_inject.load(std::memory_order_relaxed);
+  args.epi = epi;
+  args.C = static_cast<const uint16_t*>(C);
   cudaError_t e = hg::launch_skinny(split, tile_n, ma, mb, mc, args, stream);
   return e == cudaSuccess ? HGEMM_OK : cuda_fail(e);
 }
 
 int dispatch(const hgemm_half_t* A, const hgemm_half_t* B, hgemm_half_t* C, int64_t M, int64_t N,
-             int64_t K, const DeviceState& dev, cudaStream_t stream) {
+             int64_t K, const hg::EpiArgs& epi, const DeviceState& dev, cudaStream_t stream) {
   cudaError_t e;
   int split = 1, tile_n = hg::kPairBN;
-  switch (choose_path(A, B, C, M, N, K, dev.prof, &split, &tile_n)) {
+  switch (choose_path(A, B, C, M, N, K, dev.prof, epi.mode != 0, &split, &tile_n)) {
     case HGEMM_PATH_NONE:
       return HGEMM_OK;
     case HGEMM_PATH_ZERO:
-      e = hg::launch_zero_fill(C, M * N, stream);
+      e = hg::launch_empty_sum(C, M, N, epi, stream);
       return e == cudaSuccess ? HGEMM_OK : cuda_fail(e);
     case HGEMM_PATH_TC:
-      return run_tc(A, B, C, M, N, K, dev, stream);
+      return run_tc(A, B, C, M, N, K, epi, dev, stream);
     case HGEMM_PATH_TC_PAIR:
-      return run_tc_pair(A, B, C, M, N, K, dev, stream);
+      return run_tc_pair(A, B, C, M, N, K, epi, dev, stream);
     case HGEMM_PATH_TC_WIDE:
-      return run_tc_wide(A, B, C, M, N, K, dev, stream);
+      return run_tc_wide(A, B, C, M, N, K, epi, dev, stream);
     case HGEMM_PATH_SKINNY:
-      return run_skinny(A, B, C, M, N, K, split, tile_n, dev, stream);
+      return run_skinny(A, B, C, M, N, K, split, tile_n, epi, dev, stream);
     default: {
-      hg::PlainArgs pa{A, B, C, M, N, K, dev.status, g_timeout_ns.load()};
+      hg::PlainArgs pa{A, B, C, M, N, K, dev.status, g_timeout_ns.load(), epi};
       e = hg::launch_generic(pa, dev.num_sms, stream);
       return e == cudaSuccess ? HGEMM_OK : cuda_fail(e);
     }
@@ -458,7 +473,28 @@ int hgemm(const hgemm_half_t* A, const hgemm_half_t* B, hgemm_half_t* C, int64_t
   if (M == 0 || N == 0) return HGEMM_OK;
   DeviceState* dev = nullptr;
   if ((rc = current_device(&dev)) != HGEMM_OK) return rc;
-  return dispatch(A, B, C, M, N, K, *dev, stream);
+  return dispatch(A, B, C, M, N, K, kPlainEpilogue, *dev, stream);
+}
+
+int hgemm_ex(const hgemm_half_t* A, const hgemm_half_t* B, hgemm_half_t* C, int64_t M, int64_t N,
+             int64_t K, float alpha, float beta, const hgemm_half_t* bias, int relu,
+             cudaStream_t stream) {
+  int rc = validate(A, B, C, M, N, K);
+  if (rc != HGEMM_OK) return rc;
+  if (bias) {
+    if (reinterpret_cast<uintptr_t>(bias) & 1u) return HGEMM_ERR_INVALID_ARG;
+    // C is written while bias is read
+    if (M > 0 && N > 0 &&
+        ranges_overlap(C, 2 * static_cast<uint64_t>(M) * static_cast<uint64_t>(N), bias,
+                       2 * static_cast<uint64_t>(N)))
+      return HGEMM_ERR_ALIAS;
+  }
+  if (M == 0 || N == 0) return HGEMM_OK;
+  hg::EpiArgs epi{alpha, beta, reinterpret_cast<const uint16_t*>(bias), relu ? 1 : 0, 0};
+  epi.mode = beta != 0.0f ? 2 : ((alpha != 1.0f || bias || relu) ? 1 : 0);
+  DeviceState* dev = nullptr;
+  if ((rc = current_device(&dev)) != HGEMM_OK) return rc;
+  return dispatch(A, B, C, M, N, K, epi, *dev, stream);
 }
 
 int hgemm_host(const hgemm_half_t* hA, const hgemm_half_t* hB, hgemm_half_t* hC, int64_t M,
@@ -487,7 +523,7 @@ int hgemm_host(const hgemm_half_t* hA, const hgemm_half_t* hB, hgemm_half_t* hC,
     if (N * K &&
         (e = cudaMemcpyAsync(dB, hB, 2 * N * K, cudaMemcpyHostToDevice, stream)) != cudaSuccess)
       return cuda_fail(e);
-    if ((rc = dispatch(dA, dB, dC, M, N, K, *dev, stream)) != HGEMM_OK) return rc;
+    if ((rc = dispatch(dA, dB, dC, M, N, K, kPlainEpilogue, *dev, stream)) != HGEMM_OK) return rc;
     if ((e = cudaMemcpyAsync(hC, dC, 2 * M * N, cudaMemcpyDeviceToHost, stream)) != cudaSuccess)
       return cuda_fail(e);
     return HGEMM_OK;
@@ -513,7 +549,9 @@ int hgemm_host(const hgemm_half_t* hA, const hgemm_half_t* hB, hgemm_half_t* hC,
     if ((e = cudaEventRecord(in_done, hp->in)) != cudaSuccess ||
         (e = cudaStreamWaitEvent(stream, in_done, 0)) != cudaSuccess)
       return cuda_fail(e);
-    if ((rc = dispatch(dA + r0 * K, dB, dC + r0 * N, mi, N, K, *dev, stream)) != HGEMM_OK) return rc;
+    if ((rc = dispatch(dA + r0 * K, dB, dC + r0 * N, mi, N, K, kPlainEpilogue, *dev, stream)) !=
+        HGEMM_OK)
+      return rc;
     if ((e = cudaEventRecord(prod_done, stream)) != cudaSuccess ||
         (e = cudaStreamWaitEvent(hp->out, prod_done, 0)) != cudaSuccess)
       return cuda_fail(e);
@@ -533,7 +571,8 @@ int hgemm_select_path(const void* A, const void* B, const void* C, int64_t M, in
   int rc = validate(A, B, C, M, N, K);
   if (rc != HGEMM_OK) return rc;
   int split = 1, tile_n = hg::kPairBN;
-  return choose_path(A, B, C, M, N, K, *g_last_profile.load(std::memory_order_acquire), &split, &tile_n);
+  return choose_path(A, B, C, M, N, K, *g_last_profile.load(std::memory_order_acquire), false, &split,
+                     &tile_n);
 }
 
 int hgemm_force_split(int split, int tile_n) {

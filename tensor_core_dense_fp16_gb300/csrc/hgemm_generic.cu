@@ -176,9 +176,17 @@ __global__ void __launch_bounds__(GenCfg::THREADS, 1)
         tmem_ld_wait(v);
         if (gi < p.M) {
           uint16_t* dst = p.C + gi * p.N + n0 + c * 32;
+          const __half* bias = reinterpret_cast<const __half*>(p.epi.bias);
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (n0 + c * 32 + j < p.N) dst[j] = __half_as_ushort(__float2half_rn(__uint_as_float(v[j])));
+          for (int j = 0; j < 32; ++j) {
+            const int64_t col = n0 + c * 32 + j;
+            if (col >= p.N) continue;
+            float x = __uint_as_float(v[j]);
+            if (p.epi.mode != 0)
+              x = epi_value(x, p.epi, p.epi.mode == 2 ? __half2float(__ushort_as_half(dst[j])) : 0.f,
+                            bias ? __half2float(bias[col]) : 0.f);
+            dst[j] = __half_as_ushort(__float2half_rn(x));
+          }
         }
       }
     }

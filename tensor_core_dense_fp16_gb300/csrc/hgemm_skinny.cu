@@ -91,7 +91,7 @@ __device__ __forceinline__ uint32_t f32_block_offset(int r, int c, int cols) {
   return static_cast<uint32_t>(r * cols * 4 + ((c ^ (r & 7)) << 4));
 }
 
-template <int SPLIT, int BN>
+template <int SPLIT, int BN, bool FUSED>
 __global__ void __launch_bounds__(192, 1)
     hgemm_skinny_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC, const TcArgs p) {
@@ -239,6 +239,9 @@ __global__ void __launch_bounds__(192, 1)
   const int q = warp & 3;  // TMEM lanes / tile rows 32q .. 32q+31 of this CTA
   const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
   const int row = q * 32 + lane;
+  if (FUSED && warp >= 2)
+    prefetch_c_row(p.epi, p.C, p.M, p.N, static_cast<int64_t>(mb) * Cfg::BM + half * Cfg::ROWS + row,
+                   static_cast<int64_t>(nb) * Cfg::BN + own_c0, own_cols);
   // ring layout for the exchange: receive slots first, then send staging
   const uint32_t recv_base = sbase;
   const uint32_t send_base = sbase + static_cast<uint32_t>((SPLIT - 1) * Cfg::ROWS * own_cols * 4);
@@ -325,10 +328,19 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           uint4 pk;
-          pk.x = pack_half2(__float_as_uint(acc[8 * u]), __float_as_uint(acc[8 * u + 1]));
-          pk.y = pack_half2(__float_as_uint(acc[8 * u + 2]), __float_as_uint(acc[8 * u + 3]));
-          pk.z = pack_half2(__float_as_uint(acc[8 * u + 4]), __float_as_uint(acc[8 * u + 5]));
-          pk.w = pack_half2(__float_as_uint(acc[8 * u + 6]), __float_as_uint(acc[8 * u + 7]));
+          if constexpr (!FUSED) {
+            pk.x = pack_half2(__float_as_uint(acc[8 * u]), __float_as_uint(acc[8 * u + 1]));
+            pk.y = pack_half2(__float_as_uint(acc[8 * u + 2]), __float_as_uint(acc[8 * u + 3]));
+            pk.z = pack_half2(__float_as_uint(acc[8 * u + 4]), __float_as_uint(acc[8 * u + 5]));
+            pk.w = pack_half2(__float_as_uint(acc[8 * u + 6]), __float_as_uint(acc[8 * u + 7]));
+          } else {
+            uint32_t vb[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) vb[i] = __float_as_uint(acc[8 * u + i]);
+            const int64_t col0 = static_cast<int64_t>(x0) + c32 * 32 + 8 * u;
+            pk = epi_pack8(vb, p.epi, load_c_old8(p.epi, p.C, p.M, p.N, y0 + lane, col0),
+                           load_bias8(p.epi, col0, p.N));
+          }
           const int chunk = c32 * 4 + u;  // 16-byte chunk within the row
           const int box = chunk >> 3;     // 64-column box
           const int cin = chunk & 7;
@@ -365,15 +377,16 @@ template <int SPLIT, int BN>
 cudaError_t launch_split(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
                          const TcArgs& args, cudaStream_t stream) {
   using Cfg = SkCfg<SPLIT, BN>;
-  static bool attr_done[64] = {};
-  auto kern = hgemm_skinny_kernel<SPLIT, BN>;
+  static bool attr_done[2][64] = {};
+  const int fused = args.epi.mode != 0 ? 1 : 0;
+  auto kern = fused ? hgemm_skinny_kernel<SPLIT, BN, true> : hgemm_skinny_kernel<SPLIT, BN, false>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64 || !attr_done[dev]) {
+  if (dev < 0 || dev >= 64 || !attr_done[fused][dev]) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) attr_done[dev] = true;
+    if (dev >= 0 && dev < 64) attr_done[fused][dev] = true;
   }
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -393,7 +406,7 @@ cudaError_t launch_split(const CUtensorMap& a, const CUtensorMap& b, const CUten
 template <int SPLIT, int BN>
 int max_clusters_split(int num_sms) {
   using Cfg = SkCfg<SPLIT, BN>;
-  auto kern = hgemm_skinny_kernel<SPLIT, BN>;
+  auto kern = hgemm_skinny_kernel<SPLIT, BN, false>;
   int n = 0;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) ==
       cudaSuccess) {

@@ -77,7 +77,7 @@ struct TcCfg {
   static_assert(SMEM_BYTES <= 232448, "exceeds 227 KB of shared memory per CTA");
 };
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, bool FUSED>
 __global__ void __launch_bounds__(192, 1)
     hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmC, const TcArgs p) {
@@ -223,6 +223,9 @@ __global__ void __launch_bounds__(192, 1)
     for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
       int mb, nb;
       tile_coords(t, p.num_m, p.num_n, p.group_m, mb, nb);
+      if constexpr (FUSED)
+        prefetch_c_row(p.epi, p.C, p.M, p.N, static_cast<int64_t>(mb) * Cfg::BM + q * kEpiRows + lane,
+                       static_cast<int64_t>(nb) * BN, BN);
       int ok = 1;
       if (lane == 0) ok = wait_phase(accf_bar(acc), acc_phase, wd, kWdEpiAccFull) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -251,17 +254,8 @@ __global__ void __launch_bounds__(192, 1)
         __syncwarp();
         uint8_t* buf = cbuf_base + cb * Cfg::C_BOX_BYTES;
         uint8_t* row = buf + lane * 128;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint32_t* v = (j < 4) ? (v0 + 8 * j) : (v1 + 8 * (j - 4));
-          uint4 pk;
-          pk.x = pack_half2(v[0], v[1]);
-          pk.y = pack_half2(v[2], v[3]);
-          pk.z = pack_half2(v[4], v[5]);
-          pk.w = pack_half2(v[6], v[7]);
-          // 128-byte swizzle: 16-byte chunk j of row r sits at chunk j ^ (r % 8)
-          *reinterpret_cast<uint4*>(row + ((j ^ (lane & 7)) << 4)) = pk;
-        }
+        // 128-byte swizzle: 16-byte chunk j of row r sits at chunk j ^ (r % 8)
+        stage_row64<FUSED>(row, lane, v0, v1, p.epi, p.C, p.M, p.N, static_cast<int64_t>(y0) + lane, x0);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
@@ -283,11 +277,22 @@ __global__ void __launch_bounds__(192, 1)
   if (warp == 1) tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
 }
 
-__global__ void zero_fill_kernel(uint16_t* __restrict__ C, int64_t count) {
+// K = 0: every sum is empty, so C := f(beta·C_old + bias) (alpha·0 = 0), or
+// +0 for the plain product.
+__global__ void empty_sum_kernel(uint16_t* __restrict__ C, int64_t M, int64_t N, const EpiArgs e) {
+  const int64_t count = M * N;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const __half* bias = reinterpret_cast<const __half*>(e.bias);
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < count;
-       i += stride)
-    C[i] = 0;
+       i += stride) {
+    if (e.mode == 0) {
+      C[i] = 0;
+      continue;
+    }
+    const float c_old = e.mode == 2 ? __half2float(__ushort_as_half(C[i])) : 0.f;
+    const float b = bias ? __half2float(bias[i % N]) : 0.f;
+    C[i] = __half_as_ushort(__float2half_rn(epi_value(0.f, e, c_old, b)));
+  }
 }
 
 template <typename Kern>
@@ -306,9 +311,10 @@ cudaError_t ensure_smem_attr(Kern kern, int bytes, bool* done_per_device) {
 cudaError_t launch_tc_128x256(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
                               const TcArgs& args, cudaStream_t stream) {
   using Cfg = TcCfg<256, 4>;
-  static bool attr_done[64] = {};
-  auto kern = hgemm_tc_kernel<256, 4>;
-  cudaError_t e = ensure_smem_attr(kern, Cfg::SMEM_BYTES, attr_done);
+  static bool attr_done[2][64] = {};
+  const bool fused = args.epi.mode != 0;
+  auto kern = fused ? hgemm_tc_kernel<256, 4, true> : hgemm_tc_kernel<256, 4, false>;
+  cudaError_t e = ensure_smem_attr(kern, Cfg::SMEM_BYTES, attr_done[fused ? 1 : 0]);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(args.grid));
@@ -318,11 +324,13 @@ cudaError_t launch_tc_128x256(const CUtensorMap& a, const CUtensorMap& b, const 
   return cudaLaunchKernelEx(&cfg, kern, a, b, c, args);
 }
 
-cudaError_t launch_zero_fill(uint16_t* C, int64_t count, cudaStream_t stream) {
+cudaError_t launch_empty_sum(uint16_t* C, int64_t M, int64_t N, const EpiArgs& epi,
+                             cudaStream_t stream) {
+  const int64_t count = M * N;
   int blocks = static_cast<int>((count + 255) / 256);
   if (blocks > 4096) blocks = 4096;
   if (blocks < 1) blocks = 1;
-  zero_fill_kernel<<<blocks, 256, 0, stream>>>(C, count);
+  empty_sum_kernel<<<blocks, 256, 0, stream>>>(C, M, N, epi);
   return cudaGetLastError();
 }
 

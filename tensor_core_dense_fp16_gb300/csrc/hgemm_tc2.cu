@@ -101,7 +101,7 @@ __device__ __forceinline__ PairTile pair_tile(int t, const TcArgs& p) {
   return w;
 }
 
-template <int MAX_STAGES>
+template <int MAX_STAGES, bool FUSED>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     hgemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmBh, const __grid_constant__ CUtensorMap tmC,
@@ -271,6 +271,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     for (int t = cluster_id; t < p.num_tiles; t += num_clusters) {
       const PairTile w = pair_tile(t, p);
       const int chunks = w.ncols / kEpiCols;
+      if constexpr (FUSED)
+        prefetch_c_row(p.epi, p.C, p.M, p.N,
+                       static_cast<int64_t>(w.mb) * Cfg::BM + static_cast<int>(rank) * Cfg::ROWS + q * kEpiRows + lane,
+                       w.n0, w.ncols);
       int ok = 1;
       if (lane == 0)
         ok = wait_phase(accf_bar(acc), acc_phase, wd, kWdEpiAccFull) ? 1 : 0;
@@ -298,16 +302,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
         __syncwarp();
         uint8_t* buf = cbuf_base + cb * Cfg::C_BOX_BYTES;
         uint8_t* row = buf + lane * 128;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint32_t* v = (j < 4) ? (v0 + 8 * j) : (v1 + 8 * (j - 4));
-          uint4 pk;
-          pk.x = pack_half2(v[0], v[1]);
-          pk.y = pack_half2(v[2], v[3]);
-          pk.z = pack_half2(v[4], v[5]);
-          pk.w = pack_half2(v[6], v[7]);
-          *reinterpret_cast<uint4*>(row + ((j ^ (lane & 7)) << 4)) = pk;
-        }
+        // 128-byte swizzle: 16-byte chunk j of row r sits at chunk j ^ (r % 8)
+        stage_row64<FUSED>(row, lane, v0, v1, p.epi, p.C, p.M, p.N, static_cast<int64_t>(y0) + lane, x0);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
@@ -340,7 +336,7 @@ int pair_max_clusters(int num_sms) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return num_sms / 2;
   if (cached[dev] > 0) return cached[dev];
-  auto kern = hgemm_tc2_kernel<kPairStages>;
+  auto kern = hgemm_tc2_kernel<kPairStages, false>;
   int n = 0;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) ==
       cudaSuccess) {
@@ -359,15 +355,16 @@ int pair_max_clusters(int num_sms) {
 cudaError_t launch_tc_pair(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b_part,
                            const CUtensorMap& c, const TcArgs& args, cudaStream_t stream) {
   using Cfg = PairCfg<kPairStages>;
-  static bool attr_done[64] = {};
-  auto kern = hgemm_tc2_kernel<kPairStages>;
+  static bool attr_done[2][64] = {};
+  const int fused = args.epi.mode != 0 ? 1 : 0;
+  auto kern = fused ? hgemm_tc2_kernel<kPairStages, true> : hgemm_tc2_kernel<kPairStages, false>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64 || !attr_done[dev]) {
+  if (dev < 0 || dev >= 64 || !attr_done[fused][dev]) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) attr_done[dev] = true;
+    if (dev >= 0 && dev < 64) attr_done[fused][dev] = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(args.grid));

@@ -71,6 +71,7 @@ struct WideCfg {
   static_assert(SMEM_BYTES <= 232448, "exceeds 227 KB of shared memory per CTA");
 };
 
+template <bool FUSED>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
     hgemm_tc2w_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const __grid_constant__ CUtensorMap tmC, const TcArgs p) {
@@ -232,6 +233,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
     for (int t = cluster_id; t < p.num_tiles; t += num_clusters) {
       int mb, nb;
       tile_coords(t, p.num_m, p.num_n, p.group_m, mb, nb);
+      if constexpr (FUSED)
+        prefetch_c_row(p.epi, p.C, p.M, p.N,
+                       static_cast<int64_t>(mb) * Cfg::BM + static_cast<int>(rank) * Cfg::ROWS + q * kEpiRows + lane,
+                       static_cast<int64_t>(nb) * Cfg::BN + h * kPairBN, kPairBN);
       int ok = 1;
       if (lane == 0) ok = wait_phase(accf_bar, tile_phase, wd, kWdEpiAccFull) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -259,16 +264,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
         if (lane == 0) bulk_wait_group_read<0>();  // the previous store has read the box
         __syncwarp();
         uint8_t* row = buf + lane * 128;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint32_t* v = (j < 4) ? (v0 + 8 * j) : (v1 + 8 * (j - 4));
-          uint4 pk;
-          pk.x = pack_half2(v[0], v[1]);
-          pk.y = pack_half2(v[2], v[3]);
-          pk.z = pack_half2(v[4], v[5]);
-          pk.w = pack_half2(v[6], v[7]);
-          *reinterpret_cast<uint4*>(row + ((j ^ (lane & 7)) << 4)) = pk;
-        }
+        // 128-byte swizzle: 16-byte chunk j of row r sits at chunk j ^ (r % 8)
+        stage_row64<FUSED>(row, lane, v0, v1, p.epi, p.C, p.M, p.N, static_cast<int64_t>(y0) + lane, x0);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
@@ -297,13 +294,13 @@ int wide_max_clusters(int num_sms) {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return num_sms / 2;
   if (cached[dev] > 0) return cached[dev];
   int n = 0;
-  if (cudaFuncSetAttribute(hgemm_tc2w_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(hgemm_tc2w_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            WideCfg::SMEM_BYTES) == cudaSuccess) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(num_sms & ~1));
     cfg.blockDim = dim3(WideCfg::THREADS);
     cfg.dynamicSmemBytes = WideCfg::SMEM_BYTES;
-    if (cudaOccupancyMaxActiveClusters(&n, hgemm_tc2w_kernel, &cfg) != cudaSuccess) n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, hgemm_tc2w_kernel<false>, &cfg) != cudaSuccess) n = 0;
   }
   (void)cudaGetLastError();
   if (n <= 0) n = num_sms / 2;
@@ -313,22 +310,23 @@ int wide_max_clusters(int num_sms) {
 
 cudaError_t launch_tc_wide(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
                            const TcArgs& args, cudaStream_t stream) {
-  static bool attr_done[64] = {};
+  static bool attr_done[2][64] = {};
+  const int fused = args.epi.mode != 0 ? 1 : 0;
+  auto kern = fused ? hgemm_tc2w_kernel<true> : hgemm_tc2w_kernel<false>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64 || !attr_done[dev]) {
-    e = cudaFuncSetAttribute(hgemm_tc2w_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             WideCfg::SMEM_BYTES);
+  if (dev < 0 || dev >= 64 || !attr_done[fused][dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, WideCfg::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) attr_done[dev] = true;
+    if (dev >= 0 && dev < 64) attr_done[fused][dev] = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(args.grid));
   cfg.blockDim = dim3(WideCfg::THREADS);
   cfg.dynamicSmemBytes = WideCfg::SMEM_BYTES;
   cfg.stream = stream;
-  return cudaLaunchKernelEx(&cfg, hgemm_tc2w_kernel, a, b, c, args);
+  return cudaLaunchKernelEx(&cfg, kern, a, b, c, args);
 }
 
 }  // namespace hg

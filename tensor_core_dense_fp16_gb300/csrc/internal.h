@@ -20,6 +20,17 @@ enum WatchdogCode : int {
   kWdReduce = 6,          // split-K owner waiting for the other slices' partials
 };
 
+// The fused epilogue ("GPU架构与CUDA", 核函数融合): each FP32 accumulator
+// becomes alpha·acc + beta·C_old + bias[col], then max(·, 0) when relu is
+// set, before the single rounding to FP16. mode 0: plain product (the
+// accumulator is stored as is); 1: fused, C not read; 2: fused, C read.
+struct EpiArgs {
+  float alpha, beta;
+  const uint16_t* bias;  // N FP16 values (one per column of C), or null
+  int relu;
+  int mode;
+};
+
 // Everything a tensor-core launch needs besides the tensor maps.
 struct TcArgs {
   int M, N, K;
@@ -34,6 +45,8 @@ struct TcArgs {
   int* status;               // device watchdog word
   unsigned long long timeout_ns;
   int inject;                // HGEMM_INJECT_* (testing the watchdog)
+  EpiArgs epi;
+  const uint16_t* C;         // C itself, read in epilogue mode 2
 };
 
 // Plain-pointer launch arguments for the kernels that do not use TMA.
@@ -44,6 +57,7 @@ struct PlainArgs {
   int64_t M, N, K;
   int* status;
   unsigned long long timeout_ns;
+  EpiArgs epi;
 };
 
 // Launchers (each enqueues one kernel on `stream` and returns the launch
@@ -66,7 +80,9 @@ cudaError_t launch_skinny(int split, int tile_n, const CUtensorMap& a, const CUt
                           const CUtensorMap& c, const TcArgs& args, cudaStream_t stream);
 // Largest number of co-resident clusters of the split-K kernel.
 int skinny_max_clusters(int split, int tile_n, int num_sms);
-cudaError_t launch_zero_fill(uint16_t* C, int64_t count, cudaStream_t stream);
+// K = 0: C := f(beta·C_old + bias) elementwise (plain mode: +0).
+cudaError_t launch_empty_sum(uint16_t* C, int64_t M, int64_t N, const EpiArgs& epi,
+                             cudaStream_t stream);
 cudaError_t launch_generic(const PlainArgs& args, int num_sms, cudaStream_t stream);
 
 // Address of the device watchdog word on the current device.
@@ -86,9 +102,10 @@ struct DeviceProfile {
 // Kernel choice for a TMA-able product. Returns an HGEMM_PATH_* value and,
 // for the split-K path, the number of K-slices in *split and the tile width
 // in *tile_n. forced: a forced HGEMM_PATH_* or -1; forced_split and
-// forced_tile_n: a forced split-K configuration or 0.
+// forced_tile_n: a forced split-K configuration or 0; fused: the product
+// has a fused epilogue (hgemm_ex other than the plain product).
 int choose_tma_path(int64_t M, int64_t N, int64_t K, const DeviceProfile& dev, int forced,
-                    int forced_split, int forced_tile_n, int* split, int* tile_n);
+                    int forced_split, int forced_tile_n, bool fused, int* split, int* tile_n);
 
 // Tile geometry of the tensor-core path, for the host-side tensor maps.
 constexpr int kTcBM = 128;

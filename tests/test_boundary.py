@@ -139,6 +139,20 @@ def test_forced_split_configuration(lib):
         tc.hgemm_force_path(-1)
 
 
+def test_fused_argument_checks(lib):
+    """hgemm_ex rejects a misaligned bias and a bias that overlaps C before any
+    device work (fake addresses)."""
+    lib_ = tc.load()
+    rc = lib_.hgemm_ex(A16, B16, C16, 4, 8, 8, 1.0, 0.0, 0x40000001, 0, None)
+    assert rc == tc.HGEMM_ERR_INVALID_ARG
+    rc = lib_.hgemm_ex(A16, B16, C16, 4, 8, 8, 1.0, 1.0, C16 + 16, 1, None)
+    assert rc == tc.HGEMM_ERR_ALIAS
+    rc = lib_.hgemm_ex(A16, B16, C16, -1, 8, 8, 1.0, 1.0, None, 0, None)
+    assert rc == tc.HGEMM_ERR_INVALID_ARG
+    # empty output: nothing to do, no device needed
+    assert lib_.hgemm_ex(A16, B16, C16, 0, 8, 8, 2.0, 1.0, 0x40000000, 1, None) == tc.HGEMM_OK
+
+
 def test_invalid_arguments_rejected_before_any_device_work(lib):
     bad = [
         (A16, B16, C16, -1, 4, 4),
