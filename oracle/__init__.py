@@ -63,6 +63,9 @@ def _load():
                                                 i64, ctypes.c_double, ctypes.c_double, u16p, u16p,
                                                 ctypes.c_int, u16p]
         lib.oracle_hgemm_entries_ex.restype = None
+        lib.oracle_trmm.argtypes = [u16p, i64, u16p, i64, u16p, i64, i64, i64, ctypes.c_double,
+                                    ctypes.c_int]
+        lib.oracle_trmm.restype = ctypes.c_int
         lib.oracle_fp16_to_double.argtypes = [ctypes.c_uint16]
         lib.oracle_fp16_to_double.restype = ctypes.c_double
         lib.oracle_double_to_fp16.argtypes = [ctypes.c_double]
@@ -181,6 +184,26 @@ def entries_ex(a: np.ndarray, b: np.ndarray, rows, cols, c: np.ndarray | None = 
                                     bias.ctypes.data if bias is not None else None,
                                     int(bool(relu)), out.ctypes.data)
     return out
+
+
+def trmm(a: np.ndarray, b: np.ndarray, alpha: float = 1.0, nthreads: int | None = None) -> np.ndarray:
+    """The TRMM page's product C = fp16(alpha·Aᵀ·B), (n, m) float16, for a
+    (n, n) whose lower triangle is A (the rest is not read) and b (n, m).
+    Arrays are in mathematical orientation; the C code reads them column-major."""
+    a = np.asarray(a, dtype=np.float16)
+    b = np.asarray(b, dtype=np.float16)
+    n = a.shape[0]
+    if a.shape != (n, n) or b.ndim != 2 or b.shape[0] != n:
+        raise ValueError("a must be (n, n) and b (n, m)")
+    m = b.shape[1]
+    a_col = np.ascontiguousarray(a.T)      # column c of A is row c here: A(r, c) at [c*n + r]
+    b_col = np.ascontiguousarray(b.T)
+    c_col = np.empty((m, n), dtype=np.float16)
+    rc = _load().oracle_trmm(a_col.ctypes.data, n, b_col.ctypes.data, n, c_col.ctypes.data, n, n, m,
+                             float(alpha), _threads(nthreads))
+    if rc != 0:
+        raise MemoryError("oracle_trmm could not allocate its thread bookkeeping")
+    return np.ascontiguousarray(c_col.T)
 
 
 def fp16_to_double(bits: int) -> float:

@@ -262,3 +262,76 @@ void oracle_hgemm_entries_ex(const uint16_t *A, const uint16_t *B, int64_t K,
         out[t] = oracle_double_to_fp16(apply_epilogue(&ep, s, c_old ? c_old[t] : 0, cols[t]));
     }
 }
+
+/* ---- the triangular product ---------------------------------------------
+ *
+ * "异构计算中高性能TRMM与TRSM的递归算法实现", §2.2: left side, lower triangle,
+ * transposed (B ← alpha·Aᵀ·B), computed out of place, every matrix
+ * column-major as on the page:
+ *
+ *     C(i,j) = fp16_rne( alpha · Σ_{k=i}^{n-1} A(k,i) · B(k,j) )
+ *
+ * with A(r,c) = A[c*lda + r], B(r,j) = B[j*ldb + r], C(r,j) = C[j*ldc + r].
+ * Only the lower triangle of A (row k ≥ column i) is read. The sum runs in
+ * increasing k in FP64 and is rounded once: the plain definition, not the
+ * page's recursion (which reaches the same value up to rounding). */
+
+struct trmm_job {
+    const uint16_t *A, *B;
+    uint16_t *C;
+    int64_t lda, ldb, ldc, n;
+    double alpha;
+    int64_t col_lo, col_hi;
+};
+
+static void *trmm_worker(void *arg)
+{
+    const struct trmm_job *jb = (const struct trmm_job *)arg;
+    for (int64_t j = jb->col_lo; j < jb->col_hi; ++j)
+        for (int64_t i = 0; i < jb->n; ++i) {
+            double s = 0.0;
+            for (int64_t k = i; k < jb->n; ++k)
+                s += g_decode[jb->A[i * jb->lda + k]] * g_decode[jb->B[j * jb->ldb + k]];
+            jb->C[j * jb->ldc + i] = oracle_double_to_fp16(jb->alpha * s);
+        }
+    return NULL;
+}
+
+int oracle_trmm(const uint16_t *A, int64_t lda, const uint16_t *B, int64_t ldb, uint16_t *C,
+                int64_t ldc, int64_t n, int64_t m, double alpha, int nthreads)
+{
+    pthread_once(&g_decode_once, fill_decode_table);
+    if (n <= 0 || m <= 0)
+        return 0;
+    if (nthreads < 1)
+        nthreads = 1;
+    if (nthreads > m)
+        nthreads = (int)m;
+    pthread_t *th = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    struct trmm_job *jobs = (struct trmm_job *)calloc((size_t)nthreads, sizeof(struct trmm_job));
+    char *live = (char *)calloc((size_t)nthreads, 1);
+    if (!th || !jobs || !live) {
+        free(th);
+        free(jobs);
+        free(live);
+        return -1;
+    }
+    for (int t = 0; t < nthreads; ++t) {
+        struct trmm_job jb = {A, B, C, lda, ldb, ldc, n, alpha, m * t / nthreads, m * (t + 1) / nthreads};
+        jobs[t] = jb;
+        if (t == 0)
+            continue;
+        if (pthread_create(&th[t], NULL, trmm_worker, &jobs[t]) == 0)
+            live[t] = 1;
+        else
+            trmm_worker(&jobs[t]);
+    }
+    trmm_worker(&jobs[0]);
+    for (int t = 1; t < nthreads; ++t)
+        if (live[t])
+            pthread_join(th[t], NULL);
+    free(live);
+    free(th);
+    free(jobs);
+    return 0;
+}

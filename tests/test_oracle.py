@@ -338,3 +338,55 @@ def test_fused_entries_agree_with_full_product():
     cols = rng.integers(0, 33, 200)
     part = oracle.entries_ex(a, b, rows, cols, c, alpha=0.75, beta=-1.25, bias=bias, relu=True)
     assert np.array_equal(bits(part), bits(full[rows, cols]))
+
+
+# ---------------------------------------------------------------------------
+# the triangular product of the TRMM page: C = fp16(alpha·Aᵀ·B), A lower
+
+
+def test_trmm_bruteforce_exact_rationals():
+    rng = np.random.default_rng(41)
+    for n, m in [(1, 1), (2, 3), (3, 2), (5, 4), (6, 6)]:
+        a = random_fp16(rng, (n, n))
+        b = random_fp16(rng, (n, m))
+        got = bits(oracle.trmm(a, b, alpha=0.75))
+        for i in range(n):
+            for j in range(m):
+                v = Fraction(0)
+                for k in range(i, n):    # A(k, i) with k >= i: the lower triangle
+                    v += Fraction(float(a[k, i])) * Fraction(float(b[k, j]))
+                assert got[i, j] == fraction_to_fp16_bits(Fraction(0.75) * v), (n, m, i, j)
+
+
+def test_trmm_against_numpy_and_plain_product():
+    rng = np.random.default_rng(42)
+    n, m = 70, 33
+    a = rng.uniform(0, 1, size=(n, n)).astype(np.float16)
+    b = rng.uniform(0, 1, size=(n, m)).astype(np.float16)
+    got = oracle.trmm(a, b)
+    ref = np.tril(a.astype(np.float64)).T @ b.astype(np.float64)
+    assert np.allclose(got.astype(np.float64), ref, rtol=2.0 ** -10, atol=0)
+    # with zeros above the diagonal the plain product (already pinned) is the same:
+    # Cᵀ = Bᵀ·A, i.e. hgemm(a_op = Bᵀ, b_op rows = columns of A)
+    lower = np.tril(a)
+    plain = oracle.hgemm(np.ascontiguousarray(b.T), np.ascontiguousarray(lower.T)).T
+    assert np.array_equal(bits(got), bits(plain))
+
+
+def test_trmm_reads_only_the_lower_triangle():
+    rng = np.random.default_rng(43)
+    n, m = 40, 9
+    a = rng.uniform(-1, 1, size=(n, n)).astype(np.float16)
+    b = rng.uniform(-1, 1, size=(n, m)).astype(np.float16)
+    poisoned = a.copy()
+    poisoned[np.triu_indices(n, 1)] = np.nan
+    assert np.array_equal(bits(oracle.trmm(poisoned, b)), bits(oracle.trmm(a, b)))
+
+
+def test_trmm_identity_and_scaling():
+    rng = np.random.default_rng(44)
+    n, m = 17, 5
+    b = random_fp16(rng, (n, m))
+    eye = np.eye(n, dtype=np.float16)
+    assert np.array_equal(bits(oracle.trmm(eye, b)), bits(b))
+    assert np.array_equal(bits(oracle.trmm(eye, b, alpha=2.0)), bits((b.astype(np.float64) * 2).astype(np.float16)))
