@@ -49,6 +49,8 @@ def metric_for(name, spec):
     for the other workloads."""
     if name == DEFAULT_WORKLOAD:
         return METRIC
+    if spec.get("op") == "trmm":
+        return f"TRMM TFLOP/s (n(n+1)m/t) at n={spec['n']}, m={spec['m']} fp16"
     return f"HGEMM TFLOP/s (2MNK/t) at {spec['M']}x{spec['N']}x{spec['K']} fp16"
 UNIT = "TFLOP/s"
 DEFAULT_WORKLOAD = "hgemm_8192"
@@ -65,7 +67,27 @@ DESCRIPTIONS = {
     "hgemm_256_int": "M=N=K=256 fp16; A, B integers in {-2..2}",
     "hgemm_4096x256x4096_skinny": "M=4096, N=256, K=4096 fp16; A, B uniform[-1,1] "
                                   "(bandwidth-bound)",
+    "trmm_8192": "C = A^T B, A 8192x8192 lower triangular, B 8192x8192, column-major fp16; "
+                 "A, B uniform[0,1]",
+    "trmm_4096x256": "C = A^T B, A 4096x4096 lower triangular, B 4096x256, column-major fp16; "
+                     "A, B uniform[0,1]",
 }
+
+
+def trmm_launches(n, leaf=256):
+    """Kernel launches of one hgemm_trmm: the batched leaves plus one GEMM per
+    block split by the recursion (blocks split at half, rounded up to 64)."""
+    def splits(s):
+        if s <= leaf:
+            return 0
+        s1 = ((s // 2 + 63) // 64) * 64
+        return 1 + splits(s1) + splits(s - s1)
+    return 1 + splits(n)
+
+
+def trmm_flops(spec):
+    """Multiply-adds of the triangular product, two flops each: n(n+1)/2 per column."""
+    return float(spec["n"]) * (spec["n"] + 1) * spec["m"]
 
 
 def parse_args():
@@ -297,6 +319,8 @@ def oracle_sample(spec, a, b, target_s, nthreads):
 def run_reference(args, spec, a, b, world, rank):
     if rank != 0:
         return 0
+    if spec.get("op") == "trmm":
+        return run_trmm_reference(args, spec, a, b, world)
     nthreads = os.cpu_count() or 1
     per_step = max(0.05, args.reference_seconds / max(1, args.steps + args.warmup))
     import oracle
@@ -332,6 +356,176 @@ def run_reference(args, spec, a, b, world, rank):
         "gpu_launches": 0,
     }
     print(json.dumps(line), flush=True)
+    return 0
+
+
+def trmm_oracle_columns(a_col, b_col, cols, nthreads):
+    """The oracle's triangular product on the first `cols` columns of B."""
+    import oracle
+    return oracle.trmm(a_col.T, b_col[:cols].T, nthreads=nthreads)
+
+
+def run_trmm_reference(args, spec, a_col, b_col, world):
+    import oracle
+    oracle.build()
+    nthreads = os.cpu_count() or 1
+    n, m = spec["n"], spec["m"]
+    per_step = max(0.05, args.reference_seconds / max(1, args.steps + args.warmup))
+    cols = min(m, nthreads)
+    t = time.perf_counter()
+    trmm_oracle_columns(a_col, b_col, cols, nthreads)
+    dt = time.perf_counter() - t
+    cols = max(min(m, nthreads), min(m, int(cols * per_step / max(dt, 1e-6))))
+    times = []
+    for i in range(args.warmup + args.steps):
+        t = time.perf_counter()
+        trmm_oracle_columns(a_col, b_col, cols, nthreads)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t)
+    total = sum(times)
+    value = float(n) * (n + 1) * cols * len(times) / total / 1e12
+    sample = (f"the first {cols} columns of B per step (n={n}) of the {args.workload} workload; "
+              f"FP64 oracle, {nthreads} threads")
+    line = {
+        "impl": "reference", "metric": metric_for(args.workload, spec), "value": value, "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / len(times), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{args.workload}: {DESCRIPTIONS.get(args.workload, '')}",
+                   "n": n, "m": m, "seed": spec["seed"]},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": nthreads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_trmm_ours(args, spec, a_col, b_col, world, rank, local):
+    """The TRMM page's product through hgemm_trmm: same timing protocol as
+    the GEMM workloads (L2 flushed before every timed call)."""
+    import torch
+    import tensor_core_dense_fp16_gb300 as tc
+
+    tc.load()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    n, m = spec["n"], spec["m"]
+    flops = trmm_flops(spec)
+    stream = torch.cuda.current_stream(dev)
+    da = torch.from_numpy(a_col).to(dev)
+    db = torch.from_numpy(b_col).to(dev)
+    dc = torch.empty((m, n), dtype=torch.float16, device=dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2 // 4 + 1, dtype=torch.float32, device=dev)
+
+    def step():
+        tc.hgemm_trmm(da, n, db, n, dc, n, n, m, 1.0, stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    if tc.hgemm_device_status(stream) != tc.HGEMM_OK:
+        raise RuntimeError("a kernel wait timed out during warm-up")
+    sampler = ClockSampler(nvsmi_id(torch, dev, local))
+    sampler.start()
+    time.sleep(0.15)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t0 = time.time()
+    for s_ev, e_ev in evs:
+        flush.zero_()
+        s_ev.record(stream)
+        step()
+        e_ev.record(stream)
+    torch.cuda.synchronize(dev)
+    t1 = time.time()
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop(t0, t1)
+    if tc.hgemm_device_status(stream) != tc.HGEMM_OK:
+        raise RuntimeError("a kernel wait timed out in the timed region")
+    times_ms = [s_ev.elapsed_time(e_ev) for s_ev, e_ev in evs]
+    total_ms = reduce_max(sum(times_ms), dist, dev)
+    mean_ms = total_ms / args.steps
+    value = whole_job_tflops(world, args.steps, flops, total_ms)
+
+    e2e = None
+    if not args.no_e2e:
+        ha = torch.from_numpy(a_col).pin_memory()
+        hb = torch.from_numpy(b_col).pin_memory()
+        hc = torch.empty((m, n), dtype=torch.float16).pin_memory()
+        e_steps = max(3, min(args.steps, 10))
+
+        def e2e_step():
+            da.copy_(ha, non_blocking=True)
+            db.copy_(hb, non_blocking=True)
+            step()
+            hc.copy_(dc, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        s_ev, e_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s_ev.record(stream)
+        for _ in range(e_steps):
+            e2e_step()
+        e_ev.record(stream)
+        torch.cuda.synchronize(dev)
+        e_ms = reduce_max(s_ev.elapsed_time(e_ev), dist, dev)
+        e2e = {"value": whole_job_tflops(world, e_steps, flops, e_ms), "unit": UNIT,
+               "h2d_bytes_per_step": 2 * (n * n + n * m), "d2h_bytes_per_step": 2 * n * m,
+               "ms_per_step": e_ms / e_steps}
+
+    peaks, peak_src = load_peaks()
+    peak = peaks["bf16_tflops"] * FP16_PER_BF16
+    achieved = flops / (mean_ms * 1e-3) / 1e12
+    roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+            "frac": achieved / peak, "traffic": None,
+            "peak_source": f"{peak_src}: bf16_tflops (burst) x {FP16_PER_BF16} fp16/bf16",
+            "kernel": "hgemm_tri_leaves_kernel + hgemm update kernels",
+            "algorithmic_flops": flops, "algorithmic_bytes": 2.0 * (n * (n + 1) / 2 + 2 * n * m)}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        nthreads = os.cpu_count() or 1
+        cols = min(m, nthreads)
+        t = time.perf_counter()
+        trmm_oracle_columns(a_col, b_col, cols, nthreads)
+        dt = time.perf_counter() - t
+        if dt < args.cpu_seconds:
+            cols = min(m, max(cols, int(cols * args.cpu_seconds / max(dt, 1e-6))))
+            t = time.perf_counter()
+            trmm_oracle_columns(a_col, b_col, cols, nthreads)
+            dt = time.perf_counter() - t
+        cpu = {"value": float(n) * (n + 1) * cols / dt / 1e12, "unit": UNIT, "cores": nthreads,
+               "kind": "oracle",
+               "sample": f"the first {cols} columns of B (n={n}) of the {args.workload} workload "
+                         f"in {dt:.1f} s; FP64 oracle, {nthreads} threads"}
+    if rank == 0:
+        line = {
+            "metric": metric_for(args.workload, spec), "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_ms,
+            "ms_per_step_median": statistics.median(times_ms), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+            "config": {"workload": f"{args.workload}: {DESCRIPTIONS.get(args.workload, '')}",
+                       "n": n, "m": m, "seed": spec["seed"],
+                       "l2": "flushed before every timed call (write of 2x L2 size, outside the events)",
+                       "inputs": "resident in HBM", "path": "hgemm_trmm",
+                       "parallelism": f"replicas x{world}"},
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": args.steps * trmm_launches(n), "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
     return 0
 
 
@@ -500,6 +694,8 @@ def main():
     a, b, spec = synth.workload(args.workload)
     if args.impl == "reference":
         return run_reference(args, spec, a, b, world, rank)
+    if spec.get("op") == "trmm":
+        return run_trmm_ours(args, spec, a, b, world, rank, local)
     return run_ours(args, spec, a, b, world, rank, local)
 
 

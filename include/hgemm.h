@@ -75,6 +75,7 @@ typedef uint16_t hgemm_half_t; /* IEEE binary16 bit pattern */
 #define HGEMM_PATH_TC_WIDE 6  /* tcgen05 + TMA persistent kernel, CTA pairs per 256×512 tile */
 
 /* Largest M, N or K accepted (TMA coordinates are signed 32-bit). */
+#define HGEMM_TRMM_MAX_N 16384          /* largest triangle hgemm_trmm accepts */
 #define HGEMM_MAX_DIM ((int64_t)0x7FFFFFFF)
 
 /*
@@ -119,6 +120,45 @@ HGEMM_API int hgemm(const hgemm_half_t *A, const hgemm_half_t *B, hgemm_half_t *
 HGEMM_API int hgemm_ex(const hgemm_half_t *A, const hgemm_half_t *B, hgemm_half_t *C,
              int64_t M, int64_t N, int64_t K, float alpha, float beta,
              const hgemm_half_t *bias, int relu, cudaStream_t stream);
+
+/*
+ * hgemm_strided — hgemm_ex on sub-matrices, the form the recursive TRMM of
+ * "异构计算中高性能TRMM与TRSM的递归算法实现" (§2.1 blocking, §2.2 the GEMM
+ * update of an off-diagonal block) needs: row pitches in elements, with
+ * A(i,k) at A[i·lda + k], B(k,j) at B[j·ldb + k] (column j of B still
+ * contiguous) and C(i,j) at C[i·ldc + j]; lda ≥ K, ldb ≥ K, ldc ≥ N.
+ * The tensor-core paths need 16-byte-aligned base addresses, pitches that
+ * are multiples of 8 and N a multiple of 8; anything else takes
+ * HGEMM_PATH_GENERIC. The span C occupies must not overlap the spans of A, B
+ * or bias (HGEMM_ERR_ALIAS). hgemm_ex(...) is hgemm_strided with lda = ldb = K
+ * and ldc = N. Same return values as hgemm.
+ */
+HGEMM_API int hgemm_strided(const hgemm_half_t *A, int64_t lda, const hgemm_half_t *B, int64_t ldb,
+                  hgemm_half_t *C, int64_t ldc, int64_t M, int64_t N, int64_t K,
+                  float alpha, float beta, const hgemm_half_t *bias, int relu,
+                  cudaStream_t stream);
+
+/*
+ * hgemm_trmm — the triangular product of "异构计算中高性能TRMM与TRSM的递归算法实现"
+ * §2.2 (left side, lower triangle, transposed: B ← alpha·Aᵀ·B), out of place:
+ *
+ *     C = alpha · Aᵀ · B
+ *
+ * A is n×n lower triangular and only its lower triangle (row ≥ column) is
+ * read; B and C are n×m. All three are column-major, as on the page (Julia):
+ * A(r,c) at A[c·lda + r], B(r,j) at B[j·ldb + r], C(r,j) at C[j·ldc + r],
+ * with lda, ldb, ldc ≥ n; n ≤ HGEMM_TRMM_MAX_N (n or m = 0: nothing to do). By the page's
+ * recursion (§2.1, §2.2): a block splits into halves; C1 = A11ᵀ·B1, then the
+ * GEMM update C1 += A21ᵀ·B2 (hgemm's accumulate epilogue), then C2 = A22ᵀ·B2;
+ * blocks of order ≤ 256 (the page's threshold) are leaves, all computed by
+ * one launch of masked products. Storage is FP16 (each update rounds its
+ * block once), accumulation FP32 within each product. C must not overlap A
+ * or B (HGEMM_ERR_ALIAS); the calls are enqueued on `stream`. Same return
+ * values as hgemm.
+ */
+HGEMM_API int hgemm_trmm(const hgemm_half_t *A, int64_t lda, const hgemm_half_t *B, int64_t ldb,
+               hgemm_half_t *C, int64_t ldc, int64_t n, int64_t m, float alpha,
+               cudaStream_t stream);
 
 /*
  * hgemm_host — the same product for operands held in HOST memory.

@@ -24,7 +24,14 @@ Value recipes (the workloads of the benchmark configurations):
   * ``int``      : floor(5u) - 2, i.e. integers uniform in {-2, ..., 2};
   * ``normal``   : Box-Muller on consecutive uniform pairs
                    z = sqrt(-2 ln(1 - u1)) * cos(2π u2); A ~ N(0, 1) and
-                   B ~ N(0, 1)/sqrt(K), each rounded to FP16.
+                   B ~ N(0, 1)/sqrt(K), each rounded to FP16;
+  * ``unit``     : u rounded to the nearest FP16 (values in [0, 1]), like
+                   the rand(Float32) operands of the TRMM page's example (§5.1).
+
+The triangular product (``trmm_operands``) takes A (n×n, its lower triangle
+is the operand) and B (n×m), both column-major as on the TRMM page: arrays of
+n columns (A) and m columns (B) of n contiguous values. A's stream uses draws
+0 .. n*n-1, B's continues after it.
 """
 
 from __future__ import annotations
@@ -63,6 +70,8 @@ def _fill(seed: int, start: int, count: int, kind: str, scale: float) -> np.ndar
         n = min(_CHUNK, count - lo)
         if kind == "uniform":
             v = 2.0 * uniform01(seed, start + lo, n) - 1.0
+        elif kind == "unit":
+            v = uniform01(seed, start + lo, n)
         elif kind == "int":
             v = np.floor(5.0 * uniform01(seed, start + lo, n)) - 2.0
         elif kind == "normal":
@@ -94,11 +103,27 @@ WORKLOADS = {
     "hgemm_1000_ragged": dict(M=1000, N=1000, K=1000, kind="uniform", seed=1002),
     "hgemm_8192": dict(M=8192, N=8192, K=8192, kind="normal", seed=1003),
     "hgemm_4096x256x4096_skinny": dict(M=4096, N=256, K=4096, kind="uniform", seed=1004),
+    # the TRMM page's shapes: 8192×8192 (its measurements, §4.2) and A 4096×4096
+    # with a 4096×256 right-hand side (its example, §5.1)
+    "trmm_8192": dict(op="trmm", n=8192, m=8192, kind="unit", seed=1005),
+    "trmm_4096x256": dict(op="trmm", n=4096, m=256, kind="unit", seed=1006),
 }
+
+
+def trmm_operands(n: int, m: int, seed: int, kind: str = "unit"):
+    """(a_col, b_col): a_col (n, n) holds column c of A in row c (the whole
+    square is drawn; only its lower triangle, row >= column, is the operand),
+    b_col (m, n) holds column j of B in row j."""
+    a = _fill(seed, 0, n * n, kind, 1.0).reshape(n, n)
+    b = _fill(seed, n * n, m * n, kind, 1.0).reshape(m, n)
+    return a, b
 
 
 def workload(name: str):
     """(A, B, spec) for a named workload."""
     spec = WORKLOADS[name]
+    if spec.get("op") == "trmm":
+        a, b = trmm_operands(spec["n"], spec["m"], spec["seed"], spec["kind"])
+        return a, b, spec
     a, b = operands(spec["M"], spec["N"], spec["K"], spec["seed"], spec["kind"])
     return a, b, spec

@@ -28,7 +28,7 @@ __all__ = [
     "HgemmError", "library_path", "load", "hgemm", "hgemm_host", "hgemm_select_path",
     "hgemm_force_path", "hgemm_device_status", "hgemm_last_cuda_error",
     "hgemm_status_string", "hgemm_version", "hgemm_set_wait_timeout", "hgemm_debug_inject",
-    "hgemm_force_split", "hgemm_ex",
+    "hgemm_force_split", "hgemm_ex", "hgemm_strided", "hgemm_trmm", "HGEMM_TRMM_MAX_N",
     "HGEMM_INJECT_NONE", "HGEMM_INJECT_DROP_ARRIVAL", "matmul",
 ]
 
@@ -38,6 +38,7 @@ HGEMM_ERR_ALIAS = -2
 HGEMM_ERR_UNSUPPORTED_DEVICE = -3
 HGEMM_ERR_CUDA = -4
 HGEMM_ERR_TIMEOUT = -5
+HGEMM_TRMM_MAX_N = 16384
 
 HGEMM_PATH_NONE = 0
 HGEMM_PATH_ZERO = 1
@@ -88,6 +89,11 @@ def load():
     lib.hgemm_ex.argtypes = [vp, vp, vp, i64, i64, i64, ctypes.c_float, ctypes.c_float, vp,
                              i32, vp]
     lib.hgemm_ex.restype = i32
+    lib.hgemm_strided.argtypes = [vp, i64, vp, i64, vp, i64, i64, i64, i64, ctypes.c_float,
+                                  ctypes.c_float, vp, i32, vp]
+    lib.hgemm_strided.restype = i32
+    lib.hgemm_trmm.argtypes = [vp, i64, vp, i64, vp, i64, i64, i64, ctypes.c_float, vp]
+    lib.hgemm_trmm.restype = i32
     lib.hgemm_host.argtypes = [vp, vp, vp, i64, i64, i64, vp, vp, vp, vp]
     lib.hgemm_host.restype = i32
     lib.hgemm_select_path.argtypes = [vp, vp, vp, i64, i64, i64]
@@ -186,6 +192,23 @@ def hgemm_ex(A, B, C, M: int, N: int, K: int, alpha: float = 1.0, beta: float = 
         _check_tensor(bias, "bias", True)
     _raise_on(load().hgemm_ex(_ptr(A), _ptr(B), _ptr(C), M, N, K, float(alpha), float(beta),
                               _ptr(bias), int(bool(relu)), _stream(stream)), "hgemm_ex")
+
+
+def hgemm_strided(A, lda: int, B, ldb: int, C, ldc: int, M: int, N: int, K: int,
+                  alpha: float = 1.0, beta: float = 0.0, bias=None, relu: bool = False,
+                  stream=None) -> None:
+    """hgemm_ex on sub-matrices with row pitches (see hgemm.h). A, B, C may be
+    tensors (their base address is used) or raw integer addresses."""
+    _raise_on(load().hgemm_strided(_ptr(A), lda, _ptr(B), ldb, _ptr(C), ldc, M, N, K, float(alpha),
+                                   float(beta), _ptr(bias), int(bool(relu)), _stream(stream)),
+              "hgemm_strided")
+
+
+def hgemm_trmm(A, lda: int, B, ldb: int, C, ldc: int, n: int, m: int, alpha: float = 1.0,
+               stream=None) -> None:
+    """C = alpha·Aᵀ·B, A lower triangular; column-major operands (see hgemm.h)."""
+    _raise_on(load().hgemm_trmm(_ptr(A), lda, _ptr(B), ldb, _ptr(C), ldc, n, m, float(alpha),
+                                _stream(stream)), "hgemm_trmm")
 
 
 def hgemm_host(hA, hB, hC, M: int, N: int, K: int, dA, dB, dC, stream=None) -> None:

@@ -9,6 +9,7 @@
 // such as PyTorch's, not to every call).
 #include <atomic>
 #include <cstdint>
+#include <vector>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -24,6 +25,7 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;  // 2 s per wait
+constexpr int64_t kTrmmLeaf = 256;  // diagonal blocks of at most this order are leaves
 
 thread_local int t_last_cuda_error = 0;
 std::atomic<int> g_forced_path{-1};
@@ -33,11 +35,26 @@ std::atomic<int> g_inject{HGEMM_INJECT_NONE};
 
 struct DeviceState {
   std::atomic<int> ready{0};  // 0 unknown, 1 supported, -1 unsupported
+  int id = 0;
   int num_sms = 0;
   int* status = nullptr;
   hg::DeviceProfile prof{};
 };
 DeviceState g_devices[kMaxDevices];
+
+// One product: operands, sizes and row pitches in elements (A(i,k) at
+// A[i*lda + k], B(k,j) at B[j*ldb + k], C(i,j) at C[i*ldc + j]).
+struct Gemm {
+  const void* A;
+  const void* B;
+  void* C;
+  int64_t M, N, K;
+  int64_t lda, ldb, ldc;
+};
+
+Gemm dense(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K) {
+  return Gemm{A, B, C, M, N, K, K, K, N};
+}
 std::mutex g_device_mu;
 
 // GB300 figures, used by hgemm_select_path before any device has been used
@@ -78,6 +95,7 @@ int current_device(DeviceState** out) {
       } else {
         int* status = nullptr;
         if ((e = hg::status_word_address(&status)) != cudaSuccess) return cuda_fail(e);
+        st.id = dev;
         st.num_sms = sms;
         st.status = status;
         st.prof.num_sms = sms;
@@ -104,38 +122,49 @@ bool ranges_overlap(const void* a, uint64_t abytes, const void* b, uint64_t bbyt
 }
 
 // Host-only argument checks shared by every entry point.
-int validate(const void* A, const void* B, const void* C, int64_t M, int64_t N, int64_t K) {
+int validate(const Gemm& g) {
+  const int64_t M = g.M, N = g.N, K = g.K;
   if (M < 0 || N < 0 || K < 0 || M > HGEMM_MAX_DIM || N > HGEMM_MAX_DIM || K > HGEMM_MAX_DIM)
     return HGEMM_ERR_INVALID_ARG;
-  // element counts (each < 2^62) and byte counts (< 2^63) cannot overflow
-  const unsigned __int128 mk = static_cast<unsigned __int128>(M) * K;
-  const unsigned __int128 nk = static_cast<unsigned __int128>(N) * K;
-  const unsigned __int128 mn = static_cast<unsigned __int128>(M) * N;
-  const unsigned __int128 lim = static_cast<unsigned __int128>(1) << 61;
-  if (mk >= lim || nk >= lim || mn >= lim) return HGEMM_ERR_INVALID_ARG;
-  if ((mk && !A) || (nk && !B) || (mn && !C)) return HGEMM_ERR_INVALID_ARG;
-  // FP16 elements: every pointer must be at least 2-byte aligned
-  if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B) |
-       reinterpret_cast<uintptr_t>(C)) & 1u)
+  // pitches cover a row and stay far from overflow
+  const int64_t ld_lim = int64_t(1) << 40;
+  if (g.lda < K || g.ldb < K || g.ldc < N || g.lda > ld_lim || g.ldb > ld_lim || g.ldc > ld_lim)
     return HGEMM_ERR_INVALID_ARG;
-  if (mn && (ranges_overlap(C, 2 * static_cast<uint64_t>(mn), A, 2 * static_cast<uint64_t>(mk)) ||
-             ranges_overlap(C, 2 * static_cast<uint64_t>(mn), B, 2 * static_cast<uint64_t>(nk))))
+  // element spans (each < 2^61) and byte spans (< 2^62) cannot overflow
+  using u128 = unsigned __int128;
+  auto span = [](int64_t rows, int64_t ld, int64_t cols) -> u128 {
+    return (rows > 0 && cols > 0) ? static_cast<u128>(rows - 1) * ld + cols : 0;
+  };
+  const u128 sa = span(M, g.lda, K), sb = span(N, g.ldb, K), sc = span(M, g.ldc, N);
+  const u128 lim = static_cast<u128>(1) << 61;
+  if (sa >= lim || sb >= lim || sc >= lim) return HGEMM_ERR_INVALID_ARG;
+  if ((sa && !g.A) || (sb && !g.B) || (sc && !g.C)) return HGEMM_ERR_INVALID_ARG;
+  // FP16 elements: every pointer must be at least 2-byte aligned
+  if ((reinterpret_cast<uintptr_t>(g.A) | reinterpret_cast<uintptr_t>(g.B) |
+       reinterpret_cast<uintptr_t>(g.C)) & 1u)
+    return HGEMM_ERR_INVALID_ARG;
+  // C is written while A and B are read: their spans must not meet
+  if (sc && (ranges_overlap(g.C, 2 * static_cast<uint64_t>(sc), g.A, 2 * static_cast<uint64_t>(sa)) ||
+             ranges_overlap(g.C, 2 * static_cast<uint64_t>(sc), g.B, 2 * static_cast<uint64_t>(sb))))
     return HGEMM_ERR_ALIAS;
   return HGEMM_OK;
 }
 
-bool tma_ok(const void* A, const void* B, const void* C, int64_t N, int64_t K) {
+// TMA needs 16-byte-aligned bases and row pitches; the epilogue's 16-byte
+// reads of C need N to be a multiple of 8 as well.
+bool tma_ok(const Gemm& g) {
   auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
-  return al16(A) && al16(B) && al16(C) && (K % 8 == 0) && (N % 8 == 0);
+  return al16(g.A) && al16(g.B) && al16(g.C) && g.lda % 8 == 0 && g.ldb % 8 == 0 &&
+         g.ldc % 8 == 0 && g.N % 8 == 0;
 }
 
-int choose_path(const void* A, const void* B, const void* C, int64_t M, int64_t N, int64_t K,
-                const hg::DeviceProfile& prof, bool fused, int* split, int* tile_n) {
+int choose_path(const Gemm& g, const hg::DeviceProfile& prof, bool fused, int* split, int* tile_n) {
   *split = 1;
   *tile_n = hg::kPairBN;
+  const int64_t M = g.M, N = g.N, K = g.K;
   if (M == 0 || N == 0) return HGEMM_PATH_NONE;
   if (K == 0) return HGEMM_PATH_ZERO;
-  const bool tma = tma_ok(A, B, C, N, K);
+  const bool tma = tma_ok(g);
   const int forced = g_forced_path.load(std::memory_order_relaxed);
   if (forced == HGEMM_PATH_GENERIC || !tma) return HGEMM_PATH_GENERIC;
   const int fs = g_forced_split.load(std::memory_order_relaxed);
@@ -254,14 +283,15 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// Tensor map of a row-major FP16 matrix [rows][cols] read or written in
-// boxes of box_rows × box_cols (box_cols * 2 == 128 bytes: one swizzle row).
-int encode_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_rows,
-               int box_cols) {
+// Tensor map of a row-major FP16 matrix [rows][cols] with rows `pitch`
+// elements apart, read or written in boxes of box_rows × box_cols
+// (box_cols * 2 == 128 bytes: one swizzle row).
+int encode_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t pitch,
+               int box_rows, int box_cols) {
   auto encode = tensor_map_encoder();
   if (!encode) return cuda_fail(cudaErrorNotSupported);
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(pitch) * 2};
   const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t elem_strides[2] = {1, 1};
   CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims,
@@ -272,13 +302,17 @@ int encode_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, i
   return HGEMM_OK;
 }
 
-int run_tc(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
-           const hg::EpiArgs& epi, const DeviceState& dev, cudaStream_t stream) {
+int run_tc(const Gemm& g, const hg::EpiArgs& epi, const DeviceState& dev,
+       cudaStream_t stream) {
+  const void* A = g.A;
+  const void* B = g.B;
+  void* C = g.C;
+  const int64_t M = g.M, N = g.N, K = g.K;
   CUtensorMap ma, mb, mc;
   int rc;
-  if ((rc = encode_map(&ma, A, M, K, hg::kTcBM, hg::kTcBK)) != HGEMM_OK) return rc;
-  if ((rc = encode_map(&mb, B, N, K, hg::kTcBN, hg::kTcBK)) != HGEMM_OK) return rc;
-  if ((rc = encode_map(&mc, C, M, N, hg::kEpiRows, hg::kEpiCols)) != HGEMM_OK) return rc;
+  if ((rc = encode_map(&ma, A, M, K, g.lda, hg::kTcBM, hg::kTcBK)) != HGEMM_OK) return rc;
+  if ((rc = encode_map(&mb, B, N, K, g.ldb, hg::kTcBN, hg::kTcBK)) != HGEMM_OK) return rc;
+  if ((rc = encode_map(&mc, C, M, N, g.ldc, hg::kEpiRows, hg::kEpiCols)) != HGEMM_OK) return rc;
   hg::TcArgs args{};
   args.M = static_cast<int>(M);
   args.N = static_cast<int>(N);
@@ -297,12 +331,17 @@ int run_tc(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t 
   args.inject = g_inject.load(std::memory_order_relaxed);
   args.epi = epi;
   args.C = static_cast<const uint16_t*>(C);
+  args.ldc = g.ldc;
   cudaError_t e = hg::launch_tc_128x256(ma, mb, mc, args, stream);
   return e == cudaSuccess ? HGEMM_OK : cuda_fail(e);
 }
 
-int run_tc_pair(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
-                const hg::EpiArgs& epi, const DeviceState& dev, cudaStream_t stream) {
+int run_tc_pair(const Gemm& g, const hg::EpiArgs& epi, const DeviceState& dev,
+            cudaStream_t stream) {
+  const void* A = g.A;
+  const void* B = g.B;
+  void* C = g.C;
+  const int64_t M = g.M, N = g.N, K = g.K;
   hg::TcArgs args{};
   args.M = static_cast<int>(M);
   args.N = static_cast<int>(N);
@@ -338,23 +377,28 @@ int run_tc_pair(const void* A, const void* B, void* C, int64_t M, int64_t N, int
   args.inject = g_inject.load(std::memory_order_relaxed);
   args.epi = epi;
   args.C = static_cast<const uint16_t*>(C);
+  args.ldc = g.ldc;
   CUtensorMap ma, mb, mbp, mc;
   int rc;
-  if ((rc = encode_map(&ma, A, M, K, hg::kTcBM, hg::kTcBK)) != HGEMM_OK) return rc;
-  if ((rc = encode_map(&mb, B, N, K, hg::kPairBN / 2, hg::kTcBK)) != HGEMM_OK) return rc;
-  if ((rc = encode_map(&mbp, B, N, K, args.part_cols / 2, hg::kTcBK)) != HGEMM_OK) return rc;
-  if ((rc = encode_map(&mc, C, M, N, hg::kEpiRows, hg::kEpiCols)) != HGEMM_OK) return rc;
+  if ((rc = encode_map(&ma, A, M, K, g.lda, hg::kTcBM, hg::kTcBK)) != HGEMM_OK) return rc;
+  if ((rc = encode_map(&mb, B, N, K, g.ldb, hg::kPairBN / 2, hg::kTcBK)) != HGEMM_OK) return rc;
+  if ((rc = encode_map(&mbp, B, N, K, g.ldb, args.part_cols / 2, hg::kTcBK)) != HGEMM_OK) return rc;
+  if ((rc = encode_map(&mc, C, M, N, g.ldc, hg::kEpiRows, hg::kEpiCols)) != HGEMM_OK) return rc;
   cudaError_t e = hg::launch_tc_pair(ma, mb, mbp, mc, args, stream);
   return e == cudaSuccess ? HGEMM_OK : cuda_fail(e);
 }
 
-int run_tc_wide(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
-                const hg::EpiArgs& epi, const DeviceState& dev, cudaStream_t stream) {
+int run_tc_wide(const Gemm& g, const hg::EpiArgs& epi, const DeviceState& dev,
+            cudaStream_t stream) {
+  const void* A = g.A;
+  const void* B = g.B;
+  void* C = g.C;
+  const int64_t M = g.M, N = g.N, K = g.K;
   CUtensorMap ma, mb, mc;
   int rc;
-  if ((rc = encode_map(&ma, A, M, K, hg::kTcBM, hg::kTcBK)) != HGEMM_OK) return rc;
-  if ((rc = encode_map(&mb, B, N, K, hg::kPairBN / 2, hg::kTcBK)) != HGEMM_OK) return rc;
-  if ((rc = encode_map(&mc, C, M, N, hg::kEpiRows, hg::kEpiCols)) != HGEMM_OK) return rc;
+  if ((rc = encode_map(&ma, A, M, K, g.lda, hg::kTcBM, hg::kTcBK)) != HGEMM_OK) return rc;
+  if ((rc = encode_map(&mb, B, N, K, g.ldb, hg::kPairBN / 2, hg::kTcBK)) != HGEMM_OK) return rc;
+  if ((rc = encode_map(&mc, C, M, N, g.ldc, hg::kEpiRows, hg::kEpiCols)) != HGEMM_OK) return rc;
   hg::TcArgs args{};
   args.M = static_cast<int>(M);
   args.N = static_cast<int>(N);
@@ -374,17 +418,22 @@ int run_tc_wide(const void* A, const void* B, void* C, int64_t M, int64_t N, int
   args.inject = g_inject.load(std::memory_order_relaxed);
   args.epi = epi;
   args.C = static_cast<const uint16_t*>(C);
+  args.ldc = g.ldc;
   cudaError_t e = hg::launch_tc_wide(ma, mb, mc, args, stream);
   return e == cudaSuccess ? HGEMM_OK : cuda_fail(e);
 }
 
-int run_skinny(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int split,
-               int tile_n, const hg::EpiArgs& epi, const DeviceState& dev, cudaStream_t stream) {
+int run_skinny(const Gemm& g, int split, int tile_n, const hg::EpiArgs& epi, const DeviceState& dev,
+               cudaStream_t stream) {
+  const void* A = g.A;
+  const void* B = g.B;
+  void* C = g.C;
+  const int64_t M = g.M, N = g.N, K = g.K;
   CUtensorMap ma, mb, mc;
   int rc;
-  if ((rc = encode_map(&ma, A, M, K, hg::kTcBM, hg::kTcBK)) != HGEMM_OK) return rc;
-  if ((rc = encode_map(&mb, B, N, K, tile_n / 2, hg::kTcBK)) != HGEMM_OK) return rc;
-  if ((rc = encode_map(&mc, C, M, N, hg::kEpiRows, hg::kEpiCols)) != HGEMM_OK) return rc;
+  if ((rc = encode_map(&ma, A, M, K, g.lda, hg::kTcBM, hg::kTcBK)) != HGEMM_OK) return rc;
+  if ((rc = encode_map(&mb, B, N, K, g.ldb, tile_n / 2, hg::kTcBK)) != HGEMM_OK) return rc;
+  if ((rc = encode_map(&mc, C, M, N, g.ldc, hg::kEpiRows, hg::kEpiCols)) != HGEMM_OK) return rc;
   hg::TcArgs args{};
   args.M = static_cast<int>(M);
   args.N = static_cast<int>(N);
@@ -403,30 +452,32 @@ int run_skinny(const void* A, const void* B, void* C, int64_t M, int64_t N, int6
   args.inject = g_inject.load(std::memory_order_relaxed);
   args.epi = epi;
   args.C = static_cast<const uint16_t*>(C);
+  args.ldc = g.ldc;
   cudaError_t e = hg::launch_skinny(split, tile_n, ma, mb, mc, args, stream);
   return e == cudaSuccess ? HGEMM_OK : cuda_fail(e);
 }
 
-int dispatch(const hgemm_half_t* A, const hgemm_half_t* B, hgemm_half_t* C, int64_t M, int64_t N,
-             int64_t K, const hg::EpiArgs& epi, const DeviceState& dev, cudaStream_t stream) {
+int dispatch(const Gemm& g, const hg::EpiArgs& epi, const DeviceState& dev, cudaStream_t stream) {
   cudaError_t e;
   int split = 1, tile_n = hg::kPairBN;
-  switch (choose_path(A, B, C, M, N, K, dev.prof, epi.mode != 0, &split, &tile_n)) {
+  switch (choose_path(g, dev.prof, epi.mode != 0, &split, &tile_n)) {
     case HGEMM_PATH_NONE:
       return HGEMM_OK;
     case HGEMM_PATH_ZERO:
-      e = hg::launch_empty_sum(C, M, N, epi, stream);
+      e = hg::launch_empty_sum(static_cast<uint16_t*>(g.C), g.M, g.N, g.ldc, epi, stream);
       return e == cudaSuccess ? HGEMM_OK : cuda_fail(e);
     case HGEMM_PATH_TC:
-      return run_tc(A, B, C, M, N, K, epi, dev, stream);
+      return run_tc(g, epi, dev, stream);
     case HGEMM_PATH_TC_PAIR:
-      return run_tc_pair(A, B, C, M, N, K, epi, dev, stream);
+      return run_tc_pair(g, epi, dev, stream);
     case HGEMM_PATH_TC_WIDE:
-      return run_tc_wide(A, B, C, M, N, K, epi, dev, stream);
+      return run_tc_wide(g, epi, dev, stream);
     case HGEMM_PATH_SKINNY:
-      return run_skinny(A, B, C, M, N, K, split, tile_n, epi, dev, stream);
+      return run_skinny(g, split, tile_n, epi, dev, stream);
     default: {
-      hg::PlainArgs pa{A, B, C, M, N, K, dev.status, g_timeout_ns.load(), epi};
+      hg::PlainArgs pa{static_cast<const uint16_t*>(g.A), static_cast<const uint16_t*>(g.B),
+                       static_cast<uint16_t*>(g.C), g.M, g.N, g.K, g.lda, g.ldb, g.ldc,
+                       dev.status, g_timeout_ns.load(), epi};
       e = hg::launch_generic(pa, dev.num_sms, stream);
       return e == cudaSuccess ? HGEMM_OK : cuda_fail(e);
     }
@@ -462,45 +513,195 @@ int pipe_for_current_device(HostPipe** out) {
   return HGEMM_OK;
 }
 
+// Helper streams of hgemm_trmm: the independent updates of one level of the
+// recursion run on them concurrently (fork and join through events on the
+// caller's stream). Created once per device, kept for the life of the process.
+struct TrmmPipe {
+  bool ready = false;
+  static constexpr int kStreams = 4;
+  cudaStream_t s[kStreams] = {};
+  cudaEvent_t fork = nullptr;
+  cudaEvent_t join[kStreams] = {};
+  std::mutex mu;
+};
+TrmmPipe g_trmm_pipes[kMaxDevices];
+
+int trmm_pipe(int dev, TrmmPipe** out) {
+  TrmmPipe& tp = g_trmm_pipes[dev];
+  if (!tp.ready) {
+    cudaError_t e;
+    for (auto& st : tp.s)
+      if ((e = cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking)) != cudaSuccess) return cuda_fail(e);
+    if ((e = cudaEventCreateWithFlags(&tp.fork, cudaEventDisableTiming)) != cudaSuccess) return cuda_fail(e);
+    for (auto& ev : tp.join)
+      if ((e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming)) != cudaSuccess) return cuda_fail(e);
+    tp.ready = true;
+  }
+  *out = &tp;
+  return HGEMM_OK;
+}
+
 }  // namespace
 
 extern "C" {
 
 int hgemm(const hgemm_half_t* A, const hgemm_half_t* B, hgemm_half_t* C, int64_t M, int64_t N,
           int64_t K, cudaStream_t stream) {
-  int rc = validate(A, B, C, M, N, K);
+  const Gemm g = dense(A, B, C, M, N, K);
+  int rc = validate(g);
   if (rc != HGEMM_OK) return rc;
   if (M == 0 || N == 0) return HGEMM_OK;
   DeviceState* dev = nullptr;
   if ((rc = current_device(&dev)) != HGEMM_OK) return rc;
-  return dispatch(A, B, C, M, N, K, kPlainEpilogue, *dev, stream);
+  return dispatch(g, kPlainEpilogue, *dev, stream);
+}
+
+// The fused product on a validated problem: bias checks, epilogue mode.
+int run_fused(const Gemm& g, float alpha, float beta, const hgemm_half_t* bias, int relu,
+              cudaStream_t stream) {
+  if (bias) {
+    if (reinterpret_cast<uintptr_t>(bias) & 1u) return HGEMM_ERR_INVALID_ARG;
+    // C is written while bias is read
+    if (g.M > 0 && g.N > 0 &&
+        ranges_overlap(g.C, 2 * static_cast<uint64_t>((g.M - 1) * g.ldc + g.N), bias,
+                       2 * static_cast<uint64_t>(g.N)))
+      return HGEMM_ERR_ALIAS;
+  }
+  if (g.M == 0 || g.N == 0) return HGEMM_OK;
+  hg::EpiArgs epi{alpha, beta, reinterpret_cast<const uint16_t*>(bias), relu ? 1 : 0, 0};
+  epi.mode = beta != 0.0f ? 2 : ((alpha != 1.0f || bias || relu) ? 1 : 0);
+  DeviceState* dev = nullptr;
+  int rc;
+  if ((rc = current_device(&dev)) != HGEMM_OK) return rc;
+  return dispatch(g, epi, *dev, stream);
 }
 
 int hgemm_ex(const hgemm_half_t* A, const hgemm_half_t* B, hgemm_half_t* C, int64_t M, int64_t N,
              int64_t K, float alpha, float beta, const hgemm_half_t* bias, int relu,
              cudaStream_t stream) {
-  int rc = validate(A, B, C, M, N, K);
+  const Gemm g = dense(A, B, C, M, N, K);
+  const int rc = validate(g);
   if (rc != HGEMM_OK) return rc;
-  if (bias) {
-    if (reinterpret_cast<uintptr_t>(bias) & 1u) return HGEMM_ERR_INVALID_ARG;
-    // C is written while bias is read
-    if (M > 0 && N > 0 &&
-        ranges_overlap(C, 2 * static_cast<uint64_t>(M) * static_cast<uint64_t>(N), bias,
-                       2 * static_cast<uint64_t>(N)))
-      return HGEMM_ERR_ALIAS;
-  }
-  if (M == 0 || N == 0) return HGEMM_OK;
-  hg::EpiArgs epi{alpha, beta, reinterpret_cast<const uint16_t*>(bias), relu ? 1 : 0, 0};
-  epi.mode = beta != 0.0f ? 2 : ((alpha != 1.0f || bias || relu) ? 1 : 0);
+  return run_fused(g, alpha, beta, bias, relu, stream);
+}
+
+int hgemm_strided(const hgemm_half_t* A, int64_t lda, const hgemm_half_t* B, int64_t ldb,
+                  hgemm_half_t* C, int64_t ldc, int64_t M, int64_t N, int64_t K, float alpha,
+                  float beta, const hgemm_half_t* bias, int relu, cudaStream_t stream) {
+  const Gemm g{A, B, C, M, N, K, lda, ldb, ldc};
+  const int rc = validate(g);
+  if (rc != HGEMM_OK) return rc;
+  return run_fused(g, alpha, beta, bias, relu, stream);
+}
+
+int hgemm_trmm(const hgemm_half_t* A, int64_t lda, const hgemm_half_t* B, int64_t ldb,
+               hgemm_half_t* C, int64_t ldc, int64_t n, int64_t m, float alpha,
+               cudaStream_t stream) {
+  if (n < 0 || m < 0 || n > HGEMM_TRMM_MAX_N || m > HGEMM_MAX_DIM) return HGEMM_ERR_INVALID_ARG;
+  if (n == 0 || m == 0) return HGEMM_OK;
+  const int64_t ld_lim = int64_t(1) << 40;
+  if (lda < n || ldb < n || ldc < n || lda > ld_lim || ldb > ld_lim || ldc > ld_lim)
+    return HGEMM_ERR_INVALID_ARG;
+  if (!A || !B || !C) return HGEMM_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B) |
+       reinterpret_cast<uintptr_t>(C)) & 1u)
+    return HGEMM_ERR_INVALID_ARG;
+  // column-major spans (in elements): A n×n, B and C n×m
+  const unsigned __int128 sa = static_cast<unsigned __int128>(n - 1) * lda + n;
+  const unsigned __int128 sb = static_cast<unsigned __int128>(m - 1) * ldb + n;
+  const unsigned __int128 sc = static_cast<unsigned __int128>(m - 1) * ldc + n;
+  const unsigned __int128 lim = static_cast<unsigned __int128>(1) << 61;
+  if (sa >= lim || sb >= lim || sc >= lim) return HGEMM_ERR_INVALID_ARG;
+  if (ranges_overlap(C, 2 * static_cast<uint64_t>(sc), A, 2 * static_cast<uint64_t>(sa)) ||
+      ranges_overlap(C, 2 * static_cast<uint64_t>(sc), B, 2 * static_cast<uint64_t>(sb)))
+    return HGEMM_ERR_ALIAS;
   DeviceState* dev = nullptr;
+  int rc;
   if ((rc = current_device(&dev)) != HGEMM_OK) return rc;
-  return dispatch(A, B, C, M, N, K, epi, *dev, stream);
+
+  // The page's recursion on blocks [off, off + s) of the triangle: the
+  // diagonal blocks of at most kTrmmLeaf are leaves; every larger block
+  // splits at s1 (half of s rounded up to a multiple of 64, so every block
+  // starts on a multiple of 64) and adds the off-diagonal update
+  //   C[off : off+s1, :] += alpha · A[off+s1 : off+s, off : off+s1]ᵀ · B[off+s1 : off+s, :]
+  // after both halves (post-order: the update of a block sees its first
+  // half complete).
+  struct Update {
+    int64_t off, s1, s2;
+  };
+  hg::TriLeaves leaves{};
+  std::vector<std::vector<Update>> levels;  // updates by depth in the recursion
+  struct Frame {
+    int64_t off, s;
+    int depth;
+  };
+  std::vector<Frame> stack{{0, n, 0}};
+  while (!stack.empty()) {
+    const Frame f = stack.back();
+    stack.pop_back();
+    if (f.s <= kTrmmLeaf) {
+      if (leaves.count == hg::kMaxLeaves) return HGEMM_ERR_INVALID_ARG;
+      leaves.off[leaves.count] = f.off;
+      leaves.size[leaves.count] = f.s;
+      ++leaves.count;
+      continue;
+    }
+    const int64_t s1 = ((f.s / 2 + 63) / 64) * 64;
+    if (static_cast<int>(levels.size()) <= f.depth) levels.resize(f.depth + 1);
+    levels[f.depth].push_back({f.off, s1, f.s - s1});
+    stack.push_back({f.off + s1, f.s - s1, f.depth + 1});
+    stack.push_back({f.off, s1, f.depth + 1});
+  }
+
+  // In the GEMM view, Cᵀ (m × n, pitch ldc) = Bᵀ (m × n, pitch ldb) · lower(A),
+  // where row i of the second operand is column i of A (pitch lda).
+  const hg::EpiArgs scale{alpha, 0.0f, nullptr, 0, alpha != 1.0f ? 1 : 0};
+  hg::PlainArgs pa{reinterpret_cast<const uint16_t*>(B), reinterpret_cast<const uint16_t*>(A),
+                   reinterpret_cast<uint16_t*>(C), m, n, n, ldb, lda, ldc,
+                   dev->status, g_timeout_ns.load(), scale};
+  cudaError_t e = hg::launch_tri_leaves(pa, leaves, stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+
+  // Updates, deepest level first: an update reads the first half of its
+  // block complete, which every deeper level and the leaves have made. The
+  // updates of one level touch disjoint rows of C and run concurrently.
+  const hg::EpiArgs accumulate{alpha, 1.0f, nullptr, 0, 2};
+  auto issue = [&](const Update& u, cudaStream_t st) {
+    const Gemm g{B + u.off + u.s1, A + u.off * lda + u.off + u.s1, C + u.off, m, u.s1, u.s2,
+                 ldb, lda, ldc};
+    const int r = validate(g);
+    return r != HGEMM_OK ? r : dispatch(g, accumulate, *dev, st);
+  };
+  TrmmPipe* tp = nullptr;
+  bool need_pipe = false;
+  for (const auto& lv : levels) need_pipe = need_pipe || lv.size() > 1;
+  if (need_pipe && (rc = trmm_pipe(dev->id, &tp)) != HGEMM_OK) return rc;
+  std::unique_lock<std::mutex> lock;
+  if (tp) lock = std::unique_lock<std::mutex>(tp->mu);
+  for (int d = static_cast<int>(levels.size()) - 1; d >= 0; --d) {
+    const auto& lv = levels[d];
+    if (lv.size() == 1) {
+      if ((rc = issue(lv[0], stream)) != HGEMM_OK) return rc;
+      continue;
+    }
+    const int used = static_cast<int>(lv.size() < TrmmPipe::kStreams ? lv.size() : TrmmPipe::kStreams);
+    if ((e = cudaEventRecord(tp->fork, stream)) != cudaSuccess) return cuda_fail(e);
+    for (int i = 0; i < used; ++i)
+      if ((e = cudaStreamWaitEvent(tp->s[i], tp->fork, 0)) != cudaSuccess) return cuda_fail(e);
+    for (size_t k = 0; k < lv.size(); ++k)
+      if ((rc = issue(lv[k], tp->s[k % used])) != HGEMM_OK) return rc;
+    for (int i = 0; i < used; ++i) {
+      if ((e = cudaEventRecord(tp->join[i], tp->s[i])) != cudaSuccess) return cuda_fail(e);
+      if ((e = cudaStreamWaitEvent(stream, tp->join[i], 0)) != cudaSuccess) return cuda_fail(e);
+    }
+  }
+  return HGEMM_OK;
 }
 
 int hgemm_host(const hgemm_half_t* hA, const hgemm_half_t* hB, hgemm_half_t* hC, int64_t M,
                int64_t N, int64_t K, hgemm_half_t* dA, hgemm_half_t* dB, hgemm_half_t* dC,
                cudaStream_t stream) {
-  int rc = validate(dA, dB, dC, M, N, K);
+  int rc = validate(dense(dA, dB, dC, M, N, K));
   if (rc != HGEMM_OK) return rc;
   if ((M * K && !hA) || (N * K && !hB) || (M * N && !hC)) return HGEMM_ERR_INVALID_ARG;
   if (M == 0 || N == 0) return HGEMM_OK;
@@ -523,7 +724,7 @@ int hgemm_host(const hgemm_half_t* hA, const hgemm_half_t* hB, hgemm_half_t* hC,
     if (N * K &&
         (e = cudaMemcpyAsync(dB, hB, 2 * N * K, cudaMemcpyHostToDevice, stream)) != cudaSuccess)
       return cuda_fail(e);
-    if ((rc = dispatch(dA, dB, dC, M, N, K, kPlainEpilogue, *dev, stream)) != HGEMM_OK) return rc;
+    if ((rc = dispatch(dense(dA, dB, dC, M, N, K), kPlainEpilogue, *dev, stream)) != HGEMM_OK) return rc;
     if ((e = cudaMemcpyAsync(hC, dC, 2 * M * N, cudaMemcpyDeviceToHost, stream)) != cudaSuccess)
       return cuda_fail(e);
     return HGEMM_OK;
@@ -549,7 +750,7 @@ int hgemm_host(const hgemm_half_t* hA, const hgemm_half_t* hB, hgemm_half_t* hC,
     if ((e = cudaEventRecord(in_done, hp->in)) != cudaSuccess ||
         (e = cudaStreamWaitEvent(stream, in_done, 0)) != cudaSuccess)
       return cuda_fail(e);
-    if ((rc = dispatch(dA + r0 * K, dB, dC + r0 * N, mi, N, K, kPlainEpilogue, *dev, stream)) !=
+    if ((rc = dispatch(dense(dA + r0 * K, dB, dC + r0 * N, mi, N, K), kPlainEpilogue, *dev, stream)) !=
         HGEMM_OK)
       return rc;
     if ((e = cudaEventRecord(prod_done, stream)) != cudaSuccess ||
@@ -566,13 +767,12 @@ int hgemm_host(const hgemm_half_t* hA, const hgemm_half_t* hB, hgemm_half_t* hC,
   return HGEMM_OK;
 }
 
-int hgemm_select_path(const void* A, const void* B, const void* C, int64_t M, int64_t N,
-                      int64_t K) {
-  int rc = validate(A, B, C, M, N, K);
+int hgemm_select_path(const void* A, const void* B, const void* C, int64_t M, int64_t N, int64_t K) {
+  const Gemm g = dense(A, B, const_cast<void*>(C), M, N, K);
+  int rc = validate(g);
   if (rc != HGEMM_OK) return rc;
   int split = 1, tile_n = hg::kPairBN;
-  return choose_path(A, B, C, M, N, K, *g_last_profile.load(std::memory_order_acquire), false, &split,
-                     &tile_n);
+  return choose_path(g, *g_last_profile.load(std::memory_order_acquire), false, &split, &tile_n);
 }
 
 int hgemm_force_split(int split, int tile_n) {

@@ -37,8 +37,7 @@ struct GenCfg {
   static constexpr int NUM_BARS = 2 * STAGES + 2;  // full, empty, accumulator full, drain
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
-  static constexpr int LOADER_WARPS = 4;
-  static constexpr int EPI_WARP0 = 4;  // warps 4..7: warp w reads TMEM lanes 32*(w%4)..
+  static constexpr int LOADER_WARPS = 4;  // warps 0..3; warps 4..7 (epilogue) read TMEM lanes 32·(w%4)
   static constexpr int MMA_WARP = 8;
   static constexpr int THREADS = 9 * 32;
   static constexpr int TMEM_COLS = BN;
@@ -46,27 +45,53 @@ struct GenCfg {
   static_assert(SMEM_BYTES <= 232448, "exceeds 227 KB of shared memory per CTA");
 };
 
-// Row r of a K block (64 values from `src`, valid values `n`), zero-padded,
-// into the 128-byte-swizzled K-major row r of a shared-memory tile.
+// Row r of a K block (the values of `src` with index in [first, n); zeros
+// elsewhere) into the 128-byte-swizzled K-major row r of a shared-memory
+// tile. `first` > 0 masks the strictly upper triangle of a triangular operand.
 __device__ __forceinline__ void load_row_swizzled(const uint16_t* __restrict__ src, int n, uint8_t* tile,
-                                                  int r) {
+                                                  int r, int first = 0) {
   uint8_t* row = tile + r * 128;
+  if (n == 64 && (reinterpret_cast<uintptr_t>(src) & 15u) == 0) {
+    // a whole, 16-byte-aligned block: eight vector loads, then the mask
+    uint4 v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = __ldg(reinterpret_cast<const uint4*>(src) + j);
+    if (first > 0) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        uint32_t* w = reinterpret_cast<uint32_t*>(&v[j]);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int k = 8 * j + 2 * u;
+          if (k < first) w[u] &= 0xFFFF0000u;
+          if (k + 1 < first) w[u] &= 0x0000FFFFu;
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) *reinterpret_cast<uint4*>(row + ((j ^ (r & 7)) << 4)) = v[j];
+    return;
+  }
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     uint32_t w[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int k = 8 * j + 2 * u;
-      const uint32_t lo = (k < n) ? static_cast<uint32_t>(__ldg(src + k)) : 0u;
-      const uint32_t hi = (k + 1 < n) ? static_cast<uint32_t>(__ldg(src + k + 1)) : 0u;
+      const uint32_t lo = (k < n && k >= first) ? static_cast<uint32_t>(__ldg(src + k)) : 0u;
+      const uint32_t hi = (k + 1 < n && k + 1 >= first) ? static_cast<uint32_t>(__ldg(src + k + 1)) : 0u;
       w[u] = lo | (hi << 16);
     }
     *reinterpret_cast<uint4*>(row + ((j ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
   }
 }
 
-__global__ void __launch_bounds__(GenCfg::THREADS, 1)
-    hgemm_generic_kernel(const PlainArgs p, int tiles_n, int num_kb) {
+// One 128×128 tile of C at (m0, n0) over num_kb K blocks. TRI_B: the B
+// operand is the lower triangle of a square block (column i of the triangle,
+// i.e. operand row gj, holds its values from index gj on), so values at
+// k < gj are replaced by zero as they are loaded.
+template <bool TRI_B>
+__device__ __forceinline__ void generic_tile(const PlainArgs& p, int64_t m0, int64_t n0, int num_kb) {
   using Cfg = GenCfg;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -82,8 +107,6 @@ __global__ void __launch_bounds__(GenCfg::THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int64_t m0 = static_cast<int64_t>(blockIdx.x / tiles_n) * Cfg::BM;
-  const int64_t n0 = static_cast<int64_t>(blockIdx.x % tiles_n) * Cfg::BN;
   const Watchdog wd{abort_flag, p.status, p.timeout_ns};
 
   if (threadIdx.x == 0) {
@@ -118,10 +141,15 @@ __global__ void __launch_bounds__(GenCfg::THREADS, 1)
       if (!ok) break;
       const int64_t k0 = static_cast<int64_t>(kb) * Cfg::BK;
       const int64_t kn = p.K - k0 < Cfg::BK ? p.K - k0 : Cfg::BK;
-      load_row_swizzled(p.A + gi * p.K + k0, gi < p.M ? static_cast<int>(kn) : 0,
+      load_row_swizzled(p.A + gi * p.lda + k0, gi < p.M ? static_cast<int>(kn) : 0,
                         smem + Cfg::OFF_A + stage * Cfg::A_BYTES, r);
-      load_row_swizzled(p.B + gj * p.K + k0, gj < p.N ? static_cast<int>(kn) : 0,
-                        smem + Cfg::OFF_B + stage * Cfg::B_BYTES, r);
+      int first = 0;
+      if constexpr (TRI_B) {
+        const int64_t f = gj - k0;
+        first = f <= 0 ? 0 : (f >= Cfg::BK ? Cfg::BK : static_cast<int>(f));
+      }
+      load_row_swizzled(p.B + gj * p.ldb + k0, gj < p.N ? static_cast<int>(kn) : 0,
+                        smem + Cfg::OFF_B + stage * Cfg::B_BYTES, r, first);
       fence_proxy_async_smem();  // generic-proxy writes before tensor-core reads
       __syncwarp();
       if (lane == 0) mbar_arrive(full_bar(stage));
@@ -175,8 +203,29 @@ __global__ void __launch_bounds__(GenCfg::THREADS, 1)
         tmem_ld_32x32b_x32(t_row + c * 32, v);
         tmem_ld_wait(v);
         if (gi < p.M) {
-          uint16_t* dst = p.C + gi * p.N + n0 + c * 32;
+          uint16_t* dst = p.C + gi * p.ldc + n0 + c * 32;
           const __half* bias = reinterpret_cast<const __half*>(p.epi.bias);
+          if (n0 + c * 32 + 32 <= p.N && (reinterpret_cast<uintptr_t>(dst) & 15u) == 0 &&
+              (p.epi.mode == 0 || (reinterpret_cast<uintptr_t>(bias) & 15u) == 0)) {
+            // a whole, aligned 32-column piece of the row: four 16-byte stores
+            const int64_t col0 = n0 + c * 32;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              uint4 pk;
+              if (p.epi.mode == 0) {
+                pk.x = pack_half2(v[8 * u], v[8 * u + 1]);
+                pk.y = pack_half2(v[8 * u + 2], v[8 * u + 3]);
+                pk.z = pack_half2(v[8 * u + 4], v[8 * u + 5]);
+                pk.w = pack_half2(v[8 * u + 6], v[8 * u + 7]);
+              } else {
+                const uint4 c_old = p.epi.mode == 2 ? *reinterpret_cast<const uint4*>(dst + 8 * u)
+                                                    : make_uint4(0u, 0u, 0u, 0u);
+                pk = epi_pack8(v + 8 * u, p.epi, c_old, load_bias8(p.epi, col0 + 8 * u, p.N));
+              }
+              *reinterpret_cast<uint4*>(dst + 8 * u) = pk;
+            }
+            continue;
+          }
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const int64_t col = n0 + c * 32 + j;
@@ -198,19 +247,68 @@ __global__ void __launch_bounds__(GenCfg::THREADS, 1)
   if (warp == Cfg::MMA_WARP) tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
 }
 
-}  // namespace
+__global__ void __launch_bounds__(GenCfg::THREADS, 1)
+    hgemm_generic_kernel(const PlainArgs p, int tiles_n, int num_kb) {
+  generic_tile<false>(p, static_cast<int64_t>(blockIdx.x / tiles_n) * GenCfg::BM,
+                      static_cast<int64_t>(blockIdx.x % tiles_n) * GenCfg::BN, num_kb);
+}
 
-cudaError_t launch_generic(const PlainArgs& args, int /*num_sms*/, cudaStream_t stream) {
-  static bool attr_done[64] = {};
+// The diagonal blocks of a triangular product, one per blockIdx.y: leaf b is
+// the product of p's A operand shifted by off columns (M × s) with the lower
+// triangle of p's B operand at (off, off) (s × s), into C shifted by off
+// columns, where off = leaves.off[b] and s = leaves.size[b].
+__global__ void __launch_bounds__(GenCfg::THREADS, 1)
+    hgemm_tri_leaves_kernel(const PlainArgs p, const TriLeaves leaves, int tiles_m) {
+  const int b = blockIdx.y;
+  const int64_t off = leaves.off[b], s = leaves.size[b];
+  const int64_t tiles_n = (s + GenCfg::BN - 1) / GenCfg::BN;
+  if (static_cast<int64_t>(blockIdx.x) >= tiles_n * tiles_m) return;  // this leaf is narrower
+  PlainArgs q = p;
+  q.A = p.A + off;
+  q.B = p.B + off * p.ldb + off;
+  q.C = p.C + off;
+  q.N = s;
+  q.K = s;
+  generic_tile<true>(q, static_cast<int64_t>(blockIdx.x / tiles_n) * GenCfg::BM,
+                     static_cast<int64_t>(blockIdx.x % tiles_n) * GenCfg::BN,
+                     static_cast<int>((s + GenCfg::BK - 1) / GenCfg::BK));
+}
+
+template <typename Kern>
+cudaError_t prepare(Kern kern, bool* done) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64 || !attr_done[dev]) {
-    e = cudaFuncSetAttribute(hgemm_generic_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             GenCfg::SMEM_BYTES);
+  if (dev < 0 || dev >= 64 || !done[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, GenCfg::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) attr_done[dev] = true;
+    if (dev >= 0 && dev < 64) done[dev] = true;
   }
+  return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_tri_leaves(const PlainArgs& args, const TriLeaves& leaves, cudaStream_t stream) {
+  static bool attr_done[64] = {};
+  cudaError_t e = prepare(hgemm_tri_leaves_kernel, attr_done);
+  if (e != cudaSuccess) return e;
+  if (leaves.count < 1 || leaves.count > kMaxLeaves) return cudaErrorInvalidValue;
+  int64_t widest = 0;
+  for (int b = 0; b < leaves.count; ++b) widest = leaves.size[b] > widest ? leaves.size[b] : widest;
+  const int64_t tiles_m = (args.M + GenCfg::BM - 1) / GenCfg::BM;
+  const int64_t tiles = tiles_m * ((widest + GenCfg::BN - 1) / GenCfg::BN);
+  if (tiles > 0x7FFFFFFF || tiles_m > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
+  hgemm_tri_leaves_kernel<<<dim3(static_cast<unsigned>(tiles), static_cast<unsigned>(leaves.count)),
+                            GenCfg::THREADS, GenCfg::SMEM_BYTES, stream>>>(args, leaves,
+                                                                          static_cast<int>(tiles_m));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_generic(const PlainArgs& args, int /*num_sms*/, cudaStream_t stream) {
+  static bool attr_done[64] = {};
+  cudaError_t e = prepare(hgemm_generic_kernel, attr_done);
+  if (e != cudaSuccess) return e;
   const int64_t tiles_n = (args.N + GenCfg::BN - 1) / GenCfg::BN;
   const int64_t tiles = tiles_n * ((args.M + GenCfg::BM - 1) / GenCfg::BM);
   const int64_t num_kb = (args.K + GenCfg::BK - 1) / GenCfg::BK;

@@ -240,7 +240,7 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
   const int row = q * 32 + lane;
   if (FUSED && warp >= 2)
-    prefetch_c_row(p.epi, p.C, p.M, p.N, static_cast<int64_t>(mb) * Cfg::BM + half * Cfg::ROWS + row,
+    prefetch_c_row(p.epi, p.C, p.M, p.N, p.ldc, static_cast<int64_t>(mb) * Cfg::BM + half * Cfg::ROWS + row,
                    static_cast<int64_t>(nb) * Cfg::BN + own_c0, own_cols);
   // ring layout for the exchange: receive slots first, then send staging
   const uint32_t recv_base = sbase;
@@ -338,7 +338,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
             for (int i = 0; i < 8; ++i) vb[i] = __float_as_uint(acc[8 * u + i]);
             const int64_t col0 = static_cast<int64_t>(x0) + c32 * 32 + 8 * u;
-            pk = epi_pack8(vb, p.epi, load_c_old8(p.epi, p.C, p.M, p.N, y0 + lane, col0),
+            pk = epi_pack8(vb, p.epi, load_c_old8(p.epi, p.C, p.M, p.N, p.ldc, y0 + lane, col0),
                            load_bias8(p.epi, col0, p.N));
           }
           const int chunk = c32 * 4 + u;  // 16-byte chunk within the row

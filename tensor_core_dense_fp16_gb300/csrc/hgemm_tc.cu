@@ -224,7 +224,7 @@ __global__ void __launch_bounds__(192, 1)
       int mb, nb;
       tile_coords(t, p.num_m, p.num_n, p.group_m, mb, nb);
       if constexpr (FUSED)
-        prefetch_c_row(p.epi, p.C, p.M, p.N, static_cast<int64_t>(mb) * Cfg::BM + q * kEpiRows + lane,
+        prefetch_c_row(p.epi, p.C, p.M, p.N, p.ldc, static_cast<int64_t>(mb) * Cfg::BM + q * kEpiRows + lane,
                        static_cast<int64_t>(nb) * BN, BN);
       int ok = 1;
       if (lane == 0) ok = wait_phase(accf_bar(acc), acc_phase, wd, kWdEpiAccFull) ? 1 : 0;
@@ -255,7 +255,7 @@ __global__ void __launch_bounds__(192, 1)
         uint8_t* buf = cbuf_base + cb * Cfg::C_BOX_BYTES;
         uint8_t* row = buf + lane * 128;
         // 128-byte swizzle: 16-byte chunk j of row r sits at chunk j ^ (r % 8)
-        stage_row64<FUSED>(row, lane, v0, v1, p.epi, p.C, p.M, p.N, static_cast<int64_t>(y0) + lane, x0);
+        stage_row64<FUSED>(row, lane, v0, v1, p.epi, p.C, p.M, p.N, p.ldc, static_cast<int64_t>(y0) + lane, x0);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
@@ -279,19 +279,22 @@ __global__ void __launch_bounds__(192, 1)
 
 // K = 0: every sum is empty, so C := f(beta·C_old + bias) (alpha·0 = 0), or
 // +0 for the plain product.
-__global__ void empty_sum_kernel(uint16_t* __restrict__ C, int64_t M, int64_t N, const EpiArgs e) {
+__global__ void empty_sum_kernel(uint16_t* __restrict__ C, int64_t M, int64_t N, int64_t ldc,
+                                 const EpiArgs e) {
   const int64_t count = M * N;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   const __half* bias = reinterpret_cast<const __half*>(e.bias);
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < count;
        i += stride) {
+    const int64_t row = i / N, col = i - row * N;
+    uint16_t* c = C + row * ldc + col;
     if (e.mode == 0) {
-      C[i] = 0;
+      *c = 0;
       continue;
     }
-    const float c_old = e.mode == 2 ? __half2float(__ushort_as_half(C[i])) : 0.f;
-    const float b = bias ? __half2float(bias[i % N]) : 0.f;
-    C[i] = __half_as_ushort(__float2half_rn(epi_value(0.f, e, c_old, b)));
+    const float c_old = e.mode == 2 ? __half2float(__ushort_as_half(*c)) : 0.f;
+    const float b = bias ? __half2float(bias[col]) : 0.f;
+    *c = __half_as_ushort(__float2half_rn(epi_value(0.f, e, c_old, b)));
   }
 }
 
@@ -324,13 +327,13 @@ cudaError_t launch_tc_128x256(const CUtensorMap& a, const CUtensorMap& b, const 
   return cudaLaunchKernelEx(&cfg, kern, a, b, c, args);
 }
 
-cudaError_t launch_empty_sum(uint16_t* C, int64_t M, int64_t N, const EpiArgs& epi,
+cudaError_t launch_empty_sum(uint16_t* C, int64_t M, int64_t N, int64_t ldc, const EpiArgs& epi,
                              cudaStream_t stream) {
   const int64_t count = M * N;
   int blocks = static_cast<int>((count + 255) / 256);
   if (blocks > 4096) blocks = 4096;
   if (blocks < 1) blocks = 1;
-  empty_sum_kernel<<<blocks, 256, 0, stream>>>(C, M, N, epi);
+  empty_sum_kernel<<<blocks, 256, 0, stream>>>(C, M, N, ldc, epi);
   return cudaGetLastError();
 }
 

@@ -272,7 +272,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
       const PairTile w = pair_tile(t, p);
       const int chunks = w.ncols / kEpiCols;
       if constexpr (FUSED)
-        prefetch_c_row(p.epi, p.C, p.M, p.N,
+        prefetch_c_row(p.epi, p.C, p.M, p.N, p.ldc,
                        static_cast<int64_t>(w.mb) * Cfg::BM + static_cast<int>(rank) * Cfg::ROWS + q * kEpiRows + lane,
                        w.n0, w.ncols);
       int ok = 1;
@@ -303,7 +303,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
         uint8_t* buf = cbuf_base + cb * Cfg::C_BOX_BYTES;
         uint8_t* row = buf + lane * 128;
         // 128-byte swizzle: 16-byte chunk j of row r sits at chunk j ^ (r % 8)
-        stage_row64<FUSED>(row, lane, v0, v1, p.epi, p.C, p.M, p.N, static_cast<int64_t>(y0) + lane, x0);
+        stage_row64<FUSED>(row, lane, v0, v1, p.epi, p.C, p.M, p.N, p.ldc, static_cast<int64_t>(y0) + lane, x0);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {

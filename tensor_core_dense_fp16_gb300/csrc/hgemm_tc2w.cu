@@ -234,7 +234,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
       int mb, nb;
       tile_coords(t, p.num_m, p.num_n, p.group_m, mb, nb);
       if constexpr (FUSED)
-        prefetch_c_row(p.epi, p.C, p.M, p.N,
+        prefetch_c_row(p.epi, p.C, p.M, p.N, p.ldc,
                        static_cast<int64_t>(mb) * Cfg::BM + static_cast<int>(rank) * Cfg::ROWS + q * kEpiRows + lane,
                        static_cast<int64_t>(nb) * Cfg::BN + h * kPairBN, kPairBN);
       int ok = 1;
@@ -265,7 +265,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
         __syncwarp();
         uint8_t* row = buf + lane * 128;
         // 128-byte swizzle: 16-byte chunk j of row r sits at chunk j ^ (r % 8)
-        stage_row64<FUSED>(row, lane, v0, v1, p.epi, p.C, p.M, p.N, static_cast<int64_t>(y0) + lane, x0);
+        stage_row64<FUSED>(row, lane, v0, v1, p.epi, p.C, p.M, p.N, p.ldc, static_cast<int64_t>(y0) + lane, x0);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {

@@ -47,6 +47,7 @@ struct TcArgs {
   int inject;                // HGEMM_INJECT_* (testing the watchdog)
   EpiArgs epi;
   const uint16_t* C;         // C itself, read in epilogue mode 2
+  int64_t ldc;               // C's row pitch in elements
 };
 
 // Plain-pointer launch arguments for the kernels that do not use TMA.
@@ -55,9 +56,19 @@ struct PlainArgs {
   const uint16_t* B;
   uint16_t* C;
   int64_t M, N, K;
+  int64_t lda, ldb, ldc;     // row pitches in elements
   int* status;
   unsigned long long timeout_ns;
   EpiArgs epi;
+};
+
+// The diagonal blocks ("leaves") of a triangular product, for one batched
+// launch of masked products.
+constexpr int kMaxLeaves = 128;
+struct TriLeaves {
+  int count;
+  int64_t off[kMaxLeaves];   // first row (and column) of each block in the triangle
+  int64_t size[kMaxLeaves];  // its order
 };
 
 // Launchers (each enqueues one kernel on `stream` and returns the launch
@@ -81,9 +92,12 @@ cudaError_t launch_skinny(int split, int tile_n, const CUtensorMap& a, const CUt
 // Largest number of co-resident clusters of the split-K kernel.
 int skinny_max_clusters(int split, int tile_n, int num_sms);
 // K = 0: C := f(beta·C_old + bias) elementwise (plain mode: +0).
-cudaError_t launch_empty_sum(uint16_t* C, int64_t M, int64_t N, const EpiArgs& epi,
+cudaError_t launch_empty_sum(uint16_t* C, int64_t M, int64_t N, int64_t ldc, const EpiArgs& epi,
                              cudaStream_t stream);
 cudaError_t launch_generic(const PlainArgs& args, int num_sms, cudaStream_t stream);
+// Every leaf b: C + off = (A operand + off) · lower(B operand at (off, off)),
+// M × size (see hgemm_generic.cu).
+cudaError_t launch_tri_leaves(const PlainArgs& args, const TriLeaves& leaves, cudaStream_t stream);
 
 // Address of the device watchdog word on the current device.
 cudaError_t status_word_address(int** addr);

@@ -115,21 +115,23 @@ __device__ __forceinline__ float epi_value(float acc, const EpiArgs& e, float c_
 }
 
 // The previous FP16 values C[row, col0 .. col0+7] (mode 2), zeros outside C.
-// col0 and N are multiples of 8 and C's rows 16-byte aligned (TMA paths).
+// col0, N and the row pitch ldc are multiples of 8 (TMA paths), so each
+// read is one aligned 16-byte load inside row `row`.
 __device__ __forceinline__ uint4 load_c_old8(const EpiArgs& e, const uint16_t* C, int64_t M,
-                                             int64_t N, int64_t row, int64_t col0) {
+                                             int64_t N, int64_t ldc, int64_t row, int64_t col0) {
   if (e.mode != 2 || row >= M || col0 >= N) return make_uint4(0u, 0u, 0u, 0u);
-  return *reinterpret_cast<const uint4*>(C + row * N + col0);
+  return *reinterpret_cast<const uint4*>(C + row * ldc + col0);
 }
 
 // Mode 2: asks L2 for the previous C values of row `grow`, columns
 // [x0, x0 + ncols), while the tile's MMAs still run (one request per 64
 // bytes, so rows that straddle 128-byte lines are covered).
 __device__ __forceinline__ void prefetch_c_row(const EpiArgs& e, const uint16_t* C, int64_t M,
-                                               int64_t N, int64_t grow, int64_t x0, int ncols) {
+                                               int64_t N, int64_t ldc, int64_t grow, int64_t x0,
+                                               int ncols) {
   if (e.mode != 2 || grow >= M) return;
   for (int c = 0; c < ncols; c += 32)
-    if (x0 + c < N) asm volatile("prefetch.global.L2 [%0];" ::"l"(C + grow * N + x0 + c));
+    if (x0 + c < N) asm volatile("prefetch.global.L2 [%0];" ::"l"(C + grow * ldc + x0 + c));
 }
 
 // The biases of columns col0 .. col0+7 (zeros past N or without a bias);
@@ -174,8 +176,8 @@ namespace hg {
 template <bool FUSED>
 __device__ __forceinline__ void stage_row64(uint8_t* row, int lane, const uint32_t (&v0)[32],
                                             const uint32_t (&v1)[32], const EpiArgs& e,
-                                            const uint16_t* C, int64_t M, int64_t N, int64_t grow,
-                                            int64_t x0) {
+                                            const uint16_t* C, int64_t M, int64_t N, int64_t ldc,
+                                            int64_t grow, int64_t x0) {
   if constexpr (!FUSED) {
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
@@ -191,7 +193,7 @@ __device__ __forceinline__ void stage_row64(uint8_t* row, int lane, const uint32
   }
   uint4 c_old[8];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) c_old[j] = load_c_old8(e, C, M, N, grow, x0 + 8 * j);
+  for (int j = 0; j < 8; ++j) c_old[j] = load_c_old8(e, C, M, N, ldc, grow, x0 + 8 * j);
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     const uint32_t* v = (j < 4) ? (v0 + 8 * j) : (v1 + 8 * (j - 4));

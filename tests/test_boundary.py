@@ -153,6 +153,40 @@ def test_fused_argument_checks(lib):
     assert lib_.hgemm_ex(A16, B16, C16, 0, 8, 8, 2.0, 1.0, 0x40000000, 1, None) == tc.HGEMM_OK
 
 
+def test_strided_argument_checks(lib):
+    lib_ = tc.load()
+    # pitches shorter than a row
+    assert lib_.hgemm_strided(A16, 7, B16, 8, C16, 8, 4, 8, 8, 1.0, 0.0, None, 0, None) == tc.HGEMM_ERR_INVALID_ARG
+    assert lib_.hgemm_strided(A16, 8, B16, 7, C16, 8, 4, 8, 8, 1.0, 0.0, None, 0, None) == tc.HGEMM_ERR_INVALID_ARG
+    assert lib_.hgemm_strided(A16, 8, B16, 8, C16, 7, 4, 8, 8, 1.0, 0.0, None, 0, None) == tc.HGEMM_ERR_INVALID_ARG
+    # C's span (3 rows of pitch 1024) reaches A
+    assert lib_.hgemm_strided(C16 + 2 * 2048, 8, B16, 8, C16, 1024, 3, 8, 8, 1.0, 0.0, None, 0,
+                              None) == tc.HGEMM_ERR_ALIAS
+    # a huge pitch that would overflow the span
+    assert lib_.hgemm_strided(A16, 1 << 41, B16, 8, C16, 8, 4, 8, 8, 1.0, 0.0, None, 0,
+                              None) == tc.HGEMM_ERR_INVALID_ARG
+    # nothing to do
+    assert lib_.hgemm_strided(A16, 8, B16, 8, C16, 8, 0, 8, 8, 1.0, 0.0, None, 0, None) == tc.HGEMM_OK
+
+
+def test_trmm_argument_checks(lib):
+    lib_ = tc.load()
+    n, m = 64, 8
+    ok = dict(A=A16, lda=n, B=B16, ldb=n, C=C16, ldc=n)
+    def call(**kw):
+        a = {**ok, **kw}
+        return lib_.hgemm_trmm(a["A"], a["lda"], a["B"], a["ldb"], a["C"], a["ldc"], kw.get("n", n),
+                               kw.get("m", m), 1.0, None)
+    assert call(n=tc.HGEMM_TRMM_MAX_N + 1) == tc.HGEMM_ERR_INVALID_ARG
+    assert call(n=-1) == tc.HGEMM_ERR_INVALID_ARG
+    assert call(lda=n - 1) == tc.HGEMM_ERR_INVALID_ARG
+    assert call(ldc=n - 8) == tc.HGEMM_ERR_INVALID_ARG
+    assert call(A=None) == tc.HGEMM_ERR_INVALID_ARG
+    assert call(B=B16 + 1) == tc.HGEMM_ERR_INVALID_ARG
+    assert call(C=A16 + 2 * 10) == tc.HGEMM_ERR_ALIAS     # C inside A's span
+    assert call(n=0) == tc.HGEMM_OK and call(m=0) == tc.HGEMM_OK
+
+
 def test_invalid_arguments_rejected_before_any_device_work(lib):
     bad = [
         (A16, B16, C16, -1, 4, 4),

@@ -171,3 +171,55 @@ def test_fused_guard_bands_untouched(path):
     host = buf.cpu().numpy()
     assert np.all(host[:pad] == sentinel) and np.all(host[pad + M * N:] == sentinel)
     assert_close(host[pad:pad + M * N].view(np.float16).reshape(M, N), ref, what=f"guarded fused {path}")
+
+
+# ---------------------------------------------------------------------------
+# hgemm_strided: sub-matrices with row pitches
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("pitch_pad", [0, 8, 5])
+def test_strided_sub_matrices(path, pitch_pad):
+    """Operands and C inside larger arrays (pitches wider than the rows, by 8
+    elements or by 5, which sends every path to the generic loader); the
+    padding around C must be left untouched."""
+    torch = torch_cuda()
+    M, N, K = 300, 200, 136
+    lda, ldb, ldc = K + pitch_pad, K + pitch_pad + 8, N + pitch_pad
+    a, b, c_old, bias = inputs(M, N, K, seed=600 + pitch_pad)
+    big_a = np.zeros((M, lda), np.float16); big_a[:, :K] = a
+    big_b = np.zeros((N, ldb), np.float16); big_b[:, :K] = b
+    big_c = np.full((M, ldc), 7.0, np.float16); big_c[:, :N] = c_old
+    da, db, dc, dbias = to_device(big_a), to_device(big_b), to_device(big_c), to_device(bias)
+    ref = oracle.hgemm_ex(a, b, c_old, 0.5, 1.0, bias, True)
+    if path is not None:
+        tc.hgemm_force_path(path)
+    try:
+        tc.hgemm_strided(da, lda, db, ldb, dc, ldc, M, N, K, 0.5, 1.0, dbias, True)
+    finally:
+        tc.hgemm_force_path(-1)
+    assert tc.hgemm_device_status() == tc.HGEMM_OK
+    got = dc.cpu().numpy()
+    assert_close(got[:, :N], ref, what=f"strided path {path} pad {pitch_pad}")
+    assert np.all(got[:, N:] == 7.0)
+
+
+def test_strided_offset_blocks_of_one_matrix():
+    """A, B and C as blocks of larger column-major matrices, as the TRMM
+    recursion uses them (offsets into the same arrays, pitch n)."""
+    torch = torch_cuda()
+    n, m = 512, 256
+    rng = np.random.default_rng(9)
+    big_a = rng.uniform(-1, 1, size=(n, n)).astype(np.float16)   # rows: pitch n
+    big_b = rng.uniform(-1, 1, size=(n, n)).astype(np.float16)
+    big_c = np.zeros((n, n), np.float16)
+    da, db, dc = to_device(big_a), to_device(big_b), to_device(big_c)
+    h = n // 2
+    # C[h:, :m] = A[h:, h:] · B-block whose column j is big_b[j, h:]
+    tc.hgemm_strided(da.data_ptr() + 2 * (h * n + h), n, db.data_ptr() + 2 * h, n,
+                     dc.data_ptr() + 2 * (h * n), n, h, m, h)
+    assert tc.hgemm_device_status() == tc.HGEMM_OK
+    got = dc.cpu().numpy()
+    ref = oracle.hgemm(big_a[h:, h:], big_b[:m, h:])
+    assert_close(got[h:, :m], ref, what="offset blocks")
+    assert np.all(got[:h] == 0) and np.all(got[h:, m:] == 0)

@@ -1,0 +1,80 @@
+"""The triangular product of "异构计算中高性能TRMM与TRSM的递归算法实现" (§2.2,
+B ← alpha·Aᵀ·B with A lower triangular, here out of place: C = alpha·Aᵀ·B)
+through hgemm_trmm, against the oracle (GPU only).
+
+Inputs follow the page's example (§5.1: rand(Float32) operands, uniform on
+[0, 1)), here rounded to FP16. With nonnegative terms every intermediate
+block the recursion rounds to FP16 is no larger than the final value, so the
+per-element tolerance of the plain product applies."""
+
+import numpy as np
+import pytest
+
+import oracle
+import tensor_core_dense_fp16_gb300 as tc
+from gpu_helpers import assert_close, oracle_threads, to_device, torch_cuda
+
+pytestmark = pytest.mark.gpu
+
+
+def trmm_inputs(n, m, seed):
+    rng = np.random.default_rng(seed)
+    a = rng.uniform(0, 1, size=(n, n)).astype(np.float16)
+    b = rng.uniform(0, 1, size=(n, m)).astype(np.float16)
+    return a, b
+
+
+def run_trmm(a, b, alpha=1.0, pad=(0, 0, 0), poison_upper=False):
+    """Column-major device buffers with pitches n + pad."""
+    torch = torch_cuda()
+    n, m = b.shape
+    lda, ldb, ldc = n + pad[0], n + pad[1], n + pad[2]
+    a_col = np.zeros((n, lda), np.float16)     # row c holds column c of A
+    a_col[:, :n] = a.T
+    if poison_upper:
+        r, c = np.triu_indices(n, 1)            # A(r, c) with c > r: above the diagonal
+        a_col[c, r] = np.nan
+    b_col = np.zeros((m, ldb), np.float16)
+    b_col[:, :n] = b.T
+    c_col = np.full((m, ldc), 5.0, np.float16)
+    da, db, dc = to_device(a_col), to_device(b_col), to_device(c_col)
+    tc.hgemm_trmm(da, lda, db, ldb, dc, ldc, n, m, alpha)
+    assert tc.hgemm_device_status() == tc.HGEMM_OK
+    torch.cuda.synchronize()
+    out = dc.cpu().numpy()
+    assert np.all(out[:, n:] == 5.0), "pitch padding of C was written"
+    return np.ascontiguousarray(out[:, :n].T)
+
+
+@pytest.mark.parametrize("n,m", [(64, 32), (256, 100), (257, 64), (300, 136), (512, 256),
+                                 (1000, 128), (4096, 256)])
+def test_trmm_matches_oracle(n, m):
+    a, b = trmm_inputs(n, m, seed=n + m)
+    ref = oracle.trmm(a, b, nthreads=oracle_threads())
+    assert_close(run_trmm(a, b), ref, what=f"trmm {n}x{m}")
+
+
+def test_trmm_reads_only_the_lower_triangle():
+    n, m = 700, 96
+    a, b = trmm_inputs(n, m, seed=7)
+    ref = oracle.trmm(a, b, nthreads=oracle_threads())
+    assert_close(run_trmm(a, b, poison_upper=True), ref, what="NaN above the diagonal")
+
+
+@pytest.mark.parametrize("pad", [(8, 16, 8), (3, 5, 1)])
+def test_trmm_pitches_and_alpha(pad):
+    """Wider pitches (multiples of 8: tensor-core updates; odd ones: the
+    generic loader) and a scale factor."""
+    n, m = 600, 72
+    a, b = trmm_inputs(n, m, seed=11 + pad[0])
+    ref = oracle.trmm(a, b, alpha=0.5, nthreads=oracle_threads())
+    assert_close(run_trmm(a, b, alpha=0.5, pad=pad), ref, what=f"trmm pad {pad}")
+
+
+def test_trmm_repeatable():
+    torch = torch_cuda()
+    n, m = 1024, 64
+    a, b = trmm_inputs(n, m, seed=3)
+    first = run_trmm(a, b)
+    for _ in range(3):
+        assert np.array_equal(run_trmm(a, b).view(np.uint16), first.view(np.uint16))
