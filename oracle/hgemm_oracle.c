@@ -335,3 +335,87 @@ int oracle_trmm(const uint16_t *A, int64_t lda, const uint16_t *B, int64_t ldb, 
     free(jobs);
     return 0;
 }
+
+/* ---- the triangular solve ------------------------------------------------
+ *
+ * "异构计算中高性能TRMM与TRSM的递归算法实现", §2.3 (TRSM: solve for X), in the
+ * same variant as the triangular product above (left side, lower triangle,
+ * transposed), out of place, every matrix column-major:
+ *
+ *     Aᵀ · X = alpha · B,   X(i,j) = fp16_rne( x_i )  for each column j
+ *
+ * where x solves the upper-triangular system Aᵀ x = alpha·b in FP64 by back
+ * substitution, x_i = (alpha·b_i − Σ_{k>i} A(k,i)·x_k) / A(i,i), k in
+ * increasing order, rounded once at the end. Only the lower triangle of A
+ * (row ≥ column) is read; a zero on the diagonal gives ±Inf or NaN, as the
+ * division does. */
+
+struct trsm_job {
+    const uint16_t *A, *B;
+    uint16_t *X;
+    int64_t lda, ldb, ldx, n;
+    double alpha;
+    int64_t col_lo, col_hi;
+    double *work;    /* n doubles per job */
+};
+
+static void *trsm_worker(void *arg)
+{
+    const struct trsm_job *jb = (const struct trsm_job *)arg;
+    const int64_t n = jb->n;
+    double *x = jb->work;
+    for (int64_t j = jb->col_lo; j < jb->col_hi; ++j) {
+        for (int64_t i = n - 1; i >= 0; --i) {
+            double s = jb->alpha * g_decode[jb->B[j * jb->ldb + i]];
+            for (int64_t k = i + 1; k < n; ++k)
+                s -= g_decode[jb->A[i * jb->lda + k]] * x[k];
+            x[i] = s / g_decode[jb->A[i * jb->lda + i]];
+        }
+        for (int64_t i = 0; i < n; ++i)
+            jb->X[j * jb->ldx + i] = oracle_double_to_fp16(x[i]);
+    }
+    return NULL;
+}
+
+int oracle_trsm(const uint16_t *A, int64_t lda, const uint16_t *B, int64_t ldb, uint16_t *X,
+                int64_t ldx, int64_t n, int64_t m, double alpha, int nthreads)
+{
+    pthread_once(&g_decode_once, fill_decode_table);
+    if (n <= 0 || m <= 0)
+        return 0;
+    if (nthreads < 1)
+        nthreads = 1;
+    if (nthreads > m)
+        nthreads = (int)m;
+    pthread_t *th = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    struct trsm_job *jobs = (struct trsm_job *)calloc((size_t)nthreads, sizeof(struct trsm_job));
+    char *live = (char *)calloc((size_t)nthreads, 1);
+    double *work = (double *)malloc((size_t)nthreads * (size_t)n * sizeof(double));
+    if (!th || !jobs || !live || !work) {
+        free(th);
+        free(jobs);
+        free(live);
+        free(work);
+        return -1;
+    }
+    for (int t = 0; t < nthreads; ++t) {
+        struct trsm_job jb = {A, B, X, lda, ldb, ldx, n, alpha, m * t / nthreads, m * (t + 1) / nthreads,
+                              work + (size_t)t * (size_t)n};
+        jobs[t] = jb;
+        if (t == 0)
+            continue;
+        if (pthread_create(&th[t], NULL, trsm_worker, &jobs[t]) == 0)
+            live[t] = 1;
+        else
+            trsm_worker(&jobs[t]);
+    }
+    trsm_worker(&jobs[0]);
+    for (int t = 1; t < nthreads; ++t)
+        if (live[t])
+            pthread_join(th[t], NULL);
+    free(work);
+    free(live);
+    free(th);
+    free(jobs);
+    return 0;
+}

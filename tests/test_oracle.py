@@ -390,3 +390,65 @@ def test_trmm_identity_and_scaling():
     eye = np.eye(n, dtype=np.float16)
     assert np.array_equal(bits(oracle.trmm(eye, b)), bits(b))
     assert np.array_equal(bits(oracle.trmm(eye, b, alpha=2.0)), bits((b.astype(np.float64) * 2).astype(np.float16)))
+
+
+# ---------------------------------------------------------------------------
+# the triangular solve: Aᵀ·X = alpha·B, A lower
+
+
+def well_conditioned_lower(rng, n):
+    """Diagonal in [1, 2), strictly lower part in [0, 1/n): a diagonally
+    dominant triangle, so the solve is well conditioned."""
+    a = (rng.uniform(0, 1, size=(n, n)) / n).astype(np.float16)
+    a[np.diag_indices(n)] = rng.uniform(1, 2, size=n).astype(np.float16)
+    return a
+
+
+def test_trsm_against_scipy_and_residual():
+    import scipy.linalg
+    rng = np.random.default_rng(51)
+    n, m = 90, 21
+    a = well_conditioned_lower(rng, n)
+    b = rng.uniform(0, 1, size=(n, m)).astype(np.float16)
+    x = oracle.trsm(a, b, alpha=1.5)
+    lower = np.tril(a.astype(np.float64))
+    ref = scipy.linalg.solve_triangular(lower.T, 1.5 * b.astype(np.float64), lower=False)
+    # one rounding of the exact FP64 solution
+    assert np.array_equal(bits(x), bits(ref.astype(np.float16)))
+    # the rounded solution satisfies the system up to FP16 rounding
+    resid = lower.T @ x.astype(np.float64) - 1.5 * b.astype(np.float64)
+    assert np.max(np.abs(resid)) < 4 * 2.0 ** -11 * np.max(np.abs(1.5 * b.astype(np.float64))) + 1e-3
+
+
+def test_trsm_bruteforce_exact_rationals():
+    rng = np.random.default_rng(52)
+    for n, m in [(1, 1), (2, 2), (4, 3), (6, 2)]:
+        a = well_conditioned_lower(rng, n)
+        b = random_fp16(rng, (n, m))
+        got = bits(oracle.trsm(a, b, alpha=0.5))
+        for j in range(m):
+            x = [Fraction(0)] * n
+            for i in range(n - 1, -1, -1):
+                s = Fraction(0.5) * Fraction(float(b[i, j]))
+                for k in range(i + 1, n):
+                    s -= Fraction(float(a[k, i])) * x[k]
+                x[i] = s / Fraction(float(a[i, i]))
+            for i in range(n):
+                assert got[i, j] == fraction_to_fp16_bits(x[i]), (n, m, i, j)
+
+
+def test_trsm_inverts_trmm_and_ignores_the_upper_triangle():
+    rng = np.random.default_rng(53)
+    n, m = 48, 7
+    a = well_conditioned_lower(rng, n)
+    eye = np.eye(n, dtype=np.float16)
+    b = random_fp16(rng, (n, m))
+    assert np.array_equal(bits(oracle.trsm(eye, b, alpha=2.0)),
+                          bits((b.astype(np.float64) * 2).astype(np.float16)))
+    poisoned = a.copy()
+    poisoned[np.triu_indices(n, 1)] = np.nan
+    assert np.array_equal(bits(oracle.trsm(poisoned, b)), bits(oracle.trsm(a, b)))
+    # solving against the product recovers the right-hand side (to FP16 rounding)
+    c = oracle.trmm(a, b)
+    back = oracle.trsm(a, c).astype(np.float64)
+    assert np.allclose(back, b.astype(np.float64), rtol=1e-2, atol=1e-2)
