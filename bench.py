@@ -51,6 +51,8 @@ def metric_for(name, spec):
         return METRIC
     if spec.get("op") == "trmm":
         return f"TRMM TFLOP/s (n(n+1)m/t) at n={spec['n']}, m={spec['m']} fp16"
+    if spec.get("op") == "trsm":
+        return f"TRSM TFLOP/s (n^2 m/t) at n={spec['n']}, m={spec['m']} fp16"
     return f"HGEMM TFLOP/s (2MNK/t) at {spec['M']}x{spec['N']}x{spec['K']} fp16"
 UNIT = "TFLOP/s"
 DEFAULT_WORKLOAD = "hgemm_8192"
@@ -71,6 +73,10 @@ DESCRIPTIONS = {
                  "A, B uniform[0,1]",
     "trmm_4096x256": "C = A^T B, A 4096x4096 lower triangular, B 4096x256, column-major fp16; "
                      "A, B uniform[0,1]",
+    "trsm_8192": "solve A^T X = B, A 8192x8192 lower triangular (diagonal uniform[1,2], "
+                 "below it uniform[0,1/n]), B 8192x8192 uniform[0,1], column-major fp16",
+    "trsm_4096x256": "solve A^T X = B, A 4096x4096 lower triangular (diagonal uniform[1,2], "
+                     "below it uniform[0,1/n]), B 4096x256 uniform[0,1], column-major fp16",
 }
 
 
@@ -88,6 +94,31 @@ def trmm_launches(n, leaf=256):
 def trmm_flops(spec):
     """Multiply-adds of the triangular product, two flops each: n(n+1)/2 per column."""
     return float(spec["n"]) * (spec["n"] + 1) * spec["m"]
+
+
+def trsm_launches(n, leaf=256):
+    """Kernel launches of one hgemm_trsm (alpha = 1, out of place): the scaled
+    copy, one diagonal solve per leaf and one GEMM per split block."""
+    def count(s):
+        if s <= leaf:
+            return 1
+        s1 = ((s // 2 + 63) // 64) * 64
+        return 1 + count(s1) + count(s - s1)
+    return 1 + count(n)
+
+
+def trsm_flops(spec):
+    """Back substitution per column: n(n-1)/2 multiply-adds and n divisions, n^2 flops."""
+    return float(spec["n"]) * spec["n"] * spec["m"]
+
+
+# The triangular operations: the call, its oracle, its flop count and launches.
+TRI_OPS = {
+    "trmm": dict(call="hgemm_trmm", oracle="trmm", flops=trmm_flops, launches=trmm_launches,
+                 kernel="hgemm_tri_leaves_kernel + hgemm update kernels"),
+    "trsm": dict(call="hgemm_trsm", oracle="trsm", flops=trsm_flops, launches=trsm_launches,
+                 kernel="scale_copy_kernel + trsm_leaf_kernel + hgemm update kernels"),
+}
 
 
 def parse_args():
@@ -319,8 +350,8 @@ def oracle_sample(spec, a, b, target_s, nthreads):
 def run_reference(args, spec, a, b, world, rank):
     if rank != 0:
         return 0
-    if spec.get("op") == "trmm":
-        return run_trmm_reference(args, spec, a, b, world)
+    if spec.get("op") in TRI_OPS:
+        return run_tri_reference(args, spec, a, b, world)
     nthreads = os.cpu_count() or 1
     per_step = max(0.05, args.reference_seconds / max(1, args.steps + args.warmup))
     import oracle
@@ -359,31 +390,32 @@ def run_reference(args, spec, a, b, world, rank):
     return 0
 
 
-def trmm_oracle_columns(a_col, b_col, cols, nthreads):
-    """The oracle's triangular product on the first `cols` columns of B."""
+def tri_oracle_columns(op, a_col, b_col, cols, nthreads):
+    """The oracle's triangular product or solve on the first `cols` columns of B."""
     import oracle
-    return oracle.trmm(a_col.T, b_col[:cols].T, nthreads=nthreads)
+    return getattr(oracle, TRI_OPS[op]["oracle"])(a_col.T, b_col[:cols].T, nthreads=nthreads)
 
 
-def run_trmm_reference(args, spec, a_col, b_col, world):
+def run_tri_reference(args, spec, a_col, b_col, world):
     import oracle
     oracle.build()
+    op = spec["op"]
     nthreads = os.cpu_count() or 1
     n, m = spec["n"], spec["m"]
     per_step = max(0.05, args.reference_seconds / max(1, args.steps + args.warmup))
     cols = min(m, nthreads)
     t = time.perf_counter()
-    trmm_oracle_columns(a_col, b_col, cols, nthreads)
+    tri_oracle_columns(op, a_col, b_col, cols, nthreads)
     dt = time.perf_counter() - t
     cols = max(min(m, nthreads), min(m, int(cols * per_step / max(dt, 1e-6))))
     times = []
     for i in range(args.warmup + args.steps):
         t = time.perf_counter()
-        trmm_oracle_columns(a_col, b_col, cols, nthreads)
+        tri_oracle_columns(op, a_col, b_col, cols, nthreads)
         if i >= args.warmup:
             times.append(time.perf_counter() - t)
     total = sum(times)
-    value = float(n) * (n + 1) * cols * len(times) / total / 1e12
+    value = TRI_OPS[op]["flops"](dict(spec, m=cols)) * len(times) / total / 1e12
     sample = (f"the first {cols} columns of B per step (n={n}) of the {args.workload} workload; "
               f"FP64 oracle, {nthreads} threads")
     line = {
@@ -402,9 +434,9 @@ def run_trmm_reference(args, spec, a_col, b_col, world):
     return 0
 
 
-def run_trmm_ours(args, spec, a_col, b_col, world, rank, local):
-    """The TRMM page's product through hgemm_trmm: same timing protocol as
-    the GEMM workloads (L2 flushed before every timed call)."""
+def run_tri_ours(args, spec, a_col, b_col, world, rank, local):
+    """The TRMM page's product (hgemm_trmm) or solve (hgemm_trsm): same timing
+    protocol as the GEMM workloads (L2 flushed before every timed call)."""
     import torch
     import tensor_core_dense_fp16_gb300 as tc
 
@@ -416,7 +448,10 @@ def run_trmm_ours(args, spec, a_col, b_col, world, rank, local):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
     n, m = spec["n"], spec["m"]
-    flops = trmm_flops(spec)
+    op = spec["op"]
+    ops = TRI_OPS[op]
+    flops = ops["flops"](spec)
+    call = getattr(tc, ops["call"])
     stream = torch.cuda.current_stream(dev)
     da = torch.from_numpy(a_col).to(dev)
     db = torch.from_numpy(b_col).to(dev)
@@ -425,7 +460,7 @@ def run_trmm_ours(args, spec, a_col, b_col, world, rank, local):
     flush = torch.empty(2 * l2 // 4 + 1, dtype=torch.float32, device=dev)
 
     def step():
-        tc.hgemm_trmm(da, n, db, n, dc, n, n, m, 1.0, stream)
+        call(da, n, db, n, dc, n, n, m, 1.0, stream)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -491,21 +526,21 @@ def run_trmm_ours(args, spec, a_col, b_col, world, rank, local):
     roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
             "frac": achieved / peak, "traffic": None,
             "peak_source": f"{peak_src}: bf16_tflops (burst) x {FP16_PER_BF16} fp16/bf16",
-            "kernel": "hgemm_tri_leaves_kernel + hgemm update kernels",
+            "kernel": ops["kernel"],
             "algorithmic_flops": flops, "algorithmic_bytes": 2.0 * (n * (n + 1) / 2 + 2 * n * m)}
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         nthreads = os.cpu_count() or 1
         cols = min(m, nthreads)
         t = time.perf_counter()
-        trmm_oracle_columns(a_col, b_col, cols, nthreads)
+        tri_oracle_columns(op, a_col, b_col, cols, nthreads)
         dt = time.perf_counter() - t
         if dt < args.cpu_seconds:
             cols = min(m, max(cols, int(cols * args.cpu_seconds / max(dt, 1e-6))))
             t = time.perf_counter()
-            trmm_oracle_columns(a_col, b_col, cols, nthreads)
+            tri_oracle_columns(op, a_col, b_col, cols, nthreads)
             dt = time.perf_counter() - t
-        cpu = {"value": float(n) * (n + 1) * cols / dt / 1e12, "unit": UNIT, "cores": nthreads,
+        cpu = {"value": ops["flops"](dict(spec, m=cols)) / dt / 1e12, "unit": UNIT, "cores": nthreads,
                "kind": "oracle",
                "sample": f"the first {cols} columns of B (n={n}) of the {args.workload} workload "
                          f"in {dt:.1f} s; FP64 oracle, {nthreads} threads"}
@@ -518,10 +553,10 @@ def run_trmm_ours(args, spec, a_col, b_col, world, rank, local):
             "config": {"workload": f"{args.workload}: {DESCRIPTIONS.get(args.workload, '')}",
                        "n": n, "m": m, "seed": spec["seed"],
                        "l2": "flushed before every timed call (write of 2x L2 size, outside the events)",
-                       "inputs": "resident in HBM", "path": "hgemm_trmm",
+                       "inputs": "resident in HBM", "path": ops["call"],
                        "parallelism": f"replicas x{world}"},
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": args.steps * trmm_launches(n), "clocks": clocks,
+            "gpu_launches": args.steps * ops["launches"](n), "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
     if dist:
@@ -694,8 +729,8 @@ def main():
     a, b, spec = synth.workload(args.workload)
     if args.impl == "reference":
         return run_reference(args, spec, a, b, world, rank)
-    if spec.get("op") == "trmm":
-        return run_trmm_ours(args, spec, a, b, world, rank, local)
+    if spec.get("op") in TRI_OPS:
+        return run_tri_ours(args, spec, a, b, world, rank, local)
     return run_ours(args, spec, a, b, world, rank, local)
 
 

@@ -145,7 +145,8 @@ HGEMM_API int hgemm_strided(const hgemm_half_t *A, int64_t lda, const hgemm_half
  *     C = alpha · Aᵀ · B
  *
  * A is n×n lower triangular and only its lower triangle (row ≥ column) is
- * read; B and C are n×m. All three are column-major, as on the page (Julia):
+ * used: the entries above the diagonal may hold anything, NaN included (they
+ * lie inside A's span and may be loaded, never used); B and C are n×m. All three are column-major, as on the page (Julia):
  * A(r,c) at A[c·lda + r], B(r,j) at B[j·ldb + r], C(r,j) at C[j·ldc + r],
  * with lda, ldb, ldc ≥ n; n ≤ HGEMM_TRMM_MAX_N (n or m = 0: nothing to do). By the page's
  * recursion (§2.1, §2.2): a block splits into halves; C1 = A11ᵀ·B1, then the
@@ -158,6 +159,34 @@ HGEMM_API int hgemm_strided(const hgemm_half_t *A, int64_t lda, const hgemm_half
  */
 HGEMM_API int hgemm_trmm(const hgemm_half_t *A, int64_t lda, const hgemm_half_t *B, int64_t ldb,
                hgemm_half_t *C, int64_t ldc, int64_t n, int64_t m, float alpha,
+               cudaStream_t stream);
+
+/*
+ * hgemm_trsm — the triangular solve of "异构计算中高性能TRMM与TRSM的递归算法实现"
+ * §2.3, in the variant of hgemm_trmm's product (left side, lower triangle,
+ * transposed):
+ *
+ *     solve  Aᵀ · X = alpha · B  for X
+ *
+ * A is n×n lower triangular and only its lower triangle (row ≥ column) is
+ * used: the entries above the diagonal may hold anything, NaN included (they
+ * lie inside A's span and may be loaded, never used); B and X are n×m (m
+ * right-hand sides). All three are column-major:
+ * A(r,c) at A[c·lda + r], B(r,j) at B[j·ldb + r], X(r,j) at X[j·ldx + r],
+ * with lda, ldb, ldx ≥ n (n or m = 0: nothing to do). X = B with ldx = ldb
+ * solves in place (B is overwritten, as in BLAS); any other overlap of X with
+ * A or B is HGEMM_ERR_ALIAS. By the page's recursion (§2.1): X := alpha·B;
+ * a block splits into halves, the second is solved first, then the GEMM
+ * update X1 -= A21ᵀ·X2 (hgemm's accumulate epilogue with alpha = -1), then
+ * the first half; diagonal blocks of order ≤ 256 are solved by substitution,
+ * the right-hand sides spread over thread blocks and one barrier per row
+ * (§2.3). Storage is FP16 (X is rounded after the scaling, after each update
+ * and after each diagonal solve), arithmetic FP32. A zero on the diagonal is
+ * not reported: as in BLAS, the result then holds Inf or NaN. The calls are
+ * enqueued on `stream`, one after another. Same return values as hgemm.
+ */
+HGEMM_API int hgemm_trsm(const hgemm_half_t *A, int64_t lda, const hgemm_half_t *B, int64_t ldb,
+               hgemm_half_t *X, int64_t ldx, int64_t n, int64_t m, float alpha,
                cudaStream_t stream);
 
 /*

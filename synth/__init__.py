@@ -32,6 +32,12 @@ The triangular product (``trmm_operands``) takes A (n×n, its lower triangle
 is the operand) and B (n×m), both column-major as on the TRMM page: arrays of
 n columns (A) and m columns (B) of n contiguous values. A's stream uses draws
 0 .. n*n-1, B's continues after it.
+
+The triangular solve (``trsm_operands``) needs a triangle that is well
+conditioned in FP16, which a uniform [0, 1) triangle is not (its inverse
+grows exponentially with n). Its A takes the same draws u, as 1 + u on the
+diagonal and u / n elsewhere (a diagonally dominant triangle: every column
+of the strict lower part sums to less than 1 ≤ the diagonal); B is ``unit``.
 """
 
 from __future__ import annotations
@@ -107,6 +113,9 @@ WORKLOADS = {
     # with a 4096×256 right-hand side (its example, §5.1)
     "trmm_8192": dict(op="trmm", n=8192, m=8192, kind="unit", seed=1005),
     "trmm_4096x256": dict(op="trmm", n=4096, m=256, kind="unit", seed=1006),
+    # the solve on the same shapes (§4.2 times it at 8192×8192)
+    "trsm_8192": dict(op="trsm", n=8192, m=8192, kind="dominant", seed=1007),
+    "trsm_4096x256": dict(op="trsm", n=4096, m=256, kind="dominant", seed=1008),
 }
 
 
@@ -119,11 +128,27 @@ def trmm_operands(n: int, m: int, seed: int, kind: str = "unit"):
     return a, b
 
 
+def trsm_operands(n: int, m: int, seed: int):
+    """(a_col, b_col) as for trmm_operands, with the diagonally dominant A."""
+    a = np.empty(n * n, dtype=np.float16)
+    for lo in range(0, n * n, _CHUNK):
+        cnt = min(_CHUNK, n * n - lo)
+        u = uniform01(seed, lo, cnt)
+        idx = np.arange(lo, lo + cnt)
+        diag = (idx // n) == (idx % n)
+        a[lo:lo + cnt] = np.where(diag, 1.0 + u, u / n).astype(np.float16)
+    b = _fill(seed, n * n, m * n, "unit", 1.0).reshape(m, n)
+    return a.reshape(n, n), b
+
+
 def workload(name: str):
     """(A, B, spec) for a named workload."""
     spec = WORKLOADS[name]
     if spec.get("op") == "trmm":
         a, b = trmm_operands(spec["n"], spec["m"], spec["seed"], spec["kind"])
+        return a, b, spec
+    if spec.get("op") == "trsm":
+        a, b = trsm_operands(spec["n"], spec["m"], spec["seed"])
         return a, b, spec
     a, b = operands(spec["M"], spec["N"], spec["K"], spec["seed"], spec["kind"])
     return a, b, spec

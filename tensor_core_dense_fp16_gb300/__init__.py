@@ -28,7 +28,7 @@ __all__ = [
     "HgemmError", "library_path", "load", "hgemm", "hgemm_host", "hgemm_select_path",
     "hgemm_force_path", "hgemm_device_status", "hgemm_last_cuda_error",
     "hgemm_status_string", "hgemm_version", "hgemm_set_wait_timeout", "hgemm_debug_inject",
-    "hgemm_force_split", "hgemm_ex", "hgemm_strided", "hgemm_trmm", "HGEMM_TRMM_MAX_N",
+    "hgemm_force_split", "hgemm_ex", "hgemm_strided", "hgemm_trmm", "hgemm_trsm", "HGEMM_TRMM_MAX_N",
     "HGEMM_INJECT_NONE", "HGEMM_INJECT_DROP_ARRIVAL", "matmul",
 ]
 
@@ -94,6 +94,8 @@ def load():
     lib.hgemm_strided.restype = i32
     lib.hgemm_trmm.argtypes = [vp, i64, vp, i64, vp, i64, i64, i64, ctypes.c_float, vp]
     lib.hgemm_trmm.restype = i32
+    lib.hgemm_trsm.argtypes = [vp, i64, vp, i64, vp, i64, i64, i64, ctypes.c_float, vp]
+    lib.hgemm_trsm.restype = i32
     lib.hgemm_host.argtypes = [vp, vp, vp, i64, i64, i64, vp, vp, vp, vp]
     lib.hgemm_host.restype = i32
     lib.hgemm_select_path.argtypes = [vp, vp, vp, i64, i64, i64]
@@ -209,6 +211,14 @@ def hgemm_trmm(A, lda: int, B, ldb: int, C, ldc: int, n: int, m: int, alpha: flo
     """C = alpha·Aᵀ·B, A lower triangular; column-major operands (see hgemm.h)."""
     _raise_on(load().hgemm_trmm(_ptr(A), lda, _ptr(B), ldb, _ptr(C), ldc, n, m, float(alpha),
                                 _stream(stream)), "hgemm_trmm")
+
+
+def hgemm_trsm(A, lda: int, B, ldb: int, X, ldx: int, n: int, m: int, alpha: float = 1.0,
+               stream=None) -> None:
+    """Solves Aᵀ·X = alpha·B for X, A lower triangular; column-major operands;
+    X may be B itself (same pitch) to solve in place (see hgemm.h)."""
+    _raise_on(load().hgemm_trsm(_ptr(A), lda, _ptr(B), ldb, _ptr(X), ldx, n, m, float(alpha),
+                                _stream(stream)), "hgemm_trsm")
 
 
 def hgemm_host(hA, hB, hC, M: int, N: int, K: int, dA, dB, dC, stream=None) -> None:

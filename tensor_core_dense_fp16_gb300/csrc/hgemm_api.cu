@@ -12,6 +12,7 @@
 #include <vector>
 #include <cstdlib>
 #include <cstring>
+#include <functional>
 #include <mutex>
 
 #include <cuda.h>
@@ -696,6 +697,65 @@ int hgemm_trmm(const hgemm_half_t* A, int64_t lda, const hgemm_half_t* B, int64_
     }
   }
   return HGEMM_OK;
+}
+
+int hgemm_trsm(const hgemm_half_t* A, int64_t lda, const hgemm_half_t* B, int64_t ldb,
+               hgemm_half_t* X, int64_t ldx, int64_t n, int64_t m, float alpha,
+               cudaStream_t stream) {
+  if (n < 0 || m < 0 || n > HGEMM_MAX_DIM || m > HGEMM_MAX_DIM) return HGEMM_ERR_INVALID_ARG;
+  if (n == 0 || m == 0) return HGEMM_OK;
+  const int64_t ld_lim = int64_t(1) << 40;
+  if (lda < n || ldb < n || ldx < n || lda > ld_lim || ldb > ld_lim || ldx > ld_lim)
+    return HGEMM_ERR_INVALID_ARG;
+  if (!A || !B || !X) return HGEMM_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B) |
+       reinterpret_cast<uintptr_t>(X)) & 1u)
+    return HGEMM_ERR_INVALID_ARG;
+  // column-major spans (in elements): A n×n, B and X n×m
+  const unsigned __int128 sa = static_cast<unsigned __int128>(n - 1) * lda + n;
+  const unsigned __int128 sb = static_cast<unsigned __int128>(m - 1) * ldb + n;
+  const unsigned __int128 sx = static_cast<unsigned __int128>(m - 1) * ldx + n;
+  const unsigned __int128 lim = static_cast<unsigned __int128>(1) << 61;
+  if (sa >= lim || sb >= lim || sx >= lim) return HGEMM_ERR_INVALID_ARG;
+  const bool in_place = static_cast<const void*>(X) == static_cast<const void*>(B) && ldx == ldb;
+  if (ranges_overlap(X, 2 * static_cast<uint64_t>(sx), A, 2 * static_cast<uint64_t>(sa)) ||
+      (!in_place && ranges_overlap(X, 2 * static_cast<uint64_t>(sx), B, 2 * static_cast<uint64_t>(sb))))
+    return HGEMM_ERR_ALIAS;
+  DeviceState* dev = nullptr;
+  int rc;
+  if ((rc = current_device(&dev)) != HGEMM_OK) return rc;
+
+  uint16_t* x = reinterpret_cast<uint16_t*>(X);
+  const uint16_t* a = reinterpret_cast<const uint16_t*>(A);
+  cudaError_t e;
+  if (!in_place || alpha != 1.0f) {
+    e = hg::launch_scale_copy(reinterpret_cast<const uint16_t*>(B), ldb, x, ldx, n, m, alpha,
+                              dev->num_sms, stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  // The update of block [off, off + s) split at s1, in the GEMM view:
+  //   X1ᵀ (m × s1, pitch ldx) -= X2ᵀ (m × s2, pitch ldx) · A21 (s2 × s1),
+  // where column i of A21 is A[off+s1 : off+s, off+i] (pitch lda). The
+  // product reads columns [off+s1, off+s) of X and writes [off, off+s1):
+  // the element sets are disjoint, so the span check of validate(), which
+  // sees the interleaved columns as an overlap, is not applied.
+  const hg::EpiArgs subtract{-1.0f, 1.0f, nullptr, 0, 2};
+  // The page's recursion, second half first: every row of a block depends on
+  // the rows below it.
+  std::function<int(int64_t, int64_t)> solve = [&](int64_t off, int64_t s) -> int {
+    if (s <= hg::kTrsmLeaf) {
+      const cudaError_t le = hg::launch_trsm_leaf(a, lda, x, ldx, off, static_cast<int>(s), m,
+                                                  dev->num_sms, stream);
+      return le == cudaSuccess ? HGEMM_OK : cuda_fail(le);
+    }
+    const int64_t s1 = ((s / 2 + 63) / 64) * 64, s2 = s - s1;
+    int r = solve(off + s1, s2);
+    if (r != HGEMM_OK) return r;
+    const Gemm g{x + off + s1, a + off * lda + off + s1, x + off, m, s1, s2, ldx, lda, ldx};
+    if ((r = dispatch(g, subtract, *dev, stream)) != HGEMM_OK) return r;
+    return solve(off, s1);
+  };
+  return solve(0, n);
 }
 
 int hgemm_host(const hgemm_half_t* hA, const hgemm_half_t* hB, hgemm_half_t* hC, int64_t M,

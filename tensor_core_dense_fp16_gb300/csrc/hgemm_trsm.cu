@@ -1,0 +1,331 @@
+// hgemm_trsm.cu — the pieces of the triangular solve of
+// "异构计算中高性能TRMM与TRSM的递归算法实现" (§2.3) that are not products: the
+// scaled copy of the right-hand side, and the solve of one diagonal block
+// (order ≤ 256) for all right-hand sides. The recursion and its GEMM updates
+// are in hgemm_api.cu.
+//
+// The system solved, in the variant of the page's §2.2 product (left side,
+// lower triangle, transposed): Aᵀ·X = alpha·B, every matrix column-major
+// (A(r,c) at A[c·lda + r], X(r,j) at X[j·ldx + r]). Row i of the system is
+//   Σ_{k ≥ i} A(k,i)·x_k = b_i,
+// so the block is solved by back substitution, last row first.
+//
+// Leaf solve (§2.3: the right-hand sides spread over thread blocks, a light
+// barrier between steps): thread r of a block owns row r of the diagonal
+// block for COLS right-hand sides, in registers. The rows are taken in groups
+// of 32 (one warp's rows), last group first. A group's own 32×32 triangle
+// L_g is applied through its inverse, which warp g computes in FP32 at the
+// start (forward substitution on the columns of the identity), so that the
+// group's solution x_g = (L_g⁻¹)ᵀ·b_g is a small product spread over all
+// threads, not a chain of 32 dependent steps in one warp. Per group: the
+// owning warp publishes its b, barrier, all threads form x_g, barrier, and
+// every thread r above the group's first row subtracts Σ_c A(c,r)·x_c over
+// the group's rows, reading A(c0 .. c0+31, r) (contiguous in the
+// column-major A) straight from global memory, issued before the group's
+// barriers. Arithmetic is FP32 and the results are rounded once to FP16.
+#include <cuda_fp16.h>
+
+#include "internal.h"
+
+namespace hg {
+namespace {
+
+constexpr int kLeafMax = kTrsmLeaf;                     // largest diagonal block
+constexpr int kMaxDevices = 64;
+constexpr int kGroup = 32;                  // rows per barrier step: one warp's rows
+constexpr int kGroups = kLeafMax / kGroup;  // diagonal 32×32 triangles of a block
+
+// Row pitch (floats) of the published b and x rows: the padding puts
+// consecutive lanes' 16-byte accesses in different banks.
+template <int COLS>
+__host__ __device__ constexpr int pub_pitch() {
+  return COLS + 4;
+}
+
+template <int COLS>
+constexpr int leaf_smem() {
+  return kGroups * kGroup * kGroup * 4 + 2 * kGroup * pub_pitch<COLS>() * 4;
+}
+
+// A(row0 + q, col) for q < 32 (q < valid; 0 past it), packed as 32 halves.
+__device__ __forceinline__ void load_col32(const uint16_t* __restrict__ A, int64_t lda, int64_t col,
+                                           int64_t row0, int valid, bool vec, uint4 (&out)[4]) {
+  const uint16_t* src = A + col * lda + row0;
+  if (vec && valid == kGroup) {
+#pragma unroll
+    for (int p = 0; p < 4; ++p) out[p] = __ldg(reinterpret_cast<const uint4*>(src) + p);
+  } else {
+    uint32_t w[16];
+#pragma unroll
+    for (int p = 0; p < 16; ++p) {
+      const uint32_t lo = 2 * p < valid ? src[2 * p] : 0u;
+      const uint32_t hi = 2 * p + 1 < valid ? src[2 * p + 1] : 0u;
+      w[p] = lo | (hi << 16);
+    }
+#pragma unroll
+    for (int p = 0; p < 4; ++p) out[p] = make_uint4(w[4 * p], w[4 * p + 1], w[4 * p + 2], w[4 * p + 3]);
+  }
+}
+
+// Half q of a packed column segment, as FP32.
+__device__ __forceinline__ float col32_at(const uint4 (&v)[4], int q) {
+  const uint4 c = v[q / 8];
+  const uint32_t w = (q % 8) < 2 ? c.x : (q % 8) < 4 ? c.y : (q % 8) < 6 ? c.z : c.w;
+  return __half2float(__ushort_as_half(static_cast<uint16_t>(w >> (16 * (q & 1)))));
+}
+
+template <int COLS>
+__global__ void __launch_bounds__(kLeafMax, 2)
+    trsm_leaf_kernel(const uint16_t* __restrict__ A, int64_t lda, uint16_t* __restrict__ X,
+                     int64_t ldx, int64_t off, int s, int64_t m) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  // diag[g][k][j]: first L_g(k, j) in FP32 (L_g the diagonal triangle of
+  // rows 32g .. 32g+31), then, in place, (L_g⁻¹)(k, j)
+  float* diag = reinterpret_cast<float*>(smem);
+  constexpr int P = pub_pitch<COLS>();
+  float* pub_b = diag + kGroups * kGroup * kGroup;  // [kGroup][P]: b of the group's rows
+  float* pub_x = pub_b + kGroup * P;                // [kGroup][P]: x of the group's rows
+  const int r = threadIdx.x;
+  const int lane = r & 31, warp = r >> 5;
+  const int64_t j0 = static_cast<int64_t>(blockIdx.x) * COLS;
+  const int groups = (s + kGroup - 1) / kGroup;  // = the block's warps
+  // 16-byte loads of A's column segments: column starts 16-byte aligned
+  const bool vec = ((reinterpret_cast<uintptr_t>(A) & 15u) == 0) && (lda % 8) == 0 && (off % 8) == 0;
+
+  // Warp g: the inverse of its diagonal triangle L_g. Lane i loads column i
+  // of L_g, stores it transposed (rows of L_g contiguous, FP32), then
+  // computes column i of L_g⁻¹ by forward substitution on e_i, reading rows
+  // of L_g 16 bytes at a time (lane k supplies 1/L_g(k,k) by shuffle, off the
+  // dependent chain), and overwrites L_g with it. Entries above the diagonal
+  // are loaded but never read; rows and columns past the block's order are 0.
+  {
+    const int g = warp, c0 = g * kGroup, sg = min(kGroup, s - c0);
+    float* blk = diag + g * kGroup * kGroup;
+    if (lane < sg) {
+      uint4 col[4];
+      load_col32(A, lda, off + c0 + lane, off + c0, sg, vec, col);
+#pragma unroll
+      for (int k = 0; k < kGroup; ++k) blk[k * kGroup + lane] = col32_at(col, k);
+    }
+    __syncwarp();
+    const float rd_own = lane < sg ? 1.0f / blk[lane * kGroup + lane] : 0.f;
+    float mcol[kGroup];
+#pragma unroll
+    for (int k = 0; k < kGroup; ++k) {
+      const float4* rowv = reinterpret_cast<const float4*>(blk + k * kGroup);
+      const float rd = __shfl_sync(0xffffffffu, rd_own, k);
+      float acc = (k == lane) ? 1.0f : 0.0f;
+#pragma unroll
+      for (int j4 = 0; j4 < (k + 3) / 4; ++j4) {
+        const float4 l = rowv[j4];
+        if (4 * j4 + 0 < k) acc = fmaf(-l.x, mcol[4 * j4 + 0], acc);
+        if (4 * j4 + 1 < k) acc = fmaf(-l.y, mcol[4 * j4 + 1], acc);
+        if (4 * j4 + 2 < k) acc = fmaf(-l.z, mcol[4 * j4 + 2], acc);
+        if (4 * j4 + 3 < k) acc = fmaf(-l.w, mcol[4 * j4 + 3], acc);
+      }
+      mcol[k] = (k < sg && k >= lane) ? acc * rd : 0.f;
+    }
+    __syncwarp();
+#pragma unroll
+    for (int k = 0; k < kGroup; ++k) blk[k * kGroup + lane] = lane < sg ? mcol[k] : 0.f;
+  }
+
+  // This block's right-hand sides (one coalesced column of the block per jj),
+  // loaded after the inversion (kept out of its registers).
+  asm volatile("" ::: "memory");
+  float b[COLS];
+#pragma unroll
+  for (int jj = 0; jj < COLS; ++jj) {
+    const int64_t j = j0 + jj;
+    b[jj] = (r < s && j < m) ? __half2float(__ushort_as_half(X[j * ldx + off + r])) : 0.f;
+  }
+
+  for (int g = groups - 1; g >= 0; --g) {
+    const int c0 = g * kGroup, sg = min(kGroup, s - c0);
+    // A(c0 .. c0+31, r) for the update below, loaded now to land while the
+    // group is solved.
+    uint4 acol[4] = {};
+    if (r < c0) load_col32(A, lda, off + r, off + c0, sg, vec, acol);
+    // (1) the owning warp's rows, complete with every later group's update
+    if (warp == g) {
+      float4* dst = reinterpret_cast<float4*>(pub_b + lane * P);
+#pragma unroll
+      for (int q = 0; q < COLS / 4; ++q) dst[q] = make_float4(b[4 * q], b[4 * q + 1], b[4 * q + 2], b[4 * q + 3]);
+    }
+    // This barrier also orders the group's writes of pub_b and pub_x after
+    // every read of them for the previous group, and (first time round) the
+    // inverses before their use by other warps.
+    __syncthreads();
+    // (2) x_g(i, jj) = Σ_k L_g⁻¹(k, i)·b_g(k, jj): lane i, four right-hand
+    // sides per thread (jj = 4q .. 4q+3 for q = warp, warp + groups, ...).
+    {
+      const float* mi = diag + g * kGroup * kGroup + lane;
+      for (int q = warp; q < COLS / 4; q += groups) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int k = 0; k < kGroup; ++k) {
+          const float mk = mi[k * kGroup];
+          const float4 bk = *reinterpret_cast<const float4*>(pub_b + k * P + 4 * q);
+          acc.x = fmaf(mk, bk.x, acc.x);
+          acc.y = fmaf(mk, bk.y, acc.y);
+          acc.z = fmaf(mk, bk.z, acc.z);
+          acc.w = fmaf(mk, bk.w, acc.w);
+        }
+        *reinterpret_cast<float4*>(pub_x + lane * P + 4 * q) = acc;
+      }
+    }
+    __syncthreads();
+    if (warp == g) {
+      const float4* src = reinterpret_cast<const float4*>(pub_x + lane * P);
+#pragma unroll
+      for (int q = 0; q < COLS / 4; ++q) {
+        const float4 x = src[q];
+        b[4 * q] = x.x;
+        b[4 * q + 1] = x.y;
+        b[4 * q + 2] = x.z;
+        b[4 * q + 3] = x.w;
+      }
+    } else if (r < c0) {
+      // (3) rows above the group: b -= Σ_c A(c, r)·x_c over the group's rows
+      // (A(c, r) = 0 past the block's order)
+#pragma unroll
+      for (int q = 0; q < kGroup; ++q) {
+        const float a = -col32_at(acol, q);
+        const float4* xc = reinterpret_cast<const float4*>(pub_x + q * P);
+#pragma unroll
+        for (int p = 0; p < COLS / 4; ++p) {
+          const float4 x = xc[p];
+          b[4 * p] = fmaf(a, x.x, b[4 * p]);
+          b[4 * p + 1] = fmaf(a, x.y, b[4 * p + 1]);
+          b[4 * p + 2] = fmaf(a, x.z, b[4 * p + 2]);
+          b[4 * p + 3] = fmaf(a, x.w, b[4 * p + 3]);
+        }
+      }
+    }
+  }
+
+#pragma unroll
+  for (int jj = 0; jj < COLS; ++jj) {
+    const int64_t j = j0 + jj;
+    if (r < s && j < m) X[j * ldx + off + r] = __half_as_ushort(__float2half_rn(b[jj]));
+  }
+}
+
+// X(:, j) = alpha · B(:, j) for the n × m column-major operands; FP16 in and
+// out, FP32 product. In place when X == B (every element is read and written
+// by the same thread). VEC: n, ldb, ldx multiples of 8 and both bases 16-byte
+// aligned, 8 elements per 16-byte access.
+template <bool VEC>
+__global__ void scale_copy_kernel(const uint16_t* B, int64_t ldb, uint16_t* X, int64_t ldx,
+                                  int64_t n, int64_t m, float alpha) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (VEC) {
+    const int64_t per_col = n / 8, count = per_col * m;
+    for (int64_t t = t0; t < count; t += stride) {
+      const int64_t j = t / per_col, i = (t - j * per_col) * 8;
+      uint4 v = *reinterpret_cast<const uint4*>(B + j * ldb + i);
+      uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[q]));
+        const __half2 h = __floats2half2_rn(alpha * f.x, alpha * f.y);
+        w[q] = *reinterpret_cast<const uint32_t*>(&h);
+      }
+      *reinterpret_cast<uint4*>(X + j * ldx + i) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  } else {
+    const int64_t count = n * m;
+    for (int64_t t = t0; t < count; t += stride) {
+      const int64_t j = t / n, i = t - j * n;
+      const float v = __half2float(__ushort_as_half(B[j * ldb + i]));
+      X[j * ldx + i] = __half_as_ushort(__float2half_rn(alpha * v));
+    }
+  }
+}
+
+// Resident blocks per SM of each width, measured once per device (0: not yet).
+int g_resident[kMaxDevices][3] = {};
+
+template <int COLS>
+cudaError_t launch_width(const uint16_t* A, int64_t lda, uint16_t* X, int64_t ldx, int64_t off,
+                         int s, int64_t m, int threads, cudaStream_t stream) {
+  const int64_t blocks = (m + COLS - 1) / COLS;
+  if (blocks > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
+  trsm_leaf_kernel<COLS><<<static_cast<unsigned>(blocks), threads, leaf_smem<COLS>(), stream>>>(
+      A, lda, X, ldx, off, s, m);
+  return cudaGetLastError();
+}
+
+template <int COLS>
+cudaError_t resident_blocks(int* out) {
+  cudaError_t e = cudaFuncSetAttribute(trsm_leaf_kernel<COLS>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, leaf_smem<COLS>());
+  if (e != cudaSuccess) return e;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, trsm_leaf_kernel<COLS>, kLeafMax,
+                                                       leaf_smem<COLS>());
+}
+
+}  // namespace
+
+cudaError_t launch_trsm_leaf(const uint16_t* A, int64_t lda, uint16_t* X, int64_t ldx, int64_t off,
+                             int s, int64_t m, int num_sms, cudaStream_t stream) {
+  if (s < 1 || s > kLeafMax || m < 1 || num_sms < 1) return cudaErrorInvalidValue;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  int* res = g_resident[dev];
+  if (res[0] == 0) {
+    int r8 = 0, r16 = 0, r32 = 0;
+    if ((e = resident_blocks<8>(&r8)) != cudaSuccess || (e = resident_blocks<16>(&r16)) != cudaSuccess ||
+        (e = resident_blocks<32>(&r32)) != cudaSuccess)
+      return e;
+    if (r8 < 1 || r16 < 1 || r32 < 1) return cudaErrorInvalidConfiguration;
+    res[1] = r16;
+    res[2] = r32;
+    res[0] = r8;
+  }
+  // Width by estimated time: waves of blocks times the time of one block,
+  // which is mostly the s barriers (≈ the same for every width) plus the
+  // FMAs of its COLS right-hand sides.
+  const int widths[3] = {8, 16, 32};
+  int best = 0;
+  double best_cost = 0.0;
+  for (int w = 0; w < 3; ++w) {
+    const int64_t blocks = (m + widths[w] - 1) / widths[w];
+    const int64_t slots = static_cast<int64_t>(res[w]) * num_sms;
+    const double cost = static_cast<double>((blocks + slots - 1) / slots) * (1.0 + widths[w] / 32.0);
+    if (w == 0 || cost < best_cost) {
+      best = w;
+      best_cost = cost;
+    }
+  }
+  const int threads = ((s + 31) / 32) * 32;
+  switch (best) {
+    case 0:
+      return launch_width<8>(A, lda, X, ldx, off, s, m, threads, stream);
+    case 1:
+      return launch_width<16>(A, lda, X, ldx, off, s, m, threads, stream);
+    default:
+      return launch_width<32>(A, lda, X, ldx, off, s, m, threads, stream);
+  }
+}
+
+cudaError_t launch_scale_copy(const uint16_t* B, int64_t ldb, uint16_t* X, int64_t ldx, int64_t n,
+                              int64_t m, float alpha, int num_sms, cudaStream_t stream) {
+  const bool vec = n % 8 == 0 && ldb % 8 == 0 && ldx % 8 == 0 &&
+                   ((reinterpret_cast<uintptr_t>(B) | reinterpret_cast<uintptr_t>(X)) & 15u) == 0;
+  const int64_t count = vec ? n / 8 * m : n * m;
+  int64_t blocks = (count + 255) / 256;
+  const int64_t cap = static_cast<int64_t>(num_sms > 0 ? num_sms : 1) * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  if (vec)
+    scale_copy_kernel<true><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(B, ldb, X, ldx, n, m, alpha);
+  else
+    scale_copy_kernel<false><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(B, ldb, X, ldx, n, m, alpha);
+  return cudaGetLastError();
+}
+
+}  // namespace hg

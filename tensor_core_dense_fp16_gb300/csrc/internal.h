@@ -99,6 +99,16 @@ cudaError_t launch_generic(const PlainArgs& args, int num_sms, cudaStream_t stre
 // M × size (see hgemm_generic.cu).
 cudaError_t launch_tri_leaves(const PlainArgs& args, const TriLeaves& leaves, cudaStream_t stream);
 
+// Triangular solve Aᵀ·X = alpha·B (see hgemm_trsm.cu): the largest diagonal
+// block solved by substitution; X(:, j) = alpha·B(:, j) over n × m
+// column-major operands (X == B allowed); the solve of the diagonal block of
+// order s at (off, off) for all m right-hand sides, in place in X.
+constexpr int kTrsmLeaf = 256;
+cudaError_t launch_scale_copy(const uint16_t* B, int64_t ldb, uint16_t* X, int64_t ldx, int64_t n,
+                              int64_t m, float alpha, int num_sms, cudaStream_t stream);
+cudaError_t launch_trsm_leaf(const uint16_t* A, int64_t lda, uint16_t* X, int64_t ldx, int64_t off,
+                             int s, int64_t m, int num_sms, cudaStream_t stream);
+
 // Address of the device watchdog word on the current device.
 cudaError_t status_word_address(int** addr);
 

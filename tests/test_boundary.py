@@ -187,6 +187,28 @@ def test_trmm_argument_checks(lib):
     assert call(n=0) == tc.HGEMM_OK and call(m=0) == tc.HGEMM_OK
 
 
+def test_trsm_argument_checks(lib):
+    lib_ = tc.load()
+    n, m = 64, 8
+    ok = dict(A=A16, lda=n, B=B16, ldb=n, X=C16, ldx=n)
+    def call(**kw):
+        a = {**ok, **kw}
+        return lib_.hgemm_trsm(a["A"], a["lda"], a["B"], a["ldb"], a["X"], a["ldx"], kw.get("n", n),
+                               kw.get("m", m), 1.0, None)
+    assert call(n=-1) == tc.HGEMM_ERR_INVALID_ARG
+    assert call(m=-1) == tc.HGEMM_ERR_INVALID_ARG
+    assert call(n=tc.HGEMM_MAX_DIM + 1) == tc.HGEMM_ERR_INVALID_ARG
+    assert call(lda=n - 1) == tc.HGEMM_ERR_INVALID_ARG
+    assert call(ldb=n - 1) == tc.HGEMM_ERR_INVALID_ARG
+    assert call(ldx=n - 8) == tc.HGEMM_ERR_INVALID_ARG
+    assert call(A=None) == tc.HGEMM_ERR_INVALID_ARG
+    assert call(X=C16 + 1) == tc.HGEMM_ERR_INVALID_ARG
+    assert call(X=A16 + 2 * 10) == tc.HGEMM_ERR_ALIAS     # X inside A's span
+    assert call(X=B16 + 2 * 8) == tc.HGEMM_ERR_ALIAS      # X overlaps B, not in place
+    assert call(X=B16, ldx=n + 8) == tc.HGEMM_ERR_ALIAS   # X = B with another pitch
+    assert call(n=0) == tc.HGEMM_OK and call(m=0) == tc.HGEMM_OK
+
+
 def test_invalid_arguments_rejected_before_any_device_work(lib):
     bad = [
         (A16, B16, C16, -1, 4, 4),

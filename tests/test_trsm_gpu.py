@@ -1,0 +1,137 @@
+"""The triangular solve of "异构计算中高性能TRMM与TRSM的递归算法实现" (§2.3), in
+the variant of its §2.2 product: Aᵀ·X = alpha·B with A lower triangular,
+through hgemm_trsm, against the oracle (GPU only).
+
+Inputs: a diagonally dominant triangle (diagonal in [1, 2), strict lower part
+in [0, 1/n)) and B uniform on [0, 1), all FP16. Tolerance: the per-element
+bound of the product, 1e-2·max(1, |x|). The recursion rounds X to FP16 after
+the scaling, after each of its ≤ log2(n/256) + 1 updates and after the
+diagonal solve (each a relative error ≤ 2^-11), and an error in X2 reaches X1
+through A21ᵀ, whose column sums are < 1, divided by a diagonal ≥ 1, so it is
+not amplified: at n = 8192 the worst case is below 8·2^-11·max|x| ≈ 4e-3,
+inside the bound."""
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+import tensor_core_dense_fp16_gb300 as tc
+from gpu_helpers import assert_close, oracle_threads, to_device, torch_cuda
+
+pytestmark = pytest.mark.gpu
+
+
+def trsm_inputs(n, m, seed):
+    """(a, b) in mathematical orientation: a (n, n) whose lower triangle is A."""
+    a_col, b_col = synth.trsm_operands(n, m, seed)
+    return np.ascontiguousarray(a_col.T), np.ascontiguousarray(b_col.T)
+
+
+def run_trsm(a, b, alpha=1.0, pad=(0, 0, 0), poison_upper=False, in_place=False):
+    """Column-major device buffers with pitches n + pad; X (n, m) comes back."""
+    torch = torch_cuda()
+    n, m = b.shape
+    lda, ldb, ldx = n + pad[0], n + pad[1], n + pad[2]
+    if in_place:
+        ldx = ldb
+    a_col = np.zeros((n, lda), np.float16)     # row c holds column c of A
+    a_col[:, :n] = a.T
+    if poison_upper:
+        r, c = np.triu_indices(n, 1)            # A(r, c) with c > r: above the diagonal
+        a_col[c, r] = np.nan
+    b_col = np.full((m, ldb), 7.0, np.float16)
+    b_col[:, :n] = b.T
+    da, db = to_device(a_col), to_device(b_col)
+    if in_place:
+        dx = db
+    else:
+        dx = to_device(np.full((m, ldx), 5.0, np.float16))
+    tc.hgemm_trsm(da, lda, db, ldb, dx, ldx, n, m, alpha)
+    assert tc.hgemm_device_status() == tc.HGEMM_OK
+    torch.cuda.synchronize()
+    out = dx.cpu().numpy()
+    fill = 7.0 if in_place else 5.0
+    assert np.all(out[:, n:] == fill), "pitch padding of X was written"
+    if not in_place:
+        assert np.array_equal(db.cpu().numpy()[:, :n], b.T), "B was modified"
+    return np.ascontiguousarray(out[:, :n].T)
+
+
+@pytest.mark.parametrize("n,m", [(1, 1), (64, 32), (200, 7), (256, 100), (257, 64), (300, 136),
+                                 (512, 256), (1000, 128), (4096, 256)])
+def test_trsm_matches_oracle(n, m):
+    a, b = trsm_inputs(n, m, seed=n + m)
+    ref = oracle.trsm(a, b, nthreads=oracle_threads())
+    assert_close(run_trsm(a, b), ref, what=f"trsm {n}x{m}")
+
+
+@pytest.mark.parametrize("m", [4096, 8192, 8195])
+def test_trsm_leaf_widths(m):
+    """Many right-hand sides: the diagonal solves take 16 and 32 of them per
+    thread block (and a ragged last block)."""
+    n = 300
+    a, b = trsm_inputs(n, m, seed=m)
+    ref = oracle.trsm(a, b, nthreads=oracle_threads())
+    assert_close(run_trsm(a, b), ref, what=f"trsm {n}x{m}")
+
+
+def test_trsm_reads_only_the_lower_triangle():
+    n, m = 700, 96
+    a, b = trsm_inputs(n, m, seed=7)
+    ref = oracle.trsm(a, b, nthreads=oracle_threads())
+    assert_close(run_trsm(a, b, poison_upper=True), ref, what="NaN above the diagonal")
+
+
+@pytest.mark.parametrize("pad", [(8, 16, 8), (3, 5, 1)])
+def test_trsm_pitches_and_alpha(pad):
+    """Wider pitches (multiples of 8: tensor-core updates; odd ones: the
+    generic loader) and a scale factor."""
+    n, m = 600, 72
+    a, b = trsm_inputs(n, m, seed=11 + pad[0])
+    ref = oracle.trsm(a, b, alpha=-1.5, nthreads=oracle_threads())
+    assert_close(run_trsm(a, b, alpha=-1.5, pad=pad), ref, what=f"trsm pad {pad}")
+
+
+@pytest.mark.parametrize("alpha", [1.0, 0.25])
+def test_trsm_in_place(alpha):
+    n, m = 800, 40
+    a, b = trsm_inputs(n, m, seed=19)
+    ref = oracle.trsm(a, b, alpha=alpha, nthreads=oracle_threads())
+    assert_close(run_trsm(a, b, alpha=alpha, pad=(0, 8, 0), in_place=True), ref,
+                 what=f"trsm in place alpha {alpha}")
+
+
+def test_trsm_residual_identity():
+    """A = I: X = alpha·B rounded once, exactly."""
+    n, m = 520, 33
+    _, b = trsm_inputs(n, m, seed=23)
+    a = np.eye(n, dtype=np.float16)
+    got = run_trsm(a, b, alpha=0.5)
+    assert np.array_equal(got, (b.astype(np.float32) * 0.5).astype(np.float16))
+
+
+def test_trsm_repeatable():
+    n, m = 1024, 64
+    a, b = trsm_inputs(n, m, seed=3)
+    first = run_trsm(a, b)
+    for _ in range(3):
+        assert np.array_equal(run_trsm(a, b).view(np.uint16), first.view(np.uint16))
+
+
+def test_trsm_8192_sampled_columns():
+    """The 8192×8192 workload in the benchmark's launch configuration: column
+    j of X depends on column j of B alone, so the oracle solves a sample of
+    the columns (first, last and spread ones)."""
+    torch = torch_cuda()
+    a_col, b_col, spec = synth.workload("trsm_8192")
+    n, m = spec["n"], spec["m"]
+    da, db = to_device(a_col), to_device(b_col)
+    dx = torch.empty((m, n), dtype=torch.float16, device="cuda")
+    tc.hgemm_trsm(da, n, db, n, dx, n, n, m, 1.0)
+    assert tc.hgemm_device_status() == tc.HGEMM_OK
+    torch.cuda.synchronize()
+    cols = np.array([0, 1, 63, 64, 255, 1000, 4097, 8000, m - 1])
+    got = dx[torch.from_numpy(cols).cuda()].cpu().numpy().T
+    ref = oracle.trsm(a_col.T, b_col[cols].T, nthreads=oracle_threads())
+    assert_close(got, ref, what="trsm_8192 sampled columns")
