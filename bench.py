@@ -134,6 +134,10 @@ def parse_args():
                     help="target CPU time of the oracle sample")
     ap.add_argument("--reference-seconds", type=float, default=120.0,
                     help="target wall time of a whole --impl reference run")
+    ap.add_argument("--a-layout", choices=["row", "col"], default="row",
+                    help="A stored M x K row-major (the default) or K x M (column-major)")
+    ap.add_argument("--b-layout", choices=["col", "row"], default="col",
+                    help="B stored N x K (column-major, the default) or K x N row-major")
     ap.add_argument("--epilogue", choices=sorted(EPILOGUES), default="none",
                     help="fused epilogue through hgemm_ex (default: the plain product)")
     return ap.parse_args()
@@ -581,24 +585,41 @@ def run_ours(args, spec, a, b, world, rank, local):
     flops = flops_of(spec)
     stream = torch.cuda.current_stream(dev)
 
-    da = torch.from_numpy(a).to(dev)
-    db = torch.from_numpy(b).to(dev)
+    a_col, b_row = args.a_layout == "col", args.b_layout == "row"
+    layouts = a_col or b_row
+    # the same values stored in the requested order (A K x M, B K x N)
+    da = torch.from_numpy(np.ascontiguousarray(a.T) if a_col else a).to(dev)
+    db = torch.from_numpy(np.ascontiguousarray(b.T) if b_row else b).to(dev)
+    lda, ldb = (M if a_col else K), (N if b_row else K)
     dc = torch.empty((M, N), dtype=torch.float16, device=dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(2 * l2 // 4 + 1, dtype=torch.float32, device=dev)
-    path = tc.hgemm_select_path(da, db, dc, M, N, K)
     epi = EPILOGUES[args.epilogue]
+    if layouts:
+        # M- or N-contiguous operands go to the pair kernel when TMA can read them
+        tma = lda % 8 == 0 and ldb % 8 == 0 and N % 8 == 0
+        path = tc.HGEMM_PATH_TC_PAIR if tma else tc.HGEMM_PATH_GENERIC
+    else:
+        path = tc.hgemm_select_path(da, db, dc, M, N, K)
     if epi is not None and path == tc.HGEMM_PATH_TC_WIDE:
         path = tc.HGEMM_PATH_TC_PAIR   # a fused epilogue takes 256x256 tiles there (hgemm.h)
-    if epi is None:
-        def step():
-            tc.hgemm(da, db, dc, M, N, K, stream)
-    else:
-        alpha, beta, with_bias, relu = epi
+    alpha, beta, with_bias, relu = epi if epi is not None else (1.0, 0.0, False, False)
+    dbias = None
+    if epi is not None:
         gen = torch.Generator(device="cpu").manual_seed(spec["seed"] + 7)
         dbias = (torch.rand(N, generator=gen) - 0.5).half().to(dev) if with_bias else None
         dc.copy_((torch.rand((M, N), generator=gen) - 0.5).half())
+    if layouts:
+        a_l = tc.HGEMM_A_COL_MAJOR if a_col else tc.HGEMM_A_ROW_MAJOR
+        b_l = tc.HGEMM_B_ROW_MAJOR if b_row else tc.HGEMM_B_COL_MAJOR
 
+        def step():
+            tc.hgemm_layout(a_l, b_l, da, lda, db, ldb, dc, N, M, N, K, alpha, beta, dbias, relu,
+                            stream)
+    elif epi is None:
+        def step():
+            tc.hgemm(da, db, dc, M, N, K, stream)
+    else:
         def step():
             tc.hgemm_ex(da, db, dc, M, N, K, alpha, beta, dbias, relu, stream)
 
@@ -638,7 +659,7 @@ def run_ours(args, spec, a, b, world, rank, local):
 
     # ---- end to end through the host-buffer entry point (the plain product)
     e2e = None
-    if not args.no_e2e and epi is None:
+    if not args.no_e2e and epi is None and not layouts:
         ha = torch.from_numpy(a).pin_memory()
         hb = torch.from_numpy(b).pin_memory()
         hc = torch.empty((M, N), dtype=torch.float16).pin_memory()
@@ -671,7 +692,8 @@ def run_ours(args, spec, a, b, world, rank, local):
     ai = flops / nbytes
     ridge = peaks["bf16_tflops"] * FP16_PER_BF16 * 1e12 / (peaks["hbm_gbs"] * 1e9)
     sha = kernel_sources_sha(kernel)
-    traffic = profiled_traffic(kernel, args.workload, sha)
+    traffic = profiled_traffic(kernel, args.workload if not layouts else
+                               f"{args.workload}+a_{args.a_layout}/b_{args.b_layout}", sha)
     if ai >= ridge:
         peak = peaks["bf16_tflops"] * FP16_PER_BF16
         achieved = flops / (mean_ms * 1e-3) / 1e12
@@ -710,7 +732,8 @@ def run_ours(args, spec, a, b, world, rank, local):
                        "l2": "flushed before every timed launch (write of 2x L2 size, "
                              "outside the events)",
                        "inputs": "resident in HBM", "path": kernel,
-                       "epilogue": args.epilogue,
+                       "epilogue": args.epilogue, "a_layout": args.a_layout,
+                       "b_layout": args.b_layout,
                        "parallelism": f"replicas x{world}"},
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": args.steps, "clocks": clocks,

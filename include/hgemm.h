@@ -139,6 +139,32 @@ HGEMM_API int hgemm_strided(const hgemm_half_t *A, int64_t lda, const hgemm_half
                   cudaStream_t stream);
 
 /*
+ * hgemm_layout — hgemm_strided with a storage order chosen per operand, the
+ * other layouts of the product (the CUDA chapter of "GPU架构与CUDA",
+ * 共享内存与分块, stores B row-major, K×N with N contiguous):
+ *
+ *   a_layout  HGEMM_A_ROW_MAJOR: A(i,k) at A[i·lda + k], lda ≥ K (as hgemm);
+ *             HGEMM_A_COL_MAJOR: A(i,k) at A[k·lda + i], lda ≥ M;
+ *   b_layout  HGEMM_B_COL_MAJOR: B(k,j) at B[j·ldb + k], ldb ≥ K (as hgemm);
+ *             HGEMM_B_ROW_MAJOR: B(k,j) at B[k·ldb + j], ldb ≥ N;
+ *
+ * C(i,j) at C[i·ldc + j] always. Same epilogue (alpha, beta, bias, relu),
+ * ownership, alias and error rules as hgemm_ex; an unknown layout value is
+ * HGEMM_ERR_INVALID_ARG. Operands that TMA can describe (16-byte aligned
+ * bases and pitches, N a multiple of 8) go to the tensor-core pair kernel,
+ * which reads an M- or N-contiguous operand as MN-major tiles; the others to
+ * the generic kernel, which gathers them.
+ */
+#define HGEMM_A_ROW_MAJOR 0
+#define HGEMM_A_COL_MAJOR 1
+#define HGEMM_B_COL_MAJOR 0
+#define HGEMM_B_ROW_MAJOR 1
+HGEMM_API int hgemm_layout(int a_layout, int b_layout, const hgemm_half_t *A, int64_t lda,
+                 const hgemm_half_t *B, int64_t ldb, hgemm_half_t *C, int64_t ldc, int64_t M,
+                 int64_t N, int64_t K, float alpha, float beta, const hgemm_half_t *bias,
+                 int relu, cudaStream_t stream);
+
+/*
  * hgemm_trmm — the triangular product of "异构计算中高性能TRMM与TRSM的递归算法实现"
  * §2.2 (left side, lower triangle, transposed: B ← alpha·Aᵀ·B), out of place:
  *

@@ -28,7 +28,8 @@ __all__ = [
     "HgemmError", "library_path", "load", "hgemm", "hgemm_host", "hgemm_select_path",
     "hgemm_force_path", "hgemm_device_status", "hgemm_last_cuda_error",
     "hgemm_status_string", "hgemm_version", "hgemm_set_wait_timeout", "hgemm_debug_inject",
-    "hgemm_force_split", "hgemm_ex", "hgemm_strided", "hgemm_trmm", "hgemm_trsm", "HGEMM_TRMM_MAX_N",
+    "hgemm_force_split", "hgemm_ex", "hgemm_strided", "hgemm_trmm", "hgemm_trsm", "hgemm_layout", "HGEMM_TRMM_MAX_N",
+    "HGEMM_A_ROW_MAJOR", "HGEMM_A_COL_MAJOR", "HGEMM_B_COL_MAJOR", "HGEMM_B_ROW_MAJOR",
     "HGEMM_INJECT_NONE", "HGEMM_INJECT_DROP_ARRIVAL", "matmul",
 ]
 
@@ -39,6 +40,10 @@ HGEMM_ERR_UNSUPPORTED_DEVICE = -3
 HGEMM_ERR_CUDA = -4
 HGEMM_ERR_TIMEOUT = -5
 HGEMM_TRMM_MAX_N = 16384
+HGEMM_A_ROW_MAJOR = 0
+HGEMM_A_COL_MAJOR = 1
+HGEMM_B_COL_MAJOR = 0
+HGEMM_B_ROW_MAJOR = 1
 
 HGEMM_PATH_NONE = 0
 HGEMM_PATH_ZERO = 1
@@ -96,6 +101,9 @@ def load():
     lib.hgemm_trmm.restype = i32
     lib.hgemm_trsm.argtypes = [vp, i64, vp, i64, vp, i64, i64, i64, ctypes.c_float, vp]
     lib.hgemm_trsm.restype = i32
+    lib.hgemm_layout.argtypes = [i32, i32, vp, i64, vp, i64, vp, i64, i64, i64, i64, ctypes.c_float,
+                                 ctypes.c_float, vp, i32, vp]
+    lib.hgemm_layout.restype = i32
     lib.hgemm_host.argtypes = [vp, vp, vp, i64, i64, i64, vp, vp, vp, vp]
     lib.hgemm_host.restype = i32
     lib.hgemm_select_path.argtypes = [vp, vp, vp, i64, i64, i64]
@@ -204,6 +212,15 @@ def hgemm_strided(A, lda: int, B, ldb: int, C, ldc: int, M: int, N: int, K: int,
     _raise_on(load().hgemm_strided(_ptr(A), lda, _ptr(B), ldb, _ptr(C), ldc, M, N, K, float(alpha),
                                    float(beta), _ptr(bias), int(bool(relu)), _stream(stream)),
               "hgemm_strided")
+
+
+def hgemm_layout(a_layout: int, b_layout: int, A, lda: int, B, ldb: int, C, ldc: int, M: int,
+                 N: int, K: int, alpha: float = 1.0, beta: float = 0.0, bias=None,
+                 relu: bool = False, stream=None) -> None:
+    """hgemm_strided with a storage order per operand (HGEMM_A_* / HGEMM_B_*; see hgemm.h)."""
+    _raise_on(load().hgemm_layout(int(a_layout), int(b_layout), _ptr(A), lda, _ptr(B), ldb, _ptr(C),
+                                  ldc, M, N, K, float(alpha), float(beta), _ptr(bias),
+                                  int(bool(relu)), _stream(stream)), "hgemm_layout")
 
 
 def hgemm_trmm(A, lda: int, B, ldb: int, C, ldc: int, n: int, m: int, alpha: float = 1.0,

@@ -44,13 +44,15 @@ struct DeviceState {
 DeviceState g_devices[kMaxDevices];
 
 // One product: operands, sizes and row pitches in elements (A(i,k) at
-// A[i*lda + k], B(k,j) at B[j*ldb + k], C(i,j) at C[i*ldc + j]).
+// A[i*lda + k], B(k,j) at B[j*ldb + k], C(i,j) at C[i*ldc + j]; with a_mn,
+// A(i,k) at A[k*lda + i]; with b_mn, B(k,j) at B[k*ldb + j]).
 struct Gemm {
   const void* A;
   const void* B;
   void* C;
   int64_t M, N, K;
   int64_t lda, ldb, ldc;
+  bool a_mn = false, b_mn = false;
 };
 
 Gemm dense(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K) {
@@ -127,16 +129,19 @@ int validate(const Gemm& g) {
   const int64_t M = g.M, N = g.N, K = g.K;
   if (M < 0 || N < 0 || K < 0 || M > HGEMM_MAX_DIM || N > HGEMM_MAX_DIM || K > HGEMM_MAX_DIM)
     return HGEMM_ERR_INVALID_ARG;
-  // pitches cover a row and stay far from overflow
+  // pitches cover a stored row and stay far from overflow
   const int64_t ld_lim = int64_t(1) << 40;
-  if (g.lda < K || g.ldb < K || g.ldc < N || g.lda > ld_lim || g.ldb > ld_lim || g.ldc > ld_lim)
+  const int64_t a_cols = g.a_mn ? M : K, a_rows = g.a_mn ? K : M;
+  const int64_t b_cols = g.b_mn ? N : K, b_rows = g.b_mn ? K : N;
+  if (g.lda < a_cols || g.ldb < b_cols || g.ldc < N || g.lda > ld_lim || g.ldb > ld_lim ||
+      g.ldc > ld_lim)
     return HGEMM_ERR_INVALID_ARG;
   // element spans (each < 2^61) and byte spans (< 2^62) cannot overflow
   using u128 = unsigned __int128;
   auto span = [](int64_t rows, int64_t ld, int64_t cols) -> u128 {
     return (rows > 0 && cols > 0) ? static_cast<u128>(rows - 1) * ld + cols : 0;
   };
-  const u128 sa = span(M, g.lda, K), sb = span(N, g.ldb, K), sc = span(M, g.ldc, N);
+  const u128 sa = span(a_rows, g.lda, a_cols), sb = span(b_rows, g.ldb, b_cols), sc = span(M, g.ldc, N);
   const u128 lim = static_cast<u128>(1) << 61;
   if (sa >= lim || sb >= lim || sc >= lim) return HGEMM_ERR_INVALID_ARG;
   if ((sa && !g.A) || (sb && !g.B) || (sc && !g.C)) return HGEMM_ERR_INVALID_ARG;
@@ -168,6 +173,8 @@ int choose_path(const Gemm& g, const hg::DeviceProfile& prof, bool fused, int* s
   const bool tma = tma_ok(g);
   const int forced = g_forced_path.load(std::memory_order_relaxed);
   if (forced == HGEMM_PATH_GENERIC || !tma) return HGEMM_PATH_GENERIC;
+  // M- or N-contiguous operands: the pair kernel reads them as MN-major tiles
+  if (g.a_mn || g.b_mn) return HGEMM_PATH_TC_PAIR;
   const int fs = g_forced_split.load(std::memory_order_relaxed);
   return hg::choose_tma_path(M, N, K, prof, forced, fs >> 10, fs & 1023, fused, split, tile_n);
 }
@@ -362,7 +369,9 @@ int run_tc_pair(const Gemm& g, const hg::EpiArgs& epi, const DeviceState& dev,
   if (tail_split_setting() && rest > 0 && 2 * rest <= clusters) {
     parts = 2;
     const int64_t last_cols = N - static_cast<int64_t>(args.num_n - 1) * hg::kPairBN;
-    if (4 * rest <= clusters && (args.num_n > 1 || last_cols > 128)) parts = 4;
+    // (an N-contiguous B arrives in 64-column boxes: a CTA's share of a part
+    // must be at least one box, so its parts keep 128 columns)
+    if (4 * rest <= clusters && (args.num_n > 1 || last_cols > 128) && !g.b_mn) parts = 4;
   }
   args.part_cols = hg::kPairBN / parts;
   args.full_tiles = static_cast<int>(parts > 1 ? tiles - rest : tiles);
@@ -379,11 +388,23 @@ int run_tc_pair(const Gemm& g, const hg::EpiArgs& epi, const DeviceState& dev,
   args.epi = epi;
   args.C = static_cast<const uint16_t*>(C);
   args.ldc = g.ldc;
+  args.a_mn = g.a_mn ? 1 : 0;
+  args.b_mn = g.b_mn ? 1 : 0;
   CUtensorMap ma, mb, mbp, mc;
   int rc;
-  if ((rc = encode_map(&ma, A, M, K, g.lda, hg::kTcBM, hg::kTcBK)) != HGEMM_OK) return rc;
-  if ((rc = encode_map(&mb, B, N, K, g.ldb, hg::kPairBN / 2, hg::kTcBK)) != HGEMM_OK) return rc;
-  if ((rc = encode_map(&mbp, B, N, K, g.ldb, args.part_cols / 2, hg::kTcBK)) != HGEMM_OK) return rc;
+  // MN-major operands: boxes of 64 M or N elements × 64 K rows
+  if (g.a_mn)
+    rc = encode_map(&ma, A, K, M, g.lda, hg::kTcBK, 64);
+  else
+    rc = encode_map(&ma, A, M, K, g.lda, hg::kTcBM, hg::kTcBK);
+  if (rc != HGEMM_OK) return rc;
+  if (g.b_mn) {
+    if ((rc = encode_map(&mb, B, K, N, g.ldb, hg::kTcBK, 64)) != HGEMM_OK) return rc;
+    mbp = mb;
+  } else {
+    if ((rc = encode_map(&mb, B, N, K, g.ldb, hg::kPairBN / 2, hg::kTcBK)) != HGEMM_OK) return rc;
+    if ((rc = encode_map(&mbp, B, N, K, g.ldb, args.part_cols / 2, hg::kTcBK)) != HGEMM_OK) return rc;
+  }
   if ((rc = encode_map(&mc, C, M, N, g.ldc, hg::kEpiRows, hg::kEpiCols)) != HGEMM_OK) return rc;
   cudaError_t e = hg::launch_tc_pair(ma, mb, mbp, mc, args, stream);
   return e == cudaSuccess ? HGEMM_OK : cuda_fail(e);
@@ -478,7 +499,7 @@ int dispatch(const Gemm& g, const hg::EpiArgs& epi, const DeviceState& dev, cuda
     default: {
       hg::PlainArgs pa{static_cast<const uint16_t*>(g.A), static_cast<const uint16_t*>(g.B),
                        static_cast<uint16_t*>(g.C), g.M, g.N, g.K, g.lda, g.ldb, g.ldc,
-                       dev.status, g_timeout_ns.load(), epi};
+                       dev.status, g_timeout_ns.load(), epi, g.a_mn ? 1 : 0, g.b_mn ? 1 : 0};
       e = hg::launch_generic(pa, dev.num_sms, stream);
       return e == cudaSuccess ? HGEMM_OK : cuda_fail(e);
     }
@@ -590,6 +611,21 @@ int hgemm_strided(const hgemm_half_t* A, int64_t lda, const hgemm_half_t* B, int
                   hgemm_half_t* C, int64_t ldc, int64_t M, int64_t N, int64_t K, float alpha,
                   float beta, const hgemm_half_t* bias, int relu, cudaStream_t stream) {
   const Gemm g{A, B, C, M, N, K, lda, ldb, ldc};
+  const int rc = validate(g);
+  if (rc != HGEMM_OK) return rc;
+  return run_fused(g, alpha, beta, bias, relu, stream);
+}
+
+int hgemm_layout(int a_layout, int b_layout, const hgemm_half_t* A, int64_t lda,
+                 const hgemm_half_t* B, int64_t ldb, hgemm_half_t* C, int64_t ldc, int64_t M,
+                 int64_t N, int64_t K, float alpha, float beta, const hgemm_half_t* bias, int relu,
+                 cudaStream_t stream) {
+  if ((a_layout != HGEMM_A_ROW_MAJOR && a_layout != HGEMM_A_COL_MAJOR) ||
+      (b_layout != HGEMM_B_COL_MAJOR && b_layout != HGEMM_B_ROW_MAJOR))
+    return HGEMM_ERR_INVALID_ARG;
+  Gemm g{A, B, C, M, N, K, lda, ldb, ldc};
+  g.a_mn = a_layout == HGEMM_A_COL_MAJOR;
+  g.b_mn = b_layout == HGEMM_B_ROW_MAJOR;
   const int rc = validate(g);
   if (rc != HGEMM_OK) return rc;
   return run_fused(g, alpha, beta, bias, relu, stream);

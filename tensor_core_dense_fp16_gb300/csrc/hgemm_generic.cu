@@ -86,6 +86,26 @@ __device__ __forceinline__ void load_row_swizzled(const uint16_t* __restrict__ s
   }
 }
 
+// The same row r of a K block for an operand stored with K as its slow
+// index: element k at src[k * stride] (k < n; zeros elsewhere). The 2-byte
+// loads of a warp's 32 rows are consecutive in memory for each k.
+__device__ __forceinline__ void load_row_gather(const uint16_t* __restrict__ src, int64_t stride, int n,
+                                                uint8_t* tile, int r) {
+  uint8_t* row = tile + r * 128;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    uint32_t w[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int k = 8 * j + 2 * u;
+      const uint32_t lo = k < n ? static_cast<uint32_t>(__ldg(src + k * stride)) : 0u;
+      const uint32_t hi = k + 1 < n ? static_cast<uint32_t>(__ldg(src + (k + 1) * stride)) : 0u;
+      w[u] = lo | (hi << 16);
+    }
+    *reinterpret_cast<uint4*>(row + ((j ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
 // One 128×128 tile of C at (m0, n0) over num_kb K blocks. TRI_B: the B
 // operand is the lower triangle of a square block (column i of the triangle,
 // i.e. operand row gj, holds its values from index gj on), so values at
@@ -141,15 +161,23 @@ __device__ __forceinline__ void generic_tile(const PlainArgs& p, int64_t m0, int
       if (!ok) break;
       const int64_t k0 = static_cast<int64_t>(kb) * Cfg::BK;
       const int64_t kn = p.K - k0 < Cfg::BK ? p.K - k0 : Cfg::BK;
-      load_row_swizzled(p.A + gi * p.lda + k0, gi < p.M ? static_cast<int>(kn) : 0,
+      if (p.a_mn)
+        load_row_gather(p.A + k0 * p.lda + gi, p.lda, gi < p.M ? static_cast<int>(kn) : 0,
                         smem + Cfg::OFF_A + stage * Cfg::A_BYTES, r);
+      else
+        load_row_swizzled(p.A + gi * p.lda + k0, gi < p.M ? static_cast<int>(kn) : 0,
+                          smem + Cfg::OFF_A + stage * Cfg::A_BYTES, r);
       int first = 0;
       if constexpr (TRI_B) {
         const int64_t f = gj - k0;
         first = f <= 0 ? 0 : (f >= Cfg::BK ? Cfg::BK : static_cast<int>(f));
       }
-      load_row_swizzled(p.B + gj * p.ldb + k0, gj < p.N ? static_cast<int>(kn) : 0,
-                        smem + Cfg::OFF_B + stage * Cfg::B_BYTES, r, first);
+      if (!TRI_B && p.b_mn)
+        load_row_gather(p.B + k0 * p.ldb + gj, p.ldb, gj < p.N ? static_cast<int>(kn) : 0,
+                        smem + Cfg::OFF_B + stage * Cfg::B_BYTES, r);
+      else
+        load_row_swizzled(p.B + gj * p.ldb + k0, gj < p.N ? static_cast<int>(kn) : 0,
+                          smem + Cfg::OFF_B + stage * Cfg::B_BYTES, r, first);
       fence_proxy_async_smem();  // generic-proxy writes before tensor-core reads
       __syncwarp();
       if (lane == 0) mbar_arrive(full_bar(stage));

@@ -41,6 +41,11 @@
 namespace hg {
 namespace {
 
+// MN-major operands (A stored K×M, B stored K×N) arrive in boxes of 64
+// M or N elements (128 bytes, the swizzle width) × 64 K rows.
+constexpr int kMnBox = 64;
+constexpr int kMnBoxBytes = kMnBox * kTcBK * 2;
+
 template <int MAX_STAGES_>
 struct PairCfg {
   static constexpr int BM = 2 * kTcBM;   // cluster tile rows
@@ -187,8 +192,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
           const uint32_t fb = mapa_shared(full_bar(stage), 0);
           if (rank == 0 && !(p.inject == 1 && issued == 0))  // testing aid: withhold one arrival
             mbar_arrive_expect_tx(full_bar(stage), tx);
-          tma_load_2d_cg2(sA + stage * stage_bytes, &tmA, fb, kb * Cfg::BK, ya);
-          tma_load_2d_cg2(sB + stage * stage_bytes, mapb, fb, kb * Cfg::BK, yb);
+          if (p.a_mn) {
+            // A stored K×M: the CTA's 128 rows as two 64-row boxes, 8 KB apart
+            tma_load_2d_cg2(sA + stage * stage_bytes, &tmA, fb, ya, kb * Cfg::BK);
+            tma_load_2d_cg2(sA + stage * stage_bytes + kMnBoxBytes, &tmA, fb, ya + kMnBox, kb * Cfg::BK);
+          } else {
+            tma_load_2d_cg2(sA + stage * stage_bytes, &tmA, fb, kb * Cfg::BK, ya);
+          }
+          if (p.b_mn) {
+            // B stored K×N: the CTA's ncols/2 columns as 64-column boxes, 8 KB apart
+            for (int bx = 0; bx < w.ncols / 2; bx += kMnBox)
+              tma_load_2d_cg2(sB + stage * stage_bytes + (bx / kMnBox) * kMnBoxBytes, &tmB, fb, yb + bx,
+                              kb * Cfg::BK);
+          } else {
+            tma_load_2d_cg2(sB + stage * stage_bytes, mapb, fb, kb * Cfg::BK, yb);
+          }
           ++issued;
           if (++stage == STAGES) {
             stage = 0;
@@ -225,7 +243,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
       uint32_t acc_phase = 0;
       bool ok = true;
       for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters) {
-        const uint32_t idesc = t < p.full_tiles ? Cfg::IDESC : idesc_f16_f32acc(Cfg::BM, p.part_cols);
+        const uint32_t idesc = (t < p.full_tiles ? Cfg::IDESC : idesc_f16_f32acc(Cfg::BM, p.part_cols)) |
+                               idesc_major_bits(p.a_mn != 0, p.b_mn != 0);
         if (!wait_phase_cluster(acce_bar(acc), acc_phase ^ 1u, wd, kWdMmaAccEmpty)) {
           ok = false;
           break;
@@ -238,13 +257,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
             break;
           }
           tc_fence_after_sync();
-          const uint64_t a_desc = sdesc_kmajor_sw128(sA + stage * stage_bytes);
-          const uint64_t b_desc = sdesc_kmajor_sw128(sB + stage * stage_bytes);
+          // K-major: 16 K elements are 32 bytes along the row; MN-major: 16 K
+          // rows of 128 bytes
+          const uint64_t a_desc = p.a_mn ? sdesc_mnmajor_sw128(sA + stage * stage_bytes)
+                                         : sdesc_kmajor_sw128(sA + stage * stage_bytes);
+          const uint64_t b_desc = p.b_mn ? sdesc_mnmajor_sw128(sB + stage * stage_bytes)
+                                         : sdesc_kmajor_sw128(sB + stage * stage_bytes);
+          const uint32_t a_step = p.a_mn ? 128u : 2u, b_step = p.b_mn ? 128u : 2u;
 #pragma unroll
           for (int k = 0; k < Cfg::BK / Cfg::UMMA_K; ++k)
             // kb counts the tile's K steps in load order (the producer may walk
             // K backwards); the first step overwrites the accumulator
-            mma_f16_ss_cg2(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc,
+            mma_f16_ss_cg2(d_tmem, a_desc + a_step * k, b_desc + b_step * k, idesc,
                            (kb > 0 || k > 0) ? 1u : 0u);
           mma_commit_cg2_multicast(empty_bar(stage), 0x3);  // frees the stage in both CTAs
           if (++stage == STAGES) {

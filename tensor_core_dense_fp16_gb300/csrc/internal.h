@@ -48,6 +48,8 @@ struct TcArgs {
   EpiArgs epi;
   const uint16_t* C;         // C itself, read in epilogue mode 2
   int64_t ldc;               // C's row pitch in elements
+  int a_mn, b_mn;            // pair kernel: A stored M-contiguous (K×M), B stored
+                             // N-contiguous (K×N); else K-contiguous
 };
 
 // Plain-pointer launch arguments for the kernels that do not use TMA.
@@ -60,6 +62,7 @@ struct PlainArgs {
   int* status;
   unsigned long long timeout_ns;
   EpiArgs epi;
+  int a_mn = 0, b_mn = 0;    // A(i,k) at A[k*lda + i]; B(k,j) at B[k*ldb + j]
 };
 
 // The diagonal blocks ("leaves") of a triangular product, for one batched

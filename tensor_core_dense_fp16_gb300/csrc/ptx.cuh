@@ -231,12 +231,34 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr) {
   return d;
 }
 
+// Shared-memory matrix descriptor for an MN-major operand tile (M or N
+// contiguous) written by TMA with 128-byte swizzling in boxes of 64 MN
+// elements × 64 K rows: each box is 64 rows of 128 bytes (K row k at
+// k·128), 8-K-row groups 1024 bytes apart (stride byte offset), consecutive
+// 64-element MN boxes 8192 bytes apart (leading byte offset). Stepping K by
+// 16 rows adds 2048 bytes (128 in the address field) to the start address.
+__device__ __forceinline__ uint64_t sdesc_mnmajor_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(8192 >> 4) << 16;
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
 // Instruction descriptor of tcgen05.mma.kind::f16 with FP16 A and B (both
 // K-major), FP32 accumulator, dense: D format (1 = F32) in bits [4,6),
 // A and B formats (0 = F16) in [7,10) and [10,13), major-ness bits 15/16 = 0,
 // N >> 3 in [17,23), M >> 4 in [24,29).
 __host__ __device__ constexpr uint32_t idesc_f16_f32acc(int m, int n) {
   return (1u << 4) | (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+// Major-ness bits of the instruction descriptor: bit 15 set when A is
+// M-major, bit 16 when B is N-major (both clear: K-major).
+__host__ __device__ constexpr uint32_t idesc_major_bits(bool a_mn, bool b_mn) {
+  return (a_mn ? 1u << 15 : 0u) | (b_mn ? 1u << 16 : 0u);
 }
 
 // ------------------------------------------------------- clusters, 2 CTAs

@@ -209,6 +209,24 @@ def test_trsm_argument_checks(lib):
     assert call(n=0) == tc.HGEMM_OK and call(m=0) == tc.HGEMM_OK
 
 
+def test_layout_argument_checks(lib):
+    lib_ = tc.load()
+    def call(a_layout=0, b_layout=0, lda=64, ldb=64, ldc=64, M=16, N=64, K=64, C=C16):
+        return lib_.hgemm_layout(a_layout, b_layout, A16, lda, B16, ldb, C, ldc, M, N, K, 1.0, 0.0,
+                                 None, 0, None)
+    assert call(a_layout=2) == tc.HGEMM_ERR_INVALID_ARG
+    assert call(b_layout=-1) == tc.HGEMM_ERR_INVALID_ARG
+    # the pitch must cover a stored row: K for A row-major, M for A column-major,
+    # K for B column-major, N for B row-major
+    assert call(lda=63) == tc.HGEMM_ERR_INVALID_ARG
+    assert call(a_layout=1, lda=15) == tc.HGEMM_ERR_INVALID_ARG
+    assert call(ldb=63) == tc.HGEMM_ERR_INVALID_ARG
+    assert call(b_layout=1, N=72, ldb=64, ldc=72) == tc.HGEMM_ERR_INVALID_ARG
+    # spans follow the layout: A column-major is K rows of lda
+    assert call(a_layout=1, lda=16, C=A16 + 2 * 16 * 63) == tc.HGEMM_ERR_ALIAS
+    assert call(M=0) == tc.HGEMM_OK and call(a_layout=1, b_layout=1, N=0, lda=16) == tc.HGEMM_OK
+
+
 def test_invalid_arguments_rejected_before_any_device_work(lib):
     bad = [
         (A16, B16, C16, -1, 4, 4),
