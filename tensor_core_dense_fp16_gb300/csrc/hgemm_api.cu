@@ -764,10 +764,12 @@ int hgemm_trsm(const hgemm_half_t* A, int64_t lda, const hgemm_half_t* B, int64_
   uint16_t* x = reinterpret_cast<uint16_t*>(X);
   const uint16_t* a = reinterpret_cast<const uint16_t*>(A);
   cudaError_t e;
+  bool chained = false;  // a launch of this solve is already on the stream
   if (!in_place || alpha != 1.0f) {
     e = hg::launch_scale_copy(reinterpret_cast<const uint16_t*>(B), ldb, x, ldx, n, m, alpha,
                               dev->num_sms, stream);
     if (e != cudaSuccess) return cuda_fail(e);
+    chained = true;
   }
   // The update of block [off, off + s) split at s1, in the GEMM view:
   //   X1ᵀ (m × s1, pitch ldx) -= X2ᵀ (m × s2, pitch ldx) · A21 (s2 × s1),
@@ -781,7 +783,8 @@ int hgemm_trsm(const hgemm_half_t* A, int64_t lda, const hgemm_half_t* B, int64_
   std::function<int(int64_t, int64_t)> solve = [&](int64_t off, int64_t s) -> int {
     if (s <= hg::kTrsmLeaf) {
       const cudaError_t le = hg::launch_trsm_leaf(a, lda, x, ldx, off, static_cast<int>(s), m,
-                                                  dev->num_sms, stream);
+                                                  dev->num_sms, chained, stream);
+      chained = true;
       return le == cudaSuccess ? HGEMM_OK : cuda_fail(le);
     }
     const int64_t s1 = ((s / 2 + 63) / 64) * 64, s2 = s - s1;

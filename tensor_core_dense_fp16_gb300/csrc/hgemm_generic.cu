@@ -147,6 +147,9 @@ __device__ __forceinline__ void generic_tile(const PlainArgs& p, int64_t m0, int
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
+  // operands and C may come from the previous launch on the stream
+  grid_dependency_wait();
+  grid_launch_dependents();
 
   if (warp < Cfg::LOADER_WARPS) {
     // ------------------------------------------------------------ loaders
@@ -327,10 +330,9 @@ cudaError_t launch_tri_leaves(const PlainArgs& args, const TriLeaves& leaves, cu
   const int64_t tiles_m = (args.M + GenCfg::BM - 1) / GenCfg::BM;
   const int64_t tiles = tiles_m * ((widest + GenCfg::BN - 1) / GenCfg::BN);
   if (tiles > 0x7FFFFFFF || tiles_m > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
-  hgemm_tri_leaves_kernel<<<dim3(static_cast<unsigned>(tiles), static_cast<unsigned>(leaves.count)),
-                            GenCfg::THREADS, GenCfg::SMEM_BYTES, stream>>>(args, leaves,
-                                                                          static_cast<int>(tiles_m));
-  return cudaGetLastError();
+  PdlLaunch l(dim3(static_cast<unsigned>(tiles), static_cast<unsigned>(leaves.count)), dim3(GenCfg::THREADS),
+              GenCfg::SMEM_BYTES, stream);
+  return cudaLaunchKernelEx(&l.cfg, hgemm_tri_leaves_kernel, args, leaves, static_cast<int>(tiles_m));
 }
 
 cudaError_t launch_generic(const PlainArgs& args, int /*num_sms*/, cudaStream_t stream) {
@@ -341,9 +343,9 @@ cudaError_t launch_generic(const PlainArgs& args, int /*num_sms*/, cudaStream_t 
   const int64_t tiles = tiles_n * ((args.M + GenCfg::BM - 1) / GenCfg::BM);
   const int64_t num_kb = (args.K + GenCfg::BK - 1) / GenCfg::BK;
   if (tiles > 0x7FFFFFFF || num_kb > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
-  hgemm_generic_kernel<<<static_cast<unsigned>(tiles), GenCfg::THREADS, GenCfg::SMEM_BYTES, stream>>>(
-      args, static_cast<int>(tiles_n), static_cast<int>(num_kb));
-  return cudaGetLastError();
+  PdlLaunch l(dim3(static_cast<unsigned>(tiles)), dim3(GenCfg::THREADS), GenCfg::SMEM_BYTES, stream);
+  return cudaLaunchKernelEx(&l.cfg, hgemm_generic_kernel, args, static_cast<int>(tiles_n),
+                            static_cast<int>(num_kb));
 }
 
 }  // namespace hg

@@ -155,6 +155,9 @@ __global__ void __launch_bounds__(192, 1)
   cluster_sync();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
+  // operands and C may come from the previous launch on the stream
+  grid_dependency_wait();
+  grid_launch_dependents();
 
   int ok = 1;
   if (warp == 0) {
@@ -388,19 +391,10 @@ cudaError_t launch_split(const CUtensorMap& a, const CUtensorMap& b, const CUten
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_done[fused][dev] = true;
   }
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2 * SPLIT;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(args.num_tiles * 2 * SPLIT));
-  cfg.blockDim = dim3(Cfg::THREADS);
-  cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
-  cfg.stream = stream;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, a, b, c, args);
+  PdlLaunch l(dim3(static_cast<unsigned>(args.num_tiles * 2 * SPLIT)), dim3(Cfg::THREADS), Cfg::SMEM_BYTES,
+              stream);
+  l.cluster(2 * SPLIT);
+  return cudaLaunchKernelEx(&l.cfg, kern, a, b, c, args);
 }
 
 template <int SPLIT, int BN>

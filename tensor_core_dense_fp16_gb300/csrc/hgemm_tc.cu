@@ -126,6 +126,9 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
+  // operands and C may come from the previous launch on the stream
+  grid_dependency_wait();
+  grid_launch_dependents();
 
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer
@@ -281,6 +284,9 @@ __global__ void __launch_bounds__(192, 1)
 // +0 for the plain product.
 __global__ void empty_sum_kernel(uint16_t* __restrict__ C, int64_t M, int64_t N, int64_t ldc,
                                  const EpiArgs e) {
+  // C and the bias may come from the previous launch on the stream
+  grid_dependency_wait();
+  grid_launch_dependents();
   const int64_t count = M * N;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   const __half* bias = reinterpret_cast<const __half*>(e.bias);
@@ -319,12 +325,8 @@ cudaError_t launch_tc_128x256(const CUtensorMap& a, const CUtensorMap& b, const 
   auto kern = fused ? hgemm_tc_kernel<256, 4, true> : hgemm_tc_kernel<256, 4, false>;
   cudaError_t e = ensure_smem_attr(kern, Cfg::SMEM_BYTES, attr_done[fused ? 1 : 0]);
   if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(args.grid));
-  cfg.blockDim = dim3(Cfg::THREADS);
-  cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
-  cfg.stream = stream;
-  return cudaLaunchKernelEx(&cfg, kern, a, b, c, args);
+  PdlLaunch l(dim3(static_cast<unsigned>(args.grid)), dim3(Cfg::THREADS), Cfg::SMEM_BYTES, stream);
+  return cudaLaunchKernelEx(&l.cfg, kern, a, b, c, args);
 }
 
 cudaError_t launch_empty_sum(uint16_t* C, int64_t M, int64_t N, int64_t ldc, const EpiArgs& epi,
@@ -333,8 +335,8 @@ cudaError_t launch_empty_sum(uint16_t* C, int64_t M, int64_t N, int64_t ldc, con
   int blocks = static_cast<int>((count + 255) / 256);
   if (blocks > 4096) blocks = 4096;
   if (blocks < 1) blocks = 1;
-  empty_sum_kernel<<<blocks, 256, 0, stream>>>(C, M, N, ldc, epi);
-  return cudaGetLastError();
+  PdlLaunch l(dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream);
+  return cudaLaunchKernelEx(&l.cfg, empty_sum_kernel, C, M, N, ldc, epi);
 }
 
 }  // namespace hg

@@ -165,6 +165,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
   cluster_sync();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
+  // operands and C may come from the previous launch on the stream
+  grid_dependency_wait();
+  grid_launch_dependents();
 
   if (warp == 0) {
     // ------------------------------------------------ TMA producer (both CTAs)
@@ -390,12 +393,8 @@ cudaError_t launch_tc_pair(const CUtensorMap& a, const CUtensorMap& b, const CUt
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_done[fused][dev] = true;
   }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(args.grid));
-  cfg.blockDim = dim3(Cfg::THREADS);
-  cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
-  cfg.stream = stream;
-  return cudaLaunchKernelEx(&cfg, kern, a, b, b_part, c, args);
+  PdlLaunch l(dim3(static_cast<unsigned>(args.grid)), dim3(Cfg::THREADS), Cfg::SMEM_BYTES, stream);
+  return cudaLaunchKernelEx(&l.cfg, kern, a, b, b_part, c, args);
 }
 
 }  // namespace hg

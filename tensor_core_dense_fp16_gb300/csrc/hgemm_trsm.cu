@@ -26,6 +26,7 @@
 #include <cuda_fp16.h>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace hg {
 namespace {
@@ -42,9 +43,22 @@ __host__ __device__ constexpr int pub_pitch() {
   return COLS + 4;
 }
 
+// Halves per column of the FP16 copy of -x_g (the mma B operand): the
+// padding spreads a warp's 32-bit fragment loads over all banks.
+constexpr int KP = kGroup + 8;
+
 template <int COLS>
 constexpr int leaf_smem() {
-  return kGroups * kGroup * kGroup * 4 + 2 * kGroup * pub_pitch<COLS>() * 4;
+  return kGroups * kGroup * kGroup * 4 + 2 * kGroup * pub_pitch<COLS>() * 4 + COLS * KP * 2;
+}
+
+// mma.sync m16n8k16, FP16 operands, FP32 accumulator in place: d += a·b.
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
 // A(row0 + q, col) for q < 32 (q < valid; 0 past it), packed as 32 halves.
@@ -77,14 +91,16 @@ __device__ __forceinline__ float col32_at(const uint4 (&v)[4], int q) {
 template <int COLS>
 __global__ void __launch_bounds__(kLeafMax, 2)
     trsm_leaf_kernel(const uint16_t* __restrict__ A, int64_t lda, uint16_t* __restrict__ X,
-                     int64_t ldx, int64_t off, int s, int64_t m) {
+                     int64_t ldx, int64_t off, int s, int64_t m, int chained) {
   extern __shared__ __align__(16) uint8_t smem[];
+  if (!chained) grid_dependency_wait();
   // diag[g][k][j]: first L_g(k, j) in FP32 (L_g the diagonal triangle of
   // rows 32g .. 32g+31), then, in place, (L_g⁻¹)(k, j)
   float* diag = reinterpret_cast<float*>(smem);
   constexpr int P = pub_pitch<COLS>();
   float* pub_b = diag + kGroups * kGroup * kGroup;  // [kGroup][P]: b of the group's rows
   float* pub_x = pub_b + kGroup * P;                // [kGroup][P]: x of the group's rows
+  __half* pub_xh = reinterpret_cast<__half*>(pub_x + kGroup * P);  // [COLS][KP]: -x_g in FP16
   const int r = threadIdx.x;
   const int lane = r & 31, warp = r >> 5;
   const int64_t j0 = static_cast<int64_t>(blockIdx.x) * COLS;
@@ -130,34 +146,79 @@ __global__ void __launch_bounds__(kLeafMax, 2)
     for (int k = 0; k < kGroup; ++k) blk[k * kGroup + lane] = lane < sg ? mcol[k] : 0.f;
   }
 
-  // This block's right-hand sides (one coalesced column of the block per jj),
-  // loaded after the inversion (kept out of its registers).
-  asm volatile("" ::: "memory");
-  float b[COLS];
+  // The rows above a group take its update on the tensor cores: b (rows ×
+  // right-hand sides) -= A_g (rows × the group's 32 rows) · x_g, as
+  // mma.sync m16n8k16 products (FP16 operands, FP32 accumulation) whose
+  // accumulators are the b values themselves. Warp w holds its 32 rows as
+  // c[mt][nt][e]: row 16·mt + gid (+8 for e ≥ 2) of the warp's rows, column
+  // 8·nt + 2·tig (+1 for odd e), gid = lane / 4, tig = lane % 4 (the
+  // accumulator layout of that instruction).
+  constexpr int NT = COLS / 8;
+  const int gid = lane >> 2, tig = lane & 3;
+  float c[2][NT][4];
+  // X comes from the previous launch on the stream: everything above only
+  // read A, which no launch of the solve writes (a chained launch starts only
+  // after its predecessor passed its own wait, so work enqueued before the
+  // solve is complete). The first launch of a solve waits before reading A.
+  grid_dependency_wait();
+  grid_launch_dependents();
 #pragma unroll
-  for (int jj = 0; jj < COLS; ++jj) {
-    const int64_t j = j0 + jj;
-    b[jj] = (r < s && j < m) ? __half2float(__ushort_as_half(X[j * ldx + off + r])) : 0.f;
-  }
+  for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int row = warp * kGroup + 16 * mt + gid + (e >= 2 ? 8 : 0);
+        const int64_t j = j0 + 8 * nt + 2 * tig + (e & 1);
+        c[mt][nt][e] = (row < s && j < m) ? __half2float(__ushort_as_half(X[j * ldx + off + row])) : 0.f;
+      }
+  // 32-bit loads of A's K pairs: A 4-byte aligned and lda even (off is a
+  // multiple of 64)
+  const bool pairs = ((reinterpret_cast<uintptr_t>(A) & 3u) == 0) && (lda % 2) == 0;
 
   for (int g = groups - 1; g >= 0; --g) {
     const int c0 = g * kGroup, sg = min(kGroup, s - c0);
-    // A(c0 .. c0+31, r) for the update below, loaded now to land while the
-    // group is solved.
-    uint4 acol[4] = {};
-    if (r < c0) load_col32(A, lda, off + r, off + c0, sg, vec, acol);
+    // A's values for this warp's update, loaded now to land while the group
+    // is solved: af[mt][ks] is the m16k16 fragment of rows 16·mt.. of the
+    // warp and the group's rows 16·ks.., i.e. A(c0 + k, r) (contiguous in k)
+    uint32_t af[2][2][4] = {};
+    if (warp < g) {
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int64_t r = off + warp * kGroup + 16 * mt + gid + ((e & 1) ? 8 : 0);
+            const int k = 16 * ks + 2 * tig + ((e & 2) ? 8 : 0);
+            const uint16_t* src = A + r * lda + off + c0 + k;
+            if (pairs && k + 1 < sg) {
+              af[mt][ks][e] = __ldg(reinterpret_cast<const unsigned int*>(src));
+            } else {
+              const uint32_t lo = k < sg ? src[0] : 0u;
+              const uint32_t hi = k + 1 < sg ? src[1] : 0u;
+              af[mt][ks][e] = lo | (hi << 16);
+            }
+          }
+    }
     // (1) the owning warp's rows, complete with every later group's update
     if (warp == g) {
-      float4* dst = reinterpret_cast<float4*>(pub_b + lane * P);
 #pragma unroll
-      for (int q = 0; q < COLS / 4; ++q) dst[q] = make_float4(b[4 * q], b[4 * q + 1], b[4 * q + 2], b[4 * q + 3]);
+      for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          float* d = pub_b + (16 * mt + gid) * P + 8 * nt + 2 * tig;
+          *reinterpret_cast<float2*>(d) = make_float2(c[mt][nt][0], c[mt][nt][1]);
+          *reinterpret_cast<float2*>(d + 8 * P) = make_float2(c[mt][nt][2], c[mt][nt][3]);
+        }
     }
-    // This barrier also orders the group's writes of pub_b and pub_x after
+    // This barrier also orders the group's writes of the published rows after
     // every read of them for the previous group, and (first time round) the
     // inverses before their use by other warps.
     __syncthreads();
     // (2) x_g(i, jj) = Σ_k L_g⁻¹(k, i)·b_g(k, jj): lane i, four right-hand
-    // sides per thread (jj = 4q .. 4q+3 for q = warp, warp + groups, ...).
+    // sides per thread (jj = 4q .. 4q+3 for q = warp, warp + groups, ...);
+    // also -x_g in FP16, column by column, as the mma B operand
     {
       const float* mi = diag + g * kGroup * kGroup + lane;
       for (int q = warp; q < COLS / 4; q += groups) {
@@ -172,43 +233,51 @@ __global__ void __launch_bounds__(kLeafMax, 2)
           acc.w = fmaf(mk, bk.w, acc.w);
         }
         *reinterpret_cast<float4*>(pub_x + lane * P + 4 * q) = acc;
+        pub_xh[(4 * q + 0) * KP + lane] = __float2half_rn(-acc.x);
+        pub_xh[(4 * q + 1) * KP + lane] = __float2half_rn(-acc.y);
+        pub_xh[(4 * q + 2) * KP + lane] = __float2half_rn(-acc.z);
+        pub_xh[(4 * q + 3) * KP + lane] = __float2half_rn(-acc.w);
       }
     }
     __syncthreads();
     if (warp == g) {
-      const float4* src = reinterpret_cast<const float4*>(pub_x + lane * P);
 #pragma unroll
-      for (int q = 0; q < COLS / 4; ++q) {
-        const float4 x = src[q];
-        b[4 * q] = x.x;
-        b[4 * q + 1] = x.y;
-        b[4 * q + 2] = x.z;
-        b[4 * q + 3] = x.w;
-      }
-    } else if (r < c0) {
-      // (3) rows above the group: b -= Σ_c A(c, r)·x_c over the group's rows
-      // (A(c, r) = 0 past the block's order)
+      for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-      for (int q = 0; q < kGroup; ++q) {
-        const float a = -col32_at(acol, q);
-        const float4* xc = reinterpret_cast<const float4*>(pub_x + q * P);
-#pragma unroll
-        for (int p = 0; p < COLS / 4; ++p) {
-          const float4 x = xc[p];
-          b[4 * p] = fmaf(a, x.x, b[4 * p]);
-          b[4 * p + 1] = fmaf(a, x.y, b[4 * p + 1]);
-          b[4 * p + 2] = fmaf(a, x.z, b[4 * p + 2]);
-          b[4 * p + 3] = fmaf(a, x.w, b[4 * p + 3]);
+        for (int nt = 0; nt < NT; ++nt) {
+          const float* x = pub_x + (16 * mt + gid) * P + 8 * nt + 2 * tig;
+          const float2 lo = *reinterpret_cast<const float2*>(x);
+          const float2 hi = *reinterpret_cast<const float2*>(x + 8 * P);
+          c[mt][nt][0] = lo.x;
+          c[mt][nt][1] = lo.y;
+          c[mt][nt][2] = hi.x;
+          c[mt][nt][3] = hi.y;
         }
-      }
+    } else if (warp < g) {
+      // (3) rows above the group: b += A_g · (-x_g) (A = 0 past the block's order)
+#pragma unroll
+      for (int ks = 0; ks < 2; ++ks)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const __half* xb = pub_xh + (8 * nt + gid) * KP + 16 * ks + 2 * tig;
+          const uint32_t b0 = *reinterpret_cast<const uint32_t*>(xb);
+          const uint32_t b1 = *reinterpret_cast<const uint32_t*>(xb + 8);
+#pragma unroll
+          for (int mt = 0; mt < 2; ++mt) mma_16816(c[mt][nt], af[mt][ks], b0, b1);
+        }
     }
   }
 
 #pragma unroll
-  for (int jj = 0; jj < COLS; ++jj) {
-    const int64_t j = j0 + jj;
-    if (r < s && j < m) X[j * ldx + off + r] = __half_as_ushort(__float2half_rn(b[jj]));
-  }
+  for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int row = warp * kGroup + 16 * mt + gid + (e >= 2 ? 8 : 0);
+        const int64_t j = j0 + 8 * nt + 2 * tig + (e & 1);
+        if (row < s && j < m) X[j * ldx + off + row] = __half_as_ushort(__float2half_rn(c[mt][nt][e]));
+      }
 }
 
 // X(:, j) = alpha · B(:, j) for the n × m column-major operands; FP16 in and
@@ -218,6 +287,8 @@ __global__ void __launch_bounds__(kLeafMax, 2)
 template <bool VEC>
 __global__ void scale_copy_kernel(const uint16_t* B, int64_t ldb, uint16_t* X, int64_t ldx,
                                   int64_t n, int64_t m, float alpha) {
+  grid_dependency_wait();
+  grid_launch_dependents();
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   const int64_t t0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (VEC) {
@@ -249,12 +320,11 @@ int g_resident[kMaxDevices][3] = {};
 
 template <int COLS>
 cudaError_t launch_width(const uint16_t* A, int64_t lda, uint16_t* X, int64_t ldx, int64_t off,
-                         int s, int64_t m, int threads, cudaStream_t stream) {
+                         int s, int64_t m, int threads, bool chained, cudaStream_t stream) {
   const int64_t blocks = (m + COLS - 1) / COLS;
   if (blocks > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
-  trsm_leaf_kernel<COLS><<<static_cast<unsigned>(blocks), threads, leaf_smem<COLS>(), stream>>>(
-      A, lda, X, ldx, off, s, m);
-  return cudaGetLastError();
+  PdlLaunch l(dim3(static_cast<unsigned>(blocks)), dim3(threads), leaf_smem<COLS>(), stream);
+  return cudaLaunchKernelEx(&l.cfg, trsm_leaf_kernel<COLS>, A, lda, X, ldx, off, s, m, chained ? 1 : 0);
 }
 
 template <int COLS>
@@ -269,7 +339,7 @@ cudaError_t resident_blocks(int* out) {
 }  // namespace
 
 cudaError_t launch_trsm_leaf(const uint16_t* A, int64_t lda, uint16_t* X, int64_t ldx, int64_t off,
-                             int s, int64_t m, int num_sms, cudaStream_t stream) {
+                             int s, int64_t m, int num_sms, bool chained, cudaStream_t stream) {
   if (s < 1 || s > kLeafMax || m < 1 || num_sms < 1) return cudaErrorInvalidValue;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -304,11 +374,11 @@ cudaError_t launch_trsm_leaf(const uint16_t* A, int64_t lda, uint16_t* X, int64_
   const int threads = ((s + 31) / 32) * 32;
   switch (best) {
     case 0:
-      return launch_width<8>(A, lda, X, ldx, off, s, m, threads, stream);
+      return launch_width<8>(A, lda, X, ldx, off, s, m, threads, chained, stream);
     case 1:
-      return launch_width<16>(A, lda, X, ldx, off, s, m, threads, stream);
+      return launch_width<16>(A, lda, X, ldx, off, s, m, threads, chained, stream);
     default:
-      return launch_width<32>(A, lda, X, ldx, off, s, m, threads, stream);
+      return launch_width<32>(A, lda, X, ldx, off, s, m, threads, chained, stream);
   }
 }
 
@@ -321,11 +391,9 @@ cudaError_t launch_scale_copy(const uint16_t* B, int64_t ldb, uint16_t* X, int64
   const int64_t cap = static_cast<int64_t>(num_sms > 0 ? num_sms : 1) * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  if (vec)
-    scale_copy_kernel<true><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(B, ldb, X, ldx, n, m, alpha);
-  else
-    scale_copy_kernel<false><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(B, ldb, X, ldx, n, m, alpha);
-  return cudaGetLastError();
+  PdlLaunch l(dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream);
+  return cudaLaunchKernelEx(&l.cfg, vec ? scale_copy_kernel<true> : scale_copy_kernel<false>, B, ldb, X, ldx,
+                            n, m, alpha);
 }
 
 }  // namespace hg

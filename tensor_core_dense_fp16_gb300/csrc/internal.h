@@ -74,6 +74,33 @@ struct TriLeaves {
   int64_t size[kMaxLeaves];  // its order
 };
 
+// Every kernel here is launched with programmatic stream serialization: it
+// may start while the previous kernel on the stream is still running, and
+// waits for it (griddepcontrol.wait) before touching memory that kernel may
+// write, so its launch and prologue overlap the previous kernel's tail.
+struct PdlLaunch {
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t cfg;
+  PdlLaunch(dim3 grid, dim3 block, size_t smem, cudaStream_t stream) : attr{}, cfg{} {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  // clusters of x CTAs set at launch time
+  void cluster(unsigned x) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = x;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
+  }
+};
+
 // Launchers (each enqueues one kernel on `stream` and returns the launch
 // error, if any). Shared-memory attributes are set on first use per device.
 cudaError_t launch_tc_128x256(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
@@ -109,8 +136,10 @@ cudaError_t launch_tri_leaves(const PlainArgs& args, const TriLeaves& leaves, cu
 constexpr int kTrsmLeaf = 256;
 cudaError_t launch_scale_copy(const uint16_t* B, int64_t ldb, uint16_t* X, int64_t ldx, int64_t n,
                               int64_t m, float alpha, int num_sms, cudaStream_t stream);
+// chained: an earlier launch of the same solve precedes this one on the
+// stream (the kernel may then read A before waiting for it).
 cudaError_t launch_trsm_leaf(const uint16_t* A, int64_t lda, uint16_t* X, int64_t ldx, int64_t off,
-                             int s, int64_t m, int num_sms, cudaStream_t stream);
+                             int s, int64_t m, int num_sms, bool chained, cudaStream_t stream);
 
 // Address of the device watchdog word on the current device.
 cudaError_t status_word_address(int** addr);

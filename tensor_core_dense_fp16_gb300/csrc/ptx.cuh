@@ -211,6 +211,22 @@ __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32]) {
                : "memory");
 }
 
+// ------------------------------------------ programmatic dependent launch
+
+// Waits until the launches this grid depends on (the previous kernel on the
+// stream, when this one was launched with programmatic stream serialization)
+// have completed and their memory operations are visible; returns at once
+// otherwise. Every kernel here calls it before its first access to memory
+// that an earlier launch may write.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Allows the next launch on the stream to start (its own prologue then
+// overlaps this grid). Called after grid_dependency_wait, so a chained
+// kernel never starts before everything enqueued ahead of this one is done.
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ----------------------------------------------------- tcgen05 descriptors
 
 // Shared-memory matrix descriptor for a K-major operand tile written by TMA
