@@ -8,12 +8,15 @@
 // 共享内存与分块: tiles are staged in shared memory with out-of-range elements
 // replaced by zero, and only in-range outputs are stored.
 //
-// Design: one CTA per 128×128 output tile.
+// Design: one CTA per 128×128 output tile, two CTAs per SM (each one's
+// loads, MMAs and epilogue overlap the other's; measured faster than one CTA
+// with a deeper ring: the tiles of a triangular product's leaves have few K
+// blocks).
 //   * warps 0–3 (128 threads) are the loaders: thread t copies row t of the
 //     A tile and row t of the B tile for one 64-wide K block with 2-byte loads
 //     (bounds-checked, zero outside the matrices) and writes them, 16 bytes
 //     at a time, into the same 128-byte-swizzled K-major layout that a TMA
-//     copy would produce; a 4-stage ring, one barrier arrival per warp;
+//     copy would produce; a 2-stage ring, one barrier arrival per warp;
 //   * warp 8 (one thread) issues tcgen05.mma (M=128, N=128, K=16) into an
 //     FP32 accumulator in TMEM;
 //   * warps 4–7 read the accumulator with tcgen05.ld, round to FP16 and store
@@ -28,7 +31,7 @@ namespace hg {
 namespace {
 
 struct GenCfg {
-  static constexpr int BM = 128, BN = 128, BK = 64, STAGES = 4, UMMA_K = 16;
+  static constexpr int BM = 128, BN = 128, BK = 64, STAGES = 2, UMMA_K = 16;
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int OFF_A = 0;
@@ -278,7 +281,7 @@ __device__ __forceinline__ void generic_tile(const PlainArgs& p, int64_t m0, int
   if (warp == Cfg::MMA_WARP) tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
 }
 
-__global__ void __launch_bounds__(GenCfg::THREADS, 1)
+__global__ void __launch_bounds__(GenCfg::THREADS, 2)
     hgemm_generic_kernel(const PlainArgs p, int tiles_n, int num_kb) {
   generic_tile<false>(p, static_cast<int64_t>(blockIdx.x / tiles_n) * GenCfg::BM,
                       static_cast<int64_t>(blockIdx.x % tiles_n) * GenCfg::BN, num_kb);
@@ -288,7 +291,7 @@ __global__ void __launch_bounds__(GenCfg::THREADS, 1)
 // the product of p's A operand shifted by off columns (M × s) with the lower
 // triangle of p's B operand at (off, off) (s × s), into C shifted by off
 // columns, where off = leaves.off[b] and s = leaves.size[b].
-__global__ void __launch_bounds__(GenCfg::THREADS, 1)
+__global__ void __launch_bounds__(GenCfg::THREADS, 2)
     hgemm_tri_leaves_kernel(const PlainArgs p, const TriLeaves leaves, int tiles_m) {
   const int b = blockIdx.y;
   const int64_t off = leaves.off[b], s = leaves.size[b];
