@@ -18,11 +18,17 @@
 // start (forward substitution on the columns of the identity), so that the
 // group's solution x_g = (L_g⁻¹)ᵀ·b_g is a small product spread over all
 // threads, not a chain of 32 dependent steps in one warp. Per group: the
-// owning warp publishes its b, barrier, all threads form x_g, barrier, and
-// every thread r above the group's first row subtracts Σ_c A(c,r)·x_c over
-// the group's rows, reading A(c0 .. c0+31, r) (contiguous in the
-// column-major A) straight from global memory, issued before the group's
-// barriers. Arithmetic is FP32 and the results are rounded once to FP16.
+// owning warp publishes its b, barrier, all threads form x_g (FP32),
+// barrier, and every warp above the group subtracts Σ_c A(c,r)·x_c over the
+// group's rows on the tensor cores (mma.sync m16n8k16: A(c0 .. c0+31, r),
+// contiguous in the column-major A, read from global memory before the
+// group's barriers; x_g rounded to FP16, as the recursion's GEMM updates see
+// X; FP32 accumulators holding the right-hand sides). The solution is
+// rounded once to FP16.
+//
+// Launch overlap: the inverses only read A, which no launch of the solve
+// writes, so they are computed before the kernel waits for the previous
+// launch on the stream (griddepcontrol.wait) and read X.
 #include <cuda_fp16.h>
 
 #include "internal.h"
