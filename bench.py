@@ -596,9 +596,13 @@ def run_ours(args, spec, a, b, world, rank, local):
     flush = torch.empty(2 * l2 // 4 + 1, dtype=torch.float32, device=dev)
     epi = EPILOGUES[args.epilogue]
     if layouts:
-        # M- or N-contiguous operands go to the pair kernel when TMA can read them
+        # M- or N-contiguous operands take the path of the same shape in the
+        # default layout, except that the wide and single-CTA kernels read
+        # K-major operands only (the pair kernel stands in for them)
         tma = lda % 8 == 0 and ldb % 8 == 0 and N % 8 == 0
-        path = tc.HGEMM_PATH_TC_PAIR if tma else tc.HGEMM_PATH_GENERIC
+        path = tc.hgemm_select_path(da, db, dc, M, N, K) if tma else tc.HGEMM_PATH_GENERIC
+        if path in (tc.HGEMM_PATH_TC_WIDE, tc.HGEMM_PATH_TC):
+            path = tc.HGEMM_PATH_TC_PAIR
     else:
         path = tc.hgemm_select_path(da, db, dc, M, N, K)
     if epi is not None and path == tc.HGEMM_PATH_TC_WIDE:

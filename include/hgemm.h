@@ -152,8 +152,9 @@ HGEMM_API int hgemm_strided(const hgemm_half_t *A, int64_t lda, const hgemm_half
  * ownership, alias and error rules as hgemm_ex; an unknown layout value is
  * HGEMM_ERR_INVALID_ARG. Operands that TMA can describe (16-byte aligned
  * bases and pitches, N a multiple of 8) go to the tensor-core pair kernel,
- * which reads an M- or N-contiguous operand as MN-major tiles; the others to
- * the generic kernel, which gathers them.
+ * or the split-K kernel where hgemm would take it, which read an M- or
+ * N-contiguous operand as MN-major tiles; the others to the generic kernel,
+ * which gathers them.
  */
 #define HGEMM_A_ROW_MAJOR 0
 #define HGEMM_A_COL_MAJOR 1

@@ -47,6 +47,7 @@ struct SkCfg {
   static constexpr int UNITS = BN / 64;
   static constexpr int ROWS = kTcBM;     // rows per CTA
   static constexpr int BROWS = BN / 2;   // B rows per CTA
+  static_assert(BROWS % kMnBox == 0, "an N-contiguous B arrives in whole 64-column boxes");
   static constexpr int BK = kTcBK;
   static constexpr int STAGES = BN == 256 ? 6 : 8;  // 32 KB or 24 KB per stage
   static constexpr int UMMA_K = 16;
@@ -173,8 +174,22 @@ __global__ void __launch_bounds__(192, 1)
         const uint32_t fb = mapa_shared(full_bar(stage), leader);
         if (rank == leader && !(p.inject == 1 && issued == 0))  // testing aid: withhold one arrival
           mbar_arrive_expect_tx(full_bar(stage), Cfg::TX_BYTES);
-        tma_load_2d_cg2(sA + stage * Cfg::A_BYTES, &tmA, fb, kb * Cfg::BK, ya);
-        tma_load_2d_cg2(sB + stage * Cfg::B_BYTES, &tmB, fb, kb * Cfg::BK, yb);
+        if (p.a_mn) {
+          // A stored K×M: the CTA's 128 rows as two 64-row boxes, 8 KB apart
+          tma_load_2d_cg2(sA + stage * Cfg::A_BYTES, &tmA, fb, ya, kb * Cfg::BK);
+          tma_load_2d_cg2(sA + stage * Cfg::A_BYTES + kMnBoxBytes, &tmA, fb, ya + kMnBox, kb * Cfg::BK);
+        } else {
+          tma_load_2d_cg2(sA + stage * Cfg::A_BYTES, &tmA, fb, kb * Cfg::BK, ya);
+        }
+        if (p.b_mn) {
+          // B stored K×N: the CTA's BROWS columns as 64-column boxes, 8 KB apart
+#pragma unroll
+          for (int bx = 0; bx < Cfg::BROWS; bx += kMnBox)
+            tma_load_2d_cg2(sB + stage * Cfg::B_BYTES + (bx / kMnBox) * kMnBoxBytes, &tmB, fb, yb + bx,
+                            kb * Cfg::BK);
+        } else {
+          tma_load_2d_cg2(sB + stage * Cfg::B_BYTES, &tmB, fb, kb * Cfg::BK, yb);
+        }
         ++issued;
         if (++stage == Cfg::STAGES) {
           stage = 0;
@@ -209,11 +224,17 @@ __global__ void __launch_bounds__(192, 1)
           break;
         }
         tc_fence_after_sync();
-        const uint64_t a_desc = sdesc_kmajor_sw128(sA + stage * Cfg::A_BYTES);
-        const uint64_t b_desc = sdesc_kmajor_sw128(sB + stage * Cfg::B_BYTES);
+        // K-major: 16 K elements are 32 bytes along the row; MN-major: 16 K
+        // rows of 128 bytes
+        const uint64_t a_desc = p.a_mn ? sdesc_mnmajor_sw128(sA + stage * Cfg::A_BYTES)
+                                       : sdesc_kmajor_sw128(sA + stage * Cfg::A_BYTES);
+        const uint64_t b_desc = p.b_mn ? sdesc_mnmajor_sw128(sB + stage * Cfg::B_BYTES)
+                                       : sdesc_kmajor_sw128(sB + stage * Cfg::B_BYTES);
+        const uint32_t a_step = p.a_mn ? 128u : 2u, b_step = p.b_mn ? 128u : 2u;
+        const uint32_t idesc = Cfg::IDESC | idesc_major_bits(p.a_mn != 0, p.b_mn != 0);
 #pragma unroll
         for (int k = 0; k < Cfg::BK / Cfg::UMMA_K; ++k)
-          mma_f16_ss_cg2(tmem_base, a_desc + 2u * k, b_desc + 2u * k, Cfg::IDESC,
+          mma_f16_ss_cg2(tmem_base, a_desc + a_step * k, b_desc + b_step * k, idesc,
                          (kb > kb0 || k > 0) ? 1u : 0u);
         mma_commit_cg2_multicast(empty_bar(stage), pair_mask);
         if (++stage == Cfg::STAGES) {

@@ -41,11 +41,6 @@
 namespace hg {
 namespace {
 
-// MN-major operands (A stored K×M, B stored K×N) arrive in boxes of 64
-// M or N elements (128 bytes, the swizzle width) × 64 K rows.
-constexpr int kMnBox = 64;
-constexpr int kMnBoxBytes = kMnBox * kTcBK * 2;
-
 template <int MAX_STAGES_>
 struct PairCfg {
   static constexpr int BM = 2 * kTcBM;   // cluster tile rows

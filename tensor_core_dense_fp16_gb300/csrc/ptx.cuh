@@ -253,6 +253,8 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr) {
 // k·128), 8-K-row groups 1024 bytes apart (stride byte offset), consecutive
 // 64-element MN boxes 8192 bytes apart (leading byte offset). Stepping K by
 // 16 rows adds 2048 bytes (128 in the address field) to the start address.
+constexpr int kMnBox = 64;                     // MN elements per box (128 bytes)
+constexpr int kMnBoxBytes = kMnBox * 64 * 2;    // one box: 64 K rows of 128 bytes
 __device__ __forceinline__ uint64_t sdesc_mnmajor_sw128(uint32_t saddr) {
   uint64_t d = 0;
   d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);

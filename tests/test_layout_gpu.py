@@ -28,7 +28,7 @@ def stored(x, pad, fill=0.0):
 
 
 def run_layout(a, b, a_layout, b_layout, c_old=None, alpha=1.0, beta=0.0, bias=None, relu=False,
-               pad=(0, 0, 0), path=None):
+               pad=(0, 0, 0), path=None, split=None):
     """a (M, K), b (N, K) in mathematical orientation; returns C (M, N)."""
     torch = torch_cuda()
     M, K = a.shape
@@ -43,11 +43,14 @@ def run_layout(a, b, a_layout, b_layout, c_old=None, alpha=1.0, beta=0.0, bias=N
     dbias = to_device(bias) if bias is not None else None
     if path is not None:
         tc.hgemm_force_path(path)
+    if split is not None:
+        tc.hgemm_force_split(*split)
     try:
         tc.hgemm_layout(a_layout, b_layout, da, a_buf.shape[1], db, b_buf.shape[1], dc, c_buf.shape[1],
                         M, N, K, alpha, beta, dbias, relu)
     finally:
         tc.hgemm_force_path(-1)
+        tc.hgemm_force_split(0, 0)
     assert tc.hgemm_device_status() == tc.HGEMM_OK
     torch.cuda.synchronize()
     out = dc.cpu().numpy()
@@ -81,6 +84,27 @@ def test_layout_pitches(layout, pad):
     a, b = synth.operands(M, N, K, seed=5 + pad[0], kind="uniform")
     ref = oracle.hgemm(a, b, nthreads=oracle_threads())
     assert_close(run_layout(a, b, *layout, pad=pad), ref, what=f"{NAMES[layout]} pad {pad}")
+
+
+@pytest.mark.parametrize("layout", LAYOUTS, ids=lambda l: NAMES[l])
+@pytest.mark.parametrize("split", [(2, 128), (2, 256), (3, 256), (4, 256)], ids=lambda s: f"{s[0]}x{s[1]}")
+def test_layout_split_k(layout, split):
+    """The split-K cluster kernel reads M- and N-contiguous operands too
+    (ragged M, K not a multiple of the slices)."""
+    M, N, K = 1000, 512, 4000
+    a, b = synth.operands(M, N, K, seed=17 + split[0], kind="uniform")
+    ref = oracle.hgemm(a, b, nthreads=oracle_threads())
+    got = run_layout(a, b, *layout, path=tc.HGEMM_PATH_SKINNY, split=split)
+    assert_close(got, ref, what=f"{NAMES[layout]} split {split}")
+
+
+@pytest.mark.parametrize("layout", LAYOUTS, ids=lambda l: NAMES[l])
+def test_layout_skinny_shape(layout):
+    """The 4096×256×4096 shape (the TRMM page's update) takes split-K in every layout."""
+    M, N, K = 4096, 256, 4096
+    a, b = synth.operands(M, N, K, seed=1004, kind="uniform")
+    ref = oracle.hgemm(a, b, nthreads=oracle_threads())
+    assert_close(run_layout(a, b, *layout), ref, what=f"{NAMES[layout]} skinny")
 
 
 @pytest.mark.parametrize("layout", LAYOUTS, ids=lambda l: NAMES[l])
