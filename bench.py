@@ -597,11 +597,11 @@ def run_ours(args, spec, a, b, world, rank, local):
     epi = EPILOGUES[args.epilogue]
     if layouts:
         # M- or N-contiguous operands take the path of the same shape in the
-        # default layout, except that the wide and single-CTA kernels read
-        # K-major operands only (the pair kernel stands in for them)
+        # default layout, except that the single-CTA kernel reads K-major
+        # operands only (the pair kernel stands in for it)
         tma = lda % 8 == 0 and ldb % 8 == 0 and N % 8 == 0
         path = tc.hgemm_select_path(da, db, dc, M, N, K) if tma else tc.HGEMM_PATH_GENERIC
-        if path in (tc.HGEMM_PATH_TC_WIDE, tc.HGEMM_PATH_TC):
+        if path == tc.HGEMM_PATH_TC:
             path = tc.HGEMM_PATH_TC_PAIR
     else:
         path = tc.hgemm_select_path(da, db, dc, M, N, K)

@@ -151,10 +151,10 @@ HGEMM_API int hgemm_strided(const hgemm_half_t *A, int64_t lda, const hgemm_half
  * C(i,j) at C[i·ldc + j] always. Same epilogue (alpha, beta, bias, relu),
  * ownership, alias and error rules as hgemm_ex; an unknown layout value is
  * HGEMM_ERR_INVALID_ARG. Operands that TMA can describe (16-byte aligned
- * bases and pitches, N a multiple of 8) go to the tensor-core pair kernel,
- * or the split-K kernel where hgemm would take it, which read an M- or
- * N-contiguous operand as MN-major tiles; the others to the generic kernel,
- * which gathers them.
+ * bases and pitches, N a multiple of 8) take the tensor-core path hgemm
+ * would take for the shape (the pair kernel where that is the single-CTA
+ * one), reading an M- or N-contiguous operand as MN-major tiles; the others
+ * go to the generic kernel, which gathers them.
  */
 #define HGEMM_A_ROW_MAJOR 0
 #define HGEMM_A_COL_MAJOR 1

@@ -175,10 +175,9 @@ int choose_path(const Gemm& g, const hg::DeviceProfile& prof, bool fused, int* s
   if (forced == HGEMM_PATH_GENERIC || !tma) return HGEMM_PATH_GENERIC;
   const int fs = g_forced_split.load(std::memory_order_relaxed);
   const int path = hg::choose_tma_path(M, N, K, prof, forced, fs >> 10, fs & 1023, fused, split, tile_n);
-  // M- or N-contiguous operands: the pair and split-K kernels read them as
-  // MN-major tiles; the wide and single-CTA kernels take K-major ones only
-  if ((g.a_mn || g.b_mn) && (path == HGEMM_PATH_TC_WIDE || path == HGEMM_PATH_TC))
-    return HGEMM_PATH_TC_PAIR;
+  // M- or N-contiguous operands: the wide, pair and split-K kernels read
+  // them as MN-major tiles; the single-CTA kernel takes K-major ones only
+  if ((g.a_mn || g.b_mn) && path == HGEMM_PATH_TC) return HGEMM_PATH_TC_PAIR;
   return path;
 }
 
@@ -421,8 +420,13 @@ int run_tc_wide(const Gemm& g, const hg::EpiArgs& epi, const DeviceState& dev,
   const int64_t M = g.M, N = g.N, K = g.K;
   CUtensorMap ma, mb, mc;
   int rc;
-  if ((rc = encode_map(&ma, A, M, K, g.lda, hg::kTcBM, hg::kTcBK)) != HGEMM_OK) return rc;
-  if ((rc = encode_map(&mb, B, N, K, g.ldb, hg::kPairBN / 2, hg::kTcBK)) != HGEMM_OK) return rc;
+  // MN-major operands: boxes of 64 M or N elements × 64 K rows
+  if ((rc = g.a_mn ? encode_map(&ma, A, K, M, g.lda, hg::kTcBK, 64)
+                   : encode_map(&ma, A, M, K, g.lda, hg::kTcBM, hg::kTcBK)) != HGEMM_OK)
+    return rc;
+  if ((rc = g.b_mn ? encode_map(&mb, B, K, N, g.ldb, hg::kTcBK, 64)
+                   : encode_map(&mb, B, N, K, g.ldb, hg::kPairBN / 2, hg::kTcBK)) != HGEMM_OK)
+    return rc;
   if ((rc = encode_map(&mc, C, M, N, g.ldc, hg::kEpiRows, hg::kEpiCols)) != HGEMM_OK) return rc;
   hg::TcArgs args{};
   args.M = static_cast<int>(M);
@@ -444,6 +448,8 @@ int run_tc_wide(const Gemm& g, const hg::EpiArgs& epi, const DeviceState& dev,
   args.epi = epi;
   args.C = static_cast<const uint16_t*>(C);
   args.ldc = g.ldc;
+  args.a_mn = g.a_mn ? 1 : 0;
+  args.b_mn = g.b_mn ? 1 : 0;
   cudaError_t e = hg::launch_tc_wide(ma, mb, mc, args, stream);
   return e == cudaSuccess ? HGEMM_OK : cuda_fail(e);
 }

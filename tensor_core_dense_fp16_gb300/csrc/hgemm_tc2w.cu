@@ -71,7 +71,9 @@ struct WideCfg {
   static_assert(SMEM_BYTES <= 232448, "exceeds 227 KB of shared memory per CTA");
 };
 
-template <bool FUSED>
+// MN: the instantiation that also reads M-contiguous A or N-contiguous B
+// (p.a_mn, p.b_mn) as MN-major tiles; the other one takes K-major operands.
+template <bool FUSED, bool MN>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
     hgemm_tc2w_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const __grid_constant__ CUtensorMap tmC, const TcArgs p) {
@@ -151,9 +153,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
           if (rank == 0 && !(p.inject == 1 && issued == 0))  // testing aid: withhold one arrival
             mbar_arrive_expect_tx(full_bar(stage), Cfg::TX_BYTES);
           const uint32_t sb = sB + stage * Cfg::B_BYTES;
-          tma_load_2d_cg2(sA + stage * Cfg::A_BYTES, &tmA, fb, kb * Cfg::BK, ya);
-          tma_load_2d_cg2(sb, &tmB, fb, kb * Cfg::BK, yb);
-          tma_load_2d_cg2(sb + Cfg::BH_BYTES, &tmB, fb, kb * Cfg::BK, yb + kPairBN);
+          if (MN && p.a_mn) {
+            // A stored K×M: the CTA's 128 rows as two 64-row boxes, 8 KB apart
+            tma_load_2d_cg2(sA + stage * Cfg::A_BYTES, &tmA, fb, ya, kb * Cfg::BK);
+            tma_load_2d_cg2(sA + stage * Cfg::A_BYTES + kMnBoxBytes, &tmA, fb, ya + kMnBox, kb * Cfg::BK);
+          } else {
+            tma_load_2d_cg2(sA + stage * Cfg::A_BYTES, &tmA, fb, kb * Cfg::BK, ya);
+          }
+          if (MN && p.b_mn) {
+            // B stored K×N: each half's 128 columns as two 64-column boxes
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              tma_load_2d_cg2(sb + h * Cfg::BH_BYTES, &tmB, fb, yb + h * kPairBN, kb * Cfg::BK);
+              tma_load_2d_cg2(sb + h * Cfg::BH_BYTES + kMnBoxBytes, &tmB, fb, yb + h * kPairBN + kMnBox,
+                              kb * Cfg::BK);
+            }
+          } else {
+            tma_load_2d_cg2(sb, &tmB, fb, kb * Cfg::BK, yb);
+            tma_load_2d_cg2(sb + Cfg::BH_BYTES, &tmB, fb, kb * Cfg::BK, yb + kPairBN);
+          }
           ++issued;
           if (++stage == STAGES) {
             stage = 0;
@@ -192,7 +210,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
             break;
           }
           tc_fence_after_sync();
-          const uint64_t a_desc = sdesc_kmajor_sw128(sA + stage * Cfg::A_BYTES);
+          // K-major: 16 K elements are 32 bytes along the row; MN-major: 16 K
+          // rows of 128 bytes
+          const bool a_mn = MN && p.a_mn, b_mn = MN && p.b_mn;
+          const uint64_t a_desc = a_mn ? sdesc_mnmajor_sw128(sA + stage * Cfg::A_BYTES)
+                                       : sdesc_kmajor_sw128(sA + stage * Cfg::A_BYTES);
+          const uint32_t a_step = a_mn ? 128u : 2u, b_step = b_mn ? 128u : 2u;
+          const uint32_t idesc = Cfg::IDESC | idesc_major_bits(a_mn, b_mn);
           const uint32_t sb = sB + stage * Cfg::B_BYTES;
           for (int h = 0; h < 2; ++h) {
             if (kb == 0) {
@@ -203,12 +227,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
               }
               tc_fence_after_sync();
             }
-            const uint64_t b_desc = sdesc_kmajor_sw128(sb + h * Cfg::BH_BYTES);
+            const uint64_t b_desc = b_mn ? sdesc_mnmajor_sw128(sb + h * Cfg::BH_BYTES)
+                                         : sdesc_kmajor_sw128(sb + h * Cfg::BH_BYTES);
             const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(h * Cfg::HALF_COLS);
 #pragma unroll
             for (int k = 0; k < Cfg::BK / Cfg::UMMA_K; ++k)
               // kb counts K steps in load order; the first one overwrites
-              mma_f16_ss_cg2(d_tmem, a_desc + 2u * k, b_desc + 2u * k, Cfg::IDESC,
+              mma_f16_ss_cg2(d_tmem, a_desc + a_step * k, b_desc + b_step * k, idesc,
                              (kb > 0 || k > 0) ? 1u : 0u);
           }
           if (!ok) break;
@@ -297,13 +322,13 @@ int wide_max_clusters(int num_sms) {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return num_sms / 2;
   if (cached[dev] > 0) return cached[dev];
   int n = 0;
-  if (cudaFuncSetAttribute(hgemm_tc2w_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(hgemm_tc2w_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            WideCfg::SMEM_BYTES) == cudaSuccess) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(num_sms & ~1));
     cfg.blockDim = dim3(WideCfg::THREADS);
     cfg.dynamicSmemBytes = WideCfg::SMEM_BYTES;
-    if (cudaOccupancyMaxActiveClusters(&n, hgemm_tc2w_kernel<false>, &cfg) != cudaSuccess) n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, hgemm_tc2w_kernel<false, false>, &cfg) != cudaSuccess) n = 0;
   }
   (void)cudaGetLastError();
   if (n <= 0) n = num_sms / 2;
@@ -313,16 +338,18 @@ int wide_max_clusters(int num_sms) {
 
 cudaError_t launch_tc_wide(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
                            const TcArgs& args, cudaStream_t stream) {
-  static bool attr_done[2][64] = {};
+  static bool attr_done[4][64] = {};
   const int fused = args.epi.mode != 0 ? 1 : 0;
-  auto kern = fused ? hgemm_tc2w_kernel<true> : hgemm_tc2w_kernel<false>;
+  const int mn = (args.a_mn || args.b_mn) ? 1 : 0;
+  auto kern = mn ? (fused ? hgemm_tc2w_kernel<true, true> : hgemm_tc2w_kernel<false, true>)
+                 : (fused ? hgemm_tc2w_kernel<true, false> : hgemm_tc2w_kernel<false, false>);
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64 || !attr_done[fused][dev]) {
+  if (dev < 0 || dev >= 64 || !attr_done[2 * mn + fused][dev]) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, WideCfg::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) attr_done[fused][dev] = true;
+    if (dev >= 0 && dev < 64) attr_done[2 * mn + fused][dev] = true;
   }
   PdlLaunch l(dim3(static_cast<unsigned>(args.grid)), dim3(WideCfg::THREADS), WideCfg::SMEM_BYTES, stream);
   return cudaLaunchKernelEx(&l.cfg, kern, a, b, c, args);

@@ -87,6 +87,25 @@ def test_layout_pitches(layout, pad):
 
 
 @pytest.mark.parametrize("layout", LAYOUTS, ids=lambda l: NAMES[l])
+@pytest.mark.parametrize("path", [tc.HGEMM_PATH_TC_PAIR, tc.HGEMM_PATH_TC_WIDE], ids=["pair", "wide"])
+@pytest.mark.parametrize("M,N,K", [(1000, 520, 384), (513, 1032, 200)])
+def test_layout_forced_tensor_core_paths(layout, path, M, N, K):
+    """The pair and wide kernels read MN-major tiles, with ragged edges."""
+    a, b = synth.operands(M, N, K, seed=M + 3 * N, kind="uniform")
+    ref = oracle.hgemm(a, b, nthreads=oracle_threads())
+    assert_close(run_layout(a, b, *layout, path=path), ref, what=f"{NAMES[layout]} path {path}")
+
+
+@pytest.mark.parametrize("layout", LAYOUTS, ids=lambda l: NAMES[l])
+def test_layout_wide_chosen(layout):
+    """A shape with a 256×512 tile for every SM pair: the wide kernel, ragged in M and N."""
+    M, N, K = 4000, 4104, 1000
+    a, b = synth.operands(M, N, K, seed=4000, kind="uniform")
+    ref = oracle.hgemm(a, b, nthreads=oracle_threads())
+    assert_close(run_layout(a, b, *layout), ref, what=f"{NAMES[layout]} wide")
+
+
+@pytest.mark.parametrize("layout", LAYOUTS, ids=lambda l: NAMES[l])
 @pytest.mark.parametrize("split", [(2, 128), (2, 256), (3, 256), (4, 256)], ids=lambda s: f"{s[0]}x{s[1]}")
 def test_layout_split_k(layout, split):
     """The split-K cluster kernel reads M- and N-contiguous operands too
@@ -128,15 +147,19 @@ def test_layout_fused_epilogue(layout):
     assert_close(got, ref, what=f"{NAMES[layout]} fused")
 
 
-def test_row_major_b_4096_sampled():
-    """A 4096-cube with B row-major (the CUDA chapter's layout), sampled rows
-    and columns against the oracle's single entries."""
+@pytest.mark.parametrize("layout", LAYOUTS[1:], ids=lambda l: NAMES[l])
+def test_layout_4096_sampled(layout):
+    """A 4096-cube (the wide kernel) in the other layouts, sampled rows and
+    columns against the oracle's single entries."""
     torch = torch_cuda()
     M = N = K = 4096
     a, b = synth.operands(M, N, K, seed=1234, kind="normal")
-    da, db = to_device(a), to_device(np.ascontiguousarray(b.T))
+    a_l, b_l = layout
+    da = to_device(np.ascontiguousarray(a.T) if a_l == tc.HGEMM_A_COL_MAJOR else a)
+    db = to_device(np.ascontiguousarray(b.T) if b_l == tc.HGEMM_B_ROW_MAJOR else b)
     dc = torch.empty((M, N), dtype=torch.float16, device="cuda")
-    tc.hgemm_layout(tc.HGEMM_A_ROW_MAJOR, tc.HGEMM_B_ROW_MAJOR, da, K, db, N, dc, N, M, N, K)
+    tc.hgemm_layout(a_l, b_l, da, M if a_l == tc.HGEMM_A_COL_MAJOR else K, db,
+                    N if b_l == tc.HGEMM_B_ROW_MAJOR else K, dc, N, M, N, K)
     assert tc.hgemm_device_status() == tc.HGEMM_OK
     torch.cuda.synchronize()
     rng = np.random.default_rng(3)
@@ -145,5 +168,5 @@ def test_row_major_b_4096_sampled():
     rr, cc = np.meshgrid(rows, cols, indexing="ij")
     got = dc.cpu().numpy()[rr, cc]
     ref = oracle.entries(a, b, rr.ravel(), cc.ravel()).reshape(rr.shape)
-    assert_close(got, ref, what="4096 B row-major sampled")
+    assert_close(got, ref, what=f"4096 {NAMES[layout]} sampled")
 
