@@ -21,6 +21,8 @@
 //     FP32 accumulator in TMEM;
 //   * warps 4–7 read the accumulator with tcgen05.ld, round to FP16 and store
 //     each in-range element (C need not be aligned beyond 2 bytes).
+#include <atomic>
+
 #include <cuda_fp16.h>
 
 #include "internal.h"
@@ -309,7 +311,7 @@ __global__ void __launch_bounds__(GenCfg::THREADS, 2)
 }
 
 template <typename Kern>
-cudaError_t prepare(Kern kern, bool* done) {
+cudaError_t prepare(Kern kern, std::atomic<bool>* done) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -324,7 +326,7 @@ cudaError_t prepare(Kern kern, bool* done) {
 }  // namespace
 
 cudaError_t launch_tri_leaves(const PlainArgs& args, const TriLeaves& leaves, cudaStream_t stream) {
-  static bool attr_done[64] = {};
+  static std::atomic<bool> attr_done[64];
   cudaError_t e = prepare(hgemm_tri_leaves_kernel, attr_done);
   if (e != cudaSuccess) return e;
   if (leaves.count < 1 || leaves.count > kMaxLeaves) return cudaErrorInvalidValue;
@@ -339,7 +341,7 @@ cudaError_t launch_tri_leaves(const PlainArgs& args, const TriLeaves& leaves, cu
 }
 
 cudaError_t launch_generic(const PlainArgs& args, int /*num_sms*/, cudaStream_t stream) {
-  static bool attr_done[64] = {};
+  static std::atomic<bool> attr_done[64];
   cudaError_t e = prepare(hgemm_generic_kernel, attr_done);
   if (e != cudaSuccess) return e;
   const int64_t tiles_n = (args.N + GenCfg::BN - 1) / GenCfg::BN;

@@ -27,6 +27,8 @@
 //     and TMA-stores its block of C, and acknowledges, so that no copy
 //     touches a CTA that has left.
 // No global scratch memory is used.
+#include <atomic>
+
 #include <cuda_fp16.h>
 
 #include "internal.h"
@@ -401,7 +403,7 @@ template <int SPLIT, int BN>
 cudaError_t launch_split(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
                          const TcArgs& args, cudaStream_t stream) {
   using Cfg = SkCfg<SPLIT, BN>;
-  static bool attr_done[2][64] = {};
+  static std::atomic<bool> attr_done[2][64];
   const int fused = args.epi.mode != 0 ? 1 : 0;
   auto kern = fused ? hgemm_skinny_kernel<SPLIT, BN, true> : hgemm_skinny_kernel<SPLIT, BN, false>;
   int dev = 0;

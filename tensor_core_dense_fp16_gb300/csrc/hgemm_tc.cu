@@ -25,6 +25,8 @@
 //   * Every mbarrier wait is bounded in time; a wait that gives up records a
 //     code in the device watchdog word, raises a CTA-wide abort flag, and the
 //     kernel drains its in-flight copies and MMAs, frees TMEM and returns.
+#include <atomic>
+
 #include <cuda_fp16.h>
 
 #include "internal.h"
@@ -305,7 +307,7 @@ __global__ void empty_sum_kernel(uint16_t* __restrict__ C, int64_t M, int64_t N,
 }
 
 template <typename Kern>
-cudaError_t ensure_smem_attr(Kern kern, int bytes, bool* done_per_device) {
+cudaError_t ensure_smem_attr(Kern kern, int bytes, std::atomic<bool>* done_per_device) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -320,7 +322,7 @@ cudaError_t ensure_smem_attr(Kern kern, int bytes, bool* done_per_device) {
 cudaError_t launch_tc_128x256(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
                               const TcArgs& args, cudaStream_t stream) {
   using Cfg = TcCfg<256, 4>;
-  static bool attr_done[2][64] = {};
+  static std::atomic<bool> attr_done[2][64];
   const bool fused = args.epi.mode != 0;
   auto kern = fused ? hgemm_tc_kernel<256, 4, true> : hgemm_tc_kernel<256, 4, false>;
   cudaError_t e = ensure_smem_attr(kern, Cfg::SMEM_BYTES, attr_done[fused ? 1 : 0]);

@@ -32,6 +32,8 @@
 // Serpentine K: rounds of tiles alternate the direction in which they walk
 // K, so each round starts on operand blocks that the previous round read
 // last and that are still in L2 (measured: ~25% less DRAM traffic).
+#include <atomic>
+
 #include <cuda_fp16.h>
 
 #include "internal.h"
@@ -354,7 +356,7 @@ constexpr int kPairStages = 10;  // barriers for up to ten stages (the ring hold
 
 int pair_max_clusters(int num_sms) {
   using Cfg = PairCfg<kPairStages>;
-  static int cached[64] = {};
+  static std::atomic<int> cached[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return num_sms / 2;
   if (cached[dev] > 0) return cached[dev];
@@ -377,7 +379,7 @@ int pair_max_clusters(int num_sms) {
 cudaError_t launch_tc_pair(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b_part,
                            const CUtensorMap& c, const TcArgs& args, cudaStream_t stream) {
   using Cfg = PairCfg<kPairStages>;
-  static bool attr_done[2][64] = {};
+  static std::atomic<bool> attr_done[2][64];
   const int fused = args.epi.mode != 0 ? 1 : 0;
   auto kern = fused ? hgemm_tc2_kernel<kPairStages, true> : hgemm_tc2_kernel<kPairStages, false>;
   int dev = 0;

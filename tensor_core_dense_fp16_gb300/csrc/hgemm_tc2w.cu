@@ -27,6 +27,8 @@
 //     pause of the tensor cores between tiles, and two warps per quadrant
 //     halve it (measured: +0.5% at 8192³, +1.6% at 4096³);
 //   * serpentine K, epilogue, edges and watchdog as in hgemm_tc2.cu.
+#include <atomic>
+
 #include <cuda_fp16.h>
 
 #include "internal.h"
@@ -317,7 +319,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
 }  // namespace
 
 int wide_max_clusters(int num_sms) {
-  static int cached[64] = {};
+  static std::atomic<int> cached[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return num_sms / 2;
   if (cached[dev] > 0) return cached[dev];
@@ -338,7 +340,7 @@ int wide_max_clusters(int num_sms) {
 
 cudaError_t launch_tc_wide(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
                            const TcArgs& args, cudaStream_t stream) {
-  static bool attr_done[4][64] = {};
+  static std::atomic<bool> attr_done[4][64];
   const int fused = args.epi.mode != 0 ? 1 : 0;
   const int mn = (args.a_mn || args.b_mn) ? 1 : 0;
   auto kern = mn ? (fused ? hgemm_tc2w_kernel<true, true> : hgemm_tc2w_kernel<false, true>)

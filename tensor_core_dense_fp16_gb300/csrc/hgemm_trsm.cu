@@ -11,8 +11,9 @@
 // so the block is solved by back substitution, last row first.
 //
 // Leaf solve (§2.3: the right-hand sides spread over thread blocks, a light
-// barrier between steps): thread r of a block owns row r of the diagonal
-// block for COLS right-hand sides, in registers. The rows are taken in groups
+// barrier between steps): warp w of a block owns rows 32w .. 32w+31 of the
+// diagonal block for COLS right-hand sides, in registers (the accumulator
+// fragments of the tensor-core update below). The rows are taken in groups
 // of 32 (one warp's rows), last group first. A group's own 32×32 triangle
 // L_g is applied through its inverse, which warp g computes in FP32 at the
 // start (forward substitution on the columns of the identity), so that the
@@ -29,6 +30,8 @@
 // Launch overlap: the inverses only read A, which no launch of the solve
 // writes, so they are computed before the kernel waits for the previous
 // launch on the stream (griddepcontrol.wait) and read X.
+#include <atomic>
+
 #include <cuda_fp16.h>
 
 #include "internal.h"
@@ -322,7 +325,7 @@ __global__ void scale_copy_kernel(const uint16_t* B, int64_t ldb, uint16_t* X, i
 }
 
 // Resident blocks per SM of each width, measured once per device (0: not yet).
-int g_resident[kMaxDevices][3] = {};
+std::atomic<int> g_resident[kMaxDevices][3];
 
 template <int COLS>
 cudaError_t launch_width(const uint16_t* A, int64_t lda, uint16_t* X, int64_t ldx, int64_t off,
@@ -351,7 +354,7 @@ cudaError_t launch_trsm_leaf(const uint16_t* A, int64_t lda, uint16_t* X, int64_
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  int* res = g_resident[dev];
+  std::atomic<int>* res = g_resident[dev];
   if (res[0] == 0) {
     int r8 = 0, r16 = 0, r32 = 0;
     if ((e = resident_blocks<8>(&r8)) != cudaSuccess || (e = resident_blocks<16>(&r16)) != cudaSuccess ||
