@@ -712,7 +712,7 @@ int hgemm_trmm(const hgemm_half_t* A, int64_t lda, const hgemm_half_t* B, int64_
   hg::PlainArgs pa{reinterpret_cast<const uint16_t*>(B), reinterpret_cast<const uint16_t*>(A),
                    reinterpret_cast<uint16_t*>(C), m, n, n, ldb, lda, ldc,
                    dev->status, g_timeout_ns.load(), scale};
-  cudaError_t e = hg::launch_tri_leaves(pa, leaves, stream);
+  cudaError_t e = hg::launch_tri_leaves(pa, leaves, dev->num_sms, stream);
   if (e != cudaSuccess) return cuda_fail(e);
 
   // Updates, deepest level first: an update reads the first half of its

@@ -127,7 +127,8 @@ cudaError_t launch_empty_sum(uint16_t* C, int64_t M, int64_t N, int64_t ldc, con
 cudaError_t launch_generic(const PlainArgs& args, int num_sms, cudaStream_t stream);
 // Every leaf b: C + off = (A operand + off) · lower(B operand at (off, off)),
 // M × size (see hgemm_generic.cu).
-cudaError_t launch_tri_leaves(const PlainArgs& args, const TriLeaves& leaves, cudaStream_t stream);
+cudaError_t launch_tri_leaves(const PlainArgs& args, const TriLeaves& leaves, int num_sms,
+                              cudaStream_t stream);
 
 // Triangular solve Aᵀ·X = alpha·B (see hgemm_trsm.cu): the largest diagonal
 // block solved by substitution; X(:, j) = alpha·B(:, j) over n × m
