@@ -11,12 +11,13 @@
 // Design: persistent CTAs, two per SM, each walking 128×128 output tiles
 // (units) blockIdx.x, blockIdx.x + gridDim.x, ...:
 //   * warps 0–3 (128 threads) are the loaders: thread t copies row t of the
-//     A tile and row t of the B tile for one 64-wide K block with
-//     bounds-checked loads (16-byte when a whole aligned block, else 2-byte;
-//     gathers for M- or N-contiguous operands) and writes them, 16 bytes at a
-//     time, into the same 128-byte-swizzled K-major layout that a TMA copy
-//     would produce; a 3-stage ring that runs on across units, one barrier
-//     arrival per warp;
+//     A tile and row t of the B tile for one 64-wide K block into the same
+//     128-byte-swizzled K-major layout that a TMA copy would produce (zero
+//     outside the matrices): by asynchronous 16-byte copies (cp.async, two K
+//     blocks in flight per thread) when the row starts are 16-byte aligned,
+//     else through registers with bounds-checked 2-byte loads (and gathers
+//     for M- or N-contiguous operands); a 3-stage ring that runs on across
+//     units, one barrier arrival per warp;
 //   * warp 8 (one thread) issues tcgen05.mma (M=128, N=128, K=16) into one of
 //     two FP32 accumulators in TMEM (2 × 128 columns: two CTAs fill TMEM);
 //   * warps 4–7 drain the other accumulator meanwhile with tcgen05.ld, round
@@ -116,6 +117,52 @@ __device__ __forceinline__ void load_row_gather(const uint16_t* __restrict__ src
   }
 }
 
+// Row r of a K block by asynchronous 16-byte copies into the
+// 128-byte-swizzled K-major row r of a shared-memory tile: `n` valid values
+// from `src` (16-byte aligned), zero-filled past them; chunks of 8 values all
+// below `first` (a triangular mask) are zeroed instead of copied. Returns the
+// chunk that holds `first` when it is partially masked (its leading
+// first - 8·chunk values must be zeroed once the copies have landed), else -1.
+__device__ __forceinline__ int issue_row_async(const uint16_t* __restrict__ src, int n, uint8_t* tile, int r,
+                                               int first) {
+  uint8_t* row = tile + r * 128;
+  int fix = -1;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    uint8_t* dst = row + ((j ^ (r & 7)) << 4);
+    int valid = n - 8 * j;
+    valid = valid < 0 ? 0 : (valid > 8 ? 8 : valid);
+    if (8 * j + 8 <= first) valid = 0;
+    if (valid == 0) {
+      *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+      continue;
+    }
+    cp_async_16(smem_u32(dst), src + 8 * j, 2 * valid);
+    if (8 * j < first) fix = j;
+  }
+  return fix;
+}
+
+// Zeroes the first `count` values of chunk j of swizzled row r.
+__device__ __forceinline__ void zero_leading(uint8_t* tile, int r, int j, int count) {
+  uint32_t* w = reinterpret_cast<uint32_t*>(tile + r * 128 + ((j ^ (r & 7)) << 4));
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    if (2 * u + 1 < count)
+      w[u] = 0u;
+    else if (2 * u < count)
+      w[u] &= 0xFFFF0000u;
+  }
+}
+
+// A K block whose copies are in flight: its ring stage and the chunk of its
+// B row a triangular mask must still fix (-1: none).
+struct PendingBlock {
+  int stage;
+  int fix_j;
+  int fix_cnt;
+};
+
 // Work unit t of a launch: the 128×128 tile of C at (m0, n0) over num_kb K
 // blocks, with the operands it reads. Units are numbered tile by tile, N
 // tiles fastest (neighbouring units share their rows of A); for the leaves of
@@ -207,14 +254,36 @@ __device__ __forceinline__ void generic_units(const PlainArgs& p, const TriLeave
 
   if (warp < Cfg::LOADER_WARPS) {
     // ------------------------------------------------------------ loaders
+    // Rows with 16-byte aligned starts (K-contiguous operand, aligned base
+    // and pitch) go by asynchronous copies, kInFlight K blocks in flight per
+    // thread: a block is published (fence to the async proxy, one arrival
+    // per warp) once its copies have landed and a triangular mask has
+    // zeroed its leading values. Other rows go through registers.
+    constexpr int kInFlight = Cfg::STAGES - 1;
     const int r = threadIdx.x;  // tile row 0..127
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
+    static_assert(kInFlight == 2, "two pending blocks: older and newer");
+    PendingBlock older{0, -1, 0}, newer{0, -1, 0};
+    int npend = 0;
+    // the older pending block: its copies are complete (the caller waited)
+    auto publish_oldest = [&]() {
+      if (older.fix_j >= 0)
+        zero_leading(smem + Cfg::OFF_B + older.stage * Cfg::B_BYTES, r, older.fix_j, older.fix_cnt);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(full_bar(older.stage));
+      older = newer;
+      --npend;
+    };
     for (int64_t t = blockIdx.x; ok && t < units; t += gridDim.x) {
       const GenUnit u = gen_unit<TRI_B>(p, leaves, t, tiles_m, tiles_n);
       if (!u.valid) continue;
       const int64_t gi = u.m0 + r, gj = u.n0 + r;
+      const bool a_async = !u.q.a_mn && ((reinterpret_cast<uintptr_t>(u.q.A) & 15u) == 0) && u.q.lda % 8 == 0;
+      const bool b_async = (TRI_B || !u.q.b_mn) && ((reinterpret_cast<uintptr_t>(u.q.B) & 15u) == 0) &&
+                           u.q.ldb % 8 == 0;
       for (int kb = 0; kb < u.num_kb; ++kb) {
         int good = 1;
         if (lane == 0) good = wait_phase(empty_bar(stage), phase ^ 1u, wd, kWdProducerEmpty) ? 1 : 0;
@@ -227,28 +296,51 @@ __device__ __forceinline__ void generic_units(const PlainArgs& p, const TriLeave
         const int64_t kn = u.q.K - k0 < Cfg::BK ? u.q.K - k0 : Cfg::BK;
         uint8_t* sa = smem + Cfg::OFF_A + stage * Cfg::A_BYTES;
         uint8_t* sb = smem + Cfg::OFF_B + stage * Cfg::B_BYTES;
+        const int na = gi < u.q.M ? static_cast<int>(kn) : 0;
+        const int nb = gj < u.q.N ? static_cast<int>(kn) : 0;
         if (u.q.a_mn)
-          load_row_gather(u.q.A + k0 * u.q.lda + gi, u.q.lda, gi < u.q.M ? static_cast<int>(kn) : 0, sa, r);
+          load_row_gather(u.q.A + k0 * u.q.lda + gi, u.q.lda, na, sa, r);
+        else if (a_async)
+          issue_row_async(u.q.A + gi * u.q.lda + k0, na, sa, r, 0);
         else
-          load_row_swizzled(u.q.A + gi * u.q.lda + k0, gi < u.q.M ? static_cast<int>(kn) : 0, sa, r);
+          load_row_swizzled(u.q.A + gi * u.q.lda + k0, na, sa, r);
         int first = 0;
         if constexpr (TRI_B) {
           const int64_t f = gj - k0;
           first = f <= 0 ? 0 : (f >= Cfg::BK ? Cfg::BK : static_cast<int>(f));
         }
-        if (!TRI_B && u.q.b_mn)
-          load_row_gather(u.q.B + k0 * u.q.ldb + gj, u.q.ldb, gj < u.q.N ? static_cast<int>(kn) : 0, sb, r);
+        PendingBlock b{stage, -1, 0};
+        if (!TRI_B && u.q.b_mn) {
+          load_row_gather(u.q.B + k0 * u.q.ldb + gj, u.q.ldb, nb, sb, r);
+        } else if (b_async) {
+          const int fj = issue_row_async(u.q.B + gj * u.q.ldb + k0, nb, sb, r, first);
+          if (fj >= 0) {
+            b.fix_j = fj;
+            b.fix_cnt = first - 8 * fj;
+          }
+        } else {
+          load_row_swizzled(u.q.B + gj * u.q.ldb + k0, nb, sb, r, first);
+        }
+        cp_async_commit();
+        if (npend == 0)
+          older = b;
         else
-          load_row_swizzled(u.q.B + gj * u.q.ldb + k0, gj < u.q.N ? static_cast<int>(kn) : 0, sb, r, first);
-        fence_proxy_async_smem();  // generic-proxy writes before tensor-core reads
-        __syncwarp();
-        if (lane == 0) mbar_arrive(full_bar(stage));
+          newer = b;
+        ++npend;
+        if (npend == kInFlight) {
+          cp_async_wait<kInFlight - 1>();
+          publish_oldest();
+        }
         if (++stage == Cfg::STAGES) {
           stage = 0;
           phase ^= 1u;
         }
       }
     }
+    // the blocks still in flight (after a failed wait too: their copies must
+    // land before the CTA's shared memory goes away)
+    cp_async_wait<0>();
+    while (npend > 0) publish_oldest();
   } else if (warp == Cfg::MMA_WARP) {
     // -------------------------------------------------------- MMA issuer
     if (lane == 0) {

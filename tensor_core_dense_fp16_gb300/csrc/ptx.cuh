@@ -131,6 +131,19 @@ __device__ __forceinline__ void bulk_wait_group() {
 
 // Orders this thread's generic-proxy shared-memory writes before later
 // async-proxy (TMA) reads of them.
+// Asynchronous 16-byte copy global -> shared (L2 only), reading src_bytes
+// (0..16) and zero-filling the rest; both addresses 16-byte aligned.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Waits until at most N of this thread's committed copy groups are pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
