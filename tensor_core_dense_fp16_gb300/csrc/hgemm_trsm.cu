@@ -22,8 +22,8 @@
 // owning warp publishes its b, barrier, all threads form x_g (FP32),
 // barrier, and every warp above the group subtracts Σ_c A(c,r)·x_c over the
 // group's rows on the tensor cores (mma.sync m16n8k16: A(c0 .. c0+31, r),
-// contiguous in the column-major A, read from global memory before the
-// group's barriers; x_g rounded to FP16, as the recursion's GEMM updates see
+// contiguous in the column-major A, copied a group ahead into shared memory
+// and read back with ldmatrix; x_g rounded to FP16, as the recursion's GEMM updates see
 // X; FP32 accumulators holding the right-hand sides). The solution is
 // rounded once to FP16.
 //
@@ -56,9 +56,24 @@ __host__ __device__ constexpr int pub_pitch() {
 // padding spreads a warp's 32-bit fragment loads over all banks.
 constexpr int KP = kGroup + 8;
 
+// Halves per row of the staged A segments (32 values + 8 of padding: the
+// 80-byte pitch puts the 8 rows of an ldmatrix load in different banks).
+constexpr int AP = kGroup + 8;
+
 template <int COLS>
 constexpr int leaf_smem() {
-  return kGroups * kGroup * kGroup * 4 + 2 * kGroup * pub_pitch<COLS>() * 4 + COLS * KP * 2;
+  return kGroups * kGroup * kGroup * 4 + 2 * kGroup * pub_pitch<COLS>() * 4 + COLS * KP * 2 +
+         2 * kLeafMax * AP * 2;
+}
+
+// The m16k16 A fragment of mma.sync from a row-major 16×16 FP16 tile in
+// shared memory: lane l gives the address of row (l % 8) + 8·((l / 8) % 2),
+// columns 8·(l / 16) .. +7.
+__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
 }
 
 // mma.sync m16n8k16, FP16 operands, FP32 accumulator in place: d += a·b.
@@ -110,6 +125,9 @@ __global__ void __launch_bounds__(kLeafMax, 2)
   float* pub_b = diag + kGroups * kGroup * kGroup;  // [kGroup][P]: b of the group's rows
   float* pub_x = pub_b + kGroup * P;                // [kGroup][P]: x of the group's rows
   __half* pub_xh = reinterpret_cast<__half*>(pub_x + kGroup * P);  // [COLS][KP]: -x_g in FP16
+  // [2][kLeafMax][AP]: A(c0 .. c0+31, r) of a group, row r of the block,
+  // double-buffered (the next group's segments arrive during this group)
+  uint16_t* a_stage = reinterpret_cast<uint16_t*>(pub_xh + COLS * KP);
   const int r = threadIdx.x;
   const int lane = r & 31, warp = r >> 5;
   const int64_t j0 = static_cast<int64_t>(blockIdx.x) * COLS;
@@ -184,6 +202,28 @@ __global__ void __launch_bounds__(kLeafMax, 2)
   // 32-bit loads of A's K pairs: A 4-byte aligned and lda even (off is a
   // multiple of 64)
   const bool pairs = ((reinterpret_cast<uintptr_t>(A) & 3u) == 0) && (lda % 2) == 0;
+  // A's column segments staged by asynchronous 16-byte copies, a group ahead:
+  // A 16-byte aligned and lda a multiple of 8
+  const bool staged = ((reinterpret_cast<uintptr_t>(A) & 15u) == 0) && (lda % 8) == 0;
+  // thread r's segment of group g: A(off+32g .. +31, off+r), zero past the
+  // block's order, into buffer g % 2 (rows of warps above group g only)
+  auto stage_group = [&](int g) {
+    if (warp >= g) return;
+    const int c0 = g * kGroup, sg = min(kGroup, s - c0);
+    const uint16_t* src = A + (off + r) * lda + off + c0;
+    uint16_t* dst = a_stage + ((g & 1) * kLeafMax + r) * AP;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      int valid = sg - 8 * q;
+      valid = valid < 0 ? 0 : (valid > 8 ? 8 : valid);
+      if (valid > 0)
+        cp_async_16(smem_u32(dst + 8 * q), src + 8 * q, 2 * valid);
+      else
+        *reinterpret_cast<uint4*>(dst + 8 * q) = make_uint4(0u, 0u, 0u, 0u);
+    }
+  };
+  if (staged) stage_group(groups - 1);
+  cp_async_commit();
 
   for (int g = groups - 1; g >= 0; --g) {
     const int c0 = g * kGroup, sg = min(kGroup, s - c0);
@@ -191,7 +231,13 @@ __global__ void __launch_bounds__(kLeafMax, 2)
     // is solved: af[mt][ks] is the m16k16 fragment of rows 16·mt.. of the
     // warp and the group's rows 16·ks.., i.e. A(c0 + k, r) (contiguous in k)
     uint32_t af[2][2][4] = {};
-    if (warp < g) {
+    // one copy group per step: the next group's segments
+    if (staged && g >= 1) {
+      __syncwarp();  // this warp's reads of the buffer (two groups ago) are done
+      stage_group(g - 1);
+    }
+    cp_async_commit();
+    if (!staged && warp < g) {
 #pragma unroll
       for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
@@ -264,6 +310,18 @@ __global__ void __launch_bounds__(kLeafMax, 2)
         }
     } else if (warp < g) {
       // (3) rows above the group: b += A_g · (-x_g) (A = 0 past the block's order)
+      if (staged) {
+        cp_async_wait<1>();  // this group's segments (the next group's may be in flight)
+        __syncwarp();
+        const uint16_t* base = a_stage + ((g & 1) * kLeafMax + warp * kGroup) * AP;
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+          for (int ks = 0; ks < 2; ++ks) {
+            const int row = 16 * mt + (lane & 7) + ((lane >> 3) & 1) * 8;
+            ldmatrix_x4(af[mt][ks], smem_u32(base + row * AP + 16 * ks + (lane >> 4) * 8));
+          }
+      }
 #pragma unroll
       for (int ks = 0; ks < 2; ++ks)
 #pragma unroll
