@@ -82,6 +82,15 @@ int current_device(DeviceState** out) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e);
   if (dev < 0 || dev >= kMaxDevices) return HGEMM_ERR_UNSUPPORTED_DEVICE;
+  // The tensor maps are encoded by a driver-API call, which needs the
+  // device's context current on this host thread: a thread whose runtime
+  // calls so far needed no context (streams and memory from a caching
+  // allocator, say) may not have it yet. Bind it once per thread and device.
+  thread_local int t_bound_device = -1;
+  if (t_bound_device != dev) {
+    if ((e = cudaSetDevice(dev)) != cudaSuccess) return cuda_fail(e);
+    t_bound_device = dev;
+  }
   DeviceState& st = g_devices[dev];
   int r = st.ready.load(std::memory_order_acquire);
   if (r == 0) {

@@ -359,3 +359,85 @@ def test_unsupported_arguments_raise():
     with pytest.raises(tc.HgemmError) as ei:
         tc.hgemm(a, a, a, 4, 4, 8)   # C aliases A
     assert ei.value.status == tc.HGEMM_ERR_ALIAS
+
+
+@pytest.mark.parametrize("path", [None, tc.HGEMM_PATH_TC_PAIR, tc.HGEMM_PATH_TC_WIDE, tc.HGEMM_PATH_SKINNY,
+                                  tc.HGEMM_PATH_GENERIC])
+def test_pitches_beyond_32_bit_offsets(path):
+    """Rows 2^28 + 8 elements apart (A and C span over 2^31 elements, 4.3 GB
+    each, only the used rows written): every address offset must be 64-bit."""
+    torch = torch_cuda()
+    M, N, K = 9, 64, 3072
+    ld = (1 << 28) + 8
+    a, b = synth.operands(M, N, K, seed=28, kind="uniform")
+    ref = oracle.hgemm(a, b, nthreads=oracle_threads())
+    span = (M - 1) * ld + max(K, N)
+    dA = torch.empty(span, dtype=torch.float16, device="cuda")
+    dC = torch.empty(span, dtype=torch.float16, device="cuda")
+    for i in range(M):
+        dA[i * ld:i * ld + K] = torch.from_numpy(a[i]).cuda()
+        dC[i * ld:i * ld + N] = float("nan")
+    db = to_device(b)
+    if path is not None:
+        tc.hgemm_force_path(path)
+    try:
+        tc.hgemm_strided(dA, ld, db, K, dC, ld, M, N, K)
+    finally:
+        tc.hgemm_force_path(-1)
+    assert tc.hgemm_device_status() == tc.HGEMM_OK
+    torch.cuda.synchronize()
+    got = np.stack([dC[i * ld:i * ld + N].cpu().numpy() for i in range(M)])
+    assert_close(got, ref, what=f"64-bit pitches, path {path}")
+
+
+def test_concurrent_host_threads():
+    """Two host threads, each on its own stream, call the product, the
+    triangular product and the triangular solve at once, repeatedly; every
+    result equals the single-threaded one bit for bit (the host side's caches
+    and helper streams are shared)."""
+    import threading
+    torch = torch_cuda()
+    M = N = K = 1024
+    a, b = synth.operands(M, N, K, seed=91, kind="uniform")
+    ta_col, tb_col = synth.trmm_operands(1024, 96, 92)
+    sa_col, sb_col = synth.trsm_operands(1024, 96, 93)
+    dev = {name: to_device(x) for name, x in
+           [("a", a), ("b", b), ("ta", ta_col), ("tb", tb_col), ("sa", sa_col), ("sb", sb_col)]}
+
+    def run_all(stream, outs):
+        tc.hgemm(dev["a"], dev["b"], outs["c"], M, N, K, stream)
+        tc.hgemm_trmm(dev["ta"], 1024, dev["tb"], 1024, outs["t"], 1024, 1024, 96, 1.0, stream)
+        tc.hgemm_trsm(dev["sa"], 1024, dev["sb"], 1024, outs["s"], 1024, 1024, 96, 1.0, stream)
+
+    def fresh():
+        return {"c": torch.empty((M, N), dtype=torch.float16, device="cuda"),
+                "t": torch.empty((96, 1024), dtype=torch.float16, device="cuda"),
+                "s": torch.empty((96, 1024), dtype=torch.float16, device="cuda")}
+
+    want = fresh()
+    run_all(torch.cuda.current_stream().cuda_stream, want)
+    torch.cuda.synchronize()
+    want = {k: v.cpu().numpy().view(np.uint16) for k, v in want.items()}
+    errors = []
+
+    def worker(seed):
+        try:
+            stream = torch.cuda.Stream()
+            outs = fresh()
+            for _ in range(20):
+                run_all(stream.cuda_stream, outs)
+                stream.synchronize()
+                for k, v in outs.items():
+                    if not np.array_equal(v.cpu().numpy().view(np.uint16), want[k]):
+                        errors.append(f"thread {seed}: {k} differs")
+                        return
+        except Exception as ex:  # reported in the main thread
+            errors.append(f"thread {seed}: {ex!r}")
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    assert tc.hgemm_device_status() == tc.HGEMM_OK
