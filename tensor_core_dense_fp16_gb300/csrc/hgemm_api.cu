@@ -355,20 +355,36 @@ int run_tc(const Gemm& g, const hg::EpiArgs& epi, const DeviceState& dev,
   return e == cudaSuccess ? HGEMM_OK : cuda_fail(e);
 }
 
+// A batch of equal products in one launch of the pair kernel: product j
+// (j < count) is n_each columns of C by k_each of K, with A's K, B's N and
+// K, and C's N coordinates shifted by j·shift from those of the first; the
+// Gemm passed with it spans them all. n_each is a multiple of the tile
+// width and k_each of the K block, so no tile reaches past its product.
+struct PairBatch {
+  int count;
+  int64_t shift, n_each, k_each;
+};
+
 int run_tc_pair(const Gemm& g, const hg::EpiArgs& epi, const DeviceState& dev,
-            cudaStream_t stream) {
+            cudaStream_t stream, const PairBatch* batch = nullptr) {
   const void* A = g.A;
   const void* B = g.B;
   void* C = g.C;
   const int64_t M = g.M, N = g.N, K = g.K;
+  const int64_t n_one = batch ? batch->n_each : N, k_one = batch ? batch->k_each : K;
   hg::TcArgs args{};
   args.M = static_cast<int>(M);
   args.N = static_cast<int>(N);
   args.K = static_cast<int>(K);
   args.num_m = static_cast<int>((M + 2 * hg::kTcBM - 1) / (2 * hg::kTcBM));
-  args.num_n = static_cast<int>((N + hg::kPairBN - 1) / hg::kPairBN);
-  args.num_kb = static_cast<int>((K + hg::kTcBK - 1) / hg::kTcBK);
-  const int64_t tiles = static_cast<int64_t>(args.num_m) * args.num_n;
+  args.num_n = static_cast<int>((n_one + hg::kPairBN - 1) / hg::kPairBN);
+  args.num_kb = static_cast<int>((k_one + hg::kTcBK - 1) / hg::kTcBK);
+  const int64_t per = static_cast<int64_t>(args.num_m) * args.num_n;
+  const int64_t tiles = per * (batch ? batch->count : 1);
+  if (batch) {
+    args.batch_tiles = static_cast<int>(per);
+    args.batch_shift = static_cast<int>(batch->shift);
+  }
   if (tiles > 0x1FFFFFFF) return HGEMM_ERR_INVALID_ARG;
   const int64_t clusters = hg::pair_max_clusters(dev.num_sms);
   // Last (or only) wave: if its tiles leave at least half of the clusters
@@ -379,7 +395,7 @@ int run_tc_pair(const Gemm& g, const hg::EpiArgs& epi, const DeviceState& dev,
   int parts = 1;
   if (tail_split_setting() && rest > 0 && 2 * rest <= clusters) {
     parts = 2;
-    const int64_t last_cols = N - static_cast<int64_t>(args.num_n - 1) * hg::kPairBN;
+    const int64_t last_cols = n_one - static_cast<int64_t>(args.num_n - 1) * hg::kPairBN;
     // (an N-contiguous B arrives in 64-column boxes: a CTA's share of a part
     // must be at least one box, so its parts keep 128 columns)
     if (4 * rest <= clusters && (args.num_n > 1 || last_cols > 128) && !g.b_mn) parts = 4;
@@ -734,9 +750,32 @@ int hgemm_trmm(const hgemm_half_t* A, int64_t lda, const hgemm_half_t* B, int64_
     const int r = validate(g);
     return r != HGEMM_OK ? r : dispatch(g, accumulate, *dev, st);
   };
+  // A level of equal updates at a constant stride (every level when n is a
+  // power of two times 256), whose updates are whole 256-column tiles and
+  // whole K blocks, runs as one batched launch of the pair kernel on the
+  // caller's stream; other levels run update by update on helper streams.
+  const int forced = g_forced_path.load(std::memory_order_relaxed);
+  auto batch_of = [&](const std::vector<Update>& lv, Gemm* span, PairBatch* pb) {
+    if (lv.size() < 2 || (forced >= 0 && forced != HGEMM_PATH_TC_PAIR)) return false;
+    const Update& u0 = lv[0];
+    const int64_t shift = lv[1].off - u0.off;
+    if (u0.s1 % hg::kPairBN != 0 || u0.s2 % hg::kTcBK != 0 || shift <= 0) return false;
+    for (size_t k = 1; k < lv.size(); ++k)
+      if (lv[k].s1 != u0.s1 || lv[k].s2 != u0.s2 || lv[k].off != u0.off + static_cast<int64_t>(k) * shift)
+        return false;
+    const int64_t cnt = static_cast<int64_t>(lv.size());
+    *span = Gemm{B + u0.off + u0.s1, A + u0.off * lda + u0.off + u0.s1, C + u0.off, m,
+                 (cnt - 1) * shift + u0.s1, (cnt - 1) * shift + u0.s2, ldb, lda, ldc};
+    *pb = PairBatch{static_cast<int>(cnt), shift, u0.s1, u0.s2};
+    return tma_ok(*span) && validate(*span) == HGEMM_OK;
+  };
   TrmmPipe* tp = nullptr;
   bool need_pipe = false;
-  for (const auto& lv : levels) need_pipe = need_pipe || lv.size() > 1;
+  for (const auto& lv : levels) {
+    Gemm span{};
+    PairBatch pb{};
+    need_pipe = need_pipe || (lv.size() > 1 && !batch_of(lv, &span, &pb));
+  }
   if (need_pipe && (rc = trmm_pipe(dev->id, &tp)) != HGEMM_OK) return rc;
   std::unique_lock<std::mutex> lock;
   if (tp) lock = std::unique_lock<std::mutex>(tp->mu);
@@ -744,6 +783,12 @@ int hgemm_trmm(const hgemm_half_t* A, int64_t lda, const hgemm_half_t* B, int64_
     const auto& lv = levels[d];
     if (lv.size() == 1) {
       if ((rc = issue(lv[0], stream)) != HGEMM_OK) return rc;
+      continue;
+    }
+    Gemm span{};
+    PairBatch pb{};
+    if (batch_of(lv, &span, &pb)) {
+      if ((rc = run_tc_pair(span, accumulate, *dev, stream, &pb)) != HGEMM_OK) return rc;
       continue;
     }
     const int used = static_cast<int>(lv.size() < TrmmPipe::kStreams ? lv.size() : TrmmPipe::kStreams);

@@ -81,11 +81,13 @@ struct PairCfg {
 
 // Work unit t: a whole 256×256 tile below p.full_tiles, else one part of
 // p.part_cols (128 or 64) columns of a tile (256 / part_cols consecutive
-// units per tile), in raster order.
+// units per tile), in raster order. In a batched launch, whole tile w
+// belongs to product w / p.batch_tiles, whose coordinates are shifted.
 struct PairTile {
   int mb, nb;
   int n0;     // first column of C
   int ncols;  // 256, 128 or 64
+  int koff;   // shift of the K coordinate of A and B
 };
 
 __device__ __forceinline__ PairTile pair_tile(int t, const TcArgs& p) {
@@ -97,8 +99,15 @@ __device__ __forceinline__ PairTile pair_tile(int t, const TcArgs& p) {
     whole = p.full_tiles + h / parts;
     part = h - (h / parts) * parts;
   }
+  int shift = 0;
+  if (p.batch_tiles > 0) {
+    const int j = whole / p.batch_tiles;
+    whole -= j * p.batch_tiles;
+    shift = j * p.batch_shift;
+  }
   tile_coords(whole, p.num_m, p.num_n, p.group_m, w.mb, w.nb);
-  w.n0 = w.nb * kPairBN + (part < 0 ? 0 : part * p.part_cols);
+  w.koff = shift;
+  w.n0 = shift + w.nb * kPairBN + (part < 0 ? 0 : part * p.part_cols);
   w.ncols = part < 0 ? kPairBN : p.part_cols;
   return w;
 }
@@ -190,22 +199,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
             break;
           }
           const uint32_t fb = mapa_shared(full_bar(stage), 0);
+          const int kx = kb * Cfg::BK + w.koff;
           if (rank == 0 && !(p.inject == 1 && issued == 0))  // testing aid: withhold one arrival
             mbar_arrive_expect_tx(full_bar(stage), tx);
           if (p.a_mn) {
             // A stored K×M: the CTA's 128 rows as two 64-row boxes, 8 KB apart
-            tma_load_2d_cg2(sA + stage * stage_bytes, &tmA, fb, ya, kb * Cfg::BK);
-            tma_load_2d_cg2(sA + stage * stage_bytes + kMnBoxBytes, &tmA, fb, ya + kMnBox, kb * Cfg::BK);
+            tma_load_2d_cg2(sA + stage * stage_bytes, &tmA, fb, ya, kx);
+            tma_load_2d_cg2(sA + stage * stage_bytes + kMnBoxBytes, &tmA, fb, ya + kMnBox, kx);
           } else {
-            tma_load_2d_cg2(sA + stage * stage_bytes, &tmA, fb, kb * Cfg::BK, ya);
+            tma_load_2d_cg2(sA + stage * stage_bytes, &tmA, fb, kx, ya);
           }
           if (p.b_mn) {
             // B stored K×N: the CTA's ncols/2 columns as 64-column boxes, 8 KB apart
             for (int bx = 0; bx < w.ncols / 2; bx += kMnBox)
-              tma_load_2d_cg2(sB + stage * stage_bytes + (bx / kMnBox) * kMnBoxBytes, &tmB, fb, yb + bx,
-                              kb * Cfg::BK);
+              tma_load_2d_cg2(sB + stage * stage_bytes + (bx / kMnBox) * kMnBoxBytes, &tmB, fb, yb + bx, kx);
           } else {
-            tma_load_2d_cg2(sB + stage * stage_bytes, mapb, fb, kb * Cfg::BK, yb);
+            tma_load_2d_cg2(sB + stage * stage_bytes, mapb, fb, kx, yb);
           }
           ++issued;
           if (++stage == STAGES) {

@@ -50,6 +50,10 @@ struct TcArgs {
   int64_t ldc;               // C's row pitch in elements
   int a_mn, b_mn;            // pair kernel: A stored M-contiguous (K×M), B stored
                              // N-contiguous (K×N); else K-contiguous
+  int batch_tiles;           // pair kernel: whole tiles per product of a batch of
+                             // equal products in one launch (0: a single product)
+  int batch_shift;           // product j of the batch is the first one with A's K,
+                             // B's N and K, and C's N coordinates shifted by j·batch_shift
 };
 
 // Plain-pointer launch arguments for the kernels that do not use TMA.

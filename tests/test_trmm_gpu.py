@@ -78,3 +78,32 @@ def test_trmm_repeatable():
     first = run_trmm(a, b)
     for _ in range(3):
         assert np.array_equal(run_trmm(a, b).view(np.uint16), first.view(np.uint16))
+
+
+@pytest.mark.parametrize("path", [None, tc.HGEMM_PATH_TC_PAIR, tc.HGEMM_PATH_TC, tc.HGEMM_PATH_GENERIC])
+def test_trmm_equal_levels(path):
+    """n = 2048: each level of the recursion holds equal updates at a constant
+    stride (2 of 1024 columns, then 4 of 512, 8 of 256 ...). On the pair path
+    (chosen, or forced) a level runs as one batched launch; another forced
+    path runs it update by update. m = 300 leaves a ragged row of tiles,
+    with a scale factor and pitches wider than the operands."""
+    n, m = 2048, 300
+    a, b = trmm_inputs(n, m, seed=21)
+    ref = oracle.trmm(a, b, alpha=0.5, nthreads=oracle_threads())
+    if path is not None:
+        tc.hgemm_force_path(path)
+    try:
+        out = run_trmm(a, b, alpha=0.5, pad=(8, 16, 24))
+    finally:
+        if path is not None:
+            tc.hgemm_force_path(-1)
+    assert_close(out, ref, what=f"trmm 2048x300, path {path}")
+
+
+def test_trmm_equal_levels_wide_m():
+    """n = 1024, m = 1000: the batched levels with several tile rows of C per
+    update and a ragged last row."""
+    n, m = 1024, 1000
+    a, b = trmm_inputs(n, m, seed=23)
+    ref = oracle.trmm(a, b, nthreads=oracle_threads())
+    assert_close(run_trmm(a, b), ref, what="trmm 1024x1000")
