@@ -81,14 +81,30 @@ DESCRIPTIONS = {
 
 
 def trmm_launches(n, leaf=256):
-    """Kernel launches of one hgemm_trmm: the batched leaves plus one GEMM per
-    block split by the recursion (blocks split at half, rounded up to 64)."""
-    def splits(s):
+    """Kernel launches of one hgemm_trmm (pitches n, aligned operands): the
+    batched leaves, then per recursion level either one batched launch (two or
+    more equal updates at a constant stride, whole 256-column tiles and whole
+    64-wide K blocks) or one GEMM per update (blocks split at half, rounded up
+    to 64)."""
+    levels = {}
+
+    def walk(off, s, depth):
         if s <= leaf:
-            return 0
+            return
         s1 = ((s // 2 + 63) // 64) * 64
-        return 1 + splits(s1) + splits(s - s1)
-    return 1 + splits(n)
+        levels.setdefault(depth, []).append((off, s1, s - s1))
+        walk(off, s1, depth + 1)
+        walk(off + s1, s - s1, depth + 1)
+
+    walk(0, n, 0)
+    count = 1
+    for lv in levels.values():
+        off0, s1, s2 = lv[0]
+        shift = lv[1][0] - off0 if len(lv) > 1 else 0
+        batched = (len(lv) > 1 and s1 % 256 == 0 and s2 % 64 == 0 and shift > 0 and
+                   all(u == (off0 + k * shift, s1, s2) for k, u in enumerate(lv)))
+        count += 1 if batched else len(lv)
+    return count
 
 
 def trmm_flops(spec):
@@ -115,7 +131,7 @@ def trsm_flops(spec):
 # The triangular operations: the call, its oracle, its flop count and launches.
 TRI_OPS = {
     "trmm": dict(call="hgemm_trmm", oracle="trmm", flops=trmm_flops, launches=trmm_launches,
-                 kernel="hgemm_tri_leaves_kernel + hgemm update kernels"),
+                 kernel="hgemm_tri_leaves_tc_kernel (hgemm_tri_leaves_kernel when n % 64 != 0) + hgemm update kernels"),
     "trsm": dict(call="hgemm_trsm", oracle="trsm", flops=trsm_flops, launches=trsm_launches,
                  kernel="scale_copy_kernel + trsm_leaf_kernel + hgemm update kernels"),
 }

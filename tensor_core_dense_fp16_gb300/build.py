@@ -20,7 +20,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libhgemm.so")
-SOURCES = ["hgemm_api.cu", "hgemm_tc.cu", "hgemm_tc2.cu", "hgemm_tc2w.cu", "hgemm_skinny.cu", "hgemm_generic.cu", "hgemm_trsm.cu"]
+SOURCES = ["hgemm_api.cu", "hgemm_tc.cu", "hgemm_tc2.cu", "hgemm_tc2w.cu", "hgemm_skinny.cu", "hgemm_generic.cu", "hgemm_trsm.cu",
+           "hgemm_trileaf.cu"]
 HEADERS = ["ptx.cuh", "internal.h", "kernel_common.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -734,10 +734,45 @@ int hgemm_trmm(const hgemm_half_t* A, int64_t lda, const hgemm_half_t* B, int64_
   // In the GEMM view, Cᵀ (m × n, pitch ldc) = Bᵀ (m × n, pitch ldb) · lower(A),
   // where row i of the second operand is column i of A (pitch lda).
   const hg::EpiArgs scale{alpha, 0.0f, nullptr, 0, alpha != 1.0f ? 1 : 0};
-  hg::PlainArgs pa{reinterpret_cast<const uint16_t*>(B), reinterpret_cast<const uint16_t*>(A),
-                   reinterpret_cast<uint16_t*>(C), m, n, n, ldb, lda, ldc,
-                   dev->status, g_timeout_ns.load(), scale};
-  cudaError_t e = hg::launch_tri_leaves(pa, leaves, dev->num_sms, stream);
+  const int forced = g_forced_path.load(std::memory_order_relaxed);
+  // The leaves run on the tensor cores when every leaf order is a multiple of
+  // 64 (n is) and TMA can describe the operands; otherwise (or with the
+  // generic path forced) on the generic kernel, which masks as it loads.
+  cudaError_t e = cudaSuccess;
+  bool tc_leaves = forced != HGEMM_PATH_GENERIC && n % 64 == 0 && m <= (int64_t(1) << 30) &&
+                   ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B) |
+                     reinterpret_cast<uintptr_t>(C)) & 15u) == 0 &&
+                   lda % 8 == 0 && ldb % 8 == 0 && ldc % 8 == 0;
+  if (tc_leaves) {
+    // Bᵀ (m × n, pitch ldb), the triangle's rows (column i of A, pitch lda), Cᵀ
+    CUtensorMap mx, ml, mc;
+    tc_leaves = encode_map(&mx, B, m, n, ldb, hg::kTcBM, hg::kTcBK) == HGEMM_OK &&
+                encode_map(&ml, A, n, n, lda, 64, hg::kTcBK) == HGEMM_OK &&
+                encode_map(&mc, C, m, n, ldc, hg::kEpiRows, hg::kEpiCols) == HGEMM_OK;
+    if (tc_leaves) {
+      hg::TcArgs args{};
+      args.M = static_cast<int>(m);
+      args.N = static_cast<int>(n);
+      args.K = static_cast<int>(n);
+      args.num_m = static_cast<int>((m + hg::kTcBM - 1) / hg::kTcBM);
+      args.num_tiles = leaves.count * args.num_m;
+      args.full_tiles = args.num_tiles;
+      args.grid = args.num_tiles < dev->num_sms ? args.num_tiles : dev->num_sms;
+      args.status = dev->status;
+      args.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
+      args.inject = g_inject.load(std::memory_order_relaxed);
+      args.epi = scale;
+      args.C = reinterpret_cast<const uint16_t*>(C);
+      args.ldc = ldc;
+      e = hg::launch_tri_leaves_tc(mx, ml, mc, args, leaves, stream);
+    }
+  }
+  if (!tc_leaves) {
+    hg::PlainArgs pa{reinterpret_cast<const uint16_t*>(B), reinterpret_cast<const uint16_t*>(A),
+                     reinterpret_cast<uint16_t*>(C), m, n, n, ldb, lda, ldc,
+                     dev->status, g_timeout_ns.load(), scale};
+    e = hg::launch_tri_leaves(pa, leaves, dev->num_sms, stream);
+  }
   if (e != cudaSuccess) return cuda_fail(e);
 
   // Updates, deepest level first: an update reads the first half of its
@@ -754,7 +789,6 @@ int hgemm_trmm(const hgemm_half_t* A, int64_t lda, const hgemm_half_t* B, int64_
   // power of two times 256), whose updates are whole 256-column tiles and
   // whole K blocks, runs as one batched launch of the pair kernel on the
   // caller's stream; other levels run update by update on helper streams.
-  const int forced = g_forced_path.load(std::memory_order_relaxed);
   auto batch_of = [&](const std::vector<Update>& lv, Gemm* span, PairBatch* pb) {
     if (lv.size() < 2 || (forced >= 0 && forced != HGEMM_PATH_TC_PAIR)) return false;
     const Update& u0 = lv[0];

@@ -133,6 +133,12 @@ cudaError_t launch_generic(const PlainArgs& args, int num_sms, cudaStream_t stre
 // M × size (see hgemm_generic.cu).
 cudaError_t launch_tri_leaves(const PlainArgs& args, const TriLeaves& leaves, int num_sms,
                               cudaStream_t stream);
+// The same on the tensor cores for leaves whose orders are multiples of 64
+// (see hgemm_trileaf.cu): x maps Bᵀ (m × n, 128×64 boxes), l maps the rows
+// of the triangle (column i of A as row i, n × n, 64×64 boxes), c maps Cᵀ
+// (m × n, 32×64 boxes); args.num_m row tiles of 128 per leaf.
+cudaError_t launch_tri_leaves_tc(const CUtensorMap& x, const CUtensorMap& l, const CUtensorMap& c,
+                                 const TcArgs& args, const TriLeaves& leaves, cudaStream_t stream);
 
 // Triangular solve Aᵀ·X = alpha·B (see hgemm_trsm.cu): the largest diagonal
 // block solved by substitution; X(:, j) = alpha·B(:, j) over n × m

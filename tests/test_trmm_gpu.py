@@ -54,11 +54,43 @@ def test_trmm_matches_oracle(n, m):
     assert_close(run_trmm(a, b), ref, what=f"trmm {n}x{m}")
 
 
-def test_trmm_reads_only_the_lower_triangle():
-    n, m = 700, 96
+@pytest.mark.parametrize("n", [700, 1024])
+def test_trmm_reads_only_the_lower_triangle(n):
+    """NaN above the diagonal never reaches C: n = 700 takes the generic
+    leaves (masked as they load), n = 1024 the tensor-core leaves (diagonal
+    sub-blocks masked in shared memory, rows below them never loaded)."""
+    m = 96
     a, b = trmm_inputs(n, m, seed=7)
     ref = oracle.trmm(a, b, nthreads=oracle_threads())
-    assert_close(run_trmm(a, b, poison_upper=True), ref, what="NaN above the diagonal")
+    assert_close(run_trmm(a, b, poison_upper=True), ref, what=f"NaN above the diagonal, n={n}")
+
+
+@pytest.mark.parametrize("n,m", [(64, 1), (192, 129), (320, 40), (448, 257), (576, 128)])
+def test_trmm_tensor_core_leaf_orders(n, m):
+    """n a multiple of 64: the leaves run on the tensor cores, with orders
+    64, 192, 192 + 128, 256 + 192 and 320 + 256 split further (every leaf
+    order a multiple of 64 up to 256), and ragged or single rows of B."""
+    a, b = trmm_inputs(n, m, seed=31 + n)
+    ref = oracle.trmm(a, b, nthreads=oracle_threads())
+    assert_close(run_trmm(a, b), ref, what=f"trmm {n}x{m}")
+
+
+@pytest.mark.parametrize("path", [None, tc.HGEMM_PATH_GENERIC])
+def test_trmm_leaf_kernels_agree(path):
+    """The same product with the tensor-core leaves (default) and the generic
+    leaves (forced): both within the tolerance, with a scale factor and
+    pitches wider than the operands (multiples of 8, so TMA applies)."""
+    n, m = 1280, 200
+    a, b = trmm_inputs(n, m, seed=41)
+    ref = oracle.trmm(a, b, alpha=0.25, nthreads=oracle_threads())
+    if path is not None:
+        tc.hgemm_force_path(path)
+    try:
+        out = run_trmm(a, b, alpha=0.25, pad=(8, 8, 16))
+    finally:
+        if path is not None:
+            tc.hgemm_force_path(-1)
+    assert_close(out, ref, what=f"trmm 1280x200, path {path}")
 
 
 @pytest.mark.parametrize("pad", [(8, 16, 8), (3, 5, 1)])
