@@ -43,7 +43,7 @@
 namespace hg {
 namespace {
 
-template <int MAX_STAGES_>
+template <int MAX_STAGES_, int EPI_WARPS_ = 4>
 struct PairCfg {
   static constexpr int BM = 2 * kTcBM;   // cluster tile rows
   static constexpr int BN = kPairBN;     // cluster tile columns
@@ -58,9 +58,14 @@ struct PairCfg {
   static constexpr int TX_BYTES = 2 * STAGE_BYTES;          // expected by the even CTA
   static constexpr int RING_BYTES = kPairRingBytes;         // six whole-tile stages
   static_assert(RING_BYTES == 6 * STAGE_BYTES, "the ring holds six whole-tile stages");
-  static constexpr int EPI_WARPS = 4;
+  // plain products: four epilogue warps with two staging boxes each; fused
+  // ones: eight (two per TMEM lane quarter, alternate 64-column boxes) with
+  // one box each, since their epilogue arithmetic and reads of C take longer
+  // than a short main loop
+  static constexpr int EPI_WARPS = EPI_WARPS_;
+  static_assert(EPI_WARPS == 4 || EPI_WARPS == 8, "one or two epilogue warps per TMEM lane quarter");
   static constexpr int C_BOX_BYTES = kEpiRows * kEpiCols * 2;
-  static constexpr int C_BUFS = 2;
+  static constexpr int C_BUFS = EPI_WARPS == 8 ? 1 : 2;
   static constexpr int C_BYTES = EPI_WARPS * C_BUFS * C_BOX_BYTES;
   static constexpr int ACC_COLS = BN;
   static constexpr int TMEM_COLS = 2 * ACC_COLS;
@@ -70,7 +75,7 @@ struct PairCfg {
   static constexpr int NUM_BARS = 2 * MAX_STAGES + 4 + 1;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
-  static constexpr int THREADS = 192;
+  static constexpr int THREADS = 64 + 32 * EPI_WARPS;
   static constexpr uint32_t IDESC = idesc_f16_f32acc(BM, BN);
 
   static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "1024-byte aligned stages");
@@ -113,11 +118,11 @@ __device__ __forceinline__ PairTile pair_tile(int t, const TcArgs& p) {
 }
 
 template <int MAX_STAGES, bool FUSED>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED ? 320 : 192, 1)
     hgemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmBh, const __grid_constant__ CUtensorMap tmC,
                      const TcArgs p) {
-  using Cfg = PairCfg<MAX_STAGES>;
+  using Cfg = PairCfg<MAX_STAGES, FUSED ? 8 : 4>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -294,6 +299,66 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
       wait_drain(drain_bar, 0, wd);
     }
     __syncwarp();
+  } else if constexpr (FUSED) {
+    // --------------------------------------- fused epilogue (both CTAs)
+    // warps 2..5 take the even 64-column boxes of a tile, warps 6..9 the odd
+    // ones; warp w reads TMEM lanes 32·(w % 4) .. +31
+    const int q = warp & 3;
+    const int h = (warp - 2) >> 2;
+    uint8_t* buf = smem + Cfg::OFF_C + (warp - 2) * Cfg::C_BOX_BYTES;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int t = cluster_id; t < p.num_tiles; t += num_clusters) {
+      const PairTile w = pair_tile(t, p);
+      const int chunks = w.ncols / kEpiCols;
+      const int64_t grow = static_cast<int64_t>(w.mb) * Cfg::BM + static_cast<int>(rank) * Cfg::ROWS +
+                           q * kEpiRows + lane;  // this lane's row of C
+      prefetch_c_row(p.epi, p.C, p.M, p.N, p.ldc, grow, w.n0, w.ncols);
+      int ok = 1;
+      if (lane == 0) ok = wait_phase(accf_bar(acc), acc_phase, wd, kWdEpiAccFull) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after_sync();
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                             static_cast<uint32_t>(acc * Cfg::ACC_COLS);
+      const int y0 = w.mb * Cfg::BM + static_cast<int>(rank) * Cfg::ROWS + q * kEpiRows;
+      // this warp's last box (none when a 64-column part leaves the odd box out)
+      const int last = (chunks - 1 - h) >= 0 ? h + ((chunks - 1 - h) / 2) * 2 : -1;
+      if (last < 0) {
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(mapa_shared(acce_bar(acc), 0));
+      }
+#pragma unroll 1
+      for (int c = h; c < chunks; c += 2) {
+        uint32_t v0[32], v1[32];
+        tmem_ld_32x32b_x32(t_row + c * kEpiCols, v0);
+        tmem_ld_32x32b_x32(t_row + c * kEpiCols + 32, v1);
+        tmem_ld_wait(v0);
+        tmem_ld_wait(v1);
+        if (c == last) {
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(mapa_shared(acce_bar(acc), 0));
+        }
+        const int x0 = w.n0 + c * kEpiCols;
+        if (x0 >= p.N || y0 >= p.M) continue;
+        if (lane == 0) bulk_wait_group_read<0>();  // the previous store has read the box
+        __syncwarp();
+        // 128-byte swizzle: 16-byte chunk j of row r sits at chunk j ^ (r % 8)
+        stage_row64<true>(buf + lane * 128, lane, v0, v1, p.epi, p.C, p.M, p.N, p.ldc, grow, x0);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&tmC, smem_u32(buf), x0, y0);
+          bulk_commit_group();
+        }
+      }
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+    if (lane == 0) bulk_wait_group_read<0>();  // staging read; the writes finish with the grid
+    __syncwarp();
   } else {
     // ------------------------------------------------ epilogue (both CTAs)
     const int q = warp & 3;
@@ -387,10 +452,13 @@ int pair_max_clusters(int num_sms) {
 
 cudaError_t launch_tc_pair(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b_part,
                            const CUtensorMap& c, const TcArgs& args, cudaStream_t stream) {
-  using Cfg = PairCfg<kPairStages>;
+  using Cfg = PairCfg<kPairStages, 4>;
+  using FusedCfg = PairCfg<kPairStages, 8>;
+  static_assert(Cfg::SMEM_BYTES == FusedCfg::SMEM_BYTES, "both instantiations have the same footprint");
   static std::atomic<bool> attr_done[2][64];
   const int fused = args.epi.mode != 0 ? 1 : 0;
   auto kern = fused ? hgemm_tc2_kernel<kPairStages, true> : hgemm_tc2_kernel<kPairStages, false>;
+  const int threads = fused ? FusedCfg::THREADS : Cfg::THREADS;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -399,7 +467,8 @@ cudaError_t launch_tc_pair(const CUtensorMap& a, const CUtensorMap& b, const CUt
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_done[fused][dev] = true;
   }
-  PdlLaunch l(dim3(static_cast<unsigned>(args.grid)), dim3(Cfg::THREADS), Cfg::SMEM_BYTES, stream);
+  PdlLaunch l(dim3(static_cast<unsigned>(args.grid)), dim3(static_cast<unsigned>(threads)), Cfg::SMEM_BYTES,
+              stream);
   return cudaLaunchKernelEx(&l.cfg, kern, a, b, b_part, c, args);
 }
 
