@@ -133,7 +133,8 @@ TRI_OPS = {
     "trmm": dict(call="hgemm_trmm", oracle="trmm", flops=trmm_flops, launches=trmm_launches,
                  kernel="hgemm_tri_leaves_tc_kernel (hgemm_tri_leaves_kernel when n % 64 != 0) + hgemm update kernels"),
     "trsm": dict(call="hgemm_trsm", oracle="trsm", flops=trsm_flops, launches=trsm_launches,
-                 kernel="scale_copy_kernel + trsm_leaf_kernel + hgemm update kernels"),
+                 kernel="scale_copy_kernel + trsm_inverse_kernel + hgemm_tc2_kernel (diagonal blocks by their "
+                        "inverses, updates); without a workspace trsm_leaf_kernel for the diagonal blocks"),
 }
 
 
@@ -154,6 +155,8 @@ def parse_args():
                     help="A stored M x K row-major (the default) or K x M (column-major)")
     ap.add_argument("--b-layout", choices=["col", "row"], default="col",
                     help="B stored N x K (column-major, the default) or K x N row-major")
+    ap.add_argument("--no-workspace", action="store_true",
+                    help="TRSM workloads: hgemm_trsm without a workspace (substitution for every diagonal block)")
     ap.add_argument("--epilogue", choices=sorted(EPILOGUES), default="none",
                     help="fused epilogue through hgemm_ex (default: the plain product)")
     return ap.parse_args()
@@ -479,8 +482,15 @@ def run_tri_ours(args, spec, a_col, b_col, world, rank, local):
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(2 * l2 // 4 + 1, dtype=torch.float32, device=dev)
 
-    def step():
-        call(da, n, db, n, dc, n, n, m, 1.0, stream)
+    if op == "trsm" and not args.no_workspace:
+        # caller-owned workspace for the diagonal blocks' inverses, allocated once
+        work = torch.empty(tc.hgemm_trsm_workspace_size(n), dtype=torch.uint8, device=dev)
+
+        def step():
+            tc.hgemm_trsm_ws(da, n, db, n, dc, n, n, m, 1.0, work, None, stream)
+    else:
+        def step():
+            call(da, n, db, n, dc, n, n, m, 1.0, stream)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -573,10 +583,12 @@ def run_tri_ours(args, spec, a_col, b_col, world, rank, local):
             "config": {"workload": f"{args.workload}: {DESCRIPTIONS.get(args.workload, '')}",
                        "n": n, "m": m, "seed": spec["seed"],
                        "l2": "flushed before every timed call (write of 2x L2 size, outside the events)",
-                       "inputs": "resident in HBM", "path": ops["call"],
+                       "inputs": "resident in HBM",
+                       "path": "hgemm_trsm_ws" if op == "trsm" and not args.no_workspace else ops["call"],
                        "parallelism": f"replicas x{world}"},
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": args.steps * ops["launches"](n), "clocks": clocks,
+            "gpu_launches": args.steps * (ops["launches"](n) + (1 if op == "trsm" and not args.no_workspace else 0)),
+            "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
     if dist:

@@ -217,6 +217,36 @@ HGEMM_API int hgemm_trsm(const hgemm_half_t *A, int64_t lda, const hgemm_half_t 
                cudaStream_t stream);
 
 /*
+ * hgemm_trsm_workspace_size — bytes of device workspace hgemm_trsm_ws uses
+ * for a triangle of order n: 128 KiB per diagonal block of the recursion
+ * (n = 8192: 32 blocks, 4 MiB). 0 for n ≤ 0 or n beyond the recursion's
+ * 128 diagonal blocks. Pure host logic.
+ */
+HGEMM_API size_t hgemm_trsm_workspace_size(int64_t n);
+
+/*
+ * hgemm_trsm_ws — hgemm_trsm (same system, operands, recursion and return
+ * values) with a caller-owned device workspace of at least
+ * hgemm_trsm_workspace_size(n) bytes, 16-byte aligned (256 as cudaMalloc
+ * gives), not overlapping A, B or X (HGEMM_ERR_ALIAS), not used by any
+ * other work until the stream has passed this call. With it, when X is
+ * 16-byte aligned with ldx a multiple of 8, one launch first computes the
+ * inverses of all diagonal blocks (FP32 arithmetic, stored FP16 in the
+ * workspace), and each diagonal block is then solved as an in-place
+ * tensor-core product X_bᵀ := X_bᵀ · L_b⁻¹ instead of by substitution
+ * (a block whose order is not a multiple of 8 still takes the substitution
+ * kernel). The substitution then happens once per block for the identity
+ * rather than per right-hand side, so this pays for many right-hand sides.
+ * Rounding: each solved block is rounded once to FP16 as in hgemm_trsm, the
+ * inverse once more. A null workspace, one too small or not 16-byte
+ * aligned is HGEMM_ERR_INVALID_ARG; X not suited to the tensor-core path, or
+ * a path forced by hgemm_force_path, solves as hgemm_trsm does.
+ */
+HGEMM_API int hgemm_trsm_ws(const hgemm_half_t *A, int64_t lda, const hgemm_half_t *B, int64_t ldb,
+                  hgemm_half_t *X, int64_t ldx, int64_t n, int64_t m, float alpha,
+                  void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * hgemm_host — the same product for operands held in HOST memory.
  *
  * Copies hA -> dA (M*K values) and hB -> dB (N*K values), computes

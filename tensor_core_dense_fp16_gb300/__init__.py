@@ -28,7 +28,7 @@ __all__ = [
     "HgemmError", "library_path", "load", "hgemm", "hgemm_host", "hgemm_select_path",
     "hgemm_force_path", "hgemm_device_status", "hgemm_last_cuda_error",
     "hgemm_status_string", "hgemm_version", "hgemm_set_wait_timeout", "hgemm_debug_inject",
-    "hgemm_force_split", "hgemm_ex", "hgemm_strided", "hgemm_trmm", "hgemm_trsm", "hgemm_layout", "HGEMM_TRMM_MAX_N",
+    "hgemm_force_split", "hgemm_ex", "hgemm_strided", "hgemm_trmm", "hgemm_trsm", "hgemm_trsm_ws", "hgemm_trsm_workspace_size", "hgemm_layout", "HGEMM_TRMM_MAX_N",
     "HGEMM_A_ROW_MAJOR", "HGEMM_A_COL_MAJOR", "HGEMM_B_COL_MAJOR", "HGEMM_B_ROW_MAJOR",
     "HGEMM_INJECT_NONE", "HGEMM_INJECT_DROP_ARRIVAL", "matmul",
 ]
@@ -101,6 +101,10 @@ def load():
     lib.hgemm_trmm.restype = i32
     lib.hgemm_trsm.argtypes = [vp, i64, vp, i64, vp, i64, i64, i64, ctypes.c_float, vp]
     lib.hgemm_trsm.restype = i32
+    lib.hgemm_trsm_ws.argtypes = [vp, i64, vp, i64, vp, i64, i64, i64, ctypes.c_float, vp, ctypes.c_size_t, vp]
+    lib.hgemm_trsm_ws.restype = i32
+    lib.hgemm_trsm_workspace_size.argtypes = [i64]
+    lib.hgemm_trsm_workspace_size.restype = ctypes.c_size_t
     lib.hgemm_layout.argtypes = [i32, i32, vp, i64, vp, i64, vp, i64, i64, i64, i64, ctypes.c_float,
                                  ctypes.c_float, vp, i32, vp]
     lib.hgemm_layout.restype = i32
@@ -236,6 +240,21 @@ def hgemm_trsm(A, lda: int, B, ldb: int, X, ldx: int, n: int, m: int, alpha: flo
     X may be B itself (same pitch) to solve in place (see hgemm.h)."""
     _raise_on(load().hgemm_trsm(_ptr(A), lda, _ptr(B), ldb, _ptr(X), ldx, n, m, float(alpha),
                                 _stream(stream)), "hgemm_trsm")
+
+
+def hgemm_trsm_workspace_size(n: int) -> int:
+    """Bytes of device workspace hgemm_trsm_ws uses for a triangle of order n."""
+    return int(load().hgemm_trsm_workspace_size(n))
+
+
+def hgemm_trsm_ws(A, lda: int, B, ldb: int, X, ldx: int, n: int, m: int, alpha: float = 1.0,
+                  workspace=None, workspace_bytes: int | None = None, stream=None) -> None:
+    """hgemm_trsm with a caller-owned device workspace (a tensor or an
+    address; its size defaults to the tensor's bytes), see hgemm.h."""
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size() if hasattr(workspace, "numel") else 0
+    _raise_on(load().hgemm_trsm_ws(_ptr(A), lda, _ptr(B), ldb, _ptr(X), ldx, n, m, float(alpha),
+                                   _ptr(workspace), int(workspace_bytes), _stream(stream)), "hgemm_trsm_ws")
 
 
 def hgemm_host(hA, hB, hC, M: int, N: int, K: int, dA, dB, dC, stream=None) -> None:

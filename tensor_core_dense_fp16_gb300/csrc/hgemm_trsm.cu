@@ -112,10 +112,16 @@ __device__ __forceinline__ float col32_at(const uint4 (&v)[4], int q) {
   return __half2float(__ushort_as_half(static_cast<uint16_t>(w >> (16 * (q & 1)))));
 }
 
+// The solve of the diagonal block A(off .. off+s-1, off .. off+s-1) for the
+// right-hand sides j0 .. j0+COLS-1, rows xoff .. xoff+s-1 of X, in place.
+// identity: the right-hand sides are the columns of the identity (X is not
+// read), so the block computes columns j0.. of the inverse of the block's
+// transpose.
 template <int COLS>
-__global__ void __launch_bounds__(kLeafMax, 2)
-    trsm_leaf_kernel(const uint16_t* __restrict__ A, int64_t lda, uint16_t* __restrict__ X,
-                     int64_t ldx, int64_t off, int s, int64_t m, int chained) {
+__device__ __forceinline__ void trsm_leaf_body(const uint16_t* __restrict__ A, int64_t lda,
+                                               uint16_t* __restrict__ X, int64_t ldx, int64_t off,
+                                               int64_t xoff, int s, int64_t m, int chained, bool identity,
+                                               int64_t j0) {
   extern __shared__ __align__(16) uint8_t smem[];
   if (!chained) grid_dependency_wait();
   // diag[g][k][j]: first L_g(k, j) in FP32 (L_g the diagonal triangle of
@@ -130,8 +136,7 @@ __global__ void __launch_bounds__(kLeafMax, 2)
   uint16_t* a_stage = reinterpret_cast<uint16_t*>(pub_xh + COLS * KP);
   const int r = threadIdx.x;
   const int lane = r & 31, warp = r >> 5;
-  const int64_t j0 = static_cast<int64_t>(blockIdx.x) * COLS;
-  const int groups = (s + kGroup - 1) / kGroup;  // = the block's warps
+  const int groups = (s + kGroup - 1) / kGroup;  // the block's warps (warps past them only synchronise)
   // 16-byte loads of A's column segments: column starts 16-byte aligned
   const bool vec = ((reinterpret_cast<uintptr_t>(A) & 15u) == 0) && (lda % 8) == 0 && (off % 8) == 0;
 
@@ -197,7 +202,9 @@ __global__ void __launch_bounds__(kLeafMax, 2)
       for (int e = 0; e < 4; ++e) {
         const int row = warp * kGroup + 16 * mt + gid + (e >= 2 ? 8 : 0);
         const int64_t j = j0 + 8 * nt + 2 * tig + (e & 1);
-        c[mt][nt][e] = (row < s && j < m) ? __half2float(__ushort_as_half(X[j * ldx + off + row])) : 0.f;
+        c[mt][nt][e] = (row < s && j < m)
+                           ? (identity ? (row == j ? 1.f : 0.f) : __half2float(__ushort_as_half(X[j * ldx + xoff + row])))
+                           : 0.f;
       }
   // 32-bit loads of A's K pairs: A 4-byte aligned and lda even (off is a
   // multiple of 64)
@@ -276,7 +283,7 @@ __global__ void __launch_bounds__(kLeafMax, 2)
     // also -x_g in FP16, column by column, as the mma B operand
     {
       const float* mi = diag + g * kGroup * kGroup + lane;
-      for (int q = warp; q < COLS / 4; q += groups) {
+      for (int q = warp; warp < groups && q < COLS / 4; q += groups) {
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int k = 0; k < kGroup; ++k) {
@@ -343,8 +350,37 @@ __global__ void __launch_bounds__(kLeafMax, 2)
       for (int e = 0; e < 4; ++e) {
         const int row = warp * kGroup + 16 * mt + gid + (e >= 2 ? 8 : 0);
         const int64_t j = j0 + 8 * nt + 2 * tig + (e & 1);
-        if (row < s && j < m) X[j * ldx + off + row] = __half_as_ushort(__float2half_rn(c[mt][nt][e]));
+        if (row < s && j < m) X[j * ldx + xoff + row] = __half_as_ushort(__float2half_rn(c[mt][nt][e]));
       }
+}
+
+template <int COLS>
+__global__ void __launch_bounds__(kLeafMax, 2)
+    trsm_leaf_kernel(const uint16_t* __restrict__ A, int64_t lda, uint16_t* __restrict__ X,
+                     int64_t ldx, int64_t off, int s, int64_t m, int chained) {
+  trsm_leaf_body<COLS>(A, lda, X, ldx, off, off, s, m, chained, false, static_cast<int64_t>(blockIdx.x) * COLS);
+}
+
+// The inverses of every diagonal block of a solve, in one launch: block
+// b = blockIdx.y (order s_b at (off_b, off_b)) solves its transpose against
+// the identity, so W_b = W + b·kLeafMax² (column-major, pitch kLeafMax)
+// receives the transpose of its inverse: W_b[k·kLeafMax + i] = L_b⁻¹(k, i).
+// The first launch of its solve: waits for the previous launch on the
+// stream before anything else (the previous solve may still read W).
+__global__ void __launch_bounds__(kLeafMax, 2)
+    trsm_inverse_kernel(const uint16_t* __restrict__ A, int64_t lda, uint16_t* __restrict__ W,
+                        const TriLeaves leaves) {
+  constexpr int COLS = 32;
+  const int b = blockIdx.y;
+  const int s = static_cast<int>(leaves.size[b]);
+  const int64_t j0 = static_cast<int64_t>(blockIdx.x) * COLS;
+  if (j0 >= s) {  // right-hand sides past the block's order: nothing to solve
+    grid_dependency_wait();
+    grid_launch_dependents();
+    return;
+  }
+  trsm_leaf_body<COLS>(A, lda, W + static_cast<int64_t>(b) * kLeafMax * kLeafMax, kLeafMax, leaves.off[b], 0, s,
+                       s, 0, true, j0);
 }
 
 // X(:, j) = alpha · B(:, j) for the n × m column-major operands; FP16 in and
@@ -447,6 +483,25 @@ cudaError_t launch_trsm_leaf(const uint16_t* A, int64_t lda, uint16_t* X, int64_
     default:
       return launch_width<32>(A, lda, X, ldx, off, s, m, threads, chained, stream);
   }
+}
+
+cudaError_t launch_trsm_inverse(const uint16_t* A, int64_t lda, uint16_t* W, const TriLeaves& leaves,
+                                cudaStream_t stream) {
+  if (leaves.count < 1 || leaves.count > kMaxLeaves) return cudaErrorInvalidValue;
+  for (int b = 0; b < leaves.count; ++b)
+    if (leaves.size[b] < 1 || leaves.size[b] > kLeafMax) return cudaErrorInvalidValue;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  static std::atomic<bool> attr_done[kMaxDevices];
+  if (!attr_done[dev]) {
+    e = cudaFuncSetAttribute(trsm_inverse_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, leaf_smem<32>());
+    if (e != cudaSuccess) return e;
+    attr_done[dev] = true;
+  }
+  PdlLaunch l(dim3(kLeafMax / 32, static_cast<unsigned>(leaves.count)), dim3(kLeafMax), leaf_smem<32>(), stream);
+  return cudaLaunchKernelEx(&l.cfg, trsm_inverse_kernel, A, lda, W, leaves);
 }
 
 cudaError_t launch_scale_copy(const uint16_t* B, int64_t ldb, uint16_t* X, int64_t ldx, int64_t n,

@@ -28,8 +28,10 @@ def trsm_inputs(n, m, seed):
     return np.ascontiguousarray(a_col.T), np.ascontiguousarray(b_col.T)
 
 
-def run_trsm(a, b, alpha=1.0, pad=(0, 0, 0), poison_upper=False, in_place=False):
-    """Column-major device buffers with pitches n + pad; X (n, m) comes back."""
+def run_trsm(a, b, alpha=1.0, pad=(0, 0, 0), poison_upper=False, in_place=False, ws=False):
+    """Column-major device buffers with pitches n + pad; X (n, m) comes back.
+    ws: through hgemm_trsm_ws, with a workspace of the reported size followed
+    by a sentinel band that must stay untouched."""
     torch = torch_cuda()
     n, m = b.shape
     lda, ldb, ldx = n + pad[0], n + pad[1], n + pad[2]
@@ -47,9 +49,17 @@ def run_trsm(a, b, alpha=1.0, pad=(0, 0, 0), poison_upper=False, in_place=False)
         dx = db
     else:
         dx = to_device(np.full((m, ldx), 5.0, np.float16))
-    tc.hgemm_trsm(da, lda, db, ldb, dx, ldx, n, m, alpha)
+    if ws:
+        need = tc.hgemm_trsm_workspace_size(n)
+        assert need > 0 and need % (2 * 256 * 256) == 0
+        work = torch.full((need + 4096,), 0x5A, dtype=torch.uint8, device="cuda")
+        tc.hgemm_trsm_ws(da, lda, db, ldb, dx, ldx, n, m, alpha, work, need)
+    else:
+        tc.hgemm_trsm(da, lda, db, ldb, dx, ldx, n, m, alpha)
     assert tc.hgemm_device_status() == tc.HGEMM_OK
     torch.cuda.synchronize()
+    if ws:
+        assert np.all(work[need:].cpu().numpy() == 0x5A), "past the workspace was written"
     out = dx.cpu().numpy()
     fill = 7.0 if in_place else 5.0
     assert np.all(out[:, n:] == fill), "pitch padding of X was written"
@@ -58,68 +68,81 @@ def run_trsm(a, b, alpha=1.0, pad=(0, 0, 0), poison_upper=False, in_place=False)
     return np.ascontiguousarray(out[:, :n].T)
 
 
+@pytest.mark.parametrize("ws", [False, True])
 @pytest.mark.parametrize("n,m", [(1, 1), (64, 32), (200, 7), (256, 100), (257, 64), (300, 136),
                                  (512, 256), (1000, 128), (4096, 256)])
-def test_trsm_matches_oracle(n, m):
+def test_trsm_matches_oracle(n, m, ws):
+    """ws: the diagonal blocks solved as products by their inverses (blocks
+    of order 129 or 200, not multiples of 8, by substitution)."""
     a, b = trsm_inputs(n, m, seed=n + m)
     ref = oracle.trsm(a, b, nthreads=oracle_threads())
-    assert_close(run_trsm(a, b), ref, what=f"trsm {n}x{m}")
+    assert_close(run_trsm(a, b, ws=ws), ref, what=f"trsm {n}x{m} ws={ws}")
 
 
+@pytest.mark.parametrize("ws", [False, True])
 @pytest.mark.parametrize("m", [4096, 8192, 8195])
-def test_trsm_leaf_widths(m):
+def test_trsm_leaf_widths(m, ws):
     """Many right-hand sides: the diagonal solves take 16 and 32 of them per
-    thread block (and a ragged last block)."""
+    thread block (and a ragged last block); with the workspace, products by
+    the inverses over 256-row tiles and a ragged last tile."""
     n = 300
     a, b = trsm_inputs(n, m, seed=m)
     ref = oracle.trsm(a, b, nthreads=oracle_threads())
-    assert_close(run_trsm(a, b), ref, what=f"trsm {n}x{m}")
+    assert_close(run_trsm(a, b, ws=ws), ref, what=f"trsm {n}x{m} ws={ws}")
 
 
-def test_trsm_reads_only_the_lower_triangle():
-    n, m = 700, 96
+@pytest.mark.parametrize("ws", [False, True])
+def test_trsm_reads_only_the_lower_triangle(ws):
+    n, m = 704, 96
     a, b = trsm_inputs(n, m, seed=7)
     ref = oracle.trsm(a, b, nthreads=oracle_threads())
-    assert_close(run_trsm(a, b, poison_upper=True), ref, what="NaN above the diagonal")
+    assert_close(run_trsm(a, b, poison_upper=True, ws=ws), ref, what=f"NaN above the diagonal ws={ws}")
 
 
+@pytest.mark.parametrize("ws", [False, True])
 @pytest.mark.parametrize("pad", [(8, 16, 8), (3, 5, 1)])
-def test_trsm_pitches_and_alpha(pad):
+def test_trsm_pitches_and_alpha(pad, ws):
     """Wider pitches (multiples of 8: tensor-core updates; odd ones: the
-    generic loader) and a scale factor."""
+    generic loader, and with the workspace the substitution kernel) and a
+    scale factor."""
     n, m = 600, 72
     a, b = trsm_inputs(n, m, seed=11 + pad[0])
     ref = oracle.trsm(a, b, alpha=-1.5, nthreads=oracle_threads())
-    assert_close(run_trsm(a, b, alpha=-1.5, pad=pad), ref, what=f"trsm pad {pad}")
+    assert_close(run_trsm(a, b, alpha=-1.5, pad=pad, ws=ws), ref, what=f"trsm pad {pad} ws={ws}")
 
 
+@pytest.mark.parametrize("ws", [False, True])
 @pytest.mark.parametrize("alpha", [1.0, 0.25])
-def test_trsm_in_place(alpha):
+def test_trsm_in_place(alpha, ws):
     n, m = 800, 40
     a, b = trsm_inputs(n, m, seed=19)
     ref = oracle.trsm(a, b, alpha=alpha, nthreads=oracle_threads())
-    assert_close(run_trsm(a, b, alpha=alpha, pad=(0, 8, 0), in_place=True), ref,
-                 what=f"trsm in place alpha {alpha}")
+    assert_close(run_trsm(a, b, alpha=alpha, pad=(0, 8, 0), in_place=True, ws=ws), ref,
+                 what=f"trsm in place alpha {alpha} ws={ws}")
 
 
-def test_trsm_residual_identity():
-    """A = I: X = alpha·B rounded once, exactly."""
+@pytest.mark.parametrize("ws", [False, True])
+def test_trsm_residual_identity(ws):
+    """A = I: X = alpha·B rounded once, exactly (the inverses are the
+    identity, so the products by them are exact too)."""
     n, m = 520, 33
     _, b = trsm_inputs(n, m, seed=23)
     a = np.eye(n, dtype=np.float16)
-    got = run_trsm(a, b, alpha=0.5)
+    got = run_trsm(a, b, alpha=0.5, ws=ws)
     assert np.array_equal(got, (b.astype(np.float32) * 0.5).astype(np.float16))
 
 
-def test_trsm_repeatable():
+@pytest.mark.parametrize("ws", [False, True])
+def test_trsm_repeatable(ws):
     n, m = 1024, 64
     a, b = trsm_inputs(n, m, seed=3)
-    first = run_trsm(a, b)
+    first = run_trsm(a, b, ws=ws)
     for _ in range(3):
-        assert np.array_equal(run_trsm(a, b).view(np.uint16), first.view(np.uint16))
+        assert np.array_equal(run_trsm(a, b, ws=ws).view(np.uint16), first.view(np.uint16))
 
 
-def test_trsm_8192_sampled_columns():
+@pytest.mark.parametrize("ws", [False, True])
+def test_trsm_8192_sampled_columns(ws):
     """The 8192×8192 workload in the benchmark's launch configuration: column
     j of X depends on column j of B alone, so the oracle solves a sample of
     the columns (first, last and spread ones)."""
@@ -128,10 +151,40 @@ def test_trsm_8192_sampled_columns():
     n, m = spec["n"], spec["m"]
     da, db = to_device(a_col), to_device(b_col)
     dx = torch.empty((m, n), dtype=torch.float16, device="cuda")
-    tc.hgemm_trsm(da, n, db, n, dx, n, n, m, 1.0)
+    if ws:
+        work = torch.empty(tc.hgemm_trsm_workspace_size(n), dtype=torch.uint8, device="cuda")
+        tc.hgemm_trsm_ws(da, n, db, n, dx, n, n, m, 1.0, work)
+    else:
+        tc.hgemm_trsm(da, n, db, n, dx, n, n, m, 1.0)
     assert tc.hgemm_device_status() == tc.HGEMM_OK
     torch.cuda.synchronize()
     cols = np.array([0, 1, 63, 64, 255, 1000, 4097, 8000, m - 1])
     got = dx[torch.from_numpy(cols).cuda()].cpu().numpy().T
     ref = oracle.trsm(a_col.T, b_col[cols].T, nthreads=oracle_threads())
     assert_close(got, ref, what="trsm_8192 sampled columns")
+
+
+def test_trsm_workspace_arguments():
+    """Workspace size per diagonal block, and the arguments hgemm_trsm_ws
+    refuses: no workspace, one too small, a misaligned one, one overlapping X."""
+    torch = torch_cuda()
+    assert tc.hgemm_trsm_workspace_size(0) == 0
+    assert tc.hgemm_trsm_workspace_size(256) == 2 * 256 * 256
+    assert tc.hgemm_trsm_workspace_size(8192) == 32 * 2 * 256 * 256
+    assert tc.hgemm_trsm_workspace_size(300) == 2 * 2 * 256 * 256   # blocks of 192 and 108
+    n, m = 512, 64
+    a, b = trsm_inputs(n, m, seed=5)
+    da, db = to_device(np.ascontiguousarray(a.T)), to_device(np.ascontiguousarray(b.T))
+    dx = torch.empty((m, n), dtype=torch.float16, device="cuda")
+    need = tc.hgemm_trsm_workspace_size(n)
+    work = torch.empty(need + 64, dtype=torch.uint8, device="cuda")
+    with pytest.raises(tc.HgemmError):
+        tc.hgemm_trsm_ws(da, n, db, n, dx, n, n, m, 1.0, None, need)
+    with pytest.raises(tc.HgemmError):
+        tc.hgemm_trsm_ws(da, n, db, n, dx, n, n, m, 1.0, work, need - 1)
+    with pytest.raises(tc.HgemmError):
+        tc.hgemm_trsm_ws(da, n, db, n, dx, n, n, m, 1.0, work.data_ptr() + 8, need)
+    big = torch.empty((m, n + need // 2), dtype=torch.float16, device="cuda")
+    with pytest.raises(tc.HgemmError) as err:
+        tc.hgemm_trsm_ws(da, n, db, n, big, n, n, m, 1.0, big.data_ptr() + 2 * n * (m - 1), need)
+    assert err.value.status == tc.HGEMM_ERR_ALIAS
