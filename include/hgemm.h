@@ -247,6 +247,36 @@ HGEMM_API int hgemm_trsm_ws(const hgemm_half_t *A, int64_t lda, const hgemm_half
                   void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * hgemm_trsm_noalloc — hgemm_trsm_ws for callers that cannot allocate device
+ * memory: code whose device memory all belongs to another allocator (a
+ * framework's caching pool, a fixed budget reserved up front) and which may
+ * not call cudaMalloc itself, or which must not pay cudaMalloc's implicit
+ * synchronisation. The pages have no counterpart of this entry point; it is
+ * an addition for such callers.
+ *
+ * Same system, operands, results and return values as hgemm_trsm_ws, whose
+ * workspace here is a fixed array of HGEMM_TRSM_NOALLOC_MAX_BYTES (4 MiB)
+ * inside the library, present on every device that loads the library until
+ * the process exits. Nothing is allocated: no cudaMalloc or cudaFree, no
+ * allocating library call. Limit: triangles whose recursion has at most 32
+ * diagonal blocks, which is every n ≤ 8192; a larger n
+ * (hgemm_trsm_workspace_size(n) > HGEMM_TRSM_NOALLOC_MAX_BYTES) returns
+ * HGEMM_ERR_INVALID_ARG and enqueues nothing.
+ *
+ * The first call on a device (made with that device current) looks up the
+ * array's device address once (cudaGetSymbolAddress) and keeps it; make that
+ * first call before any stream capture on the device. Every call on a device
+ * shares the one array, which keeps the last call's contents (each call
+ * writes every entry it reads, so nothing needs clearing): calls whose work
+ * overlaps on the GPU (other streams, other host threads) race on it and
+ * must be ordered by the caller, e.g. issued on one stream.
+ */
+#define HGEMM_TRSM_NOALLOC_MAX_BYTES (4u << 20)
+HGEMM_API int hgemm_trsm_noalloc(const hgemm_half_t *A, int64_t lda, const hgemm_half_t *B, int64_t ldb,
+                       hgemm_half_t *X, int64_t ldx, int64_t n, int64_t m, float alpha,
+                       cudaStream_t stream);
+
+/*
  * hgemm_host — the same product for operands held in HOST memory.
  *
  * Copies hA -> dA (M*K values) and hB -> dB (N*K values), computes

@@ -28,7 +28,7 @@ __all__ = [
     "HgemmError", "library_path", "load", "hgemm", "hgemm_host", "hgemm_select_path",
     "hgemm_force_path", "hgemm_device_status", "hgemm_last_cuda_error",
     "hgemm_status_string", "hgemm_version", "hgemm_set_wait_timeout", "hgemm_debug_inject",
-    "hgemm_force_split", "hgemm_ex", "hgemm_strided", "hgemm_trmm", "hgemm_trsm", "hgemm_trsm_ws", "hgemm_trsm_workspace_size", "hgemm_layout", "HGEMM_TRMM_MAX_N",
+    "hgemm_force_split", "hgemm_ex", "hgemm_strided", "hgemm_trmm", "hgemm_trsm", "hgemm_trsm_ws", "hgemm_trsm_workspace_size", "hgemm_trsm_noalloc", "hgemm_layout", "HGEMM_TRMM_MAX_N", "HGEMM_TRSM_NOALLOC_MAX_BYTES",
     "HGEMM_A_ROW_MAJOR", "HGEMM_A_COL_MAJOR", "HGEMM_B_COL_MAJOR", "HGEMM_B_ROW_MAJOR",
     "HGEMM_INJECT_NONE", "HGEMM_INJECT_DROP_ARRIVAL", "matmul",
 ]
@@ -40,6 +40,7 @@ HGEMM_ERR_UNSUPPORTED_DEVICE = -3
 HGEMM_ERR_CUDA = -4
 HGEMM_ERR_TIMEOUT = -5
 HGEMM_TRMM_MAX_N = 16384
+HGEMM_TRSM_NOALLOC_MAX_BYTES = 4 << 20
 HGEMM_A_ROW_MAJOR = 0
 HGEMM_A_COL_MAJOR = 1
 HGEMM_B_COL_MAJOR = 0
@@ -105,6 +106,8 @@ def load():
     lib.hgemm_trsm_ws.restype = i32
     lib.hgemm_trsm_workspace_size.argtypes = [i64]
     lib.hgemm_trsm_workspace_size.restype = ctypes.c_size_t
+    lib.hgemm_trsm_noalloc.argtypes = [vp, i64, vp, i64, vp, i64, i64, i64, ctypes.c_float, vp]
+    lib.hgemm_trsm_noalloc.restype = i32
     lib.hgemm_layout.argtypes = [i32, i32, vp, i64, vp, i64, vp, i64, i64, i64, i64, ctypes.c_float,
                                  ctypes.c_float, vp, i32, vp]
     lib.hgemm_layout.restype = i32
@@ -240,6 +243,16 @@ def hgemm_trsm(A, lda: int, B, ldb: int, X, ldx: int, n: int, m: int, alpha: flo
     X may be B itself (same pitch) to solve in place (see hgemm.h)."""
     _raise_on(load().hgemm_trsm(_ptr(A), lda, _ptr(B), ldb, _ptr(X), ldx, n, m, float(alpha),
                                 _stream(stream)), "hgemm_trsm")
+
+
+def hgemm_trsm_noalloc(A, lda: int, B, ldb: int, X, ldx: int, n: int, m: int, alpha: float = 1.0,
+                       stream=None) -> None:
+    """hgemm_trsm_ws with the library's fixed device workspace instead of one
+    from the caller: allocates nothing (for callers that cannot allocate);
+    n up to 8192 (see hgemm.h for the set-up on first use and the sharing
+    of the workspace between calls)."""
+    _raise_on(load().hgemm_trsm_noalloc(_ptr(A), lda, _ptr(B), ldb, _ptr(X), ldx, n, m, float(alpha),
+                                        _stream(stream)), "hgemm_trsm_noalloc")
 
 
 def hgemm_trsm_workspace_size(n: int) -> int:

@@ -984,6 +984,45 @@ int hgemm_trsm_ws(const hgemm_half_t* A, int64_t lda, const hgemm_half_t* B, int
                    stream);
 }
 
+// ---------------------------------------------------------------------------
+// hgemm_trsm_noalloc: hgemm_trsm_ws for callers that cannot allocate device
+// memory. Its workspace is this fixed array, part of the library's module on
+// every device that loads it (4 MiB there until the process exits). In host
+// code the name g_trsm_noalloc_scratch stands for a host-side shadow, not the
+// device memory, so the array's device address is taken once per device with
+// cudaGetSymbolAddress (with that device current) and passed on.
+namespace {
+
+__device__ __align__(256) uint16_t g_trsm_noalloc_scratch[HGEMM_TRSM_NOALLOC_MAX_BYTES / 2];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kMaxDevices] = {};  // device address of the array per device (null: not yet)
+
+}  // namespace
+
+int hgemm_trsm_noalloc(const hgemm_half_t* A, int64_t lda, const hgemm_half_t* B, int64_t ldb,
+                       hgemm_half_t* X, int64_t ldx, int64_t n, int64_t m, float alpha, cudaStream_t stream) {
+  if (n < 0 || m < 0) return HGEMM_ERR_INVALID_ARG;
+  if (n == 0 || m == 0) return HGEMM_OK;
+  const size_t need = hgemm_trsm_workspace_size(n);
+  if (need == 0 || need > HGEMM_TRSM_NOALLOC_MAX_BYTES) return HGEMM_ERR_INVALID_ARG;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= kMaxDevices) return HGEMM_ERR_UNSUPPORTED_DEVICE;
+  void* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_addr[dev]) {
+      void* p = nullptr;
+      if ((e = cudaGetSymbolAddress(&p, g_trsm_noalloc_scratch)) != cudaSuccess) return cuda_fail(e);
+      g_noalloc_addr[dev] = p;
+    }
+    scratch = g_noalloc_addr[dev];
+  }
+  return hgemm_trsm_ws(A, lda, B, ldb, X, ldx, n, m, alpha, scratch, HGEMM_TRSM_NOALLOC_MAX_BYTES, stream);
+}
+
 int hgemm_host(const hgemm_half_t* hA, const hgemm_half_t* hB, hgemm_half_t* hC, int64_t M,
                int64_t N, int64_t K, hgemm_half_t* dA, hgemm_half_t* dB, hgemm_half_t* dC,
                cudaStream_t stream) {
