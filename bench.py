@@ -99,6 +99,12 @@ def trmm_launches(n, leaf=256):
     walk(0, n, 0)
     count = 1
     for lv in levels.values():
+        # with the tensor-core leaves (n a multiple of 64), a leaf carries the
+        # update of the block whose first half it is
+        if n % 64 == 0:
+            lv = [u for u in lv if u[1] > leaf]
+        if not lv:
+            continue
         off0, s1, s2 = lv[0]
         shift = lv[1][0] - off0 if len(lv) > 1 else 0
         batched = (len(lv) > 1 and s1 % 256 == 0 and s2 % 64 == 0 and shift > 0 and

@@ -766,7 +766,26 @@ int hgemm_trmm(const hgemm_half_t* A, int64_t lda, const hgemm_half_t* B, int64_
       args.epi = scale;
       args.C = reinterpret_cast<const uint16_t*>(C);
       args.ldc = ldc;
-      e = hg::launch_tri_leaves_tc(mx, ml, mc, args, leaves, stream);
+      // An update whose block's first half is a leaf (s1 ≤ kTrmmLeaf) adds
+      // into exactly that leaf's columns of C before any other update does:
+      // the leaf carries it (its product runs on over A21 and B2), and it
+      // leaves the list of updates.
+      hg::TriLeafExt ext{};
+      for (auto& lv : levels) {
+        std::vector<Update> rest;
+        for (const Update& u : lv) {
+          int b = -1;
+          if (u.s1 <= kTrmmLeaf)
+            for (int k = 0; k < leaves.count; ++k)
+              if (leaves.off[k] == u.off && leaves.size[k] == u.s1) b = k;
+          if (b >= 0)
+            ext.ext[b] = static_cast<int32_t>(u.s2);
+          else
+            rest.push_back(u);
+        }
+        lv.swap(rest);
+      }
+      e = hg::launch_tri_leaves_tc(mx, ml, mc, args, leaves, ext, stream);
     }
   }
   if (!tc_leaves) {
@@ -817,6 +836,7 @@ int hgemm_trmm(const hgemm_half_t* A, int64_t lda, const hgemm_half_t* B, int64_
   if (tp) lock = std::unique_lock<std::mutex>(tp->mu);
   for (int d = static_cast<int>(levels.size()) - 1; d >= 0; --d) {
     const auto& lv = levels[d];
+    if (lv.empty()) continue;  // every update of the level carried by a leaf
     if (lv.size() == 1) {
       if ((rc = issue(lv[0], stream)) != HGEMM_OK) return rc;
       continue;

@@ -31,6 +31,12 @@
 //     the accumulator is double-buffered in TMEM (2 × 256 columns) and the
 //     epilogue warps (TMEM → alpha·acc → FP16 round to nearest even →
 //     swizzled staging → TMA store) drain one unit while the next one runs;
+//   * a leaf may also carry the off-diagonal update of the block whose first
+//     half it is (C1 += alpha·A21ᵀ·B2 in the page's recursion): its product
+//     then runs on over K columns [off+s, off+s+ext) with whole rows of the
+//     second operand (A21 lies below the diagonal), processed first (N = s,
+//     initialising the accumulator), so the update costs no launch, no
+//     read-modify-write of C and no intermediate FP16 rounding;
 //   * every wait is bounded, as in the other tensor-core kernels (watchdog
 //     word, abort flag, drain, TMEM freed).
 #include <atomic>
@@ -104,7 +110,7 @@ template <bool FUSED>
 __global__ void __launch_bounds__(192, 1)
     hgemm_tri_leaves_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmL,
                                const __grid_constant__ CUtensorMap tmC, const TcArgs p,
-                               const TriLeaves leaves) {
+                               const TriLeaves leaves, const TriLeafExt lext) {
   using Cfg = LeafCfg;
   constexpr int STAGES = Cfg::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -167,8 +173,12 @@ __global__ void __launch_bounds__(192, 1)
         const int b = t / p.num_m, mt = t - b * p.num_m;
         const int off = static_cast<int>(leaves.off[b]);
         const int nkb = static_cast<int>(leaves.size[b]) / Cfg::BK;
-        for (int j = 0; j < nkb; ++j) {
-          const int kb = nkb - 1 - j;
+        const int nke = lext.ext[b] / Cfg::BK;  // K blocks of the carried update
+        for (int j = 0; j < nke + nkb; ++j) {
+          // update blocks first (all nkb row boxes), then the triangle's,
+          // widest first (kb + 1 row boxes)
+          const int kb = j < nke ? nkb - 1 : nkb - 1 - (j - nke);
+          const int x = j < nke ? off + nkb * Cfg::BK + j * Cfg::BK : off + kb * Cfg::BK;
           if (!wait_phase(empty_bar(stage), phase ^ 1u, wd, kWdProducerEmpty)) {
             ok = false;
             break;
@@ -176,7 +186,6 @@ __global__ void __launch_bounds__(192, 1)
           if (!(p.inject == 1 && issued == 0))  // testing aid: withhold one arrival
             mbar_arrive_expect_tx(full_bar(stage),
                                   static_cast<uint32_t>(Cfg::A_BYTES + (kb + 1) * Cfg::L_BOX_BYTES));
-          const int x = off + kb * Cfg::BK;
           tma_load_2d(sA + stage * Cfg::A_BYTES, &tmX, full_bar(stage), x, mt * Cfg::BM);
           for (int r = 0; r <= kb; ++r)
             tma_load_2d(sB + stage * Cfg::B_BYTES + r * Cfg::L_BOX_BYTES, &tmL, full_bar(stage), x,
@@ -212,6 +221,7 @@ __global__ void __launch_bounds__(192, 1)
     for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
       const int b = t / p.num_m;
       const int nkb = static_cast<int>(leaves.size[b]) / Cfg::BK;
+      const int nke = lext.ext[b] / Cfg::BK;
       int free_acc = 1;
       if (lane == 0) free_acc = wait_phase(acce_bar(acc), acc_phase ^ 1u, wd, kWdMmaAccEmpty) ? 1 : 0;
       if (!__shfl_sync(0xffffffffu, free_acc, 0)) {
@@ -220,15 +230,16 @@ __global__ void __launch_bounds__(192, 1)
       }
       tc_fence_after_sync();
       const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * Cfg::ACC_COLS);
-      for (int j = 0; j < nkb; ++j) {
-        const int kb = nkb - 1 - j;
+      for (int j = 0; j < nke + nkb; ++j) {
+        const bool update = j < nke;  // a K block of the carried update: whole rows, no mask
+        const int kb = update ? nkb - 1 : nkb - 1 - (j - nke);
         // every lane waits for the copy: its masking stores come after it
         const int landed = wait_phase(full_bar(stage), phase, wd, kWdMmaFull) ? 1 : 0;
         if (!__all_sync(0xffffffffu, landed)) {
           ok = false;
           break;
         }
-        mask_diagonal_block(smem + Cfg::OFF_B + stage * Cfg::B_BYTES + kb * Cfg::L_BOX_BYTES, lane);
+        if (!update) mask_diagonal_block(smem + Cfg::OFF_B + stage * Cfg::B_BYTES + kb * Cfg::L_BOX_BYTES, lane);
         fence_proxy_async_smem();  // the tensor cores read the stage through the async proxy
         __syncwarp();
         if (lane == 0) {
@@ -321,12 +332,14 @@ __global__ void __launch_bounds__(192, 1)
 }  // namespace
 
 cudaError_t launch_tri_leaves_tc(const CUtensorMap& x, const CUtensorMap& l, const CUtensorMap& c,
-                                 const TcArgs& args, const TriLeaves& leaves, cudaStream_t stream) {
+                                 const TcArgs& args, const TriLeaves& leaves, const TriLeafExt& ext,
+                                 cudaStream_t stream) {
   static std::atomic<bool> attr_done[2][64];
   const int fused = args.epi.mode != 0 ? 1 : 0;
   auto kern = fused ? hgemm_tri_leaves_tc_kernel<true> : hgemm_tri_leaves_tc_kernel<false>;
   for (int b = 0; b < leaves.count; ++b)
-    if (leaves.size[b] <= 0 || leaves.size[b] > LeafCfg::MAX_S || leaves.size[b] % LeafCfg::BK != 0)
+    if (leaves.size[b] <= 0 || leaves.size[b] > LeafCfg::MAX_S || leaves.size[b] % LeafCfg::BK != 0 ||
+        ext.ext[b] < 0 || ext.ext[b] > LeafCfg::MAX_S || ext.ext[b] % LeafCfg::BK != 0)
       return cudaErrorInvalidValue;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -337,7 +350,7 @@ cudaError_t launch_tri_leaves_tc(const CUtensorMap& x, const CUtensorMap& l, con
     if (dev >= 0 && dev < 64) attr_done[fused][dev] = true;
   }
   PdlLaunch pl(dim3(static_cast<unsigned>(args.grid)), dim3(LeafCfg::THREADS), LeafCfg::SMEM_BYTES, stream);
-  return cudaLaunchKernelEx(&pl.cfg, kern, x, l, c, args, leaves);
+  return cudaLaunchKernelEx(&pl.cfg, kern, x, l, c, args, leaves, ext);
 }
 
 }  // namespace hg

@@ -137,8 +137,16 @@ cudaError_t launch_tri_leaves(const PlainArgs& args, const TriLeaves& leaves, in
 // (see hgemm_trileaf.cu): x maps Bᵀ (m × n, 128×64 boxes), l maps the rows
 // of the triangle (column i of A as row i, n × n, 64×64 boxes), c maps Cᵀ
 // (m × n, 32×64 boxes); args.num_m row tiles of 128 per leaf.
+// ext[b]: K columns past leaf b's own block that its product also covers,
+// [off_b + s_b, off_b + s_b + ext[b]) (whole rows of the second operand:
+// the off-diagonal update of the block whose first half leaf b is), a
+// multiple of 64, or 0.
+struct TriLeafExt {
+  int32_t ext[kMaxLeaves];
+};
 cudaError_t launch_tri_leaves_tc(const CUtensorMap& x, const CUtensorMap& l, const CUtensorMap& c,
-                                 const TcArgs& args, const TriLeaves& leaves, cudaStream_t stream);
+                                 const TcArgs& args, const TriLeaves& leaves, const TriLeafExt& ext,
+                                 cudaStream_t stream);
 
 // Triangular solve Aᵀ·X = alpha·B (see hgemm_trsm.cu): the largest diagonal
 // block solved by substitution; X(:, j) = alpha·B(:, j) over n × m
