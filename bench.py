@@ -80,7 +80,7 @@ DESCRIPTIONS = {
 }
 
 
-def trmm_launches(n, leaf=256):
+def trmm_launches(n, m, leaf=256):
     """Kernel launches of one hgemm_trmm (pitches n, aligned operands): the
     batched leaves, then per recursion level either one batched launch (two or
     more equal updates at a constant stride, whole 256-column tiles and whole
@@ -99,10 +99,10 @@ def trmm_launches(n, leaf=256):
     walk(0, n, 0)
     count = 1
     for lv in levels.values():
-        # with the tensor-core leaves (n a multiple of 64), a leaf carries the
-        # update of the block whose first half it is
+        # with the tensor-core leaves (n a multiple of 64), the leaves carry
+        # the updates of at most 2^33 multiply-adds
         if n % 64 == 0:
-            lv = [u for u in lv if u[1] > leaf]
+            lv = [u for u in lv if m * u[1] * u[2] > 2 ** 33]
         if not lv:
             continue
         off0, s1, s2 = lv[0]
@@ -118,7 +118,7 @@ def trmm_flops(spec):
     return float(spec["n"]) * (spec["n"] + 1) * spec["m"]
 
 
-def trsm_launches(n, leaf=256):
+def trsm_launches(n, m=None, leaf=256):
     """Kernel launches of one hgemm_trsm (alpha = 1, out of place): the scaled
     copy, one diagonal solve per leaf and one GEMM per split block."""
     def count(s):
@@ -593,7 +593,7 @@ def run_tri_ours(args, spec, a_col, b_col, world, rank, local):
                        "path": "hgemm_trsm_ws" if op == "trsm" and not args.no_workspace else ops["call"],
                        "parallelism": f"replicas x{world}"},
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": args.steps * (ops["launches"](n) + (1 if op == "trsm" and not args.no_workspace else 0)),
+            "gpu_launches": args.steps * (ops["launches"](n, m) + (1 if op == "trsm" and not args.no_workspace else 0)),
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)

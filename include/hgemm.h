@@ -179,8 +179,11 @@ HGEMM_API int hgemm_layout(int a_layout, int b_layout, const hgemm_half_t *A, in
  * recursion (§2.1, §2.2): a block splits into halves; C1 = A11ᵀ·B1, then the
  * GEMM update C1 += A21ᵀ·B2 (hgemm's accumulate epilogue), then C2 = A22ᵀ·B2;
  * blocks of order ≤ 256 (the page's threshold) are leaves, all computed by
- * one launch of masked products. Storage is FP16 (each update rounds its
- * block once), accumulation FP32 within each product. C must not overlap A
+ * one launch of masked products, which also carries the updates of at most
+ * 2^33 multiply-adds (m·s1·s2) when n is a multiple of 64: a leaf's product
+ * then runs on over those updates' columns of A and B (the same sum, one FP16
+ * rounding fewer). Storage is FP16 (each update rounds its block once),
+ * accumulation FP32 within each product. C must not overlap A
  * or B (HGEMM_ERR_ALIAS); the calls are enqueued on `stream`. Same return
  * values as hgemm.
  */
@@ -313,8 +316,11 @@ HGEMM_API int hgemm_select_path(const void *A, const void *B, const void *C,
  * HGEMM_PATH_TC_PAIR, HGEMM_PATH_TC_WIDE, HGEMM_PATH_SKINNY or
  * HGEMM_PATH_GENERIC, or -1 to
  * restore automatic selection. A forced TMA path still falls back to GENERIC
- * when the operands are not aligned for TMA. Returns HGEMM_OK or
- * HGEMM_ERR_INVALID_ARG.
+ * when the operands are not aligned for TMA. In hgemm_trmm a forced path runs
+ * every off-diagonal update as a product of its own (none is carried by the
+ * leaves; HGEMM_PATH_GENERIC also computes the leaves on the generic
+ * kernel); in hgemm_trsm_ws it solves the diagonal blocks by substitution.
+ * Returns HGEMM_OK or HGEMM_ERR_INVALID_ARG.
  *
  * Tuning overrides read once per process from the environment:
  * HGEMM_GROUP_M (a positive integer) sets how many M-tiles the tensor-core

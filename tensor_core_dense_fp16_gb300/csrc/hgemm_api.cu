@@ -7,6 +7,7 @@
 // never allocates device memory: buffers come from the caller, who owns them
 // ("GPU架构与CUDA", 内存池分配器: allocation belongs to a caching allocator
 // such as PyTorch's, not to every call).
+#include <algorithm>
 #include <atomic>
 #include <cstdint>
 #include <vector>
@@ -27,6 +28,12 @@ namespace {
 constexpr int kMaxDevices = 64;
 constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;  // 2 s per wait
 constexpr int64_t kTrmmLeaf = 256;  // diagonal blocks of at most this order are leaves
+// Updates of at most this many multiply-adds (m·s1·s2; 8192 × 1024 × 1024)
+// are carried by the tensor-core leaves. Measured: at n = m = 8192 carrying
+// the updates of blocks up to 1024, 2048 and 4096 gave 407, 397 and 400 µs
+// (the 8192 × 2048 × 2048 updates run better on the pair kernel); at
+// n = 4096, m = 256 (every update small) 42.5, 37.9 and 34.5 µs.
+constexpr int64_t kTrmmFoldMacs = int64_t(1) << 33;
 
 thread_local int t_last_cuda_error = 0;
 std::atomic<int> g_forced_path{-1};
@@ -766,24 +773,47 @@ int hgemm_trmm(const hgemm_half_t* A, int64_t lda, const hgemm_half_t* B, int64_
       args.epi = scale;
       args.C = reinterpret_cast<const uint16_t*>(C);
       args.ldc = ldc;
-      // An update whose block's first half is a leaf (s1 ≤ kTrmmLeaf) adds
-      // into exactly that leaf's columns of C before any other update does:
-      // the leaf carries it (its product runs on over A21 and B2), and it
-      // leaves the list of updates.
+      // The update of a block adds into the leaves of its first half before
+      // any larger block's update does; when it is small (kTrmmFoldMacs),
+      // those leaves carry it: each leaf's product runs on over the update's K
+      // columns [off+s1, off+s). Taken deepest first, the carried ranges of
+      // a leaf join into one range right after it (each block's second half
+      // starts where the first half around the leaf ends); if they do not
+      // (checked), nothing is carried. The leaves are then launched longest
+      // first.
       hg::TriLeafExt ext{};
-      for (auto& lv : levels) {
-        std::vector<Update> rest;
-        for (const Update& u : lv) {
-          int b = -1;
-          if (u.s1 <= kTrmmLeaf)
-            for (int k = 0; k < leaves.count; ++k)
-              if (leaves.off[k] == u.off && leaves.size[k] == u.s1) b = k;
-          if (b >= 0)
-            ext.ext[b] = static_cast<int32_t>(u.s2);
-          else
-            rest.push_back(u);
+      {
+        std::vector<int64_t> end(leaves.count);
+        for (int b = 0; b < leaves.count; ++b) end[b] = leaves.off[b] + leaves.size[b];
+        std::vector<std::vector<Update>> kept(levels.size());
+        bool joined = true;
+        for (int d = static_cast<int>(levels.size()) - 1; d >= 0; --d)
+          for (const Update& u : levels[d]) {
+            if (m * u.s1 * u.s2 > kTrmmFoldMacs || forced >= 0) {  // a forced path takes every update
+              kept[d].push_back(u);
+              continue;
+            }
+            for (int b = 0; b < leaves.count; ++b)
+              if (leaves.off[b] >= u.off && leaves.off[b] < u.off + u.s1) {
+                joined = joined && end[b] == u.off + u.s1;
+                end[b] = u.off + u.s1 + u.s2;
+              }
+          }
+        if (joined) {
+          levels.swap(kept);
+          std::vector<int> order(leaves.count);
+          for (int b = 0; b < leaves.count; ++b) order[b] = b;
+          std::stable_sort(order.begin(), order.end(), [&](int x, int y) {
+            return end[x] - leaves.off[x] > end[y] - leaves.off[y];
+          });
+          const hg::TriLeaves by_work = leaves;
+          for (int k = 0; k < leaves.count; ++k) {
+            const int b = order[k];
+            leaves.off[k] = by_work.off[b];
+            leaves.size[k] = by_work.size[b];
+            ext.ext[k] = static_cast<int32_t>(end[b] - by_work.off[b] - by_work.size[b]);
+          }
         }
-        lv.swap(rest);
       }
       e = hg::launch_tri_leaves_tc(mx, ml, mc, args, leaves, ext, stream);
     }

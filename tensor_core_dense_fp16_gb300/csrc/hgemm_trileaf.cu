@@ -31,12 +31,12 @@
 //     the accumulator is double-buffered in TMEM (2 × 256 columns) and the
 //     epilogue warps (TMEM → alpha·acc → FP16 round to nearest even →
 //     swizzled staging → TMA store) drain one unit while the next one runs;
-//   * a leaf may also carry the off-diagonal update of the block whose first
-//     half it is (C1 += alpha·A21ᵀ·B2 in the page's recursion): its product
-//     then runs on over K columns [off+s, off+s+ext) with whole rows of the
-//     second operand (A21 lies below the diagonal), processed first (N = s,
-//     initialising the accumulator), so the update costs no launch, no
-//     read-modify-write of C and no intermediate FP16 rounding;
+//   * a leaf may also carry the off-diagonal updates (C1 += alpha·A21ᵀ·B2 in
+//     the page's recursion) of the small blocks whose first half holds it:
+//     its product then runs on over K columns [off+s, off+s+ext) with whole
+//     rows of the second operand (A21 lies below the diagonal), processed
+//     first (N = s, initialising the accumulator), so those updates cost no
+//     launch, no read-modify-write of C and no intermediate FP16 rounding;
 //   * every wait is bounded, as in the other tensor-core kernels (watchdog
 //     word, abort flag, drain, TMEM freed).
 #include <atomic>
@@ -339,7 +339,7 @@ cudaError_t launch_tri_leaves_tc(const CUtensorMap& x, const CUtensorMap& l, con
   auto kern = fused ? hgemm_tri_leaves_tc_kernel<true> : hgemm_tri_leaves_tc_kernel<false>;
   for (int b = 0; b < leaves.count; ++b)
     if (leaves.size[b] <= 0 || leaves.size[b] > LeafCfg::MAX_S || leaves.size[b] % LeafCfg::BK != 0 ||
-        ext.ext[b] < 0 || ext.ext[b] > LeafCfg::MAX_S || ext.ext[b] % LeafCfg::BK != 0)
+        ext.ext[b] < 0 || ext.ext[b] % LeafCfg::BK != 0)
       return cudaErrorInvalidValue;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);

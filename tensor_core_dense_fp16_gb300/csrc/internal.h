@@ -139,7 +139,7 @@ cudaError_t launch_tri_leaves(const PlainArgs& args, const TriLeaves& leaves, in
 // (m × n, 32×64 boxes); args.num_m row tiles of 128 per leaf.
 // ext[b]: K columns past leaf b's own block that its product also covers,
 // [off_b + s_b, off_b + s_b + ext[b]) (whole rows of the second operand:
-// the off-diagonal update of the block whose first half leaf b is), a
+// the off-diagonal updates of the blocks whose first half holds leaf b), a
 // multiple of 64, or 0.
 struct TriLeafExt {
   int32_t ext[kMaxLeaves];

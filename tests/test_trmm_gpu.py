@@ -139,3 +139,13 @@ def test_trmm_equal_levels_wide_m():
     a, b = trmm_inputs(n, m, seed=23)
     ref = oracle.trmm(a, b, nthreads=oracle_threads())
     assert_close(run_trmm(a, b), ref, what="trmm 1024x1000")
+
+
+def test_trmm_carried_and_separate_updates():
+    """n = 2048, m = 8200 (automatic path): the updates of the 1024-blocks
+    and below are carried by the leaves, the top one (8200 × 1024 × 1024
+    multiply-adds, above 2^33) runs as a product of its own after them."""
+    n, m = 2048, 8200
+    a, b = trmm_inputs(n, m, seed=29)
+    ref = oracle.trmm(a, b, nthreads=oracle_threads())
+    assert_close(run_trmm(a, b), ref, what="trmm 2048x8200")
