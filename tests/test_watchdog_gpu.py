@@ -46,3 +46,32 @@ def test_withheld_arrival_times_out_and_the_context_survives(path):
     # the same context computes correctly afterwards
     ref = oracle.hgemm(a, b)
     assert_close(run_gpu(a, b, path=path), ref, what=f"after timeout, path {path}")
+
+
+@pytest.mark.gpu
+def test_withheld_arrival_in_the_trmm_leaf_kernel():
+    """The same on the triangular product: the tensor-core leaf kernel (the
+    first launch of hgemm_trmm, n a multiple of 64) records the timeout and
+    returns; afterwards the same context computes the product correctly."""
+    torch = torch_cuda()
+    n, m = 512, 256
+    rng = np.random.default_rng(37)
+    a = rng.uniform(0, 1, size=(n, n)).astype(np.float16)
+    b = rng.uniform(0, 1, size=(n, m)).astype(np.float16)
+    da, db = to_device(np.ascontiguousarray(a.T)), to_device(np.ascontiguousarray(b.T))
+    dc = torch.zeros((m, n), dtype=torch.float16, device="cuda")
+    assert tc.hgemm_device_status() == tc.HGEMM_OK
+    tc.hgemm_set_wait_timeout(50_000_000)   # 50 ms per wait
+    tc.hgemm_debug_inject(tc.HGEMM_INJECT_DROP_ARRIVAL)
+    try:
+        tc.hgemm_trmm(da, n, db, n, dc, n, n, m, 1.0)
+        assert tc.hgemm_device_status() == tc.HGEMM_ERR_TIMEOUT
+        assert tc.hgemm_device_status() == tc.HGEMM_OK
+    finally:
+        tc.hgemm_debug_inject(tc.HGEMM_INJECT_NONE)
+        tc.hgemm_set_wait_timeout(0)
+    tc.hgemm_trmm(da, n, db, n, dc, n, n, m, 1.0)
+    assert tc.hgemm_device_status() == tc.HGEMM_OK
+    torch.cuda.synchronize()
+    ref = oracle.trmm(a, b)
+    assert_close(np.ascontiguousarray(dc.cpu().numpy().T), ref, what="trmm after timeout")
