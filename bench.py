@@ -120,7 +120,9 @@ def trmm_flops(spec):
 
 def trsm_launches(n, m=None, leaf=256):
     """Kernel launches of one hgemm_trsm (alpha = 1, out of place): the scaled
-    copy, one diagonal solve per leaf and one GEMM per split block."""
+    copy, one diagonal solve per leaf and one GEMM per split block. With the
+    workspace (leaf=512): the same count over blocks of 512, each leaf one
+    product by its inverse (the inverses' launch is counted by the caller)."""
     def count(s):
         if s <= leaf:
             return 1
@@ -593,7 +595,8 @@ def run_tri_ours(args, spec, a_col, b_col, world, rank, local):
                        "path": "hgemm_trsm_ws" if op == "trsm" and not args.no_workspace else ops["call"],
                        "parallelism": f"replicas x{world}"},
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": args.steps * (ops["launches"](n, m) + (1 if op == "trsm" and not args.no_workspace else 0)),
+            "gpu_launches": args.steps * ((ops["launches"](n, m, 512) + 1) if op == "trsm" and not args.no_workspace
+                                          else ops["launches"](n, m)),
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)

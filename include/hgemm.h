@@ -221,9 +221,9 @@ HGEMM_API int hgemm_trsm(const hgemm_half_t *A, int64_t lda, const hgemm_half_t 
 
 /*
  * hgemm_trsm_workspace_size — bytes of device workspace hgemm_trsm_ws uses
- * for a triangle of order n: 128 KiB per diagonal block of the recursion
- * (n = 8192: 32 blocks, 4 MiB). 0 for n ≤ 0 or n beyond the recursion's
- * 128 diagonal blocks. Pure host logic.
+ * for a triangle of order n: 512 KiB per diagonal block of order ≤ 512 of
+ * the recursion (n = 8192: 16 blocks, 8 MiB). 0 for n ≤ 0 or n beyond 128
+ * such blocks. Pure host logic.
  */
 HGEMM_API size_t hgemm_trsm_workspace_size(int64_t n);
 
@@ -233,13 +233,14 @@ HGEMM_API size_t hgemm_trsm_workspace_size(int64_t n);
  * hgemm_trsm_workspace_size(n) bytes, 16-byte aligned (256 as cudaMalloc
  * gives), not overlapping A, B or X (HGEMM_ERR_ALIAS), not used by any
  * other work until the stream has passed this call. With it, when X is
- * 16-byte aligned with ldx a multiple of 8, one launch first computes the
- * inverses of all diagonal blocks (FP32 arithmetic, stored FP16 in the
- * workspace), and each diagonal block is then solved as an in-place
- * tensor-core product X_bᵀ := X_bᵀ · L_b⁻¹ instead of by substitution
- * (a block whose order is not a multiple of 8 still takes the substitution
- * kernel). The substitution then happens once per block for the identity
- * rather than per right-hand side, so this pays for many right-hand sides.
+ * 16-byte aligned with ldx a multiple of 8, the recursion stops at diagonal
+ * blocks of order ≤ 512: one launch first computes their inverses (FP32
+ * arithmetic, stored FP16 in the workspace), and each is then solved as an
+ * in-place tensor-core product X_bᵀ := X_bᵀ · L_b⁻¹ instead of by
+ * substitution (a block whose order is not a multiple of 8 still recurses to
+ * the substitution kernel). The substitution then happens once per block for
+ * the identity rather than per right-hand side, and the deepest updates of
+ * the recursion are inside the inverses.
  * Rounding: each solved block is rounded once to FP16 as in hgemm_trsm, the
  * inverse once more. A null workspace, one too small or not 16-byte
  * aligned is HGEMM_ERR_INVALID_ARG; X not suited to the tensor-core path, or
@@ -258,11 +259,11 @@ HGEMM_API int hgemm_trsm_ws(const hgemm_half_t *A, int64_t lda, const hgemm_half
  * an addition for such callers.
  *
  * Same system, operands, results and return values as hgemm_trsm_ws, whose
- * workspace here is a fixed array of HGEMM_TRSM_NOALLOC_MAX_BYTES (4 MiB)
+ * workspace here is a fixed array of HGEMM_TRSM_NOALLOC_MAX_BYTES (8 MiB)
  * inside the library, present on every device that loads the library until
  * the process exits. Nothing is allocated: no cudaMalloc or cudaFree, no
- * allocating library call. Limit: triangles whose recursion has at most 32
- * diagonal blocks, which is every n ≤ 8192; a larger n
+ * allocating library call. Limit: triangles whose recursion has at most 16
+ * diagonal blocks of order ≤ 512, which is every n ≤ 8192; a larger n
  * (hgemm_trsm_workspace_size(n) > HGEMM_TRSM_NOALLOC_MAX_BYTES) returns
  * HGEMM_ERR_INVALID_ARG and enqueues nothing.
  *
@@ -274,7 +275,7 @@ HGEMM_API int hgemm_trsm_ws(const hgemm_half_t *A, int64_t lda, const hgemm_half
  * overlaps on the GPU (other streams, other host threads) race on it and
  * must be ordered by the caller, e.g. issued on one stream.
  */
-#define HGEMM_TRSM_NOALLOC_MAX_BYTES (4u << 20)
+#define HGEMM_TRSM_NOALLOC_MAX_BYTES (8u << 20)
 HGEMM_API int hgemm_trsm_noalloc(const hgemm_half_t *A, int64_t lda, const hgemm_half_t *B, int64_t ldb,
                        hgemm_half_t *X, int64_t ldx, int64_t n, int64_t m, float alpha,
                        cudaStream_t stream);

@@ -40,7 +40,7 @@ HGEMM_ERR_UNSUPPORTED_DEVICE = -3
 HGEMM_ERR_CUDA = -4
 HGEMM_ERR_TIMEOUT = -5
 HGEMM_TRMM_MAX_N = 16384
-HGEMM_TRSM_NOALLOC_MAX_BYTES = 4 << 20
+HGEMM_TRSM_NOALLOC_MAX_BYTES = 8 << 20
 HGEMM_A_ROW_MAJOR = 0
 HGEMM_A_COL_MAJOR = 1
 HGEMM_B_COL_MAJOR = 0

@@ -893,12 +893,13 @@ int hgemm_trmm(const hgemm_half_t* A, int64_t lda, const hgemm_half_t* B, int64_
 
 namespace {
 
-// The diagonal blocks of the TRSM recursion in the order it solves them
-// (second half first); false when there are more than the table holds.
-bool trsm_leaves(int64_t n, hg::TriLeaves* leaves) {
+// The diagonal blocks of order ≤ leaf of the TRSM recursion in the order it
+// solves them (second half first); false when there are more than the table
+// holds.
+bool trsm_leaves(int64_t n, int64_t leaf, hg::TriLeaves* leaves) {
   leaves->count = 0;
   std::function<bool(int64_t, int64_t)> walk = [&](int64_t off, int64_t s) -> bool {
-    if (s <= hg::kTrsmLeaf) {
+    if (s <= leaf) {
       if (leaves->count == hg::kMaxLeaves) return false;
       leaves->off[leaves->count] = off;
       leaves->size[leaves->count] = s;
@@ -911,7 +912,8 @@ bool trsm_leaves(int64_t n, hg::TriLeaves* leaves) {
   return n > 0 && walk(0, n);
 }
 
-constexpr uint64_t kTrsmInverseBytes = 2ull * hg::kTrsmLeaf * hg::kTrsmLeaf;  // one leaf's inverse
+// one inverse in the workspace: FP16, kTrsmInverseLeaf² (512 KiB)
+constexpr uint64_t kTrsmInverseBytes = 2ull * hg::kTrsmInverseLeaf * hg::kTrsmInverseLeaf;
 
 // hgemm_trsm and hgemm_trsm_ws: W (may be null) holds room for the inverses
 // of the diagonal blocks.
@@ -938,7 +940,8 @@ int trsm_impl(const hgemm_half_t* A, int64_t lda, const hgemm_half_t* B, int64_t
     return HGEMM_ERR_ALIAS;
   hg::TriLeaves leaves{};
   if (W) {
-    if (!trsm_leaves(n, &leaves) || w_bytes < kTrsmInverseBytes * static_cast<uint64_t>(leaves.count) ||
+    if (!trsm_leaves(n, hg::kTrsmInverseLeaf, &leaves) ||
+        w_bytes < kTrsmInverseBytes * static_cast<uint64_t>(leaves.count) ||
         (reinterpret_cast<uintptr_t>(W) & 15u))
       return HGEMM_ERR_INVALID_ARG;
     const uint64_t wb = kTrsmInverseBytes * static_cast<uint64_t>(leaves.count);
@@ -955,11 +958,11 @@ int trsm_impl(const hgemm_half_t* A, int64_t lda, const hgemm_half_t* B, int64_t
   const uint16_t* a = reinterpret_cast<const uint16_t*>(A);
   cudaError_t e;
   bool chained = false;  // a launch of this solve is already on the stream
-  // With a workspace, each diagonal block is solved as an in-place
-  // tensor-core product by its inverse (all inverses computed in one launch
-  // first): X_bᵀ := X_bᵀ · L_b⁻¹. X must suit TMA. Measured against the
-  // substitution kernel: 1.30 -> 0.89 ms at n = m = 8192, 255 -> 251 µs at
-  // n = 4096, m = 256.
+  // With a workspace, the recursion stops at blocks of order ≤
+  // kTrsmInverseLeaf, each solved as an in-place tensor-core product by its
+  // inverse (all inverses computed in one launch first): X_bᵀ := X_bᵀ · L_b⁻¹.
+  // X must suit TMA. Measured at n = m = 8192: substitution for the blocks of
+  // 256, 1.30 ms; products by the inverses of the blocks of 256, 0.89 ms.
   const bool by_inverse = W && (reinterpret_cast<uintptr_t>(X) & 15u) == 0 && ldx % 8 == 0 &&
                           g_forced_path.load(std::memory_order_relaxed) < 0;
   if (by_inverse) {
@@ -983,33 +986,43 @@ int trsm_impl(const hgemm_half_t* A, int64_t lda, const hgemm_half_t* B, int64_t
   const hg::EpiArgs subtract{-1.0f, 1.0f, nullptr, 0, 2};
   // The page's recursion, second half first: every row of a block depends on
   // the rows below it.
-  std::function<int(int64_t, int64_t)> solve = [&](int64_t off, int64_t s) -> int {
-    if (s <= hg::kTrsmLeaf) {
+  // inverse: the block's inverse is in the workspace (a block of the
+  // inverse-product recursion); otherwise the blocks of order ≤ kTrsmLeaf
+  // are solved by substitution.
+  std::function<int(int64_t, int64_t, bool)> solve = [&](int64_t off, int64_t s, bool inverse) -> int {
+    if (inverse && s <= hg::kTrsmInverseLeaf) {
       const int b = leaf_index++;
-      if (by_inverse && s % 8 == 0) {
+      if (s % 8 == 0) {
         // Xᵀ[:, off : off+s] (m × s, pitch ldx) := itself · L⁻¹, where row k of
         // L⁻¹ is contiguous in W_b (an N-contiguous second operand, pitch
-        // kTrsmLeaf). Each 256-row tile reads every column it writes and no
-        // other tile reads them, so whole tiles compute it in place.
-        Gemm g{x + off, W + static_cast<int64_t>(b) * hg::kTrsmLeaf * hg::kTrsmLeaf, x + off, m, s, s,
-               ldx, hg::kTrsmLeaf, ldx};
+        // kTrsmInverseLeaf). A tile of 256 rows × all s ≤ 512 columns (the wide
+        // kernel's, or the pair kernel's for s ≤ 256, never cut into column
+        // parts) reads every column it writes and no other tile reads them,
+        // so the product runs in place.
+        Gemm g{x + off, W + static_cast<int64_t>(b) * hg::kTrsmInverseLeaf * hg::kTrsmInverseLeaf, x + off, m,
+               s, s, ldx, hg::kTrsmInverseLeaf, ldx};
         g.b_mn = true;
         chained = true;
-        return run_tc_pair(g, kPlainEpilogue, *dev, stream, nullptr, true);
+        return s > hg::kPairBN ? run_tc_wide(g, kPlainEpilogue, *dev, stream)
+                               : run_tc_pair(g, kPlainEpilogue, *dev, stream, nullptr, true);
       }
+      // order not a multiple of 8: this block by substitution
+      return solve(off, s, false);
+    }
+    if (s <= hg::kTrsmLeaf) {
       const cudaError_t le = hg::launch_trsm_leaf(a, lda, x, ldx, off, static_cast<int>(s), m,
                                                   dev->num_sms, chained, stream);
       chained = true;
       return le == cudaSuccess ? HGEMM_OK : cuda_fail(le);
     }
     const int64_t s1 = ((s / 2 + 63) / 64) * 64, s2 = s - s1;
-    int r = solve(off + s1, s2);
+    int r = solve(off + s1, s2, inverse);
     if (r != HGEMM_OK) return r;
     const Gemm g{x + off + s1, a + off * lda + off + s1, x + off, m, s1, s2, ldx, lda, ldx};
     if ((r = dispatch(g, subtract, *dev, stream)) != HGEMM_OK) return r;
-    return solve(off, s1);
+    return solve(off, s1, inverse);
   };
-  return solve(0, n);
+  return solve(0, n, by_inverse);
 }
 
 }  // namespace
@@ -1022,7 +1035,7 @@ int hgemm_trsm(const hgemm_half_t* A, int64_t lda, const hgemm_half_t* B, int64_
 
 size_t hgemm_trsm_workspace_size(int64_t n) {
   hg::TriLeaves leaves{};
-  if (n <= 0 || n > HGEMM_MAX_DIM || !trsm_leaves(n, &leaves)) return 0;
+  if (n <= 0 || n > HGEMM_MAX_DIM || !trsm_leaves(n, hg::kTrsmInverseLeaf, &leaves)) return 0;
   return static_cast<size_t>(kTrsmInverseBytes * static_cast<uint64_t>(leaves.count));
 }
 
@@ -1037,7 +1050,7 @@ int hgemm_trsm_ws(const hgemm_half_t* A, int64_t lda, const hgemm_half_t* B, int
 // ---------------------------------------------------------------------------
 // hgemm_trsm_noalloc: hgemm_trsm_ws for callers that cannot allocate device
 // memory. Its workspace is this fixed array, part of the library's module on
-// every device that loads it (4 MiB there until the process exits). In host
+// every device that loads it (8 MiB there until the process exits). In host
 // code the name g_trsm_noalloc_scratch stands for a host-side shadow, not the
 // device memory, so the array's device address is taken once per device with
 // cudaGetSymbolAddress (with that device current) and passed on.

@@ -40,10 +40,9 @@
 namespace hg {
 namespace {
 
-constexpr int kLeafMax = kTrsmLeaf;                     // largest diagonal block
+constexpr int kLeafMax = kTrsmLeaf;                     // largest diagonal block solved per right-hand side
 constexpr int kMaxDevices = 64;
 constexpr int kGroup = 32;                  // rows per barrier step: one warp's rows
-constexpr int kGroups = kLeafMax / kGroup;  // diagonal 32×32 triangles of a block
 
 // Row pitch (floats) of the published b and x rows: the padding puts
 // consecutive lanes' 16-byte accesses in different banks.
@@ -60,10 +59,11 @@ constexpr int KP = kGroup + 8;
 // 80-byte pitch puts the 8 rows of an ldmatrix load in different banks).
 constexpr int AP = kGroup + 8;
 
-template <int COLS>
+// LEAF: the largest block order the kernel takes (one warp per 32 rows).
+template <int COLS, int LEAF = kLeafMax>
 constexpr int leaf_smem() {
-  return kGroups * kGroup * kGroup * 4 + 2 * kGroup * pub_pitch<COLS>() * 4 + COLS * KP * 2 +
-         2 * kLeafMax * AP * 2;
+  return (LEAF / kGroup) * kGroup * kGroup * 4 + 2 * kGroup * pub_pitch<COLS>() * 4 + COLS * KP * 2 +
+         2 * LEAF * AP * 2;
 }
 
 // The m16k16 A fragment of mma.sync from a row-major 16×16 FP16 tile in
@@ -117,7 +117,7 @@ __device__ __forceinline__ float col32_at(const uint4 (&v)[4], int q) {
 // identity: the right-hand sides are the columns of the identity (X is not
 // read), so the block computes columns j0.. of the inverse of the block's
 // transpose.
-template <int COLS>
+template <int COLS, int LEAF>
 __device__ __forceinline__ void trsm_leaf_body(const uint16_t* __restrict__ A, int64_t lda,
                                                uint16_t* __restrict__ X, int64_t ldx, int64_t off,
                                                int64_t xoff, int s, int64_t m, int chained, bool identity,
@@ -128,10 +128,10 @@ __device__ __forceinline__ void trsm_leaf_body(const uint16_t* __restrict__ A, i
   // rows 32g .. 32g+31), then, in place, (L_g⁻¹)(k, j)
   float* diag = reinterpret_cast<float*>(smem);
   constexpr int P = pub_pitch<COLS>();
-  float* pub_b = diag + kGroups * kGroup * kGroup;  // [kGroup][P]: b of the group's rows
+  float* pub_b = diag + (LEAF / kGroup) * kGroup * kGroup;  // [kGroup][P]: b of the group's rows
   float* pub_x = pub_b + kGroup * P;                // [kGroup][P]: x of the group's rows
   __half* pub_xh = reinterpret_cast<__half*>(pub_x + kGroup * P);  // [COLS][KP]: -x_g in FP16
-  // [2][kLeafMax][AP]: A(c0 .. c0+31, r) of a group, row r of the block,
+  // [2][LEAF][AP]: A(c0 .. c0+31, r) of a group, row r of the block,
   // double-buffered (the next group's segments arrive during this group)
   uint16_t* a_stage = reinterpret_cast<uint16_t*>(pub_xh + COLS * KP);
   const int r = threadIdx.x;
@@ -218,7 +218,7 @@ __device__ __forceinline__ void trsm_leaf_body(const uint16_t* __restrict__ A, i
     if (warp >= g) return;
     const int c0 = g * kGroup, sg = min(kGroup, s - c0);
     const uint16_t* src = A + (off + r) * lda + off + c0;
-    uint16_t* dst = a_stage + ((g & 1) * kLeafMax + r) * AP;
+    uint16_t* dst = a_stage + ((g & 1) * LEAF + r) * AP;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       int valid = sg - 8 * q;
@@ -320,7 +320,7 @@ __device__ __forceinline__ void trsm_leaf_body(const uint16_t* __restrict__ A, i
       if (staged) {
         cp_async_wait<1>();  // this group's segments (the next group's may be in flight)
         __syncwarp();
-        const uint16_t* base = a_stage + ((g & 1) * kLeafMax + warp * kGroup) * AP;
+        const uint16_t* base = a_stage + ((g & 1) * LEAF + warp * kGroup) * AP;
 #pragma unroll
         for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
@@ -358,16 +358,18 @@ template <int COLS>
 __global__ void __launch_bounds__(kLeafMax, 2)
     trsm_leaf_kernel(const uint16_t* __restrict__ A, int64_t lda, uint16_t* __restrict__ X,
                      int64_t ldx, int64_t off, int s, int64_t m, int chained) {
-  trsm_leaf_body<COLS>(A, lda, X, ldx, off, off, s, m, chained, false, static_cast<int64_t>(blockIdx.x) * COLS);
+  trsm_leaf_body<COLS, kLeafMax>(A, lda, X, ldx, off, off, s, m, chained, false,
+                                 static_cast<int64_t>(blockIdx.x) * COLS);
 }
 
 // The inverses of every diagonal block of a solve, in one launch: block
-// b = blockIdx.y (order s_b at (off_b, off_b)) solves its transpose against
-// the identity, so W_b = W + b·kLeafMax² (column-major, pitch kLeafMax)
-// receives the transpose of its inverse: W_b[k·kLeafMax + i] = L_b⁻¹(k, i).
+// b = blockIdx.y (order s_b ≤ LEAF at (off_b, off_b)) solves its transpose
+// against the identity, so W_b = W + b·LEAF² (column-major, pitch LEAF)
+// receives the transpose of its inverse: W_b[k·LEAF + i] = L_b⁻¹(k, i).
 // The first launch of its solve: waits for the previous launch on the
 // stream before anything else (the previous solve may still read W).
-__global__ void __launch_bounds__(kLeafMax, 2)
+template <int LEAF>
+__global__ void __launch_bounds__(LEAF, LEAF <= 256 ? 2 : 1)
     trsm_inverse_kernel(const uint16_t* __restrict__ A, int64_t lda, uint16_t* __restrict__ W,
                         const TriLeaves leaves) {
   constexpr int COLS = 32;
@@ -379,8 +381,8 @@ __global__ void __launch_bounds__(kLeafMax, 2)
     grid_launch_dependents();
     return;
   }
-  trsm_leaf_body<COLS>(A, lda, W + static_cast<int64_t>(b) * kLeafMax * kLeafMax, kLeafMax, leaves.off[b], 0, s,
-                       s, 0, true, j0);
+  trsm_leaf_body<COLS, LEAF>(A, lda, W + static_cast<int64_t>(b) * LEAF * LEAF, LEAF, leaves.off[b], 0, s, s, 0,
+                             true, j0);
 }
 
 // X(:, j) = alpha · B(:, j) for the n × m column-major operands; FP16 in and
@@ -489,19 +491,21 @@ cudaError_t launch_trsm_inverse(const uint16_t* A, int64_t lda, uint16_t* W, con
                                 cudaStream_t stream) {
   if (leaves.count < 1 || leaves.count > kMaxLeaves) return cudaErrorInvalidValue;
   for (int b = 0; b < leaves.count; ++b)
-    if (leaves.size[b] < 1 || leaves.size[b] > kLeafMax) return cudaErrorInvalidValue;
+    if (leaves.size[b] < 1 || leaves.size[b] > kTrsmInverseLeaf) return cudaErrorInvalidValue;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  constexpr int LEAF = kTrsmInverseLeaf;
   static std::atomic<bool> attr_done[kMaxDevices];
   if (!attr_done[dev]) {
-    e = cudaFuncSetAttribute(trsm_inverse_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, leaf_smem<32>());
+    e = cudaFuncSetAttribute(trsm_inverse_kernel<LEAF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             leaf_smem<32, LEAF>());
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
-  PdlLaunch l(dim3(kLeafMax / 32, static_cast<unsigned>(leaves.count)), dim3(kLeafMax), leaf_smem<32>(), stream);
-  return cudaLaunchKernelEx(&l.cfg, trsm_inverse_kernel, A, lda, W, leaves);
+  PdlLaunch l(dim3(LEAF / 32, static_cast<unsigned>(leaves.count)), dim3(LEAF), leaf_smem<32, LEAF>(), stream);
+  return cudaLaunchKernelEx(&l.cfg, trsm_inverse_kernel<LEAF>, A, lda, W, leaves);
 }
 
 cudaError_t launch_scale_copy(const uint16_t* B, int64_t ldb, uint16_t* X, int64_t ldx, int64_t n,

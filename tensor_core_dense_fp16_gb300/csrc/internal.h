@@ -157,10 +157,11 @@ cudaError_t launch_scale_copy(const uint16_t* B, int64_t ldb, uint16_t* X, int64
                               int64_t m, float alpha, int num_sms, cudaStream_t stream);
 // chained: an earlier launch of the same solve precedes this one on the
 // stream (the kernel may then read A before waiting for it).
-// The inverses of every diagonal block (leaf b of order s_b at (off_b, off_b))
-// in one launch: W + b·kTrsmLeaf² receives, column-major with pitch
-// kTrsmLeaf, the transpose of the block's inverse (row k of the inverse is
-// contiguous), FP16.
+// The inverses of every diagonal block (leaf b of order s_b ≤ kTrsmInverseLeaf
+// at (off_b, off_b)) in one launch: W + b·kTrsmInverseLeaf² receives,
+// column-major with pitch kTrsmInverseLeaf, the transpose of the block's
+// inverse (row k of the inverse is contiguous), FP16.
+constexpr int kTrsmInverseLeaf = 512;
 cudaError_t launch_trsm_inverse(const uint16_t* A, int64_t lda, uint16_t* W, const TriLeaves& leaves,
                                 cudaStream_t stream);
 cudaError_t launch_trsm_leaf(const uint16_t* A, int64_t lda, uint16_t* X, int64_t ldx, int64_t off,

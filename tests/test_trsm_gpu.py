@@ -51,7 +51,7 @@ def run_trsm(a, b, alpha=1.0, pad=(0, 0, 0), poison_upper=False, in_place=False,
         dx = to_device(np.full((m, ldx), 5.0, np.float16))
     if ws:
         need = tc.hgemm_trsm_workspace_size(n)
-        assert need > 0 and need % (2 * 256 * 256) == 0
+        assert need > 0 and need % (2 * 512 * 512) == 0
         work = torch.full((need + 4096,), 0x5A, dtype=torch.uint8, device="cuda")
         tc.hgemm_trsm_ws(da, lda, db, ldb, dx, ldx, n, m, alpha, work, need)
     else:
@@ -72,8 +72,9 @@ def run_trsm(a, b, alpha=1.0, pad=(0, 0, 0), poison_upper=False, in_place=False,
 @pytest.mark.parametrize("n,m", [(1, 1), (64, 32), (200, 7), (256, 100), (257, 64), (300, 136),
                                  (512, 256), (1000, 128), (4096, 256)])
 def test_trsm_matches_oracle(n, m, ws):
-    """ws: the diagonal blocks solved as products by their inverses (blocks
-    of order 129 or 200, not multiples of 8, by substitution)."""
+    """ws: the diagonal blocks of order ≤ 512 solved as products by their
+    inverses (blocks of order 257, 300 or 200, not multiples of 8, by
+    substitution)."""
     a, b = trsm_inputs(n, m, seed=n + m)
     ref = oracle.trsm(a, b, nthreads=oracle_threads())
     assert_close(run_trsm(a, b, ws=ws), ref, what=f"trsm {n}x{m} ws={ws}")
@@ -169,9 +170,9 @@ def test_trsm_workspace_arguments():
     refuses: no workspace, one too small, a misaligned one, one overlapping X."""
     torch = torch_cuda()
     assert tc.hgemm_trsm_workspace_size(0) == 0
-    assert tc.hgemm_trsm_workspace_size(256) == 2 * 256 * 256
-    assert tc.hgemm_trsm_workspace_size(8192) == 32 * 2 * 256 * 256
-    assert tc.hgemm_trsm_workspace_size(300) == 2 * 2 * 256 * 256   # blocks of 192 and 108
+    assert tc.hgemm_trsm_workspace_size(256) == 2 * 512 * 512
+    assert tc.hgemm_trsm_workspace_size(8192) == 16 * 2 * 512 * 512
+    assert tc.hgemm_trsm_workspace_size(1000) == 2 * 2 * 512 * 512   # blocks of 512 and 488
     n, m = 512, 64
     a, b = trsm_inputs(n, m, seed=5)
     da, db = to_device(np.ascontiguousarray(a.T)), to_device(np.ascontiguousarray(b.T))
