@@ -1,8 +1,11 @@
 // hgemm_trsm.cu — the pieces of the triangular solve of
 // "异构计算中高性能TRMM与TRSM的递归算法实现" (§2.3) that are not products: the
-// scaled copy of the right-hand side, and the solve of one diagonal block
-// (order ≤ 256) for all right-hand sides. The recursion and its GEMM updates
-// are in hgemm_api.cu.
+// scaled copy of the right-hand side, the solve of one diagonal block (order
+// ≤ 256) for all right-hand sides, and, for the entry points with a
+// workspace, the inverses of all diagonal blocks of order ≤ 512 (the same
+// solve against the columns of the identity, one warp per 32 rows). The
+// recursion, its GEMM updates and the products by the inverses are in
+// hgemm_api.cu.
 //
 // The system solved, in the variant of the page's §2.2 product (left side,
 // lower triangle, transposed): Aᵀ·X = alpha·B, every matrix column-major
