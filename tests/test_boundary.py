@@ -209,6 +209,39 @@ def test_trsm_argument_checks(lib):
     assert call(n=0) == tc.HGEMM_OK and call(m=0) == tc.HGEMM_OK
 
 
+def test_trsm_workspace_argument_checks(lib):
+    """hgemm_trsm_ws and hgemm_trsm_noalloc check their arguments on the host
+    before any device work: workspace size per diagonal block of order ≤ 512,
+    a missing, short or misaligned workspace, one overlapping an operand, and
+    a triangle beyond the fixed array."""
+    lib_ = tc.load()
+    assert tc.hgemm_trsm_workspace_size(0) == 0
+    assert tc.hgemm_trsm_workspace_size(-5) == 0
+    assert tc.hgemm_trsm_workspace_size(512) == 2 * 512 * 512
+    assert tc.hgemm_trsm_workspace_size(513) == 2 * 2 * 512 * 512
+    assert tc.hgemm_trsm_workspace_size(8192) == 16 * 2 * 512 * 512 == tc.HGEMM_TRSM_NOALLOC_MAX_BYTES
+    assert tc.hgemm_trsm_workspace_size(8193) > tc.HGEMM_TRSM_NOALLOC_MAX_BYTES
+    n, m = 64, 8
+    need = tc.hgemm_trsm_workspace_size(n)
+    W16 = 0x50000000
+    ok = dict(A=A16, lda=n, B=B16, ldb=n, X=C16, ldx=n, W=W16, bytes=need)
+    def call(**kw):
+        a = {**ok, **kw}
+        return lib_.hgemm_trsm_ws(a["A"], a["lda"], a["B"], a["ldb"], a["X"], a["ldx"], kw.get("n", n),
+                                  kw.get("m", m), 1.0, a["W"], a["bytes"], None)
+    assert call(W=None) == tc.HGEMM_ERR_INVALID_ARG
+    assert call(bytes=need - 1) == tc.HGEMM_ERR_INVALID_ARG
+    assert call(W=W16 + 8) == tc.HGEMM_ERR_INVALID_ARG
+    assert call(W=A16) == tc.HGEMM_ERR_ALIAS
+    assert call(W=C16 - 16) == tc.HGEMM_ERR_ALIAS
+    assert call(n=-1) == tc.HGEMM_ERR_INVALID_ARG
+    assert call(n=0) == tc.HGEMM_OK and call(m=0) == tc.HGEMM_OK
+    big = 8193
+    assert lib_.hgemm_trsm_noalloc(A16, big, B16, big, C16, big, big, 1, 1.0, None) == tc.HGEMM_ERR_INVALID_ARG
+    assert lib_.hgemm_trsm_noalloc(A16, n, B16, n, C16, n, -1, m, 1.0, None) == tc.HGEMM_ERR_INVALID_ARG
+    assert lib_.hgemm_trsm_noalloc(A16, n, B16, n, C16, n, 0, m, 1.0, None) == tc.HGEMM_OK
+
+
 def test_layout_argument_checks(lib):
     lib_ = tc.load()
     def call(a_layout=0, b_layout=0, lda=64, ldb=64, ldc=64, M=16, N=64, K=64, C=C16):
