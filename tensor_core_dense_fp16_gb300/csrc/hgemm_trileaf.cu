@@ -14,9 +14,10 @@
 // of 64 (every leaf when n is); the generic kernel takes the others.
 //
 // Design (one CTA per SM, tcgen05 with M = 128):
-//   * persistent CTAs walk units (leaf, 128-row tile of X), the tiles of one
-//     leaf consecutively, so the CTAs at work share that leaf's triangle in
-//     L2 and every row of X is read from memory once;
+//   * persistent CTAs walk units (128-row tile of X, leaf), all leaves of one
+//     tile consecutively (longest first), so the CTAs at work share those
+//     rows of X, each read from memory once, while the leaves' operand rows
+//     (A's lower part) stay in L2;
 //   * a unit's 64-wide K blocks go in reverse order. K block kb meets only
 //     rows i ≤ 64·kb + 63 of L_b (rows below are zero there), so TMA loads
 //     just those 64·(kb + 1) rows and the MMA is N = 64·(kb + 1) wide: the
@@ -161,7 +162,9 @@ __global__ void __launch_bounds__(192, 1)
   grid_dependency_wait();
   grid_launch_dependents();
 
-  // unit t: leaf t / num_m, rows [128·(t % num_m), +128) of X
+  // unit t: rows [128·mt, +128) of X with mt = t / leaves, for leaf t % leaves:
+  // the CTAs at work share those rows of X (read from memory once) and the
+  // leaves' operand rows, which stay in L2
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer
     if (lane == 0) {
@@ -170,7 +173,7 @@ __global__ void __launch_bounds__(192, 1)
       long long issued = 0;
       bool ok = true;
       for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
-        const int b = t / p.num_m, mt = t - b * p.num_m;
+        const int mt = t / leaves.count, b = t - mt * leaves.count;
         const int off = static_cast<int>(leaves.off[b]);
         const int nkb = static_cast<int>(leaves.size[b]) / Cfg::BK;
         const int nke = lext.ext[b] / Cfg::BK;  // K blocks of the carried update
@@ -219,7 +222,7 @@ __global__ void __launch_bounds__(192, 1)
     uint32_t acc_phase = 0;
     bool ok = true;
     for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
-      const int b = t / p.num_m;
+      const int b = t % leaves.count;
       const int nkb = static_cast<int>(leaves.size[b]) / Cfg::BK;
       const int nke = lext.ext[b] / Cfg::BK;
       int free_acc = 1;
@@ -277,7 +280,7 @@ __global__ void __launch_bounds__(192, 1)
     uint32_t acc_phase = 0;
     int cb = 0;
     for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
-      const int b = t / p.num_m, mt = t - b * p.num_m;
+      const int mt = t / leaves.count, b = t - mt * leaves.count;
       const int off = static_cast<int>(leaves.off[b]);
       const int boxes = static_cast<int>(leaves.size[b]) / kEpiCols;
       int ok = 1;
