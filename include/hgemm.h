@@ -209,8 +209,8 @@ HGEMM_API int hgemm_trmm(const hgemm_half_t *A, int64_t lda, const hgemm_half_t 
  * a block splits into halves, the second is solved first, then the GEMM
  * update X1 -= A21ᵀ·X2 (hgemm's accumulate epilogue with alpha = -1), then
  * the first half; diagonal blocks of order ≤ 256 are solved by substitution,
- * the right-hand sides spread over thread blocks and one barrier per row
- * (§2.3). Storage is FP16 (X is rounded after the scaling, after each update
+ * the right-hand sides spread over thread blocks (§2.3; the page puts a
+ * barrier after every row, this kernel one per group of 32 rows). Storage is FP16 (X is rounded after the scaling, after each update
  * and after each diagonal solve), arithmetic FP32. A zero on the diagonal is
  * not reported: as in BLAS, the result then holds Inf or NaN. The calls are
  * enqueued on `stream`, one after another. Same return values as hgemm.
