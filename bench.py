@@ -6,10 +6,15 @@ are resident in HBM before the timed region starts. Every timed launch is
 bracketed by CUDA events on the stream it is launched on, and L2 is flushed
 (a write of twice its size) before each launch, outside the events.
 
-Prints one JSON line on rank 0. Under torchrun each rank runs an independent
-replica of the workload on its own GPU (the product does not shard: there is
-no data-path collective); `value` is the work of all ranks over the slowest
-rank's time.
+Prints one JSON line on rank 0. `value` is the work of one step on every
+rank over the median step time (the slowest rank's median under torchrun,
+where each rank runs an independent replica of the workload on its own GPU:
+the product does not shard, there is no data-path collective). In the
+default run the line also carries `configs`: the other configurations of the
+problem (256-cube uniform and integer, 2048-cube, ragged 1000-cube, skinny
+4096×256×4096) timed the same way after the headline, each with its median,
+TFLOP/s and roofline fraction. `clocks` comes from in-process NVML samples
+(about every millisecond) taken inside the timed region.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload NAME]
@@ -155,6 +160,8 @@ def parse_args():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer measurement")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip timing the other configurations after the 8192-cube headline")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle sample")
     ap.add_argument("--reference-seconds", type=float, default=120.0,
@@ -318,6 +325,81 @@ def _num(s):
         return False
 
 
+class NvmlSampler:
+    """In-process, read-only NVML sampling (libnvidia-ml through ctypes) of
+    the SM clock, board power and clock-event reasons, about every
+    millisecond in a background thread, so that even a region of a few
+    milliseconds gets samples while the kernels run. Changes no setting."""
+
+    NVML_CLOCK_SM = 1
+    # nvmlClocksEventReason* bits
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, uuid, period_s=0.001):
+        import ctypes
+        import threading
+        self.ct = ctypes
+        self.period = period_s
+        self.samples = []
+        self.stop_flag = threading.Event()
+        self.thread = None
+        self.error = None
+        try:
+            self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.lib.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit_v2 failed")
+            self.handle = ctypes.c_void_p()
+            if self.lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.handle)) != 0:
+                raise OSError(f"no NVML device with UUID {uuid}")
+            self.reason_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+            mx = ctypes.c_uint()
+            self.max_mhz = (float(mx.value) if self.lib.nvmlDeviceGetMaxClockInfo(
+                self.handle, self.NVML_CLOCK_SM, ctypes.byref(mx)) == 0 else None)
+        except (OSError, AttributeError) as e:
+            self.lib = None
+            self.error = str(e)
+
+    def _run(self):
+        ct = self.ct
+        clk, mw, why = ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        while not self.stop_flag.is_set():
+            t = time.perf_counter()
+            ok = self.lib.nvmlDeviceGetClockInfo(self.handle, self.NVML_CLOCK_SM, ct.byref(clk)) == 0
+            pw = self.lib.nvmlDeviceGetPowerUsage(self.handle, ct.byref(mw)) == 0
+            rs = self.reason_fn(self.handle, ct.byref(why)) == 0
+            if ok:
+                self.samples.append((t, float(clk.value), mw.value / 1000.0 if pw else None,
+                                     int(why.value) if rs else 0))
+            time.sleep(self.period)
+
+    def start(self):
+        import threading
+        if self.lib is None:
+            return
+        self.thread = threading.Thread(target=self._run, daemon=True)
+        self.thread.start()
+
+    def stop(self, t0, t1):
+        """Summary of the samples taken between perf_counter times t0 and t1."""
+        if self.lib is None:
+            return {"source": "nvml unavailable", "error": self.error, "samples": 0}
+        self.stop_flag.set()
+        self.thread.join(timeout=2)
+        self.lib.nvmlShutdown()
+        use = [r for r in self.samples if t0 <= r[0] <= t1]
+        sm = [r[1] for r in use]
+        power = [r[2] for r in use if r[2] is not None]
+        reasons = sorted({name for r in use for bit, name in self.REASONS.items() if r[3] & bit})
+        return {"source": f"nvml, every {self.period * 1e3:.0f} ms inside the timed region",
+                "sm_mhz": statistics.median(sm) if sm else None,
+                "sm_mhz_min": min(sm) if sm else None, "sm_mhz_max": max(sm) if sm else None,
+                "sm_max_mhz": self.max_mhz, "reasons": reasons, "samples": len(use),
+                "power_w_median": statistics.median(power) if power else None,
+                "power_w_max": max(power) if power else None}
+
+
 def nvsmi_id(torch, dev, local):
     """An nvidia-smi --id for this process's GPU (nvidia-smi ignores
     CUDA_VISIBLE_DEVICES, so prefer the device UUID)."""
@@ -347,7 +429,7 @@ def reduce_max(value, dist, device):
 
 def whole_job_tflops(world, steps, flops, max_total_ms):
     """Work of all ranks (each ran `steps` products of `flops`) over the
-    slowest rank's total time."""
+    slowest rank's time for them."""
     return world * steps * flops / (max_total_ms * 1e-3) / 1e12
 
 
@@ -356,6 +438,98 @@ def dist_setup():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return world, rank, local
+
+
+def timed_region(torch, dev, local, stream, step, flush, steps, dist):
+    """Times `steps` calls of step(), each after an L2 flush (outside the
+    events) and bracketed by CUDA events on `stream`, between barriers, while
+    NVML (in-process, ~1 ms) and nvidia-smi (20 ms) sample the clocks.
+    Returns (per-call times in ms, clock summary)."""
+    gpu_id = nvsmi_id(torch, dev, local)
+    smi = ClockSampler(gpu_id)
+    nv = NvmlSampler(gpu_id)
+    smi.start()
+    nv.start()
+    time.sleep(0.15)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    switch = sys.getswitchinterval()
+    sys.setswitchinterval(0.0005)   # let the sampling thread in while the loop launches
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t0, p0 = time.time(), time.perf_counter()
+    for s_ev, e_ev in evs:
+        flush.zero_()
+        s_ev.record(stream)
+        step()
+        e_ev.record(stream)
+    torch.cuda.synchronize(dev)
+    t1, p1 = time.time(), time.perf_counter()
+    sys.setswitchinterval(switch)
+    if dist:
+        dist.barrier()
+    clocks = nv.stop(p0, p1)
+    clocks["nvidia_smi"] = smi.stop(t0, t1)
+    if not clocks.get("sm_mhz"):
+        for key in ("sm_mhz", "sm_max_mhz", "reasons", "power_w_max"):
+            clocks[key] = clocks["nvidia_smi"].get(key)
+    return [s_ev.elapsed_time(e_ev) for s_ev, e_ev in evs], clocks
+
+
+# The other configurations of the problem, timed after the headline in the
+# default run with the same protocol (L2 flush before each launch, CUDA
+# events on the launching stream, median).
+CONFIG_WORKLOADS = ["hgemm_256", "hgemm_256_int", "hgemm_2048", "hgemm_1000_ragged",
+                    "hgemm_4096x256x4096_skinny"]
+KERNEL_OF_PATH = {2: "hgemm_tc_kernel", 5: "hgemm_tc2_kernel", 6: "hgemm_tc2w_kernel",
+                  3: "hgemm_skinny_kernel", 4: "hgemm_generic_kernel"}
+
+
+def roofline_of(flops, nbytes, ms, peaks):
+    """Roofline time = the slower of the flops at the dense FP16 peak and the
+    bytes at HBM bandwidth; fraction = roofline time / measured time."""
+    peak = peaks["bf16_tflops"] * FP16_PER_BF16
+    t_tensor = flops / (peak * 1e12)
+    t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
+    bound = "tensor" if t_tensor >= t_hbm else "hbm"
+    return {"bound": bound, "frac": max(t_tensor, t_hbm) / (ms * 1e-3),
+            "tflops": flops / (ms * 1e-3) / 1e12, "gbs": nbytes / (ms * 1e-3) / 1e9,
+            "roofline_us": 1e6 * max(t_tensor, t_hbm)}
+
+
+def time_configs(torch, tc, dev, stream, flush, peaks, launches=50, warmup=5):
+    """Each configuration: `launches` flushed, event-timed calls of hgemm."""
+    out = {}
+    for name in CONFIG_WORKLOADS:
+        a, b, spec = synth.workload(name)
+        M, N, K = spec["M"], spec["N"], spec["K"]
+        da = torch.from_numpy(a).to(dev)
+        db = torch.from_numpy(b).to(dev)
+        dc = torch.empty((M, N), dtype=torch.float16, device=dev)
+        path = tc.hgemm_select_path(da, db, dc, M, N, K)
+        for _ in range(warmup):
+            flush.zero_()
+            tc.hgemm(da, db, dc, M, N, K, stream)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(launches)]
+        torch.cuda.synchronize(dev)
+        for s_ev, e_ev in evs:
+            flush.zero_()
+            s_ev.record(stream)
+            tc.hgemm(da, db, dc, M, N, K, stream)
+            e_ev.record(stream)
+        torch.cuda.synchronize(dev)
+        if tc.hgemm_device_status(stream) != tc.HGEMM_OK:
+            raise RuntimeError(f"a kernel wait timed out timing {name}")
+        times = [s_ev.elapsed_time(e_ev) for s_ev, e_ev in evs]
+        med = statistics.median(times)
+        rec = {"M": M, "N": N, "K": K, "seed": spec["seed"], "values": spec["kind"],
+               "launches": launches, "ms_median": med, "ms_mean": statistics.fmean(times),
+               "ms_min": min(times), "path": KERNEL_OF_PATH.get(path, f"path {path}")}
+        rec.update(roofline_of(flops_of(spec), bytes_of(spec), med, peaks))
+        out[name] = rec
+    return out
 
 
 # ------------------------------------------------------------ the oracle leg
@@ -506,31 +680,13 @@ def run_tri_ours(args, spec, a_col, b_col, world, rank, local):
     torch.cuda.synchronize(dev)
     if tc.hgemm_device_status(stream) != tc.HGEMM_OK:
         raise RuntimeError("a kernel wait timed out during warm-up")
-    sampler = ClockSampler(nvsmi_id(torch, dev, local))
-    sampler.start()
-    time.sleep(0.15)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize(dev)
-    t0 = time.time()
-    for s_ev, e_ev in evs:
-        flush.zero_()
-        s_ev.record(stream)
-        step()
-        e_ev.record(stream)
-    torch.cuda.synchronize(dev)
-    t1 = time.time()
-    if dist:
-        dist.barrier()
-    clocks = sampler.stop(t0, t1)
+    times_ms, clocks = timed_region(torch, dev, local, stream, step, flush, args.steps, dist)
     if tc.hgemm_device_status(stream) != tc.HGEMM_OK:
         raise RuntimeError("a kernel wait timed out in the timed region")
-    times_ms = [s_ev.elapsed_time(e_ev) for s_ev, e_ev in evs]
-    total_ms = reduce_max(sum(times_ms), dist, dev)
-    mean_ms = total_ms / args.steps
-    value = whole_job_tflops(world, args.steps, flops, total_ms)
+    # value and roofline from the median call (the slowest rank's median)
+    median_ms = reduce_max(statistics.median(times_ms), dist, dev)
+    mean_ms = reduce_max(statistics.fmean(times_ms), dist, dev)
+    value = whole_job_tflops(world, 1, flops, median_ms)
 
     e2e = None
     if not args.no_e2e:
@@ -560,11 +716,11 @@ def run_tri_ours(args, spec, a_col, b_col, world, rank, local):
 
     peaks, peak_src = load_peaks()
     peak = peaks["bf16_tflops"] * FP16_PER_BF16
-    achieved = flops / (mean_ms * 1e-3) / 1e12
+    achieved = flops / (median_ms * 1e-3) / 1e12
     roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
             "frac": achieved / peak, "traffic": None,
             "peak_source": f"{peak_src}: bf16_tflops (burst) x {FP16_PER_BF16} fp16/bf16",
-            "kernel": ops["kernel"],
+            "timing": "median call", "kernel": ops["kernel"],
             "algorithmic_flops": flops, "algorithmic_bytes": 2.0 * (n * (n + 1) / 2 + 2 * n * m)}
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -585,8 +741,8 @@ def run_tri_ours(args, spec, a_col, b_col, world, rank, local):
     if rank == 0:
         line = {
             "metric": metric_for(args.workload, spec), "value": value, "unit": UNIT, "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_ms,
-            "ms_per_step_median": statistics.median(times_ms), "higher_is_better": True,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": median_ms,
+            "ms_per_step_mean": mean_ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
             "config": {"workload": f"{args.workload}: {DESCRIPTIONS.get(args.workload, '')}",
                        "n": n, "m": m, "seed": spec["seed"],
@@ -597,7 +753,8 @@ def run_tri_ours(args, spec, a_col, b_col, world, rank, local):
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": args.steps * ((ops["launches"](n, m, 512) + 1) if op == "trsm" and not args.no_workspace
                                           else ops["launches"](n, m)),
-            "clocks": clocks,
+            "clocks": dict(clocks, kcycles_per_step=(median_ms * clocks["sm_mhz"]
+                                                     if clocks.get("sm_mhz") else None)),
         }
         print(json.dumps(line), flush=True)
     if dist:
@@ -671,32 +828,13 @@ def run_ours(args, spec, a, b, world, rank, local):
     if tc.hgemm_device_status(stream) != tc.HGEMM_OK:
         raise RuntimeError("a kernel wait timed out during warm-up")
 
-    sampler = ClockSampler(nvsmi_id(torch, dev, local))
-    sampler.start()
-    time.sleep(0.15)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize(dev)
-    t0 = time.time()
-    for s, e in evs:
-        flush.zero_()
-        s.record(stream)
-        step()
-        e.record(stream)
-    torch.cuda.synchronize(dev)
-    t1 = time.time()
-    if dist:
-        dist.barrier()
-    clocks = sampler.stop(t0, t1)
+    times_ms, clocks = timed_region(torch, dev, local, stream, step, flush, args.steps, dist)
     if tc.hgemm_device_status(stream) != tc.HGEMM_OK:
         raise RuntimeError("a kernel wait timed out in the timed region")
-    times_ms = [s.elapsed_time(e) for s, e in evs]
-    total_ms = reduce_max(sum(times_ms), dist, dev)
-    mean_ms = total_ms / args.steps
-    median_ms = statistics.median(times_ms)
-    value = whole_job_tflops(world, args.steps, flops, total_ms)
+    # value and roofline from the median launch (the slowest rank's median)
+    median_ms = reduce_max(statistics.median(times_ms), dist, dev)
+    mean_ms = reduce_max(statistics.fmean(times_ms), dist, dev)
+    value = whole_job_tflops(world, 1, flops, median_ms)
 
     # ---- end to end through the host-buffer entry point (the plain product)
     e2e = None
@@ -737,18 +875,29 @@ def run_ours(args, spec, a, b, world, rank, local):
                                f"{args.workload}+a_{args.a_layout}/b_{args.b_layout}", sha)
     if ai >= ridge:
         peak = peaks["bf16_tflops"] * FP16_PER_BF16
-        achieved = flops / (mean_ms * 1e-3) / 1e12
+        achieved = flops / (median_ms * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": traffic,
                 "peak_source": f"{peak_src}: bf16_tflops (burst) x {FP16_PER_BF16} fp16/bf16"}
     else:
         peak = peaks["hbm_gbs"]
-        achieved = nbytes / (mean_ms * 1e-3) / 1e9
+        achieved = nbytes / (median_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": traffic,
                 "peak_source": f"{peak_src}: hbm_gbs"}
-    roof.update({"kernel": kernel, "algorithmic_flops": flops,
+    roof.update({"timing": "median launch", "kernel": kernel, "algorithmic_flops": flops,
                  "algorithmic_bytes": nbytes, "source_sha": sha})
+
+    # ---- the other configurations (default run, rank 0)
+    configs = None
+    if (rank == 0 and args.workload == DEFAULT_WORKLOAD and not args.no_configs and epi is None
+            and not layouts):
+        configs = {args.workload: dict({"M": M, "N": N, "K": K, "seed": spec["seed"],
+                                        "values": spec["kind"], "launches": args.steps,
+                                        "ms_median": median_ms, "ms_mean": mean_ms,
+                                        "ms_min": min(times_ms), "path": kernel},
+                                       **roofline_of(flops, nbytes, median_ms, peaks))}
+        configs.update(time_configs(torch, tc, dev, stream, flush, peaks))
 
     # ---- the oracle on this host's cores (rank 0, one GPU only)
     cpu = None
@@ -765,8 +914,8 @@ def run_ours(args, spec, a, b, world, rank, local):
     if rank == 0:
         line = {
             "metric": metric_for(args.workload, spec), "value": value, "unit": UNIT, "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_ms,
-            "ms_per_step_median": median_ms, "higher_is_better": True, "scaling": "weak",
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": median_ms,
+            "ms_per_step_mean": mean_ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f16", "data": "synthetic",
             "config": {"workload": f"{args.workload}: {DESCRIPTIONS.get(args.workload, '')}",
                        "M": M, "N": N, "K": K, "seed": spec["seed"],
@@ -777,7 +926,10 @@ def run_ours(args, spec, a, b, world, rank, local):
                        "b_layout": args.b_layout,
                        "parallelism": f"replicas x{world}"},
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": args.steps, "clocks": clocks,
+            "gpu_launches": args.steps,
+            "clocks": dict(clocks, kcycles_per_step=(median_ms * clocks["sm_mhz"]
+                                                     if clocks.get("sm_mhz") else None)),
+            "configs": configs,
         }
         print(json.dumps(line), flush=True)
     if dist:

@@ -267,8 +267,13 @@ HGEMM_API int hgemm_trsm_ws(const hgemm_half_t *A, int64_t lda, const hgemm_half
  * (hgemm_trsm_workspace_size(n) > HGEMM_TRSM_NOALLOC_MAX_BYTES) returns
  * HGEMM_ERR_INVALID_ARG and enqueues nothing.
  *
- * The first call on a device (made with that device current) looks up the
- * array's device address once (cudaGetSymbolAddress) and keeps it; make that
+ * The device check comes first: on a device other than an sm_103 GPU the
+ * call returns HGEMM_ERR_UNSUPPORTED_DEVICE, like hgemm_trsm_ws. The first
+ * call on a host thread in a given CUDA context (the device's primary context
+ * as the runtime makes it current) looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current) and keeps it for that
+ * thread and context; a call in another context, or after the primary context
+ * was recreated by a device reset, looks it up again. Make each host thread's
  * first call before any stream capture on the device. Every call on a device
  * shares the one array, which keeps the last call's contents (each call
  * writes every entry it reads, so nothing needs clearing): calls whose work

@@ -69,6 +69,8 @@ def _load():
         lib.oracle_trsm.argtypes = [u16p, i64, u16p, i64, u16p, i64, i64, i64, ctypes.c_double,
                                     ctypes.c_int]
         lib.oracle_trsm.restype = ctypes.c_int
+        lib.oracle_trsm_n.argtypes = lib.oracle_trsm.argtypes
+        lib.oracle_trsm_n.restype = ctypes.c_int
         lib.oracle_fp16_to_double.argtypes = [ctypes.c_uint16]
         lib.oracle_fp16_to_double.restype = ctypes.c_double
         lib.oracle_double_to_fp16.argtypes = [ctypes.c_double]
@@ -226,6 +228,27 @@ def trsm(a: np.ndarray, b: np.ndarray, alpha: float = 1.0, nthreads: int | None 
                              float(alpha), _threads(nthreads))
     if rc != 0:
         raise MemoryError("oracle_trsm could not allocate its work space")
+    return np.ascontiguousarray(x_col.T)
+
+
+def trsm_n(a: np.ndarray, b: np.ndarray, alpha: float = 1.0, nthreads: int | None = None) -> np.ndarray:
+    """The solve in the TRMM page's literal orientation (§2.3, X = A\\B):
+    X (n, m) float16 with A·X = alpha·B, A the lower triangle of a (n, n)
+    (the rest is not read), b (n, m), in mathematical orientation; FP64
+    forward substitution, one rounding."""
+    a = np.asarray(a, dtype=np.float16)
+    b = np.asarray(b, dtype=np.float16)
+    n = a.shape[0]
+    if a.shape != (n, n) or b.ndim != 2 or b.shape[0] != n:
+        raise ValueError("a must be (n, n) and b (n, m)")
+    m = b.shape[1]
+    a_col = np.ascontiguousarray(a.T)
+    b_col = np.ascontiguousarray(b.T)
+    x_col = np.empty((m, n), dtype=np.float16)
+    rc = _load().oracle_trsm_n(a_col.ctypes.data, n, b_col.ctypes.data, n, x_col.ctypes.data, n, n, m,
+                               float(alpha), _threads(nthreads))
+    if rc != 0:
+        raise MemoryError("oracle_trsm_n could not allocate its work space")
     return np.ascontiguousarray(x_col.T)
 
 

@@ -357,6 +357,7 @@ struct trsm_job {
     double alpha;
     int64_t col_lo, col_hi;
     double *work;    /* n doubles per job */
+    int trans;       /* 1: Aᵀ·X = alpha·B (back substitution); 0: A·X = alpha·B (forward) */
 };
 
 static void *trsm_worker(void *arg)
@@ -365,11 +366,22 @@ static void *trsm_worker(void *arg)
     const int64_t n = jb->n;
     double *x = jb->work;
     for (int64_t j = jb->col_lo; j < jb->col_hi; ++j) {
-        for (int64_t i = n - 1; i >= 0; --i) {
-            double s = jb->alpha * g_decode[jb->B[j * jb->ldb + i]];
-            for (int64_t k = i + 1; k < n; ++k)
-                s -= g_decode[jb->A[i * jb->lda + k]] * x[k];
-            x[i] = s / g_decode[jb->A[i * jb->lda + i]];
+        if (jb->trans) {
+            /* row i of Aᵀ holds A(k,i) for k >= i: last row first */
+            for (int64_t i = n - 1; i >= 0; --i) {
+                double s = jb->alpha * g_decode[jb->B[j * jb->ldb + i]];
+                for (int64_t k = i + 1; k < n; ++k)
+                    s -= g_decode[jb->A[i * jb->lda + k]] * x[k];
+                x[i] = s / g_decode[jb->A[i * jb->lda + i]];
+            }
+        } else {
+            /* row i of A holds A(i,k) for k <= i: first row first */
+            for (int64_t i = 0; i < n; ++i) {
+                double s = jb->alpha * g_decode[jb->B[j * jb->ldb + i]];
+                for (int64_t k = 0; k < i; ++k)
+                    s -= g_decode[jb->A[k * jb->lda + i]] * x[k];
+                x[i] = s / g_decode[jb->A[i * jb->lda + i]];
+            }
         }
         for (int64_t i = 0; i < n; ++i)
             jb->X[j * jb->ldx + i] = oracle_double_to_fp16(x[i]);
@@ -377,8 +389,29 @@ static void *trsm_worker(void *arg)
     return NULL;
 }
 
+static int trsm_run(const uint16_t *A, int64_t lda, const uint16_t *B, int64_t ldb, uint16_t *X,
+                    int64_t ldx, int64_t n, int64_t m, double alpha, int nthreads, int trans);
+
 int oracle_trsm(const uint16_t *A, int64_t lda, const uint16_t *B, int64_t ldb, uint16_t *X,
                 int64_t ldx, int64_t n, int64_t m, double alpha, int nthreads)
+{
+    return trsm_run(A, lda, B, ldb, X, ldx, n, m, alpha, nthreads, 1);
+}
+
+/* The page's literal orientation of the solve (§2.3: X = A\B column by
+ * column): A·X = alpha·B with the same lower triangle A, untransposed, so
+ * row i of the system is sum_{k <= i} A(i,k)·x_k = alpha·b_i, solved by
+ * forward substitution, x_i = (alpha·b_i − Σ_{k<i} A(i,k)·x_k) / A(i,i), k
+ * increasing, in FP64, each x_i rounded once at the end. Same operands,
+ * layout and reading of the lower triangle only as oracle_trsm. */
+int oracle_trsm_n(const uint16_t *A, int64_t lda, const uint16_t *B, int64_t ldb, uint16_t *X,
+                  int64_t ldx, int64_t n, int64_t m, double alpha, int nthreads)
+{
+    return trsm_run(A, lda, B, ldb, X, ldx, n, m, alpha, nthreads, 0);
+}
+
+static int trsm_run(const uint16_t *A, int64_t lda, const uint16_t *B, int64_t ldb, uint16_t *X,
+                    int64_t ldx, int64_t n, int64_t m, double alpha, int nthreads, int trans)
 {
     pthread_once(&g_decode_once, fill_decode_table);
     if (n <= 0 || m <= 0)
@@ -400,7 +433,7 @@ int oracle_trsm(const uint16_t *A, int64_t lda, const uint16_t *B, int64_t ldb, 
     }
     for (int t = 0; t < nthreads; ++t) {
         struct trsm_job jb = {A, B, X, lda, ldb, ldx, n, alpha, m * t / nthreads, m * (t + 1) / nthreads,
-                              work + (size_t)t * (size_t)n};
+                              work + (size_t)t * (size_t)n, trans};
         jobs[t] = jb;
         if (t == 0)
             continue;

@@ -25,6 +25,9 @@ Value recipes (the workloads of the benchmark configurations):
   * ``normal``   : Box-Muller on consecutive uniform pairs
                    z = sqrt(-2 ln(1 - u1)) * cos(2π u2); A ~ N(0, 1) and
                    B ~ N(0, 1)/sqrt(K), each rounded to FP16;
+  * ``normal_both``: the same draws with both operands scaled by 1/sqrt(K)
+                   (the literal reading of "N(0,1) values scaled by
+                   1/sqrt(K)"; C then has standard deviation 1/sqrt(K));
   * ``unit``     : u rounded to the nearest FP16 (values in [0, 1]), like
                    the rand(Float32) operands of the TRMM page's example (§5.1).
 
@@ -71,7 +74,7 @@ def uniform01(seed: int, start: int, count: int) -> np.ndarray:
 
 def _fill(seed: int, start: int, count: int, kind: str, scale: float) -> np.ndarray:
     out = np.empty(count, dtype=np.float16)
-    per = 2 if kind == "normal" else 1
+    per = 2 if kind in ("normal", "normal_both") else 1
     for lo in range(0, count, _CHUNK):
         n = min(_CHUNK, count - lo)
         if kind == "uniform":
@@ -80,7 +83,7 @@ def _fill(seed: int, start: int, count: int, kind: str, scale: float) -> np.ndar
             v = uniform01(seed, start + lo, n)
         elif kind == "int":
             v = np.floor(5.0 * uniform01(seed, start + lo, n)) - 2.0
-        elif kind == "normal":
+        elif kind in ("normal", "normal_both"):
             u = uniform01(seed, start + per * lo, per * n)
             u1, u2 = u[0::2], u[1::2]
             v = np.sqrt(-2.0 * np.log1p(-u1)) * np.cos(2.0 * np.pi * u2) * scale
@@ -93,9 +96,10 @@ def _fill(seed: int, start: int, count: int, kind: str, scale: float) -> np.ndar
 def operands(M: int, N: int, K: int, seed: int, kind: str = "uniform"):
     """Returns (A, B): A as an (M, K) array, B as an (N, K) array whose row j
     is column j of the K×N operand, both float16 and C-contiguous."""
-    per = 2 if kind == "normal" else 1
-    b_scale = 1.0 / np.sqrt(K) if (kind == "normal" and K > 0) else 1.0
-    a = _fill(seed, 0, M * K, kind, 1.0).reshape(M, K)
+    per = 2 if kind in ("normal", "normal_both") else 1
+    b_scale = 1.0 / np.sqrt(K) if (kind in ("normal", "normal_both") and K > 0) else 1.0
+    a_scale = 1.0 / np.sqrt(K) if (kind == "normal_both" and K > 0) else 1.0
+    a = _fill(seed, 0, M * K, kind, a_scale).reshape(M, K)
     b = _fill(seed, per * M * K, N * K, kind, b_scale).reshape(N, K)
     return a, b
 
@@ -108,6 +112,8 @@ WORKLOADS = {
     "hgemm_2048": dict(M=2048, N=2048, K=2048, kind="uniform", seed=1001),
     "hgemm_1000_ragged": dict(M=1000, N=1000, K=1000, kind="uniform", seed=1002),
     "hgemm_8192": dict(M=8192, N=8192, K=8192, kind="normal", seed=1003),
+    # the same draws with A scaled as well (a secondary parity case)
+    "hgemm_8192_both_scaled": dict(M=8192, N=8192, K=8192, kind="normal_both", seed=1003),
     "hgemm_4096x256x4096_skinny": dict(M=4096, N=256, K=4096, kind="uniform", seed=1004),
     # the TRMM page's shapes: 8192×8192 (its measurements, §4.2) and A 4096×4096
     # with a 4096×256 right-hand side (its example, §5.1)

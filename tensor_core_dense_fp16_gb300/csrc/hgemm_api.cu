@@ -45,10 +45,46 @@ struct DeviceState {
   std::atomic<int> ready{0};  // 0 unknown, 1 supported, -1 unsupported
   int id = 0;
   int num_sms = 0;
-  int* status = nullptr;
   hg::DeviceProfile prof{};
 };
 DeviceState g_devices[kMaxDevices];
+
+// Device addresses of the library's static device variables (the watchdog
+// word, the fixed TRSM workspace) belong to the context they were looked up
+// in. Each host thread keeps the ones of its current context and looks them
+// up again when that context changes (another context on the device, or the
+// primary context recreated after a device reset).
+struct ContextCache {
+  unsigned long long ctx = 0;  // cuCtxGetId of the context, 0: none cached
+  int* status = nullptr;       // the watchdog word
+  void* noalloc = nullptr;     // hgemm_trsm_noalloc's array (null: not yet looked up)
+};
+thread_local ContextCache t_ctx;
+
+// Unique identity (for the life of the process) of the calling thread's
+// current context, or 0 when it cannot be determined.
+unsigned long long current_context_id() {
+  static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx ||
+      get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
 
 // One product: operands, sizes and row pitches in elements (A(i,k) at
 // A[i*lda + k], B(k,j) at B[j*ldb + k], C(i,j) at C[i*ldc + j]; with a_mn,
@@ -112,11 +148,8 @@ int current_device(DeviceState** out) {
       if (major != 10 || minor != 3) {
         r = -1;
       } else {
-        int* status = nullptr;
-        if ((e = hg::status_word_address(&status)) != cudaSuccess) return cuda_fail(e);
         st.id = dev;
         st.num_sms = sms;
-        st.status = status;
         st.prof.num_sms = sms;
         st.prof.pair_clusters = hg::pair_max_clusters(sms);
         st.prof.split2_clusters = hg::skinny_max_clusters(2, 256, sms);
@@ -129,6 +162,13 @@ int current_device(DeviceState** out) {
     }
   }
   if (r < 0) return HGEMM_ERR_UNSUPPORTED_DEVICE;
+  // the watchdog word's address in the calling thread's current context
+  const unsigned long long ctx = current_context_id();
+  if (ctx == 0 || ctx != t_ctx.ctx) {
+    int* status = nullptr;
+    if ((e = hg::status_word_address(&status)) != cudaSuccess) return cuda_fail(e);
+    t_ctx = ContextCache{ctx, status, nullptr};
+  }
   g_last_profile.store(&st.prof, std::memory_order_release);
   *out = &st;
   return HGEMM_OK;
@@ -352,7 +392,7 @@ int run_tc(const Gemm& g, const hg::EpiArgs& epi, const DeviceState& dev,
   args.full_tiles = args.num_tiles;
   args.group_m = group_m_setting();
   args.grid = static_cast<int>(tiles < dev.num_sms ? tiles : dev.num_sms);
-  args.status = dev.status;
+  args.status = t_ctx.status;
   args.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
   args.inject = g_inject.load(std::memory_order_relaxed);
   args.epi = epi;
@@ -418,7 +458,7 @@ int run_tc_pair(const Gemm& g, const hg::EpiArgs& epi, const DeviceState& dev,
   args.num_tiles = static_cast<int>(parts > 1 ? tiles - rest + parts * rest : tiles);
   args.group_m = group_m_setting();
   args.grid = static_cast<int>(2 * (args.num_tiles < clusters ? args.num_tiles : clusters));
-  args.status = dev.status;
+  args.status = t_ctx.status;
   args.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
   args.inject = g_inject.load(std::memory_order_relaxed);
   args.epi = epi;
@@ -476,7 +516,7 @@ int run_tc_wide(const Gemm& g, const hg::EpiArgs& epi, const DeviceState& dev,
   args.group_m = group_m_setting();
   const int64_t clusters = hg::wide_max_clusters(dev.num_sms);
   args.grid = static_cast<int>(2 * (tiles < clusters ? tiles : clusters));
-  args.status = dev.status;
+  args.status = t_ctx.status;
   args.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
   args.inject = g_inject.load(std::memory_order_relaxed);
   args.epi = epi;
@@ -517,7 +557,7 @@ int run_skinny(const Gemm& g, int split, int tile_n, const hg::EpiArgs& epi, con
   args.full_tiles = args.num_tiles;
   args.group_m = 1;
   args.grid = static_cast<int>(tiles * 2 * split);
-  args.status = dev.status;
+  args.status = t_ctx.status;
   args.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
   args.inject = g_inject.load(std::memory_order_relaxed);
   args.epi = epi;
@@ -549,7 +589,7 @@ int dispatch(const Gemm& g, const hg::EpiArgs& epi, const DeviceState& dev, cuda
     default: {
       hg::PlainArgs pa{static_cast<const uint16_t*>(g.A), static_cast<const uint16_t*>(g.B),
                        static_cast<uint16_t*>(g.C), g.M, g.N, g.K, g.lda, g.ldb, g.ldc,
-                       dev.status, g_timeout_ns.load(), epi, g.a_mn ? 1 : 0, g.b_mn ? 1 : 0};
+                       t_ctx.status, g_timeout_ns.load(), epi, g.a_mn ? 1 : 0, g.b_mn ? 1 : 0};
       e = hg::launch_generic(pa, dev.num_sms, stream);
       return e == cudaSuccess ? HGEMM_OK : cuda_fail(e);
     }
@@ -767,7 +807,7 @@ int hgemm_trmm(const hgemm_half_t* A, int64_t lda, const hgemm_half_t* B, int64_
       args.num_tiles = leaves.count * args.num_m;
       args.full_tiles = args.num_tiles;
       args.grid = args.num_tiles < dev->num_sms ? args.num_tiles : dev->num_sms;
-      args.status = dev->status;
+      args.status = t_ctx.status;
       args.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
       args.inject = g_inject.load(std::memory_order_relaxed);
       args.epi = scale;
@@ -821,7 +861,7 @@ int hgemm_trmm(const hgemm_half_t* A, int64_t lda, const hgemm_half_t* B, int64_
   if (!tc_leaves) {
     hg::PlainArgs pa{reinterpret_cast<const uint16_t*>(B), reinterpret_cast<const uint16_t*>(A),
                      reinterpret_cast<uint16_t*>(C), m, n, n, ldb, lda, ldc,
-                     dev->status, g_timeout_ns.load(), scale};
+                     t_ctx.status, g_timeout_ns.load(), scale};
     e = hg::launch_tri_leaves(pa, leaves, dev->num_sms, stream);
   }
   if (e != cudaSuccess) return cuda_fail(e);
@@ -1058,9 +1098,6 @@ namespace {
 
 __device__ __align__(256) uint16_t g_trsm_noalloc_scratch[HGEMM_TRSM_NOALLOC_MAX_BYTES / 2];
 
-std::mutex g_noalloc_mu;
-void* g_noalloc_addr[kMaxDevices] = {};  // device address of the array per device (null: not yet)
-
 }  // namespace
 
 int hgemm_trsm_noalloc(const hgemm_half_t* A, int64_t lda, const hgemm_half_t* B, int64_t ldb,
@@ -1069,21 +1106,19 @@ int hgemm_trsm_noalloc(const hgemm_half_t* A, int64_t lda, const hgemm_half_t* B
   if (n == 0 || m == 0) return HGEMM_OK;
   const size_t need = hgemm_trsm_workspace_size(n);
   if (need == 0 || need > HGEMM_TRSM_NOALLOC_MAX_BYTES) return HGEMM_ERR_INVALID_ARG;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_fail(e);
-  if (dev < 0 || dev >= kMaxDevices) return HGEMM_ERR_UNSUPPORTED_DEVICE;
-  void* scratch = nullptr;
-  {
-    std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (!g_noalloc_addr[dev]) {
-      void* p = nullptr;
-      if ((e = cudaGetSymbolAddress(&p, g_trsm_noalloc_scratch)) != cudaSuccess) return cuda_fail(e);
-      g_noalloc_addr[dev] = p;
-    }
-    scratch = g_noalloc_addr[dev];
+  // the device check (sm_103) first; it also binds the device's context to
+  // this thread and refreshes t_ctx when that context changed
+  DeviceState* dev = nullptr;
+  const int rc = current_device(&dev);
+  if (rc != HGEMM_OK) return rc;
+  if (!t_ctx.noalloc) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_trsm_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e);
+    t_ctx.noalloc = p;
   }
-  return hgemm_trsm_ws(A, lda, B, ldb, X, ldx, n, m, alpha, scratch, HGEMM_TRSM_NOALLOC_MAX_BYTES, stream);
+  return hgemm_trsm_ws(A, lda, B, ldb, X, ldx, n, m, alpha, t_ctx.noalloc, HGEMM_TRSM_NOALLOC_MAX_BYTES,
+                       stream);
 }
 
 int hgemm_host(const hgemm_half_t* hA, const hgemm_half_t* hB, hgemm_half_t* hC, int64_t M,
@@ -1186,11 +1221,11 @@ int hgemm_device_status(cudaStream_t stream) {
   cudaError_t e = cudaStreamSynchronize(stream);
   if (e != cudaSuccess) return cuda_fail(e);
   int word = 0;
-  if ((e = cudaMemcpy(&word, dev->status, sizeof(int), cudaMemcpyDeviceToHost)) != cudaSuccess)
+  if ((e = cudaMemcpy(&word, t_ctx.status, sizeof(int), cudaMemcpyDeviceToHost)) != cudaSuccess)
     return cuda_fail(e);
   if (word != 0) {
     const int zero = 0;
-    if ((e = cudaMemcpy(dev->status, &zero, sizeof(int), cudaMemcpyHostToDevice)) != cudaSuccess)
+    if ((e = cudaMemcpy(t_ctx.status, &zero, sizeof(int), cudaMemcpyHostToDevice)) != cudaSuccess)
       return cuda_fail(e);
     return HGEMM_ERR_TIMEOUT;
   }

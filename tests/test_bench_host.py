@@ -1,0 +1,58 @@
+"""Host-side logic of the benchmark (CPU only): the roofline arithmetic of
+each configuration and the clock sampler's behaviour without a GPU."""
+
+import pytest
+
+import bench
+
+PEAKS = {"hbm_gbs": 6789.0, "bf16_tflops": 1874.3}
+
+
+def test_roofline_tensor_bound_8192_cube():
+    spec = dict(M=8192, N=8192, K=8192)
+    flops, nbytes = bench.flops_of(spec), bench.bytes_of(spec)
+    assert flops == 2.0 * 8192 ** 3
+    assert nbytes == 2.0 * 3 * 8192 ** 2
+    r = bench.roofline_of(flops, nbytes, 0.6, PEAKS)
+    assert r["bound"] == "tensor"
+    # 1.0995e12 flop at 1874.3 TFLOP/s = 586.6 us; measured 600 us
+    assert r["roofline_us"] == pytest.approx(flops / 1874.3e12 * 1e6)
+    assert r["frac"] == pytest.approx(flops / 1874.3e12 / 0.6e-3)
+    assert r["tflops"] == pytest.approx(flops / 0.6e-3 / 1e12)
+
+
+def test_roofline_hbm_bound_skinny():
+    spec = dict(M=4096, N=256, K=4096)
+    flops, nbytes = bench.flops_of(spec), bench.bytes_of(spec)
+    assert nbytes == 37748736.0
+    r = bench.roofline_of(flops, nbytes, 0.0209, PEAKS)
+    assert r["bound"] == "hbm"
+    assert r["roofline_us"] == pytest.approx(nbytes / 6789e9 * 1e6)   # 5.56 us
+    assert r["frac"] == pytest.approx(nbytes / 6789e9 / 20.9e-6)      # 0.266
+    assert r["gbs"] == pytest.approx(nbytes / 20.9e-6 / 1e9)
+
+
+def test_fused_epilogue_bytes():
+    spec = dict(M=64, N=32, K=16)
+    plain = bench.bytes_of(spec)
+    assert bench.bytes_of(spec, (1.0, 1.0, True, False)) == plain + 2 * 64 * 32 + 2 * 32
+    assert bench.bytes_of(spec, (2.0, 0.0, False, True)) == plain
+
+
+def test_config_list_covers_the_other_workloads():
+    import synth
+    assert set(bench.CONFIG_WORKLOADS) <= set(synth.WORKLOADS)
+    assert bench.DEFAULT_WORKLOAD not in bench.CONFIG_WORKLOADS
+    names = {"hgemm_256", "hgemm_256_int", "hgemm_2048", "hgemm_1000_ragged",
+             "hgemm_4096x256x4096_skinny"}
+    assert set(bench.CONFIG_WORKLOADS) == names
+
+
+def test_nvml_sampler_without_a_device_reports_itself_unavailable():
+    s = bench.NvmlSampler("GPU-00000000-0000-0000-0000-000000000000")
+    s.start()
+    rec = s.stop(0.0, 1.0)
+    if s.lib is None:
+        assert rec["samples"] == 0 and "unavailable" in rec["source"]
+    else:   # a host with a GPU: whatever it sampled is summarised
+        assert rec["samples"] >= 0

@@ -50,6 +50,13 @@ def test_recipes_and_layout():
     assert abs(float(an.astype(np.float64).std()) - 1.0) < 0.02
     assert abs(float(bn.astype(np.float64).std()) * 32.0 - 1.0) < 0.03  # 1/sqrt(1024)
 
+    # both operands scaled: the same draws, A divided by sqrt(K) as well
+    a2, b2 = synth.operands(128, 64, 1024, seed=5, kind="normal_both")
+    assert np.array_equal(b2, bn)
+    u = synth.uniform01(5, 0, 2 * 128 * 1024)
+    z = np.sqrt(-2 * np.log1p(-u[0::2])) * np.cos(2 * np.pi * u[1::2]) / 32.0
+    assert np.array_equal(a2.reshape(-1), z.astype(np.float16))
+
 
 def test_chunking_is_invisible():
     n = synth._CHUNK + 1000

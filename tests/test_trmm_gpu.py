@@ -149,3 +149,82 @@ def test_trmm_carried_and_separate_updates():
     a, b = trmm_inputs(n, m, seed=29)
     ref = oracle.trmm(a, b, nthreads=oracle_threads())
     assert_close(run_trmm(a, b), ref, what="trmm 2048x8200")
+
+
+# ---- signed operands: the envelope of the recursion's FP16 intermediates
+
+def signed_inputs(n, m, seed):
+    rng = np.random.default_rng(seed)
+    a = rng.uniform(-1, 1, size=(n, n)).astype(np.float16)
+    b = rng.uniform(-1, 1, size=(n, m)).astype(np.float16)
+    return a, b
+
+
+def separate_update_levels(n, m, tc_leaves, forced=False):
+    """Levels of the recursion whose updates run as products of their own
+    (each rounds the rows it updates to FP16 once more); the other updates
+    are carried by the tensor-core leaves, inside their single rounding.
+    Blocks split at half rounded up to 64 and stop at 256; a leaf carries an
+    update of at most 2^33 multiply-adds."""
+    levels = set()
+
+    def walk(s, depth):
+        if s <= 256:
+            return
+        s1 = ((s // 2 + 63) // 64) * 64
+        if not tc_leaves or forced or m * s1 * (s - s1) > 2 ** 33:
+            levels.add(depth)
+        walk(s1, depth + 1)
+        walk(s - s1, depth + 1)
+
+    walk(n, 0)
+    return len(levels)
+
+
+@pytest.mark.parametrize("n,m", [(2048, 512), (4096, 256), (8192, 512)])
+def test_trmm_signed_single_rounding(n, m):
+    """Operands uniform on [-1, 1]: where every update is carried by the
+    tensor-core leaves (n a multiple of 64, m·s1·s2 <= 2^33 for every
+    update, including n = 8192 with m = 512), each output is one FP32 sum
+    rounded once, like a product, and the product's tolerance holds."""
+    assert separate_update_levels(n, m, tc_leaves=True) == 0
+    a, b = signed_inputs(n, m, seed=101 + n)
+    ref = oracle.trmm(a, b, nthreads=oracle_threads())
+    assert_close(run_trmm(a, b), ref, what=f"signed trmm {n}x{m}")
+
+
+@pytest.mark.parametrize("n,m,path", [(2048, 8200, None), (1000, 128, None),
+                                      (2048, 300, tc.HGEMM_PATH_TC_PAIR)])
+def test_trmm_signed_separate_updates_envelope(n, m, path):
+    """Operands uniform on [-1, 1] where some updates run as separate
+    products (a large update, generic leaves at n = 1000, or a forced path):
+    each such level rounds a partial sum P of the output to FP16 once more,
+    an error of at most 2^-11·|P| <= 2^-11·S with S = sum |A(k,i)|·|B(k,j)|
+    (the oracle's product of the absolute values). With R such levels the
+    product's tolerance widens by R·2^-11·S; with nonnegative operands
+    S = |C| and the widening is inside the product's tolerance, which the
+    other tests apply. A dropped or doubled update, or a wrong sign, is off
+    by far more than the widening."""
+    a, b = signed_inputs(n, m, seed=211 + n + m)
+    r = separate_update_levels(n, m, tc_leaves=(n % 64 == 0), forced=path is not None)
+    assert r >= 1
+    ref = oracle.trmm(a, b, nthreads=oracle_threads()).astype(np.float64)
+    s_abs = oracle.trmm(np.abs(a), np.abs(b), nthreads=oracle_threads()).astype(np.float64)
+    if path is not None:
+        tc.hgemm_force_path(path)
+    try:
+        got = run_trmm(a, b).astype(np.float64)
+    finally:
+        if path is not None:
+            tc.hgemm_force_path(-1)
+    assert not np.isnan(got).any()
+    err = np.abs(got - ref)
+    lim = 1e-2 * np.maximum(1.0, np.abs(ref)) + r * 2.0 ** -11 * s_abs * (1 + 2.0 ** -10)
+    assert np.all(err <= lim), (
+        f"signed trmm {n}x{m} ({r} separate levels): {int((err > lim).sum())} outputs out of "
+        f"the envelope, worst {float((err / lim).max()):.3g}x")
+    # a dropped update of the top level would leave rows [0, s1) off by the
+    # whole update, far outside the envelope there
+    s1 = ((n // 2 + 63) // 64) * 64
+    upd = (a[s1:, :s1].astype(np.float64).T @ b[s1:].astype(np.float64))
+    assert np.mean(np.abs(upd) > lim[:s1]) > 0.5
