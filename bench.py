@@ -498,8 +498,31 @@ def roofline_of(flops, nbytes, ms, peaks):
             "roofline_us": 1e6 * max(t_tensor, t_hbm)}
 
 
-def time_configs(torch, tc, dev, stream, flush, peaks, launches=50, warmup=5):
-    """Each configuration: `launches` flushed, event-timed calls of hgemm."""
+def time_launch_floor(torch, tc, dev, stream, flush, launches=200, warmup=5):
+    """The fixed cost of one launch under the same protocol: a kernel that
+    does nothing, in the pair kernel's launch configuration, after an L2
+    flush, bracketed by CUDA events."""
+    for _ in range(warmup):
+        flush.zero_()
+        tc.hgemm_launch_floor(True, stream)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(launches)]
+    torch.cuda.synchronize(dev)
+    for s_ev, e_ev in evs:
+        flush.zero_()
+        s_ev.record(stream)
+        tc.hgemm_launch_floor(True, stream)
+        e_ev.record(stream)
+    torch.cuda.synchronize(dev)
+    times = [s_ev.elapsed_time(e_ev) for s_ev, e_ev in evs]
+    return {"kernel": "hgemm_launch_floor (empty kernel, the pair kernel's launch configuration)",
+            "launches": launches, "ms_median": statistics.median(times),
+            "ms_mean": statistics.fmean(times), "ms_min": min(times)}
+
+
+def time_configs(torch, tc, dev, stream, flush, peaks, launches=50, warmup=5, floor_ms=None):
+    """Each configuration: `launches` flushed, event-timed calls of hgemm.
+    With the launch floor, also the fraction of (roofline + floor) time."""
     out = {}
     for name in CONFIG_WORKLOADS:
         a, b, spec = synth.workload(name)
@@ -528,6 +551,9 @@ def time_configs(torch, tc, dev, stream, flush, peaks, launches=50, warmup=5):
                "launches": launches, "ms_median": med, "ms_mean": statistics.fmean(times),
                "ms_min": min(times), "path": KERNEL_OF_PATH.get(path, f"path {path}")}
         rec.update(roofline_of(flops_of(spec), bytes_of(spec), med, peaks))
+        if floor_ms is not None:
+            rec["frac_with_floor"] = (rec["roofline_us"] * 1e-3 + floor_ms) / med
+        rec["traffic"] = profiled_traffic(rec["path"], name, kernel_sources_sha(rec["path"]))
         out[name] = rec
     return out
 
@@ -892,12 +918,14 @@ def run_ours(args, spec, a, b, world, rank, local):
     configs = None
     if (rank == 0 and args.workload == DEFAULT_WORKLOAD and not args.no_configs and epi is None
             and not layouts):
+        floor = time_launch_floor(torch, tc, dev, stream, flush)
         configs = {args.workload: dict({"M": M, "N": N, "K": K, "seed": spec["seed"],
                                         "values": spec["kind"], "launches": args.steps,
                                         "ms_median": median_ms, "ms_mean": mean_ms,
-                                        "ms_min": min(times_ms), "path": kernel},
+                                        "ms_min": min(times_ms), "path": kernel, "traffic": traffic},
                                        **roofline_of(flops, nbytes, median_ms, peaks))}
-        configs.update(time_configs(torch, tc, dev, stream, flush, peaks))
+        configs.update(time_configs(torch, tc, dev, stream, flush, peaks, floor_ms=floor["ms_median"]))
+        configs["launch_floor"] = floor
 
     # ---- the oracle on this host's cores (rank 0, one GPU only)
     cpu = None

@@ -245,6 +245,18 @@ HGEMM_API size_t hgemm_trsm_workspace_size(int64_t n);
  * inverse once more. A null workspace, one too small or not 16-byte
  * aligned is HGEMM_ERR_INVALID_ARG; X not suited to the tensor-core path, or
  * a path forced by hgemm_force_path, solves as hgemm_trsm does.
+ * Accuracy against hgemm_trsm: rounding L_b⁻¹ to FP16 adds at most
+ * 2^-11·(|L_b⁻¹|ᵀ·|b_b|) to each x in block b (b_b the block's right-hand
+ * side after the updates), so the result meets the per-element tolerance
+ * 1e-2·max(1, |x|) wherever |L_b⁻¹|ᵀ·|b_b| <= 16·max(1, |x_b|), i.e. while
+ * the diagonal blocks' inverses do not cancel heavily. Measured against the
+ * FP64 solve: with a diagonal in [1, 2) and a strict lower part below c/n,
+ * both entry points stay within that tolerance up to c = 512 at n = 4096
+ * and 8192 (entries up to 1/8 and 1/16) and up to c = 256 at n = 1024
+ * (entries up to 1/4); past that (n = 1024, c = 512: the solution grows to
+ * ~350 from a right-hand side below 1) neither does, while the
+ * componentwise backward error |Aᵀ·X − alpha·B| / (|Aᵀ|·|X| + |alpha·B|)
+ * of both stays below 4·2^-11.
  */
 HGEMM_API int hgemm_trsm_ws(const hgemm_half_t *A, int64_t lda, const hgemm_half_t *B, int64_t ldb,
                   hgemm_half_t *X, int64_t ldx, int64_t n, int64_t m, float alpha,
@@ -383,6 +395,18 @@ HGEMM_API int hgemm_debug_inject(int what);
 /* hgemm_last_cuda_error — the cudaError_t behind the last HGEMM_ERR_CUDA
  * returned on this host thread (0 if none). */
 HGEMM_API int hgemm_last_cuda_error(void);
+
+/*
+ * hgemm_launch_floor — measurement aid: enqueues a kernel that does nothing,
+ * so that a caller can time the fixed cost of one launch on its GPU and
+ * stream (the part of a small product's time that no kernel design
+ * removes). pair_config = 0: one CTA of one warp; otherwise the launch
+ * configuration of the CTA-pair product kernel (one CTA per SM in clusters
+ * of two, 192 threads, the pair kernel's dynamic shared memory,
+ * programmatic stream serialization). Touches no memory. Same return values
+ * as hgemm (HGEMM_ERR_UNSUPPORTED_DEVICE, HGEMM_ERR_CUDA).
+ */
+HGEMM_API int hgemm_launch_floor(int pair_config, cudaStream_t stream);
 
 /* hgemm_status_string — static text for a status code; never NULL. */
 HGEMM_API const char *hgemm_status_string(int status);

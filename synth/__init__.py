@@ -134,15 +134,17 @@ def trmm_operands(n: int, m: int, seed: int, kind: str = "unit"):
     return a, b
 
 
-def trsm_operands(n: int, m: int, seed: int):
-    """(a_col, b_col) as for trmm_operands, with the diagonally dominant A."""
+def trsm_operands(n: int, m: int, seed: int, c: float = 1.0):
+    """(a_col, b_col) as for trmm_operands, with the diagonally dominant A
+    (c = 1). c > 1 scales the strict lower part to c·u/n: column sums up to
+    c, a triangle that is no longer diagonally dominant for c > 1."""
     a = np.empty(n * n, dtype=np.float16)
     for lo in range(0, n * n, _CHUNK):
         cnt = min(_CHUNK, n * n - lo)
         u = uniform01(seed, lo, cnt)
         idx = np.arange(lo, lo + cnt)
         diag = (idx // n) == (idx % n)
-        a[lo:lo + cnt] = np.where(diag, 1.0 + u, u / n).astype(np.float16)
+        a[lo:lo + cnt] = np.where(diag, 1.0 + u, c * u / n).astype(np.float16)
     b = _fill(seed, n * n, m * n, "unit", 1.0).reshape(m, n)
     return a.reshape(n, n), b
 

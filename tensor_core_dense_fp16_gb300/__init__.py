@@ -28,7 +28,7 @@ __all__ = [
     "HgemmError", "library_path", "load", "hgemm", "hgemm_host", "hgemm_select_path",
     "hgemm_force_path", "hgemm_device_status", "hgemm_last_cuda_error",
     "hgemm_status_string", "hgemm_version", "hgemm_set_wait_timeout", "hgemm_debug_inject",
-    "hgemm_force_split", "hgemm_ex", "hgemm_strided", "hgemm_trmm", "hgemm_trsm", "hgemm_trsm_ws", "hgemm_trsm_workspace_size", "hgemm_trsm_noalloc", "hgemm_layout", "HGEMM_TRMM_MAX_N", "HGEMM_TRSM_NOALLOC_MAX_BYTES",
+    "hgemm_force_split", "hgemm_launch_floor", "hgemm_ex", "hgemm_strided", "hgemm_trmm", "hgemm_trsm", "hgemm_trsm_ws", "hgemm_trsm_workspace_size", "hgemm_trsm_noalloc", "hgemm_layout", "HGEMM_TRMM_MAX_N", "HGEMM_TRSM_NOALLOC_MAX_BYTES",
     "HGEMM_A_ROW_MAJOR", "HGEMM_A_COL_MAJOR", "HGEMM_B_COL_MAJOR", "HGEMM_B_ROW_MAJOR",
     "HGEMM_INJECT_NONE", "HGEMM_INJECT_DROP_ARRIVAL", "matmul",
 ]
@@ -131,6 +131,8 @@ def load():
     lib.hgemm_debug_inject.restype = i32
     lib.hgemm_force_split.argtypes = [i32, i32]
     lib.hgemm_force_split.restype = i32
+    lib.hgemm_launch_floor.argtypes = [i32, vp]
+    lib.hgemm_launch_floor.restype = i32
     _lib = lib
     return lib
 
@@ -296,6 +298,12 @@ def hgemm_device_status(stream=None) -> int:
     if st in (HGEMM_OK, HGEMM_ERR_TIMEOUT):
         return st
     raise HgemmError(st, "hgemm_device_status")
+
+
+def hgemm_launch_floor(pair_config: bool = True, stream=None) -> None:
+    """Enqueues a kernel that does nothing (the pair kernel's launch
+    configuration when pair_config), to time the fixed cost of a launch."""
+    _raise_on(load().hgemm_launch_floor(1 if pair_config else 0, _stream(stream)), "hgemm_launch_floor")
 
 
 def hgemm_last_cuda_error() -> int:

@@ -1232,6 +1232,14 @@ int hgemm_device_status(cudaStream_t stream) {
   return HGEMM_OK;
 }
 
+int hgemm_launch_floor(int pair_config, cudaStream_t stream) {
+  DeviceState* dev = nullptr;
+  int rc = current_device(&dev);
+  if (rc != HGEMM_OK) return rc;
+  const cudaError_t e = hg::launch_floor(pair_config, dev->num_sms, hg::pair_smem_bytes(), stream);
+  return e == cudaSuccess ? HGEMM_OK : cuda_fail(e);
+}
+
 int hgemm_set_wait_timeout(unsigned long long ns) {
   g_timeout_ns.store(ns ? ns : kDefaultTimeoutNs);
   return HGEMM_OK;

@@ -306,6 +306,12 @@ __global__ void empty_sum_kernel(uint16_t* __restrict__ C, int64_t M, int64_t N,
   }
 }
 
+// Kernels that do nothing, for measuring the fixed cost of a launch: the
+// second one with the launch configuration of the pair kernel (clusters of
+// two CTAs of 192 threads, its dynamic shared memory).
+__global__ void floor_kernel() {}
+__global__ void __cluster_dims__(2, 1, 1) floor_pair_kernel() {}
+
 template <typename Kern>
 cudaError_t ensure_smem_attr(Kern kern, int bytes, std::atomic<bool>* done_per_device) {
   int dev = 0;
@@ -329,6 +335,18 @@ cudaError_t launch_tc_128x256(const CUtensorMap& a, const CUtensorMap& b, const 
   if (e != cudaSuccess) return e;
   PdlLaunch l(dim3(static_cast<unsigned>(args.grid)), dim3(Cfg::THREADS), Cfg::SMEM_BYTES, stream);
   return cudaLaunchKernelEx(&l.cfg, kern, a, b, c, args);
+}
+
+cudaError_t launch_floor(int pair_config, int num_sms, int smem_bytes, cudaStream_t stream) {
+  if (!pair_config) {
+    PdlLaunch l(dim3(1), dim3(32), 0, stream);
+    return cudaLaunchKernelEx(&l.cfg, floor_kernel);
+  }
+  static std::atomic<bool> attr_done[64];
+  cudaError_t e = ensure_smem_attr(floor_pair_kernel, smem_bytes, attr_done);
+  if (e != cudaSuccess) return e;
+  PdlLaunch l(dim3(static_cast<unsigned>(num_sms & ~1)), dim3(192), static_cast<size_t>(smem_bytes), stream);
+  return cudaLaunchKernelEx(&l.cfg, floor_pair_kernel);
 }
 
 cudaError_t launch_empty_sum(uint16_t* C, int64_t M, int64_t N, int64_t ldc, const EpiArgs& epi,

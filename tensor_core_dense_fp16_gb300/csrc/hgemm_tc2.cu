@@ -450,6 +450,8 @@ int pair_max_clusters(int num_sms) {
   return n;
 }
 
+int pair_smem_bytes() { return PairCfg<kPairStages>::SMEM_BYTES; }
+
 cudaError_t launch_tc_pair(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b_part,
                            const CUtensorMap& c, const TcArgs& args, cudaStream_t stream) {
   using Cfg = PairCfg<kPairStages, 4>;

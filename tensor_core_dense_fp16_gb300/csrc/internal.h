@@ -129,6 +129,11 @@ int skinny_max_clusters(int split, int tile_n, int num_sms);
 cudaError_t launch_empty_sum(uint16_t* C, int64_t M, int64_t N, int64_t ldc, const EpiArgs& epi,
                              cudaStream_t stream);
 cudaError_t launch_generic(const PlainArgs& args, int num_sms, cudaStream_t stream);
+// A kernel that does nothing: one CTA of one warp, or (pair_config) one CTA
+// per SM in clusters of two with `smem_bytes` of dynamic shared memory each.
+cudaError_t launch_floor(int pair_config, int num_sms, int smem_bytes, cudaStream_t stream);
+// Dynamic shared memory of one pair-kernel CTA.
+int pair_smem_bytes();
 // Every leaf b: C + off = (A operand + off) · lower(B operand at (off, off)),
 // M × size (see hgemm_generic.cu).
 cudaError_t launch_tri_leaves(const PlainArgs& args, const TriLeaves& leaves, int num_sms,

@@ -452,3 +452,61 @@ def test_trsm_inverts_trmm_and_ignores_the_upper_triangle():
     c = oracle.trmm(a, b)
     back = oracle.trsm(a, c).astype(np.float64)
     assert np.allclose(back, b.astype(np.float64), rtol=1e-2, atol=1e-2)
+
+
+# ---- the solve in the page's literal orientation, A·X = alpha·B (forward substitution)
+
+def test_trsm_n_against_scipy_and_residual():
+    import scipy.linalg
+    rng = np.random.default_rng(61)
+    n, m = 90, 21
+    a = well_conditioned_lower(rng, n)
+    b = rng.uniform(0, 1, size=(n, m)).astype(np.float16)
+    x = oracle.trsm_n(a, b, alpha=1.5)
+    lower = np.tril(a.astype(np.float64))
+    ref = scipy.linalg.solve_triangular(lower, 1.5 * b.astype(np.float64), lower=True)
+    # one rounding of the exact FP64 solution
+    assert np.array_equal(bits(x), bits(ref.astype(np.float16)))
+    resid = lower @ x.astype(np.float64) - 1.5 * b.astype(np.float64)
+    assert np.max(np.abs(resid)) < 4 * 2.0 ** -11 * np.max(np.abs(1.5 * b.astype(np.float64))) + 1e-3
+    # not the transposed system: a wrong orientation fails the residual
+    wrong = oracle.trsm(a, b, alpha=1.5).astype(np.float64)
+    assert np.max(np.abs(lower @ wrong - 1.5 * b.astype(np.float64))) > 1e-2
+
+
+def test_trsm_n_bruteforce_exact_rationals():
+    rng = np.random.default_rng(62)
+    for n, m in [(1, 1), (2, 2), (4, 3), (6, 2)]:
+        a = well_conditioned_lower(rng, n)
+        b = random_fp16(rng, (n, m))
+        got = bits(oracle.trsm_n(a, b, alpha=0.5))
+        for j in range(m):
+            x = [Fraction(0)] * n
+            for i in range(n):
+                s = Fraction(0.5) * Fraction(float(b[i, j]))
+                for k in range(i):
+                    s -= Fraction(float(a[i, k])) * x[k]
+                x[i] = s / Fraction(float(a[i, i]))
+            for i in range(n):
+                assert got[i, j] == fraction_to_fp16_bits(x[i]), (n, m, i, j)
+
+
+def test_trsm_n_special_cases_and_the_reversed_transposed_system():
+    rng = np.random.default_rng(63)
+    n, m = 48, 7
+    a = well_conditioned_lower(rng, n)
+    eye = np.eye(n, dtype=np.float16)
+    b = random_fp16(rng, (n, m))
+    assert np.array_equal(bits(oracle.trsm_n(eye, b, alpha=2.0)),
+                          bits((b.astype(np.float64) * 2).astype(np.float16)))
+    poisoned = a.copy()
+    poisoned[np.triu_indices(n, 1)] = np.nan
+    assert np.array_equal(bits(oracle.trsm_n(poisoned, b)), bits(oracle.trsm_n(a, b)))
+    # With J the order reversal, A·X = B is (J·Aᵀ·J)ᵀ·(J·X) = J·B, the
+    # transposed system of the lower triangle J·Aᵀ·J: the already-pinned
+    # transposed solve gives the same solution up to the summation order
+    # (within one FP16 step of each other).
+    rev = np.ascontiguousarray(a.T[::-1, ::-1])
+    other = oracle.trsm(rev, np.ascontiguousarray(b[::-1]))[::-1].astype(np.float64)
+    mine = oracle.trsm_n(a, b).astype(np.float64)
+    assert np.all(np.abs(mine - other) <= 2.0 ** -10 * np.maximum(np.abs(mine), 2.0 ** -14))

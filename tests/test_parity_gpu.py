@@ -511,3 +511,15 @@ def test_cuda_graph_capture_and_replay():
             assert np.array_equal(graph_out[k].cpu().numpy().view(np.uint16),
                                   eager[k].cpu().numpy().view(np.uint16)), k
     assert tc.hgemm_device_status() == tc.HGEMM_OK
+
+
+def test_launch_floor_kernel_runs():
+    """The measurement aid the benchmark times beside the small products:
+    an empty launch in either configuration completes and leaves the
+    watchdog word clear."""
+    torch = torch_cuda()
+    tc.load()
+    for pair in (False, True):
+        tc.hgemm_launch_floor(pair)
+    assert tc.hgemm_device_status() == tc.HGEMM_OK
+    torch.cuda.synchronize()
