@@ -58,6 +58,8 @@ def metric_for(name, spec):
         return f"TRMM TFLOP/s (n(n+1)m/t) at n={spec['n']}, m={spec['m']} fp16"
     if spec.get("op") == "trsm":
         return f"TRSM TFLOP/s (n^2 m/t) at n={spec['n']}, m={spec['m']} fp16"
+    if spec.get("op") == "trsm_n":
+        return f"TRSM (A X = B) TFLOP/s (n^2 m/t) at n={spec['n']}, m={spec['m']} fp16"
     return f"HGEMM TFLOP/s (2MNK/t) at {spec['M']}x{spec['N']}x{spec['K']} fp16"
 UNIT = "TFLOP/s"
 DEFAULT_WORKLOAD = "hgemm_8192"
@@ -82,6 +84,10 @@ DESCRIPTIONS = {
                  "below it uniform[0,1/n]), B 8192x8192 uniform[0,1], column-major fp16",
     "trsm_4096x256": "solve A^T X = B, A 4096x4096 lower triangular (diagonal uniform[1,2], "
                      "below it uniform[0,1/n]), B 4096x256 uniform[0,1], column-major fp16",
+    "trsm_n_8192": "solve A X = B, A 8192x8192 lower triangular (diagonal uniform[1,2], "
+                   "below it uniform[0,1/n]), B 8192x8192 uniform[0,1], column-major fp16",
+    "trsm_n_4096x256": "solve A X = B, A 4096x4096 lower triangular (diagonal uniform[1,2], "
+                       "below it uniform[0,1/n]), B 4096x256 uniform[0,1], column-major fp16",
 }
 
 
@@ -148,6 +154,10 @@ TRI_OPS = {
     "trsm": dict(call="hgemm_trsm", oracle="trsm", flops=trsm_flops, launches=trsm_launches,
                  kernel="scale_copy_kernel + trsm_inverse_kernel + hgemm_tc2_kernel (diagonal blocks by their "
                         "inverses, updates); without a workspace trsm_leaf_kernel for the diagonal blocks"),
+    "trsm_n": dict(call="hgemm_trsm_op", oracle="trsm_n", flops=trsm_flops, launches=trsm_launches,
+                   kernel="scale_copy_kernel + trsm_inverse_kernel + hgemm_tc2(w)_kernel (products by the "
+                          "inverses' transposes, updates with N-contiguous A21^T); without a workspace "
+                          "trsm_leaf_kernel (forward) for the diagonal blocks"),
 }
 
 
@@ -696,6 +706,12 @@ def run_tri_ours(args, spec, a_col, b_col, world, rank, local):
 
         def step():
             tc.hgemm_trsm_ws(da, n, db, n, dc, n, n, m, 1.0, work, None, stream)
+    elif op == "trsm_n":
+        work = (None if args.no_workspace else
+                torch.empty(tc.hgemm_trsm_workspace_size(n), dtype=torch.uint8, device=dev))
+
+        def step():
+            tc.hgemm_trsm_op(tc.HGEMM_OP_N, da, n, db, n, dc, n, n, m, 1.0, work, None, stream)
     else:
         def step():
             call(da, n, db, n, dc, n, n, m, 1.0, stream)
@@ -774,10 +790,13 @@ def run_tri_ours(args, spec, a_col, b_col, world, rank, local):
                        "n": n, "m": m, "seed": spec["seed"],
                        "l2": "flushed before every timed call (write of 2x L2 size, outside the events)",
                        "inputs": "resident in HBM",
-                       "path": "hgemm_trsm_ws" if op == "trsm" and not args.no_workspace else ops["call"],
+                       "path": ("hgemm_trsm_ws" if op == "trsm" and not args.no_workspace else
+                                "hgemm_trsm_op(N, workspace)" if op == "trsm_n" and not args.no_workspace else
+                                ops["call"]),
                        "parallelism": f"replicas x{world}"},
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": args.steps * ((ops["launches"](n, m, 512) + 1) if op == "trsm" and not args.no_workspace
+            "gpu_launches": args.steps * ((ops["launches"](n, m, 512) + 1)
+                                          if op in ("trsm", "trsm_n") and not args.no_workspace
                                           else ops["launches"](n, m)),
             "clocks": dict(clocks, kcycles_per_step=(median_ms * clocks["sm_mhz"]
                                                      if clocks.get("sm_mhz") else None)),

@@ -263,6 +263,38 @@ HGEMM_API int hgemm_trsm_ws(const hgemm_half_t *A, int64_t lda, const hgemm_half
                   void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * hgemm_trsm_op — the triangular solve in either orientation, with or
+ * without a workspace:
+ *
+ *     op = HGEMM_OP_N:  solve  A · X = alpha · B   (the page's literal reading
+ *                                                    of §2.3, X = A\B column by
+ *                                                    column)
+ *     op = HGEMM_OP_T:  solve  Aᵀ · X = alpha · B  (hgemm_trsm's system)
+ *
+ * Same operands as hgemm_trsm: A n×n lower triangular (only row ≥ column is
+ * used), B and X n×m, all column-major with pitches ≥ n; X = B with ldx = ldb
+ * solves in place; any other overlap is HGEMM_ERR_ALIAS. With op =
+ * HGEMM_OP_N the recursion (§2.1) runs the other way round: a block's first
+ * half is solved first, then the GEMM update X2 -= A21·X1 (hgemm_layout's
+ * N-contiguous second operand: row k of A21ᵀ is a piece of column k of A),
+ * then the second half; diagonal blocks of order ≤ 256 are solved by forward
+ * substitution with the right-hand sides spread over thread blocks, like
+ * hgemm_trsm's. workspace may be null (workspace_bytes then 0) to solve
+ * every diagonal block by substitution, as hgemm_trsm does; otherwise it is
+ * hgemm_trsm_ws's workspace (same size, alignment and rules) and the blocks
+ * of order ≤ 512 are solved through their inverses, the same inverses for
+ * both orientations (op = N multiplies X_bᵀ by L_b⁻ᵀ, op = T by L_b⁻¹).
+ * Storage, rounding and accuracy as hgemm_trsm and hgemm_trsm_ws. An op
+ * other than the two, or a null workspace with a nonzero size, is
+ * HGEMM_ERR_INVALID_ARG; otherwise the same return values as hgemm_trsm_ws.
+ */
+#define HGEMM_OP_N 0
+#define HGEMM_OP_T 1
+HGEMM_API int hgemm_trsm_op(int op, const hgemm_half_t *A, int64_t lda, const hgemm_half_t *B, int64_t ldb,
+                  hgemm_half_t *X, int64_t ldx, int64_t n, int64_t m, float alpha,
+                  void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * hgemm_trsm_noalloc — hgemm_trsm_ws for callers that cannot allocate device
  * memory: code whose device memory all belongs to another allocator (a
  * framework's caching pool, a fixed budget reserved up front) and which may

@@ -122,6 +122,9 @@ WORKLOADS = {
     # the solve on the same shapes (§4.2 times it at 8192×8192)
     "trsm_8192": dict(op="trsm", n=8192, m=8192, kind="dominant", seed=1007),
     "trsm_4096x256": dict(op="trsm", n=4096, m=256, kind="dominant", seed=1008),
+    # the same operands solved in the page's literal orientation, A·X = B
+    "trsm_n_8192": dict(op="trsm_n", n=8192, m=8192, kind="dominant", seed=1007),
+    "trsm_n_4096x256": dict(op="trsm_n", n=4096, m=256, kind="dominant", seed=1008),
 }
 
 
@@ -155,7 +158,7 @@ def workload(name: str):
     if spec.get("op") == "trmm":
         a, b = trmm_operands(spec["n"], spec["m"], spec["seed"], spec["kind"])
         return a, b, spec
-    if spec.get("op") == "trsm":
+    if spec.get("op") in ("trsm", "trsm_n"):
         a, b = trsm_operands(spec["n"], spec["m"], spec["seed"])
         return a, b, spec
     a, b = operands(spec["M"], spec["N"], spec["K"], spec["seed"], spec["kind"])

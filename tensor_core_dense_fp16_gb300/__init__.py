@@ -28,7 +28,7 @@ __all__ = [
     "HgemmError", "library_path", "load", "hgemm", "hgemm_host", "hgemm_select_path",
     "hgemm_force_path", "hgemm_device_status", "hgemm_last_cuda_error",
     "hgemm_status_string", "hgemm_version", "hgemm_set_wait_timeout", "hgemm_debug_inject",
-    "hgemm_force_split", "hgemm_launch_floor", "hgemm_ex", "hgemm_strided", "hgemm_trmm", "hgemm_trsm", "hgemm_trsm_ws", "hgemm_trsm_workspace_size", "hgemm_trsm_noalloc", "hgemm_layout", "HGEMM_TRMM_MAX_N", "HGEMM_TRSM_NOALLOC_MAX_BYTES",
+    "hgemm_force_split", "hgemm_launch_floor", "hgemm_ex", "hgemm_strided", "hgemm_trmm", "hgemm_trsm", "hgemm_trsm_ws", "hgemm_trsm_workspace_size", "hgemm_trsm_noalloc", "hgemm_trsm_op", "HGEMM_OP_N", "HGEMM_OP_T", "hgemm_layout", "HGEMM_TRMM_MAX_N", "HGEMM_TRSM_NOALLOC_MAX_BYTES",
     "HGEMM_A_ROW_MAJOR", "HGEMM_A_COL_MAJOR", "HGEMM_B_COL_MAJOR", "HGEMM_B_ROW_MAJOR",
     "HGEMM_INJECT_NONE", "HGEMM_INJECT_DROP_ARRIVAL", "matmul",
 ]
@@ -41,6 +41,8 @@ HGEMM_ERR_CUDA = -4
 HGEMM_ERR_TIMEOUT = -5
 HGEMM_TRMM_MAX_N = 16384
 HGEMM_TRSM_NOALLOC_MAX_BYTES = 8 << 20
+HGEMM_OP_N = 0
+HGEMM_OP_T = 1
 HGEMM_A_ROW_MAJOR = 0
 HGEMM_A_COL_MAJOR = 1
 HGEMM_B_COL_MAJOR = 0
@@ -106,6 +108,9 @@ def load():
     lib.hgemm_trsm_ws.restype = i32
     lib.hgemm_trsm_workspace_size.argtypes = [i64]
     lib.hgemm_trsm_workspace_size.restype = ctypes.c_size_t
+    lib.hgemm_trsm_op.argtypes = [i32, vp, i64, vp, i64, vp, i64, i64, i64, ctypes.c_float, vp,
+                                  ctypes.c_size_t, vp]
+    lib.hgemm_trsm_op.restype = i32
     lib.hgemm_trsm_noalloc.argtypes = [vp, i64, vp, i64, vp, i64, i64, i64, ctypes.c_float, vp]
     lib.hgemm_trsm_noalloc.restype = i32
     lib.hgemm_layout.argtypes = [i32, i32, vp, i64, vp, i64, vp, i64, i64, i64, i64, ctypes.c_float,
@@ -270,6 +275,18 @@ def hgemm_trsm_ws(A, lda: int, B, ldb: int, X, ldx: int, n: int, m: int, alpha: 
         workspace_bytes = workspace.numel() * workspace.element_size() if hasattr(workspace, "numel") else 0
     _raise_on(load().hgemm_trsm_ws(_ptr(A), lda, _ptr(B), ldb, _ptr(X), ldx, n, m, float(alpha),
                                    _ptr(workspace), int(workspace_bytes), _stream(stream)), "hgemm_trsm_ws")
+
+
+def hgemm_trsm_op(op: int, A, lda: int, B, ldb: int, X, ldx: int, n: int, m: int, alpha: float = 1.0,
+                  workspace=None, workspace_bytes: int | None = None, stream=None) -> None:
+    """Solves A·X = alpha·B (op = HGEMM_OP_N, the page's literal X = A\\B) or
+    Aᵀ·X = alpha·B (HGEMM_OP_T) for X, A lower triangular, column-major
+    operands; with an optional workspace as hgemm_trsm_ws takes (see hgemm.h)."""
+    if workspace_bytes is None:
+        workspace_bytes = (workspace.numel() * workspace.element_size() if hasattr(workspace, "numel")
+                           else 0)
+    _raise_on(load().hgemm_trsm_op(int(op), _ptr(A), lda, _ptr(B), ldb, _ptr(X), ldx, n, m, float(alpha),
+                                   _ptr(workspace), int(workspace_bytes), _stream(stream)), "hgemm_trsm_op")
 
 
 def hgemm_host(hA, hB, hC, M: int, N: int, K: int, dA, dB, dC, stream=None) -> None:

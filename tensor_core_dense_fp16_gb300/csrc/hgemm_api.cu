@@ -934,9 +934,9 @@ int hgemm_trmm(const hgemm_half_t* A, int64_t lda, const hgemm_half_t* B, int64_
 namespace {
 
 // The diagonal blocks of order ≤ leaf of the TRSM recursion in the order it
-// solves them (second half first); false when there are more than the table
-// holds.
-bool trsm_leaves(int64_t n, int64_t leaf, hg::TriLeaves* leaves) {
+// solves them (second half first; first half first when fwd); false when
+// there are more than the table holds.
+bool trsm_leaves(int64_t n, int64_t leaf, hg::TriLeaves* leaves, bool fwd = false) {
   leaves->count = 0;
   std::function<bool(int64_t, int64_t)> walk = [&](int64_t off, int64_t s) -> bool {
     if (s <= leaf) {
@@ -947,7 +947,7 @@ bool trsm_leaves(int64_t n, int64_t leaf, hg::TriLeaves* leaves) {
       return true;
     }
     const int64_t s1 = ((s / 2 + 63) / 64) * 64;
-    return walk(off + s1, s - s1) && walk(off, s1);
+    return fwd ? (walk(off, s1) && walk(off + s1, s - s1)) : (walk(off + s1, s - s1) && walk(off, s1));
   };
   return n > 0 && walk(0, n);
 }
@@ -955,10 +955,12 @@ bool trsm_leaves(int64_t n, int64_t leaf, hg::TriLeaves* leaves) {
 // one inverse in the workspace: FP16, kTrsmInverseLeaf² (512 KiB)
 constexpr uint64_t kTrsmInverseBytes = 2ull * hg::kTrsmInverseLeaf * hg::kTrsmInverseLeaf;
 
-// hgemm_trsm and hgemm_trsm_ws: W (may be null) holds room for the inverses
-// of the diagonal blocks.
+// hgemm_trsm, hgemm_trsm_ws and hgemm_trsm_op: W (may be null) holds room
+// for the inverses of the diagonal blocks. fwd: the literal orientation
+// A·X = alpha·B (forward); otherwise Aᵀ·X = alpha·B.
 int trsm_impl(const hgemm_half_t* A, int64_t lda, const hgemm_half_t* B, int64_t ldb, hgemm_half_t* X,
-              int64_t ldx, int64_t n, int64_t m, float alpha, uint16_t* W, uint64_t w_bytes, cudaStream_t stream) {
+              int64_t ldx, int64_t n, int64_t m, float alpha, uint16_t* W, uint64_t w_bytes, cudaStream_t stream,
+              bool fwd = false) {
   if (n < 0 || m < 0 || n > HGEMM_MAX_DIM || m > HGEMM_MAX_DIM) return HGEMM_ERR_INVALID_ARG;
   if (n == 0 || m == 0) return HGEMM_OK;
   const int64_t ld_lim = int64_t(1) << 40;
@@ -980,7 +982,7 @@ int trsm_impl(const hgemm_half_t* A, int64_t lda, const hgemm_half_t* B, int64_t
     return HGEMM_ERR_ALIAS;
   hg::TriLeaves leaves{};
   if (W) {
-    if (!trsm_leaves(n, hg::kTrsmInverseLeaf, &leaves) ||
+    if (!trsm_leaves(n, hg::kTrsmInverseLeaf, &leaves, fwd) ||
         w_bytes < kTrsmInverseBytes * static_cast<uint64_t>(leaves.count) ||
         (reinterpret_cast<uintptr_t>(W) & 15u))
       return HGEMM_ERR_INVALID_ARG;
@@ -1023,9 +1025,13 @@ int trsm_impl(const hgemm_half_t* A, int64_t lda, const hgemm_half_t* B, int64_t
   // product reads columns [off+s1, off+s) of X and writes [off, off+s1):
   // the element sets are disjoint, so the span check of validate(), which
   // sees the interleaved columns as an overlap, is not applied.
+  // Forward (A·X = B): X2ᵀ (m × s2) -= X1ᵀ (m × s1) · A21ᵀ (s1 × s2), where
+  // row k of A21ᵀ is A[off+s1 : off+s, off+k], contiguous (an N-contiguous
+  // second operand, pitch lda); it reads [off, off+s1) and writes
+  // [off+s1, off+s).
   const hg::EpiArgs subtract{-1.0f, 1.0f, nullptr, 0, 2};
   // The page's recursion, second half first: every row of a block depends on
-  // the rows below it.
+  // the rows below it (forward: first half first, on the rows above).
   // inverse: the block's inverse is in the workspace (a block of the
   // inverse-product recursion); otherwise the blocks of order ≤ kTrsmLeaf
   // are solved by substitution.
@@ -1039,9 +1045,11 @@ int trsm_impl(const hgemm_half_t* A, int64_t lda, const hgemm_half_t* B, int64_t
         // kernel's, or the pair kernel's for s ≤ 256, never cut into column
         // parts) reads every column it writes and no other tile reads them,
         // so the product runs in place.
+        // forward: X_bᵀ := X_bᵀ · L⁻ᵀ, whose column j is row j of L⁻¹: the
+        // same workspace read as a K-contiguous second operand
         Gemm g{x + off, W + static_cast<int64_t>(b) * hg::kTrsmInverseLeaf * hg::kTrsmInverseLeaf, x + off, m,
                s, s, ldx, hg::kTrsmInverseLeaf, ldx};
-        g.b_mn = true;
+        g.b_mn = !fwd;
         chained = true;
         return s > hg::kPairBN ? run_tc_wide(g, kPlainEpilogue, *dev, stream)
                                : run_tc_pair(g, kPlainEpilogue, *dev, stream, nullptr, true);
@@ -1051,11 +1059,19 @@ int trsm_impl(const hgemm_half_t* A, int64_t lda, const hgemm_half_t* B, int64_t
     }
     if (s <= hg::kTrsmLeaf) {
       const cudaError_t le = hg::launch_trsm_leaf(a, lda, x, ldx, off, static_cast<int>(s), m,
-                                                  dev->num_sms, chained, stream);
+                                                  dev->num_sms, chained, fwd, stream);
       chained = true;
       return le == cudaSuccess ? HGEMM_OK : cuda_fail(le);
     }
     const int64_t s1 = ((s / 2 + 63) / 64) * 64, s2 = s - s1;
+    if (fwd) {
+      int r = solve(off, s1, inverse);
+      if (r != HGEMM_OK) return r;
+      Gemm g{x + off, a + off * lda + off + s1, x + off + s1, m, s2, s1, ldx, lda, ldx};
+      g.b_mn = true;
+      if ((r = dispatch(g, subtract, *dev, stream)) != HGEMM_OK) return r;
+      return solve(off + s1, s2, inverse);
+    }
     int r = solve(off + s1, s2, inverse);
     if (r != HGEMM_OK) return r;
     const Gemm g{x + off + s1, a + off * lda + off + s1, x + off, m, s1, s2, ldx, lda, ldx};
@@ -1085,6 +1101,15 @@ int hgemm_trsm_ws(const hgemm_half_t* A, int64_t lda, const hgemm_half_t* B, int
   if (!workspace) return HGEMM_ERR_INVALID_ARG;
   return trsm_impl(A, lda, B, ldb, X, ldx, n, m, alpha, static_cast<uint16_t*>(workspace), workspace_bytes,
                    stream);
+}
+
+int hgemm_trsm_op(int op, const hgemm_half_t* A, int64_t lda, const hgemm_half_t* B, int64_t ldb,
+                  hgemm_half_t* X, int64_t ldx, int64_t n, int64_t m, float alpha, void* workspace,
+                  size_t workspace_bytes, cudaStream_t stream) {
+  if (op != HGEMM_OP_N && op != HGEMM_OP_T) return HGEMM_ERR_INVALID_ARG;
+  if (!workspace && workspace_bytes != 0) return HGEMM_ERR_INVALID_ARG;
+  return trsm_impl(A, lda, B, ldb, X, ldx, n, m, alpha, static_cast<uint16_t*>(workspace), workspace_bytes,
+                   stream, op == HGEMM_OP_N);
 }
 
 // ---------------------------------------------------------------------------

@@ -30,6 +30,17 @@
 // X; FP32 accumulators holding the right-hand sides). The solution is
 // rounded once to FP16.
 //
+// The page's literal orientation (FWD, §2.3: X = A\B): A·X = alpha·B with
+// the same lower A, untransposed. Row i is Σ_{k ≤ i} A(i,k)·x_k = b_i, so
+// the block is solved by forward substitution: the groups go first to last,
+// each applied through the inverse of its diagonal triangle (warp g computes
+// the rows of L_g⁻¹ by back substitution on the columns of L_g, so that
+// x_g = L_g⁻¹·b_g is the same small product), and the warps below the group
+// subtract Σ_c A(r,c)·x_c: A(r0 .. r0+31, c) is contiguous for each of the
+// group's columns c, so each warp stages its own rows of the group's 32
+// columns (k-major, a group ahead) and reads them back transposed with
+// ldmatrix.trans as the same m16k16 fragments.
+//
 // Launch overlap: the inverses only read A, which no launch of the solve
 // writes, so they are computed before the kernel waits for the previous
 // launch on the stream (griddepcontrol.wait) and read X.
@@ -68,12 +79,29 @@ constexpr int leaf_smem() {
   return (LEAF / kGroup) * kGroup * kGroup * 4 + 2 * kGroup * pub_pitch<COLS>() * 4 + COLS * KP * 2 +
          2 * LEAF * AP * 2;
 }
+// Halves per k-row of the forward solve's staged columns: the block's rows
+// plus 8 of padding (the 8 k-rows of an ldmatrix load land in different banks).
+template <int LEAF>
+constexpr int fwd_pitch() {
+  return LEAF + 8;
+}
+static_assert(2 * kGroup * fwd_pitch<kLeafMax>() <= 2 * kLeafMax * AP, "the forward stage fits in the same space");
 
 // The m16k16 A fragment of mma.sync from a row-major 16×16 FP16 tile in
 // shared memory: lane l gives the address of row (l % 8) + 8·((l / 8) % 2),
 // columns 8·(l / 16) .. +7.
 __device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t addr) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+
+// The same fragment from a 16×16 tile stored transposed (k-major: 16 rows of
+// k, each 16 contiguous row values): lane l gives the address of k-row
+// (l % 8) + 8·(l / 16), row values 8·((l / 8) % 2) .. +7.
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                : "r"(addr)
                : "memory");
@@ -120,7 +148,9 @@ __device__ __forceinline__ float col32_at(const uint4 (&v)[4], int q) {
 // identity: the right-hand sides are the columns of the identity (X is not
 // read), so the block computes columns j0.. of the inverse of the block's
 // transpose.
-template <int COLS, int LEAF>
+// FWD: the literal orientation A·X = B (forward substitution); otherwise
+// Aᵀ·X = B (back substitution).
+template <int COLS, int LEAF, bool FWD = false>
 __device__ __forceinline__ void trsm_leaf_body(const uint16_t* __restrict__ A, int64_t lda,
                                                uint16_t* __restrict__ X, int64_t ldx, int64_t off,
                                                int64_t xoff, int s, int64_t m, int chained, bool identity,
@@ -161,22 +191,39 @@ __device__ __forceinline__ void trsm_leaf_body(const uint16_t* __restrict__ A, i
     __syncwarp();
     const float rd_own = lane < sg ? 1.0f / blk[lane * kGroup + lane] : 0.f;
     float mcol[kGroup];
+    if constexpr (!FWD) {
 #pragma unroll
-    for (int k = 0; k < kGroup; ++k) {
-      const float4* rowv = reinterpret_cast<const float4*>(blk + k * kGroup);
-      const float rd = __shfl_sync(0xffffffffu, rd_own, k);
-      float acc = (k == lane) ? 1.0f : 0.0f;
+      for (int k = 0; k < kGroup; ++k) {
+        const float4* rowv = reinterpret_cast<const float4*>(blk + k * kGroup);
+        const float rd = __shfl_sync(0xffffffffu, rd_own, k);
+        float acc = (k == lane) ? 1.0f : 0.0f;
 #pragma unroll
-      for (int j4 = 0; j4 < (k + 3) / 4; ++j4) {
-        const float4 l = rowv[j4];
-        if (4 * j4 + 0 < k) acc = fmaf(-l.x, mcol[4 * j4 + 0], acc);
-        if (4 * j4 + 1 < k) acc = fmaf(-l.y, mcol[4 * j4 + 1], acc);
-        if (4 * j4 + 2 < k) acc = fmaf(-l.z, mcol[4 * j4 + 2], acc);
-        if (4 * j4 + 3 < k) acc = fmaf(-l.w, mcol[4 * j4 + 3], acc);
+        for (int j4 = 0; j4 < (k + 3) / 4; ++j4) {
+          const float4 l = rowv[j4];
+          if (4 * j4 + 0 < k) acc = fmaf(-l.x, mcol[4 * j4 + 0], acc);
+          if (4 * j4 + 1 < k) acc = fmaf(-l.y, mcol[4 * j4 + 1], acc);
+          if (4 * j4 + 2 < k) acc = fmaf(-l.z, mcol[4 * j4 + 2], acc);
+          if (4 * j4 + 3 < k) acc = fmaf(-l.w, mcol[4 * j4 + 3], acc);
+        }
+        mcol[k] = (k < sg && k >= lane) ? acc * rd : 0.f;
       }
-      mcol[k] = (k < sg && k >= lane) ? acc * rd : 0.f;
+    } else {
+      // row `lane` of L_g⁻¹: y with L_gᵀ·y = e_lane, by back substitution on
+      // the columns of L_g (every lane reads the same entry: a broadcast);
+      // its entries past the lane's own index are zero
+#pragma unroll
+      for (int k = kGroup - 1; k >= 0; --k) {
+        const float rd = __shfl_sync(0xffffffffu, rd_own, k);
+        float acc = (k == lane) ? 1.0f : 0.0f;
+#pragma unroll
+        for (int j = k + 1; j < kGroup; ++j) acc = fmaf(-blk[j * kGroup + k], mcol[j], acc);
+        mcol[k] = (k < sg && k <= lane) ? acc * rd : 0.f;
+      }
     }
     __syncwarp();
+    // L_g⁻¹ in place: (transposed) blk[k][i] = L_g⁻¹(k, i), column `lane`;
+    // (forward) blk[k][i] = L_g⁻¹(i, k), row `lane`. Either way step (2)
+    // below reads blk[k][lane].
 #pragma unroll
     for (int k = 0; k < kGroup; ++k) blk[k * kGroup + lane] = lane < sg ? mcol[k] : 0.f;
   }
@@ -215,9 +262,36 @@ __device__ __forceinline__ void trsm_leaf_body(const uint16_t* __restrict__ A, i
   // A's column segments staged by asynchronous 16-byte copies, a group ahead:
   // A 16-byte aligned and lda a multiple of 8
   const bool staged = ((reinterpret_cast<uintptr_t>(A) & 15u) == 0) && (lda % 8) == 0;
+  // warps that take group g's update: above it (transposed), or below it
+  // among the block's warps (forward)
+  auto updates = [&](int w, int g) { return FWD ? (w > g && w < groups) : (w < g); };
+  constexpr int FPITCH = fwd_pitch<LEAF>();
+  // forward: warp w's rows of group g's columns, A(off+32w .. +31, off+32g+k)
+  // for k < 32 (each contiguous), k-major into buffer g % 2, zero past the
+  // block's order (rows and columns)
+  auto stage_fwd = [&](int g) {
+    if (!updates(warp, g)) return;
+    const int c0 = g * kGroup, sg = min(kGroup, s - c0);
+    uint16_t* buf = a_stage + (g & 1) * kGroup * FPITCH;
+#pragma unroll
+    for (int i = lane; i < kGroup * 4; i += 32) {
+      const int k = i >> 2, row = warp * kGroup + 8 * (i & 3);
+      int valid = s - row;
+      valid = valid < 0 ? 0 : (valid > 8 ? 8 : valid);
+      uint16_t* dst = buf + k * FPITCH + row;
+      if (k < sg && valid > 0)
+        cp_async_16(smem_u32(dst), A + (off + c0 + k) * lda + off + row, 2 * valid);
+      else
+        *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+    }
+  };
   // thread r's segment of group g: A(off+32g .. +31, off+r), zero past the
   // block's order, into buffer g % 2 (rows of warps above group g only)
   auto stage_group = [&](int g) {
+    if constexpr (FWD) {
+      stage_fwd(g);
+      return;
+    }
     if (warp >= g) return;
     const int c0 = g * kGroup, sg = min(kGroup, s - c0);
     const uint16_t* src = A + (off + r) * lda + off + c0;
@@ -232,37 +306,47 @@ __device__ __forceinline__ void trsm_leaf_body(const uint16_t* __restrict__ A, i
         *reinterpret_cast<uint4*>(dst + 8 * q) = make_uint4(0u, 0u, 0u, 0u);
     }
   };
-  if (staged) stage_group(groups - 1);
+  if (staged) stage_group(FWD ? 0 : groups - 1);
   cp_async_commit();
 
-  for (int g = groups - 1; g >= 0; --g) {
+  for (int gi = 0; gi < groups; ++gi) {
+    const int g = FWD ? gi : groups - 1 - gi;  // forward: first group first; else last first
     const int c0 = g * kGroup, sg = min(kGroup, s - c0);
     // A's values for this warp's update, loaded now to land while the group
     // is solved: af[mt][ks] is the m16k16 fragment of rows 16·mt.. of the
     // warp and the group's rows 16·ks.., i.e. A(c0 + k, r) (contiguous in k)
     uint32_t af[2][2][4] = {};
     // one copy group per step: the next group's segments
-    if (staged && g >= 1) {
+    const int gn = FWD ? g + 1 : g - 1;
+    if (staged && gn >= 0 && gn < groups) {
       __syncwarp();  // this warp's reads of the buffer (two groups ago) are done
-      stage_group(g - 1);
+      stage_group(gn);
     }
     cp_async_commit();
-    if (!staged && warp < g) {
+    if (!staged && updates(warp, g)) {
 #pragma unroll
       for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
         for (int ks = 0; ks < 2; ++ks)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const int64_t r = off + warp * kGroup + 16 * mt + gid + ((e & 1) ? 8 : 0);
+            const int rr = warp * kGroup + 16 * mt + gid + ((e & 1) ? 8 : 0);  // row in the block
             const int k = 16 * ks + 2 * tig + ((e & 2) ? 8 : 0);
-            const uint16_t* src = A + r * lda + off + c0 + k;
-            if (pairs && k + 1 < sg) {
-              af[mt][ks][e] = __ldg(reinterpret_cast<const unsigned int*>(src));
-            } else {
-              const uint32_t lo = k < sg ? src[0] : 0u;
-              const uint32_t hi = k + 1 < sg ? src[1] : 0u;
+            if constexpr (FWD) {
+              // A(off + rr, off + c0 + k) and the next column: lda apart
+              const uint16_t* src = A + (off + c0 + k) * lda + off + rr;
+              const uint32_t lo = (k < sg && rr < s) ? src[0] : 0u;
+              const uint32_t hi = (k + 1 < sg && rr < s) ? src[lda] : 0u;
               af[mt][ks][e] = lo | (hi << 16);
+            } else {
+              const uint16_t* src = A + (off + rr) * lda + off + c0 + k;
+              if (pairs && k + 1 < sg) {
+                af[mt][ks][e] = __ldg(reinterpret_cast<const unsigned int*>(src));
+              } else {
+                const uint32_t lo = k < sg ? src[0] : 0u;
+                const uint32_t hi = k + 1 < sg ? src[1] : 0u;
+                af[mt][ks][e] = lo | (hi << 16);
+              }
             }
           }
     }
@@ -318,19 +402,32 @@ __device__ __forceinline__ void trsm_leaf_body(const uint16_t* __restrict__ A, i
           c[mt][nt][2] = hi.x;
           c[mt][nt][3] = hi.y;
         }
-    } else if (warp < g) {
-      // (3) rows above the group: b += A_g · (-x_g) (A = 0 past the block's order)
+    } else if (updates(warp, g)) {
+      // (3) rows above (below, forward) the group: b += A_g · (-x_g) (A = 0
+      // past the block's order)
       if (staged) {
         cp_async_wait<1>();  // this group's segments (the next group's may be in flight)
         __syncwarp();
-        const uint16_t* base = a_stage + ((g & 1) * LEAF + warp * kGroup) * AP;
+        if constexpr (FWD) {
+          const uint16_t* base = a_stage + (g & 1) * kGroup * FPITCH + warp * kGroup;
 #pragma unroll
-        for (int mt = 0; mt < 2; ++mt)
+          for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-          for (int ks = 0; ks < 2; ++ks) {
-            const int row = 16 * mt + (lane & 7) + ((lane >> 3) & 1) * 8;
-            ldmatrix_x4(af[mt][ks], smem_u32(base + row * AP + 16 * ks + (lane >> 4) * 8));
-          }
+            for (int ks = 0; ks < 2; ++ks) {
+              const int k = 16 * ks + (lane & 7) + ((lane >> 4) << 3);
+              const int row = 16 * mt + ((lane >> 3) & 1) * 8;
+              ldmatrix_x4_trans(af[mt][ks], smem_u32(base + k * FPITCH + row));
+            }
+        } else {
+          const uint16_t* base = a_stage + ((g & 1) * LEAF + warp * kGroup) * AP;
+#pragma unroll
+          for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+            for (int ks = 0; ks < 2; ++ks) {
+              const int row = 16 * mt + (lane & 7) + ((lane >> 3) & 1) * 8;
+              ldmatrix_x4(af[mt][ks], smem_u32(base + row * AP + 16 * ks + (lane >> 4) * 8));
+            }
+        }
       }
 #pragma unroll
       for (int ks = 0; ks < 2; ++ks)
@@ -357,12 +454,12 @@ __device__ __forceinline__ void trsm_leaf_body(const uint16_t* __restrict__ A, i
       }
 }
 
-template <int COLS>
+template <int COLS, bool FWD>
 __global__ void __launch_bounds__(kLeafMax, 2)
     trsm_leaf_kernel(const uint16_t* __restrict__ A, int64_t lda, uint16_t* __restrict__ X,
                      int64_t ldx, int64_t off, int s, int64_t m, int chained) {
-  trsm_leaf_body<COLS, kLeafMax>(A, lda, X, ldx, off, off, s, m, chained, false,
-                                 static_cast<int64_t>(blockIdx.x) * COLS);
+  trsm_leaf_body<COLS, kLeafMax, FWD>(A, lda, X, ldx, off, off, s, m, chained, false,
+                                      static_cast<int64_t>(blockIdx.x) * COLS);
 }
 
 // The inverses of every diagonal block of a solve, in one launch: block
@@ -428,26 +525,32 @@ std::atomic<int> g_resident[kMaxDevices][3];
 
 template <int COLS>
 cudaError_t launch_width(const uint16_t* A, int64_t lda, uint16_t* X, int64_t ldx, int64_t off,
-                         int s, int64_t m, int threads, bool chained, cudaStream_t stream) {
+                         int s, int64_t m, int threads, bool chained, bool fwd, cudaStream_t stream) {
   const int64_t blocks = (m + COLS - 1) / COLS;
   if (blocks > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
   PdlLaunch l(dim3(static_cast<unsigned>(blocks)), dim3(threads), leaf_smem<COLS>(), stream);
-  return cudaLaunchKernelEx(&l.cfg, trsm_leaf_kernel<COLS>, A, lda, X, ldx, off, s, m, chained ? 1 : 0);
+  return fwd ? cudaLaunchKernelEx(&l.cfg, trsm_leaf_kernel<COLS, true>, A, lda, X, ldx, off, s, m, chained ? 1 : 0)
+             : cudaLaunchKernelEx(&l.cfg, trsm_leaf_kernel<COLS, false>, A, lda, X, ldx, off, s, m, chained ? 1 : 0);
 }
 
+// Sets both orientations' shared-memory size; the resident count is the same
+// for both (same size, same launch bounds).
 template <int COLS>
 cudaError_t resident_blocks(int* out) {
-  cudaError_t e = cudaFuncSetAttribute(trsm_leaf_kernel<COLS>,
+  cudaError_t e = cudaFuncSetAttribute(trsm_leaf_kernel<COLS, false>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, leaf_smem<COLS>());
   if (e != cudaSuccess) return e;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, trsm_leaf_kernel<COLS>, kLeafMax,
+  e = cudaFuncSetAttribute(trsm_leaf_kernel<COLS, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           leaf_smem<COLS>());
+  if (e != cudaSuccess) return e;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, trsm_leaf_kernel<COLS, false>, kLeafMax,
                                                        leaf_smem<COLS>());
 }
 
 }  // namespace
 
 cudaError_t launch_trsm_leaf(const uint16_t* A, int64_t lda, uint16_t* X, int64_t ldx, int64_t off,
-                             int s, int64_t m, int num_sms, bool chained, cudaStream_t stream) {
+                             int s, int64_t m, int num_sms, bool chained, bool fwd, cudaStream_t stream) {
   if (s < 1 || s > kLeafMax || m < 1 || num_sms < 1) return cudaErrorInvalidValue;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -482,11 +585,11 @@ cudaError_t launch_trsm_leaf(const uint16_t* A, int64_t lda, uint16_t* X, int64_
   const int threads = ((s + 31) / 32) * 32;
   switch (best) {
     case 0:
-      return launch_width<8>(A, lda, X, ldx, off, s, m, threads, chained, stream);
+      return launch_width<8>(A, lda, X, ldx, off, s, m, threads, chained, fwd, stream);
     case 1:
-      return launch_width<16>(A, lda, X, ldx, off, s, m, threads, chained, stream);
+      return launch_width<16>(A, lda, X, ldx, off, s, m, threads, chained, fwd, stream);
     default:
-      return launch_width<32>(A, lda, X, ldx, off, s, m, threads, chained, stream);
+      return launch_width<32>(A, lda, X, ldx, off, s, m, threads, chained, fwd, stream);
   }
 }
 

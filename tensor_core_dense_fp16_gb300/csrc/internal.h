@@ -169,8 +169,9 @@ cudaError_t launch_scale_copy(const uint16_t* B, int64_t ldb, uint16_t* X, int64
 constexpr int kTrsmInverseLeaf = 512;
 cudaError_t launch_trsm_inverse(const uint16_t* A, int64_t lda, uint16_t* W, const TriLeaves& leaves,
                                 cudaStream_t stream);
+// fwd: the literal orientation A·X = alpha·B (forward substitution).
 cudaError_t launch_trsm_leaf(const uint16_t* A, int64_t lda, uint16_t* X, int64_t ldx, int64_t off,
-                             int s, int64_t m, int num_sms, bool chained, cudaStream_t stream);
+                             int s, int64_t m, int num_sms, bool chained, bool fwd, cudaStream_t stream);
 
 // Address of the device watchdog word on the current device.
 cudaError_t status_word_address(int** addr);

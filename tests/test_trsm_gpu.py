@@ -28,10 +28,11 @@ def trsm_inputs(n, m, seed, c=1.0):
     return np.ascontiguousarray(a_col.T), np.ascontiguousarray(b_col.T)
 
 
-def run_trsm(a, b, alpha=1.0, pad=(0, 0, 0), poison_upper=False, in_place=False, ws=False):
+def run_trsm(a, b, alpha=1.0, pad=(0, 0, 0), poison_upper=False, in_place=False, ws=False, op=None):
     """Column-major device buffers with pitches n + pad; X (n, m) comes back.
     ws: through hgemm_trsm_ws, with a workspace of the reported size followed
-    by a sentinel band that must stay untouched."""
+    by a sentinel band that must stay untouched. op: through hgemm_trsm_op
+    with that orientation (with the workspace when ws)."""
     torch = torch_cuda()
     n, m = b.shape
     lda, ldb, ldx = n + pad[0], n + pad[1], n + pad[2]
@@ -53,7 +54,12 @@ def run_trsm(a, b, alpha=1.0, pad=(0, 0, 0), poison_upper=False, in_place=False,
         need = tc.hgemm_trsm_workspace_size(n)
         assert need > 0 and need % (2 * 512 * 512) == 0
         work = torch.full((need + 4096,), 0x5A, dtype=torch.uint8, device="cuda")
-        tc.hgemm_trsm_ws(da, lda, db, ldb, dx, ldx, n, m, alpha, work, need)
+        if op is None:
+            tc.hgemm_trsm_ws(da, lda, db, ldb, dx, ldx, n, m, alpha, work, need)
+        else:
+            tc.hgemm_trsm_op(op, da, lda, db, ldb, dx, ldx, n, m, alpha, work, need)
+    elif op is not None:
+        tc.hgemm_trsm_op(op, da, lda, db, ldb, dx, ldx, n, m, alpha, None, 0)
     else:
         tc.hgemm_trsm(da, lda, db, ldb, dx, ldx, n, m, alpha)
     assert tc.hgemm_device_status() == tc.HGEMM_OK
@@ -225,3 +231,113 @@ def test_trsm_workspace_arguments():
     with pytest.raises(tc.HgemmError) as err:
         tc.hgemm_trsm_ws(da, n, db, n, big, n, n, m, 1.0, big.data_ptr() + 2 * n * (m - 1), need)
     assert err.value.status == tc.HGEMM_ERR_ALIAS
+
+
+# ---- the page's literal orientation, A·X = alpha·B (hgemm_trsm_op with HGEMM_OP_N)
+# The diagonally dominant triangle is dominant by rows as well (a row of the
+# strict lower part sums to less than 1 <= the diagonal), so forward
+# substitution does not amplify errors either and the same tolerance applies.
+
+@pytest.mark.parametrize("ws", [False, True])
+@pytest.mark.parametrize("n,m", [(1, 1), (64, 32), (200, 7), (256, 100), (257, 64), (300, 136),
+                                 (512, 256), (1000, 128), (4096, 256)])
+def test_trsm_n_matches_oracle(n, m, ws):
+    """Forward substitution in the leaves (blocks of order 200, 257, 300 and
+    the last one of 1000 are not multiples of 32: a partial last group), the
+    updates X2 -= A21·X1 on N-contiguous second operands; with the workspace,
+    products by L_b⁻ᵀ."""
+    a, b = trsm_inputs(n, m, seed=2 * n + m)
+    ref = oracle.trsm_n(a, b, nthreads=oracle_threads())
+    assert_close(run_trsm(a, b, ws=ws, op=tc.HGEMM_OP_N), ref, what=f"trsm_n {n}x{m} ws={ws}")
+
+
+@pytest.mark.parametrize("ws", [False, True])
+@pytest.mark.parametrize("m", [4096, 8195])
+def test_trsm_n_leaf_widths(m, ws):
+    n = 300
+    a, b = trsm_inputs(n, m, seed=m + 7)
+    ref = oracle.trsm_n(a, b, nthreads=oracle_threads())
+    assert_close(run_trsm(a, b, ws=ws, op=tc.HGEMM_OP_N), ref, what=f"trsm_n {n}x{m} ws={ws}")
+
+
+@pytest.mark.parametrize("ws", [False, True])
+def test_trsm_n_reads_only_the_lower_triangle(ws):
+    n, m = 704, 96
+    a, b = trsm_inputs(n, m, seed=77)
+    ref = oracle.trsm_n(a, b, nthreads=oracle_threads())
+    assert_close(run_trsm(a, b, poison_upper=True, ws=ws, op=tc.HGEMM_OP_N), ref,
+                 what=f"trsm_n NaN above the diagonal ws={ws}")
+
+
+@pytest.mark.parametrize("ws", [False, True])
+@pytest.mark.parametrize("pad", [(8, 16, 8), (3, 5, 1)])
+def test_trsm_n_pitches_and_alpha(pad, ws):
+    """Odd pitches: the leaf kernel's direct loads of A's rows and the
+    generic kernel's gathered second operand."""
+    n, m = 600, 72
+    a, b = trsm_inputs(n, m, seed=13 + pad[0])
+    ref = oracle.trsm_n(a, b, alpha=-1.5, nthreads=oracle_threads())
+    assert_close(run_trsm(a, b, alpha=-1.5, pad=pad, ws=ws, op=tc.HGEMM_OP_N), ref,
+                 what=f"trsm_n pad {pad} ws={ws}")
+
+
+@pytest.mark.parametrize("ws", [False, True])
+def test_trsm_n_in_place(ws):
+    n, m = 800, 40
+    a, b = trsm_inputs(n, m, seed=29)
+    ref = oracle.trsm_n(a, b, alpha=0.25, nthreads=oracle_threads())
+    assert_close(run_trsm(a, b, alpha=0.25, pad=(0, 8, 0), in_place=True, ws=ws, op=tc.HGEMM_OP_N), ref,
+                 what=f"trsm_n in place ws={ws}")
+
+
+@pytest.mark.parametrize("ws", [False, True])
+def test_trsm_op_t_is_hgemm_trsm(ws):
+    """HGEMM_OP_T is the same solve as hgemm_trsm / hgemm_trsm_ws, bit for bit."""
+    n, m = 1000, 64
+    a, b = trsm_inputs(n, m, seed=31)
+    got = run_trsm(a, b, ws=ws, op=tc.HGEMM_OP_T)
+    assert np.array_equal(got.view(np.uint16), run_trsm(a, b, ws=ws).view(np.uint16))
+
+
+def test_trsm_n_is_not_the_transposed_solve():
+    """Both orientations of the same operands differ (a swapped orientation
+    would pass neither oracle comparison): A·X = B and Aᵀ·X = B."""
+    n, m = 512, 16
+    a, b = trsm_inputs(n, m, seed=37, c=64)
+    x_n = run_trsm(a, b, ws=True, op=tc.HGEMM_OP_N).astype(np.float64)
+    x_t = run_trsm(a, b, ws=True, op=tc.HGEMM_OP_T).astype(np.float64)
+    assert np.max(np.abs(x_n - x_t)) > 1e-2
+    low = np.tril(a.astype(np.float64))
+    assert np.max(np.abs(low @ x_n - b.astype(np.float64))) < 1e-2
+
+
+def test_trsm_op_arguments():
+    torch = torch_cuda()
+    n, m = 64, 8
+    a, b = trsm_inputs(n, m, seed=41)
+    da, db = to_device(np.ascontiguousarray(a.T)), to_device(np.ascontiguousarray(b.T))
+    dx = torch.empty((m, n), dtype=torch.float16, device="cuda")
+    with pytest.raises(tc.HgemmError) as err:
+        tc.hgemm_trsm_op(2, da, n, db, n, dx, n, n, m, 1.0, None, 0)
+    assert err.value.status == tc.HGEMM_ERR_INVALID_ARG
+    with pytest.raises(tc.HgemmError) as err:
+        tc.hgemm_trsm_op(tc.HGEMM_OP_N, da, n, db, n, dx, n, n, m, 1.0, None, 4096)
+    assert err.value.status == tc.HGEMM_ERR_INVALID_ARG
+
+
+def test_trsm_n_8192_sampled_columns():
+    """The 8192×8192 solve in the literal orientation with the workspace:
+    sampled columns of X against the oracle."""
+    torch = torch_cuda()
+    a_col, b_col, spec = synth.workload("trsm_8192")
+    n, m = spec["n"], spec["m"]
+    da, db = to_device(a_col), to_device(b_col)
+    dx = torch.empty((m, n), dtype=torch.float16, device="cuda")
+    work = torch.empty(tc.hgemm_trsm_workspace_size(n), dtype=torch.uint8, device="cuda")
+    tc.hgemm_trsm_op(tc.HGEMM_OP_N, da, n, db, n, dx, n, n, m, 1.0, work)
+    assert tc.hgemm_device_status() == tc.HGEMM_OK
+    torch.cuda.synchronize()
+    cols = np.array([0, 1, 63, 64, 255, 1000, 4097, 8000, m - 1])
+    got = dx[torch.from_numpy(cols).cuda()].cpu().numpy().T
+    ref = oracle.trsm_n(a_col.T, b_col[cols].T, nthreads=oracle_threads())
+    assert_close(got, ref, what="trsm_n 8192 sampled columns")
