@@ -227,7 +227,7 @@ def load_peaks():
 KERNEL_SOURCES = {"hgemm_tc_kernel": "hgemm_tc.cu", "hgemm_tc2_kernel": "hgemm_tc2.cu",
                   "hgemm_tc2w_kernel": "hgemm_tc2w.cu", "hgemm_skinny_kernel": "hgemm_skinny.cu",
                   "hgemm_generic_kernel": "hgemm_generic.cu"}
-SHARED_SOURCES = ["internal.h", "kernel_common.cuh", "ptx.cuh"]
+SHARED_SOURCES = ["internal.h", "kernel_common.cuh", "ptx.cuh", "debug.cuh"]
 
 
 def kernel_sources_sha(kernel):

@@ -64,6 +64,7 @@ typedef uint16_t hgemm_half_t; /* IEEE binary16 bit pattern */
 #define HGEMM_ERR_UNSUPPORTED_DEVICE (-3) /* current device is not compute capability 10.3 */
 #define HGEMM_ERR_CUDA (-4)               /* a CUDA runtime/driver call failed (see hgemm_last_cuda_error) */
 #define HGEMM_ERR_TIMEOUT (-5)            /* a kernel's bounded wait gave up (see hgemm_device_status) */
+#define HGEMM_ERR_DEBUG_CHECK (-6)        /* a device-side check of the -DHGEMM_DEBUG build failed */
 
 /* kernel paths, as reported by hgemm_select_path */
 #define HGEMM_PATH_NONE 0     /* M == 0 or N == 0: nothing to do */
@@ -397,7 +398,9 @@ HGEMM_API int hgemm_force_split(int split, int tile_n);
  * library's device watchdog word on the current device. Every wait inside the
  * kernels is bounded in time; a wait that gives up records itself there and
  * its kernel returns early, leaving C incomplete. Returns HGEMM_OK,
- * HGEMM_ERR_TIMEOUT, or HGEMM_ERR_CUDA if the synchronisation failed.
+ * HGEMM_ERR_TIMEOUT, HGEMM_ERR_DEBUG_CHECK (debug build: a device-side check
+ * failed; it outranks a timeout the skipped access caused), or
+ * HGEMM_ERR_CUDA if the synchronisation failed.
  */
 HGEMM_API int hgemm_device_status(cudaStream_t stream);
 
@@ -439,6 +442,29 @@ HGEMM_API int hgemm_last_cuda_error(void);
  * as hgemm (HGEMM_ERR_UNSUPPORTED_DEVICE, HGEMM_ERR_CUDA).
  */
 HGEMM_API int hgemm_launch_floor(int pair_config, cudaStream_t stream);
+
+/*
+ * The -DHGEMM_DEBUG build (tensor_core_dense_fp16_gb300/build.py --debug:
+ * _build/debug/libhgemm.so, loaded when HGEMM_LIBRARY_VARIANT=debug). Its
+ * kernels check every shared-memory address a barrier, TMA copy, bulk or
+ * asynchronous copy, or ldmatrix uses against the CTA's own shared memory,
+ * every TMA innermost coordinate for 16-byte alignment, every TMEM load
+ * against lanes 0..127 and columns 0..511, and the global indices and
+ * vector alignments of the kernels that address memory themselves. A failed
+ * check records a code and skips the access (no trap); hgemm_device_status
+ * then returns HGEMM_ERR_DEBUG_CHECK and clears it, and hgemm_debug_code
+ * returns the code (101 shared-memory range, 102 TMA coordinate, 103 TMEM
+ * range, 104 global index, 105 alignment). The release build has no checks.
+ *
+ * hgemm_debug_build — 1 in the debug build, 0 otherwise.
+ * hgemm_debug_code — the code behind this thread's last HGEMM_ERR_DEBUG_CHECK.
+ * hgemm_debug_selftest — host-only: evaluates the checks' predicates on
+ *   values inside and just outside their ranges; 0 when every case is
+ *   decided correctly, else a bit per wrong case. Needs no GPU.
+ */
+HGEMM_API int hgemm_debug_build(void);
+HGEMM_API int hgemm_debug_code(void);
+HGEMM_API int hgemm_debug_selftest(void);
 
 /* hgemm_status_string — static text for a status code; never NULL. */
 HGEMM_API const char *hgemm_status_string(int status);

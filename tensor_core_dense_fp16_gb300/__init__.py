@@ -22,7 +22,8 @@ import os
 
 __all__ = [
     "HGEMM_OK", "HGEMM_ERR_INVALID_ARG", "HGEMM_ERR_ALIAS", "HGEMM_ERR_UNSUPPORTED_DEVICE",
-    "HGEMM_ERR_CUDA", "HGEMM_ERR_TIMEOUT", "HGEMM_PATH_NONE", "HGEMM_PATH_ZERO",
+    "HGEMM_ERR_CUDA", "HGEMM_ERR_TIMEOUT", "HGEMM_ERR_DEBUG_CHECK", "hgemm_debug_build", "hgemm_debug_code",
+    "hgemm_debug_selftest", "HGEMM_PATH_NONE", "HGEMM_PATH_ZERO",
     "HGEMM_PATH_TC", "HGEMM_PATH_SKINNY", "HGEMM_PATH_GENERIC", "HGEMM_PATH_TC_PAIR",
     "HGEMM_PATH_TC_WIDE", "HGEMM_MAX_DIM",
     "HgemmError", "library_path", "load", "hgemm", "hgemm_host", "hgemm_select_path",
@@ -39,6 +40,7 @@ HGEMM_ERR_ALIAS = -2
 HGEMM_ERR_UNSUPPORTED_DEVICE = -3
 HGEMM_ERR_CUDA = -4
 HGEMM_ERR_TIMEOUT = -5
+HGEMM_ERR_DEBUG_CHECK = -6
 HGEMM_TRMM_MAX_N = 16384
 HGEMM_TRSM_NOALLOC_MAX_BYTES = 8 << 20
 HGEMM_OP_N = 0
@@ -62,7 +64,10 @@ HGEMM_INJECT_NONE = 0
 HGEMM_INJECT_DROP_ARRIVAL = 1
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_LIB_PATH = os.path.join(_HERE, "_build", "libhgemm.so")
+# HGEMM_LIBRARY_VARIANT=debug: the -DHGEMM_DEBUG build with device-side checks
+_LIB_PATH = (os.path.join(_HERE, "_build", "debug", "libhgemm.so")
+             if os.environ.get("HGEMM_LIBRARY_VARIANT") == "debug"
+             else os.path.join(_HERE, "_build", "libhgemm.so"))
 _lib = None
 
 
@@ -138,6 +143,9 @@ def load():
     lib.hgemm_force_split.restype = i32
     lib.hgemm_launch_floor.argtypes = [i32, vp]
     lib.hgemm_launch_floor.restype = i32
+    for name in ("hgemm_debug_build", "hgemm_debug_code", "hgemm_debug_selftest"):
+        getattr(lib, name).argtypes = []
+        getattr(lib, name).restype = i32
     _lib = lib
     return lib
 
@@ -310,11 +318,24 @@ def hgemm_force_path(path: int) -> None:
 
 
 def hgemm_device_status(stream=None) -> int:
-    """Synchronises `stream`; returns HGEMM_OK or HGEMM_ERR_TIMEOUT (raises otherwise)."""
+    """Synchronises `stream`; returns HGEMM_OK, HGEMM_ERR_TIMEOUT or (debug
+    build) HGEMM_ERR_DEBUG_CHECK; raises otherwise."""
     st = load().hgemm_device_status(_stream(stream))
-    if st in (HGEMM_OK, HGEMM_ERR_TIMEOUT):
+    if st in (HGEMM_OK, HGEMM_ERR_TIMEOUT, HGEMM_ERR_DEBUG_CHECK):
         return st
     raise HgemmError(st, "hgemm_device_status")
+
+
+def hgemm_debug_build() -> int:
+    return int(load().hgemm_debug_build())
+
+
+def hgemm_debug_code() -> int:
+    return int(load().hgemm_debug_code())
+
+
+def hgemm_debug_selftest() -> int:
+    return int(load().hgemm_debug_selftest())
 
 
 def hgemm_launch_floor(pair_config: bool = True, stream=None) -> None:

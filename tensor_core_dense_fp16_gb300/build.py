@@ -4,6 +4,11 @@ Each translation unit is compiled in parallel, then linked into
 ``tensor_core_dense_fp16_gb300/_build/libhgemm.so`` with the CUDA runtime
 linked statically (the library then loads on hosts without a GPU driver,
 and finds the driver lazily when first used).
+
+``build(debug=True)`` (``python -m tensor_core_dense_fp16_gb300.build --debug``)
+makes the checking variant ``_build/debug/libhgemm.so`` with -DHGEMM_DEBUG
+(device-side range and alignment checks, see csrc/debug.cuh); the binding
+loads it when HGEMM_LIBRARY_VARIANT=debug.
 """
 
 from __future__ import annotations
@@ -20,9 +25,11 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libhgemm.so")
+DEBUG_DIR = os.path.join(OUT_DIR, "debug")
+DEBUG_LIB = os.path.join(DEBUG_DIR, "libhgemm.so")
 SOURCES = ["hgemm_api.cu", "hgemm_tc.cu", "hgemm_tc2.cu", "hgemm_tc2w.cu", "hgemm_skinny.cu", "hgemm_generic.cu", "hgemm_trsm.cu",
            "hgemm_trileaf.cu"]
-HEADERS = ["ptx.cuh", "internal.h", "kernel_common.cuh"]
+HEADERS = ["ptx.cuh", "internal.h", "kernel_common.cuh", "debug.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
@@ -36,26 +43,30 @@ def _nvcc() -> str:
     raise RuntimeError("nvcc not found: the CUDA toolkit is required to build libhgemm.so")
 
 
-def _stale() -> bool:
-    if not os.path.exists(LIB):
+def _stale(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     deps = [os.path.join(CSRC, f) for f in SOURCES + HEADERS]
     deps.append(os.path.join(INCLUDE, "hgemm.h"))
     deps.append(os.path.abspath(__file__))
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compiles and links libhgemm.so if it is missing or out of date."""
-    if not force and not _stale():
-        return LIB
+def build(force: bool = False, verbose: bool = False, debug: bool = False) -> str:
+    """Compiles and links libhgemm.so (debug: the checking variant) if it is
+    missing or out of date."""
+    lib, out_dir = (DEBUG_LIB, DEBUG_DIR) if debug else (LIB, OUT_DIR)
+    if not force and not _stale(lib):
+        return lib
     nvcc = _nvcc()
-    os.makedirs(OUT_DIR, exist_ok=True)
+    os.makedirs(out_dir, exist_ok=True)
     extra = ["-Xptxas", "-v"] if verbose else []
+    if debug:
+        extra = extra + ["-DHGEMM_DEBUG"]
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(OUT_DIR, src.replace(".cu", ".o"))
+        obj = os.path.join(out_dir, src.replace(".cu", ".o"))
         cmd = [nvcc, *ARCH, *NVCC_FLAGS, *extra, "-I", INCLUDE, "-I", CSRC, "-c",
                os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -67,14 +78,14 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB + f".{os.getpid()}.tmp"
+    tmp = lib + f".{os.getpid()}.tmp"
     cmd = [nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, debug="--debug" in sys.argv))

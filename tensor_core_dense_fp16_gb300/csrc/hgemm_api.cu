@@ -21,6 +21,7 @@
 #include <cuda_runtime.h>
 
 #include "hgemm.h"
+#include "debug.cuh"
 #include "internal.h"
 
 namespace {
@@ -58,8 +59,23 @@ struct ContextCache {
   unsigned long long ctx = 0;  // cuCtxGetId of the context, 0: none cached
   int* status = nullptr;       // the watchdog word
   void* noalloc = nullptr;     // hgemm_trsm_noalloc's array (null: not yet looked up)
+  int* debug[hg::kDebugWords] = {};  // the debug build's check words (null in the release build)
 };
 thread_local ContextCache t_ctx;
+thread_local int t_debug_code = 0;  // the last check code hgemm_device_status read
+
+// The debug build's check words in the current context.
+cudaError_t debug_words(int* (&out)[hg::kDebugWords]) {
+  cudaError_t (*const get[hg::kDebugWords])(int**) = {hg::debug_word_tc,      hg::debug_word_tc2,
+                                                      hg::debug_word_tc2w,    hg::debug_word_skinny,
+                                                      hg::debug_word_generic, hg::debug_word_trsm,
+                                                      hg::debug_word_trileaf};
+  for (int i = 0; i < hg::kDebugWords; ++i) {
+    const cudaError_t e = get[i](&out[i]);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
 
 // Unique identity (for the life of the process) of the calling thread's
 // current context, or 0 when it cannot be determined.
@@ -167,7 +183,9 @@ int current_device(DeviceState** out) {
   if (ctx == 0 || ctx != t_ctx.ctx) {
     int* status = nullptr;
     if ((e = hg::status_word_address(&status)) != cudaSuccess) return cuda_fail(e);
-    t_ctx = ContextCache{ctx, status, nullptr};
+    ContextCache fresh{ctx, status, nullptr, {}};
+    if ((e = debug_words(fresh.debug)) != cudaSuccess) return cuda_fail(e);
+    t_ctx = fresh;
   }
   g_last_profile.store(&st.prof, std::memory_order_release);
   *out = &st;
@@ -1248,13 +1266,68 @@ int hgemm_device_status(cudaStream_t stream) {
   int word = 0;
   if ((e = cudaMemcpy(&word, t_ctx.status, sizeof(int), cudaMemcpyDeviceToHost)) != cudaSuccess)
     return cuda_fail(e);
+  const int zero = 0;
+  // the debug build's check words: a failed check outranks the timeout it
+  // may have caused (a skipped copy leaves a barrier short)
+  int check = 0;
+  for (int* w : t_ctx.debug) {
+    if (!w) continue;
+    int v = 0;
+    if ((e = cudaMemcpy(&v, w, sizeof(int), cudaMemcpyDeviceToHost)) != cudaSuccess) return cuda_fail(e);
+    if (v != 0) {
+      if (check == 0) check = v;
+      if ((e = cudaMemcpy(w, &zero, sizeof(int), cudaMemcpyHostToDevice)) != cudaSuccess) return cuda_fail(e);
+    }
+  }
   if (word != 0) {
-    const int zero = 0;
     if ((e = cudaMemcpy(t_ctx.status, &zero, sizeof(int), cudaMemcpyHostToDevice)) != cudaSuccess)
       return cuda_fail(e);
-    return HGEMM_ERR_TIMEOUT;
   }
-  return HGEMM_OK;
+  if (check != 0) {
+    t_debug_code = check;
+    return HGEMM_ERR_DEBUG_CHECK;
+  }
+  return word != 0 ? HGEMM_ERR_TIMEOUT : HGEMM_OK;
+}
+
+int hgemm_debug_code(void) { return t_debug_code; }
+
+int hgemm_debug_build(void) {
+#ifdef HGEMM_DEBUG
+  return 1;
+#else
+  return 0;
+#endif
+}
+
+int hgemm_debug_selftest(void) {
+  // The predicates of the device checks on values inside and just outside
+  // their ranges (never run on a GPU with bad values). Bit i set: case i wrong.
+  int bad = 0, i = 0;
+  auto expect = [&](bool got, bool want) {
+    if (got != want) bad |= 1 << i;
+    ++i;
+  };
+  expect(hg::dbg_range_ok(1024, 16, 1024, 4096), true);
+  expect(hg::dbg_range_ok(1024 + 4096 - 16, 16, 1024, 4096), true);
+  expect(hg::dbg_range_ok(1024 + 4096 - 8, 16, 1024, 4096), false);   // runs past the end
+  expect(hg::dbg_range_ok(1016, 16, 1024, 4096), false);              // starts in the reserved part
+  expect(hg::dbg_range_ok(0xFFFFFFF0u, 32, 1024, 4096), false);       // wraps around
+  expect(hg::dbg_range_ok(1024, 8192, 1024, 4096), false);            // larger than the window
+  expect(hg::dbg_tma_x_ok(64, 2), true);
+  expect(hg::dbg_tma_x_ok(8, 2), true);
+  expect(hg::dbg_tma_x_ok(4, 2), false);                              // 8 bytes: not a multiple of 16
+  expect(hg::dbg_tma_x_ok(-8, 2), true);                              // negative but aligned
+  expect(hg::dbg_tma_x_ok(-3, 2), false);
+  expect(hg::dbg_tmem_ok((127u << 16) | 480u, 32), true);
+  expect(hg::dbg_tmem_ok(481u, 32), false);                           // past column 511
+  expect(hg::dbg_tmem_ok(128u << 16, 32), false);                     // past lane 127
+  expect(hg::dbg_index_ok(0, 1), true);
+  expect(hg::dbg_index_ok(1, 1), false);
+  expect(hg::dbg_index_ok(-1, 5), false);
+  expect(hg::dbg_aligned(4096, 16), true);
+  expect(hg::dbg_aligned(4104, 16), false);
+  return bad;
 }
 
 int hgemm_launch_floor(int pair_config, cudaStream_t stream) {
@@ -1292,6 +1365,8 @@ const char* hgemm_status_string(int status) {
       return "a CUDA call failed (see hgemm_last_cuda_error)";
     case HGEMM_ERR_TIMEOUT:
       return "a kernel wait timed out; the output is incomplete";
+    case HGEMM_ERR_DEBUG_CHECK:
+      return "a device-side check of the debug build failed (see hgemm_debug_code); the output is incomplete";
     default:
       return "unknown status";
   }

@@ -298,6 +298,7 @@ __device__ __forceinline__ void generic_units(const PlainArgs& p, const TriLeave
         uint8_t* sb = smem + Cfg::OFF_B + stage * Cfg::B_BYTES;
         const int na = gi < u.q.M ? static_cast<int>(kn) : 0;
         const int nb = gj < u.q.N ? static_cast<int>(kn) : 0;
+        (void)HG_DBG_INDEX(k0 + kn - 1, u.q.K);
         if (u.q.a_mn)
           load_row_gather(u.q.A + k0 * u.q.lda + gi, u.q.lda, na, sa, r);
         else if (a_async)
@@ -410,6 +411,7 @@ __device__ __forceinline__ void generic_units(const PlainArgs& p, const TriLeave
             (c.epi.mode == 0 || (reinterpret_cast<uintptr_t>(bias) & 15u) == 0)) {
           // a whole, aligned 32-column piece of the row: four 16-byte stores
           const int64_t col0 = u.n0 + ch * 32;
+          if (!HG_DBG_INDEX(gi, c.M) || !HG_DBG_INDEX(col0 + 31, c.N) || !HG_DBG_ALIGN(dst, 16)) continue;
 #pragma unroll
           for (int w = 0; w < 4; ++w) {
             uint4 pk;
@@ -513,5 +515,8 @@ cudaError_t launch_generic(const PlainArgs& args, int num_sms, cudaStream_t stre
               stream);
   return cudaLaunchKernelEx(&l.cfg, hgemm_generic_kernel, args, tiles_m, tiles_n);
 }
+
+// The -DHGEMM_DEBUG build's check word of this file (null otherwise).
+HG_DEBUG_WORD_ACCESSOR(generic)
 
 }  // namespace hg

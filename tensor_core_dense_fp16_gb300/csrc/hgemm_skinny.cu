@@ -476,4 +476,7 @@ cudaError_t launch_skinny(int split, int tile_n, const CUtensorMap& a, const CUt
   }
 }
 
+// The -DHGEMM_DEBUG build's check word of this file (null otherwise).
+HG_DEBUG_WORD_ACCESSOR(skinny)
+
 }  // namespace hg

@@ -359,4 +359,7 @@ cudaError_t launch_empty_sum(uint16_t* C, int64_t M, int64_t N, int64_t ldc, con
   return cudaLaunchKernelEx(&l.cfg, empty_sum_kernel, C, M, N, ldc, epi);
 }
 
+// The -DHGEMM_DEBUG build's check word of this file (null otherwise).
+HG_DEBUG_WORD_ACCESSOR(tc)
+
 }  // namespace hg

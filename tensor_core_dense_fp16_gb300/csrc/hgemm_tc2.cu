@@ -474,4 +474,7 @@ cudaError_t launch_tc_pair(const CUtensorMap& a, const CUtensorMap& b, const CUt
   return cudaLaunchKernelEx(&l.cfg, kern, a, b, b_part, c, args);
 }
 
+// The -DHGEMM_DEBUG build's check word of this file (null otherwise).
+HG_DEBUG_WORD_ACCESSOR(tc2)
+
 }  // namespace hg

@@ -357,4 +357,7 @@ cudaError_t launch_tc_wide(const CUtensorMap& a, const CUtensorMap& b, const CUt
   return cudaLaunchKernelEx(&l.cfg, kern, a, b, c, args);
 }
 
+// The -DHGEMM_DEBUG build's check word of this file (null otherwise).
+HG_DEBUG_WORD_ACCESSOR(tc2w)
+
 }  // namespace hg

@@ -356,4 +356,7 @@ cudaError_t launch_tri_leaves_tc(const CUtensorMap& x, const CUtensorMap& l, con
   return cudaLaunchKernelEx(&pl.cfg, kern, x, l, c, args, leaves, ext);
 }
 
+// The -DHGEMM_DEBUG build's check word of this file (null otherwise).
+HG_DEBUG_WORD_ACCESSOR(trileaf)
+
 }  // namespace hg

@@ -91,6 +91,7 @@ static_assert(2 * kGroup * fwd_pitch<kLeafMax>() <= 2 * kLeafMax * AP, "the forw
 // shared memory: lane l gives the address of row (l % 8) + 8·((l / 8) % 2),
 // columns 8·(l / 16) .. +7.
 __device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t addr) {
+  if (!HG_DBG_SMEM(addr, 16)) return;
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                : "r"(addr)
@@ -101,6 +102,7 @@ __device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t addr) {
 // k, each 16 contiguous row values): lane l gives the address of k-row
 // (l % 8) + 8·(l / 16), row values 8·((l / 8) % 2) .. +7.
 __device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], uint32_t addr) {
+  if (!HG_DBG_SMEM(addr, 16)) return;
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                : "r"(addr)
@@ -279,6 +281,8 @@ __device__ __forceinline__ void trsm_leaf_body(const uint16_t* __restrict__ A, i
       int valid = s - row;
       valid = valid < 0 ? 0 : (valid > 8 ? 8 : valid);
       uint16_t* dst = buf + k * FPITCH + row;
+      // the group's columns and the warp's rows stay inside the block
+      if (valid > 0 && k < sg && (!HG_DBG_INDEX(c0 + k, s) || !HG_DBG_INDEX(row + valid - 1, s))) continue;
       if (k < sg && valid > 0)
         cp_async_16(smem_u32(dst), A + (off + c0 + k) * lda + off + row, 2 * valid);
       else
@@ -500,6 +504,9 @@ __global__ void scale_copy_kernel(const uint16_t* B, int64_t ldb, uint16_t* X, i
     const int64_t per_col = n / 8, count = per_col * m;
     for (int64_t t = t0; t < count; t += stride) {
       const int64_t j = t / per_col, i = (t - j * per_col) * 8;
+      if (!HG_DBG_INDEX(j, m) || !HG_DBG_INDEX(i + 7, n) || !HG_DBG_ALIGN(B + j * ldb + i, 16) ||
+          !HG_DBG_ALIGN(X + j * ldx + i, 16))
+        continue;
       uint4 v = *reinterpret_cast<const uint4*>(B + j * ldb + i);
       uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -638,5 +645,8 @@ cudaError_t launch_scale_copy(const uint16_t* B, int64_t ldb, uint16_t* X, int64
   return cudaLaunchKernelEx(&l.cfg, vec ? scale_copy_kernel<true> : scale_copy_kernel<false>, B, ldb, X, ldx,
                             n, m, alpha);
 }
+
+// The -DHGEMM_DEBUG build's check word of this file (null otherwise).
+HG_DEBUG_WORD_ACCESSOR(trsm)
 
 }  // namespace hg

@@ -176,6 +176,17 @@ cudaError_t launch_trsm_leaf(const uint16_t* A, int64_t lda, uint16_t* X, int64_
 // Address of the device watchdog word on the current device.
 cudaError_t status_word_address(int** addr);
 
+// The -DHGEMM_DEBUG build's check words, one per kernel file (each sets
+// *out to null in the release build).
+cudaError_t debug_word_tc(int** out);
+cudaError_t debug_word_tc2(int** out);
+cudaError_t debug_word_tc2w(int** out);
+cudaError_t debug_word_skinny(int** out);
+cudaError_t debug_word_generic(int** out);
+cudaError_t debug_word_trsm(int** out);
+cudaError_t debug_word_trileaf(int** out);
+constexpr int kDebugWords = 7;
+
 // Co-residency limits of the cluster kernels on one device, measured once
 // (or nominal GB300 figures when no device has been queried).
 struct DeviceProfile {

@@ -4,6 +4,7 @@
 
 #include <cuda_fp16.h>
 
+#include "debug.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -120,7 +121,9 @@ __device__ __forceinline__ float epi_value(float acc, const EpiArgs& e, float c_
 __device__ __forceinline__ uint4 load_c_old8(const EpiArgs& e, const uint16_t* C, int64_t M,
                                              int64_t N, int64_t ldc, int64_t row, int64_t col0) {
   if (e.mode != 2 || row >= M || col0 >= N) return make_uint4(0u, 0u, 0u, 0u);
-  return *reinterpret_cast<const uint4*>(C + row * ldc + col0);
+  const uint16_t* src = C + row * ldc + col0;
+  if (!HG_DBG_INDEX(col0 + 7, N) || !HG_DBG_ALIGN(src, 16)) return make_uint4(0u, 0u, 0u, 0u);
+  return *reinterpret_cast<const uint4*>(src);
 }
 
 // Mode 2: asks L2 for the previous C values of row `grow`, columns

@@ -4,11 +4,16 @@
 // Each wrapper is one PTX instruction (or a short fixed sequence) with the
 // operand conventions of the PTX ISA. Shared-memory operands are 32-bit
 // shared-window addresses (see smem_u32). No TMA multicast form is used.
+// In the -DHGEMM_DEBUG build every wrapper that takes a shared-memory
+// address of this CTA checks it (and TMA coordinates, TMEM addresses) first
+// and skips the instruction when the check fails (debug.cuh).
 #pragma once
 
 #include <cstdint>
 
 #include <cuda.h>  // CUtensorMap
+
+#include "debug.cuh"
 
 namespace hg {
 
@@ -25,6 +30,7 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 // ---------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  if (!HG_DBG_SMEM(bar, 8)) return;
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
 
@@ -34,11 +40,13 @@ __device__ __forceinline__ void fence_barrier_init() {
 }
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  if (!HG_DBG_SMEM(bar, 8)) return;
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
 // Arrives once and raises the barrier's expected transaction count by `bytes`.
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  if (!HG_DBG_SMEM(bar, 8)) return;
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                : "memory");
 }
@@ -50,6 +58,7 @@ constexpr uint32_t kSuspendHintNs = 1000000;
 // True once the phase with parity `parity` has completed; the thread is
 // suspended meanwhile (up to kSuspendHintNs) instead of polling.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  if (!HG_DBG_SMEM(bar, 8)) return false;  // the caller's bounded wait then gives up
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
@@ -72,6 +81,7 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
 // Out-of-bounds elements of the box are filled with zeros.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
                                             int32_t x, int32_t y) {
+  if (!HG_DBG_SMEM(dst, 16) || !HG_DBG_SMEM(bar, 8) || !HG_DBG_TMA_X(x)) return;
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
@@ -83,6 +93,7 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
 __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap *map,
                                                  uint32_t bar, int32_t x, int32_t y,
                                                  uint64_t policy) {
+  if (!HG_DBG_SMEM(dst, 16) || !HG_DBG_SMEM(bar, 8) || !HG_DBG_TMA_X(x)) return;
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
@@ -106,6 +117,7 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
 // tensor are not written. Tracked by the bulk async-group of this thread.
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t src, int32_t x,
                                              int32_t y) {
+  if (!HG_DBG_SMEM(src, 16) || !HG_DBG_TMA_X(x)) return;
   asm volatile(
       "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
           reinterpret_cast<uint64_t>(map)),
@@ -134,6 +146,7 @@ __device__ __forceinline__ void bulk_wait_group() {
 // Asynchronous 16-byte copy global -> shared (L2 only), reading src_bytes
 // (0..16) and zero-filling the rest; both addresses 16-byte aligned.
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, int src_bytes) {
+  if (!HG_DBG_SMEM(dst, 16) || !HG_DBG_ALIGN(src, 16)) return;
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
                : "memory");
 }
@@ -198,6 +211,11 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
 // 32 lanes x 32 bits, 32 consecutive columns: thread t of the warp receives
 // TMEM lane (lane field of taddr) + t, columns col .. col+31.
 __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
+  if (!HG_DBG_TMEM(taddr, 32)) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) r[i] = 0u;
+    return;
+  }
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
       "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
@@ -308,6 +326,7 @@ __device__ __forceinline__ void cluster_sync() {
 
 // The shared::cluster address of the same shared-memory offset in CTA `rank`.
 __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  (void)HG_DBG_SMEM(addr, 8);  // the same offset in the other CTA: checked against ours
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
   return r;
@@ -323,6 +342,7 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
 // No suspend-time hint here: measured faster for phases completed by
 // arrivals from other CTAs.
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  if (!HG_DBG_SMEM(bar, 8)) return false;  // the caller's bounded wait then gives up
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
@@ -338,6 +358,7 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
 // on a barrier of either CTA of the pair (`bar` is a shared::cluster address).
 __device__ __forceinline__ void tma_load_2d_cg2(uint32_t dst, const CUtensorMap *map, uint32_t bar,
                                                 int32_t x, int32_t y) {
+  if (!HG_DBG_SMEM(dst, 16) || !HG_DBG_TMA_X(x)) return;
   asm volatile(
       "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
@@ -397,6 +418,7 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t cluster_addr, uint32_t a,
 // the destination CTA's barrier `bar` (a shared::cluster address).
 __device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst, uint32_t src, uint32_t bytes,
                                                      uint32_t bar) {
+  if (!HG_DBG_SMEM(src, bytes)) return;
   asm volatile(
       "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
           dst),
