@@ -51,21 +51,32 @@ struct SkCfg {
   static constexpr int BROWS = BN / 2;   // B rows per CTA
   static_assert(BROWS % kMnBox == 0, "an N-contiguous B arrives in whole 64-column boxes");
   static constexpr int BK = kTcBK;
-  static constexpr int STAGES = BN == 256 ? 6 : 8;  // 32 KB or 24 KB per stage
+  static constexpr int STAGES = BN == 256 ? 7 : 9;  // 32 KB or 24 KB per stage
   static constexpr int UMMA_K = 16;
   static constexpr int A_BYTES = ROWS * BK * 2;
   static constexpr int B_BYTES = BROWS * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int TX_BYTES = 2 * STAGE_BYTES;
-  static constexpr int RING_BYTES = STAGES * STAGE_BYTES;     // reused for the reduction
+  static constexpr int RING_BYTES = STAGES * STAGE_BYTES;     // reused for the reduction and the C staging
   // the last slice owns the most units
   static constexpr int MAX_OWN_COLS = 64 * (owned_unit(SPLIT, SPLIT, UNITS) - owned_unit(SPLIT - 1, SPLIT, UNITS));
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
-  static constexpr int OFF_C = OFF_B + STAGES * B_BYTES;     // FP16 staging of C
   static constexpr int C_WARP_BYTES = kEpiRows * MAX_OWN_COLS * 2;
   static constexpr int C_BYTES = 4 * C_WARP_BYTES;
-  static constexpr int OFF_BAR = OFF_C + C_BYTES;
+  // bytes a CTA owning `cols` columns receives (S-1 blocks) plus sends
+  // (its partial outside its range), FP32, 128 rows; the most for the
+  // largest range
+  static constexpr int exchange_bytes(int cols) {
+    return (SPLIT - 1) * ROWS * cols * 4 + ROWS * (BN - cols) * 4;
+  }
+  // The FP16 staging of C, inside the ring after the exchange area: the ring
+  // is free once the CTA's own MMAs are done, and the staging is written only
+  // after the received partials have been summed (so the ring holds one more
+  // stage than with a separate staging area).
+  static constexpr int OFF_C = (exchange_bytes(MAX_OWN_COLS) + 1023) / 1024 * 1024;
+  static constexpr int RING_END = OFF_B + STAGES * B_BYTES;
+  static constexpr int OFF_BAR = RING_END;
   // full, empty, accumulator full, drain, partials received, owner ready
   // (one per slice), partials acknowledged
   static constexpr int NUM_BARS = 2 * STAGES + 3 + 4 + 1;
@@ -75,12 +86,7 @@ struct SkCfg {
   static constexpr int TMEM_COLS = BN;
   static constexpr uint32_t IDESC = idesc_f16_f32acc(BM, BN);
 
-  // bytes a CTA owning `cols` columns receives (S-1 blocks) plus sends
-  // (its partial outside its range), FP32, 128 rows
-  static constexpr int exchange_bytes(int cols) {
-    return (SPLIT - 1) * ROWS * cols * 4 + ROWS * (BN - cols) * 4;
-  }
-  static_assert(exchange_bytes(MAX_OWN_COLS) <= RING_BYTES, "reduction fits in the ring");
+  static_assert(OFF_C + C_BYTES <= RING_BYTES, "reduction and C staging fit in the ring");
   static_assert(exchange_bytes(64) <= RING_BYTES, "reduction fits in the ring");
   static_assert(SMEM_BYTES <= 232448, "exceeds 227 KB of shared memory per CTA");
   static_assert(C_WARP_BYTES % 1024 == 0, "staging boxes stay 1024-byte aligned");
@@ -155,7 +161,8 @@ __global__ void __launch_bounds__(192, 1)
     tmem_relinquish_alloc_permit_cg2();
   }
   tc_fence_before_sync();
-  cluster_sync();
+  __syncthreads();  // the TMEM address and the abort flag, within the CTA
+  cluster_sync_after_init();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
   // operands and C may come from the previous launch on the stream

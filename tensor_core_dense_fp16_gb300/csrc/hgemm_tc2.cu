@@ -173,7 +173,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED ? 320 : 192, 1
   // barrier initialisation must be visible to the peer before any remote
   // arrive or TMA completion can target it
   tc_fence_before_sync();
-  cluster_sync();
+  __syncthreads();  // the TMEM address and the abort flag, within the CTA
+  cluster_sync_after_init();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
   // operands and C may come from the previous launch on the stream

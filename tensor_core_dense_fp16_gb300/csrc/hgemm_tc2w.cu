@@ -124,7 +124,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
     tmem_relinquish_alloc_permit_cg2();
   }
   tc_fence_before_sync();
-  cluster_sync();
+  __syncthreads();  // the TMEM address and the abort flag, within the CTA
+  cluster_sync_after_init();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
   // operands and C may come from the previous launch on the stream

@@ -324,6 +324,16 @@ __device__ __forceinline__ void cluster_sync() {
                    : "memory");
 }
 
+// The first cluster barrier after the barriers' initialisation: a relaxed
+// arrive (the initialiser's fence.mbarrier_init already released the
+// barriers at cluster scope) and an acquiring wait. Anything else a CTA's own
+// threads must see from each other (the TMEM address, flags) needs a CTA
+// barrier before it. Measured on the pair kernel: ~540 cycles less than the
+// release/acquire barrier.
+__device__ __forceinline__ void cluster_sync_after_init() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // The shared::cluster address of the same shared-memory offset in CTA `rank`.
 __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
   (void)HG_DBG_SMEM(addr, 8);  // the same offset in the other CTA: checked against ours
