@@ -325,7 +325,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED ? 320 : 192, 1
       const int y0 = w.mb * Cfg::BM + static_cast<int>(rank) * Cfg::ROWS + q * kEpiRows;
       // this warp's last box (none when a 64-column part leaves the odd box out)
       const int last = (chunks - 1 - h) >= 0 ? h + ((chunks - 1 - h) / 2) * 2 : -1;
-      if (last < 0) {
+      // After a CTA's last tile no MMA waits for its accumulator again, so
+      // its release (a cluster-scope release, ~1,000 cycles) is skipped.
+      const bool reused = t + num_clusters < p.num_tiles;
+      if (last < 0 && reused) {
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(mapa_shared(acce_bar(acc), 0));
@@ -337,7 +340,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED ? 320 : 192, 1
         tmem_ld_32x32b_x32(t_row + c * kEpiCols + 32, v1);
         tmem_ld_wait(v0);
         tmem_ld_wait(v1);
-        if (c == last) {
+        if (c == last && reused) {
           tc_fence_before_sync();
           __syncwarp();
           if (lane == 0) mbar_arrive_cluster(mapa_shared(acce_bar(acc), 0));
@@ -390,7 +393,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED ? 320 : 192, 1
         tmem_ld_32x32b_x32(t_row + c * kEpiCols + 32, v1);
         tmem_ld_wait(v0);
         tmem_ld_wait(v1);
-        if (c == chunks - 1) {
+        // no release after this CTA's last tile: no MMA waits for it again
+        if (c == chunks - 1 && t + num_clusters < p.num_tiles) {
           tc_fence_before_sync();
           __syncwarp();
           if (lane == 0) mbar_arrive_cluster(mapa_shared(acce_bar(acc), 0));
@@ -419,8 +423,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED ? 320 : 192, 1
   }
 
   // Neither CTA frees TMEM before the pair's last MMA and last TMEM read.
+  // Execution order is all this barrier needs: no copy or remote arrival
+  // between the two CTAs is in flight by now (the last tile's accumulator
+  // is not released, the MMAs and loads completed on waited barriers), so
+  // its arrive is relaxed (a release costs ~1,000 cycles).
   tc_fence_before_sync();
-  cluster_sync();
+  cluster_sync_relaxed();
   tc_fence_after_sync();
   if (warp == 1) tmem_dealloc_cg2(tmem_base, Cfg::TMEM_COLS);
 }

@@ -284,8 +284,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
         tmem_ld_32x32b_x32(t_row + c * kEpiCols + 32, v1);
         tmem_ld_wait(v0);
         tmem_ld_wait(v1);
-        if (c == chunks - 1) {
-          // half h has been read: the next tile's MMAs may overwrite it
+        if (c == chunks - 1 && t + num_clusters < p.num_tiles) {
+          // half h has been read: the next tile's MMAs may overwrite it (after
+          // this CTA's last tile nothing waits, and the cluster-scope release
+          // is skipped)
           tc_fence_before_sync();
           __syncwarp();
           if (lane == 0) mbar_arrive_cluster(mapa_shared(acce_bar(h), 0));
@@ -310,9 +312,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
     __syncwarp();
   }
 
-  // Neither CTA frees TMEM before the pair's last MMA and last TMEM read.
+  // Neither CTA frees TMEM before the pair's last MMA and last TMEM read;
+  // execution order is all this barrier needs (nothing between the two CTAs
+  // is in flight by now), so its arrive is relaxed.
   tc_fence_before_sync();
-  cluster_sync();
+  cluster_sync_relaxed();
   tc_fence_after_sync();
   if (warp == 1) tmem_dealloc_cg2(tmem_base, Cfg::TMEM_COLS);
 }

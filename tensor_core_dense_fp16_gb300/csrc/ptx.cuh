@@ -334,6 +334,12 @@ __device__ __forceinline__ void cluster_sync_after_init() {
   asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// A cluster barrier for execution order only (relaxed arrive, acquiring
+// wait), when no memory operation between the CTAs is left in flight.
+__device__ __forceinline__ void cluster_sync_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // The shared::cluster address of the same shared-memory offset in CTA `rank`.
 __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
   (void)HG_DBG_SMEM(addr, 8);  // the same offset in the other CTA: checked against ours
