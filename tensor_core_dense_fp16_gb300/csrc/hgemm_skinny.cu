@@ -262,11 +262,12 @@ __global__ void __launch_bounds__(192, 1)
     ok = __shfl_sync(0xffffffffu, ok, 0);
     tc_fence_after_sync();
     // this CTA's operand ring is now free: tell the other slices of the same
-    // half that they may send their partials of our column range
+    // half that they may send their partials of our column range (relaxed:
+    // the ring's last readers, the MMAs, completed before accf did)
     if (warp == 2 && lane == 0 && ok)
       for (int s2 = 0; s2 < SPLIT; ++s2)
         if (s2 != slice)
-          mbar_arrive_cluster(mapa_shared(ready_bar0 + 8u * slice, static_cast<uint32_t>(2 * s2 + half)));
+          mbar_arrive_cluster_relaxed(mapa_shared(ready_bar0 + 8u * slice, static_cast<uint32_t>(2 * s2 + half)));
   }
 
   const int q = warp & 3;  // TMEM lanes / tile rows 32q .. 32q+31 of this CTA
@@ -318,9 +319,11 @@ __global__ void __launch_bounds__(192, 1)
     int got = 1;
     if (lane == 0) got = wait_phase_cluster(recv_bar, 0, wd, kWdReduce) ? 1 : 0;
     got = __shfl_sync(0xffffffffu, got, 0);
+    // every copy into us has completed (its bytes were counted): the senders
+    // may leave (relaxed: this reports completion already observed)
     if (got && warp == 2 && lane == 0)
       for (int s2 = 0; s2 < SPLIT; ++s2)
-        if (s2 != slice) mbar_arrive_cluster(mapa_shared(ack_bar, static_cast<uint32_t>(2 * s2 + half)));
+        if (s2 != slice) mbar_arrive_cluster_relaxed(mapa_shared(ack_bar, static_cast<uint32_t>(2 * s2 + half)));
     if (got) {
       const int x0 = nb * Cfg::BN + own_c0;
       const int y0 = mb * Cfg::BM + half * Cfg::ROWS + q * kEpiRows;

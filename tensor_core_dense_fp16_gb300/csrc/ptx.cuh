@@ -354,6 +354,14 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
                : "memory");
 }
 
+// The same arrival without release semantics (~1,000 cycles cheaper), for a
+// signal that only reports work already observed complete (a barrier the
+// arriving thread has waited on), with nothing of its own to publish.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+
 // Wait with cluster-scope acquire (for barriers that receive remote arrives).
 // No suspend-time hint here: measured faster for phases completed by
 // arrivals from other CTAs.
