@@ -943,6 +943,8 @@ def run_ours(args, spec, a, b, world, rank, local):
                                         "ms_median": median_ms, "ms_mean": mean_ms,
                                         "ms_min": min(times_ms), "path": kernel, "traffic": traffic},
                                        **roofline_of(flops, nbytes, median_ms, peaks))}
+        configs[args.workload]["frac_with_floor"] = (
+            (configs[args.workload]["roofline_us"] * 1e-3 + floor["ms_median"]) / median_ms)
         configs.update(time_configs(torch, tc, dev, stream, flush, peaks, floor_ms=floor["ms_median"]))
         configs["launch_floor"] = floor
 
