@@ -161,6 +161,15 @@ TRI_OPS = {
 }
 
 
+# hgemm_trsm_last_schedule's values, by name (bench.py reports the schedule a
+# solve took), and the kernels of the one-launch schedule.
+SCHEDULE_NAMES = {1: "substitution", 2: "recursive (products by the inverses and GEMM updates, one launch each)",
+                  3: "chain (the inverses' launch, then one persistent cooperative launch)"}
+CHAIN_KERNELS = ("trsm_inverse_kernel (the inverses of the diagonal blocks of 512) + trsm_chain_kernel (one "
+                 "persistent cooperative launch: X := B, then per block its product by the inverse and the "
+                 "update of every block still to be solved, grid barriers between the phases)")
+
+
 def parse_args():
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -722,6 +731,9 @@ def run_tri_ours(args, spec, a_col, b_col, world, rank, local):
     torch.cuda.synchronize(dev)
     if tc.hgemm_device_status(stream) != tc.HGEMM_OK:
         raise RuntimeError("a kernel wait timed out during warm-up")
+    # the solve's schedule (hgemm_trsm_ws picks it from the shape)
+    schedule = tc.hgemm_trsm_last_schedule() if op in ("trsm", "trsm_n") else None
+    chain = schedule == tc.HGEMM_TRSM_CHAIN
     times_ms, clocks = timed_region(torch, dev, local, stream, step, flush, args.steps, dist)
     if tc.hgemm_device_status(stream) != tc.HGEMM_OK:
         raise RuntimeError("a kernel wait timed out in the timed region")
@@ -762,7 +774,7 @@ def run_tri_ours(args, spec, a_col, b_col, world, rank, local):
     roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
             "frac": achieved / peak, "traffic": None,
             "peak_source": f"{peak_src}: bf16_tflops (burst) x {FP16_PER_BF16} fp16/bf16",
-            "timing": "median call", "kernel": ops["kernel"],
+            "timing": "median call", "kernel": CHAIN_KERNELS if chain else ops["kernel"],
             "algorithmic_flops": flops, "algorithmic_bytes": 2.0 * (n * (n + 1) / 2 + 2 * n * m)}
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -793,9 +805,11 @@ def run_tri_ours(args, spec, a_col, b_col, world, rank, local):
                        "path": ("hgemm_trsm_ws" if op == "trsm" and not args.no_workspace else
                                 "hgemm_trsm_op(N, workspace)" if op == "trsm_n" and not args.no_workspace else
                                 ops["call"]),
+                       "schedule": SCHEDULE_NAMES.get(schedule),
                        "parallelism": f"replicas x{world}"},
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": args.steps * ((ops["launches"](n, m, 512) + 1)
+            "gpu_launches": args.steps * (2 if chain else
+                                          (ops["launches"](n, m, 512) + 1)
                                           if op in ("trsm", "trsm_n") and not args.no_workspace
                                           else ops["launches"](n, m)),
             "clocks": dict(clocks, kcycles_per_step=(median_ms * clocks["sm_mhz"]

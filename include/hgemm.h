@@ -223,8 +223,9 @@ HGEMM_API int hgemm_trsm(const hgemm_half_t *A, int64_t lda, const hgemm_half_t 
 /*
  * hgemm_trsm_workspace_size — bytes of device workspace hgemm_trsm_ws uses
  * for a triangle of order n: 512 KiB per diagonal block of order ≤ 512 of
- * the recursion (n = 8192: 16 blocks, 8 MiB). 0 for n ≤ 0 or n beyond 128
- * such blocks. Pure host logic.
+ * the recursion, plus 4 KiB of synchronisation words for the one-launch
+ * schedule (n = 8192: 16 blocks, 8 MiB + 4 KiB). 0 for n ≤ 0 or n beyond
+ * 128 such blocks. Pure host logic.
  */
 HGEMM_API size_t hgemm_trsm_workspace_size(int64_t n);
 
@@ -242,8 +243,22 @@ HGEMM_API size_t hgemm_trsm_workspace_size(int64_t n);
  * the substitution kernel). The substitution then happens once per block for
  * the identity rather than per right-hand side, and the deepest updates of
  * the recursion are inside the inverses.
- * Rounding: each solved block is rounded once to FP16 as in hgemm_trsm, the
- * inverse once more. A null workspace, one too small or not 16-byte
+ * Schedule: when m ≤ 1024, the workspace also holds the synchronisation
+ * words (the full hgemm_trsm_workspace_size(n)), A is 16-byte aligned with
+ * lda a multiple of 8 and the recursion has at most 32 diagonal blocks,
+ * everything after the inverses runs as ONE persistent cooperative launch: the blocks in the
+ * recursion's order, each solved by its product, then each block's
+ * contribution subtracted at once from all blocks still to be solved (the
+ * recursion's update sums, split per block: right-looking), grid-wide
+ * barriers between these phases. Otherwise (a workspace of exactly the
+ * inverses' size, as earlier versions asked for, or the limits above) the
+ * recursion runs as a sequence of launches (products by the inverses, GEMM
+ * updates). hgemm_force_trsm_schedule chooses for testing;
+ * hgemm_trsm_last_schedule tells which one a call took.
+ * Rounding: each solved block is rounded once to FP16, the inverse once
+ * more; X is rounded after every update it receives (the recursion: once per
+ * level whose first half holds the block; the one launch: once per block
+ * solved before it). A null workspace, one too small or not 16-byte
  * aligned is HGEMM_ERR_INVALID_ARG; X not suited to the tensor-core path, or
  * a path forced by hgemm_force_path, solves as hgemm_trsm does.
  * Accuracy against hgemm_trsm: rounding L_b⁻¹ to FP16 adds at most
@@ -296,6 +311,36 @@ HGEMM_API int hgemm_trsm_op(int op, const hgemm_half_t *A, int64_t lda, const hg
                   void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * TRSM schedules (hgemm_trsm_last_schedule, hgemm_force_trsm_schedule):
+ * SUBSTITUTION: no workspace (or X not suited to it): the recursion's
+ * launches with every diagonal block of order ≤ 256 solved by substitution;
+ * RECURSIVE: the recursion's launches, blocks of order ≤ 512 solved by
+ * their inverses; CHAIN: the inverses' launch, then one persistent launch
+ * (hgemm_trsm_ws).
+ */
+#define HGEMM_TRSM_AUTO 0
+#define HGEMM_TRSM_SUBSTITUTION 1
+#define HGEMM_TRSM_RECURSIVE 2
+#define HGEMM_TRSM_CHAIN 3
+
+/*
+ * hgemm_force_trsm_schedule — testing and profiling aid: HGEMM_TRSM_RECURSIVE
+ * keeps later solves with a workspace on the recursion's launches;
+ * HGEMM_TRSM_CHAIN takes the one-launch schedule wherever it can run (also
+ * past m = 1024, where it is slower: its product phases must fit one wave
+ * of tiles, m up to ~9,700); HGEMM_TRSM_AUTO (the default) chooses as
+ * hgemm_trsm_ws describes. Returns HGEMM_OK, or HGEMM_ERR_INVALID_ARG for
+ * another value. Process-wide, like hgemm_force_path.
+ */
+HGEMM_API int hgemm_force_trsm_schedule(int schedule);
+
+/*
+ * hgemm_trsm_last_schedule — the HGEMM_TRSM_* schedule of the last
+ * triangular solve enqueued on this host thread (0 before any). Host logic.
+ */
+HGEMM_API int hgemm_trsm_last_schedule(void);
+
+/*
  * hgemm_trsm_noalloc — hgemm_trsm_ws for callers that cannot allocate device
  * memory: code whose device memory all belongs to another allocator (a
  * framework's caching pool, a fixed budget reserved up front) and which may
@@ -304,8 +349,8 @@ HGEMM_API int hgemm_trsm_op(int op, const hgemm_half_t *A, int64_t lda, const hg
  * an addition for such callers.
  *
  * Same system, operands, results and return values as hgemm_trsm_ws, whose
- * workspace here is a fixed array of HGEMM_TRSM_NOALLOC_MAX_BYTES (8 MiB)
- * inside the library, present on every device that loads the library until
+ * workspace here is a fixed array of HGEMM_TRSM_NOALLOC_MAX_BYTES (8 MiB +
+ * 4 KiB) inside the library, present on every device that loads the library until
  * the process exits. Nothing is allocated: no cudaMalloc or cudaFree, no
  * allocating library call. Limit: triangles whose recursion has at most 16
  * diagonal blocks of order ≤ 512, which is every n ≤ 8192; a larger n
@@ -325,7 +370,7 @@ HGEMM_API int hgemm_trsm_op(int op, const hgemm_half_t *A, int64_t lda, const hg
  * overlaps on the GPU (other streams, other host threads) race on it and
  * must be ordered by the caller, e.g. issued on one stream.
  */
-#define HGEMM_TRSM_NOALLOC_MAX_BYTES (8u << 20)
+#define HGEMM_TRSM_NOALLOC_MAX_BYTES ((8u << 20) + 4096u)
 HGEMM_API int hgemm_trsm_noalloc(const hgemm_half_t *A, int64_t lda, const hgemm_half_t *B, int64_t ldb,
                        hgemm_half_t *X, int64_t ldx, int64_t n, int64_t m, float alpha,
                        cudaStream_t stream);

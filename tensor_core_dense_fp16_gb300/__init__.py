@@ -30,6 +30,8 @@ __all__ = [
     "hgemm_force_path", "hgemm_device_status", "hgemm_last_cuda_error",
     "hgemm_status_string", "hgemm_version", "hgemm_set_wait_timeout", "hgemm_debug_inject",
     "hgemm_force_split", "hgemm_launch_floor", "hgemm_ex", "hgemm_strided", "hgemm_trmm", "hgemm_trsm", "hgemm_trsm_ws", "hgemm_trsm_workspace_size", "hgemm_trsm_noalloc", "hgemm_trsm_op", "HGEMM_OP_N", "HGEMM_OP_T", "hgemm_layout", "HGEMM_TRMM_MAX_N", "HGEMM_TRSM_NOALLOC_MAX_BYTES",
+    "hgemm_force_trsm_schedule", "hgemm_trsm_last_schedule", "HGEMM_TRSM_AUTO", "HGEMM_TRSM_SUBSTITUTION",
+    "HGEMM_TRSM_RECURSIVE", "HGEMM_TRSM_CHAIN",
     "HGEMM_A_ROW_MAJOR", "HGEMM_A_COL_MAJOR", "HGEMM_B_COL_MAJOR", "HGEMM_B_ROW_MAJOR",
     "HGEMM_INJECT_NONE", "HGEMM_INJECT_DROP_ARRIVAL", "matmul",
 ]
@@ -42,7 +44,11 @@ HGEMM_ERR_CUDA = -4
 HGEMM_ERR_TIMEOUT = -5
 HGEMM_ERR_DEBUG_CHECK = -6
 HGEMM_TRMM_MAX_N = 16384
-HGEMM_TRSM_NOALLOC_MAX_BYTES = 8 << 20
+HGEMM_TRSM_NOALLOC_MAX_BYTES = (8 << 20) + 4096
+HGEMM_TRSM_AUTO = 0
+HGEMM_TRSM_SUBSTITUTION = 1
+HGEMM_TRSM_RECURSIVE = 2
+HGEMM_TRSM_CHAIN = 3
 HGEMM_OP_N = 0
 HGEMM_OP_T = 1
 HGEMM_A_ROW_MAJOR = 0
@@ -143,7 +149,9 @@ def load():
     lib.hgemm_force_split.restype = i32
     lib.hgemm_launch_floor.argtypes = [i32, vp]
     lib.hgemm_launch_floor.restype = i32
-    for name in ("hgemm_debug_build", "hgemm_debug_code", "hgemm_debug_selftest"):
+    lib.hgemm_force_trsm_schedule.argtypes = [i32]
+    lib.hgemm_force_trsm_schedule.restype = i32
+    for name in ("hgemm_debug_build", "hgemm_debug_code", "hgemm_debug_selftest", "hgemm_trsm_last_schedule"):
         getattr(lib, name).argtypes = []
         getattr(lib, name).restype = i32
     _lib = lib
@@ -315,6 +323,18 @@ def hgemm_select_path(A, B, C, M: int, N: int, K: int) -> int:
 
 def hgemm_force_path(path: int) -> None:
     _raise_on(load().hgemm_force_path(path), "hgemm_force_path")
+
+
+def hgemm_force_trsm_schedule(schedule: int) -> None:
+    """Testing aid: HGEMM_TRSM_RECURSIVE keeps solves with a workspace on the
+    recursion's launches; HGEMM_TRSM_AUTO / HGEMM_TRSM_CHAIN allow the one
+    persistent launch."""
+    _raise_on(load().hgemm_force_trsm_schedule(schedule), "hgemm_force_trsm_schedule")
+
+
+def hgemm_trsm_last_schedule() -> int:
+    """The HGEMM_TRSM_* schedule of the last solve enqueued on this thread."""
+    return int(load().hgemm_trsm_last_schedule())
 
 
 def hgemm_device_status(stream=None) -> int:

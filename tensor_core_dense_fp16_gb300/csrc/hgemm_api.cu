@@ -41,6 +41,8 @@ std::atomic<int> g_forced_path{-1};
 std::atomic<int> g_forced_split{0};  // split * 1024 + tile_n, or 0
 std::atomic<unsigned long long> g_timeout_ns{kDefaultTimeoutNs};
 std::atomic<int> g_inject{HGEMM_INJECT_NONE};
+std::atomic<int> g_trsm_schedule{HGEMM_TRSM_AUTO};  // hgemm_force_trsm_schedule
+thread_local int t_trsm_schedule = 0;               // hgemm_trsm_last_schedule
 
 struct DeviceState {
   std::atomic<int> ready{0};  // 0 unknown, 1 supported, -1 unsupported
@@ -69,7 +71,7 @@ cudaError_t debug_words(int* (&out)[hg::kDebugWords]) {
   cudaError_t (*const get[hg::kDebugWords])(int**) = {hg::debug_word_tc,      hg::debug_word_tc2,
                                                       hg::debug_word_tc2w,    hg::debug_word_skinny,
                                                       hg::debug_word_generic, hg::debug_word_trsm,
-                                                      hg::debug_word_trileaf};
+                                                      hg::debug_word_trileaf, hg::debug_word_chain};
   for (int i = 0; i < hg::kDebugWords; ++i) {
     const cudaError_t e = get[i](&out[i]);
     if (e != cudaSuccess) return e;
@@ -970,8 +972,84 @@ bool trsm_leaves(int64_t n, int64_t leaf, hg::TriLeaves* leaves, bool fwd = fals
   return n > 0 && walk(0, n);
 }
 
+// Largest number of right-hand sides for which hgemm_trsm_ws takes the chain
+// schedule by itself.
+constexpr int64_t kChainAutoMaxM = 1024;
+
 // one inverse in the workspace: FP16, kTrsmInverseLeaf² (512 KiB)
 constexpr uint64_t kTrsmInverseBytes = 2ull * hg::kTrsmInverseLeaf * hg::kTrsmInverseLeaf;
+
+// The tile of one chain phase: all m rows × ncols columns with K steps of
+// 64 on `grid` CTAs. The operand bytes an SM takes in are (bm + bn) per K
+// element per tile, so the cost is waves × (bm + bn); ties go to the larger
+// tile. A product phase's tiles must all run at once (tiles ≤ grid).
+// Returns false when no tile fits.
+bool chain_tile(int64_t m, int64_t ncols, int grid, bool product, int* bm, int* bn) {
+  static constexpr int kBm[2] = {128, 64};
+  static constexpr int kBn[3] = {256, 128, 64};
+  int64_t best = -1;
+  for (int i : kBm)
+    for (int j : kBn) {
+      const int64_t tiles = ((m + i - 1) / i) * ((ncols + j - 1) / j);
+      if (product && tiles > grid) continue;
+      const int64_t cost = ((tiles + grid - 1) / grid) * (i + j);
+      if (best < 0 || cost < best) {
+        best = cost;
+        *bm = i;
+        *bn = j;
+      }
+    }
+  return best >= 0;
+}
+
+// Plans the chain launch of a solve whose inverses are (or will be) in W:
+// fills args (phases, operands) and *grid. False when the chain does not
+// apply (too many blocks or rows, a product phase wider than the grid).
+bool chain_plan(const hg::TriLeaves& leaves, int64_t n, int64_t m, bool copy, bool fwd, int max_grid,
+                hg::ChainArgs* args, int* grid, int* ragged) {
+  if (leaves.count < 1 || leaves.count > hg::kChainMaxLeaves || max_grid < 1) return false;
+  if (m < 1 || (m + 63) / 64 > hg::kChainMaxRowGroups || n > (int64_t(1) << 30)) return false;
+  int np = 0, max_tiles = 1;
+  uint32_t target = 0;
+  *ragged = -1;
+  if (copy) args->phase[np++] = hg::ChainPhase{hg::chain_flags(hg::kChainCopy, 0, 0, 0, 0), 0, 0, 0, 0, 0, 0, 0};
+  for (int b = 0; b < leaves.count; ++b) {
+    const int64_t off = leaves.off[b], sz = leaves.size[b];
+    const int ksteps = static_cast<int>((sz + 63) / 64);
+    const bool rag = sz % 64 != 0;  // only the block that ends at n (the edge of every map)
+    if (rag) {
+      if (off + sz != n || *ragged >= 0) return false;
+      *ragged = b;
+    }
+    int bm = 0, bn = 0;
+    if (!chain_tile(m, sz, max_grid, true, &bm, &bn)) return false;
+    const int64_t pn = (sz + bn - 1) / bn;
+    target += static_cast<uint32_t>(pn);
+    max_tiles = std::max<int64_t>(max_tiles, ((m + bm - 1) / bm) * pn);
+    // the product: Aᵀ·X = B reads L_b⁻¹ N-contiguous (k, n) at W row b·512 + k;
+    // A·X = B reads L_b⁻ᵀ K-contiguous (k, n) at W row b·512 + n
+    const int wbase = rag ? 0 : b * hg::kTrsmInverseLeaf;
+    args->phase[np++] = hg::ChainPhase{
+        hg::chain_flags(hg::kChainProduct, rag ? hg::kChainMapWRagged : hg::kChainMapW, fwd ? 0 : 1, bm, bn),
+        static_cast<int>(off), static_cast<int>(off + sz), static_cast<int>(off), ksteps,
+        fwd ? 0 : wbase, fwd ? wbase : 0, target};
+    // the update of every block still to be solved: Aᵀ·X = B, columns [0, off)
+    // minus Xᵀ_b · A(b rows, those columns), A read K-contiguous at (off + k, n);
+    // A·X = B, columns [off + sz, n) minus Xᵀ_b · A(those rows, b columns)ᵀ,
+    // A read N-contiguous at (n, off + k)
+    const int64_t u0 = fwd ? off + sz : 0, u1 = fwd ? n : off;
+    if (u1 > u0) {
+      if (!chain_tile(m, u1 - u0, max_grid, false, &bm, &bn)) return false;
+      max_tiles = std::max<int64_t>(max_tiles, ((m + bm - 1) / bm) * ((u1 - u0 + bn - 1) / bn));
+      args->phase[np++] = hg::ChainPhase{
+          hg::chain_flags(hg::kChainUpdate, hg::kChainMapA, fwd ? 1 : 0, bm, bn), static_cast<int>(u0),
+          static_cast<int>(u1), static_cast<int>(off), ksteps, static_cast<int>(off), static_cast<int>(u0), 0};
+    }
+  }
+  args->num_phases = np;
+  *grid = std::min(max_grid, max_tiles);
+  return true;
+}
 
 // hgemm_trsm, hgemm_trsm_ws and hgemm_trsm_op: W (may be null) holds room
 // for the inverses of the diagonal blocks. fwd: the literal orientation
@@ -999,12 +1077,14 @@ int trsm_impl(const hgemm_half_t* A, int64_t lda, const hgemm_half_t* B, int64_t
       (!in_place && ranges_overlap(X, 2 * static_cast<uint64_t>(sx), B, 2 * static_cast<uint64_t>(sb))))
     return HGEMM_ERR_ALIAS;
   hg::TriLeaves leaves{};
+  uint64_t inv_bytes = 0;  // the inverses' part of the workspace
   if (W) {
     if (!trsm_leaves(n, hg::kTrsmInverseLeaf, &leaves, fwd) ||
         w_bytes < kTrsmInverseBytes * static_cast<uint64_t>(leaves.count) ||
         (reinterpret_cast<uintptr_t>(W) & 15u))
       return HGEMM_ERR_INVALID_ARG;
-    const uint64_t wb = kTrsmInverseBytes * static_cast<uint64_t>(leaves.count);
+    inv_bytes = kTrsmInverseBytes * static_cast<uint64_t>(leaves.count);
+    const uint64_t wb = std::min<uint64_t>(w_bytes, inv_bytes + hg::kChainSyncBytes);
     if (ranges_overlap(W, wb, A, 2 * static_cast<uint64_t>(sa)) ||
         ranges_overlap(W, wb, B, 2 * static_cast<uint64_t>(sb)) ||
         ranges_overlap(W, wb, X, 2 * static_cast<uint64_t>(sx)))
@@ -1025,10 +1105,55 @@ int trsm_impl(const hgemm_half_t* A, int64_t lda, const hgemm_half_t* B, int64_t
   // 256, 1.30 ms; products by the inverses of the blocks of 256, 0.89 ms.
   const bool by_inverse = W && (reinterpret_cast<uintptr_t>(X) & 15u) == 0 && ldx % 8 == 0 &&
                           g_forced_path.load(std::memory_order_relaxed) < 0;
+  t_trsm_schedule = by_inverse ? HGEMM_TRSM_RECURSIVE : HGEMM_TRSM_SUBSTITUTION;
+  // The chain: everything after the inverses in one persistent launch (the
+  // workspace's synchronisation words after the inverses, the triangle
+  // suited to TMA).
+  // Automatic choice: the chain for at most kChainAutoMaxM right-hand sides,
+  // where its one launch beats the recursion's chain of launches (measured);
+  // past that the recursion's large products are faster.
+  const int schedule = g_trsm_schedule.load(std::memory_order_relaxed);
+  hg::ChainArgs chain{};
+  int chain_grid = 0, ragged = -1;
+  const bool use_chain = by_inverse && schedule != HGEMM_TRSM_RECURSIVE &&
+                         (schedule == HGEMM_TRSM_CHAIN || m <= kChainAutoMaxM) &&
+                         w_bytes >= inv_bytes + hg::kChainSyncBytes &&
+                         (reinterpret_cast<uintptr_t>(A) & 15u) == 0 && lda % 8 == 0 &&
+                         chain_plan(leaves, n, m, !in_place || alpha != 1.0f, fwd,
+                                    hg::chain_max_grid(dev->num_sms), &chain, &chain_grid, &ragged);
+  uint32_t* sync = use_chain ? reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(W) + inv_bytes) : nullptr;
   if (by_inverse) {
-    e = hg::launch_trsm_inverse(a, lda, W, leaves, stream);
+    e = hg::launch_trsm_inverse(a, lda, W, leaves, sync, stream);
     if (e != cudaSuccess) return cuda_fail(e);
     chained = true;
+  }
+  if (use_chain) {
+    CUtensorMap mx, mw, mwr, ma;
+    const int64_t L = hg::kTrsmInverseLeaf;
+    if ((rc = encode_map(&mx, x, m, n, ldx, 64, 64)) != HGEMM_OK ||
+        (rc = encode_map(&mw, W, static_cast<int64_t>(leaves.count) * L, L, L, 64, 64)) != HGEMM_OK ||
+        (rc = encode_map(&ma, a, n, n, lda, 64, 64)) != HGEMM_OK)
+      return rc;
+    mwr = mw;
+    if (ragged >= 0 && (rc = encode_map(&mwr, W + ragged * L * L, leaves.size[ragged], leaves.size[ragged], L,
+                                        64, 64)) != HGEMM_OK)
+      return rc;
+    chain.X = x;
+    chain.ldx = ldx;
+    chain.B = reinterpret_cast<const uint16_t*>(B);
+    chain.ldb = ldb;
+    chain.alpha = alpha;
+    chain.m = static_cast<int>(m);
+    chain.n = static_cast<int>(n);
+    chain.copy_vec = n % 8 == 0 && ldb % 8 == 0 && (reinterpret_cast<uintptr_t>(B) & 15u) == 0;
+    chain.sync = sync;
+    chain.status = t_ctx.status;
+    chain.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
+    chain.inject = g_inject.load(std::memory_order_relaxed);
+    e = hg::launch_trsm_chain(mx, mw, mwr, ma, chain, chain_grid, stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    t_trsm_schedule = HGEMM_TRSM_CHAIN;
+    return HGEMM_OK;
   }
   int leaf_index = 0;  // position in `leaves` (the order of the solve)
   if (!in_place || alpha != 1.0f) {
@@ -1110,7 +1235,7 @@ int hgemm_trsm(const hgemm_half_t* A, int64_t lda, const hgemm_half_t* B, int64_
 size_t hgemm_trsm_workspace_size(int64_t n) {
   hg::TriLeaves leaves{};
   if (n <= 0 || n > HGEMM_MAX_DIM || !trsm_leaves(n, hg::kTrsmInverseLeaf, &leaves)) return 0;
-  return static_cast<size_t>(kTrsmInverseBytes * static_cast<uint64_t>(leaves.count));
+  return static_cast<size_t>(kTrsmInverseBytes * static_cast<uint64_t>(leaves.count) + hg::kChainSyncBytes);
 }
 
 int hgemm_trsm_ws(const hgemm_half_t* A, int64_t lda, const hgemm_half_t* B, int64_t ldb,
@@ -1248,6 +1373,15 @@ int hgemm_force_split(int split, int tile_n) {
   g_forced_split.store(split * 1024 + tile_n);
   return HGEMM_OK;
 }
+
+int hgemm_force_trsm_schedule(int schedule) {
+  if (schedule != HGEMM_TRSM_AUTO && schedule != HGEMM_TRSM_RECURSIVE && schedule != HGEMM_TRSM_CHAIN)
+    return HGEMM_ERR_INVALID_ARG;
+  g_trsm_schedule.store(schedule);
+  return HGEMM_OK;
+}
+
+int hgemm_trsm_last_schedule(void) { return t_trsm_schedule; }
 
 int hgemm_force_path(int path) {
   if (path != -1 && path != HGEMM_PATH_TC && path != HGEMM_PATH_TC_PAIR &&

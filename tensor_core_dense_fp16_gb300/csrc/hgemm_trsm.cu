@@ -473,10 +473,16 @@ __global__ void __launch_bounds__(kLeafMax, 2)
 // The first launch of its solve: waits for the previous launch on the
 // stream before anything else (the previous solve may still read W).
 // COLS right-hand sides (columns of the identity) per thread block.
+// sync (null: none): the synchronisation words of a chain launch that
+// follows, zeroed by the first block once the previous launch is done.
 template <int LEAF, int COLS>
 __global__ void __launch_bounds__(LEAF, LEAF <= 256 ? 2 : 1)
     trsm_inverse_kernel(const uint16_t* __restrict__ A, int64_t lda, uint16_t* __restrict__ W,
-                        const TriLeaves leaves) {
+                        const TriLeaves leaves, uint32_t* __restrict__ sync) {
+  if (sync && blockIdx.x == 0 && blockIdx.y == 0) {
+    grid_dependency_wait();
+    for (int i = threadIdx.x; i < kChainSyncBytes / 4; i += blockDim.x) sync[i] = 0u;
+  }
   const int b = blockIdx.y;
   const int s = static_cast<int>(leaves.size[b]);
   const int64_t j0 = static_cast<int64_t>(blockIdx.x) * COLS;
@@ -601,7 +607,7 @@ cudaError_t launch_trsm_leaf(const uint16_t* A, int64_t lda, uint16_t* X, int64_
 }
 
 cudaError_t launch_trsm_inverse(const uint16_t* A, int64_t lda, uint16_t* W, const TriLeaves& leaves,
-                                cudaStream_t stream) {
+                                uint32_t* sync, cudaStream_t stream) {
   if (leaves.count < 1 || leaves.count > kMaxLeaves) return cudaErrorInvalidValue;
   for (int b = 0; b < leaves.count; ++b)
     if (leaves.size[b] < 1 || leaves.size[b] > kTrsmInverseLeaf) return cudaErrorInvalidValue;
@@ -626,10 +632,10 @@ cudaError_t launch_trsm_inverse(const uint16_t* A, int64_t lda, uint16_t* W, con
   // 58 -> 43 µs, at 8 blocks 32 stays better)
   if (static_cast<int64_t>(leaves.count) * (LEAF / 32) <= sms) {
     PdlLaunch l(dim3(LEAF / 32, static_cast<unsigned>(leaves.count)), dim3(LEAF), leaf_smem<32, LEAF>(), stream);
-    return cudaLaunchKernelEx(&l.cfg, trsm_inverse_kernel<LEAF, 32>, A, lda, W, leaves);
+    return cudaLaunchKernelEx(&l.cfg, trsm_inverse_kernel<LEAF, 32>, A, lda, W, leaves, sync);
   }
   PdlLaunch l(dim3(LEAF / 64, static_cast<unsigned>(leaves.count)), dim3(LEAF), leaf_smem<64, LEAF>(), stream);
-  return cudaLaunchKernelEx(&l.cfg, trsm_inverse_kernel<LEAF, 64>, A, lda, W, leaves);
+  return cudaLaunchKernelEx(&l.cfg, trsm_inverse_kernel<LEAF, 64>, A, lda, W, leaves, sync);
 }
 
 cudaError_t launch_scale_copy(const uint16_t* B, int64_t ldb, uint16_t* X, int64_t ldx, int64_t n,

@@ -18,6 +18,8 @@ enum WatchdogCode : int {
   kWdEpiAccFull = 4,      // epilogue waiting for a finished accumulator
   kWdDrain = 5,           // end-of-kernel drain of in-flight copies or MMAs
   kWdReduce = 6,          // split-K owner waiting for the other slices' partials
+  kWdGridBarrier = 7,     // a CTA of a cooperative launch waiting for all others at a phase boundary
+  kWdRowGroup = 8,        // an epilogue waiting for the CTAs that read the rows it overwrites
 };
 
 // The fused epilogue ("GPU架构与CUDA", 核函数融合): each FP32 accumulator
@@ -167,11 +169,76 @@ cudaError_t launch_scale_copy(const uint16_t* B, int64_t ldb, uint16_t* X, int64
 // column-major with pitch kTrsmInverseLeaf, the transpose of the block's
 // inverse (row k of the inverse is contiguous), FP16.
 constexpr int kTrsmInverseLeaf = 512;
+// sync (may be null): kChainSyncBytes that the launch zeroes (after waiting
+// for the previous launch on the stream) for a chain launch that follows.
 cudaError_t launch_trsm_inverse(const uint16_t* A, int64_t lda, uint16_t* W, const TriLeaves& leaves,
-                                cudaStream_t stream);
+                                uint32_t* sync, cudaStream_t stream);
 // fwd: the literal orientation A·X = alpha·B (forward substitution).
 cudaError_t launch_trsm_leaf(const uint16_t* A, int64_t lda, uint16_t* X, int64_t ldx, int64_t off,
                              int s, int64_t m, int num_sms, bool chained, bool fwd, cudaStream_t stream);
+
+// The solve with inverses as one persistent, cooperative launch (see
+// hgemm_trsm_chain.cu): an optional copy phase X := alpha·B, then, for each
+// diagonal block in the order of the solve, a product phase (the block by its
+// inverse) and an update phase (every block still to be solved minus its
+// coupling to this one), grid-wide barriers between phases. Xᵀ is the m × n
+// row-major view of X (column j of X is row j).
+enum ChainKind : int { kChainCopy = 0, kChainProduct = 1, kChainUpdate = 2 };
+enum ChainMap : int { kChainMapW = 0, kChainMapWRagged = 1, kChainMapA = 2 };
+constexpr int kChainMaxLeaves = 32;
+constexpr int kChainMaxPhases = 1 + 2 * kChainMaxLeaves;
+// Words of the workspace's synchronisation area (zeroed by the inverses'
+// launch before the chain starts): the grid barrier's arrival count, the
+// launch's abort flag, then one counter per 64 rows of Xᵀ.
+constexpr int kChainSyncBarrier = 0;
+constexpr int kChainSyncAbort = 1;
+constexpr int kChainSyncRowGroup0 = 32;
+constexpr int kChainSyncBytes = 4096;
+constexpr int kChainMaxRowGroups = kChainSyncBytes / 4 - kChainSyncRowGroup0;
+
+// One phase. Tiles are bm × bn (bm 64 or 128, bn 64, 128 or 256) over
+// output columns [n0, n_end) of Xᵀ and all m rows; the first operand is Xᵀ,
+// columns k0 + 64·kk for kk < ksteps; the second operand's box coordinates
+// at k-step kk of a tile whose first column is n0 + nc are
+// (k, n) = (b_kbase + 64·kk, b_nbase + nc) in its map (b_map), stored
+// N-contiguous when b_mn. Product phases: every 64-row group of Xᵀ has a
+// counter that each tile covering it raises once its first operand has
+// landed; a tile stores its rows only when their counters reach rg_target.
+struct ChainPhase {
+  int flags;  // kind | b_map << 2 | b_mn << 4 | (bm / 64) << 5 | (bn / 64) << 8
+  int n0, n_end;
+  int k0, ksteps;
+  int b_kbase, b_nbase;
+  uint32_t rg_target;
+};
+__host__ __device__ constexpr int chain_flags(int kind, int b_map, int b_mn, int bm, int bn) {
+  return kind | (b_map << 2) | (b_mn << 4) | ((bm / 64) << 5) | ((bn / 64) << 8);
+}
+
+struct ChainArgs {
+  uint16_t* X;
+  int64_t ldx;
+  const uint16_t* B;  // the right-hand side (the copy phase), may be X
+  int64_t ldb;
+  float alpha;
+  int m, n;
+  int copy_vec;       // the copy phase moves 8 elements per access
+  uint32_t* sync;     // kChainSyncBytes in the workspace
+  int* status;
+  unsigned long long timeout_ns;
+  int inject;
+  int num_phases;
+  ChainPhase phase[kChainMaxPhases];
+};
+
+// x: Xᵀ (m × n, pitch ldx); w: the workspace's inverses (count·512 rows of
+// 512); wr: the ragged last block's inverse (s × s, pitch 512), or a copy of w;
+// a: the triangle as stored (n columns of n rows, pitch lda). Every map has
+// 64 × 64 boxes with 128-byte swizzling.
+cudaError_t launch_trsm_chain(const CUtensorMap& x, const CUtensorMap& w, const CUtensorMap& wr,
+                              const CUtensorMap& a, const ChainArgs& args, int grid, cudaStream_t stream);
+// Largest grid of the chain kernel that is co-resident on this device (0 on error).
+int chain_max_grid(int num_sms);
 
 // Address of the device watchdog word on the current device.
 cudaError_t status_word_address(int** addr);
@@ -185,7 +252,8 @@ cudaError_t debug_word_skinny(int** out);
 cudaError_t debug_word_generic(int** out);
 cudaError_t debug_word_trsm(int** out);
 cudaError_t debug_word_trileaf(int** out);
-constexpr int kDebugWords = 7;
+cudaError_t debug_word_chain(int** out);
+constexpr int kDebugWords = 8;
 
 // Co-residency limits of the cluster kernels on one device, measured once
 // (or nominal GB300 figures when no device has been queried).

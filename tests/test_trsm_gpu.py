@@ -28,11 +28,41 @@ def trsm_inputs(n, m, seed, c=1.0):
     return np.ascontiguousarray(a_col.T), np.ascontiguousarray(b_col.T)
 
 
+SCHEDULES = [False, "rec", "chain"]
+
+
+class schedule:
+    """Forces a TRSM schedule for the duration of a with-block: "rec" the
+    recursion's launches, "chain" the one persistent launch wherever it can
+    run; anything else the automatic choice."""
+
+    def __init__(self, ws):
+        self.value = {"rec": tc.HGEMM_TRSM_RECURSIVE, "chain": tc.HGEMM_TRSM_CHAIN}.get(ws, tc.HGEMM_TRSM_AUTO)
+
+    def __enter__(self):
+        tc.hgemm_force_trsm_schedule(self.value)
+
+    def __exit__(self, *exc):
+        tc.hgemm_force_trsm_schedule(tc.HGEMM_TRSM_AUTO)
+
+
+def expected_schedule(ws, lda, ldx):
+    """The schedule a solve must report: no workspace, or X not suited to
+    TMA, substitution; "rec" (or a triangle TMA cannot read) the recursion;
+    "chain" the one launch."""
+    if not ws or ldx % 8:
+        return tc.HGEMM_TRSM_SUBSTITUTION
+    if ws == "rec" or lda % 8:
+        return tc.HGEMM_TRSM_RECURSIVE
+    return tc.HGEMM_TRSM_CHAIN
+
+
 def run_trsm(a, b, alpha=1.0, pad=(0, 0, 0), poison_upper=False, in_place=False, ws=False, op=None):
     """Column-major device buffers with pitches n + pad; X (n, m) comes back.
     ws: through hgemm_trsm_ws, with a workspace of the reported size followed
-    by a sentinel band that must stay untouched. op: through hgemm_trsm_op
-    with that orientation (with the workspace when ws)."""
+    by a sentinel band that must stay untouched ("rec" / "chain": that
+    schedule forced, and checked to be the one taken). op: through
+    hgemm_trsm_op with that orientation (with the workspace when ws)."""
     torch = torch_cuda()
     n, m = b.shape
     lda, ldb, ldx = n + pad[0], n + pad[1], n + pad[2]
@@ -52,12 +82,15 @@ def run_trsm(a, b, alpha=1.0, pad=(0, 0, 0), poison_upper=False, in_place=False,
         dx = to_device(np.full((m, ldx), 5.0, np.float16))
     if ws:
         need = tc.hgemm_trsm_workspace_size(n)
-        assert need > 0 and need % (2 * 512 * 512) == 0
+        assert need > 4096 and (need - 4096) % (2 * 512 * 512) == 0
         work = torch.full((need + 4096,), 0x5A, dtype=torch.uint8, device="cuda")
-        if op is None:
-            tc.hgemm_trsm_ws(da, lda, db, ldb, dx, ldx, n, m, alpha, work, need)
-        else:
-            tc.hgemm_trsm_op(op, da, lda, db, ldb, dx, ldx, n, m, alpha, work, need)
+        with schedule(ws):
+            if op is None:
+                tc.hgemm_trsm_ws(da, lda, db, ldb, dx, ldx, n, m, alpha, work, need)
+            else:
+                tc.hgemm_trsm_op(op, da, lda, db, ldb, dx, ldx, n, m, alpha, work, need)
+        if ws in ("rec", "chain"):
+            assert tc.hgemm_trsm_last_schedule() == expected_schedule(ws, lda, ldx)
     elif op is not None:
         tc.hgemm_trsm_op(op, da, lda, db, ldb, dx, ldx, n, m, alpha, None, 0)
     else:
@@ -74,7 +107,7 @@ def run_trsm(a, b, alpha=1.0, pad=(0, 0, 0), poison_upper=False, in_place=False,
     return np.ascontiguousarray(out[:, :n].T)
 
 
-@pytest.mark.parametrize("ws", [False, True])
+@pytest.mark.parametrize("ws", SCHEDULES)
 @pytest.mark.parametrize("n,m", [(1, 1), (64, 32), (200, 7), (256, 100), (257, 64), (300, 136),
                                  (512, 256), (1000, 128), (4096, 256)])
 def test_trsm_matches_oracle(n, m, ws):
@@ -86,7 +119,7 @@ def test_trsm_matches_oracle(n, m, ws):
     assert_close(run_trsm(a, b, ws=ws), ref, what=f"trsm {n}x{m} ws={ws}")
 
 
-@pytest.mark.parametrize("ws", [False, True])
+@pytest.mark.parametrize("ws", SCHEDULES)
 @pytest.mark.parametrize("m", [4096, 8192, 8195])
 def test_trsm_leaf_widths(m, ws):
     """Many right-hand sides: the diagonal solves take 16 and 32 of them per
@@ -98,7 +131,7 @@ def test_trsm_leaf_widths(m, ws):
     assert_close(run_trsm(a, b, ws=ws), ref, what=f"trsm {n}x{m} ws={ws}")
 
 
-@pytest.mark.parametrize("ws", [False, True])
+@pytest.mark.parametrize("ws", SCHEDULES)
 def test_trsm_reads_only_the_lower_triangle(ws):
     n, m = 704, 96
     a, b = trsm_inputs(n, m, seed=7)
@@ -106,7 +139,7 @@ def test_trsm_reads_only_the_lower_triangle(ws):
     assert_close(run_trsm(a, b, poison_upper=True, ws=ws), ref, what=f"NaN above the diagonal ws={ws}")
 
 
-@pytest.mark.parametrize("ws", [False, True])
+@pytest.mark.parametrize("ws", SCHEDULES)
 @pytest.mark.parametrize("pad", [(8, 16, 8), (3, 5, 1)])
 def test_trsm_pitches_and_alpha(pad, ws):
     """Wider pitches (multiples of 8: tensor-core updates; odd ones: the
@@ -118,7 +151,7 @@ def test_trsm_pitches_and_alpha(pad, ws):
     assert_close(run_trsm(a, b, alpha=-1.5, pad=pad, ws=ws), ref, what=f"trsm pad {pad} ws={ws}")
 
 
-@pytest.mark.parametrize("ws", [False, True])
+@pytest.mark.parametrize("ws", SCHEDULES)
 @pytest.mark.parametrize("alpha", [1.0, 0.25])
 def test_trsm_in_place(alpha, ws):
     n, m = 800, 40
@@ -128,7 +161,7 @@ def test_trsm_in_place(alpha, ws):
                  what=f"trsm in place alpha {alpha} ws={ws}")
 
 
-@pytest.mark.parametrize("ws", [False, True])
+@pytest.mark.parametrize("ws", SCHEDULES)
 def test_trsm_residual_identity(ws):
     """A = I: X = alpha·B rounded once, exactly (the inverses are the
     identity, so the products by them are exact too)."""
@@ -139,7 +172,7 @@ def test_trsm_residual_identity(ws):
     assert np.array_equal(got, (b.astype(np.float32) * 0.5).astype(np.float16))
 
 
-@pytest.mark.parametrize("ws", [False, True])
+@pytest.mark.parametrize("ws", SCHEDULES)
 def test_trsm_repeatable(ws):
     n, m = 1024, 64
     a, b = trsm_inputs(n, m, seed=3)
@@ -148,7 +181,7 @@ def test_trsm_repeatable(ws):
         assert np.array_equal(run_trsm(a, b, ws=ws).view(np.uint16), first.view(np.uint16))
 
 
-@pytest.mark.parametrize("ws", [False, True])
+@pytest.mark.parametrize("ws", SCHEDULES)
 def test_trsm_8192_sampled_columns(ws):
     """The 8192×8192 workload in the benchmark's launch configuration: column
     j of X depends on column j of B alone, so the oracle solves a sample of
@@ -160,7 +193,9 @@ def test_trsm_8192_sampled_columns(ws):
     dx = torch.empty((m, n), dtype=torch.float16, device="cuda")
     if ws:
         work = torch.empty(tc.hgemm_trsm_workspace_size(n), dtype=torch.uint8, device="cuda")
-        tc.hgemm_trsm_ws(da, n, db, n, dx, n, n, m, 1.0, work)
+        with schedule(ws):
+            tc.hgemm_trsm_ws(da, n, db, n, dx, n, n, m, 1.0, work)
+        assert tc.hgemm_trsm_last_schedule() == expected_schedule(ws, n, n)
     else:
         tc.hgemm_trsm(da, n, db, n, dx, n, n, m, 1.0)
     assert tc.hgemm_device_status() == tc.HGEMM_OK
@@ -171,7 +206,7 @@ def test_trsm_8192_sampled_columns(ws):
     assert_close(got, ref, what="trsm_8192 sampled columns")
 
 
-@pytest.mark.parametrize("ws", [False, True])
+@pytest.mark.parametrize("ws", SCHEDULES)
 @pytest.mark.parametrize("c", [16, 128, 512])
 def test_trsm_weaker_dominance(c, ws):
     """Triangles that are not diagonally dominant: strict lower part
@@ -187,7 +222,7 @@ def test_trsm_weaker_dominance(c, ws):
     assert_close(run_trsm(a, b, ws=ws), ref, what=f"trsm c={c} ws={ws}")
 
 
-@pytest.mark.parametrize("ws", [False, True])
+@pytest.mark.parametrize("ws", SCHEDULES)
 def test_trsm_ill_conditioned_backward_error(ws):
     """n = 1024 with c = 512 (entries up to 1/2: the solution grows to ~350
     from a right-hand side below 1) is past the envelope: both entry points
@@ -208,13 +243,14 @@ def test_trsm_ill_conditioned_backward_error(ws):
 
 
 def test_trsm_workspace_arguments():
-    """Workspace size per diagonal block, and the arguments hgemm_trsm_ws
-    refuses: no workspace, one too small, a misaligned one, one overlapping X."""
+    """Workspace size per diagonal block (plus the one launch's synchronisation
+    words), and the arguments hgemm_trsm_ws refuses: no workspace, one smaller
+    than the inverses, a misaligned one, one overlapping X."""
     torch = torch_cuda()
     assert tc.hgemm_trsm_workspace_size(0) == 0
-    assert tc.hgemm_trsm_workspace_size(256) == 2 * 512 * 512
-    assert tc.hgemm_trsm_workspace_size(8192) == 16 * 2 * 512 * 512
-    assert tc.hgemm_trsm_workspace_size(1000) == 2 * 2 * 512 * 512   # blocks of 512 and 488
+    assert tc.hgemm_trsm_workspace_size(256) == 2 * 512 * 512 + 4096
+    assert tc.hgemm_trsm_workspace_size(8192) == 16 * 2 * 512 * 512 + 4096
+    assert tc.hgemm_trsm_workspace_size(1000) == 2 * 2 * 512 * 512 + 4096   # blocks of 512 and 488
     n, m = 512, 64
     a, b = trsm_inputs(n, m, seed=5)
     da, db = to_device(np.ascontiguousarray(a.T)), to_device(np.ascontiguousarray(b.T))
@@ -223,8 +259,16 @@ def test_trsm_workspace_arguments():
     work = torch.empty(need + 64, dtype=torch.uint8, device="cuda")
     with pytest.raises(tc.HgemmError):
         tc.hgemm_trsm_ws(da, n, db, n, dx, n, n, m, 1.0, None, need)
+    # the inverses alone: accepted, and solved by the recursion's launches (the
+    # one-launch schedule needs the synchronisation words after them)
+    inverses = need - 4096
     with pytest.raises(tc.HgemmError):
-        tc.hgemm_trsm_ws(da, n, db, n, dx, n, n, m, 1.0, work, need - 1)
+        tc.hgemm_trsm_ws(da, n, db, n, dx, n, n, m, 1.0, work, inverses - 1)
+    tc.hgemm_trsm_ws(da, n, db, n, dx, n, n, m, 1.0, work, inverses)
+    assert tc.hgemm_trsm_last_schedule() == tc.HGEMM_TRSM_RECURSIVE
+    tc.hgemm_trsm_ws(da, n, db, n, dx, n, n, m, 1.0, work, need)
+    assert tc.hgemm_trsm_last_schedule() == tc.HGEMM_TRSM_CHAIN
+    assert tc.hgemm_device_status() == tc.HGEMM_OK
     with pytest.raises(tc.HgemmError):
         tc.hgemm_trsm_ws(da, n, db, n, dx, n, n, m, 1.0, work.data_ptr() + 8, need)
     big = torch.empty((m, n + need // 2), dtype=torch.float16, device="cuda")
@@ -238,7 +282,7 @@ def test_trsm_workspace_arguments():
 # strict lower part sums to less than 1 <= the diagonal), so forward
 # substitution does not amplify errors either and the same tolerance applies.
 
-@pytest.mark.parametrize("ws", [False, True])
+@pytest.mark.parametrize("ws", SCHEDULES)
 @pytest.mark.parametrize("n,m", [(1, 1), (64, 32), (200, 7), (256, 100), (257, 64), (300, 136),
                                  (512, 256), (1000, 128), (4096, 256)])
 def test_trsm_n_matches_oracle(n, m, ws):
@@ -251,7 +295,7 @@ def test_trsm_n_matches_oracle(n, m, ws):
     assert_close(run_trsm(a, b, ws=ws, op=tc.HGEMM_OP_N), ref, what=f"trsm_n {n}x{m} ws={ws}")
 
 
-@pytest.mark.parametrize("ws", [False, True])
+@pytest.mark.parametrize("ws", SCHEDULES)
 @pytest.mark.parametrize("m", [4096, 8195])
 def test_trsm_n_leaf_widths(m, ws):
     n = 300
@@ -260,7 +304,7 @@ def test_trsm_n_leaf_widths(m, ws):
     assert_close(run_trsm(a, b, ws=ws, op=tc.HGEMM_OP_N), ref, what=f"trsm_n {n}x{m} ws={ws}")
 
 
-@pytest.mark.parametrize("ws", [False, True])
+@pytest.mark.parametrize("ws", SCHEDULES)
 def test_trsm_n_reads_only_the_lower_triangle(ws):
     n, m = 704, 96
     a, b = trsm_inputs(n, m, seed=77)
@@ -269,7 +313,7 @@ def test_trsm_n_reads_only_the_lower_triangle(ws):
                  what=f"trsm_n NaN above the diagonal ws={ws}")
 
 
-@pytest.mark.parametrize("ws", [False, True])
+@pytest.mark.parametrize("ws", SCHEDULES)
 @pytest.mark.parametrize("pad", [(8, 16, 8), (3, 5, 1)])
 def test_trsm_n_pitches_and_alpha(pad, ws):
     """Odd pitches: the leaf kernel's direct loads of A's rows and the
@@ -281,7 +325,7 @@ def test_trsm_n_pitches_and_alpha(pad, ws):
                  what=f"trsm_n pad {pad} ws={ws}")
 
 
-@pytest.mark.parametrize("ws", [False, True])
+@pytest.mark.parametrize("ws", SCHEDULES)
 def test_trsm_n_in_place(ws):
     n, m = 800, 40
     a, b = trsm_inputs(n, m, seed=29)
@@ -290,7 +334,7 @@ def test_trsm_n_in_place(ws):
                  what=f"trsm_n in place ws={ws}")
 
 
-@pytest.mark.parametrize("ws", [False, True])
+@pytest.mark.parametrize("ws", SCHEDULES)
 def test_trsm_op_t_is_hgemm_trsm(ws):
     """HGEMM_OP_T is the same solve as hgemm_trsm / hgemm_trsm_ws, bit for bit."""
     n, m = 1000, 64

@@ -75,3 +75,37 @@ def test_withheld_arrival_in_the_trmm_leaf_kernel():
     torch.cuda.synchronize()
     ref = oracle.trmm(a, b)
     assert_close(np.ascontiguousarray(dc.cpu().numpy().T), ref, what="trmm after timeout")
+
+
+@pytest.mark.gpu
+def test_withheld_arrival_in_the_one_launch_solve():
+    """The persistent TRSM launch (hgemm_trsm_ws, chain schedule): every
+    CTA's producer withholds its first arrival, so the MMA issuers' waits run
+    out; each CTA raises its abort flag, the launch's abort word reaches the
+    CTAs waiting at the grid barrier, and all drain, free TMEM and return.
+    Afterwards the same context solves correctly."""
+    torch = torch_cuda()
+    n, m = 1024, 64
+    a_col, b_col = synth.trsm_operands(n, m, 43)
+    da, db = to_device(a_col), to_device(b_col)
+    dx = torch.zeros((m, n), dtype=torch.float16, device="cuda")
+    work = torch.empty(tc.hgemm_trsm_workspace_size(n), dtype=torch.uint8, device="cuda")
+    assert tc.hgemm_device_status() == tc.HGEMM_OK
+    tc.hgemm_set_wait_timeout(50_000_000)   # 50 ms per wait
+    tc.hgemm_debug_inject(tc.HGEMM_INJECT_DROP_ARRIVAL)
+    tc.hgemm_force_trsm_schedule(tc.HGEMM_TRSM_CHAIN)
+    try:
+        tc.hgemm_trsm_ws(da, n, db, n, dx, n, n, m, 1.0, work)
+        assert tc.hgemm_trsm_last_schedule() == tc.HGEMM_TRSM_CHAIN
+        assert tc.hgemm_device_status() == tc.HGEMM_ERR_TIMEOUT
+        assert tc.hgemm_device_status() == tc.HGEMM_OK
+    finally:
+        tc.hgemm_debug_inject(tc.HGEMM_INJECT_NONE)
+        tc.hgemm_set_wait_timeout(0)
+        tc.hgemm_force_trsm_schedule(tc.HGEMM_TRSM_AUTO)
+    tc.hgemm_trsm_ws(da, n, db, n, dx, n, n, m, 1.0, work)
+    assert tc.hgemm_trsm_last_schedule() == tc.HGEMM_TRSM_CHAIN
+    assert tc.hgemm_device_status() == tc.HGEMM_OK
+    torch.cuda.synchronize()
+    ref = oracle.trsm(a_col.T, b_col.T)
+    assert_close(np.ascontiguousarray(dx.cpu().numpy().T), ref, what="trsm after a timeout")
