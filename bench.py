@@ -164,7 +164,10 @@ TRI_OPS = {
 # hgemm_trsm_last_schedule's values, by name (bench.py reports the schedule a
 # solve took), and the kernels of the one-launch schedule.
 SCHEDULE_NAMES = {1: "substitution", 2: "recursive (products by the inverses and GEMM updates, one launch each)",
-                  3: "chain (the inverses' launch, then one persistent cooperative launch)"}
+                  4: "chain, fused plan (the inverses' launch, then one persistent cooperative launch, "
+                     "one phase per diagonal block)",
+                  5: "chain, split plan (the inverses' launch, then one persistent cooperative launch, "
+                     "a product phase and an update phase per diagonal block)"}
 CHAIN_KERNELS = ("trsm_inverse_kernel (the inverses of the diagonal blocks of 512) + trsm_chain_kernel (one "
                  "persistent cooperative launch: X := B, then per block its product by the inverse and the "
                  "update of every block still to be solved, grid barriers between the phases)")
@@ -733,7 +736,7 @@ def run_tri_ours(args, spec, a_col, b_col, world, rank, local):
         raise RuntimeError("a kernel wait timed out during warm-up")
     # the solve's schedule (hgemm_trsm_ws picks it from the shape)
     schedule = tc.hgemm_trsm_last_schedule() if op in ("trsm", "trsm_n") else None
-    chain = schedule == tc.HGEMM_TRSM_CHAIN
+    chain = schedule in (tc.HGEMM_TRSM_CHAIN_FUSED, tc.HGEMM_TRSM_CHAIN_SPLIT)
     times_ms, clocks = timed_region(torch, dev, local, stream, step, flush, args.steps, dist)
     if tc.hgemm_device_status(stream) != tc.HGEMM_OK:
         raise RuntimeError("a kernel wait timed out in the timed region")

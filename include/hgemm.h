@@ -223,9 +223,9 @@ HGEMM_API int hgemm_trsm(const hgemm_half_t *A, int64_t lda, const hgemm_half_t 
 /*
  * hgemm_trsm_workspace_size — bytes of device workspace hgemm_trsm_ws uses
  * for a triangle of order n: 512 KiB per diagonal block of order ≤ 512 of
- * the recursion, plus 4 KiB of synchronisation words for the one-launch
- * schedule (n = 8192: 16 blocks, 8 MiB + 4 KiB). 0 for n ≤ 0 or n beyond
- * 128 such blocks. Pure host logic.
+ * the recursion, plus, for the one-launch schedule, one spare block of 512
+ * KiB and 4 KiB of synchronisation words (n = 8192: 16 blocks, 8.5 MiB +
+ * 4 KiB). 0 for n ≤ 0 or n beyond 128 such blocks. Pure host logic.
  */
 HGEMM_API size_t hgemm_trsm_workspace_size(int64_t n);
 
@@ -243,22 +243,26 @@ HGEMM_API size_t hgemm_trsm_workspace_size(int64_t n);
  * the substitution kernel). The substitution then happens once per block for
  * the identity rather than per right-hand side, and the deepest updates of
  * the recursion are inside the inverses.
- * Schedule: when m ≤ 1024, the workspace also holds the synchronisation
- * words (the full hgemm_trsm_workspace_size(n)), A is 16-byte aligned with
- * lda a multiple of 8 and the recursion has at most 32 diagonal blocks,
- * everything after the inverses runs as ONE persistent cooperative launch: the blocks in the
- * recursion's order, each solved by its product, then each block's
- * contribution subtracted at once from all blocks still to be solved (the
- * recursion's update sums, split per block: right-looking), grid-wide
- * barriers between these phases. Otherwise (a workspace of exactly the
- * inverses' size, as earlier versions asked for, or the limits above) the
- * recursion runs as a sequence of launches (products by the inverses, GEMM
- * updates). hgemm_force_trsm_schedule chooses for testing;
- * hgemm_trsm_last_schedule tells which one a call took.
+ * Schedule: when m ≤ 1024, the workspace is the full
+ * hgemm_trsm_workspace_size(n), A is 16-byte aligned with lda a multiple of
+ * 8 and the recursion has at most 16 diagonal blocks (n ≤ 8192),
+ * everything after the inverses runs as ONE persistent cooperative launch,
+ * one phase per block in the recursion's order with grid-wide barriers
+ * between them: phase k solves block k as one product,
+ * X_kᵀ := T_kᵀ·L_k⁻¹ − X_{k−1}ᵀ·M_k, where T_k is block k's right-hand side
+ * after the updates from the blocks solved up to two before it and
+ * M_k = C_k·L_k⁻¹ (C_k the part of A coupling block k−1 to block k,
+ * computed one phase ahead into a spare slot of the workspace), and
+ * subtracts X_{k−1}'s contribution from every block after k at once (the
+ * recursion's update sums, split per block: right-looking). Otherwise (a
+ * workspace of only the inverses' size, as earlier versions asked for, or
+ * the limits above) the recursion runs as a sequence of launches (products
+ * by the inverses, GEMM updates). hgemm_force_trsm_schedule chooses for
+ * testing; hgemm_trsm_last_schedule tells which one a call took.
  * Rounding: each solved block is rounded once to FP16, the inverse once
  * more; X is rounded after every update it receives (the recursion: once per
  * level whose first half holds the block; the one launch: once per block
- * solved before it). A null workspace, one too small or not 16-byte
+ * solved two or more before it, and M_k once). A null workspace, one too small or not 16-byte
  * aligned is HGEMM_ERR_INVALID_ARG; X not suited to the tensor-core path, or
  * a path forced by hgemm_force_path, solves as hgemm_trsm does.
  * Accuracy against hgemm_trsm: rounding L_b⁻¹ to FP16 adds at most
@@ -316,27 +320,37 @@ HGEMM_API int hgemm_trsm_op(int op, const hgemm_half_t *A, int64_t lda, const hg
  * launches with every diagonal block of order ≤ 256 solved by substitution;
  * RECURSIVE: the recursion's launches, blocks of order ≤ 512 solved by
  * their inverses; CHAIN: the inverses' launch, then one persistent launch
- * (hgemm_trsm_ws).
+ * (hgemm_trsm_ws), in one of two plans: CHAIN_FUSED, one phase per block
+ * (its product folds in the update from the block before through M_k),
+ * or CHAIN_SPLIT, two phases per block (the product by the inverse, then
+ * the update of every later block); the library takes the plan its cost
+ * model of the two finds faster (fused for few right-hand sides).
  */
 #define HGEMM_TRSM_AUTO 0
 #define HGEMM_TRSM_SUBSTITUTION 1
 #define HGEMM_TRSM_RECURSIVE 2
 #define HGEMM_TRSM_CHAIN 3
+#define HGEMM_TRSM_CHAIN_FUSED 4
+#define HGEMM_TRSM_CHAIN_SPLIT 5
 
 /*
  * hgemm_force_trsm_schedule — testing and profiling aid: HGEMM_TRSM_RECURSIVE
  * keeps later solves with a workspace on the recursion's launches;
  * HGEMM_TRSM_CHAIN takes the one-launch schedule wherever it can run (also
  * past m = 1024, where it is slower: its product phases must fit one wave
- * of tiles, m up to ~9,700); HGEMM_TRSM_AUTO (the default) chooses as
- * hgemm_trsm_ws describes. Returns HGEMM_OK, or HGEMM_ERR_INVALID_ARG for
- * another value. Process-wide, like hgemm_force_path.
+ * of tiles, m up to ~9,700; n ≤ 8192) with the plan of the library's
+ * choice, HGEMM_TRSM_CHAIN_FUSED or HGEMM_TRSM_CHAIN_SPLIT with that plan;
+ * HGEMM_TRSM_AUTO (the default) chooses as hgemm_trsm_ws describes.
+ * Returns HGEMM_OK, or HGEMM_ERR_INVALID_ARG for another value.
+ * Process-wide, like hgemm_force_path.
  */
 HGEMM_API int hgemm_force_trsm_schedule(int schedule);
 
 /*
  * hgemm_trsm_last_schedule — the HGEMM_TRSM_* schedule of the last
- * triangular solve enqueued on this host thread (0 before any). Host logic.
+ * triangular solve enqueued on this host thread (0 before any; a chain
+ * reports its plan, HGEMM_TRSM_CHAIN_FUSED or HGEMM_TRSM_CHAIN_SPLIT). Host
+ * logic.
  */
 HGEMM_API int hgemm_trsm_last_schedule(void);
 
@@ -349,7 +363,7 @@ HGEMM_API int hgemm_trsm_last_schedule(void);
  * an addition for such callers.
  *
  * Same system, operands, results and return values as hgemm_trsm_ws, whose
- * workspace here is a fixed array of HGEMM_TRSM_NOALLOC_MAX_BYTES (8 MiB +
+ * workspace here is a fixed array of HGEMM_TRSM_NOALLOC_MAX_BYTES (8.5 MiB +
  * 4 KiB) inside the library, present on every device that loads the library until
  * the process exits. Nothing is allocated: no cudaMalloc or cudaFree, no
  * allocating library call. Limit: triangles whose recursion has at most 16
@@ -370,7 +384,7 @@ HGEMM_API int hgemm_trsm_last_schedule(void);
  * overlaps on the GPU (other streams, other host threads) race on it and
  * must be ordered by the caller, e.g. issued on one stream.
  */
-#define HGEMM_TRSM_NOALLOC_MAX_BYTES ((8u << 20) + 4096u)
+#define HGEMM_TRSM_NOALLOC_MAX_BYTES ((17u << 19) + 4096u)
 HGEMM_API int hgemm_trsm_noalloc(const hgemm_half_t *A, int64_t lda, const hgemm_half_t *B, int64_t ldb,
                        hgemm_half_t *X, int64_t ldx, int64_t n, int64_t m, float alpha,
                        cudaStream_t stream);

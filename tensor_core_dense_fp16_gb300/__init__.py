@@ -31,7 +31,7 @@ __all__ = [
     "hgemm_status_string", "hgemm_version", "hgemm_set_wait_timeout", "hgemm_debug_inject",
     "hgemm_force_split", "hgemm_launch_floor", "hgemm_ex", "hgemm_strided", "hgemm_trmm", "hgemm_trsm", "hgemm_trsm_ws", "hgemm_trsm_workspace_size", "hgemm_trsm_noalloc", "hgemm_trsm_op", "HGEMM_OP_N", "HGEMM_OP_T", "hgemm_layout", "HGEMM_TRMM_MAX_N", "HGEMM_TRSM_NOALLOC_MAX_BYTES",
     "hgemm_force_trsm_schedule", "hgemm_trsm_last_schedule", "HGEMM_TRSM_AUTO", "HGEMM_TRSM_SUBSTITUTION",
-    "HGEMM_TRSM_RECURSIVE", "HGEMM_TRSM_CHAIN",
+    "HGEMM_TRSM_RECURSIVE", "HGEMM_TRSM_CHAIN", "HGEMM_TRSM_CHAIN_FUSED", "HGEMM_TRSM_CHAIN_SPLIT",
     "HGEMM_A_ROW_MAJOR", "HGEMM_A_COL_MAJOR", "HGEMM_B_COL_MAJOR", "HGEMM_B_ROW_MAJOR",
     "HGEMM_INJECT_NONE", "HGEMM_INJECT_DROP_ARRIVAL", "matmul",
 ]
@@ -44,11 +44,13 @@ HGEMM_ERR_CUDA = -4
 HGEMM_ERR_TIMEOUT = -5
 HGEMM_ERR_DEBUG_CHECK = -6
 HGEMM_TRMM_MAX_N = 16384
-HGEMM_TRSM_NOALLOC_MAX_BYTES = (8 << 20) + 4096
+HGEMM_TRSM_NOALLOC_MAX_BYTES = (17 << 19) + 4096
 HGEMM_TRSM_AUTO = 0
 HGEMM_TRSM_SUBSTITUTION = 1
 HGEMM_TRSM_RECURSIVE = 2
 HGEMM_TRSM_CHAIN = 3
+HGEMM_TRSM_CHAIN_FUSED = 4
+HGEMM_TRSM_CHAIN_SPLIT = 5
 HGEMM_OP_N = 0
 HGEMM_OP_T = 1
 HGEMM_A_ROW_MAJOR = 0
@@ -327,8 +329,9 @@ def hgemm_force_path(path: int) -> None:
 
 def hgemm_force_trsm_schedule(schedule: int) -> None:
     """Testing aid: HGEMM_TRSM_RECURSIVE keeps solves with a workspace on the
-    recursion's launches; HGEMM_TRSM_AUTO / HGEMM_TRSM_CHAIN allow the one
-    persistent launch."""
+    recursion's launches; HGEMM_TRSM_CHAIN (either plan), HGEMM_TRSM_CHAIN_FUSED
+    or HGEMM_TRSM_CHAIN_SPLIT force the one persistent launch; HGEMM_TRSM_AUTO
+    chooses."""
     _raise_on(load().hgemm_force_trsm_schedule(schedule), "hgemm_force_trsm_schedule")
 
 

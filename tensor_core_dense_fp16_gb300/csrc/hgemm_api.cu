@@ -979,76 +979,247 @@ constexpr int64_t kChainAutoMaxM = 1024;
 // one inverse in the workspace: FP16, kTrsmInverseLeaf² (512 KiB)
 constexpr uint64_t kTrsmInverseBytes = 2ull * hg::kTrsmInverseLeaf * hg::kTrsmInverseLeaf;
 
-// The tile of one chain phase: all m rows × ncols columns with K steps of
-// 64 on `grid` CTAs. The operand bytes an SM takes in are (bm + bn) per K
-// element per tile, so the cost is waves × (bm + bn); ties go to the larger
-// tile. A product phase's tiles must all run at once (tiles ≤ grid).
-// Returns false when no tile fits.
-bool chain_tile(int64_t m, int64_t ncols, int grid, bool product, int* bm, int* bn) {
+// ---- the chain schedule's plan (see hgemm_trsm_chain.cu)
+//
+// Cost model of a tile (measured on the chain kernel): an MMA issuer takes
+// ~0.24 µs per 64-deep K step of an N ≤ 128 tile (~61-65 cycles per
+// M=128 MMA instruction whatever N up to 128, plus its wait) and ~0.40 µs at
+// N = 256; an SM takes in operands at ~100 GB/s, (bm + bn)·128 bytes per
+// step. A phase costs the longest CTA's tiles plus ~3 µs of barrier, launch
+// of the first copies and epilogue.
+double chain_step_us(int bm, int bn) {
+  const double mma = bn <= 128 ? 0.24 : 0.40;
+  const double intake = (bm + bn) * 128.0 / 1.0e5;
+  return mma > intake ? mma : intake;
+}
+constexpr double kChainPhaseUs = 3.0;
+
+struct ChainTile {
+  int bm, bn, tiles;
+  double us;  // one tile
+};
+
+// The tile shapes of a group of rows × ncols outputs with ksteps K steps.
+int chain_tiles(int64_t rows, int64_t ncols, int ksteps, ChainTile (&out)[6]) {
   static constexpr int kBm[2] = {128, 64};
   static constexpr int kBn[3] = {256, 128, 64};
-  int64_t best = -1;
+  int n = 0;
   for (int i : kBm)
-    for (int j : kBn) {
-      const int64_t tiles = ((m + i - 1) / i) * ((ncols + j - 1) / j);
-      if (product && tiles > grid) continue;
-      const int64_t cost = ((tiles + grid - 1) / grid) * (i + j);
-      if (best < 0 || cost < best) {
-        best = cost;
-        *bm = i;
-        *bn = j;
-      }
-    }
-  return best >= 0;
+    for (int j : kBn)
+      out[n++] = ChainTile{i, j, static_cast<int>(((rows + i - 1) / i) * ((ncols + j - 1) / j)),
+                           ksteps * chain_step_us(i, j)};
+  return n;
 }
 
-// Plans the chain launch of a solve whose inverses are (or will be) in W:
-// fills args (phases, operands) and *grid. False when the chain does not
-// apply (too many blocks or rows, a product phase wider than the grid).
-bool chain_plan(const hg::TriLeaves& leaves, int64_t n, int64_t m, bool copy, bool fwd, int max_grid,
-                hg::ChainArgs* args, int* grid, int* ragged) {
-  if (leaves.count < 1 || leaves.count > hg::kChainMaxLeaves || max_grid < 1) return false;
-  if (m < 1 || (m + 63) / 64 > hg::kChainMaxRowGroups || n > (int64_t(1) << 30)) return false;
-  int np = 0, max_tiles = 1;
-  uint32_t target = 0;
-  *ragged = -1;
-  if (copy) args->phase[np++] = hg::ChainPhase{hg::chain_flags(hg::kChainCopy, 0, 0, 0, 0), 0, 0, 0, 0, 0, 0, 0};
-  for (int b = 0; b < leaves.count; ++b) {
-    const int64_t off = leaves.off[b], sz = leaves.size[b];
-    const int ksteps = static_cast<int>((sz + 63) / 64);
-    const bool rag = sz % 64 != 0;  // only the block that ends at n (the edge of every map)
-    if (rag) {
-      if (off + sz != n || *ragged >= 0) return false;
-      *ragged = b;
-    }
-    int bm = 0, bn = 0;
-    if (!chain_tile(m, sz, max_grid, true, &bm, &bn)) return false;
-    const int64_t pn = (sz + bn - 1) / bn;
-    target += static_cast<uint32_t>(pn);
-    max_tiles = std::max<int64_t>(max_tiles, ((m + bm - 1) / bm) * pn);
-    // the product: Aᵀ·X = B reads L_b⁻¹ N-contiguous (k, n) at W row b·512 + k;
-    // A·X = B reads L_b⁻ᵀ K-contiguous (k, n) at W row b·512 + n
-    const int wbase = rag ? 0 : b * hg::kTrsmInverseLeaf;
-    args->phase[np++] = hg::ChainPhase{
-        hg::chain_flags(hg::kChainProduct, rag ? hg::kChainMapWRagged : hg::kChainMapW, fwd ? 0 : 1, bm, bn),
-        static_cast<int>(off), static_cast<int>(off + sz), static_cast<int>(off), ksteps,
-        fwd ? 0 : wbase, fwd ? wbase : 0, target};
-    // the update of every block still to be solved: Aᵀ·X = B, columns [0, off)
-    // minus Xᵀ_b · A(b rows, those columns), A read K-contiguous at (off + k, n);
-    // A·X = B, columns [off + sz, n) minus Xᵀ_b · A(those rows, b columns)ᵀ,
-    // A read N-contiguous at (n, off + k)
-    const int64_t u0 = fwd ? off + sz : 0, u1 = fwd ? n : off;
-    if (u1 > u0) {
-      if (!chain_tile(m, u1 - u0, max_grid, false, &bm, &bn)) return false;
-      max_tiles = std::max<int64_t>(max_tiles, ((m + bm - 1) / bm) * ((u1 - u0 + bn - 1) / bn));
-      args->phase[np++] = hg::ChainPhase{
-          hg::chain_flags(hg::kChainUpdate, hg::kChainMapA, fwd ? 1 : 0, bm, bn), static_cast<int>(u0),
-          static_cast<int>(u1), static_cast<int>(off), ksteps, static_cast<int>(off), static_cast<int>(u0), 0};
+// Best shapes for a phase's non-critical groups (couplings, updates: either
+// may be absent, rows 0) on `span` CTAs: the longest CTA's time.
+double chain_others(int64_t c_rows, int64_t c_cols, int c_steps, int64_t u_rows, int64_t u_cols, int u_steps,
+                    int span, ChainTile* c_best, ChainTile* u_best) {
+  ChainTile ct[6], ut[6];
+  const int nc = c_rows > 0 ? chain_tiles(c_rows, c_cols, c_steps, ct) : 1;
+  const int nu = u_rows > 0 ? chain_tiles(u_rows, u_cols, u_steps, ut) : 1;
+  if (c_rows <= 0) ct[0] = ChainTile{0, 0, 0, 0.0};
+  if (u_rows <= 0) ut[0] = ChainTile{0, 0, 0, 0.0};
+  double best = -1.0;
+  for (int a = 0; a < nc; ++a) {
+    if (c_rows > 0 && ct[a].bm != 128) continue;  // a coupling's rows are a whole block: 128-row tiles
+    for (int b = 0; b < nu; ++b) {
+      const int tiles = ct[a].tiles + ut[b].tiles;
+      const int waves = span > 0 ? (tiles + span - 1) / span : (tiles > 0 ? 1 << 20 : 0);
+      const double t = waves * (ct[a].us > ut[b].us ? ct[a].us : ut[b].us);
+      if (best < 0 || t < best - 1e-9) {
+        best = t;
+        *c_best = ct[a];
+        *u_best = ut[b];
+      }
     }
   }
-  args->num_phases = np;
+  return best;
+}
+
+// Plans the chain launch of a solve whose inverses are (or will be) in
+// slots 0 .. count-1 of W, with slot `count` spare, as one of two plans:
+//  fused (one phase per block, k in the order of the solve):
+//   products of block k (critical: CTAs of their own), K segments for
+//     L_k⁻¹ (· L_k⁻ᵀ for A·X = B) and, from the second block on, M_k;
+//   couplings M_{k+1} = −C(k, k+1)·L_{k+1}⁻¹ into slot k-1 (M_1: the spare
+//     slot), a slot whose inverse the solve has used;
+//   updates of every block after k from Xᵀ_{k−1} (from the second block on);
+//  split (two phases per block): the products of block k by L_k⁻¹ alone,
+//   then the update of every block after it from Xᵀ_k.
+// The plan with the lower modelled time is taken (plan: 0 either, 1 fused,
+// 2 split). scale: X must become alpha·B first (not in place, or alpha !=
+// 1); fold: B suits TMA and alpha != 0, so the first phases read B
+// themselves instead of a copy phase: the first block's product reads B
+// (scale alpha); fused, the second block's product reads B_1 and M_1 / alpha
+// (scale alpha); the first update subtracts from alpha·B. Returns 0 when the
+// chain does not apply (too many blocks or rows, products wider than the
+// grid), else the plan taken.
+int chain_plan(const hg::TriLeaves& leaves, int64_t n, int64_t m, bool scale, bool fold, float alpha, bool fwd,
+               int max_grid, int plan, hg::ChainArgs* args, int* grid, int* ragged) {
+  const int nb = leaves.count;
+  if (nb < 1 || nb > hg::kChainMaxLeaves || max_grid < 2) return 0;
+  if (m < 1 || (m + 63) / 64 > hg::kChainMaxRowGroups || n > (int64_t(1) << 30)) return 0;
+  const int64_t L = hg::kTrsmInverseLeaf;
+  fold = fold && scale;
+  *ragged = -1;
+  for (int b = 0; b < nb; ++b)
+    if (leaves.size[b] % 64 != 0) {
+      // only the block that ends at n (the edge of every map) may be ragged
+      if (leaves.off[b] + leaves.size[b] != n || *ragged >= 0) return 0;
+      *ragged = b;
+    }
+  auto steps = [](int64_t s) { return static_cast<int>((s + 63) / 64); };
+  // the columns of the blocks after k: [0, off_k) for Aᵀ·X = B, [off_k + s_k, n) for A·X = B
+  auto after = [&](int k, int64_t* u0, int64_t* u1) {
+    *u0 = fwd ? leaves.off[k] + leaves.size[k] : 0;
+    *u1 = fwd ? n : leaves.off[k];
+  };
+  // The fused plan's shapes per phase, and its modelled time.
+  struct FusedPhase {
+    ChainTile prod, coup, upd;
+  };
+  FusedPhase fp[hg::kChainMaxLeaves];
+  double t_fused = 0.0;
+  bool fused_ok = true;
+  for (int k = 0; k < nb && fused_ok; ++k) {
+    const int64_t sz = leaves.size[k];
+    const int kall = steps(sz) + (k >= 1 ? steps(leaves.size[k - 1]) : 0);
+    ChainTile pt[6];
+    const int np = chain_tiles(m, sz, kall, pt);
+    int64_t u0 = 0, u1 = 0;
+    if (k >= 1) after(k, &u0, &u1);
+    const bool coup = k + 1 < nb, upd = k >= 1 && u1 > u0;
+    double best = -1.0;
+    for (int a = 0; a < np; ++a) {
+      if (pt[a].tiles > max_grid - ((coup || upd) ? 1 : 0)) continue;
+      ChainTile c{}, u{};
+      const double others =
+          (coup || upd) ? chain_others(coup ? sz : 0, coup ? leaves.size[k + 1] : 0, coup ? steps(leaves.size[k + 1]) : 0,
+                                       upd ? m : 0, u1 - u0, k >= 1 ? steps(leaves.size[k - 1]) : 0,
+                                       max_grid - pt[a].tiles, &c, &u)
+                        : 0.0;
+      const double t = pt[a].us > others ? pt[a].us : others;
+      if (best < 0 || t < best - 1e-9) {
+        best = t;
+        fp[k] = FusedPhase{pt[a], c, u};
+      }
+    }
+    if (best < 0) fused_ok = false;
+    t_fused += best + kChainPhaseUs;
+  }
+  // The split plan's shapes and time.
+  FusedPhase sp[hg::kChainMaxLeaves];
+  double t_split = 0.0;
+  bool split_ok = true;
+  for (int k = 0; k < nb && split_ok; ++k) {
+    const int64_t sz = leaves.size[k];
+    ChainTile pt[6];
+    const int np = chain_tiles(m, sz, steps(sz), pt);
+    double best = -1.0;
+    for (int a = 0; a < np; ++a) {
+      if (pt[a].tiles > max_grid) continue;
+      const double t = pt[a].us * ((pt[a].tiles + max_grid - 1) / max_grid);
+      if (best < 0 || t < best - 1e-9) {
+        best = t;
+        sp[k].prod = pt[a];
+      }
+    }
+    if (best < 0) split_ok = false;
+    t_split += best + kChainPhaseUs;
+    int64_t u0 = 0, u1 = 0;
+    after(k, &u0, &u1);
+    if (u1 > u0) {
+      ChainTile c{}, u{};
+      t_split += chain_others(0, 0, 0, m, u1 - u0, steps(sz), max_grid, &c, &u) + kChainPhaseUs;
+      sp[k].upd = u;
+    }
+  }
+  if (plan == 1 && !fused_ok) return 0;
+  if (plan == 2 && !split_ok) return 0;
+  if (!fused_ok && !split_ok) return 0;
+  const bool fused = plan == 1 || (plan == 0 && fused_ok && (!split_ok || t_fused <= t_split));
+
+  int ng = 0, max_tiles = 1;
+  uint32_t target = 0;
+  auto mslot = [&](int k) { return k == 1 ? nb : k - 2; };  // where M_k lives
+  auto group_flags = [](int kind, int a_map, int a_mn, int b_map, int b_mn, const ChainTile& t, int old_from_b,
+                        int critical) {
+    return hg::chain_group_flags(kind, a_map, a_mn, b_map, b_mn, t.bm, t.bn, old_from_b, 0, critical);
+  };
+  auto end_phase = [&](int tiles) {
+    args->group[ng - 1].flags |= 1u << 16;  // the phase's last group
+    max_tiles = std::max(max_tiles, tiles);
+  };
+  if (scale && !fold) {
+    args->group[ng++] = hg::ChainGroup{hg::chain_group_flags(hg::kChainCopy, 0, 0, 0, 0, 0, 0, 0, 0, 0), 0, 0, 0, 0,
+                                       0, 0, 0, 0, 0, 0, 0, -1, 1.0f, 0};
+    end_phase(1);
+  }
+  for (int k = 0; k < nb; ++k) {
+    const int64_t off = leaves.off[k], sz = leaves.size[k];
+    const bool rag = k == *ragged;
+    const int wbase = rag ? 0 : static_cast<int>(k * L);
+    const int wmap = rag ? hg::kChainMapWRagged : hg::kChainMapW;
+    const FusedPhase& f = fused ? fp[k] : sp[k];
+    // the products (critical)
+    const int64_t pn = (sz + f.prod.bn - 1) / f.prod.bn;
+    target += static_cast<uint32_t>(pn);
+    const bool from_b = fold && (k == 0 || (fused && k == 1));
+    hg::ChainGroup prod{group_flags(hg::kChainProduct, from_b ? hg::kChainMapB : hg::kChainMapX, 0, wmap, fwd ? 0 : 1,
+                                    f.prod, 0, 1),
+                        static_cast<int>(m), static_cast<int>(off), static_cast<int>(off + sz),
+                        static_cast<int>(off), 0, steps(sz), fwd ? 0 : wbase, fwd ? wbase : 0, 0, 0, 0, -1,
+                        from_b ? alpha : 1.0f, target};
+    if (fused && k >= 1) {
+      prod.a2_kbase = static_cast<int>(leaves.off[k - 1]);
+      prod.b2_kbase = static_cast<int>(mslot(k) * L);
+      prod.ksteps2 = steps(leaves.size[k - 1]);
+    }
+    args->group[ng++] = prod;
+    int tiles_phase = f.prod.tiles;
+    if (fused) {
+      // the coupling of block k to block k+1: rows i of block k, K and N over
+      // block k+1. Aᵀ·X = B: C(i, j) = A(off_k + i, off_{k+1} + j), M-contiguous;
+      // A·X = B: C(i, j) = A(off_{k+1} + j, off_k + i), K-contiguous.
+      if (k + 1 < nb) {
+        const int64_t no = leaves.off[k + 1], ns = leaves.size[k + 1];
+        const bool rag1 = k + 1 == *ragged;
+        const int wb1 = rag1 ? 0 : static_cast<int>((k + 1) * L);
+        args->group[ng++] = hg::ChainGroup{
+            group_flags(hg::kChainCoupling, hg::kChainMapA, fwd ? 0 : 1, rag1 ? hg::kChainMapWRagged : hg::kChainMapW,
+                        fwd ? 0 : 1, f.coup, 0, 0),
+            static_cast<int>(sz), 0, static_cast<int>(ns), static_cast<int>(no), static_cast<int>(off), steps(ns),
+            fwd ? 0 : wb1, fwd ? wb1 : 0, 0, 0, 0, mslot(k + 1), fold && k == 0 ? -1.0f / alpha : -1.0f, 0};
+        tiles_phase += f.coup.tiles;
+      }
+    }
+    // the update from block j (fused: k-1, split: k, in a phase of its own)
+    // of every block after k. Aᵀ·X = B: columns [0, off_k) minus Xᵀ_j ·
+    // A(block j rows, those columns), A read K-contiguous; A·X = B: columns
+    // [off_k + s_k, n) minus Xᵀ_j · A(those rows, block j columns)ᵀ, A read
+    // N-contiguous.
+    const int jb = fused ? k - 1 : k;
+    int64_t u0 = 0, u1 = 0;
+    after(k, &u0, &u1);
+    if (jb >= 0 && u1 > u0) {
+      if (!fused) {
+        end_phase(tiles_phase);
+        tiles_phase = 0;
+      }
+      const int64_t po = leaves.off[jb], ps = leaves.size[jb];
+      args->group[ng++] = hg::ChainGroup{
+          group_flags(hg::kChainUpdate, hg::kChainMapX, 0, hg::kChainMapA, fwd ? 1 : 0, f.upd,
+                      fold && jb == 0 ? 1 : 0, 0),
+          static_cast<int>(m), static_cast<int>(u0), static_cast<int>(u1), static_cast<int>(po), 0, steps(ps),
+          static_cast<int>(po), static_cast<int>(u0), 0, 0, 0, -1, 1.0f, 0};
+      tiles_phase += f.upd.tiles;
+    }
+    end_phase(tiles_phase);
+  }
+  args->num_groups = ng;
   *grid = std::min(max_grid, max_tiles);
-  return true;
+  return fused ? 1 : 2;
 }
 
 // hgemm_trsm, hgemm_trsm_ws and hgemm_trsm_op: W (may be null) holds room
@@ -1078,13 +1249,15 @@ int trsm_impl(const hgemm_half_t* A, int64_t lda, const hgemm_half_t* B, int64_t
     return HGEMM_ERR_ALIAS;
   hg::TriLeaves leaves{};
   uint64_t inv_bytes = 0;  // the inverses' part of the workspace
+  uint64_t full_bytes = 0; // with the spare slot and the synchronisation words
   if (W) {
     if (!trsm_leaves(n, hg::kTrsmInverseLeaf, &leaves, fwd) ||
         w_bytes < kTrsmInverseBytes * static_cast<uint64_t>(leaves.count) ||
         (reinterpret_cast<uintptr_t>(W) & 15u))
       return HGEMM_ERR_INVALID_ARG;
     inv_bytes = kTrsmInverseBytes * static_cast<uint64_t>(leaves.count);
-    const uint64_t wb = std::min<uint64_t>(w_bytes, inv_bytes + hg::kChainSyncBytes);
+    full_bytes = inv_bytes + kTrsmInverseBytes + hg::kChainSyncBytes;
+    const uint64_t wb = std::min<uint64_t>(w_bytes, full_bytes);
     if (ranges_overlap(W, wb, A, 2 * static_cast<uint64_t>(sa)) ||
         ranges_overlap(W, wb, B, 2 * static_cast<uint64_t>(sb)) ||
         ranges_overlap(W, wb, X, 2 * static_cast<uint64_t>(sx)))
@@ -1113,25 +1286,32 @@ int trsm_impl(const hgemm_half_t* A, int64_t lda, const hgemm_half_t* B, int64_t
   // where its one launch beats the recursion's chain of launches (measured);
   // past that the recursion's large products are faster.
   const int schedule = g_trsm_schedule.load(std::memory_order_relaxed);
+  const bool b_tma = (reinterpret_cast<uintptr_t>(B) & 15u) == 0 && ldb % 8 == 0;
   hg::ChainArgs chain{};
   int chain_grid = 0, ragged = -1;
-  const bool use_chain = by_inverse && schedule != HGEMM_TRSM_RECURSIVE &&
-                         (schedule == HGEMM_TRSM_CHAIN || m <= kChainAutoMaxM) &&
-                         w_bytes >= inv_bytes + hg::kChainSyncBytes &&
-                         (reinterpret_cast<uintptr_t>(A) & 15u) == 0 && lda % 8 == 0 &&
-                         chain_plan(leaves, n, m, !in_place || alpha != 1.0f, fwd,
-                                    hg::chain_max_grid(dev->num_sms), &chain, &chain_grid, &ragged);
-  uint32_t* sync = use_chain ? reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(W) + inv_bytes) : nullptr;
+  const bool forced_chain = schedule == HGEMM_TRSM_CHAIN || schedule == HGEMM_TRSM_CHAIN_FUSED ||
+                            schedule == HGEMM_TRSM_CHAIN_SPLIT;
+  const int plan = schedule == HGEMM_TRSM_CHAIN_FUSED ? 1 : schedule == HGEMM_TRSM_CHAIN_SPLIT ? 2 : 0;
+  int planned = 0;
+  const bool use_chain = by_inverse && schedule != HGEMM_TRSM_RECURSIVE && (forced_chain || m <= kChainAutoMaxM) &&
+                         w_bytes >= full_bytes && (reinterpret_cast<uintptr_t>(A) & 15u) == 0 && lda % 8 == 0 &&
+                         (planned = chain_plan(leaves, n, m, !in_place || alpha != 1.0f, b_tma && alpha != 0.0f,
+                                               alpha, fwd, hg::chain_max_grid(dev->num_sms), plan, &chain,
+                                               &chain_grid, &ragged)) != 0;
+  uint32_t* sync = use_chain ? reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(W) + inv_bytes +
+                                                           kTrsmInverseBytes)
+                             : nullptr;
   if (by_inverse) {
     e = hg::launch_trsm_inverse(a, lda, W, leaves, sync, stream);
     if (e != cudaSuccess) return cuda_fail(e);
     chained = true;
   }
   if (use_chain) {
-    CUtensorMap mx, mw, mwr, ma;
+    CUtensorMap mx, mb, mw, mwr, ma;
     const int64_t L = hg::kTrsmInverseLeaf;
     if ((rc = encode_map(&mx, x, m, n, ldx, 64, 64)) != HGEMM_OK ||
-        (rc = encode_map(&mw, W, static_cast<int64_t>(leaves.count) * L, L, L, 64, 64)) != HGEMM_OK ||
+        (rc = b_tma ? encode_map(&mb, B, m, n, ldb, 64, 64) : encode_map(&mb, x, m, n, ldx, 64, 64)) != HGEMM_OK ||
+        (rc = encode_map(&mw, W, static_cast<int64_t>(leaves.count + 1) * L, L, L, 64, 64)) != HGEMM_OK ||
         (rc = encode_map(&ma, a, n, n, lda, 64, 64)) != HGEMM_OK)
       return rc;
     mwr = mw;
@@ -1142,6 +1322,7 @@ int trsm_impl(const hgemm_half_t* A, int64_t lda, const hgemm_half_t* B, int64_t
     chain.ldx = ldx;
     chain.B = reinterpret_cast<const uint16_t*>(B);
     chain.ldb = ldb;
+    chain.W = W;
     chain.alpha = alpha;
     chain.m = static_cast<int>(m);
     chain.n = static_cast<int>(n);
@@ -1150,9 +1331,9 @@ int trsm_impl(const hgemm_half_t* A, int64_t lda, const hgemm_half_t* B, int64_t
     chain.status = t_ctx.status;
     chain.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
     chain.inject = g_inject.load(std::memory_order_relaxed);
-    e = hg::launch_trsm_chain(mx, mw, mwr, ma, chain, chain_grid, stream);
+    e = hg::launch_trsm_chain(mx, mb, mw, mwr, ma, chain, chain_grid, stream);
     if (e != cudaSuccess) return cuda_fail(e);
-    t_trsm_schedule = HGEMM_TRSM_CHAIN;
+    t_trsm_schedule = planned == 1 ? HGEMM_TRSM_CHAIN_FUSED : HGEMM_TRSM_CHAIN_SPLIT;
     return HGEMM_OK;
   }
   int leaf_index = 0;  // position in `leaves` (the order of the solve)
@@ -1235,7 +1416,7 @@ int hgemm_trsm(const hgemm_half_t* A, int64_t lda, const hgemm_half_t* B, int64_
 size_t hgemm_trsm_workspace_size(int64_t n) {
   hg::TriLeaves leaves{};
   if (n <= 0 || n > HGEMM_MAX_DIM || !trsm_leaves(n, hg::kTrsmInverseLeaf, &leaves)) return 0;
-  return static_cast<size_t>(kTrsmInverseBytes * static_cast<uint64_t>(leaves.count) + hg::kChainSyncBytes);
+  return static_cast<size_t>(kTrsmInverseBytes * static_cast<uint64_t>(leaves.count + 1) + hg::kChainSyncBytes);
 }
 
 int hgemm_trsm_ws(const hgemm_half_t* A, int64_t lda, const hgemm_half_t* B, int64_t ldb,
@@ -1375,7 +1556,8 @@ int hgemm_force_split(int split, int tile_n) {
 }
 
 int hgemm_force_trsm_schedule(int schedule) {
-  if (schedule != HGEMM_TRSM_AUTO && schedule != HGEMM_TRSM_RECURSIVE && schedule != HGEMM_TRSM_CHAIN)
+  if (schedule != HGEMM_TRSM_AUTO && schedule != HGEMM_TRSM_RECURSIVE && schedule != HGEMM_TRSM_CHAIN &&
+      schedule != HGEMM_TRSM_CHAIN_FUSED && schedule != HGEMM_TRSM_CHAIN_SPLIT)
     return HGEMM_ERR_INVALID_ARG;
   g_trsm_schedule.store(schedule);
   return HGEMM_OK;

@@ -20,8 +20,11 @@
 //   * a cooperative launch of one CTA per SM (all CTAs co-resident); phases
 //     are separated by a grid-wide barrier: an arrival counter in the
 //     workspace (released at GPU scope, polled with acquire, bounded in time);
-//   * phase 0 (unless the solve is in place with alpha = 1): X := alpha·B,
-//     grid-stride, FP32 product rounded to FP16;
+//   * X := alpha·B is folded into the first phase that reads each block:
+//     the first product takes its first operand from B and scales its
+//     accumulator by alpha, the first update subtracts from alpha·B (one
+//     FP32 product and one rounding per element). Only when B does not suit
+//     TMA is a copy phase (grid-stride, by the epilogue warps) run first;
 //   * every other phase is a set of bm × bn output tiles (bm 64 or 128, bn
 //     64, 128 or 256, chosen per phase by the host so that the tiles fill the
 //     grid with the fewest operand bytes per SM), one or more per CTA, each
@@ -62,93 +65,177 @@ namespace hg {
 namespace {
 
 constexpr int kThreads = 192;                     // producer, MMA issuer, four epilogue warps
-constexpr int kRingBytes = 192 * 1024;            // operand ring, regrouped into stages per phase
+constexpr int kRingBytes = 192 * 1024;            // operand ring, regrouped into stages per tile shape
 constexpr int kMaxStages = 8;
-constexpr int kASlot = kTcBM * kTcBK * 2;         // 16 KB: an M=128 MMA reads 128 rows of Xᵀ
+constexpr int kASlot = kTcBM * kTcBK * 2;         // 16 KB: an M=128 MMA reads 128 rows
 constexpr int kBox = 64;                          // every TMA box is 64 × 64 elements
 constexpr int kBoxBytes = kBox * kBox * 2;        // 8 KB
 constexpr int kAccCols = 256;                     // the widest tile: 256 FP32 columns
 constexpr int kTmemCols = 2 * kAccCols;           // two accumulators
+constexpr int kSlot = kTrsmInverseLeaf;           // rows and columns of a workspace slot
 constexpr int kOffBar = kRingBytes;
 // full, empty, accumulator full ×2 / empty ×2, drain
 constexpr int kNumBars = 2 * kMaxStages + 4 + 1;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;  // TMEM address, abort flag, barriers passed, epilogue verdict
-constexpr int kOffPhases = kOffMisc + 16;         // the phase table, copied from the parameters
-constexpr int kSmemBytes = kOffPhases + kChainMaxPhases * static_cast<int>(sizeof(ChainPhase)) + 1024;
+constexpr int kOffGroups = kOffMisc + 16;         // the group table, decoded from the parameters
 constexpr int kEpiThreads = 128;                  // warps 2–5
 constexpr int kEpiBarrier = 1;                    // named barrier of the epilogue warps
-static_assert(kSmemBytes <= 232448, "exceeds 227 KB of shared memory per CTA");
 static_assert(kRingBytes / (kASlot + 64 * kTcBK * 2) >= kMaxStages, "the narrowest stages fill the ring");
+static_assert(5 * sizeof(CUtensorMap) + sizeof(ChainArgs) <= 4096, "kernel parameters beyond 4 KB");
 
-// A phase, decoded.
-struct Phase {
-  int kind, b_map, b_mn, bm, bn;
-  int num_m, num_n, num_tiles;
-  int n0, n_end, k0, ksteps, b_kbase, b_nbase;
+// A group, decoded.
+struct Group {
+  int kind, a_map, a_mn, b_map, b_mn, bm, bn, old_from_b, last, critical;
+  int rows, n0, n_end;
+  int a_kbase, a_mbase, ksteps, b_kbase, b_nbase, a2_kbase, b2_kbase, ksteps2, out_slot;
+  float scale;
   uint32_t rg_target;
-  int stages;
+  int num_m, num_n, tiles;
   uint32_t stage_bytes, tx_bytes;
+  int stages;
+};
+constexpr int kSmemBytes = kOffGroups + kChainMaxGroups * static_cast<int>(sizeof(Group)) + 1024;
+static_assert(kSmemBytes <= 232448, "exceeds 227 KB of shared memory per CTA");
+
+__device__ __forceinline__ Group decode(const ChainGroup& c) {
+  Group g;
+  g.kind = c.flags & 3u;
+  g.a_map = (c.flags >> 2) & 7u;
+  g.a_mn = (c.flags >> 5) & 1u;
+  g.b_map = (c.flags >> 6) & 7u;
+  g.b_mn = (c.flags >> 9) & 1u;
+  g.bm = ((c.flags >> 10) & 3u) * 64;
+  g.bn = ((c.flags >> 12) & 7u) * 64;
+  g.old_from_b = (c.flags >> 15) & 1u;
+  g.last = (c.flags >> 16) & 1u;
+  g.critical = (c.flags >> 17) & 1u;
+  g.rows = c.rows;
+  g.n0 = c.n0;
+  g.n_end = c.n_end;
+  g.a_kbase = c.a_kbase;
+  g.a_mbase = c.a_mbase;
+  g.ksteps = c.ksteps;
+  g.b_kbase = c.b_kbase;
+  g.b_nbase = c.b_nbase;
+  g.a2_kbase = c.a2_kbase;
+  g.b2_kbase = c.b2_kbase;
+  g.ksteps2 = c.ksteps2;
+  g.out_slot = c.out_slot;
+  g.scale = c.scale;
+  g.rg_target = c.rg_target;
+  if (g.kind == kChainCopy || g.bm == 0 || g.bn == 0) {
+    g.num_m = g.num_n = g.tiles = 0;
+    g.stages = 1;
+    g.stage_bytes = g.tx_bytes = 0;
+    return g;
+  }
+  g.num_m = (g.rows + g.bm - 1) / g.bm;
+  g.num_n = (g.n_end - g.n0 + g.bn - 1) / g.bn;
+  g.tiles = g.num_m * g.num_n;
+  g.stage_bytes = static_cast<uint32_t>(kASlot + g.bn * kTcBK * 2);
+  g.stages = min(kMaxStages, static_cast<int>(kRingBytes / g.stage_bytes));
+  g.tx_bytes = static_cast<uint32_t>((g.bm / kBox + g.bn / kBox) * kBoxBytes);
+  return g;
+}
+
+// Tile t of a group: row tile mi, column tile ni (column-tile major, so that
+// concurrently running tiles share the second operand's boxes).
+__device__ __forceinline__ void tile_of(const Group& g, int t, int& mi, int& ni) {
+  ni = t / g.num_m;
+  mi = t - ni * g.num_m;
+}
+
+// One unit of work of a CTA: a group index and a tile of it.
+struct Task {
+  int group, tile;
 };
 
-__device__ __forceinline__ Phase decode(const ChainPhase& c, int m) {
-  Phase p;
-  p.kind = c.flags & 3;
-  p.b_map = (c.flags >> 2) & 3;
-  p.b_mn = (c.flags >> 4) & 1;
-  p.bm = ((c.flags >> 5) & 3) * 64;
-  p.bn = ((c.flags >> 8) & 7) * 64;
-  p.n0 = c.n0;
-  p.n_end = c.n_end;
-  p.k0 = c.k0;
-  p.ksteps = c.ksteps;
-  p.b_kbase = c.b_kbase;
-  p.b_nbase = c.b_nbase;
-  p.rg_target = c.rg_target;
-  if (p.kind == kChainCopy || p.bm == 0 || p.bn == 0) {
-    p.num_m = p.num_n = p.num_tiles = 0;
-    p.stages = 1;
-    p.stage_bytes = p.tx_bytes = 0;
-    return p;
+// The tasks of CTA `cta` (of `ctas`) in the phase whose groups are [g0, g1]:
+// the critical group's tiles (the products) one per CTA on CTAs [0, P), then
+// the other groups' tiles, concatenated, round-robin over CTAs [P, ctas)
+// (over all CTAs when P fills the grid). Task i of the CTA, or group -1.
+__device__ __forceinline__ Task task_at(const Group* groups, int g0, int g1, int cta, int ctas, int i) {
+  const Group& first = groups[g0];
+  const int crit = first.critical ? first.tiles : 0;
+  if (cta < crit) {
+    if (i == 0) return Task{g0, cta};
+    --i;
   }
-  p.num_m = (m + p.bm - 1) / p.bm;
-  p.num_n = (p.n_end - p.n0 + p.bn - 1) / p.bn;
-  p.num_tiles = p.num_m * p.num_n;
-  p.stage_bytes = static_cast<uint32_t>(kASlot + p.bn * kTcBK * 2);
-  p.stages = min(kMaxStages, static_cast<int>(kRingBytes / p.stage_bytes));
-  p.tx_bytes = static_cast<uint32_t>((p.bm / kBox + p.bn / kBox) * kBoxBytes);
-  return p;
+  const int lo = crit < ctas ? crit : 0;  // the CTAs that take the other groups
+  if (cta < lo) return Task{-1, 0};
+  const int span = ctas - lo;
+  int idx = (cta - lo) + i * span;
+  for (int g = first.critical ? g0 + 1 : g0; g <= g1; ++g) {
+    const int n = groups[g].tiles;
+    if (idx < n) return Task{g, idx};
+    idx -= n;
+  }
+  return Task{-1, 0};
 }
 
-// Tile t of a phase: row tile mi, column tile ni (column-tile major, so that
-// concurrently running tiles share the second operand's boxes).
-__device__ __forceinline__ void tile_of(const Phase& ph, int t, int& mi, int& ni) {
-  ni = t / ph.num_m;
-  mi = t - ni * ph.num_m;
+// The last group of the phase that starts at group g0.
+__device__ __forceinline__ int phase_end(const Group* groups, int g0, int num_groups) {
+  int g = g0;
+  while (g + 1 < num_groups && !groups[g].last) ++g;
+  return g;
 }
 
-__device__ __forceinline__ const CUtensorMap* map_b(const Phase& ph, const CUtensorMap* w,
-                                                    const CUtensorMap* wr, const CUtensorMap* a) {
-  return ph.b_map == kChainMapW ? w : ph.b_map == kChainMapWRagged ? wr : a;
+__device__ __forceinline__ const CUtensorMap* map_of(int which, const CUtensorMap* x, const CUtensorMap* b,
+                                                     const CUtensorMap* w, const CUtensorMap* wr,
+                                                     const CUtensorMap* a) {
+  return which == kChainMapX ? x : which == kChainMapB ? b : which == kChainMapW ? w : which == kChainMapWRagged ? wr : a;
 }
 
-// The second operand's boxes of k-step kk of column tile ni into `sb`.
-__device__ __forceinline__ void load_b(const Phase& ph, const CUtensorMap* map, uint32_t sb, uint32_t bar,
-                                       int ni, int kk) {
-  const int kc = ph.b_kbase + kk * kTcBK;
-  for (int i = 0; i < ph.bn / kBox; ++i) {
-    const int nc = ph.b_nbase + ni * ph.bn + i * kBox;
-    if (ph.b_mn)
+// Operand boxes of k-step kk (of both segments) of tile (mi, ni) into the
+// stage at `sa` (first operand) and `sa + kASlot` (second operand).
+// b_only / a_only: one operand (the second is prefetched before a barrier).
+struct Maps {
+  const CUtensorMap *x, *b, *w, *wr, *a;
+};
+
+__device__ __forceinline__ void load_b(const Group& g, const Maps& m, uint32_t sb, uint32_t bar, int ni, int kk) {
+  const bool seg2 = kk >= g.ksteps;
+  const CUtensorMap* map = seg2 ? m.w : map_of(g.b_map, m.x, m.b, m.w, m.wr, m.a);
+  const int kc = seg2 ? g.b2_kbase + (kk - g.ksteps) * kTcBK : g.b_kbase + kk * kTcBK;
+  const int nb = seg2 ? 0 : g.b_nbase;
+  const bool mn = seg2 || g.b_mn;
+  for (int i = 0; i < g.bn / kBox; ++i) {
+    const int nc = nb + ni * g.bn + i * kBox;
+    if (mn)
       tma_load_2d(sb + i * kBoxBytes, map, bar, nc, kc);  // box: 64 N (contiguous) × 64 K rows
     else
       tma_load_2d(sb + i * kBoxBytes, map, bar, kc, nc);  // box: 64 N rows × 64 K (contiguous)
   }
 }
 
-// The Xᵀ boxes of k-step kk of row tile mi into `sa`.
-__device__ __forceinline__ void load_a(const Phase& ph, const CUtensorMap* map, uint32_t sa, uint32_t bar,
-                                       int mi, int kk) {
-  for (int i = 0; i < ph.bm / kBox; ++i)
-    tma_load_2d(sa + i * kBoxBytes, map, bar, ph.k0 + kk * kTcBK, mi * ph.bm + i * kBox);
+__device__ __forceinline__ void load_a(const Group& g, const Maps& m, uint32_t sa, uint32_t bar, int mi, int kk) {
+  const bool seg2 = kk >= g.ksteps;
+  const CUtensorMap* map = seg2 ? m.x : map_of(g.a_map, m.x, m.b, m.w, m.wr, m.a);
+  const int kc = seg2 ? g.a2_kbase + (kk - g.ksteps) * kTcBK : g.a_kbase + kk * kTcBK;
+  const bool mn = !seg2 && g.a_mn;
+  for (int i = 0; i < g.bm / kBox; ++i) {
+    const int mc = (seg2 ? 0 : g.a_mbase) + mi * g.bm + i * kBox;
+    if (mn)
+      tma_load_2d(sa + i * kBoxBytes, map, bar, mc, kc);  // box: 64 M (contiguous) × 64 K rows
+    else
+      tma_load_2d(sa + i * kBoxBytes, map, bar, kc, mc);  // box: 64 M rows × 64 K (contiguous)
+  }
+}
+
+// True once the phase with parity `parity` of `bar` has completed, without
+// suspending (a stage that landed during the previous stage's MMAs is then
+// taken at once; otherwise the caller falls back to the suspending wait).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  if (!HG_DBG_SMEM(bar, 8)) return false;
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
 }
 
 __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
@@ -298,10 +385,12 @@ __device__ void copy_phase(const ChainArgs& p) {
   }
 }
 
-// The previous values of columns [col, col + 32) of row `row` of Xᵀ, when
-// all 32 lie before n_end (else zeros: store32 then reads them one by one).
-__device__ __forceinline__ void load_old32(const ChainArgs& p, int64_t row, int col, int n_end, uint4 (&old)[4]) {
-  const uint16_t* src = p.X + row * p.ldx + col;
+// The previous values of columns [col, col + 32) of row `row` of Xᵀ (from_b:
+// of Bᵀ), when all 32 lie before n_end (else zeros: store32 then reads them
+// one by one).
+__device__ __forceinline__ void load_old32(const ChainArgs& p, bool from_b, int64_t row, int col, int n_end,
+                                           uint4 (&old)[4]) {
+  const uint16_t* src = from_b ? p.B + row * p.ldb + col : p.X + row * p.ldx + col;
   if (col + 32 <= n_end && HG_DBG_ALIGN(src, 16)) {
 #pragma unroll
     for (int j = 0; j < 4; ++j) old[j] = __ldcg(reinterpret_cast<const uint4*>(src) + j);
@@ -311,13 +400,15 @@ __device__ __forceinline__ void load_old32(const ChainArgs& p, int64_t row, int 
   }
 }
 
-// The epilogue of 32 columns [col, col + 32) of row `row` of Xᵀ: products
-// store the accumulator, updates the previous value (`old`, from load_old32)
-// minus it (one FP32 subtraction, one rounding). Columns at or past n_end
-// are left alone.
-__device__ __forceinline__ void store32(const ChainArgs& p, int kind, int64_t row, int col, int n_end,
-                                        const uint32_t (&v)[32], const uint4 (&old)[4]) {
-  uint16_t* dst = p.X + row * p.ldx + col;
+// The epilogue of 32 columns [col, col + 32) of row `row`: updates store the
+// previous value (`old`, from load_old32; alpha·B when from_b) minus the
+// accumulator (one FP32 operation, one rounding), products and couplings
+// scale · acc, into `dst` (the row's element `col`). Columns at or past
+// n_end are left alone.
+__device__ __forceinline__ void store32(const ChainArgs& p, bool update, bool from_b, float scale, uint16_t* dst,
+                                        const uint16_t* src_old, int col, int n_end, const uint32_t (&v)[32],
+                                        const uint4 (&old)[4]) {
+  const float oscale = from_b ? p.alpha : 1.0f;
   if (col + 32 <= n_end && HG_DBG_ALIGN(dst, 16)) {
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -326,7 +417,7 @@ __device__ __forceinline__ void store32(const ChainArgs& p, int kind, int64_t ro
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const float acc = __uint_as_float(v[8 * j + i]);
-        f[i] = kind == kChainUpdate ? __half2float(oh[i]) - acc : acc;
+        f[i] = update ? oscale * __half2float(oh[i]) - acc : scale * acc;
       }
       uint4 r;
       r.x = pack_half2(__float_as_uint(f[0]), __float_as_uint(f[1]));
@@ -341,15 +432,15 @@ __device__ __forceinline__ void store32(const ChainArgs& p, int kind, int64_t ro
   for (int i = 0; i < 32; ++i) {
     if (col + i >= n_end) break;
     const float acc = __uint_as_float(v[i]);
-    const float f = kind == kChainUpdate ? __half2float(__ushort_as_half(__ldcg(dst + i))) - acc : acc;
+    const float f = update ? oscale * __half2float(__ushort_as_half(__ldcg(src_old + i))) - acc : scale * acc;
     dst[i] = __half_as_ushort(__float2half_rn(f));
   }
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    trsm_chain_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
-                      const __grid_constant__ CUtensorMap tmWr, const __grid_constant__ CUtensorMap tmA,
-                      const __grid_constant__ ChainArgs p) {
+    trsm_chain_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmB,
+                      const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmWr,
+                      const __grid_constant__ CUtensorMap tmA, const __grid_constant__ ChainArgs p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -360,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
   volatile uint32_t* passed = reinterpret_cast<volatile uint32_t*>(smem + kOffMisc + 8);  // grid barriers passed
   volatile int* epi_ok = reinterpret_cast<volatile int*>(smem + kOffMisc + 12);
-  ChainPhase* phases = reinterpret_cast<ChainPhase*>(smem + kOffPhases);
+  Group* groups = reinterpret_cast<Group*>(smem + kOffGroups);
 
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (kMaxStages + s); };
@@ -370,11 +461,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const Watchdog wd{abort_flag, p.status, p.timeout_ns};
-  const int num_phases = p.num_phases;
+  const int num_groups = p.num_groups;
+  const int cta = static_cast<int>(blockIdx.x), ctas = static_cast<int>(gridDim.x);
+  const Maps maps{&tmX, &tmB, &tmW, &tmWr, &tmA};
 
-  // The phase table, read once from the parameters (reads of a new entry
-  // there at every phase would each wait on the constant cache).
-  for (int i = threadIdx.x; i < num_phases; i += blockDim.x) phases[i] = p.phase[i];
+  // The group table, read once from the parameters and decoded (reads of a
+  // new entry there at every phase would each wait on the constant cache).
+  for (int i = threadIdx.x; i < num_groups; i += blockDim.x) groups[i] = decode(p.group[i]);
   if (threadIdx.x == 0) {
     for (int s = 0; s < kMaxStages; ++s) {
       mbar_init(full_bar(s), 1);   // the producer's arrive.expect_tx (+ TMA bytes)
@@ -390,6 +483,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     *epi_ok = 1;
     fence_barrier_init();
     prefetch_tensormap(&tmX);
+    prefetch_tensormap(&tmB);
     prefetch_tensormap(&tmW);
     prefetch_tensormap(&tmWr);
     prefetch_tensormap(&tmA);
@@ -414,80 +508,98 @@ __global__ void __launch_bounds__(kThreads, 1)
       // its last fill completes; filled: stages filled at least once
       uint32_t ebits = 0xFFFFFFFFu, filled = 0u;
       long long fills = 0;
-      int pref = 0;        // stages of this phase's first tile whose B boxes are already in flight
+      uint32_t cur_sb = 0;  // the ring's current stage size (0: none yet)
+      int s = 0;            // next stage
+      int pref = 0;         // stages of the phase's first task whose second operand is already in flight
+      int pref_group = -1, pref_tile = 0;
       bool ok = true;
-      int j = 0;
-      for (; j < num_phases && ok; ++j) {
-        const Phase ph = decode(phases[j], p.m);
+      int j = 0, g0 = 0;
+      // every stage consumed, then the ring regrouped for stages of sb bytes
+      auto regroup = [&](uint32_t sb) {
+        for (int s2 = 0; s2 < kMaxStages && ok; ++s2)
+          ok = wait_phase(empty_bar(s2), (ebits >> s2) & 1u, wd, kWdProducerEmpty);
+        cur_sb = sb;
+        s = 0;
+      };
+      for (; g0 < num_groups && ok; ++j) {
+        const int g1 = phase_end(groups, g0, num_groups);
         if (j > 0) {
-          // grid barrier j passed: the other CTAs' writes of X are visible,
-          // and ordered before this thread's TMA reads
+          // grid barrier j passed: the other CTAs' writes are visible, and
+          // ordered before this thread's TMA reads
           ok = wait_passed(passed, static_cast<uint32_t>(j), wd);
           if (!ok) break;
           fence_proxy_async_global();
         }
-        if (ph.kind != kChainCopy) {
-          const CUtensorMap* mb = map_b(ph, &tmW, &tmWr, &tmA);
-          int s = 0;
-          bool first = true;
-          for (int t = blockIdx.x; ok && t < ph.num_tiles; t += gridDim.x) {
-            int mi, ni;
-            tile_of(ph, t, mi, ni);
-            for (int kk = 0; kk < ph.ksteps; ++kk) {
-              const uint32_t sa = ring + s * ph.stage_bytes;
-              if (!(first && kk < pref)) {
-                if (!wait_phase(empty_bar(s), (ebits >> s) & 1u, wd, kWdProducerEmpty)) {
-                  ok = false;
-                  break;
-                }
-                ebits ^= 1u << s;
-                filled |= 1u << s;
-                if (!(p.inject == 1 && fills == 0))  // testing aid: withhold one arrival
-                  mbar_arrive_expect_tx(full_bar(s), ph.tx_bytes);
-                ++fills;
-                load_b(ph, mb, sa + kASlot, full_bar(s), ni, kk);
+        for (int i = 0; ok; ++i) {
+          const Task tk = task_at(groups, g0, g1, cta, ctas, i);
+          if (tk.group < 0) break;
+          const Group g = groups[tk.group];  // a copy: the loops below read it from registers
+          if (g.kind == kChainCopy) continue;
+          const bool prefetched = i == 0 && pref > 0;
+          if (!prefetched && g.stage_bytes != cur_sb) regroup(g.stage_bytes);
+          int mi, ni;
+          tile_of(g, tk.tile, mi, ni);
+          const int kall = g.ksteps + g.ksteps2;
+          for (int kk = 0; ok && kk < kall; ++kk) {
+            const uint32_t sa = ring + s * g.stage_bytes;
+            if (!(prefetched && kk < pref)) {
+              if (!wait_phase(empty_bar(s), (ebits >> s) & 1u, wd, kWdProducerEmpty)) {
+                ok = false;
+                break;
               }
-              load_a(ph, &tmX, sa, full_bar(s), mi, kk);
-              if (++s == ph.stages) s = 0;
+              ebits ^= 1u << s;
+              filled |= 1u << s;
+              if (!(p.inject == 1 && fills == 0))  // testing aid: withhold one arrival
+                mbar_arrive_expect_tx(full_bar(s), g.tx_bytes);
+              ++fills;
+              load_b(g, maps, sa + kASlot, full_bar(s), ni, kk);
             }
-            first = false;
+            load_a(g, maps, sa, full_bar(s), mi, kk);
+            if (++s == g.stages) s = 0;
           }
         }
         pref = 0;
-        // The next phase's first stages of the second operand (which no
-        // phase writes), before its barrier. The ring's geometry may change
-        // with the phase, so every stage of this one must be consumed first.
-        if (ok && j + 1 < num_phases) {
-          const Phase nx = decode(phases[j + 1], p.m);
-          if (nx.kind != kChainCopy && static_cast<int>(blockIdx.x) < nx.num_tiles) {
-            for (int s2 = 0; s2 < kMaxStages && ok; ++s2)
-              ok = wait_phase(empty_bar(s2), (ebits >> s2) & 1u, wd, kWdProducerEmpty);
-            int mi, ni;
-            tile_of(nx, blockIdx.x, mi, ni);
-            const CUtensorMap* nmb = map_b(nx, &tmW, &tmWr, &tmA);
-            const int np = min(nx.ksteps, nx.stages);
-            for (int kk = 0; ok && kk < np; ++kk) {
-              ebits ^= 1u << kk;
-              filled |= 1u << kk;
-              if (!(p.inject == 1 && fills == 0)) mbar_arrive_expect_tx(full_bar(kk), nx.tx_bytes);
-              ++fills;
-              load_b(nx, nmb, ring + kk * nx.stage_bytes + kASlot, full_bar(kk), ni, kk);
-              pref = kk + 1;
+        pref_group = -1;
+        // The next phase's first task: the stages of its first K segment
+        // take their second operand (an inverse or the triangle, which no
+        // phase writes while it is still to be read) before the barrier.
+        const int n0g = g1 + 1;
+        if (ok && n0g < num_groups) {
+          const int n1g = phase_end(groups, n0g, num_groups);
+          const Task tk = task_at(groups, n0g, n1g, cta, ctas, 0);
+          if (tk.group >= 0) {
+            const Group g = groups[tk.group];  // a copy: the loops below read it from registers
+            if (g.kind != kChainCopy) {
+              regroup(g.stage_bytes);
+              int mi, ni;
+              tile_of(g, tk.tile, mi, ni);
+              const int np = min(g.ksteps, g.stages);
+              pref_group = tk.group;
+              pref_tile = tk.tile;
+              for (int kk = 0; ok && kk < np; ++kk) {
+                ebits ^= 1u << kk;
+                filled |= 1u << kk;
+                if (!(p.inject == 1 && fills == 0)) mbar_arrive_expect_tx(full_bar(kk), g.tx_bytes);
+                ++fills;
+                load_b(g, maps, ring + kk * g.stage_bytes + kASlot, full_bar(kk), ni, kk);
+                pref = kk + 1;
+              }
             }
           }
         }
+        g0 = g1 + 1;
       }
-      // Stages whose B boxes went out before an aborted barrier still expect
-      // their Xᵀ bytes: issue those loads (phase j), then wait until every
-      // fill has landed.
-      if (pref > 0 && j < num_phases) {
-        const Phase nx = decode(phases[j], p.m);
+      // Stages whose second operand went out before an aborted barrier still
+      // expect their Xᵀ bytes: issue those loads, then wait until every fill
+      // has landed.
+      if (pref > 0 && pref_group >= 0) {
+        const Group g = groups[pref_group];
         int mi, ni;
-        tile_of(nx, blockIdx.x, mi, ni);
-        for (int kk = 0; kk < pref; ++kk) load_a(nx, &tmX, ring + kk * nx.stage_bytes, full_bar(kk), mi, kk);
+        tile_of(g, pref_tile, mi, ni);
+        for (int kk = 0; kk < pref; ++kk) load_a(g, maps, ring + kk * g.stage_bytes, full_bar(kk), mi, kk);
       }
-      for (int s = 0; s < kMaxStages; ++s)
-        if ((filled >> s) & 1u) wait_drain(full_bar(s), (ebits >> s) & 1u, wd);
+      for (int s2 = 0; s2 < kMaxStages; ++s2)
+        if ((filled >> s2) & 1u) wait_drain(full_bar(s2), (ebits >> s2) & 1u, wd);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -496,49 +608,66 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t fbits = 0;  // parity of the next wait on full[s]
       int acc = 0;
       uint32_t acc_phase = 0;
+      uint32_t cur_sb = 0;
+      int s = 0;
       bool ok = true;
-      for (int j = 0; j < num_phases && ok; ++j) {
-        const Phase ph = decode(phases[j], p.m);
-        if (ph.kind == kChainCopy) continue;
-        const uint32_t idesc = idesc_f16_f32acc(kTcBM, ph.bn) | idesc_major_bits(false, ph.b_mn != 0);
-        const uint32_t b_step = ph.b_mn ? 128u : 2u;  // 16 K: 16 rows of 128 B, or 32 B along the row
-        int s = 0;
-        for (int t = blockIdx.x; ok && t < ph.num_tiles; t += gridDim.x) {
+      for (int g0 = 0; g0 < num_groups && ok;) {
+        const int g1 = phase_end(groups, g0, num_groups);
+        for (int i = 0; ok; ++i) {
+          const Task tk = task_at(groups, g0, g1, cta, ctas, i);
+          if (tk.group < 0) break;
+          const Group g = groups[tk.group];  // a copy: the loops below read it from registers
+          if (g.kind == kChainCopy) continue;
+          // the producer regroups the ring at the same points
+          if (g.stage_bytes != cur_sb) {
+            cur_sb = g.stage_bytes;
+            s = 0;
+          }
+          // prefetched first tasks start on stage 0 as well
+          if (i == 0) s = 0;
           int mi, ni;
-          tile_of(ph, t, mi, ni);
+          tile_of(g, tk.tile, mi, ni);
           if (!wait_phase(acce_bar(acc), acc_phase ^ 1u, wd, kWdMmaAccEmpty)) {
             ok = false;
             break;
           }
           tc_fence_after_sync();
           const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kAccCols);
-          for (int kk = 0; kk < ph.ksteps; ++kk) {
-            if (!wait_phase(full_bar(s), (fbits >> s) & 1u, wd, kWdMmaFull)) {
+          const int kall = g.ksteps + g.ksteps2;
+          for (int kk = 0; kk < kall; ++kk) {
+            if (!mbar_test_wait(full_bar(s), (fbits >> s) & 1u) &&
+                !wait_phase(full_bar(s), (fbits >> s) & 1u, wd, kWdMmaFull)) {
               ok = false;
               break;
             }
             fbits ^= 1u << s;
-            if (ph.kind == kChainProduct && kk == ph.ksteps - 1) {
-              // every Xᵀ box of this tile has landed: its reads of the rows are done
-              const int g0 = mi * ph.bm / 64;
-              for (int g = g0; g < g0 + ph.bm / 64 && g < kChainMaxRowGroups; ++g)
-                red_relaxed_gpu(p.sync + kChainSyncRowGroup0 + g, 1u);
+            if (g.critical && kk == kall - 1) {
+              // every Xᵀ box of this product tile has landed: its reads of the rows are done
+              const int r0 = mi * g.bm / 64;
+              for (int r = r0; r < r0 + g.bm / 64 && r < kChainMaxRowGroups; ++r)
+                red_relaxed_gpu(p.sync + kChainSyncRowGroup0 + r, 1u);
             }
             tc_fence_after_sync();
-            const uint32_t sa = ring + s * ph.stage_bytes;
-            const uint64_t a_desc = sdesc_kmajor_sw128(sa);
-            const uint64_t b_desc = ph.b_mn ? sdesc_mnmajor_sw128(sa + kASlot) : sdesc_kmajor_sw128(sa + kASlot);
+            const bool seg2 = kk >= g.ksteps;
+            const bool amn = !seg2 && g.a_mn, bmn = seg2 || g.b_mn;
+            const uint32_t idesc = idesc_f16_f32acc(kTcBM, g.bn) | idesc_major_bits(amn, bmn);
+            const uint32_t sa = ring + s * g.stage_bytes;
+            const uint64_t a_desc = amn ? sdesc_mnmajor_sw128(sa) : sdesc_kmajor_sw128(sa);
+            const uint64_t b_desc = bmn ? sdesc_mnmajor_sw128(sa + kASlot) : sdesc_kmajor_sw128(sa + kASlot);
+            // 16 K: 16 rows of 128 B (N/M-contiguous), or 32 B along the row
+            const uint32_t a_step = amn ? 128u : 2u, b_step = bmn ? 128u : 2u;
 #pragma unroll
             for (int k = 0; k < kTcBK / 16; ++k)
-              mma_f16_ss(d_tmem, a_desc + 2u * k, b_desc + b_step * k, idesc, (kk > 0 || k > 0) ? 1u : 0u);
+              mma_f16_ss(d_tmem, a_desc + a_step * k, b_desc + b_step * k, idesc, (kk > 0 || k > 0) ? 1u : 0u);
             mma_commit(empty_bar(s));
-            if (++s == ph.stages) s = 0;
+            if (++s == g.stages) s = 0;
           }
           if (!ok) break;
           mma_commit(accf_bar(acc));
           acc ^= 1;
           if (acc == 0) acc_phase ^= 1u;
         }
+        g0 = g1 + 1;
       }
       mma_commit(drain_bar);  // every MMA issued above completes before TMEM is freed
       wait_drain(drain_bar, 0, wd);
@@ -550,28 +679,39 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
-    for (int j = 0; j < num_phases && ok; ++j) {
-      const Phase ph = decode(phases[j], p.m);
-      if (ph.kind == kChainCopy) copy_phase(p);
-      for (int t = blockIdx.x; ok && t < ph.num_tiles; t += gridDim.x) {
+    uint32_t barrier = 0;
+    for (int g0 = 0; g0 < num_groups && ok;) {
+      const int g1 = phase_end(groups, g0, num_groups);
+      if (groups[g0].kind == kChainCopy) copy_phase(p);
+      for (int i = 0; ok; ++i) {
+        const Task tk = task_at(groups, g0, g1, cta, ctas, i);
+        if (tk.group < 0) break;
+        const Group g = groups[tk.group];  // a copy: the loops below read it from registers
+        if (g.kind == kChainCopy) continue;
         int mi, ni;
-        tile_of(ph, t, mi, ni);
-        const int r0 = mi * ph.bm + 32 * q;  // this warp's first row
-        const bool rows = 32 * q < ph.bm && r0 < p.m;
+        tile_of(g, tk.tile, mi, ni);
+        const bool coupling = g.kind == kChainCoupling, upd = g.kind == kChainUpdate;
+        const int r0 = mi * g.bm + 32 * q;  // this warp's first row
+        const int row_lim = coupling ? kSlot : g.rows;
+        const bool rows = 32 * q < g.bm && r0 < row_lim;
         const int64_t row = static_cast<int64_t>(r0) + lane;
-        const int c0 = ph.n0 + ni * ph.bn;
-        const bool upd = ph.kind == kChainUpdate;
-        // updates: the first 32 previous values are read while the MMAs run
-        uint4 old[4] = {};
-        if (upd && rows && row < p.m) load_old32(p, row, c0, ph.n_end, old);
+        const int c0 = g.n0 + ni * g.bn;
+        const bool from_b = g.old_from_b != 0;
+        // updates: the previous values of the first 64 columns (a 64-column
+        // tile's all) are read while the MMAs run
+        uint4 old[4] = {}, old2[4] = {};
+        if (upd && rows && row < row_lim) {
+          load_old32(p, from_b, row, c0, g.n_end, old);
+          load_old32(p, from_b, row, c0 + 32, g.n_end, old2);
+        }
         int good = 1;
         if (lane == 0) {
-          if (ph.kind == kChainProduct && rows) {
+          if (g.critical && rows) {
             // the other tiles of these rows must have read them
             const uint32_t* ctr = p.sync + kChainSyncRowGroup0 + r0 / 64;
-            if (ld_relaxed_gpu(ctr) < ph.rg_target) {
+            if (ld_relaxed_gpu(ctr) < g.rg_target) {
               const uint64_t t0 = globaltimer_ns();
-              while (ld_relaxed_gpu(ctr) < ph.rg_target) {
+              while (ld_relaxed_gpu(ctr) < g.rg_target) {
                 if (*abort_flag || launch_aborted(p)) {
                   *abort_flag = 1;
                   good = 0;
@@ -596,17 +736,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (rows) {
           const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
                                  static_cast<uint32_t>(acc * kAccCols);
+          uint16_t* drow = coupling ? p.W + static_cast<int64_t>(g.out_slot) * kSlot * kSlot + row * kSlot
+                                    : p.X + row * p.ldx;
+          const uint16_t* orow = from_b ? p.B + row * p.ldb : p.X + row * p.ldx;
 #pragma unroll 1
-          for (int c = 0; c < ph.bn / 32; ++c) {
+          for (int c = 0; c < g.bn / 32; ++c) {
             uint32_t v[32];
             tmem_ld_32x32b_x32(t_row + 32 * c, v);
-            // the next chunk's previous values, in flight during this one
+            // the previous values two chunks ahead, in flight during this one
             uint4 nxt[4] = {};
-            if (upd && row < p.m && c + 1 < ph.bn / 32) load_old32(p, row, c0 + 32 * (c + 1), ph.n_end, nxt);
+            if (upd && row < row_lim && c + 2 < g.bn / 32) load_old32(p, from_b, row, c0 + 32 * (c + 2), g.n_end, nxt);
             tmem_ld_wait(v);
-            if (row < p.m && c0 + 32 * c < ph.n_end) store32(p, ph.kind, row, c0 + 32 * c, ph.n_end, v, old);
+            const int col = c0 + 32 * c;
+            if (row < row_lim && col < g.n_end)
+              store32(p, upd, from_b, g.scale, drow + col, orow + col, col, g.n_end, v, old);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) old[i] = nxt[i];
+            for (int k = 0; k < 4; ++k) {
+              old[k] = old2[k];
+              old2[k] = nxt[k];
+            }
           }
         }
         tc_fence_before_sync();
@@ -618,7 +766,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // A role that gave up raised the CTA's abort flag; the barrier spreads
       // it (every epilogue warp calls it, whether its own tiles went well or
       // not, and all four take the leader's verdict).
-      if (j + 1 < num_phases) ok = grid_barrier(p, static_cast<uint32_t>(j) + 1u, abort_flag, passed, epi_ok);
+      g0 = g1 + 1;
+      if (g0 < num_groups) ok = grid_barrier(p, ++barrier, abort_flag, passed, epi_ok);
     }
   }
 
@@ -650,9 +799,10 @@ int chain_max_grid(int num_sms) {
   return g;
 }
 
-cudaError_t launch_trsm_chain(const CUtensorMap& x, const CUtensorMap& w, const CUtensorMap& wr,
-                              const CUtensorMap& a, const ChainArgs& args, int grid, cudaStream_t stream) {
-  if (grid < 1 || args.num_phases < 1 || args.num_phases > kChainMaxPhases) return cudaErrorInvalidValue;
+cudaError_t launch_trsm_chain(const CUtensorMap& x, const CUtensorMap& b, const CUtensorMap& w,
+                              const CUtensorMap& wr, const CUtensorMap& a, const ChainArgs& args, int grid,
+                              cudaStream_t stream) {
+  if (grid < 1 || args.num_groups < 1 || args.num_groups > kChainMaxGroups) return cudaErrorInvalidValue;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -682,7 +832,7 @@ cudaError_t launch_trsm_chain(const CUtensorMap& x, const CUtensorMap& w, const 
   const bool known = dev >= 0 && dev < kMaxDevices;
   if (!known || pdl_ok[dev] >= 0) {
     cfg.numAttrs = 2;
-    e = cudaLaunchKernelEx(&cfg, trsm_chain_kernel, x, w, wr, a, args);
+    e = cudaLaunchKernelEx(&cfg, trsm_chain_kernel, x, b, w, wr, a, args);
     if (e == cudaSuccess) {
       if (known) pdl_ok[dev] = 1;
       return e;
@@ -692,7 +842,7 @@ cudaError_t launch_trsm_chain(const CUtensorMap& x, const CUtensorMap& w, const 
     pdl_ok[dev] = -1;
   }
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, trsm_chain_kernel, x, w, wr, a, args);
+  return cudaLaunchKernelEx(&cfg, trsm_chain_kernel, x, b, w, wr, a, args);
 }
 
 // The -DHGEMM_DEBUG build's check word of this file (null otherwise).

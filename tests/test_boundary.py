@@ -29,7 +29,7 @@ def declared_functions():
 def declared_constants():
     text = open(HEADER, encoding="utf-8").read()
     out = {}
-    for name, val in re.findall(r"#define\s+(HGEMM_(?:OK|ERR_\w+|PATH_\w+|TRSM_(?:AUTO|SUBSTITUTION|RECURSIVE|CHAIN)))\s+\(?(-?\d+)\)?", text):
+    for name, val in re.findall(r"#define\s+(HGEMM_(?:OK|ERR_\w+|PATH_\w+|TRSM_(?:AUTO|SUBSTITUTION|RECURSIVE|CHAIN\w*)))\s+\(?(-?\d+)\)?", text):
         out[name] = int(val)
     return out
 
@@ -53,19 +53,20 @@ def test_binding_constants_match_header():
 
 
 def test_trsm_schedule_hooks(lib):
-    """The schedule override takes the four HGEMM_TRSM_* values' three
-    settable ones and nothing else; the last schedule is host state."""
+    """The schedule override takes the settable HGEMM_TRSM_* values and
+    nothing else; the last schedule is host state."""
     try:
-        for bad in (-1, tc.HGEMM_TRSM_SUBSTITUTION, 4, 99):
+        for bad in (-1, tc.HGEMM_TRSM_SUBSTITUTION, 6, 99):
             with pytest.raises(tc.HgemmError) as err:
                 tc.hgemm_force_trsm_schedule(bad)
             assert err.value.status == tc.HGEMM_ERR_INVALID_ARG
-        for ok in (tc.HGEMM_TRSM_RECURSIVE, tc.HGEMM_TRSM_CHAIN, tc.HGEMM_TRSM_AUTO):
+        for ok in (tc.HGEMM_TRSM_RECURSIVE, tc.HGEMM_TRSM_CHAIN, tc.HGEMM_TRSM_CHAIN_FUSED,
+                   tc.HGEMM_TRSM_CHAIN_SPLIT, tc.HGEMM_TRSM_AUTO):
             tc.hgemm_force_trsm_schedule(ok)
     finally:
         tc.hgemm_force_trsm_schedule(tc.HGEMM_TRSM_AUTO)
     assert tc.hgemm_trsm_last_schedule() in (0, tc.HGEMM_TRSM_SUBSTITUTION, tc.HGEMM_TRSM_RECURSIVE,
-                                             tc.HGEMM_TRSM_CHAIN)
+                                             tc.HGEMM_TRSM_CHAIN_FUSED, tc.HGEMM_TRSM_CHAIN_SPLIT)
 
 
 def test_status_strings(lib):
@@ -233,10 +234,10 @@ def test_trsm_workspace_argument_checks(lib):
     lib_ = tc.load()
     assert tc.hgemm_trsm_workspace_size(0) == 0
     assert tc.hgemm_trsm_workspace_size(-5) == 0
-    # 512 KiB per diagonal block of order <= 512, plus 4 KiB of synchronisation words
-    assert tc.hgemm_trsm_workspace_size(512) == 2 * 512 * 512 + 4096
-    assert tc.hgemm_trsm_workspace_size(513) == 2 * 2 * 512 * 512 + 4096
-    assert tc.hgemm_trsm_workspace_size(8192) == 16 * 2 * 512 * 512 + 4096 == tc.HGEMM_TRSM_NOALLOC_MAX_BYTES
+    # 512 KiB per diagonal block of order <= 512, one spare block, 4 KiB of synchronisation words
+    assert tc.hgemm_trsm_workspace_size(512) == 2 * 2 * 512 * 512 + 4096
+    assert tc.hgemm_trsm_workspace_size(513) == 3 * 2 * 512 * 512 + 4096
+    assert tc.hgemm_trsm_workspace_size(8192) == 17 * 2 * 512 * 512 + 4096 == tc.HGEMM_TRSM_NOALLOC_MAX_BYTES
     assert tc.hgemm_trsm_workspace_size(8193) > tc.HGEMM_TRSM_NOALLOC_MAX_BYTES
     n, m = 64, 8
     need = tc.hgemm_trsm_workspace_size(n)
@@ -248,7 +249,7 @@ def test_trsm_workspace_argument_checks(lib):
                                   kw.get("m", m), 1.0, a["W"], a["bytes"], None)
     assert call(W=None) == tc.HGEMM_ERR_INVALID_ARG
     # the inverses alone (an older workspace size) are still accepted; less is not
-    assert call(bytes=need - 4096 - 1) == tc.HGEMM_ERR_INVALID_ARG
+    assert call(bytes=need - 4096 - 2 * 512 * 512 - 1) == tc.HGEMM_ERR_INVALID_ARG
     assert call(W=W16 + 8) == tc.HGEMM_ERR_INVALID_ARG
     assert call(W=A16) == tc.HGEMM_ERR_ALIAS
     assert call(W=C16 - 16) == tc.HGEMM_ERR_ALIAS

@@ -28,7 +28,7 @@ def trsm_inputs(n, m, seed, c=1.0):
     return np.ascontiguousarray(a_col.T), np.ascontiguousarray(b_col.T)
 
 
-SCHEDULES = [False, "rec", "chain"]
+SCHEDULES = [False, "rec", "fused", "split"]
 
 
 class schedule:
@@ -37,7 +37,8 @@ class schedule:
     run; anything else the automatic choice."""
 
     def __init__(self, ws):
-        self.value = {"rec": tc.HGEMM_TRSM_RECURSIVE, "chain": tc.HGEMM_TRSM_CHAIN}.get(ws, tc.HGEMM_TRSM_AUTO)
+        self.value = {"rec": tc.HGEMM_TRSM_RECURSIVE, "chain": tc.HGEMM_TRSM_CHAIN,
+                      "fused": tc.HGEMM_TRSM_CHAIN_FUSED, "split": tc.HGEMM_TRSM_CHAIN_SPLIT}.get(ws, tc.HGEMM_TRSM_AUTO)
 
     def __enter__(self):
         tc.hgemm_force_trsm_schedule(self.value)
@@ -49,12 +50,13 @@ class schedule:
 def expected_schedule(ws, lda, ldx):
     """The schedule a solve must report: no workspace, or X not suited to
     TMA, substitution; "rec" (or a triangle TMA cannot read) the recursion;
-    "chain" the one launch."""
+    "fused" / "split" the one launch with that plan."""
     if not ws or ldx % 8:
-        return tc.HGEMM_TRSM_SUBSTITUTION
+        return (tc.HGEMM_TRSM_SUBSTITUTION,)
     if ws == "rec" or lda % 8:
-        return tc.HGEMM_TRSM_RECURSIVE
-    return tc.HGEMM_TRSM_CHAIN
+        return (tc.HGEMM_TRSM_RECURSIVE,)
+    return {"fused": (tc.HGEMM_TRSM_CHAIN_FUSED,), "split": (tc.HGEMM_TRSM_CHAIN_SPLIT,)}.get(
+        ws, (tc.HGEMM_TRSM_CHAIN_FUSED, tc.HGEMM_TRSM_CHAIN_SPLIT))
 
 
 def run_trsm(a, b, alpha=1.0, pad=(0, 0, 0), poison_upper=False, in_place=False, ws=False, op=None):
@@ -89,8 +91,8 @@ def run_trsm(a, b, alpha=1.0, pad=(0, 0, 0), poison_upper=False, in_place=False,
                 tc.hgemm_trsm_ws(da, lda, db, ldb, dx, ldx, n, m, alpha, work, need)
             else:
                 tc.hgemm_trsm_op(op, da, lda, db, ldb, dx, ldx, n, m, alpha, work, need)
-        if ws in ("rec", "chain"):
-            assert tc.hgemm_trsm_last_schedule() == expected_schedule(ws, lda, ldx)
+        if ws in ("rec", "chain", "fused", "split"):
+            assert tc.hgemm_trsm_last_schedule() in expected_schedule(ws, lda, ldx)
     elif op is not None:
         tc.hgemm_trsm_op(op, da, lda, db, ldb, dx, ldx, n, m, alpha, None, 0)
     else:
@@ -195,7 +197,7 @@ def test_trsm_8192_sampled_columns(ws):
         work = torch.empty(tc.hgemm_trsm_workspace_size(n), dtype=torch.uint8, device="cuda")
         with schedule(ws):
             tc.hgemm_trsm_ws(da, n, db, n, dx, n, n, m, 1.0, work)
-        assert tc.hgemm_trsm_last_schedule() == expected_schedule(ws, n, n)
+        assert tc.hgemm_trsm_last_schedule() in expected_schedule(ws, n, n)
     else:
         tc.hgemm_trsm(da, n, db, n, dx, n, n, m, 1.0)
     assert tc.hgemm_device_status() == tc.HGEMM_OK
@@ -248,9 +250,9 @@ def test_trsm_workspace_arguments():
     than the inverses, a misaligned one, one overlapping X."""
     torch = torch_cuda()
     assert tc.hgemm_trsm_workspace_size(0) == 0
-    assert tc.hgemm_trsm_workspace_size(256) == 2 * 512 * 512 + 4096
-    assert tc.hgemm_trsm_workspace_size(8192) == 16 * 2 * 512 * 512 + 4096
-    assert tc.hgemm_trsm_workspace_size(1000) == 2 * 2 * 512 * 512 + 4096   # blocks of 512 and 488
+    assert tc.hgemm_trsm_workspace_size(256) == 2 * 2 * 512 * 512 + 4096
+    assert tc.hgemm_trsm_workspace_size(8192) == 17 * 2 * 512 * 512 + 4096
+    assert tc.hgemm_trsm_workspace_size(1000) == 3 * 2 * 512 * 512 + 4096   # blocks of 512 and 488, a spare
     n, m = 512, 64
     a, b = trsm_inputs(n, m, seed=5)
     da, db = to_device(np.ascontiguousarray(a.T)), to_device(np.ascontiguousarray(b.T))
@@ -260,14 +262,14 @@ def test_trsm_workspace_arguments():
     with pytest.raises(tc.HgemmError):
         tc.hgemm_trsm_ws(da, n, db, n, dx, n, n, m, 1.0, None, need)
     # the inverses alone: accepted, and solved by the recursion's launches (the
-    # one-launch schedule needs the synchronisation words after them)
-    inverses = need - 4096
+    # one-launch schedule needs a spare block and the synchronisation words after them)
+    inverses = need - 4096 - 2 * 512 * 512
     with pytest.raises(tc.HgemmError):
         tc.hgemm_trsm_ws(da, n, db, n, dx, n, n, m, 1.0, work, inverses - 1)
     tc.hgemm_trsm_ws(da, n, db, n, dx, n, n, m, 1.0, work, inverses)
     assert tc.hgemm_trsm_last_schedule() == tc.HGEMM_TRSM_RECURSIVE
     tc.hgemm_trsm_ws(da, n, db, n, dx, n, n, m, 1.0, work, need)
-    assert tc.hgemm_trsm_last_schedule() == tc.HGEMM_TRSM_CHAIN
+    assert tc.hgemm_trsm_last_schedule() in (tc.HGEMM_TRSM_CHAIN_FUSED, tc.HGEMM_TRSM_CHAIN_SPLIT)
     assert tc.hgemm_device_status() == tc.HGEMM_OK
     with pytest.raises(tc.HgemmError):
         tc.hgemm_trsm_ws(da, n, db, n, dx, n, n, m, 1.0, work.data_ptr() + 8, need)
