@@ -236,9 +236,10 @@ def load_peaks():
 # The source file of each kernel; with the shared headers and the build
 # flags it determines the compiled kernel, so a recorded ncu traffic figure
 # stays valid while their hash is unchanged.
-KERNEL_SOURCES = {"hgemm_tc_kernel": "hgemm_tc.cu", "hgemm_tc2_kernel": "hgemm_tc2.cu",
-                  "hgemm_tc2w_kernel": "hgemm_tc2w.cu", "hgemm_skinny_kernel": "hgemm_skinny.cu",
-                  "hgemm_generic_kernel": "hgemm_generic.cu"}
+KERNEL_SOURCES = {"hgemm_tc_kernel": ("hgemm_tc.cu",), "hgemm_tc2_kernel": ("hgemm_tc2.cu",),
+                  "hgemm_tc2w_kernel": ("hgemm_tc2w.cu",), "hgemm_skinny_kernel": ("hgemm_skinny.cu",),
+                  "hgemm_generic_kernel": ("hgemm_generic.cu",),
+                  "trsm_chain_kernel": ("hgemm_trsm_chain.cu", "trsm_chain.h")}
 SHARED_SOURCES = ["internal.h", "kernel_common.cuh", "ptx.cuh", "debug.cuh"]
 
 
@@ -246,8 +247,8 @@ def kernel_sources_sha(kernel):
     h = hashlib.sha256()
     pkg = os.path.join(ROOT, "tensor_core_dense_fp16_gb300")
     files = [os.path.join(pkg, "csrc", n) for n in SHARED_SOURCES]
-    if kernel in KERNEL_SOURCES:
-        files.append(os.path.join(pkg, "csrc", KERNEL_SOURCES[kernel]))
+    for name in KERNEL_SOURCES.get(kernel, ()):
+        files.append(os.path.join(pkg, "csrc", name))
     files.append(os.path.join(pkg, "build.py"))
     for f in files:
         h.update(os.path.basename(f).encode())
@@ -774,8 +775,13 @@ def run_tri_ours(args, spec, a_col, b_col, world, rank, local):
     peaks, peak_src = load_peaks()
     peak = peaks["bf16_tflops"] * FP16_PER_BF16
     achieved = flops / (median_ms * 1e-3) / 1e12
+    # DRAM traffic of the chain kernel (the solve's dominant launch), from a
+    # committed ncu record of the current sources, per launch
+    traffic = (profiled_traffic("trsm_chain_kernel", args.workload, kernel_sources_sha("trsm_chain_kernel"))
+               if chain else None)
     roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-            "frac": achieved / peak, "traffic": None,
+            "frac": achieved / peak, "traffic": traffic,
+            "traffic_kernel": "trsm_chain_kernel" if chain else None,
             "peak_source": f"{peak_src}: bf16_tflops (burst) x {FP16_PER_BF16} fp16/bf16",
             "timing": "median call", "kernel": CHAIN_KERNELS if chain else ops["kernel"],
             "algorithmic_flops": flops, "algorithmic_bytes": 2.0 * (n * (n + 1) / 2 + 2 * n * m)}

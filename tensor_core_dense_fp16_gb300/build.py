@@ -29,7 +29,7 @@ DEBUG_DIR = os.path.join(OUT_DIR, "debug")
 DEBUG_LIB = os.path.join(DEBUG_DIR, "libhgemm.so")
 SOURCES = ["hgemm_api.cu", "hgemm_tc.cu", "hgemm_tc2.cu", "hgemm_tc2w.cu", "hgemm_skinny.cu", "hgemm_generic.cu", "hgemm_trsm.cu",
            "hgemm_trileaf.cu", "hgemm_trsm_chain.cu"]
-HEADERS = ["ptx.cuh", "internal.h", "kernel_common.cuh", "debug.cuh"]
+HEADERS = ["ptx.cuh", "internal.h", "kernel_common.cuh", "debug.cuh", "trsm_chain.h"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",

@@ -23,6 +23,7 @@
 #include "hgemm.h"
 #include "debug.cuh"
 #include "internal.h"
+#include "trsm_chain.h"
 
 namespace {
 

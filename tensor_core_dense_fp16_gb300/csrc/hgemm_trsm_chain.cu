@@ -58,6 +58,7 @@
 #include <cuda_fp16.h>
 
 #include "internal.h"
+#include "trsm_chain.h"
 #include "kernel_common.cuh"
 #include "ptx.cuh"
 
