@@ -505,8 +505,10 @@ def timed_region(torch, dev, local, stream, step, flush, steps, dist):
 # events on the launching stream, median).
 CONFIG_WORKLOADS = ["hgemm_256", "hgemm_256_int", "hgemm_2048", "hgemm_1000_ragged",
                     "hgemm_4096x256x4096_skinny"]
-KERNEL_OF_PATH = {2: "hgemm_tc_kernel", 5: "hgemm_tc2_kernel", 6: "hgemm_tc2w_kernel",
-                  3: "hgemm_skinny_kernel", 4: "hgemm_generic_kernel"}
+KERNEL_OF_PATH = {2: "hgemm_tc_kernel", 7: "hgemm_tc_kernel", 5: "hgemm_tc2_kernel",
+                  6: "hgemm_tc2w_kernel", 3: "hgemm_skinny_kernel", 4: "hgemm_generic_kernel"}
+TILES_OF_PATH = {2: "128x256", 7: "128x64", 5: "256x256 pairs", 6: "256x512 pairs",
+                 3: "split K", 4: "generic"}
 
 
 def roofline_of(flops, nbytes, ms, peaks):
@@ -572,7 +574,8 @@ def time_configs(torch, tc, dev, stream, flush, peaks, launches=50, warmup=5, fl
         med = statistics.median(times)
         rec = {"M": M, "N": N, "K": K, "seed": spec["seed"], "values": spec["kind"],
                "launches": launches, "ms_median": med, "ms_mean": statistics.fmean(times),
-               "ms_min": min(times), "path": KERNEL_OF_PATH.get(path, f"path {path}")}
+               "ms_min": min(times), "path": KERNEL_OF_PATH.get(path, f"path {path}"),
+               "tiles": TILES_OF_PATH.get(path, "?")}
         rec.update(roofline_of(flops_of(spec), bytes_of(spec), med, peaks))
         if floor_ms is not None:
             rec["frac_with_floor"] = (rec["roofline_us"] * 1e-3 + floor_ms) / med
@@ -863,7 +866,7 @@ def run_ours(args, spec, a, b, world, rank, local):
         # operands only (the pair kernel stands in for it)
         tma = lda % 8 == 0 and ldb % 8 == 0 and N % 8 == 0
         path = tc.hgemm_select_path(da, db, dc, M, N, K) if tma else tc.HGEMM_PATH_GENERIC
-        if path == tc.HGEMM_PATH_TC:
+        if path in (tc.HGEMM_PATH_TC, tc.HGEMM_PATH_TC_NARROW):
             path = tc.HGEMM_PATH_TC_PAIR
     else:
         path = tc.hgemm_select_path(da, db, dc, M, N, K)
@@ -931,7 +934,8 @@ def run_ours(args, spec, a, b, world, rank, local):
 
     # ---- roofline of the dominant (only) kernel
     peaks, peak_src = load_peaks()
-    kernel = {tc.HGEMM_PATH_TC: "hgemm_tc_kernel", tc.HGEMM_PATH_TC_PAIR: "hgemm_tc2_kernel",
+    kernel = {tc.HGEMM_PATH_TC: "hgemm_tc_kernel", tc.HGEMM_PATH_TC_NARROW: "hgemm_tc_kernel",
+              tc.HGEMM_PATH_TC_PAIR: "hgemm_tc2_kernel",
               tc.HGEMM_PATH_TC_WIDE: "hgemm_tc2w_kernel",
               tc.HGEMM_PATH_SKINNY: "hgemm_skinny_kernel",
               tc.HGEMM_PATH_GENERIC: "hgemm_generic_kernel"}.get(path, f"path {path}")

@@ -74,6 +74,7 @@ typedef uint16_t hgemm_half_t; /* IEEE binary16 bit pattern */
 #define HGEMM_PATH_GENERIC 4  /* tcgen05 kernel fed by plain loads: any alignment */
 #define HGEMM_PATH_TC_PAIR 5  /* tcgen05 + TMA persistent kernel, CTA pairs per 256×256 tile */
 #define HGEMM_PATH_TC_WIDE 6  /* tcgen05 + TMA persistent kernel, CTA pairs per 256×512 tile */
+#define HGEMM_PATH_TC_NARROW 7 /* the HGEMM_PATH_TC kernel on 128×64 tiles: outputs one wave covers */
 
 /* Largest M, N or K accepted (TMA coordinates are signed 32-bit). */
 #define HGEMM_TRMM_MAX_N 16384          /* largest triangle hgemm_trmm accepts */
@@ -423,8 +424,8 @@ HGEMM_API int hgemm_select_path(const void *A, const void *B, const void *C,
 /*
  * hgemm_force_path — overrides path selection for later calls in this
  * process (testing and profiling). `path` is HGEMM_PATH_TC,
- * HGEMM_PATH_TC_PAIR, HGEMM_PATH_TC_WIDE, HGEMM_PATH_SKINNY or
- * HGEMM_PATH_GENERIC, or -1 to
+ * HGEMM_PATH_TC_NARROW, HGEMM_PATH_TC_PAIR, HGEMM_PATH_TC_WIDE,
+ * HGEMM_PATH_SKINNY or HGEMM_PATH_GENERIC, or -1 to
  * restore automatic selection. A forced TMA path still falls back to GENERIC
  * when the operands are not aligned for TMA. In hgemm_trmm a forced path runs
  * every off-diagonal update as a product of its own (none is carried by the

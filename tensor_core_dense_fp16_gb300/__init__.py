@@ -25,7 +25,7 @@ __all__ = [
     "HGEMM_ERR_CUDA", "HGEMM_ERR_TIMEOUT", "HGEMM_ERR_DEBUG_CHECK", "hgemm_debug_build", "hgemm_debug_code",
     "hgemm_debug_selftest", "HGEMM_PATH_NONE", "HGEMM_PATH_ZERO",
     "HGEMM_PATH_TC", "HGEMM_PATH_SKINNY", "HGEMM_PATH_GENERIC", "HGEMM_PATH_TC_PAIR",
-    "HGEMM_PATH_TC_WIDE", "HGEMM_MAX_DIM",
+    "HGEMM_PATH_TC_WIDE", "HGEMM_PATH_TC_NARROW", "HGEMM_MAX_DIM",
     "HgemmError", "library_path", "load", "hgemm", "hgemm_host", "hgemm_select_path",
     "hgemm_force_path", "hgemm_device_status", "hgemm_last_cuda_error",
     "hgemm_status_string", "hgemm_version", "hgemm_set_wait_timeout", "hgemm_debug_inject",
@@ -65,6 +65,7 @@ HGEMM_PATH_SKINNY = 3
 HGEMM_PATH_GENERIC = 4
 HGEMM_PATH_TC_PAIR = 5
 HGEMM_PATH_TC_WIDE = 6
+HGEMM_PATH_TC_NARROW = 7
 
 HGEMM_MAX_DIM = 0x7FFFFFFF
 

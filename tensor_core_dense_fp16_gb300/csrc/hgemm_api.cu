@@ -254,7 +254,8 @@ int choose_path(const Gemm& g, const hg::DeviceProfile& prof, bool fused, int* s
   const int path = hg::choose_tma_path(M, N, K, prof, forced, fs >> 10, fs & 1023, fused, split, tile_n);
   // M- or N-contiguous operands: the wide, pair and split-K kernels read
   // them as MN-major tiles; the single-CTA kernel takes K-major ones only
-  if ((g.a_mn || g.b_mn) && path == HGEMM_PATH_TC) return HGEMM_PATH_TC_PAIR;
+  if ((g.a_mn || g.b_mn) && (path == HGEMM_PATH_TC || path == HGEMM_PATH_TC_NARROW))
+    return HGEMM_PATH_TC_PAIR;
   return path;
 }
 
@@ -316,12 +317,21 @@ int choose_tma_path(int64_t M, int64_t N, int64_t K, const DeviceProfile& dev, i
     }
     return found;
   };
-  if (forced == HGEMM_PATH_TC || forced == HGEMM_PATH_TC_PAIR || forced == HGEMM_PATH_TC_WIDE)
+  if (forced == HGEMM_PATH_TC || forced == HGEMM_PATH_TC_NARROW || forced == HGEMM_PATH_TC_PAIR ||
+      forced == HGEMM_PATH_TC_WIDE)
     return forced;
   if (forced == HGEMM_PATH_SKINNY) return choose(false) ? HGEMM_PATH_SKINNY : HGEMM_PATH_TC_PAIR;
   // Exchanging the partial sums costs a few microseconds; splitting pays
   // when each pair would otherwise walk a long K (48 blocks or more).
   if (num_kb >= 48 && choose(true)) return HGEMM_PATH_SKINNY;
+  // An output that one wave of 128×64 tiles covers: one CTA per tile, no
+  // cluster. With a short K the launch is bound by its fixed chain of
+  // dependent steps, which the single-CTA kernel keeps shorter than the
+  // pair kernel's (measured, flushed: 256³ 8.2 against 8.9 µs, 1000³ 12.3
+  // against 14.3 µs), though each CTA reads 20% more operand bytes than in
+  // the pair kernel's 64-column parts.
+  const int64_t narrow_tiles = ((M + kTcBM - 1) / kTcBM) * ((N + kNarrowBN - 1) / kNarrowBN);
+  if (narrow_tiles <= dev.num_sms) return HGEMM_PATH_TC_NARROW;
   // A CTA pair covers 256 rows; with 128 rows or fewer half of it would idle.
   if (M <= kTcBM) return HGEMM_PATH_TC;
   // 256×512 tiles move 25% fewer operand bytes per flop than 256×256 ones
@@ -389,8 +399,9 @@ int encode_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, i
   return HGEMM_OK;
 }
 
-int run_tc(const Gemm& g, const hg::EpiArgs& epi, const DeviceState& dev,
-       cudaStream_t stream) {
+// bn: the tile width, hg::kTcBN (128×256 tiles) or hg::kNarrowBN (128×64).
+int run_tc(const Gemm& g, const hg::EpiArgs& epi, const DeviceState& dev, cudaStream_t stream,
+           int bn) {
   const void* A = g.A;
   const void* B = g.B;
   void* C = g.C;
@@ -398,14 +409,14 @@ int run_tc(const Gemm& g, const hg::EpiArgs& epi, const DeviceState& dev,
   CUtensorMap ma, mb, mc;
   int rc;
   if ((rc = encode_map(&ma, A, M, K, g.lda, hg::kTcBM, hg::kTcBK)) != HGEMM_OK) return rc;
-  if ((rc = encode_map(&mb, B, N, K, g.ldb, hg::kTcBN, hg::kTcBK)) != HGEMM_OK) return rc;
+  if ((rc = encode_map(&mb, B, N, K, g.ldb, bn, hg::kTcBK)) != HGEMM_OK) return rc;
   if ((rc = encode_map(&mc, C, M, N, g.ldc, hg::kEpiRows, hg::kEpiCols)) != HGEMM_OK) return rc;
   hg::TcArgs args{};
   args.M = static_cast<int>(M);
   args.N = static_cast<int>(N);
   args.K = static_cast<int>(K);
   args.num_m = static_cast<int>((M + hg::kTcBM - 1) / hg::kTcBM);
-  args.num_n = static_cast<int>((N + hg::kTcBN - 1) / hg::kTcBN);
+  args.num_n = static_cast<int>((N + bn - 1) / bn);
   args.num_kb = static_cast<int>((K + hg::kTcBK - 1) / hg::kTcBK);
   const int64_t tiles = static_cast<int64_t>(args.num_m) * args.num_n;
   if (tiles > 0x7FFFFFFF) return HGEMM_ERR_INVALID_ARG;
@@ -419,7 +430,8 @@ int run_tc(const Gemm& g, const hg::EpiArgs& epi, const DeviceState& dev,
   args.epi = epi;
   args.C = static_cast<const uint16_t*>(C);
   args.ldc = g.ldc;
-  cudaError_t e = hg::launch_tc_128x256(ma, mb, mc, args, stream);
+  cudaError_t e = bn == hg::kNarrowBN ? hg::launch_tc_128x64(ma, mb, mc, args, stream)
+                                      : hg::launch_tc_128x256(ma, mb, mc, args, stream);
   return e == cudaSuccess ? HGEMM_OK : cuda_fail(e);
 }
 
@@ -600,7 +612,9 @@ int dispatch(const Gemm& g, const hg::EpiArgs& epi, const DeviceState& dev, cuda
       e = hg::launch_empty_sum(static_cast<uint16_t*>(g.C), g.M, g.N, g.ldc, epi, stream);
       return e == cudaSuccess ? HGEMM_OK : cuda_fail(e);
     case HGEMM_PATH_TC:
-      return run_tc(g, epi, dev, stream);
+      return run_tc(g, epi, dev, stream, hg::kTcBN);
+    case HGEMM_PATH_TC_NARROW:
+      return run_tc(g, epi, dev, stream, hg::kNarrowBN);
     case HGEMM_PATH_TC_PAIR:
       return run_tc_pair(g, epi, dev, stream);
     case HGEMM_PATH_TC_WIDE:
@@ -1567,7 +1581,7 @@ int hgemm_force_trsm_schedule(int schedule) {
 int hgemm_trsm_last_schedule(void) { return t_trsm_schedule; }
 
 int hgemm_force_path(int path) {
-  if (path != -1 && path != HGEMM_PATH_TC && path != HGEMM_PATH_TC_PAIR &&
+  if (path != -1 && path != HGEMM_PATH_TC && path != HGEMM_PATH_TC_NARROW && path != HGEMM_PATH_TC_PAIR &&
       path != HGEMM_PATH_TC_WIDE && path != HGEMM_PATH_SKINNY && path != HGEMM_PATH_GENERIC)
     return HGEMM_ERR_INVALID_ARG;
   g_forced_path.store(path);

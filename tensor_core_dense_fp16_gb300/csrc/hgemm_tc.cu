@@ -337,6 +337,18 @@ cudaError_t launch_tc_128x256(const CUtensorMap& a, const CUtensorMap& b, const 
   return cudaLaunchKernelEx(&l.cfg, kern, a, b, c, args);
 }
 
+cudaError_t launch_tc_128x64(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
+                             const TcArgs& args, cudaStream_t stream) {
+  using Cfg = TcCfg<64, 8>;
+  static std::atomic<bool> attr_done[2][64];
+  const bool fused = args.epi.mode != 0;
+  auto kern = fused ? hgemm_tc_kernel<64, 8, true> : hgemm_tc_kernel<64, 8, false>;
+  cudaError_t e = ensure_smem_attr(kern, Cfg::SMEM_BYTES, attr_done[fused ? 1 : 0]);
+  if (e != cudaSuccess) return e;
+  PdlLaunch l(dim3(static_cast<unsigned>(args.grid)), dim3(Cfg::THREADS), Cfg::SMEM_BYTES, stream);
+  return cudaLaunchKernelEx(&l.cfg, kern, a, b, c, args);
+}
+
 cudaError_t launch_floor(int pair_config, int num_sms, int smem_bytes, cudaStream_t stream) {
   if (!pair_config) {
     PdlLaunch l(dim3(1), dim3(32), 0, stream);

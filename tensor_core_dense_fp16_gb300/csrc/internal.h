@@ -111,6 +111,8 @@ struct PdlLaunch {
 // error, if any). Shared-memory attributes are set on first use per device.
 cudaError_t launch_tc_128x256(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
                               const TcArgs& args, cudaStream_t stream);
+cudaError_t launch_tc_128x64(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
+                             const TcArgs& args, cudaStream_t stream);
 // b_part: the B map with part_cols / 2-row boxes, for the tile parts of the last wave.
 cudaError_t launch_tc_pair(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b_part,
                            const CUtensorMap& c, const TcArgs& args, cudaStream_t stream);
@@ -217,6 +219,7 @@ int choose_tma_path(int64_t M, int64_t N, int64_t K, const DeviceProfile& dev, i
 // Tile geometry of the tensor-core path, for the host-side tensor maps.
 constexpr int kTcBM = 128;
 constexpr int kTcBN = 256;
+constexpr int kNarrowBN = 64;  // single-CTA kernel for outputs of one wave of 128×64 tiles
 constexpr int kTcBK = 64;
 constexpr int kPairBN = 256;   // pair kernel: 256×256 tiles, 128 B rows per CTA
 constexpr int kPairRingBytes = 6 * 32768;  // pair kernel: six whole-tile stages of A and B

@@ -33,8 +33,8 @@ def main() -> int:
         assert st == tc.HGEMM_OK, f"{what}: status {st}, check code {tc.hgemm_debug_code()}"
 
     # the product on every path, ragged shapes
-    for path in (tc.HGEMM_PATH_TC, tc.HGEMM_PATH_TC_PAIR, tc.HGEMM_PATH_TC_WIDE, tc.HGEMM_PATH_SKINNY,
-                 tc.HGEMM_PATH_GENERIC):
+    for path in (tc.HGEMM_PATH_TC, tc.HGEMM_PATH_TC_NARROW, tc.HGEMM_PATH_TC_PAIR, tc.HGEMM_PATH_TC_WIDE,
+                 tc.HGEMM_PATH_SKINNY, tc.HGEMM_PATH_GENERIC):
         for M, N, K in [(300, 264, 200), (1000, 1000, 1000), (129, 8, 3000)]:
             a, b = synth.operands(M, N, K, seed=M + N + K, kind="uniform")
             da, db = to_device(a), to_device(b)

@@ -94,16 +94,21 @@ def test_path_selection(lib):
     # few tiles and a long K (48 K blocks or more): split K over clusters of pairs
     assert sel(A16, B16, C16, 4096, 256, 4096) == tc.HGEMM_PATH_SKINNY
     assert sel(A16, B16, C16, 512, 512, 3072) == tc.HGEMM_PATH_SKINNY
-    # a shorter K is not worth the exchange of partial sums: 256-wide pair
-    # tiles cut into 128- or 64-column parts
-    assert sel(A16, B16, C16, 1000, 1000, 1000) == tc.HGEMM_PATH_TC_PAIR
-    assert sel(A16, B16, C16, 256, 256, 256) == tc.HGEMM_PATH_TC_PAIR
-    assert sel(A16, B16, C16, 4096, 256, 2048) == tc.HGEMM_PATH_TC_PAIR
+    # a shorter K is not worth the exchange of partial sums; an output that
+    # one wave of 128x64 tiles covers (152 on a GB300) takes one CTA per tile
+    assert sel(A16, B16, C16, 1000, 1000, 1000) == tc.HGEMM_PATH_TC_NARROW
+    assert sel(A16, B16, C16, 256, 256, 256) == tc.HGEMM_PATH_TC_NARROW
+    assert sel(A16, B16, C16, 4096, 256, 2048) == tc.HGEMM_PATH_TC_NARROW
+    assert sel(A16, B16, C16, 19 * 128, 8 * 64, 1024) == tc.HGEMM_PATH_TC_NARROW   # 152 tiles
+    # one more tile row: 256-wide pair tiles, cut into 128- or 64-column parts
+    assert sel(A16, B16, C16, 20 * 128, 8 * 64, 1024) == tc.HGEMM_PATH_TC_PAIR
+    assert sel(A16, B16, C16, 4096, 512, 2048) == tc.HGEMM_PATH_TC_PAIR
     # more than half of the pairs busy without splitting: no split
     assert sel(A16, B16, C16, 256 * 39, 256, 4096) == tc.HGEMM_PATH_TC_PAIR
     # too little K to split: one K block
-    assert sel(A16, B16, C16, 4096, 256, 64) == tc.HGEMM_PATH_TC_PAIR
-    assert sel(A16, B16, C16, 128, 256, 64) == tc.HGEMM_PATH_TC
+    assert sel(A16, B16, C16, 4096, 256, 64) == tc.HGEMM_PATH_TC_NARROW
+    assert sel(A16, B16, C16, 8192, 256, 64) == tc.HGEMM_PATH_TC_PAIR
+    assert sel(A16, B16, C16, 128, 256, 64) == tc.HGEMM_PATH_TC_NARROW
     # 128 rows or fewer with many tiles: one CTA per 128x256 tile
     assert sel(A16, B16, C16, 128, 16384, 4096) == tc.HGEMM_PATH_TC
     # TMA needs 16-byte row pitches and 16-byte base addresses
@@ -113,8 +118,10 @@ def test_path_selection(lib):
     assert sel(A16, B16 + 8, C16, 64, 64, 64) == tc.HGEMM_PATH_GENERIC
     assert sel(A16, B16, C16 + 4, 64, 64, 64) == tc.HGEMM_PATH_GENERIC
     # M is free: any M works with TMA
-    assert sel(A16, B16, C16, 1001, 64, 64) == tc.HGEMM_PATH_TC_PAIR
-    assert sel(A16, B16, C16, 1, 64, 64) == tc.HGEMM_PATH_TC
+    assert sel(A16, B16, C16, 1001, 64, 64) == tc.HGEMM_PATH_TC_NARROW
+    assert sel(A16, B16, C16, 1200, 1024, 64) == tc.HGEMM_PATH_TC_PAIR
+    assert sel(A16, B16, C16, 1, 64, 64) == tc.HGEMM_PATH_TC_NARROW
+    assert sel(A16, B16, C16, 1, 10240, 64) == tc.HGEMM_PATH_TC
     assert sel(A16, B16, C16, 1, 64, 4096) == tc.HGEMM_PATH_SKINNY
 
 
@@ -124,6 +131,8 @@ def test_forced_paths(lib):
         assert tc.hgemm_select_path(A16, B16, C16, 256, 256, 256) == tc.HGEMM_PATH_GENERIC
         tc.hgemm_force_path(tc.HGEMM_PATH_TC)
         assert tc.hgemm_select_path(A16, B16, C16, 256, 256, 256) == tc.HGEMM_PATH_TC
+        tc.hgemm_force_path(tc.HGEMM_PATH_TC_NARROW)
+        assert tc.hgemm_select_path(A16, B16, C16, 8192, 8192, 8192) == tc.HGEMM_PATH_TC_NARROW
         tc.hgemm_force_path(tc.HGEMM_PATH_TC_PAIR)
         assert tc.hgemm_select_path(A16, B16, C16, 64, 256, 256) == tc.HGEMM_PATH_TC_PAIR
         tc.hgemm_force_path(tc.HGEMM_PATH_TC_WIDE)
@@ -139,7 +148,7 @@ def test_forced_paths(lib):
             tc.hgemm_force_path(77)
     finally:
         tc.hgemm_force_path(-1)
-    assert tc.hgemm_select_path(A16, B16, C16, 256, 256, 256) == tc.HGEMM_PATH_TC_PAIR
+    assert tc.hgemm_select_path(A16, B16, C16, 256, 256, 256) == tc.HGEMM_PATH_TC_NARROW
 
 
 def test_forced_split_configuration(lib):
@@ -311,9 +320,9 @@ def test_alias_detection(lib):
     # C overlapping the head of B
     assert lib.hgemm_select_path(A16, B16, B16 - 16, M, N, K) == tc.HGEMM_ERR_ALIAS
     # adjacent but disjoint is fine
-    assert lib.hgemm_select_path(A16, B16, A16 + a_bytes, M, N, K) == tc.HGEMM_PATH_TC
+    assert lib.hgemm_select_path(A16, B16, A16 + a_bytes, M, N, K) == tc.HGEMM_PATH_TC_NARROW
     # A and B may alias each other (both are read-only)
-    assert lib.hgemm_select_path(A16, A16, C16, M, N, K) == tc.HGEMM_PATH_TC
+    assert lib.hgemm_select_path(A16, A16, C16, M, N, K) == tc.HGEMM_PATH_TC_NARROW
 
 
 def test_binding_type_checks():

@@ -12,7 +12,7 @@ from gpu_helpers import assert_close, oracle_threads, to_device, torch_cuda
 
 pytestmark = pytest.mark.gpu
 
-PATHS = [None, tc.HGEMM_PATH_TC, tc.HGEMM_PATH_TC_PAIR, tc.HGEMM_PATH_TC_WIDE,
+PATHS = [None, tc.HGEMM_PATH_TC, tc.HGEMM_PATH_TC_NARROW, tc.HGEMM_PATH_TC_PAIR, tc.HGEMM_PATH_TC_WIDE,
          tc.HGEMM_PATH_SKINNY, tc.HGEMM_PATH_GENERIC]
 EPILOGUES = [  # alpha, beta, with bias, relu
     (1.0, 0.0, True, True),      # the page's matmul + bias + ReLU

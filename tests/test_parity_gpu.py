@@ -21,8 +21,8 @@ from gpu_helpers import assert_close, oracle_threads, run_gpu, to_device, torch_
 pytestmark = pytest.mark.gpu
 
 
-TMA_PATHS = [None, tc.HGEMM_PATH_TC, tc.HGEMM_PATH_TC_PAIR, tc.HGEMM_PATH_TC_WIDE,
-             tc.HGEMM_PATH_SKINNY]   # None: automatic choice
+TMA_PATHS = [None, tc.HGEMM_PATH_TC, tc.HGEMM_PATH_TC_NARROW, tc.HGEMM_PATH_TC_PAIR,
+             tc.HGEMM_PATH_TC_WIDE, tc.HGEMM_PATH_SKINNY]   # None: automatic choice
 
 
 @pytest.mark.parametrize("path", TMA_PATHS)
@@ -105,7 +105,8 @@ def test_8192_cube_both_operands_scaled():
     assert worst < 1e-2, f"max |err| / sigma = {worst:.3g}"
 
 
-@pytest.mark.parametrize("path", [tc.HGEMM_PATH_TC, tc.HGEMM_PATH_TC_PAIR, tc.HGEMM_PATH_TC_WIDE,
+@pytest.mark.parametrize("path", [tc.HGEMM_PATH_TC, tc.HGEMM_PATH_TC_NARROW, tc.HGEMM_PATH_TC_PAIR,
+                                  tc.HGEMM_PATH_TC_WIDE,
                                   tc.HGEMM_PATH_SKINNY, tc.HGEMM_PATH_GENERIC])
 def test_subnormal_operands_are_honoured(path):
     """FP16 subnormal inputs keep their value (no flush to zero): each case's
@@ -153,7 +154,8 @@ def _edge_cases(aligned):
     return sorted(set(keep) | {cases[i] for i in picked})
 
 
-@pytest.mark.parametrize("path", [tc.HGEMM_PATH_TC, tc.HGEMM_PATH_TC_PAIR, tc.HGEMM_PATH_TC_WIDE,
+@pytest.mark.parametrize("path", [tc.HGEMM_PATH_TC, tc.HGEMM_PATH_TC_NARROW, tc.HGEMM_PATH_TC_PAIR,
+                                  tc.HGEMM_PATH_TC_WIDE,
                                   tc.HGEMM_PATH_SKINNY])
 @pytest.mark.parametrize("M,N,K", _edge_cases(aligned=True))
 def test_edges_tensor_core_paths(M, N, K, path):
@@ -161,7 +163,7 @@ def test_edges_tensor_core_paths(M, N, K, path):
     ref = oracle.hgemm(a, b, nthreads=oracle_threads())
     # with 16-byte aligned buffers (as torch allocates) these take a TMA path
     assert tc.hgemm_select_path(0x10000000, 0x20000000, 0x30000000, M, N, K) in (
-        tc.HGEMM_PATH_TC, tc.HGEMM_PATH_TC_PAIR, tc.HGEMM_PATH_SKINNY)
+        tc.HGEMM_PATH_TC, tc.HGEMM_PATH_TC_NARROW, tc.HGEMM_PATH_TC_PAIR, tc.HGEMM_PATH_SKINNY)
     assert_close(run_gpu(a, b, path=path), ref, what=f"path {path} {M}x{N}x{K}")
 
 
@@ -207,7 +209,8 @@ def test_misaligned_pointers_take_the_generic_path():
     assert_close(bc[1:].cpu().numpy().reshape(M, N), ref, what="misaligned")
 
 
-@pytest.mark.parametrize("path", [tc.HGEMM_PATH_TC, tc.HGEMM_PATH_TC_PAIR, tc.HGEMM_PATH_TC_WIDE,
+@pytest.mark.parametrize("path", [tc.HGEMM_PATH_TC, tc.HGEMM_PATH_TC_NARROW, tc.HGEMM_PATH_TC_PAIR,
+                                  tc.HGEMM_PATH_TC_WIDE,
                                   tc.HGEMM_PATH_SKINNY, tc.HGEMM_PATH_GENERIC])
 def test_guard_bands_untouched(path):
     """Nothing outside C is written: C sits inside a sentinel-filled buffer."""

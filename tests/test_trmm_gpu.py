@@ -112,7 +112,8 @@ def test_trmm_repeatable():
         assert np.array_equal(run_trmm(a, b).view(np.uint16), first.view(np.uint16))
 
 
-@pytest.mark.parametrize("path", [None, tc.HGEMM_PATH_TC_PAIR, tc.HGEMM_PATH_TC, tc.HGEMM_PATH_GENERIC])
+@pytest.mark.parametrize("path", [None, tc.HGEMM_PATH_TC_PAIR, tc.HGEMM_PATH_TC, tc.HGEMM_PATH_TC_NARROW,
+                                  tc.HGEMM_PATH_GENERIC])
 def test_trmm_equal_levels(path):
     """n = 2048: each level of the recursion holds equal updates at a constant
     stride (2 of 1024 columns, then 4 of 512, 8 of 256 ...). On the pair path

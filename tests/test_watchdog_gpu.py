@@ -22,7 +22,8 @@ def test_hook_arguments_are_checked():
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("path", [tc.HGEMM_PATH_TC, tc.HGEMM_PATH_TC_PAIR, tc.HGEMM_PATH_TC_WIDE,
+@pytest.mark.parametrize("path", [tc.HGEMM_PATH_TC, tc.HGEMM_PATH_TC_NARROW, tc.HGEMM_PATH_TC_PAIR,
+                                  tc.HGEMM_PATH_TC_WIDE,
                                   tc.HGEMM_PATH_SKINNY])
 def test_withheld_arrival_times_out_and_the_context_survives(path):
     torch = torch_cuda()
