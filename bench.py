@@ -196,7 +196,14 @@ def parse_args():
                     help="TRSM workloads: hgemm_trsm without a workspace (substitution for every diagonal block)")
     ap.add_argument("--epilogue", choices=sorted(EPILOGUES), default="none",
                     help="fused epilogue through hgemm_ex (default: the plain product)")
+    ap.add_argument("--force-path", choices=sorted(FORCED_PATHS), default="auto",
+                    help="profiling aid, GEMM workloads: run the product on this kernel (hgemm_force_path) "
+                         "instead of the one the library chooses")
     return ap.parse_args()
+
+
+# hgemm_force_path values by name (the HGEMM_PATH_* constants of hgemm.h)
+FORCED_PATHS = {"auto": -1, "tc": 2, "skinny": 3, "generic": 4, "pair": 5, "wide": 6, "narrow": 7}
 
 
 # Fused epilogues of hgemm_ex: (alpha, beta, with bias, relu). bias_relu is the
@@ -840,6 +847,7 @@ def run_ours(args, spec, a, b, world, rank, local):
     import tensor_core_dense_fp16_gb300 as tc
 
     tc.load()  # fails loudly if the extension is missing
+    tc.hgemm_force_path(FORCED_PATHS[args.force_path])
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     dist = None
@@ -998,6 +1006,7 @@ def run_ours(args, spec, a, b, world, rank, local):
                        "l2": "flushed before every timed launch (write of 2x L2 size, "
                              "outside the events)",
                        "inputs": "resident in HBM", "path": kernel,
+                       "forced_path": args.force_path,
                        "epilogue": args.epilogue, "a_layout": args.a_layout,
                        "b_layout": args.b_layout,
                        "parallelism": f"replicas x{world}"},
