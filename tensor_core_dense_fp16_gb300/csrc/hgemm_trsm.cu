@@ -310,11 +310,27 @@ __device__ __forceinline__ void trsm_leaf_body(const uint16_t* __restrict__ A, i
         *reinterpret_cast<uint4*>(dst + 8 * q) = make_uint4(0u, 0u, 0u, 0u);
     }
   };
-  if (staged) stage_group(FWD ? 0 : groups - 1);
+  // Against the identity, the right-hand sides j0 .. j0+COLS-1 have zero
+  // solutions past the last of them (transposed: the inverse of Lᵀ is upper
+  // triangular) or before the first (forward: L⁻¹ is lower triangular); the
+  // groups holding only such rows have b = 0, so x_g = 0 and their updates
+  // change nothing: they are skipped (their rows keep the identity's 0).
+  int g_begin = FWD ? 0 : groups - 1, steps = groups;
+  if (identity) {
+    if constexpr (FWD) {
+      g_begin = static_cast<int>(j0 / kGroup);
+      steps = groups - g_begin;
+    } else {
+      const int64_t last = (j0 + COLS - 1) / kGroup;
+      g_begin = last < groups - 1 ? static_cast<int>(last) : groups - 1;
+      steps = g_begin + 1;
+    }
+  }
+  if (staged && steps > 0) stage_group(g_begin);
   cp_async_commit();
 
-  for (int gi = 0; gi < groups; ++gi) {
-    const int g = FWD ? gi : groups - 1 - gi;  // forward: first group first; else last first
+  for (int gi = 0; gi < steps; ++gi) {
+    const int g = FWD ? g_begin + gi : g_begin - gi;  // forward: first group first; else last first
     const int c0 = g * kGroup, sg = min(kGroup, s - c0);
     // A's values for this warp's update, loaded now to land while the group
     // is solved: af[mt][ks] is the m16k16 fragment of rows 16·mt.. of the
@@ -472,7 +488,12 @@ __global__ void __launch_bounds__(kLeafMax, 2)
 // receives the transpose of its inverse: W_b[k·LEAF + i] = L_b⁻¹(k, i).
 // The first launch of its solve: waits for the previous launch on the
 // stream before anything else (the previous solve may still read W).
-// COLS right-hand sides (columns of the identity) per thread block.
+// COLS right-hand sides (columns of the identity) per thread block: block b
+// = blockIdx.x, columns j0 = (gridDim.y − 1 − blockIdx.y)·COLS. A block
+// with right-hand sides j0 .. j0+COLS-1 walks the groups up to the one
+// holding j0+COLS-1 (the solutions are zero below the diagonal of Lᵀ's
+// inverse), so the blocks of the last columns are the longest: they are
+// launched first.
 // sync (null: none): the synchronisation words of a chain launch that
 // follows, zeroed by the first block once the previous launch is done.
 template <int LEAF, int COLS>
@@ -483,9 +504,9 @@ __global__ void __launch_bounds__(LEAF, LEAF <= 256 ? 2 : 1)
     grid_dependency_wait();
     for (int i = threadIdx.x; i < kChainSyncBytes / 4; i += blockDim.x) sync[i] = 0u;
   }
-  const int b = blockIdx.y;
+  const int b = blockIdx.x;
   const int s = static_cast<int>(leaves.size[b]);
-  const int64_t j0 = static_cast<int64_t>(blockIdx.x) * COLS;
+  const int64_t j0 = static_cast<int64_t>(gridDim.y - 1 - blockIdx.y) * COLS;
   if (j0 >= s) {  // right-hand sides past the block's order: nothing to solve
     grid_dependency_wait();
     grid_launch_dependents();
@@ -618,7 +639,9 @@ cudaError_t launch_trsm_inverse(const uint16_t* A, int64_t lda, uint16_t* W, con
   constexpr int LEAF = kTrsmInverseLeaf;
   static std::atomic<bool> attr_done[kMaxDevices];
   if (!attr_done[dev]) {
-    if ((e = cudaFuncSetAttribute(trsm_inverse_kernel<LEAF, 32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if ((e = cudaFuncSetAttribute(trsm_inverse_kernel<LEAF, 16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  leaf_smem<16, LEAF>())) != cudaSuccess ||
+        (e = cudaFuncSetAttribute(trsm_inverse_kernel<LEAF, 32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   leaf_smem<32, LEAF>())) != cudaSuccess ||
         (e = cudaFuncSetAttribute(trsm_inverse_kernel<LEAF, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   leaf_smem<64, LEAF>())) != cudaSuccess)
@@ -627,15 +650,49 @@ cudaError_t launch_trsm_inverse(const uint16_t* A, int64_t lda, uint16_t* W, con
   }
   int sms = 0;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-  // one block per SM: 32 right-hand sides per block while that fills one
-  // wave, else 64 (fewer, longer blocks; measured at 16 blocks of 512:
-  // 58 -> 43 µs, at 8 blocks 32 stays better)
-  if (static_cast<int64_t>(leaves.count) * (LEAF / 32) <= sms) {
-    PdlLaunch l(dim3(LEAF / 32, static_cast<unsigned>(leaves.count)), dim3(LEAF), leaf_smem<32, LEAF>(), stream);
-    return cudaLaunchKernelEx(&l.cfg, trsm_inverse_kernel<LEAF, 32>, A, lda, W, leaves, sync);
+  // Width by estimated time, one block per SM: a block of COLS right-hand
+  // sides takes one group step per group up to its last column's, each step
+  // ~(1.1 + COLS/40) µs (measured: 32 columns ~1.9 µs, 64 ~2.7 µs); blocks
+  // are launched longest first, so the launch lasts about the longer of the
+  // longest block and the total steps spread over the SMs.
+  const int widths[3] = {16, 32, 64};
+  int best = 1;
+  double best_cost = 0.0;
+  for (int w = 0; w < 3; ++w) {
+    const int cols = widths[w];
+    int64_t total = 0;
+    int longest = 0;
+    for (int b = 0; b < leaves.count; ++b) {
+      const int groups = static_cast<int>((leaves.size[b] + 31) / 32);
+      for (int64_t j0 = 0; j0 < leaves.size[b]; j0 += cols) {
+        const int64_t last = (j0 + cols - 1) / 32;
+        const int steps = static_cast<int>(last < groups - 1 ? last : groups - 1) + 1;
+        total += steps;
+        longest = steps > longest ? steps : longest;
+      }
+    }
+    const int64_t spread = (total + sms - 1) / sms;
+    const double cost = static_cast<double>(spread > longest ? spread : longest) * (1.1 + cols / 40.0);
+    if (w == 0 || cost < best_cost) {
+      best = w;
+      best_cost = cost;
+    }
   }
-  PdlLaunch l(dim3(LEAF / 64, static_cast<unsigned>(leaves.count)), dim3(LEAF), leaf_smem<64, LEAF>(), stream);
-  return cudaLaunchKernelEx(&l.cfg, trsm_inverse_kernel<LEAF, 64>, A, lda, W, leaves, sync);
+  const dim3 grid(static_cast<unsigned>(leaves.count), static_cast<unsigned>(LEAF / widths[best]));
+  switch (best) {
+    case 0: {
+      PdlLaunch l(grid, dim3(LEAF), leaf_smem<16, LEAF>(), stream);
+      return cudaLaunchKernelEx(&l.cfg, trsm_inverse_kernel<LEAF, 16>, A, lda, W, leaves, sync);
+    }
+    case 1: {
+      PdlLaunch l(grid, dim3(LEAF), leaf_smem<32, LEAF>(), stream);
+      return cudaLaunchKernelEx(&l.cfg, trsm_inverse_kernel<LEAF, 32>, A, lda, W, leaves, sync);
+    }
+    default: {
+      PdlLaunch l(grid, dim3(LEAF), leaf_smem<64, LEAF>(), stream);
+      return cudaLaunchKernelEx(&l.cfg, trsm_inverse_kernel<LEAF, 64>, A, lda, W, leaves, sync);
+    }
+  }
 }
 
 cudaError_t launch_scale_copy(const uint16_t* B, int64_t ldb, uint16_t* X, int64_t ldx, int64_t n,
