@@ -38,6 +38,13 @@
 //     rows of the second operand (A21 lies below the diagonal), processed
 //     first (N = s, initialising the accumulator), so those updates cost no
 //     launch, no read-modify-write of C and no intermediate FP16 rounding;
+//   * with few units (a short X: m of a few hundred rows), each leaf is cut
+//     into 64-column parts (p.part_cols = 64), one unit each: part q takes
+//     rows 64q .. 64q+63 of L_b (N = 64), the carried update's K blocks and
+//     the triangle's K blocks kb ≥ q (the blocks below are zero for those
+//     rows), masking block q. Four times as many SMs then share the longest
+//     leaves' operand streams, each reading the X tile and a quarter of the
+//     triangle rows;
 //   * every wait is bounded, as in the other tensor-core kernels (watchdog
 //     word, abort flag, drain, TMEM freed).
 #include <atomic>
@@ -71,11 +78,18 @@ struct LeafCfg {
   static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
   static constexpr int OFF_C = OFF_B + STAGES * B_BYTES;
   static constexpr int OFF_BAR = OFF_C + C_BYTES;
-  static constexpr int NUM_BARS = 2 * STAGES + 4 + 1;          // full, empty, acc full/empty, drain
+  // With 64-column parts a stage needs only the X tile and one row box
+  // (24 KB): the same ring space then holds twice the stages, interleaved.
+  static constexpr int PART_STAGE_BYTES = A_BYTES + L_BOX_BYTES;
+  static constexpr int PART_STAGES = STAGES * (A_BYTES + B_BYTES) / PART_STAGE_BYTES;  // 8
+  static constexpr int MAX_STAGES = PART_STAGES;
+  static constexpr int NUM_BARS = 2 * MAX_STAGES + 4 + 1;      // full, empty, acc full/empty, drain
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;      // tmem address, abort flag
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;      // + slack to align the base
   static constexpr int THREADS = 192;
 
+  static_assert(PART_STAGES * PART_STAGE_BYTES <= STAGES * (A_BYTES + B_BYTES) && PART_STAGES >= STAGES,
+                "the parts' stages fit in the ring");
   static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0 && L_BOX_BYTES % 1024 == 0 &&
                     C_BOX_BYTES % 1024 == 0,
                 "swizzled buffers must stay 1024-byte aligned");
@@ -113,7 +127,7 @@ __global__ void __launch_bounds__(192, 1)
                                const __grid_constant__ CUtensorMap tmC, const TcArgs p,
                                const TriLeaves leaves, const TriLeafExt lext) {
   using Cfg = LeafCfg;
-  constexpr int STAGES = Cfg::STAGES;
+  constexpr int MAXST = Cfg::MAX_STAGES;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -121,21 +135,31 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t sA = sbase + Cfg::OFF_A;
   const uint32_t sB = sbase + Cfg::OFF_B;
   const uint32_t bar0 = sbase + Cfg::OFF_BAR;
-  const uint32_t drain_bar = bar0 + 8 * (2 * STAGES + 4);
+  const uint32_t drain_bar = bar0 + 8 * (2 * MAXST + 4);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::OFF_MISC + 4);
 
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
-  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
-  auto accf_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
-  auto acce_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (MAXST + s); };
+  auto accf_bar = [&](int b) { return bar0 + 8u * (2 * MAXST + b); };
+  auto acce_bar = [&](int b) { return bar0 + 8u * (2 * MAXST + 2 + b); };
+  // the ring: Cfg::STAGES stages of an X tile and up to four row boxes
+  // (whole leaves), or Cfg::PART_STAGES of an X tile and one row box (parts)
+  const int parts = p.part_cols > 0 ? Cfg::MAX_S / p.part_cols : 1;
+  const int nstages = parts > 1 ? Cfg::PART_STAGES : Cfg::STAGES;
+  auto stage_a = [&](int s) {
+    return parts > 1 ? sA + s * Cfg::PART_STAGE_BYTES : sA + s * Cfg::A_BYTES;
+  };
+  auto stage_b = [&](int s) {
+    return parts > 1 ? sA + s * Cfg::PART_STAGE_BYTES + Cfg::A_BYTES : sB + s * Cfg::B_BYTES;
+  };
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const Watchdog wd{abort_flag, p.status, p.timeout_ns};
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < MAXST; ++s) {
       mbar_init(full_bar(s), 1);   // producer's arrive.expect_tx (+ TMA bytes)
       mbar_init(empty_bar(s), 1);  // MMA issuer's tcgen05.commit
     }
@@ -164,7 +188,22 @@ __global__ void __launch_bounds__(192, 1)
 
   // unit t: rows [128·mt, +128) of X with mt = t / leaves, for leaf t % leaves:
   // the CTAs at work share those rows of X (read from memory once) and the
-  // leaves' operand rows, which stay in L2
+  // leaves' operand rows, which stay in L2. With parts (X then fits in L2),
+  // leaf-major instead, so that the CTAs take the longest leaves' parts of
+  // every tile first: u = t / parts = b·num_m + mt, part t % parts. A part
+  // past a narrower leaf's columns is skipped by every role.
+  auto decode = [&](int t, int& mt, int& b, int& part) {
+    if (parts > 1) {
+      const int u = t / parts;
+      part = t - u * parts;
+      b = u / p.num_m;
+      mt = u - b * p.num_m;
+    } else {
+      part = 0;
+      mt = t / leaves.count;
+      b = t - mt * leaves.count;
+    }
+  };
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer
     if (lane == 0) {
@@ -173,39 +212,44 @@ __global__ void __launch_bounds__(192, 1)
       long long issued = 0;
       bool ok = true;
       for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
-        const int mt = t / leaves.count, b = t - mt * leaves.count;
+        int mt, b, part;
+        decode(t, mt, b, part);
         const int off = static_cast<int>(leaves.off[b]);
         const int nkb = static_cast<int>(leaves.size[b]) / Cfg::BK;
         const int nke = lext.ext[b] / Cfg::BK;  // K blocks of the carried update
-        for (int j = 0; j < nke + nkb; ++j) {
+        if (parts > 1 && part >= nkb) continue;
+        // triangle blocks: all of them (whole leaf), or kb ≥ part (a part)
+        const int ntri = parts > 1 ? nkb - part : nkb;
+        for (int j = 0; j < nke + ntri; ++j) {
           // update blocks first (all nkb row boxes), then the triangle's,
-          // widest first (kb + 1 row boxes)
+          // widest first (kb + 1 row boxes); a part loads its one row box
           const int kb = j < nke ? nkb - 1 : nkb - 1 - (j - nke);
           const int x = j < nke ? off + nkb * Cfg::BK + j * Cfg::BK : off + kb * Cfg::BK;
+          const int r0 = parts > 1 ? part : 0, r1 = parts > 1 ? part : kb;
           if (!wait_phase(empty_bar(stage), phase ^ 1u, wd, kWdProducerEmpty)) {
             ok = false;
             break;
           }
           if (!(p.inject == 1 && issued == 0))  // testing aid: withhold one arrival
             mbar_arrive_expect_tx(full_bar(stage),
-                                  static_cast<uint32_t>(Cfg::A_BYTES + (kb + 1) * Cfg::L_BOX_BYTES));
-          tma_load_2d(sA + stage * Cfg::A_BYTES, &tmX, full_bar(stage), x, mt * Cfg::BM);
-          for (int r = 0; r <= kb; ++r)
-            tma_load_2d(sB + stage * Cfg::B_BYTES + r * Cfg::L_BOX_BYTES, &tmL, full_bar(stage), x,
+                                  static_cast<uint32_t>(Cfg::A_BYTES + (r1 - r0 + 1) * Cfg::L_BOX_BYTES));
+          tma_load_2d(stage_a(stage), &tmX, full_bar(stage), x, mt * Cfg::BM);
+          for (int r = r0; r <= r1; ++r)
+            tma_load_2d(stage_b(stage) + (r - r0) * Cfg::L_BOX_BYTES, &tmL, full_bar(stage), x,
                         off + r * Cfg::L_BOX_ROWS);
           ++issued;
-          if (++stage == STAGES) {
+          if (++stage == nstages) {
             stage = 0;
             phase ^= 1u;
           }
         }
       }
-      // Drain: the last min(issued, STAGES) loads land before the CTA exits.
+      // Drain: the last min(issued, nstages) loads land before the CTA exits.
       int s = stage;
       uint32_t ph = phase;
-      for (long long i = 0; i < issued && i < STAGES; ++i) {
+      for (long long i = 0; i < issued && i < nstages; ++i) {
         if (s == 0) {
-          s = STAGES - 1;
+          s = nstages - 1;
           ph ^= 1u;
         } else {
           --s;
@@ -222,9 +266,12 @@ __global__ void __launch_bounds__(192, 1)
     uint32_t acc_phase = 0;
     bool ok = true;
     for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
-      const int b = t % leaves.count;
+      int mt, b, part;
+      decode(t, mt, b, part);
       const int nkb = static_cast<int>(leaves.size[b]) / Cfg::BK;
       const int nke = lext.ext[b] / Cfg::BK;
+      if (parts > 1 && part >= nkb) continue;
+      const int ntri = parts > 1 ? nkb - part : nkb;
       int free_acc = 1;
       if (lane == 0) free_acc = wait_phase(acce_bar(acc), acc_phase ^ 1u, wd, kWdMmaAccEmpty) ? 1 : 0;
       if (!__shfl_sync(0xffffffffu, free_acc, 0)) {
@@ -233,7 +280,7 @@ __global__ void __launch_bounds__(192, 1)
       }
       tc_fence_after_sync();
       const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * Cfg::ACC_COLS);
-      for (int j = 0; j < nke + nkb; ++j) {
+      for (int j = 0; j < nke + ntri; ++j) {
         const bool update = j < nke;  // a K block of the carried update: whole rows, no mask
         const int kb = update ? nkb - 1 : nkb - 1 - (j - nke);
         // every lane waits for the copy: its masking stores come after it
@@ -242,21 +289,25 @@ __global__ void __launch_bounds__(192, 1)
           ok = false;
           break;
         }
-        if (!update) mask_diagonal_block(smem + Cfg::OFF_B + stage * Cfg::B_BYTES + kb * Cfg::L_BOX_BYTES, lane);
-        fence_proxy_async_smem();  // the tensor cores read the stage through the async proxy
+        // the diagonal sub-block: row box kb of the whole leaf, or the part's
+        // own box when kb is the part's index (its other blocks are whole)
+        if (!update && (parts == 1 || kb == part)) {
+          mask_diagonal_block(smem + (stage_b(stage) - sbase) + (parts > 1 ? 0 : kb) * Cfg::L_BOX_BYTES, lane);
+          fence_proxy_async_smem();  // the tensor cores read the masked stage through the async proxy
+        }
         __syncwarp();
         if (lane == 0) {
           tc_fence_after_sync();
-          const uint64_t a_desc = sdesc_kmajor_sw128(sA + stage * Cfg::A_BYTES);
-          const uint64_t b_desc = sdesc_kmajor_sw128(sB + stage * Cfg::B_BYTES);
-          const uint32_t idesc = idesc_f16_f32acc(Cfg::BM, (kb + 1) * Cfg::L_BOX_ROWS);
+          const uint64_t a_desc = sdesc_kmajor_sw128(stage_a(stage));
+          const uint64_t b_desc = sdesc_kmajor_sw128(stage_b(stage));
+          const uint32_t idesc = idesc_f16_f32acc(Cfg::BM, parts > 1 ? Cfg::L_BOX_ROWS : (kb + 1) * Cfg::L_BOX_ROWS);
 #pragma unroll
           for (int k = 0; k < Cfg::BK / Cfg::UMMA_K; ++k)
             mma_f16_ss(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc, (j > 0 || k > 0) ? 1u : 0u);
           mma_commit(empty_bar(stage));  // frees the stage once read
         }
         __syncwarp();
-        if (++stage == STAGES) {
+        if (++stage == nstages) {
           stage = 0;
           phase ^= 1u;
         }
@@ -280,9 +331,13 @@ __global__ void __launch_bounds__(192, 1)
     uint32_t acc_phase = 0;
     int cb = 0;
     for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
-      const int mt = t / leaves.count, b = t - mt * leaves.count;
-      const int off = static_cast<int>(leaves.off[b]);
-      const int boxes = static_cast<int>(leaves.size[b]) / kEpiCols;
+      int mt, b, part;
+      decode(t, mt, b, part);
+      const int nkb = static_cast<int>(leaves.size[b]) / Cfg::BK;
+      if (parts > 1 && part >= nkb) continue;
+      // the part's one 64-column box, or the whole leaf's
+      const int off = static_cast<int>(leaves.off[b]) + (parts > 1 ? part * kEpiCols : 0);
+      const int boxes = parts > 1 ? 1 : static_cast<int>(leaves.size[b]) / kEpiCols;
       int ok = 1;
       if (lane == 0) ok = wait_phase(accf_bar(acc), acc_phase, wd, kWdEpiAccFull) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -344,6 +399,7 @@ cudaError_t launch_tri_leaves_tc(const CUtensorMap& x, const CUtensorMap& l, con
     if (leaves.size[b] <= 0 || leaves.size[b] > LeafCfg::MAX_S || leaves.size[b] % LeafCfg::BK != 0 ||
         ext.ext[b] < 0 || ext.ext[b] % LeafCfg::BK != 0)
       return cudaErrorInvalidValue;
+  if (args.part_cols != 0 && args.part_cols != LeafCfg::L_BOX_ROWS) return cudaErrorInvalidValue;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
