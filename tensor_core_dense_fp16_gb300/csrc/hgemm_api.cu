@@ -890,19 +890,6 @@ int hgemm_trmm(const hgemm_half_t* A, int64_t lda, const hgemm_half_t* B, int64_
           }
         }
       }
-      // Few units (a short m): every leaf in 64-column parts, a unit each, when
-      // four times the units still fit in one wave of CTAs. The longest
-      // leaves' operand streams are then shared by four SMs each (the X tile
-      // is read by every part, the triangle rows split between them): at
-      // n = 4096, m = 256 the longest unit streams 1.5 MB instead of 3 MB
-      // (32.8 -> 30.7 µs; n = 2048, m = 128: 22.1 -> 18.4 µs). With two waves
-      // of parts it was slower (n = 4096, m = 512: 34.4 -> 38.9 µs).
-      if (static_cast<int64_t>(args.num_tiles) * 4 <= static_cast<int64_t>(dev->num_sms)) {
-        args.part_cols = 64;
-        args.num_tiles *= 4;
-        args.full_tiles = args.num_tiles;
-        args.grid = args.num_tiles < dev->num_sms ? args.num_tiles : dev->num_sms;
-      }
       e = hg::launch_tri_leaves_tc(mx, ml, mc, args, leaves, ext, stream);
     }
   }

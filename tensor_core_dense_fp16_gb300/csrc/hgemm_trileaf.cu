@@ -38,13 +38,9 @@
 //     rows of the second operand (A21 lies below the diagonal), processed
 //     first (N = s, initialising the accumulator), so those updates cost no
 //     launch, no read-modify-write of C and no intermediate FP16 rounding;
-//   * with few units (a short X: m of a few hundred rows), each leaf is cut
-//     into 64-column parts (p.part_cols = 64), one unit each: part q takes
-//     rows 64q .. 64q+63 of L_b (N = 64), the carried update's K blocks and
-//     the triangle's K blocks kb ≥ q (the blocks below are zero for those
-//     rows), masking block q. Four times as many SMs then share the longest
-//     leaves' operand streams, each reading the X tile and a quarter of the
-//     triangle rows;
+//   * with few units (a short X), each unit's K blocks are split over a
+//     cluster of CTAs instead, the partial sums reduced through distributed
+//     shared memory (hgemm_tri_leaves_split_kernel below);
 //   * every wait is bounded, as in the other tensor-core kernels (watchdog
 //     word, abort flag, drain, TMEM freed).
 #include <atomic>
@@ -78,18 +74,13 @@ struct LeafCfg {
   static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
   static constexpr int OFF_C = OFF_B + STAGES * B_BYTES;
   static constexpr int OFF_BAR = OFF_C + C_BYTES;
-  // With 64-column parts a stage needs only the X tile and one row box
-  // (24 KB): the same ring space then holds twice the stages, interleaved.
-  static constexpr int PART_STAGE_BYTES = A_BYTES + L_BOX_BYTES;
-  static constexpr int PART_STAGES = STAGES * (A_BYTES + B_BYTES) / PART_STAGE_BYTES;  // 8
-  static constexpr int MAX_STAGES = PART_STAGES;
-  static constexpr int NUM_BARS = 2 * MAX_STAGES + 4 + 1;      // full, empty, acc full/empty, drain
+  // full, empty, then: acc full/empty and drain (persistent kernel), or acc
+  // full, drain, partials received and one "owner ready" per slice (split K)
+  static constexpr int NUM_BARS = 2 * STAGES + 8;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;      // tmem address, abort flag
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;      // + slack to align the base
   static constexpr int THREADS = 192;
 
-  static_assert(PART_STAGES * PART_STAGE_BYTES <= STAGES * (A_BYTES + B_BYTES) && PART_STAGES >= STAGES,
-                "the parts' stages fit in the ring");
   static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0 && L_BOX_BYTES % 1024 == 0 &&
                     C_BOX_BYTES % 1024 == 0,
                 "swizzled buffers must stay 1024-byte aligned");
@@ -127,7 +118,7 @@ __global__ void __launch_bounds__(192, 1)
                                const __grid_constant__ CUtensorMap tmC, const TcArgs p,
                                const TriLeaves leaves, const TriLeafExt lext) {
   using Cfg = LeafCfg;
-  constexpr int MAXST = Cfg::MAX_STAGES;
+  constexpr int STAGES = Cfg::STAGES;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -135,31 +126,21 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t sA = sbase + Cfg::OFF_A;
   const uint32_t sB = sbase + Cfg::OFF_B;
   const uint32_t bar0 = sbase + Cfg::OFF_BAR;
-  const uint32_t drain_bar = bar0 + 8 * (2 * MAXST + 4);
+  const uint32_t drain_bar = bar0 + 8 * (2 * STAGES + 4);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::OFF_MISC + 4);
 
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
-  auto empty_bar = [&](int s) { return bar0 + 8u * (MAXST + s); };
-  auto accf_bar = [&](int b) { return bar0 + 8u * (2 * MAXST + b); };
-  auto acce_bar = [&](int b) { return bar0 + 8u * (2 * MAXST + 2 + b); };
-  // the ring: Cfg::STAGES stages of an X tile and up to four row boxes
-  // (whole leaves), or Cfg::PART_STAGES of an X tile and one row box (parts)
-  const int parts = p.part_cols > 0 ? Cfg::MAX_S / p.part_cols : 1;
-  const int nstages = parts > 1 ? Cfg::PART_STAGES : Cfg::STAGES;
-  auto stage_a = [&](int s) {
-    return parts > 1 ? sA + s * Cfg::PART_STAGE_BYTES : sA + s * Cfg::A_BYTES;
-  };
-  auto stage_b = [&](int s) {
-    return parts > 1 ? sA + s * Cfg::PART_STAGE_BYTES + Cfg::A_BYTES : sB + s * Cfg::B_BYTES;
-  };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  auto accf_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
+  auto acce_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const Watchdog wd{abort_flag, p.status, p.timeout_ns};
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < MAXST; ++s) {
+    for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);   // producer's arrive.expect_tx (+ TMA bytes)
       mbar_init(empty_bar(s), 1);  // MMA issuer's tcgen05.commit
     }
@@ -188,22 +169,7 @@ __global__ void __launch_bounds__(192, 1)
 
   // unit t: rows [128·mt, +128) of X with mt = t / leaves, for leaf t % leaves:
   // the CTAs at work share those rows of X (read from memory once) and the
-  // leaves' operand rows, which stay in L2. With parts (X then fits in L2),
-  // leaf-major instead, so that the CTAs take the longest leaves' parts of
-  // every tile first: u = t / parts = b·num_m + mt, part t % parts. A part
-  // past a narrower leaf's columns is skipped by every role.
-  auto decode = [&](int t, int& mt, int& b, int& part) {
-    if (parts > 1) {
-      const int u = t / parts;
-      part = t - u * parts;
-      b = u / p.num_m;
-      mt = u - b * p.num_m;
-    } else {
-      part = 0;
-      mt = t / leaves.count;
-      b = t - mt * leaves.count;
-    }
-  };
+  // leaves' operand rows, which stay in L2
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer
     if (lane == 0) {
@@ -212,44 +178,39 @@ __global__ void __launch_bounds__(192, 1)
       long long issued = 0;
       bool ok = true;
       for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
-        int mt, b, part;
-        decode(t, mt, b, part);
+        const int mt = t / leaves.count, b = t - mt * leaves.count;
         const int off = static_cast<int>(leaves.off[b]);
         const int nkb = static_cast<int>(leaves.size[b]) / Cfg::BK;
         const int nke = lext.ext[b] / Cfg::BK;  // K blocks of the carried update
-        if (parts > 1 && part >= nkb) continue;
-        // triangle blocks: all of them (whole leaf), or kb ≥ part (a part)
-        const int ntri = parts > 1 ? nkb - part : nkb;
-        for (int j = 0; j < nke + ntri; ++j) {
+        for (int j = 0; j < nke + nkb; ++j) {
           // update blocks first (all nkb row boxes), then the triangle's,
-          // widest first (kb + 1 row boxes); a part loads its one row box
+          // widest first (kb + 1 row boxes)
           const int kb = j < nke ? nkb - 1 : nkb - 1 - (j - nke);
           const int x = j < nke ? off + nkb * Cfg::BK + j * Cfg::BK : off + kb * Cfg::BK;
-          const int r0 = parts > 1 ? part : 0, r1 = parts > 1 ? part : kb;
           if (!wait_phase(empty_bar(stage), phase ^ 1u, wd, kWdProducerEmpty)) {
             ok = false;
             break;
           }
           if (!(p.inject == 1 && issued == 0))  // testing aid: withhold one arrival
             mbar_arrive_expect_tx(full_bar(stage),
-                                  static_cast<uint32_t>(Cfg::A_BYTES + (r1 - r0 + 1) * Cfg::L_BOX_BYTES));
-          tma_load_2d(stage_a(stage), &tmX, full_bar(stage), x, mt * Cfg::BM);
-          for (int r = r0; r <= r1; ++r)
-            tma_load_2d(stage_b(stage) + (r - r0) * Cfg::L_BOX_BYTES, &tmL, full_bar(stage), x,
+                                  static_cast<uint32_t>(Cfg::A_BYTES + (kb + 1) * Cfg::L_BOX_BYTES));
+          tma_load_2d(sA + stage * Cfg::A_BYTES, &tmX, full_bar(stage), x, mt * Cfg::BM);
+          for (int r = 0; r <= kb; ++r)
+            tma_load_2d(sB + stage * Cfg::B_BYTES + r * Cfg::L_BOX_BYTES, &tmL, full_bar(stage), x,
                         off + r * Cfg::L_BOX_ROWS);
           ++issued;
-          if (++stage == nstages) {
+          if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
       }
-      // Drain: the last min(issued, nstages) loads land before the CTA exits.
+      // Drain: the last min(issued, STAGES) loads land before the CTA exits.
       int s = stage;
       uint32_t ph = phase;
-      for (long long i = 0; i < issued && i < nstages; ++i) {
+      for (long long i = 0; i < issued && i < STAGES; ++i) {
         if (s == 0) {
-          s = nstages - 1;
+          s = STAGES - 1;
           ph ^= 1u;
         } else {
           --s;
@@ -266,12 +227,9 @@ __global__ void __launch_bounds__(192, 1)
     uint32_t acc_phase = 0;
     bool ok = true;
     for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
-      int mt, b, part;
-      decode(t, mt, b, part);
+      const int b = t % leaves.count;
       const int nkb = static_cast<int>(leaves.size[b]) / Cfg::BK;
       const int nke = lext.ext[b] / Cfg::BK;
-      if (parts > 1 && part >= nkb) continue;
-      const int ntri = parts > 1 ? nkb - part : nkb;
       int free_acc = 1;
       if (lane == 0) free_acc = wait_phase(acce_bar(acc), acc_phase ^ 1u, wd, kWdMmaAccEmpty) ? 1 : 0;
       if (!__shfl_sync(0xffffffffu, free_acc, 0)) {
@@ -280,7 +238,7 @@ __global__ void __launch_bounds__(192, 1)
       }
       tc_fence_after_sync();
       const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * Cfg::ACC_COLS);
-      for (int j = 0; j < nke + ntri; ++j) {
+      for (int j = 0; j < nke + nkb; ++j) {
         const bool update = j < nke;  // a K block of the carried update: whole rows, no mask
         const int kb = update ? nkb - 1 : nkb - 1 - (j - nke);
         // every lane waits for the copy: its masking stores come after it
@@ -289,25 +247,21 @@ __global__ void __launch_bounds__(192, 1)
           ok = false;
           break;
         }
-        // the diagonal sub-block: row box kb of the whole leaf, or the part's
-        // own box when kb is the part's index (its other blocks are whole)
-        if (!update && (parts == 1 || kb == part)) {
-          mask_diagonal_block(smem + (stage_b(stage) - sbase) + (parts > 1 ? 0 : kb) * Cfg::L_BOX_BYTES, lane);
-          fence_proxy_async_smem();  // the tensor cores read the masked stage through the async proxy
-        }
+        if (!update) mask_diagonal_block(smem + Cfg::OFF_B + stage * Cfg::B_BYTES + kb * Cfg::L_BOX_BYTES, lane);
+        fence_proxy_async_smem();  // the tensor cores read the stage through the async proxy
         __syncwarp();
         if (lane == 0) {
           tc_fence_after_sync();
-          const uint64_t a_desc = sdesc_kmajor_sw128(stage_a(stage));
-          const uint64_t b_desc = sdesc_kmajor_sw128(stage_b(stage));
-          const uint32_t idesc = idesc_f16_f32acc(Cfg::BM, parts > 1 ? Cfg::L_BOX_ROWS : (kb + 1) * Cfg::L_BOX_ROWS);
+          const uint64_t a_desc = sdesc_kmajor_sw128(sA + stage * Cfg::A_BYTES);
+          const uint64_t b_desc = sdesc_kmajor_sw128(sB + stage * Cfg::B_BYTES);
+          const uint32_t idesc = idesc_f16_f32acc(Cfg::BM, (kb + 1) * Cfg::L_BOX_ROWS);
 #pragma unroll
           for (int k = 0; k < Cfg::BK / Cfg::UMMA_K; ++k)
             mma_f16_ss(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc, (j > 0 || k > 0) ? 1u : 0u);
           mma_commit(empty_bar(stage));  // frees the stage once read
         }
         __syncwarp();
-        if (++stage == nstages) {
+        if (++stage == STAGES) {
           stage = 0;
           phase ^= 1u;
         }
@@ -331,13 +285,9 @@ __global__ void __launch_bounds__(192, 1)
     uint32_t acc_phase = 0;
     int cb = 0;
     for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
-      int mt, b, part;
-      decode(t, mt, b, part);
-      const int nkb = static_cast<int>(leaves.size[b]) / Cfg::BK;
-      if (parts > 1 && part >= nkb) continue;
-      // the part's one 64-column box, or the whole leaf's
-      const int off = static_cast<int>(leaves.off[b]) + (parts > 1 ? part * kEpiCols : 0);
-      const int boxes = parts > 1 ? 1 : static_cast<int>(leaves.size[b]) / kEpiCols;
+      const int mt = t / leaves.count, b = t - mt * leaves.count;
+      const int off = static_cast<int>(leaves.off[b]);
+      const int boxes = static_cast<int>(leaves.size[b]) / kEpiCols;
       int ok = 1;
       if (lane == 0) ok = wait_phase(accf_bar(acc), acc_phase, wd, kWdEpiAccFull) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -387,26 +337,407 @@ __global__ void __launch_bounds__(192, 1)
   if (warp == 1) tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
 }
 
+// ---------------------------------------------------------------------------
+// Split-K leaves: with few units, the leaf that carries the most updates walks
+// by far the most K blocks. Here one cluster of CL CTAs takes one unit (a
+// 128-row tile of X, a whole leaf of s columns), each CTA a contiguous range
+// of its K blocks: the carried update's blocks are shared out, and the last
+// CTA also takes the triangle's blocks (widest first, so every CTA's first
+// block initialises all s accumulator columns). The CL partial sums are then
+// reduced through distributed shared memory, as in the split-K GEMM: the s
+// columns are cut into CL ranges of whole 64-column boxes, the CTA of slice r
+// owns range r; once an owner's own MMAs are done (its ring is free) it tells
+// the slices that have a partial, each of them stages its 32 rows per warp of
+// the owner's range in its own shared memory and pushes them with one bulk
+// copy into the owner's ring, whose barrier counts the bytes; the owner adds
+// the partials in slice order (the result does not depend on timing), applies
+// alpha, rounds to FP16 and stores its range. A final cluster barrier keeps
+// every CTA until the others are done, so no copy or remote arrival touches
+// a CTA that has left (an owner reaches it only after its partials landed).
+// A CTA with no K blocks (a leaf with few carried blocks) has no partial: it
+// sends nothing and only owns.
+
+// K blocks [j0, j1) of slice r out of cl, in the unit's block order (the nke
+// carried blocks, then the nkb triangle blocks, which the last slice takes).
+// A triangle block counts as 1.5 carried ones: it is narrower, but masked by
+// the whole MMA warp (measured: the last slice of the longest leaf finished
+// ~1.5 µs after the others with equal counts).
+__device__ __forceinline__ void split_range(int nke, int nkb, int r, int cl, int& j0, int& j1) {
+  const int per = (2 * nke + 3 * nkb + 2 * cl - 1) / (2 * cl);
+  j0 = min(nke, r * per);
+  j1 = r < cl - 1 ? min(nke, (r + 1) * per) : nke + nkb;
+}
+
+// Row grow of C, columns x0 .. x0+63 (v0: the first 32, v1: the rest),
+// rounded to FP16 (through the fused epilogue when FUSED) and stored with
+// 16-byte stores (x0, N and ldc are multiples of 8 here). Rows past M are
+// skipped.
+template <bool FUSED>
+__device__ __forceinline__ void store_row64(const uint32_t (&v0)[32], const uint32_t (&v1)[32],
+                                            const EpiArgs& e, uint16_t* C, int64_t M, int64_t N,
+                                            int64_t ldc, int64_t grow, int64_t x0) {
+  if (grow >= M) return;
+  uint16_t* out = C + grow * ldc + x0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    if (x0 + 8 * j >= N) break;
+    if (!HG_DBG_INDEX(x0 + 8 * j + 7, N) || !HG_DBG_ALIGN(out + 8 * j, 16)) break;
+    const uint32_t* v = (j < 4) ? (v0 + 8 * j) : (v1 + 8 * (j - 4));
+    uint4 pk;
+    if constexpr (FUSED) {
+      pk = epi_pack8(v, e, load_c_old8(e, C, M, N, ldc, grow, x0 + 8 * j), load_bias8(e, x0 + 8 * j, N));
+    } else {
+      pk.x = pack_half2(v[0], v[1]);
+      pk.y = pack_half2(v[2], v[3]);
+      pk.z = pack_half2(v[4], v[5]);
+      pk.w = pack_half2(v[6], v[7]);
+    }
+    *reinterpret_cast<uint4*>(out + 8 * j) = pk;
+  }
+}
+
+// First 64-column box of the range owned by slice r, for a leaf of `boxes`
+// boxes.
+__host__ __device__ constexpr int owned_box(int r, int cl, int boxes) { return (boxes * r) / cl; }
+
+// Swizzled FP32 block of `cols` columns: row q occupies cols·4 bytes at
+// q·cols·4, and its 16-byte chunk c sits at chunk position c ^ (q % 8), so the
+// 32 rows a warp writes at once spread over all banks.
+__device__ __forceinline__ uint32_t split_block_offset(int q, int c, int cols) {
+  return static_cast<uint32_t>(q * cols * 4 + ((c ^ (q & 7)) << 4));
+}
+
+template <int CL, bool FUSED>
+__global__ void __launch_bounds__(192, 1)
+    hgemm_tri_leaves_split_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmL,
+                                  const __grid_constant__ CUtensorMap tmC, const TcArgs p,
+                                  const TriLeaves leaves, const TriLeafExt lext) {
+  using Cfg = LeafCfg;
+  constexpr int STAGES = Cfg::STAGES;
+  static_assert(CL >= 2 && CL <= 4, "one 64-column box per owner at least, four ready barriers");
+  static_assert(2 * (CL - 1) * Cfg::BM * (Cfg::MAX_S / CL) * 4 <= Cfg::OFF_C, "the exchange fits in the ring");
+  static_assert(2 * STAGES + 3 + CL <= Cfg::NUM_BARS, "the barriers fit");
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t sA = sbase + Cfg::OFF_A;
+  const uint32_t sB = sbase + Cfg::OFF_B;
+  const uint32_t bar0 = sbase + Cfg::OFF_BAR;
+  const uint32_t accf_bar = bar0 + 8u * (2 * STAGES);
+  const uint32_t drain_bar = accf_bar + 8u;
+  const uint32_t recv_bar = drain_bar + 8u;
+  const uint32_t ready_bar0 = recv_bar + 8u;   // ready_bar0 + 8o: owner o may receive
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::OFF_MISC + 4);
+  auto full_bar = [&](int st) { return bar0 + 8u * st; };
+  auto empty_bar = [&](int st) { return bar0 + 8u * (STAGES + st); };
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int r = static_cast<int>(cluster_ctarank());
+  const int u = blockIdx.x / CL;
+  const int mt = u / leaves.count, b = u - mt * leaves.count;
+  const int off = static_cast<int>(leaves.off[b]);
+  const int nkb = static_cast<int>(leaves.size[b]) / Cfg::BK;
+  const int nke = lext.ext[b] / Cfg::BK;
+  const int boxes = nkb;  // 64-column boxes of the leaf
+  int j0, j1;
+  split_range(nke, nkb, r, CL, j0, j1);
+  auto has_partial = [&](int sl) {
+    int a0, a1;
+    split_range(nke, nkb, sl, CL, a0, a1);
+    return a1 > a0;
+  };
+  auto own_box0 = [&](int sl) { return owned_box(sl, CL, boxes); };
+  auto own_cols = [&](int sl) { return 64 * (owned_box(sl + 1, CL, boxes) - owned_box(sl, CL, boxes)); };
+  const bool mine = j1 > j0;  // this CTA has a partial
+  const Watchdog wd{abort_flag, p.status, p.timeout_ns};
+
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < STAGES; ++st) {
+      mbar_init(full_bar(st), 1);
+      mbar_init(empty_bar(st), 1);
+    }
+    mbar_init(accf_bar, 1);
+    mbar_init(drain_bar, 1);
+    // the other slices' partials of this CTA's range
+    int senders = 0;
+    for (int sl = 0; sl < CL; ++sl)
+      if (sl != r && has_partial(sl)) ++senders;
+    mbar_init(recv_bar, 1);
+    mbar_arrive_expect_tx(recv_bar, static_cast<uint32_t>(senders * Cfg::BM * own_cols(r) * 4));
+    for (int o = 0; o < CL; ++o) mbar_init(ready_bar0 + 8u * o, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    prefetch_tensormap(&tmX);
+    prefetch_tensormap(&tmL);
+    prefetch_tensormap(&tmC);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), Cfg::ACC_COLS);
+    tmem_relinquish_alloc_permit();
+  }
+  tc_fence_before_sync();
+  __syncthreads();  // the TMEM address and the abort flag, within the CTA
+  cluster_sync_after_init();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+  // A, B and C may come from the previous launch on the stream
+  grid_dependency_wait();
+  grid_launch_dependents();
+
+  int ok = 1;
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      long long issued = 0;
+      for (int j = j0; j < j1; ++j) {
+        // carried blocks: all nkb row boxes; triangle blocks: kb + 1 of them
+        const int kb = j < nke ? nkb - 1 : nkb - 1 - (j - nke);
+        const int x = j < nke ? off + nkb * Cfg::BK + j * Cfg::BK : off + kb * Cfg::BK;
+        if (!wait_phase(empty_bar(stage), phase ^ 1u, wd, kWdProducerEmpty)) break;
+        if (!(p.inject == 1 && issued == 0))  // testing aid: withhold one arrival
+          mbar_arrive_expect_tx(full_bar(stage), static_cast<uint32_t>(Cfg::A_BYTES + (kb + 1) * Cfg::L_BOX_BYTES));
+        tma_load_2d(sA + stage * Cfg::A_BYTES, &tmX, full_bar(stage), x, mt * Cfg::BM);
+        for (int rb = 0; rb <= kb; ++rb)
+          tma_load_2d(sB + stage * Cfg::B_BYTES + rb * Cfg::L_BOX_BYTES, &tmL, full_bar(stage), x,
+                      off + rb * Cfg::L_BOX_ROWS);
+        ++issued;
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      // Drain: the last min(issued, STAGES) loads land before the ring is reused.
+      int st = stage;
+      uint32_t ph = phase;
+      for (long long i = 0; i < issued && i < STAGES; ++i) {
+        if (st == 0) {
+          st = STAGES - 1;
+          ph ^= 1u;
+        } else {
+          --st;
+        }
+        wait_drain(full_bar(st), ph, wd);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------- MMA warp: masks each stage, lane 0 issues
+    int stage = 0;
+    uint32_t phase = 0;
+    bool good = true;
+    for (int j = j0; j < j1; ++j) {
+      const bool update = j < nke;
+      const int kb = update ? nkb - 1 : nkb - 1 - (j - nke);
+      const int landed = wait_phase(full_bar(stage), phase, wd, kWdMmaFull) ? 1 : 0;
+      if (!__all_sync(0xffffffffu, landed)) {
+        good = false;
+        break;
+      }
+      if (!update) {
+        mask_diagonal_block(smem + Cfg::OFF_B + stage * Cfg::B_BYTES + kb * Cfg::L_BOX_BYTES, lane);
+        fence_proxy_async_smem();  // the tensor cores read the masked stage through the async proxy
+      }
+      __syncwarp();
+      if (lane == 0) {
+        tc_fence_after_sync();
+        const uint64_t a_desc = sdesc_kmajor_sw128(sA + stage * Cfg::A_BYTES);
+        const uint64_t b_desc = sdesc_kmajor_sw128(sB + stage * Cfg::B_BYTES);
+        const uint32_t idesc = idesc_f16_f32acc(Cfg::BM, (kb + 1) * Cfg::L_BOX_ROWS);
+#pragma unroll
+        for (int k = 0; k < Cfg::BK / Cfg::UMMA_K; ++k)
+          mma_f16_ss(tmem_base, a_desc + 2u * k, b_desc + 2u * k, idesc, (j > j0 || k > 0) ? 1u : 0u);
+        mma_commit(empty_bar(stage));
+      }
+      __syncwarp();
+      if (++stage == STAGES) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+    if (lane == 0) {
+      if (good && mine) mma_commit(accf_bar);  // the partial is complete
+      mma_commit(drain_bar);
+      wait_drain(drain_bar, 0, wd);
+    }
+    __syncwarp();
+  } else {
+    // epilogue warps: the partial is complete, and the operand ring is free
+    if (mine) {
+      if (lane == 0) ok = wait_phase(accf_bar, 0, wd, kWdEpiAccFull) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+    }
+    tc_fence_after_sync();
+    // tell the slices that have a partial that they may send theirs of this
+    // CTA's range (relaxed: the ring's last readers, the MMAs, completed
+    // before accf did; a CTA without a partial never used its ring)
+    if (warp == 2 && lane == 0 && ok && own_cols(r) > 0)
+      for (int sl = 0; sl < CL; ++sl)
+        if (sl != r && has_partial(sl))
+          mbar_arrive_cluster_relaxed(mapa_shared(ready_bar0 + 8u * r, static_cast<uint32_t>(sl)));
+  }
+
+  const int q = warp & 3;  // TMEM lanes / tile rows 32q .. 32q+31
+  const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+  const int row = q * 32 + lane;
+  const int oc = own_cols(r);
+  const int ox0 = 64 * own_box0(r);  // first column of the owned range, within the leaf
+  // ring layout for the exchange: receive slots (one per other slice), then
+  // the send staging
+  const uint32_t recv_base = sbase;
+  const uint32_t send_base = sbase + static_cast<uint32_t>((CL - 1) * Cfg::BM * (64 * ((boxes + CL - 1) / CL)) * 4);
+  if (warp >= 2 && ok) {
+    if (mine) {
+      // every other owner's range of this warp's 32 rows, into the send
+      // staging (this CTA's own ring) ...
+      uint32_t send_off = send_base;
+      for (int o = 0; o < CL; ++o) {
+        const int cols = own_cols(o);
+        if (o == r || cols == 0) continue;
+        const int c0 = 64 * own_box0(o);
+        uint8_t* blk = smem + (send_off - sbase);
+#pragma unroll 1
+        for (int c32 = 0; c32 < cols / 32; ++c32) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(t_row + c0 + c32 * 32, v);
+          tmem_ld_wait(v);
+#pragma unroll
+          for (int w = 0; w < 8; ++w)
+            *reinterpret_cast<uint4*>(blk + split_block_offset(row, c32 * 8 + w, cols)) =
+                make_uint4(v[4 * w], v[4 * w + 1], v[4 * w + 2], v[4 * w + 3]);
+        }
+        send_off += static_cast<uint32_t>(Cfg::BM * cols * 4);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      // ... then one bulk copy per owner once its ring is free
+      send_off = send_base;
+      for (int o = 0; o < CL; ++o) {
+        const int cols = own_cols(o);
+        if (o == r || cols == 0) continue;
+        int rdy = 1;
+        if (lane == 0) rdy = wait_phase_cluster(ready_bar0 + 8u * o, 0, wd, kWdReduce) ? 1 : 0;
+        rdy = __shfl_sync(0xffffffffu, rdy, 0);
+        if (!rdy) {
+          ok = 0;
+          break;
+        }
+        if (lane == 0) {
+          // this warp's 32 rows, into owner o's slot for slice r
+          const int idx = r < o ? r : r - 1;
+          const uint32_t rows_off = static_cast<uint32_t>(q * 32 * cols * 4);
+          const uint32_t dst = mapa_shared(recv_base + idx * Cfg::BM * cols * 4 + rows_off, static_cast<uint32_t>(o));
+          bulk_copy_to_cluster(dst, send_off + rows_off, static_cast<uint32_t>(32 * cols * 4),
+                               mapa_shared(recv_bar, static_cast<uint32_t>(o)));
+        }
+        send_off += static_cast<uint32_t>(Cfg::BM * cols * 4);
+      }
+    }
+    if (ok && oc > 0) {
+      // own range: wait for the other slices' partials, add in slice order
+      int got = 1;
+      if (lane == 0) got = wait_phase_cluster(recv_bar, 0, wd, kWdReduce) ? 1 : 0;
+      got = __shfl_sync(0xffffffffu, got, 0);
+      if (got) {
+        const int x0 = off + ox0;
+        const int y0 = mt * Cfg::BM + q * kEpiRows;
+        if constexpr (FUSED)
+          prefetch_c_row(p.epi, p.C, p.M, p.N, p.ldc, static_cast<int64_t>(y0) + lane, x0, oc);
+#pragma unroll 1
+        for (int c64 = 0; c64 < oc / 64; ++c64) {
+          float acc[64];
+          bool first = true;
+          for (int sl = 0; sl < CL; ++sl) {
+            if (!has_partial(sl)) continue;
+            if (sl == r) {
+              uint32_t v0[32], v1[32];
+              tmem_ld_32x32b_x32(t_row + ox0 + c64 * 64, v0);
+              tmem_ld_32x32b_x32(t_row + ox0 + c64 * 64 + 32, v1);
+              tmem_ld_wait(v0);
+              tmem_ld_wait(v1);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                acc[i] = first ? __uint_as_float(v0[i]) : acc[i] + __uint_as_float(v0[i]);
+                acc[32 + i] = first ? __uint_as_float(v1[i]) : acc[32 + i] + __uint_as_float(v1[i]);
+              }
+            } else {
+              const int idx = sl < r ? sl : sl - 1;
+              const uint8_t* blk = smem + idx * Cfg::BM * oc * 4;
+#pragma unroll
+              for (int w = 0; w < 16; ++w) {
+                const float4 f = *reinterpret_cast<const float4*>(blk + split_block_offset(row, c64 * 16 + w, oc));
+                acc[4 * w] = first ? f.x : acc[4 * w] + f.x;
+                acc[4 * w + 1] = first ? f.y : acc[4 * w + 1] + f.y;
+                acc[4 * w + 2] = first ? f.z : acc[4 * w + 2] + f.z;
+                acc[4 * w + 3] = first ? f.w : acc[4 * w + 3] + f.w;
+              }
+            }
+            first = false;
+          }
+          uint32_t v0[32], v1[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            v0[i] = __float_as_uint(acc[i]);
+            v1[i] = __float_as_uint(acc[32 + i]);
+          }
+          // one row of 64 columns per thread, straight from registers
+          store_row64<FUSED>(v0, v1, p.epi, const_cast<uint16_t*>(p.C), p.M, p.N, p.ldc,
+                             static_cast<int64_t>(y0) + lane, x0 + c64 * 64);
+        }
+      } else {
+        ok = 0;
+      }
+    }
+  }
+
+  // Leaving: an owner arrives here only after its partials have landed, so
+  // once every CTA of the cluster has arrived no copy reads or writes a
+  // CTA's shared memory and no remote arrival is pending.
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  if (warp == 1) tmem_dealloc(tmem_base, Cfg::ACC_COLS);
+  cluster_sync();
+}
+
 }  // namespace
 
 cudaError_t launch_tri_leaves_tc(const CUtensorMap& x, const CUtensorMap& l, const CUtensorMap& c,
                                  const TcArgs& args, const TriLeaves& leaves, const TriLeafExt& ext,
                                  cudaStream_t stream) {
-  static std::atomic<bool> attr_done[2][64];
+  static std::atomic<bool> attr_done[3][2][64];
   const int fused = args.epi.mode != 0 ? 1 : 0;
-  auto kern = fused ? hgemm_tri_leaves_tc_kernel<true> : hgemm_tri_leaves_tc_kernel<false>;
   for (int b = 0; b < leaves.count; ++b)
     if (leaves.size[b] <= 0 || leaves.size[b] > LeafCfg::MAX_S || leaves.size[b] % LeafCfg::BK != 0 ||
         ext.ext[b] < 0 || ext.ext[b] % LeafCfg::BK != 0)
       return cudaErrorInvalidValue;
-  if (args.part_cols != 0 && args.part_cols != LeafCfg::L_BOX_ROWS) return cudaErrorInvalidValue;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64 || !attr_done[fused][dev]) {
+  int sms = 0;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  // Few units (a short X): each unit's K blocks split over a cluster of four
+  // CTAs when four times the units fit in one wave, else of two when twice
+  // the units do.
+  const int64_t units = args.num_tiles;
+  const int slices = units * 4 <= sms ? 4 : units * 2 <= sms ? 2 : 1;
+  auto kern = slices == 4 ? (fused ? hgemm_tri_leaves_split_kernel<4, true> : hgemm_tri_leaves_split_kernel<4, false>)
+              : slices == 2 ? (fused ? hgemm_tri_leaves_split_kernel<2, true> : hgemm_tri_leaves_split_kernel<2, false>)
+                            : (fused ? hgemm_tri_leaves_tc_kernel<true> : hgemm_tri_leaves_tc_kernel<false>);
+  const int kind = slices == 4 ? 2 : slices == 2 ? 1 : 0;
+  if (dev < 0 || dev >= 64 || !attr_done[kind][fused][dev]) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LeafCfg::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) attr_done[fused][dev] = true;
+    if (dev >= 0 && dev < 64) attr_done[kind][fused][dev] = true;
+  }
+  if (slices > 1) {
+    PdlLaunch pl(dim3(static_cast<unsigned>(units * slices)), dim3(LeafCfg::THREADS), LeafCfg::SMEM_BYTES, stream);
+    pl.cluster(static_cast<unsigned>(slices));
+    return cudaLaunchKernelEx(&pl.cfg, kern, x, l, c, args, leaves, ext);
   }
   PdlLaunch pl(dim3(static_cast<unsigned>(args.grid)), dim3(LeafCfg::THREADS), LeafCfg::SMEM_BYTES, stream);
   return cudaLaunchKernelEx(&pl.cfg, kern, x, l, c, args, leaves, ext);

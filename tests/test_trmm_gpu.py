@@ -75,6 +75,21 @@ def test_trmm_tensor_core_leaf_orders(n, m):
     assert_close(run_trmm(a, b), ref, what=f"trmm {n}x{m}")
 
 
+@pytest.mark.parametrize("n,m,slices", [(4096, 256, 4), (1280, 200, 4), (2048, 1100, 2), (1088, 1200, 2),
+                                        (2048, 2500, 1)])
+def test_trmm_leaves_split_over_clusters(n, m, slices):
+    """With few leaf units (tiles of 128 rows of Bᵀ × leaves) every unit's K
+    blocks are split over a cluster of four CTAs (four times the units fit on
+    the GPU's 152 SMs at once) or two (twice do), the partial sums reduced
+    through distributed shared memory; more units take the persistent kernel.
+    Leaves of 256 columns carrying up to 3840 update columns (4096 x 256),
+    leaves of other orders (1088) and ragged rows of B; n = 2048, m = 1100 has
+    72 units, 1088 x 1200 has 60."""
+    a, b = trmm_inputs(n, m, seed=53 + n + m)
+    ref = oracle.trmm(a, b, alpha=0.75, nthreads=oracle_threads())
+    assert_close(run_trmm(a, b, alpha=0.75), ref, what=f"trmm {n}x{m}, {slices} slices")
+
+
 @pytest.mark.parametrize("path", [None, tc.HGEMM_PATH_GENERIC])
 def test_trmm_leaf_kernels_agree(path):
     """The same product with the tensor-core leaves (default) and the generic
