@@ -150,7 +150,9 @@ def trsm_flops(spec):
 # The triangular operations: the call, its oracle, its flop count and launches.
 TRI_OPS = {
     "trmm": dict(call="hgemm_trmm", oracle="trmm", flops=trmm_flops, launches=trmm_launches,
-                 kernel="hgemm_tri_leaves_tc_kernel (hgemm_tri_leaves_kernel when n % 64 != 0) + hgemm update kernels"),
+                 kernel="hgemm_tri_leaves_tc_kernel, or hgemm_tri_leaves_split_kernel (each leaf unit's K split "
+                        "over a cluster) when few leaf units run (hgemm_tri_leaves_kernel when n % 64 != 0) "
+                        "+ hgemm update kernels"),
     "trsm": dict(call="hgemm_trsm", oracle="trsm", flops=trsm_flops, launches=trsm_launches,
                  kernel="scale_copy_kernel + trsm_inverse_kernel + hgemm_tc2_kernel (diagonal blocks by their "
                         "inverses, updates); without a workspace trsm_leaf_kernel for the diagonal blocks"),
@@ -246,7 +248,9 @@ def load_peaks():
 KERNEL_SOURCES = {"hgemm_tc_kernel": ("hgemm_tc.cu",), "hgemm_tc2_kernel": ("hgemm_tc2.cu",),
                   "hgemm_tc2w_kernel": ("hgemm_tc2w.cu",), "hgemm_skinny_kernel": ("hgemm_skinny.cu",),
                   "hgemm_generic_kernel": ("hgemm_generic.cu",),
-                  "trsm_chain_kernel": ("hgemm_trsm_chain.cu", "trsm_chain.h")}
+                  "trsm_chain_kernel": ("hgemm_trsm_chain.cu", "trsm_chain.h"),
+                  "hgemm_tri_leaves_tc_kernel": ("hgemm_trileaf.cu",),
+                  "hgemm_tri_leaves_split_kernel": ("hgemm_trileaf.cu",)}
 SHARED_SOURCES = ["internal.h", "kernel_common.cuh", "ptx.cuh", "debug.cuh"]
 
 
@@ -785,13 +789,22 @@ def run_tri_ours(args, spec, a_col, b_col, world, rank, local):
     peaks, peak_src = load_peaks()
     peak = peaks["bf16_tflops"] * FP16_PER_BF16
     achieved = flops / (median_ms * 1e-3) / 1e12
-    # DRAM traffic of the chain kernel (the solve's dominant launch), from a
-    # committed ncu record of the current sources, per launch
-    traffic = (profiled_traffic("trsm_chain_kernel", args.workload, kernel_sources_sha("trsm_chain_kernel"))
-               if chain else None)
+    # DRAM traffic of the solve's dominant launch (the chain kernel), or of a
+    # TRMM that is one launch of the leaves, from a committed ncu record of the
+    # current sources, per launch
+    traffic, traffic_kernel = None, None
+    if chain:
+        traffic_kernel = "trsm_chain_kernel"
+    elif op == "trmm" and n % 64 == 0 and trmm_launches(n, m) == 1:
+        for k in ("hgemm_tri_leaves_split_kernel", "hgemm_tri_leaves_tc_kernel"):
+            if profiled_traffic(k, args.workload, kernel_sources_sha(k)) is not None:
+                traffic_kernel = k
+                break
+    if traffic_kernel:
+        traffic = profiled_traffic(traffic_kernel, args.workload, kernel_sources_sha(traffic_kernel))
     roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
             "frac": achieved / peak, "traffic": traffic,
-            "traffic_kernel": "trsm_chain_kernel" if chain else None,
+            "traffic_kernel": traffic_kernel,
             "peak_source": f"{peak_src}: bf16_tflops (burst) x {FP16_PER_BF16} fp16/bf16",
             "timing": "median call", "kernel": CHAIN_KERNELS if chain else ops["kernel"],
             "algorithmic_flops": flops, "algorithmic_bytes": 2.0 * (n * (n + 1) / 2 + 2 * n * m)}
