@@ -50,12 +50,16 @@ def test_withheld_arrival_times_out_and_the_context_survives(path):
 
 
 @pytest.mark.gpu
-def test_withheld_arrival_in_the_trmm_leaf_kernel():
+@pytest.mark.parametrize("m", [256, 8192], ids=["split-clusters", "persistent"])
+def test_withheld_arrival_in_the_trmm_leaf_kernel(m):
     """The same on the triangular product: the tensor-core leaf kernel (the
     first launch of hgemm_trmm, n a multiple of 64) records the timeout and
-    returns; afterwards the same context computes the product correctly."""
+    returns; afterwards the same context computes the product correctly.
+    m = 256: 4 leaf units, each split over a cluster of four CTAs (the CTAs
+    without K blocks still wait for partials that never come); m = 8192: 128
+    units on the persistent kernel."""
     torch = torch_cuda()
-    n, m = 512, 256
+    n = 512
     rng = np.random.default_rng(37)
     a = rng.uniform(0, 1, size=(n, n)).astype(np.float16)
     b = rng.uniform(0, 1, size=(n, m)).astype(np.float16)
