@@ -704,6 +704,33 @@ __global__ void __launch_bounds__(192, 1)
   cluster_sync();
 }
 
+// Clusters of CL CTAs of the split kernel that the device holds at once (0:
+// none, e.g. on a partition too small for them), measured once per device.
+template <int CL>
+int split_clusters_resident(int dev, int sms) {
+  static std::atomic<int> cached[64];  // count + 1; 0: not measured
+  if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev] - 1;
+  auto kern = hgemm_tri_leaves_split_kernel<CL, false>;
+  int n = 0;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LeafCfg::SMEM_BYTES) == cudaSuccess) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CL;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>((sms / CL) * CL));
+    cfg.blockDim = dim3(LeafCfg::THREADS);
+    cfg.dynamicSmemBytes = LeafCfg::SMEM_BYTES;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
+  }
+  (void)cudaGetLastError();
+  if (dev >= 0 && dev < 64) cached[dev] = n + 1;
+  return n;
+}
+
 }  // namespace
 
 cudaError_t launch_tri_leaves_tc(const CUtensorMap& x, const CUtensorMap& l, const CUtensorMap& c,
@@ -722,9 +749,11 @@ cudaError_t launch_tri_leaves_tc(const CUtensorMap& x, const CUtensorMap& l, con
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
   // Few units (a short X): each unit's K blocks split over a cluster of four
   // CTAs when four times the units fit in one wave, else of two when twice
-  // the units do.
+  // the units do, and when the device holds that many such clusters at once.
   const int64_t units = args.num_tiles;
-  const int slices = units * 4 <= sms ? 4 : units * 2 <= sms ? 2 : 1;
+  const int slices = units * 4 <= sms && units <= split_clusters_resident<4>(dev, sms)   ? 4
+                     : units * 2 <= sms && units <= split_clusters_resident<2>(dev, sms) ? 2
+                                                                                         : 1;
   auto kern = slices == 4 ? (fused ? hgemm_tri_leaves_split_kernel<4, true> : hgemm_tri_leaves_split_kernel<4, false>)
               : slices == 2 ? (fused ? hgemm_tri_leaves_split_kernel<2, true> : hgemm_tri_leaves_split_kernel<2, false>)
                             : (fused ? hgemm_tri_leaves_tc_kernel<true> : hgemm_tri_leaves_tc_kernel<false>);
