@@ -115,6 +115,10 @@ struct Gemm {
   int64_t M, N, K;
   int64_t lda, ldb, ldc;
   bool a_mn = false, b_mn = false;
+  // where a fused epilogue reads C_old (row pitch ld_src), when not from C
+  // itself: the TMA paths only (the generic kernel reads C_old from C)
+  const void* c_src = nullptr;
+  int64_t ld_src = 0;
 };
 
 Gemm dense(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K) {
@@ -238,7 +242,7 @@ int validate(const Gemm& g) {
 bool tma_ok(const Gemm& g) {
   auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
   return al16(g.A) && al16(g.B) && al16(g.C) && g.lda % 8 == 0 && g.ldb % 8 == 0 &&
-         g.ldc % 8 == 0 && g.N % 8 == 0;
+         g.ldc % 8 == 0 && g.N % 8 == 0 && (!g.c_src || (al16(g.c_src) && g.ld_src % 8 == 0));
 }
 
 int choose_path(const Gemm& g, const hg::DeviceProfile& prof, bool fused, int* split, int* tile_n) {
@@ -428,8 +432,8 @@ int run_tc(const Gemm& g, const hg::EpiArgs& epi, const DeviceState& dev, cudaSt
   args.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
   args.inject = g_inject.load(std::memory_order_relaxed);
   args.epi = epi;
-  args.C = static_cast<const uint16_t*>(C);
-  args.ldc = g.ldc;
+  args.C = static_cast<const uint16_t*>(g.c_src ? g.c_src : C);  // C_old, for a fused epilogue
+  args.ldc = g.c_src ? g.ld_src : g.ldc;
   cudaError_t e = bn == hg::kNarrowBN ? hg::launch_tc_128x64(ma, mb, mc, args, stream)
                                       : hg::launch_tc_128x256(ma, mb, mc, args, stream);
   return e == cudaSuccess ? HGEMM_OK : cuda_fail(e);
@@ -495,8 +499,8 @@ int run_tc_pair(const Gemm& g, const hg::EpiArgs& epi, const DeviceState& dev,
   args.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
   args.inject = g_inject.load(std::memory_order_relaxed);
   args.epi = epi;
-  args.C = static_cast<const uint16_t*>(C);
-  args.ldc = g.ldc;
+  args.C = static_cast<const uint16_t*>(g.c_src ? g.c_src : C);  // C_old, for a fused epilogue
+  args.ldc = g.c_src ? g.ld_src : g.ldc;
   args.a_mn = g.a_mn ? 1 : 0;
   args.b_mn = g.b_mn ? 1 : 0;
   CUtensorMap ma, mb, mbp, mc;
@@ -553,8 +557,8 @@ int run_tc_wide(const Gemm& g, const hg::EpiArgs& epi, const DeviceState& dev,
   args.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
   args.inject = g_inject.load(std::memory_order_relaxed);
   args.epi = epi;
-  args.C = static_cast<const uint16_t*>(C);
-  args.ldc = g.ldc;
+  args.C = static_cast<const uint16_t*>(g.c_src ? g.c_src : C);  // C_old, for a fused epilogue
+  args.ldc = g.c_src ? g.ld_src : g.ldc;
   args.a_mn = g.a_mn ? 1 : 0;
   args.b_mn = g.b_mn ? 1 : 0;
   cudaError_t e = hg::launch_tc_wide(ma, mb, mc, args, stream);
@@ -594,8 +598,8 @@ int run_skinny(const Gemm& g, int split, int tile_n, const hg::EpiArgs& epi, con
   args.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
   args.inject = g_inject.load(std::memory_order_relaxed);
   args.epi = epi;
-  args.C = static_cast<const uint16_t*>(C);
-  args.ldc = g.ldc;
+  args.C = static_cast<const uint16_t*>(g.c_src ? g.c_src : C);  // C_old, for a fused epilogue
+  args.ldc = g.c_src ? g.ld_src : g.ldc;
   args.a_mn = g.a_mn ? 1 : 0;
   args.b_mn = g.b_mn ? 1 : 0;
   cudaError_t e = hg::launch_skinny(split, tile_n, ma, mb, mc, args, stream);
@@ -609,6 +613,7 @@ int dispatch(const Gemm& g, const hg::EpiArgs& epi, const DeviceState& dev, cuda
     case HGEMM_PATH_NONE:
       return HGEMM_OK;
     case HGEMM_PATH_ZERO:
+      if (g.c_src) return HGEMM_ERR_INVALID_ARG;  // the empty sum reads C_old from C
       e = hg::launch_empty_sum(static_cast<uint16_t*>(g.C), g.M, g.N, g.ldc, epi, stream);
       return e == cudaSuccess ? HGEMM_OK : cuda_fail(e);
     case HGEMM_PATH_TC:
@@ -622,6 +627,7 @@ int dispatch(const Gemm& g, const hg::EpiArgs& epi, const DeviceState& dev, cuda
     case HGEMM_PATH_SKINNY:
       return run_skinny(g, split, tile_n, epi, dev, stream);
     default: {
+      if (g.c_src) return HGEMM_ERR_INVALID_ARG;  // the generic kernel reads C_old from C
       hg::PlainArgs pa{static_cast<const uint16_t*>(g.A), static_cast<const uint16_t*>(g.B),
                        static_cast<uint16_t*>(g.C), g.M, g.N, g.K, g.lda, g.ldb, g.ldc,
                        t_ctx.status, g_timeout_ns.load(), epi, g.a_mn ? 1 : 0, g.b_mn ? 1 : 0};
@@ -1352,9 +1358,17 @@ int trsm_impl(const hgemm_half_t* A, int64_t lda, const hgemm_half_t* B, int64_t
     return HGEMM_OK;
   }
   int leaf_index = 0;  // position in `leaves` (the order of the solve)
-  if (!in_place || alpha != 1.0f) {
-    e = hg::launch_scale_copy(reinterpret_cast<const uint16_t*>(B), ldb, x, ldx, n, m, alpha,
-                              dev->num_sms, stream);
+  // X := alpha·B, folded into the solve when it goes by the inverses and B
+  // suits TMA: the first write of every row block of X is then either its
+  // product by the inverse, reading alpha·B (the block the recursion reaches
+  // first), or an update that reads alpha·B as C_old (its first half, or
+  // second forward); a block solved by substitution copies its rows first.
+  // Otherwise one scaled copy of all of B first.
+  const bool b_src = (reinterpret_cast<uintptr_t>(B) & 15u) == 0 && ldb % 8 == 0;
+  const bool fold = by_inverse && b_src && (!in_place || alpha != 1.0f);
+  const uint16_t* bsrc = reinterpret_cast<const uint16_t*>(B);
+  if (!fold && (!in_place || alpha != 1.0f)) {
+    e = hg::launch_scale_copy(bsrc, ldb, x, ldx, n, m, alpha, dev->num_sms, stream);
     if (e != cudaSuccess) return cuda_fail(e);
     chained = true;
   }
@@ -1369,12 +1383,17 @@ int trsm_impl(const hgemm_half_t* A, int64_t lda, const hgemm_half_t* B, int64_t
   // second operand, pitch lda); it reads [off, off+s1) and writes
   // [off+s1, off+s).
   const hg::EpiArgs subtract{-1.0f, 1.0f, nullptr, 0, 2};
+  // the first write of a row block when the copy is folded: alpha·B - product
+  const hg::EpiArgs subtract_from_b{-1.0f, alpha, nullptr, 0, 2};
+  const hg::EpiArgs scale_b{alpha, 0.0f, nullptr, 0, alpha != 1.0f ? 1 : 0};
   // The page's recursion, second half first: every row of a block depends on
   // the rows below it (forward: first half first, on the rows above).
   // inverse: the block's inverse is in the workspace (a block of the
   // inverse-product recursion); otherwise the blocks of order ≤ kTrsmLeaf
   // are solved by substitution.
-  std::function<int(int64_t, int64_t, bool)> solve = [&](int64_t off, int64_t s, bool inverse) -> int {
+  // fresh: rows [off, off + s) of X not yet written (alpha·B not yet copied)
+  std::function<int(int64_t, int64_t, bool, bool)> solve = [&](int64_t off, int64_t s, bool inverse,
+                                                               bool fresh) -> int {
     if (inverse && s <= hg::kTrsmInverseLeaf) {
       const int b = leaf_index++;
       if (s % 8 == 0) {
@@ -1386,17 +1405,26 @@ int trsm_impl(const hgemm_half_t* A, int64_t lda, const hgemm_half_t* B, int64_t
         // so the product runs in place.
         // forward: X_bᵀ := X_bᵀ · L⁻ᵀ, whose column j is row j of L⁻¹: the
         // same workspace read as a K-contiguous second operand
-        Gemm g{x + off, W + static_cast<int64_t>(b) * hg::kTrsmInverseLeaf * hg::kTrsmInverseLeaf, x + off, m,
-               s, s, ldx, hg::kTrsmInverseLeaf, ldx};
+        // fresh: X_bᵀ := alpha·B_bᵀ · L⁻¹, the first operand read from B
+        Gemm g{fresh ? static_cast<const void*>(bsrc + off) : static_cast<const void*>(x + off),
+               W + static_cast<int64_t>(b) * hg::kTrsmInverseLeaf * hg::kTrsmInverseLeaf, x + off, m,
+               s, s, fresh ? ldb : ldx, hg::kTrsmInverseLeaf, ldx};
         g.b_mn = !fwd;
         chained = true;
-        return s > hg::kPairBN ? run_tc_wide(g, kPlainEpilogue, *dev, stream)
-                               : run_tc_pair(g, kPlainEpilogue, *dev, stream, nullptr, true);
+        const hg::EpiArgs& epi = fresh ? scale_b : kPlainEpilogue;
+        return s > hg::kPairBN ? run_tc_wide(g, epi, *dev, stream)
+                               : run_tc_pair(g, epi, *dev, stream, nullptr, true);
       }
       // order not a multiple of 8: this block by substitution
-      return solve(off, s, false);
+      return solve(off, s, false, fresh);
     }
     if (s <= hg::kTrsmLeaf) {
+      if (fresh) {
+        // the substitution works in place: this block's rows of alpha·B first
+        e = hg::launch_scale_copy(bsrc + off, ldb, x + off, ldx, s, m, alpha, dev->num_sms, stream);
+        if (e != cudaSuccess) return cuda_fail(e);
+        chained = true;
+      }
       const cudaError_t le = hg::launch_trsm_leaf(a, lda, x, ldx, off, static_cast<int>(s), m,
                                                   dev->num_sms, chained, fwd, stream);
       chained = true;
@@ -1404,20 +1432,28 @@ int trsm_impl(const hgemm_half_t* A, int64_t lda, const hgemm_half_t* B, int64_t
     }
     const int64_t s1 = ((s / 2 + 63) / 64) * 64, s2 = s - s1;
     if (fwd) {
-      int r = solve(off, s1, inverse);
+      int r = solve(off, s1, inverse, fresh);
       if (r != HGEMM_OK) return r;
       Gemm g{x + off, a + off * lda + off + s1, x + off + s1, m, s2, s1, ldx, lda, ldx};
       g.b_mn = true;
-      if ((r = dispatch(g, subtract, *dev, stream)) != HGEMM_OK) return r;
-      return solve(off + s1, s2, inverse);
+      if (fresh) {
+        g.c_src = bsrc + off + s1;
+        g.ld_src = ldb;
+      }
+      if ((r = dispatch(g, fresh ? subtract_from_b : subtract, *dev, stream)) != HGEMM_OK) return r;
+      return solve(off + s1, s2, inverse, false);
     }
-    int r = solve(off + s1, s2, inverse);
+    int r = solve(off + s1, s2, inverse, fresh);
     if (r != HGEMM_OK) return r;
-    const Gemm g{x + off + s1, a + off * lda + off + s1, x + off, m, s1, s2, ldx, lda, ldx};
-    if ((r = dispatch(g, subtract, *dev, stream)) != HGEMM_OK) return r;
-    return solve(off, s1, inverse);
+    Gemm g{x + off + s1, a + off * lda + off + s1, x + off, m, s1, s2, ldx, lda, ldx};
+    if (fresh) {
+      g.c_src = bsrc + off;
+      g.ld_src = ldb;
+    }
+    if ((r = dispatch(g, fresh ? subtract_from_b : subtract, *dev, stream)) != HGEMM_OK) return r;
+    return solve(off, s1, inverse, false);
   };
-  return solve(0, n, by_inverse);
+  return solve(0, n, by_inverse, fold);
 }
 
 }  // namespace
