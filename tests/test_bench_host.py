@@ -56,3 +56,39 @@ def test_nvml_sampler_without_a_device_reports_itself_unavailable():
         assert rec["samples"] == 0 and "unavailable" in rec["source"]
     else:   # a host with a GPU: whatever it sampled is summarised
         assert rec["samples"] >= 0
+
+
+def test_path_tables_match_the_header():
+    """The benchmark's names for the kernel paths agree with hgemm.h."""
+    import tensor_core_dense_fp16_gb300 as tc
+    paths = {"tc": tc.HGEMM_PATH_TC, "skinny": tc.HGEMM_PATH_SKINNY, "generic": tc.HGEMM_PATH_GENERIC,
+             "pair": tc.HGEMM_PATH_TC_PAIR, "wide": tc.HGEMM_PATH_TC_WIDE, "narrow": tc.HGEMM_PATH_TC_NARROW}
+    assert bench.FORCED_PATHS == dict(paths, auto=-1)
+    assert set(bench.KERNEL_OF_PATH) == set(paths.values()) == set(bench.TILES_OF_PATH)
+    # each kernel a path names has its sources listed for the traffic records
+    assert set(bench.KERNEL_OF_PATH.values()) <= set(bench.KERNEL_SOURCES)
+
+
+def test_traffic_records_are_well_formed():
+    """Every traffic_record line of profiles/ parses, names a kernel whose
+    sources the benchmark hashes and a known workload, and carries a 16-digit
+    hash and a positive byte count."""
+    import glob
+    import json
+    import os
+    import re
+    import synth
+    found = 0
+    for path in sorted(glob.glob(os.path.join(bench.ROOT, "profiles", "*.md"))):
+        with open(path, encoding="utf-8") as f:
+            for line in f:
+                m = re.match(r"\s*traffic_record:\s*(\{.*\})\s*$", line)
+                if not m:
+                    continue
+                rec = json.loads(m.group(1))
+                found += 1
+                assert rec["kernel"] in bench.KERNEL_SOURCES, (path, rec)
+                assert rec["workload"].split("+")[0] in synth.WORKLOADS, (path, rec)
+                assert re.fullmatch(r"[0-9a-f]{16}", rec["source_sha"]), (path, rec)
+                assert rec["bytes_per_launch"] > 0, (path, rec)
+    assert found >= 8
