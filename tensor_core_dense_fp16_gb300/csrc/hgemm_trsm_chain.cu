@@ -223,6 +223,52 @@ __device__ __forceinline__ void load_a(const Group& g, const Maps& m, uint32_t s
   }
 }
 
+// The TMA boxes of one operand over one K segment of a task, worked out
+// once per task so that the producer's per-step work is a few additions and
+// the copies: box i of the segment's k-step kk is at
+// (x0 + kk·kdx + i·bdx, y0 + kk·kdy + i·bdy) of `map`.
+struct OperandStream {
+  const CUtensorMap* map;
+  int x0, y0, kdx, kdy, bdx, bdy, boxes;
+};
+
+// The coordinates load_a and load_b use, as streams: the first operand of
+// segment `seg2` (0: the task's first K segment) for row tile mi, the second
+// for column tile ni.
+__device__ __forceinline__ OperandStream stream_a(const Group& g, const Maps& m, int mi, bool seg2) {
+  const bool mn = !seg2 && g.a_mn;
+  const int kc0 = seg2 ? g.a2_kbase : g.a_kbase;
+  const int mc0 = (seg2 ? 0 : g.a_mbase) + mi * g.bm;
+  OperandStream o;
+  o.map = seg2 ? m.x : map_of(g.a_map, m.x, m.b, m.w, m.wr, m.a);
+  o.boxes = g.bm / kBox;
+  if (mn) {
+    o.x0 = mc0, o.y0 = kc0, o.kdx = 0, o.kdy = kTcBK, o.bdx = kBox, o.bdy = 0;
+  } else {
+    o.x0 = kc0, o.y0 = mc0, o.kdx = kTcBK, o.kdy = 0, o.bdx = 0, o.bdy = kBox;
+  }
+  return o;
+}
+__device__ __forceinline__ OperandStream stream_b(const Group& g, const Maps& m, int ni, bool seg2) {
+  const bool mn = seg2 || g.b_mn;
+  const int kc0 = seg2 ? g.b2_kbase : g.b_kbase;
+  const int nc0 = (seg2 ? 0 : g.b_nbase) + ni * g.bn;
+  OperandStream o;
+  o.map = seg2 ? m.w : map_of(g.b_map, m.x, m.b, m.w, m.wr, m.a);
+  o.boxes = g.bn / kBox;
+  if (mn) {
+    o.x0 = nc0, o.y0 = kc0, o.kdx = 0, o.kdy = kTcBK, o.bdx = kBox, o.bdy = 0;
+  } else {
+    o.x0 = kc0, o.y0 = nc0, o.kdx = kTcBK, o.kdy = 0, o.bdx = 0, o.bdy = kBox;
+  }
+  return o;
+}
+__device__ __forceinline__ void load_stream(const OperandStream& o, uint32_t dst, uint32_t bar, int kk) {
+  const int x = o.x0 + kk * o.kdx, y = o.y0 + kk * o.kdy;
+  tma_load_2d(dst, o.map, bar, x, y);
+  for (int i = 1; i < o.boxes; ++i) tma_load_2d(dst + i * kBoxBytes, o.map, bar, x + i * o.bdx, y + i * o.bdy);
+}
+
 // True once the phase with parity `parity` of `bar` has completed, without
 // suspending (a stage that landed during the previous stage's MMAs is then
 // taken at once; otherwise the caller falls back to the suspending wait).
@@ -541,10 +587,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           int mi, ni;
           tile_of(g, tk.tile, mi, ni);
           const int kall = g.ksteps + g.ksteps2;
+          const OperandStream a1 = stream_a(g, maps, mi, false), a2 = stream_a(g, maps, mi, true);
+          const OperandStream b1 = stream_b(g, maps, ni, false), b2 = stream_b(g, maps, ni, true);
           for (int kk = 0; ok && kk < kall; ++kk) {
             const uint32_t sa = ring + s * g.stage_bytes;
+            const bool seg2 = kk >= g.ksteps;
+            const int kl = seg2 ? kk - g.ksteps : kk;
             if (!(prefetched && kk < pref)) {
-              if (!wait_phase(empty_bar(s), (ebits >> s) & 1u, wd, kWdProducerEmpty)) {
+              // a stage freed during the previous copies is taken without suspending
+              if (!mbar_test_wait(empty_bar(s), (ebits >> s) & 1u) &&
+                  !wait_phase(empty_bar(s), (ebits >> s) & 1u, wd, kWdProducerEmpty)) {
                 ok = false;
                 break;
               }
@@ -553,9 +605,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (!(p.inject == 1 && fills == 0))  // testing aid: withhold one arrival
                 mbar_arrive_expect_tx(full_bar(s), g.tx_bytes);
               ++fills;
-              load_b(g, maps, sa + kASlot, full_bar(s), ni, kk);
+              load_stream(seg2 ? b2 : b1, sa + kASlot, full_bar(s), kl);
             }
-            load_a(g, maps, sa, full_bar(s), mi, kk);
+            load_stream(seg2 ? a2 : a1, sa, full_bar(s), kl);
             if (++s == g.stages) s = 0;
           }
         }
