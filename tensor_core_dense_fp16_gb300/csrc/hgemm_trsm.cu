@@ -289,8 +289,11 @@ __device__ __forceinline__ void trsm_leaf_body(const uint16_t* __restrict__ A, i
         *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
     }
   };
-  // thread r's segment of group g: A(off+32g .. +31, off+r), zero past the
-  // block's order, into buffer g % 2 (rows of warps above group g only)
+  // the warp's rows' segments of group g: A(off+32g .. +31, off+rr) for its
+  // rows rr, zero past the block's order, into buffer g % 2 (warps above
+  // group g only). Each segment is 64 contiguous bytes of A, copied by four
+  // consecutive lanes, so that one copy instruction of the warp touches 8
+  // segments rather than 32 (the copies' cost is in the lines they touch).
   auto stage_group = [&](int g) {
     if constexpr (FWD) {
       stage_fwd(g);
@@ -298,16 +301,17 @@ __device__ __forceinline__ void trsm_leaf_body(const uint16_t* __restrict__ A, i
     }
     if (warp >= g) return;
     const int c0 = g * kGroup, sg = min(kGroup, s - c0);
-    const uint16_t* src = A + (off + r) * lda + off + c0;
-    uint16_t* dst = a_stage + ((g & 1) * LEAF + r) * AP;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int it = 0; it < 4; ++it) {
+      const int i = it * 32 + lane;
+      const int rr = warp * kGroup + (i >> 2), q = i & 3;
       int valid = sg - 8 * q;
       valid = valid < 0 ? 0 : (valid > 8 ? 8 : valid);
+      uint16_t* dst = a_stage + ((g & 1) * LEAF + rr) * AP + 8 * q;
       if (valid > 0)
-        cp_async_16(smem_u32(dst + 8 * q), src + 8 * q, 2 * valid);
+        cp_async_16(smem_u32(dst), A + (off + rr) * lda + off + c0 + 8 * q, 2 * valid);
       else
-        *reinterpret_cast<uint4*>(dst + 8 * q) = make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
     }
   };
   // Against the identity, the right-hand sides j0 .. j0+COLS-1 have zero
