@@ -77,8 +77,8 @@ typedef uint16_t hgemm_half_t; /* IEEE binary16 bit pattern */
 #define HGEMM_PATH_TC_NARROW 7 /* the HGEMM_PATH_TC kernel on 128×64 tiles: outputs one wave covers */
 
 /* Largest M, N or K accepted (TMA coordinates are signed 32-bit). */
-#define HGEMM_TRMM_MAX_N 16384          /* largest triangle hgemm_trmm accepts */
 #define HGEMM_MAX_DIM ((int64_t)0x7FFFFFFF)
+#define HGEMM_TRMM_MAX_N 16384          /* largest triangle hgemm_trmm accepts */
 
 /*
  * hgemm — C = A·B on `stream` (see the top of this file for layouts).
