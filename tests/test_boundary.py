@@ -5,6 +5,7 @@ status text) behaves as documented. No computing call is made here."""
 import ctypes
 import os
 import re
+import shutil
 
 import pytest
 
@@ -333,3 +334,54 @@ def test_binding_type_checks():
     h = torch.zeros(4, 4, dtype=torch.float16)
     with pytest.raises(ValueError):
         tc.hgemm(h, h, h, 4, 4, 4, stream=0)  # host tensors for a device call
+
+
+def _cuda_include_dir():
+    nvcc = shutil.which("nvcc")
+    roots = [os.path.dirname(os.path.dirname(nvcc))] if nvcc else []
+    roots += [os.environ.get("CUDA_HOME", ""), "/usr/local/cuda"]
+    for r in roots:
+        if r and os.path.exists(os.path.join(r, "include", "cuda_runtime_api.h")):
+            return os.path.join(r, "include")
+    return None
+
+
+def test_header_is_a_c_interface(lib, tmp_path):
+    """A plain C11 program (gcc, pedantic, warnings as errors) includes the
+    header, takes the address of every function it declares, links against
+    the library and calls the host-only entry points; their answers match
+    the binding's. Nothing of C++ leaks through the boundary."""
+    gcc, inc = shutil.which("gcc"), _cuda_include_dir()
+    if gcc is None or inc is None:
+        pytest.skip("gcc or the CUDA runtime headers are not available")
+    names = declared_functions()
+    src = ["#include <stdio.h>", '#include "hgemm.h"', "typedef void (*fn_t)(void);",
+           "static const fn_t fns[] = {"]
+    src += [f"  (fn_t)&{n}," for n in names]
+    src += ["};",
+            "int main(void) {",
+            '  printf("%d\\n", (int)(sizeof(fns) / sizeof(fns[0])));',
+            '  printf("%d\\n", hgemm_version());',
+            '  printf("%s\\n", hgemm_status_string(HGEMM_ERR_ALIAS));',
+            '  printf("%zu\\n", hgemm_trsm_workspace_size(8192));',
+            f'  printf("%d\\n", hgemm_select_path((const void *){A16:#x}, (const void *){B16:#x}, '
+            f'(const void *){C16:#x}, 4096, 256, 4096));',
+            f'  printf("%d\\n", hgemm_select_path((const void *){A16:#x}, (const void *){B16:#x}, '
+            f'(const void *){A16:#x}, 64, 64, 64));',
+            "  return 0;",
+            "}"]
+    c_file = tmp_path / "consumer.c"
+    c_file.write_text("\n".join(src) + "\n")
+    libdir = os.path.dirname(tc.library_path())
+    exe = tmp_path / "consumer"
+    import subprocess
+    subprocess.run([gcc, "-std=c11", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I",
+                    os.path.join(ROOT, "include"), "-I", inc, str(c_file), "-L", libdir, "-lhgemm",
+                    f"-Wl,-rpath,{libdir}", "-o", str(exe)], check=True, capture_output=True, text=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split("\n")
+    assert int(out[0]) == len(names)
+    assert int(out[1]) == lib.hgemm_version()
+    assert out[2] == tc.hgemm_status_string(tc.HGEMM_ERR_ALIAS)
+    assert int(out[3]) == tc.hgemm_trsm_workspace_size(8192)
+    assert int(out[4]) == tc.hgemm_select_path(A16, B16, C16, 4096, 256, 4096) == tc.HGEMM_PATH_SKINNY
+    assert int(out[5]) == tc.HGEMM_ERR_ALIAS
