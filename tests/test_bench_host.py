@@ -1,9 +1,13 @@
 """Host-side logic of the benchmark (CPU only): the roofline arithmetic of
 each configuration and the clock sampler's behaviour without a GPU."""
 
+import os
+
 import pytest
 
 import bench
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 PEAKS = {"hbm_gbs": 6789.0, "bf16_tflops": 1874.3}
 
@@ -92,3 +96,32 @@ def test_traffic_records_are_well_formed():
                 assert re.fullmatch(r"[0-9a-f]{16}", rec["source_sha"]), (path, rec)
                 assert rec["bytes_per_launch"] > 0, (path, rec)
     assert found >= 8
+
+
+@pytest.mark.parametrize("workload", ["hgemm_256", "trsm_n_4096x256"])
+def test_reference_arm_line(workload):
+    """`bench.py --impl reference` (the oracle on this host's cores) prints one
+    JSON line with the GPU arm's metric, unit and direction, a bounded sample
+    described in cpu_baseline, and an e2e of its own value with no copies."""
+    import json
+    import subprocess
+    import sys
+
+    import synth
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--workload", workload, "--steps", "2", "--warmup", "1"],
+                         check=True, capture_output=True, text=True, timeout=600, cwd=ROOT).stdout
+    lines = [ln for ln in out.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    spec = synth.WORKLOADS[workload]
+    assert d["impl"] == "reference"
+    assert d["metric"] == bench.metric_for(workload, spec)
+    assert d["unit"] == "TFLOP/s" and d["higher_is_better"] is True
+    assert d["steps"] == 2 and d["warmup"] == 1 and d["n_gpus"] == 1
+    assert d["value"] > 0 and d["ms_per_step"] > 0
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
+    assert d["config"]["workload"].startswith(workload)
