@@ -50,3 +50,23 @@ def test_single_process_needs_no_group():
     import bench
     assert bench.reduce_max(12.5, None, "cpu") == 12.5
     assert bench.whole_job_tflops(1, 4, 1.0e12, 2.0) == pytest.approx(2000.0)
+
+
+def test_reference_arm_under_two_ranks():
+    """`bench.py --impl reference` launched as two ranks (torchrun, as for an
+    N-GPU run): rank 0 alone times the oracle and prints the one line, the
+    other rank exits 0 without work."""
+    import json
+    import subprocess
+    import sys
+
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(_free_port()), "bench.py", "--impl",
+           "reference", "--workload", "hgemm_256", "--steps", "1", "--warmup", "1", "--gpus", "2"]
+    res = subprocess.run(cmd, capture_output=True, text=True, timeout=300, cwd=root)
+    assert res.returncode == 0, res.stderr[-2000:]
+    lines = [ln for ln in res.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
